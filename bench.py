@@ -1,0 +1,483 @@
+"""Benchmark of the OSCAR-style rotated INT2 KV hot path on GB300.
+
+Workload (one GPU): Qwen3-8B-shaped layer, 32 query / 8 KV heads, head_dim
+128, group 64, clip 0.9, batch 32, every sequence at 100,000 tokens (64 BF16
+sink + 99,680 INT2 history + 256 BF16 recent) with a token-granular page
+table shuffled over a pool of 32 × 100,100+ slots.  A step is one decode step
+of the hot path: oscar_quantize_append of one new token per request (the
+token leaving the recent window spills into INT2) followed by
+oscar_decode_attention.  Steps cycle through the 100-step decode sequence
+(L = 100,001 … 100,100).  Inputs are seeded synthetic data (no model weights).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own batch
+of 32 requests on its own GPU (requests are independent: weak scaling, no
+collective on the data path); `value` aggregates over ranks.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV tokens/s & HBM GB/s (% of ~8 TB/s) at 100K ctx; append GB/s"
+UNIT = "KV tokens/s"
+SEED = 1234
+
+B, HQ, HKV, D, G = 32, 32, 8, 128, 64
+L_BASE = 100_000          # tokens cached before the first decode step
+CYCLE = 100               # decode steps of the sequence
+S_SINK, W_RECENT = 64, 256
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--decode-kernel", choices=["auto", "simt"], default="auto")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-append", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 4:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                bits = int(parts[3], 16)
+            except ValueError:
+                continue
+            for bit, name in REASON_BITS.items():
+                if bits & bit:
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; barrier + max over ranks only)
+# --------------------------------------------------------------------------
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# workload
+# --------------------------------------------------------------------------
+def rotations(d):
+    from rotated_int2_kv_gb300 import ops, synth
+    Ck = ops.covariance(synth.calib_samples(SEED, 0, d))
+    Cv = ops.covariance(synth.calib_samples(SEED, 1, d))
+    Rk, _, _ = ops.build_rotation(Ck, d)
+    Rv, _, _ = ops.build_rotation(Cv, d)
+    return Rk, Rv
+
+
+def build_decode_workload(rank, steps_total):
+    import torch
+    from rotated_int2_kv_gb300 import ops, synth
+    dev = torch.device("cuda")
+    seed = SEED + 7919 * rank
+    cfg = ops.Config(D, HQ, HKV, G, S_SINK, W_RECENT, 0.9)
+    Rk, Rv = rotations(D)
+    max_len = L_BASE + CYCLE
+    pool = B * max_len
+    pt = synth.page_table(seed, B, max_len, pool).to(dev)
+    cache = ops.LayerCache(cfg, pool, B, Rk, Rv, device=dev)
+    scales = synth.outlier_scales(seed, HKV, D, "fixed4")
+    # fill every request to L_BASE tokens with chunked appends
+    chunk = 8192
+    pos = 0
+    while pos < L_BASE:
+        n = min(chunk, L_BASE - pos)
+        kk, vv = [], []
+        for b in range(B):
+            k, v = synth.kv_tokens(seed, b, pos, n, HKV, D, scales, device=dev)
+            kk.append(k)
+            vv.append(v)
+        k = torch.cat(kk)
+        v = torch.cat(vv)
+        cu = torch.arange(0, (B + 1) * n, n, dtype=torch.int32, device=dev)
+        start = torch.full((B,), pos, dtype=torch.int32, device=dev)
+        ops.quantize_append(cache, k, v, cu, start, pt)
+        pos += n
+        del k, v, kk, vv
+    torch.cuda.synchronize()
+    # per-step inputs of the 100-step cycle (device-resident)
+    newk, newv, qs = [], [], []
+    for s in range(CYCLE):
+        kk, vv = zip(*[synth.kv_tokens(seed, b, L_BASE + s, 1, HKV, D, scales, device=dev) for b in range(B)])
+        newk.append(torch.cat(kk))
+        newv.append(torch.cat(vv))
+        qs.append(synth.queries(seed, s, B, HQ, D, device=dev))
+    starts = [torch.full((B,), L_BASE + s, dtype=torch.int32, device=dev) for s in range(CYCLE)]
+    lens = [torch.full((B,), L_BASE + s + 1, dtype=torch.int32, device=dev) for s in range(CYCLE)]
+    cu1 = torch.arange(0, B + 1, dtype=torch.int32, device=dev)
+    ws = ops.alloc_workspace(cfg, B, max_len, device=dev)
+    out = torch.empty((B, HQ, D), dtype=torch.float32, device=dev)
+    return dict(cfg=cfg, cache=cache, pt=pt, newk=newk, newv=newv, qs=qs, starts=starts, lens=lens, cu1=cu1,
+                ws=ws, out=out, max_len=max_len, Rk=Rk, Rv=Rv, seed=seed, scales=scales)
+
+
+def decode_step(w, i, kernel):
+    from rotated_int2_kv_gb300 import ops
+    s = i % CYCLE
+    ops.quantize_append(w["cache"], w["newk"][s], w["newv"][s], w["cu1"], w["starts"][s], w["pt"])
+    ops.decode_attention(w["cache"], w["qs"][s], w["pt"], w["lens"][s], w["max_len"], w["ws"], out=w["out"],
+                         impl=kernel)
+
+
+def launches_per_step():
+    # quantize + window copy (append) ; prep + history + combine (decode)
+    return 5
+
+
+def algorithmic_history_bytes(rec_bytes_per_token, L):
+    hist = max(0, L - W_RECENT) - S_SINK
+    return hist * (rec_bytes_per_token + 4)   # records + page-table entry
+
+
+# --------------------------------------------------------------------------
+# the oracle as CPU baseline / reference arm
+# --------------------------------------------------------------------------
+def oracle_sample(seed, L=L_BASE + 1):
+    """Builds (untimed) an oracle cache of one request at L tokens; returns a closure timing one decode."""
+    import torch
+    import oracle
+    from rotated_int2_kv_gb300 import synth
+    Ck = oracle.covariance(synth.calib_samples(SEED, 0, D))
+    Cv = oracle.covariance(synth.calib_samples(SEED, 1, D))
+    Rk = oracle.build_rotation(Ck, D)[0].astype(np.float32)
+    Rv = oracle.build_rotation(Cv, D)[0].astype(np.float32)
+    oc = oracle.OracleCache(oracle.OracleConfig(D, HQ, HKV, G, S_SINK, W_RECENT, 0.9), L, 1, Rk, Rv)
+    scales = synth.outlier_scales(seed, HKV, D, "fixed4")
+    k, v = synth.kv_tokens(seed, 0, 0, L, HKV, D, scales)
+    pt = np.arange(L, dtype=np.int64)[None, :]
+    oc.append(k.float().numpy(), v.float().numpy(), [0, L], [0], [0], pt)
+    q = synth.queries(seed, 0, 1, HQ, D).float().numpy()
+
+    def run():
+        t0 = time.perf_counter()
+        oracle.decode_attention(oc, q, pt, [L], [0])
+        return time.perf_counter() - t0
+    return run, L
+
+
+def cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, rank, ws):
+    if rank != 0:
+        return
+    run, L = oracle_sample(SEED)
+    for _ in range(args.warmup):
+        run()
+    t = sum(run() for _ in range(args.steps))
+    val = args.steps * L / t
+    sample = "oracle fp64 decode of 1 request x 32 q heads at L=%d (cache built untimed)" % L
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(),
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config():
+    return {"workload": "Qwen3-8B-shaped decode step (append 1 token + attention), batch 32, "
+                        "context 100,000 (64 sink + 99,680 INT2 + 256 recent), 32 q / 8 KV heads, d 128, "
+                        "group 64, clip 0.9, shuffled page table, page_size 1",
+            "batch": B, "context": L_BASE, "q_heads": HQ, "kv_heads": HKV, "head_dim": D, "group_size": G,
+            "l2": "inputs larger than L2 (2.05 GB INT2 history per step)",
+            "parallelism": "replicas (independent requests per GPU)"}
+
+
+# --------------------------------------------------------------------------
+def main():
+    args = parse()
+    rank, ws, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, ws)
+        return
+    import torch
+    from rotated_int2_kv_gb300 import ops
+    if not os.path.exists(ops._LIB_PATH):
+        from rotated_int2_kv_gb300 import build
+        build.build()
+    ops.lib()
+    steps_total = args.steps + args.warmup
+    w = build_decode_workload(rank, steps_total)
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        decode_step(w, i, args.decode_kernel)
+    torch.cuda.synchronize()
+    assert ops.device_status() == 0
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    ops.profile_enable(True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        decode_step(w, args.warmup + i, args.decode_kernel)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms = e0.elapsed_time(e1)
+    hist_ms, hist_n = ops.profile_read(0)
+    ops.profile_enable(False)
+    clk = clocks.stop()
+    ms = max_over_ranks(ms, ws)
+
+    rec_tok, _ = ops.cache_bytes_per_token(w["cfg"])
+    tokens = 0
+    hist_bytes = 0
+    for i in range(args.steps):
+        L = L_BASE + (args.warmup + i) % CYCLE + 1
+        tokens += B * L
+        hist_bytes += B * algorithmic_history_bytes(rec_tok, L)
+    tokens_all = sum_over_ranks(tokens, ws)
+    value = tokens_all / (ms / 1e3)
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    achieved = (hist_bytes / hist_n) / (hist_ms / hist_n / 1e3) / 1e9 if hist_n else None
+    traffic = None
+    try:
+        prof = json.load(open(os.path.join(ROOT, "profiles", "history_traffic.json")))
+        if prof.get("kernel") == "history_mma_kernel" and args.decode_kernel == "auto":
+            traffic = prof.get("bytes_per_launch_full")
+    except (OSError, ValueError):
+        pass
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if args.decode_kernel == "simt" else "f16 mma / f32 accumulate",
+            "data": "synthetic", "config": workload_config(),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": (achieved / hbm_peak) if achieved else None, "traffic": traffic,
+                         "kernel": "history kernel (INT2 split-K)", "peak_source": "measured hbm_gbs",
+                         "history_ms_per_step": hist_ms / max(hist_n, 1),
+                         "pct_of_8TBs": (achieved / 8000.0) if achieved else None},
+            "gpu_launches": launches_per_step() * args.steps,
+            "bits_per_kv_element": (16.0 * 320 + (2 + 32.0 / G) * (L_BASE - 320)) / L_BASE,
+            "clocks": clk}
+    # ---- end to end through the C ABI with host buffers ----------------------
+    if not args.no_e2e:
+        line["e2e"] = e2e_measure(w, args, ws)
+    if not args.no_append:
+        line["append"] = append_measure()
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        run, L = oracle_sample(w["seed"])
+        run()
+        t = 0.0
+        n = 0
+        while t < 10.0 and n < 8:
+            t += run()
+            n += 1
+        line["cpu_baseline"] = {"value": n * L / t, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                                "sample": "%d x oracle fp64 decode of 1 request x 32 q heads at L=%d "
+                                          "(cache built untimed)" % (n, L)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def e2e_measure(w, args, ws):
+    """Same metric with per-step inputs in pinned host memory and the output read back."""
+    import torch
+    from rotated_int2_kv_gb300 import ops
+    dev = torch.device("cuda")
+    n = max(10, min(args.steps, 500))
+    hk = [t.cpu().pin_memory() for t in w["newk"]]
+    hv = [t.cpu().pin_memory() for t in w["newv"]]
+    hq = [t.cpu().pin_memory() for t in w["qs"]]
+    hout = torch.empty((B, HQ, D), dtype=torch.float32).pin_memory()
+    dk = torch.empty_like(w["newk"][0])
+    dv = torch.empty_like(w["newv"][0])
+    dq = torch.empty_like(w["qs"][0])
+    stream = torch.cuda.current_stream()
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    tokens = 0
+    for i in range(n):
+        s = i % CYCLE
+        dk.copy_(hk[s], non_blocking=True)
+        dv.copy_(hv[s], non_blocking=True)
+        dq.copy_(hq[s], non_blocking=True)
+        ops.quantize_append(w["cache"], dk, dv, w["cu1"], w["starts"][s], w["pt"])
+        ops.decode_attention(w["cache"], dq, w["pt"], w["lens"][s], w["max_len"], w["ws"], out=w["out"])
+        hout.copy_(w["out"], non_blocking=True)
+        tokens += B * (L_BASE + s + 1)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), ws)
+    tokens = sum_over_ranks(tokens, ws)
+    h2d = dk.numel() * 2 + dv.numel() * 2 + dq.numel() * 2
+    return {"value": tokens / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": hout.numel() * 4, "steps": n}
+
+
+def append_measure():
+    """Chunked-prefill append of a 32,768-token Qwen3-8B-shaped request (32,448 INT2 + 320 BF16)."""
+    import torch
+    from rotated_int2_kv_gb300 import ops, synth
+    dev = torch.device("cuda")
+    L = 32768
+    cfg = ops.Config(D, HQ, HKV, G, S_SINK, W_RECENT, 0.9)
+    Rk, Rv = rotations(D)
+    pt = synth.page_table(SEED, 1, L, L).to(dev)
+    cache = ops.LayerCache(cfg, L, 1, Rk, Rv, device=dev)
+    scales = synth.outlier_scales(SEED, HKV, D, "fixed4")
+    k, v = synth.kv_tokens(SEED, 0, 0, L, HKV, D, scales, device=dev)
+    cu = torch.tensor([0, L], dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        ops.quantize_append(cache, k, v, cu, st, pt)
+    torch.cuda.synchronize()
+    ops.profile_enable(True)
+    reps = 20
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        ops.quantize_append(cache, k, v, cu, st, pt)
+    e1.record()
+    torch.cuda.synchronize()
+    qms, qn = ops.profile_read(1)
+    ops.profile_enable(False)
+    call_ms = e0.elapsed_time(e1) / reps
+    hist = L - S_SINK - W_RECENT
+    rec_tok, _ = ops.cache_bytes_per_token(cfg)
+    alg_bytes = hist * (HKV * D * 2 * 2 + rec_tok + 4)   # bf16 K,V in + records out + page table
+    kern_ms = qms / max(qn, 1)
+    flops = hist * HKV * 2 * 2 * D * D
+    fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12       # TFLOP/s, FFMA at max clock
+    return {"workload": "one 32,768-token request appended at once (32,448 INT2 + 320 BF16), "
+                        "Qwen3-8B-shaped layer", "value": alg_bytes / (call_ms / 1e3) / 1e9, "unit": "GB/s",
+            "ms_per_call": call_ms, "quantize_kernel_ms": kern_ms,
+            "roofline": {"bound": "alu", "achieved": flops / (kern_ms / 1e3) / 1e12,
+                         "peak": fp32_peak, "unit": "TFLOP/s",
+                         "frac": flops / (kern_ms / 1e3) / 1e12 / fp32_peak,
+                         "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz"}}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,452 @@
+// Quantise-on-append: rotate, clip, quantise and pack new K/V head vectors
+// into the INT2 pool, and write the BF16 sink / recent windows.
+//
+// [OSCAR news] "サービングシステム：混合精度キャッシュレイアウト": the first 64
+// tokens and the last 256 tokens of a request stay BF16; every token in between
+// is stored as INT2 after the OSCAR rotation and clipping.  [Escha log] part 2,
+// settings table: one (scale, zero) per group of 64 channels; fix 1: 0.25 byte
+// per code.
+//
+// Two kernels, in stream order:
+//  1. quantize_kernel: every position entering the history in this call
+//     ([max(S, L0-W), max(S, L1-W)) of each request) -- read from the recent
+//     ring if it was cached before, else from the new input -- is rotated
+//     y = x·R in fp32 (FFMA, R staged in shared memory), then per group:
+//     lo = r·min, hi = r·max, s = fp16((hi-lo)/3), z = fp16(lo),
+//     c = clamp(rint((y - z)/s), 0, 3); codes are packed 4 per byte.
+//  2. window_copy_kernel: new positions below S go to the sink, new positions at
+//     or after max(S, L1-W) to the ring slot p % W.  Running it second keeps
+//     the spill reads of kernel 1 ahead of the ring overwrites.
+#include <algorithm>
+
+#include "oscar_internal.h"
+#include "oscar_device.cuh"
+
+namespace oscar {
+
+constexpr int kMaxAppendBatch = 4096;
+constexpr int kTileVec = 64;        // head vectors per tile (one matrix: K or V)
+constexpr int kColBlock = 64;       // columns of R per GEMM pass
+constexpr int kAppendThreads = 256;
+
+struct AppendParams {
+    const void* k;
+    const void* v;
+    int kv_dtype;
+    const int32_t* cu_new;
+    const int32_t* start_pos;
+    const int32_t* req_idx;
+    const int32_t* page_table;
+    int64_t pt_stride;
+    int batch;
+    uint8_t* records;
+    uint16_t* sink;
+    uint16_t* recent;
+    const float* rot_k;
+    const float* rot_v;
+    int64_t num_slots;
+    int max_reqs;
+    int Hkv, S, W, G, rec_bytes;
+    float clip;
+    int64_t total_new;
+    int* status;
+};
+
+__device__ __forceinline__ int hist_hi(int L, int S, int W) { return max(S, L - W); }
+
+// Exclusive prefix over requests of the number of positions entering the
+// history; prefix[batch] is the total.  All threads of the block participate.
+__device__ void build_prefix(const AppendParams& P, int* prefix, int* scratch) {
+    const int tid = threadIdx.x;
+    const int per = (P.batch + blockDim.x - 1) / blockDim.x;
+    const int b0 = min(P.batch, tid * per), b1 = min(P.batch, b0 + per);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) {
+        const int L0 = P.start_pos[b];
+        const int n = P.cu_new[b + 1] - P.cu_new[b];
+        int cnt = 0;
+        if (L0 < 0 || n < 0) {
+            set_status(P.status, OSCAR_DEV_BAD_LEN);
+        } else {
+            cnt = hist_hi(L0 + n, P.S, P.W) - hist_hi(L0, P.S, P.W);
+        }
+        prefix[b] = cnt;  // temporarily the count
+        local += cnt;
+    }
+    scratch[tid] = local;
+    __syncthreads();
+    for (int off = 1; off < blockDim.x; off <<= 1) {  // inclusive Hillis-Steele scan
+        const int x = tid >= off ? scratch[tid - off] : 0;
+        __syncthreads();
+        scratch[tid] += x;
+        __syncthreads();
+    }
+    int run = tid ? scratch[tid - 1] : 0;
+    for (int b = b0; b < b1; ++b) {
+        const int c = prefix[b];
+        prefix[b] = run;
+        run += c;
+    }
+    if (tid == blockDim.x - 1) prefix[P.batch] = scratch[tid];
+    __syncthreads();
+}
+
+// Largest b with prefix[b] <= u (prefix non-decreasing, prefix[0] = 0).
+__device__ __forceinline__ int find_request(const int* prefix, int batch, int u) {
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAppendThreads)
+quantize_kernel(AppendParams P) {
+    constexpr bool kResidentR = (D * D * 4 <= 64 * 1024);
+    constexpr int kNB = D / kColBlock;           // column blocks of R
+    constexpr int kYStride = D + 4;
+    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int kRCols = kResidentR ? D : kColBlock;
+    constexpr int kXT = D * kTileVec;                   // transposed X tile, floats
+    constexpr int kY = kTileVec * kYStride;             // Y tile, floats
+    constexpr int kXY = kResidentR ? (kXT > kY ? kXT : kY) : kXT + kY;
+    float* sR = reinterpret_cast<float*>(smem);         // D x kRCols
+    float* sXT = sR + D * kRCols;                       // D x 64
+    float* sY = kResidentR ? sXT : sXT + kXT;           // 64 x (D + 4); aliases sXT if R is resident
+    int* prefix = reinterpret_cast<int*>(sR + D * kRCols + kXY);   // batch + 1
+    int* scratch = prefix + P.batch + 1;                // blockDim.x
+    __shared__ int s_meta[kTileVec][4];                               // b, p, h, slot (-1: skip)
+
+    const int mat = blockIdx.y;                                       // 0: K, 1: V
+    const float* R = mat ? P.rot_v : P.rot_k;
+    const void* src_new = mat ? P.v : P.k;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    build_prefix(P, prefix, scratch);
+    const int64_t total_vec = (int64_t)prefix[P.batch] * P.Hkv;
+    const int64_t ntiles = (total_vec + kTileVec - 1) / kTileVec;
+    if ((int64_t)blockIdx.x >= ntiles) return;
+
+    if (kResidentR) {
+        for (int i = tid * 4; i < D * D; i += kAppendThreads * 4)
+            *reinterpret_cast<float4*>(sR + i) = *reinterpret_cast<const float4*>(R + i);
+    }
+    const int rec_off_codes = mat ? D / 4 : 0;
+    const int ng = D / P.G;
+    const int rec_off_sz = D / 2 + (mat ? 4 * ng : 0);
+
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int64_t e0 = tile * kTileVec;
+        const int nvec = (int)(total_vec - e0 < kTileVec ? total_vec - e0 : kTileVec);
+        // ---- resolve vectors of the tile ---------------------------------
+        if (tid < kTileVec) {
+            int b = -1, p = 0, h = 0, slot = -1;
+            if (tid < nvec) {
+                const int64_t e = e0 + tid;
+                const int u = (int)(e / P.Hkv);
+                h = (int)(e % P.Hkv);
+                b = find_request(prefix, P.batch, u);
+                const int L0 = P.start_pos[b];
+                p = hist_hi(L0, P.S, P.W) + (u - prefix[b]);
+                if (p >= P.pt_stride) {
+                    set_status(P.status, OSCAR_DEV_BAD_LEN);
+                } else {
+                    const int s = P.page_table[(int64_t)b * P.pt_stride + p];
+                    if (s < 0 || s >= P.num_slots) set_status(P.status, OSCAR_DEV_BAD_SLOT);
+                    else slot = s;
+                }
+                const int rq = P.req_idx ? P.req_idx[b] : b;
+                if (p < L0 && (rq < 0 || rq >= P.max_reqs)) {
+                    set_status(P.status, OSCAR_DEV_BAD_REQ);
+                    slot = -1;
+                }
+                if (p >= L0 && (int64_t)P.cu_new[b] + (p - L0) >= P.total_new) {
+                    set_status(P.status, OSCAR_DEV_BAD_LEN);
+                    slot = -1;
+                }
+            }
+            s_meta[tid][0] = b;
+            s_meta[tid][1] = p;
+            s_meta[tid][2] = h;
+            s_meta[tid][3] = slot;
+        }
+        __syncthreads();
+        // ---- gather X (bf16-rounded) into sXT[k][v] ------------------------
+        for (int idx = tid; idx < kTileVec * (D / 8); idx += kAppendThreads) {
+            const int v = idx % kTileVec, c8 = idx / kTileVec;
+            float x[8];
+            if (v < nvec && s_meta[v][3] >= 0) {
+                const int b = s_meta[v][0], p = s_meta[v][1], h = s_meta[v][2];
+                const int L0 = P.start_pos[b];
+                if (p < L0) {
+                    const int rq = P.req_idx ? P.req_idx[b] : b;
+                    const uint16_t* row = P.recent + ((((int64_t)rq * P.W + p % P.W) * P.Hkv + h) * 2 + mat) * D;
+                    const uint4 raw = *reinterpret_cast<const uint4*>(row + c8 * 8);
+                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        x[2 * j] = __uint_as_float(w4[j] << 16);
+                        x[2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+                    }
+                } else {
+                    const int64_t t = P.cu_new[b] + (p - L0);
+                    const int64_t base = (t * P.Hkv + h) * D + c8 * 8;
+                    if (t < P.total_new) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            x[j] = bf16_bits_to_f32(f32_to_bf16_bits(load_elem(src_new, base + j, P.kv_dtype)));
+                    } else {                 // cu_new disagrees with total_new: flagged, row skipped
+                        set_status(P.status, OSCAR_DEV_BAD_LEN);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) x[j] = 0.f;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) x[j] = 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sXT[(c8 * 8 + j) * kTileVec + v] = x[j];
+        }
+        __syncthreads();
+        // ---- Y = X · R, 4x4 register tile per thread per column block -------
+        const int tv = warp * 2 + (lane >> 4), tc = lane & 15;
+        float acc_all[kResidentR ? kNB : 1][4][4];
+#pragma unroll
+        for (int cb = 0; cb < kNB; ++cb) {
+            const float* Rb;
+            if (kResidentR) {
+                Rb = sR + cb * kColBlock;
+            } else {
+                __syncthreads();
+                for (int i = tid * 4; i < D * kColBlock; i += kAppendThreads * 4) {
+                    const int row = i / kColBlock, col = i % kColBlock;
+                    *reinterpret_cast<float4*>(sR + i) =
+                        *reinterpret_cast<const float4*>(R + (int64_t)row * D + cb * kColBlock + col);
+                }
+                __syncthreads();
+                Rb = sR;
+            }
+            const int ldr = kResidentR ? D : kColBlock;
+            float acc[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 4
+            for (int kk = 0; kk < D; ++kk) {
+                const float4 xv = *reinterpret_cast<const float4*>(sXT + kk * kTileVec + 4 * tv);
+                const float4 rv = *reinterpret_cast<const float4*>(Rb + kk * ldr + 4 * tc);
+                const float xs[4] = {xv.x, xv.y, xv.z, xv.w};
+                const float rs[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xs[i], rs[j], acc[i][j]);
+            }
+            if (kResidentR) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc_all[kResidentR ? cb : 0][i][j] = acc[i][j];
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<float4*>(sY + (4 * tv + i) * kYStride + cb * kColBlock + 4 * tc) =
+                        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+            }
+        }
+        if (kResidentR) {
+            __syncthreads();  // sY aliases sXT
+#pragma unroll
+            for (int cb = 0; cb < kNB; ++cb)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<float4*>(sY + (4 * tv + i) * kYStride + cb * kColBlock + 4 * tc) =
+                        make_float4(acc_all[kResidentR ? cb : 0][i][0], acc_all[kResidentR ? cb : 0][i][1],
+                                    acc_all[kResidentR ? cb : 0][i][2], acc_all[kResidentR ? cb : 0][i][3]);
+        }
+        __syncthreads();
+        // ---- quantise: one warp per vector, D/32 contiguous channels per lane ----
+        constexpr int CPL = D / 32;
+        const int lpg = P.G / CPL;       // lanes per group (4..32)
+        const float r = P.clip;
+        for (int v = warp; v < nvec; v += kAppendThreads / 32) {
+            const int slot = s_meta[v][3];
+            if (slot < 0) continue;      // warp-uniform
+            const int h = s_meta[v][2];
+            float y[CPL];
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) y[j] = sY[v * kYStride + lane * CPL + j];
+            float mn = y[0], mx = y[0];
+#pragma unroll
+            for (int j = 1; j < CPL; ++j) { mn = fminf(mn, y[j]); mx = fmaxf(mx, y[j]); }
+            for (int off = 1; off < lpg; off <<= 1) {
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            }
+            const float lo = __fmul_rn(r, mn);
+            const float hi = __fmul_rn(r, mx);
+            const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 3.0f));
+            const __half z16 = __float2half_rn(lo);
+            const float s = __half2float(s16), z = __half2float(z16);
+            uint32_t bits = 0;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                uint32_t c = 0;
+                if (s != 0.0f) {
+                    const float u = __fdiv_rn(__fsub_rn(y[j], z), s);
+                    const float cr = fminf(fmaxf(rintf(u), 0.0f), 3.0f);
+                    c = (uint32_t)cr;
+                }
+                bits |= c << (2 * j);
+            }
+            uint8_t* rec = P.records + ((int64_t)slot * P.Hkv + h) * P.rec_bytes;
+            if (CPL >= 4) {
+#pragma unroll
+                for (int bj = 0; bj < CPL / 4; ++bj)
+                    rec[rec_off_codes + lane * (CPL / 4) + bj] = (uint8_t)(bits >> (8 * bj));
+            } else {  // CPL == 2: two lanes share a byte
+                const uint32_t other = __shfl_xor_sync(0xffffffffu, bits, 1);
+                if ((lane & 1) == 0) rec[rec_off_codes + lane / 2] = (uint8_t)(bits | (other << 4));
+            }
+            if ((lane % lpg) == 0) {
+                const int gi = lane / lpg;
+                __half2 sz = __halves2half2(s16, z16);
+                *reinterpret_cast<__half2*>(rec + rec_off_sz + 4 * gi) = sz;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// Copies each new row to the sink or the recent ring (bf16).  One block per row.
+template <int D>
+__global__ void __launch_bounds__(128)
+window_copy_kernel(AppendParams P, int64_t total_new) {
+    __shared__ int s_b;
+    for (int64_t t = blockIdx.x; t < total_new; t += gridDim.x) {
+        if (threadIdx.x == 0) {
+            int lo = 0, hi = P.batch - 1;  // last b with cu_new[b] <= t
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (P.cu_new[mid] <= t) lo = mid; else hi = mid - 1;
+            }
+            s_b = lo;
+        }
+        __syncthreads();
+        const int b = s_b;
+        __syncthreads();
+        const int L0 = P.start_pos[b];
+        const int n = P.cu_new[b + 1] - P.cu_new[b];
+        if (L0 < 0 || n < 0) continue;
+        const int p = L0 + (int)(t - P.cu_new[b]);
+        const int L1 = L0 + n;
+        uint16_t* dst = nullptr;
+        const int rq = P.req_idx ? P.req_idx[b] : b;
+        if (rq < 0 || rq >= P.max_reqs) {
+            if (threadIdx.x == 0) set_status(P.status, OSCAR_DEV_BAD_REQ);
+            continue;
+        }
+        if (p < P.S) dst = P.sink + ((int64_t)rq * P.S + p) * P.Hkv * 2 * D;
+        else if (p >= hist_hi(L1, P.S, P.W)) dst = P.recent + ((int64_t)rq * P.W + p % P.W) * P.Hkv * 2 * D;
+        if (!dst) continue;
+        for (int i = threadIdx.x; i < P.Hkv * 2 * D; i += blockDim.x) {
+            const int h = i / (2 * D), mat = (i / D) & 1, c = i % D;
+            const void* src = mat ? P.v : P.k;
+            dst[i] = f32_to_bf16_bits(load_elem(src, (t * P.Hkv + h) * D + c, P.kv_dtype));
+        }
+    }
+}
+
+template <int D>
+static int launch_append(const AppendParams& P, int64_t total_new, cudaStream_t stream) {
+    constexpr bool kResidentR = (D * D * 4 <= 64 * 1024);
+    const int r_cols = kResidentR ? D : kColBlock;
+    size_t smem = (size_t)D * r_cols * 4;  // must match the carve-up in quantize_kernel
+    const size_t xt = (size_t)D * kTileVec * 4, y = (size_t)kTileVec * (D + 4) * 4;
+    smem += kResidentR ? std::max(xt, y) : xt + y;
+    smem += (size_t)(P.batch + 1 + kAppendThreads) * 4;
+    auto kern = quantize_kernel<D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return check_cuda("cudaFuncSetAttribute(quantize_kernel)");
+    // Upper bound of the vectors entering the history: every new row plus
+    // every row that can leave the ring.
+    const int64_t max_units = total_new + (int64_t)P.batch * P.W;
+    const int64_t max_tiles = (max_units * P.Hkv + kTileVec - 1) / kTileVec;
+    // blockIdx.y selects K or V, so the two halves together fill every SM
+    // with its resident CTAs (2 per SM when R stays in shared memory).
+    const int per_sm = kResidentR ? 2 : 1;
+    const int64_t grid_x = std::max<int64_t>(1, std::min<int64_t>(max_tiles, (int64_t)sm_count() * per_sm / 2));
+    if (max_tiles > 0) {
+        const int prof = prof_begin(1, stream);
+        kern<<<dim3((unsigned)grid_x, 2), kAppendThreads, smem, stream>>>(P);
+        prof_end(prof, stream);
+        int rc = check_cuda("quantize_kernel launch");
+        if (rc) return rc;
+    }
+    if (total_new > 0) {
+        const int64_t grid = std::min<int64_t>(total_new, (int64_t)sm_count() * 8);
+        window_copy_kernel<D><<<(unsigned)grid, 128, 0, stream>>>(P, total_new);
+        int rc = check_cuda("window_copy_kernel launch");
+        if (rc) return rc;
+    }
+    return OSCAR_OK;
+}
+
+}  // namespace oscar
+
+using namespace oscar;
+
+extern "C" int oscar_quantize_append(const oscar_config* cfg, const oscar_layer_cache* cache,
+                                     const void* k, const void* v, int64_t total_new,
+                                     const int32_t* cu_new, const int32_t* start_pos,
+                                     const int32_t* req_idx, const int32_t* page_table,
+                                     int64_t pt_stride, int32_t batch, void* stream) {
+    clear_error();
+    int rc = validate_config(cfg);
+    if (rc) return rc;
+    rc = validate_cache(cfg, cache);
+    if (rc) return rc;
+    if (batch < 0 || batch > kMaxAppendBatch)
+        return fail(OSCAR_ERR_ARG, "batch must be in [0, %d] (got %d)", kMaxAppendBatch, batch);
+    if (total_new < 0) return fail(OSCAR_ERR_ARG, "total_new must be >= 0");
+    if (batch == 0) return OSCAR_OK;
+    if (!cu_new || !start_pos || !page_table) return fail(OSCAR_ERR_NULL, "cu_new, start_pos and page_table are required");
+    if (total_new > 0 && (!k || !v)) return fail(OSCAR_ERR_NULL, "k and v are required when total_new > 0");
+    if (pt_stride < 1) return fail(OSCAR_ERR_ARG, "pt_stride must be >= 1");
+    AppendParams P;
+    P.k = k;
+    P.v = v;
+    P.kv_dtype = cfg->kv_dtype;
+    P.cu_new = cu_new;
+    P.start_pos = start_pos;
+    P.req_idx = req_idx;
+    P.page_table = page_table;
+    P.pt_stride = pt_stride;
+    P.batch = batch;
+    P.records = cache->records;
+    P.sink = cache->sink;
+    P.recent = cache->recent;
+    P.rot_k = cache->rot_k;
+    P.rot_v = cache->rot_v;
+    P.num_slots = cache->num_slots;
+    P.max_reqs = cache->max_reqs;
+    P.Hkv = cfg->num_kv_heads;
+    P.S = cfg->sink;
+    P.W = cfg->recent;
+    P.G = cfg->group_size;
+    P.rec_bytes = record_layout(cfg->head_dim, cfg->group_size).bytes;
+    P.clip = cfg->clip_ratio;
+    P.total_new = total_new;
+    P.status = status_word();
+    if (!P.status) return OSCAR_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    switch (cfg->head_dim) {
+        case 64: return launch_append<64>(P, total_new, st);
+        case 128: return launch_append<128>(P, total_new, st);
+        default: return launch_append<256>(P, total_new, st);
+    }
+}

@@ -1,0 +1,618 @@
+// Decode attention over the mixed-precision cache: prep (query rotation and
+// request metadata), split-K history kernel over the INT2 region, and the
+// combine kernel (BF16 windows, log-sum-exp merge of the history partials,
+// R_Vᵀ epilogue).
+//
+// [OSCAR news] "サービングシステム：混合精度キャッシュレイアウト": 64 BF16 sink
+// tokens, 256 BF16 recent tokens, INT2 history in between, paged attention.
+// "OSCARの違い": keys and values are stored rotated (x·R_K, x·R_V), so the
+// history logit is taken with q·R_K and the weighted sum of rotated values is
+// mapped back with R_Vᵀ once, after the sum.  [Escha log] part 2, fix 4: query
+// head h reads KV head h / (Hq/Hkv).
+//
+// This file holds the CUDA-core history kernel (history_simt_kernel); the
+// tensor-core one lives in oscar_decode_mma.cu.  Both write the same partials.
+#include <algorithm>
+#include <cmath>
+
+#include "oscar_internal.h"
+#include "oscar_device.cuh"
+#include "oscar_decode_common.cuh"
+
+namespace oscar {
+
+constexpr int kMaxDecodeBatch = 4096;
+
+__device__ __forceinline__ int d_hist_hi(int L, int S, int W) { return max(S, L - W); }
+
+// Number of history chunks of a request of L tokens.
+__device__ __forceinline__ int n_chunks(int L, const DecodeParams& P) {
+    const int h = d_hist_hi(L, P.S, P.W) - P.S;
+    return h > 0 ? (h + P.chunk - 1) / P.chunk : 0;
+}
+
+__device__ __forceinline__ bool request_valid(const DecodeParams& P, int b, int* L_out, int* rq_out) {
+    const int L = P.seq_lens[b];
+    const int rq = P.req_idx ? P.req_idx[b] : b;
+    *rq_out = rq;
+    *L_out = L;
+    return L >= 1 && L <= P.max_seq_len && L <= P.pt_stride && rq >= 0 && rq < P.max_reqs;
+}
+
+// ---------------------------------------------------------------------------
+// prep: per request, q̃ = q·R_K·(log2 e/√d) for every query head (fp32), its
+// fp16 hi/lo split packed as mma B fragments, the per-group sums of hi+lo,
+// the effective length / window row, and (block 0) the chunk prefix.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
+    __shared__ float sq[16][D];
+    __shared__ float sqt[16][D];
+    __shared__ int scan[256];
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x;
+    if (b == 0) {
+        // chunk prefix over all requests (re-derives validity locally)
+        const int per = (P.batch + 255) / 256;
+        const int b0 = min(P.batch, tid * per), b1 = min(P.batch, b0 + per);
+        int local = 0;
+        for (int r = b0; r < b1; ++r) {
+            int L, rq;
+            if (request_valid(P, r, &L, &rq)) local += n_chunks(L, P);
+        }
+        scan[tid] = local;
+        __syncthreads();
+        for (int off = 1; off < 256; off <<= 1) {
+            const int x = tid >= off ? scan[tid - off] : 0;
+            __syncthreads();
+            scan[tid] += x;
+            __syncthreads();
+        }
+        int run = tid ? scan[tid - 1] : 0;
+        for (int r = b0; r < b1; ++r) {
+            P.cprefix[r] = run;
+            int L, rq;
+            if (request_valid(P, r, &L, &rq)) run += n_chunks(L, P);
+        }
+        if (tid == 255) P.cprefix[P.batch] = scan[255];
+        __syncthreads();
+    }
+    int L, rq;
+    const bool ok = request_valid(P, b, &L, &rq);
+    if (tid == 0) {
+        P.len[b] = ok ? L : 0;
+        P.req[b] = ok ? rq : 0;
+        if (!ok) {
+            int bits = 0;
+            if (!(L >= 1 && L <= P.max_seq_len && L <= P.pt_stride)) bits |= OSCAR_DEV_BAD_LEN;
+            if (!(rq >= 0 && rq < P.max_reqs)) bits |= OSCAR_DEV_BAD_REQ;
+            set_status(P.status, bits);
+        }
+    }
+    for (int h0 = 0; h0 < P.Hq; h0 += 16) {
+        const int nh = min(16, P.Hq - h0);
+        __syncthreads();
+        for (int i = tid; i < nh * D; i += 256)
+            sq[i / D][i % D] = load_elem(P.q, ((int64_t)b * P.Hq + h0 + i / D) * D + i % D, P.q_dtype);
+        __syncthreads();
+        for (int col = tid; col < D; col += 256) {
+            float acc[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+            for (int k = 0; k < D; ++k) {
+                const float r = P.rot_k[(int64_t)k * D + col];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[j] = fmaf(sq[j][k], r, acc[j]);
+            }
+            for (int j = 0; j < nh; ++j) {
+                const float v = acc[j] * P.qscale;
+                sqt[j][col] = v;
+                P.qt[((int64_t)b * P.Hq + h0 + j) * D + col] = v;
+            }
+        }
+        __syncthreads();
+        // per-group sums of the fp16 hi + lo parts
+        for (int i = tid; i < nh * P.ng; i += 256) {
+            const int j = i / P.ng, gi = i % P.ng;
+            float s = 0.f;
+            for (int c = gi * P.G; c < (gi + 1) * P.G; ++c) {
+                const float x = sqt[j][c];
+                const __half hi = __float2half_rn(x);
+                const __half lo = __float2half_rn(x - __half2float(hi));
+                s += __half2float(hi) + __half2float(lo);
+            }
+            P.qsum[((int64_t)b * P.Hq + h0 + j) * P.ng + gi] = s;
+        }
+        // B fragments: [Hkv][n_tiles][D/16][32 lanes] of (b0b1, b2b3);
+        // column n of tile nt is (head 4nt + n/2 of the KV group, part n%2).
+        const int nfr = P.Hkv * P.n_frag_tiles * (D / 16) * 32;
+        for (int i = tid; i < nfr; i += 256) {
+            const int lane = i & 31;
+            const int kk = (i >> 5) % (D / 16);
+            const int nt = (i / (32 * (D / 16))) % P.n_frag_tiles;
+            const int hk = i / (32 * (D / 16) * P.n_frag_tiles);
+            const int n = lane >> 2, j = lane & 3;
+            const int head = hk * P.g + 4 * nt + (n >> 1);
+            const int part = n & 1;
+            if (4 * nt + (n >> 1) >= P.g) {         // padding column: zero, written once
+                if (h0 == 0)
+                    P.qfrag[(((int64_t)b * P.Hkv + hk) * P.n_frag_tiles + nt) * (D / 16) * 32 + kk * 32 + lane] =
+                        make_uint2(0u, 0u);
+                continue;
+            }
+            if (head < h0 || head >= h0 + nh) continue;
+            const int chans[4] = {16 * kk + 2 * j, 16 * kk + 2 * j + 8, 16 * kk + 2 * j + 1, 16 * kk + 2 * j + 9};
+            uint16_t hv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float x = sqt[head - h0][chans[e]];
+                const __half hi = __float2half_rn(x);
+                const __half v = part ? __float2half_rn(x - __half2float(hi)) : hi;
+                hv[e] = *reinterpret_cast<const uint16_t*>(&v);
+            }
+            P.qfrag[(((int64_t)b * P.Hkv + hk) * P.n_frag_tiles + nt) * (D / 16) * 32 + kk * 32 + lane] =
+                make_uint2((uint32_t)hv[0] | ((uint32_t)hv[1] << 16), (uint32_t)hv[2] | ((uint32_t)hv[3] << 16));
+        }
+    }
+}
+
+// Maps flattened chunk index f to (request, chunk-in-request) by binary search
+// over the exclusive prefix cprefix[0..batch].
+__device__ __forceinline__ int chunk_request(const int32_t* cprefix, int batch, int64_t f) {
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cprefix[mid] <= f) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ---------------------------------------------------------------------------
+// CUDA-core history kernel.  Persistent grid; CTA i owns flattened chunks
+// [i·N/n, (i+1)·N/n).  One warp per KV head (heads loop when Hkv exceeds the
+// warp count).  Per 32-token tile: lane = token for the logits (factored
+// dequant: logit = Σ_g s_g·Σ q̃·c + z_g·Σ q̃), warp-wide online softmax, then
+// lane = channel slice for P·V (again factored: Σ (p·s)·c + Σ p·z).
+// Codes enter the fp32 arithmetic as 1 + c/4 (exact), and the offset is
+// removed with the group sums.
+// ---------------------------------------------------------------------------
+template <int D, int GQ>
+__global__ void __launch_bounds__(512) history_simt_kernel(DecodeParams P) {
+    constexpr int CPL = D / 32;                 // channels per lane in P·V
+    extern __shared__ __align__(16) float s_dyn[];
+    float* sQ = s_dyn;                          // [Hq][D] q̃ of the current request
+    float* sP = sQ + P.Hq * D;                  // [warps][GQ][32] probabilities
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int64_t N = P.cprefix[P.batch];
+    const int64_t f0 = (int64_t)blockIdx.x * N / gridDim.x;
+    const int64_t f1 = (int64_t)(blockIdx.x + 1) * N / gridDim.x;
+    if (f0 >= f1) return;
+    const int ng = P.ng;
+    int cur_b = -1;
+    float* myP = sP + warp * GQ * 32;
+    int64_t f = f0;
+    while (f < f1) {
+        // segment: chunks [f, fe) of one request
+        const int b = chunk_request(P.cprefix, P.batch, f);
+        const int64_t fe = min(f1, (int64_t)P.cprefix[b + 1]);
+        const int c_first = (int)(f - P.cprefix[b]);
+        const int L = P.len[b];
+        const int h_end = d_hist_hi(L, P.S, P.W);
+        if (b != cur_b) {
+            __syncthreads();
+            for (int i = threadIdx.x; i < P.Hq * D; i += blockDim.x)
+                sQ[i] = P.qt[(int64_t)b * P.Hq * D + i];
+            __syncthreads();
+            cur_b = b;
+        }
+        const int t_begin = P.S + c_first * P.chunk;
+        const int t_end = min(h_end, P.S + (int)(fe - P.cprefix[b]) * P.chunk);
+        for (int hk = warp; hk < P.Hkv; hk += nwarps) {
+            const float* q = sQ + hk * P.g * D;
+            float m[GQ], l[GQ], acc[GQ][CPL], zacc[GQ];
+#pragma unroll
+            for (int j = 0; j < GQ; ++j) {
+                m[j] = -INFINITY;
+                l[j] = 0.f;
+                zacc[j] = 0.f;
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) acc[j][c] = 0.f;
+            }
+            const int my_gi = (lane * CPL) / P.G;   // group of this lane's channels
+            for (int t0 = t_begin; t0 < t_end; t0 += 32) {
+                const int p = t0 + lane;
+                const bool valid = p < t_end;
+                int slot = 0;
+                if (valid) {
+                    slot = P.page_table[(int64_t)b * P.pt_stride + p];
+                    if (slot < 0 || slot >= P.num_slots) {
+                        set_status(P.status, OSCAR_DEV_BAD_SLOT);
+                        slot = -1;
+                    }
+                }
+                const bool use = valid && slot >= 0;
+                const uint8_t* rec = P.records + ((int64_t)(use ? slot : 0) * P.Hkv + hk) * P.rec_bytes;
+                // ---- logits, lane = token ----
+                float logit[GQ];
+#pragma unroll
+                for (int j = 0; j < GQ; ++j) logit[j] = 0.f;
+                if (use) {
+                    for (int gi = 0; gi < ng; ++gi) {
+                        float dot[GQ];
+#pragma unroll
+                        for (int j = 0; j < GQ; ++j) dot[j] = 0.f;
+                        for (int w = gi * P.G / 16; w < (gi + 1) * P.G / 16; ++w) {
+                            const uint32_t word = *reinterpret_cast<const uint32_t*>(rec + 4 * w);
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                float cf[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    cf[e] = __uint_as_float(0x3F800000u | (((word >> (8 * q4 + 2 * e)) & 3u) << 21));
+#pragma unroll
+                                for (int j = 0; j < GQ; ++j) {
+                                    if (j < P.g) {
+                                        const float4 qv = *reinterpret_cast<const float4*>(q + j * D + 16 * w + 4 * q4);
+                                        dot[j] = fmaf(qv.x, cf[0], fmaf(qv.y, cf[1], fmaf(qv.z, cf[2], fmaf(qv.w, cf[3], dot[j]))));
+                                    }
+                                }
+                            }
+                        }
+                        const __half2 sz = *reinterpret_cast<const __half2*>(rec + D / 2 + 4 * gi);
+                        const float s = __low2float(sz), z = __high2float(sz);
+#pragma unroll
+                        for (int j = 0; j < GQ; ++j) {
+                            if (j < P.g) {
+                                const float Q = P.qsum[((int64_t)b * P.Hq + hk * P.g + j) * ng + gi];
+                                // Σ q̃(1 + c/4) = Q + Σq̃c/4  =>  s·Σq̃c + z·Q = 4s·(dot - Q) + z·Q
+                                logit[j] += 4.f * s * (dot[j] - Q) + z * Q;
+                            }
+                        }
+                    }
+                }
+                // ---- online softmax over the tile ----
+                float alpha[GQ];
+#pragma unroll
+                for (int j = 0; j < GQ; ++j) {
+                    float x = use ? logit[j] : -INFINITY;
+                    float tm = x;
+#pragma unroll
+                    for (int off = 16; off; off >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, off));
+                    const float mn = fmaxf(m[j], tm);
+                    alpha[j] = (m[j] == -INFINITY) ? 0.f : exp2f(m[j] - mn);
+                    const float pj = use ? exp2f(x - mn) : 0.f;
+                    m[j] = mn;
+                    float ps = pj;
+#pragma unroll
+                    for (int off = 16; off; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+                    l[j] = l[j] * alpha[j] + ps;
+                    myP[j * 32 + lane] = pj;
+                }
+#pragma unroll
+                for (int j = 0; j < GQ; ++j) {
+                    zacc[j] *= alpha[j];
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) acc[j][c] *= alpha[j];
+                }
+                __syncwarp();
+                // ---- P·V, lane = channels [lane·CPL, lane·CPL + CPL) ----
+                const int ntok = min(32, t_end - t0);
+                for (int t = 0; t < ntok; ++t) {
+                    const int st = __shfl_sync(0xffffffffu, use ? slot : -1, t);
+                    if (st < 0) continue;
+                    const uint8_t* rt = P.records + ((int64_t)st * P.Hkv + hk) * P.rec_bytes;
+                    uint32_t bits;
+                    if (CPL == 8) bits = *reinterpret_cast<const uint16_t*>(rt + D / 4 + lane * 2);
+                    else if (CPL == 4) bits = rt[D / 4 + lane];
+                    else bits = (rt[D / 4 + lane / 2] >> (4 * (lane & 1))) & 0xFu;
+                    const __half2 sz = *reinterpret_cast<const __half2*>(rt + D / 2 + 4 * ng + 4 * my_gi);
+                    const float s = __low2float(sz), z = __high2float(sz);
+                    float cf[CPL];
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) cf[c] = (float)((bits >> (2 * c)) & 3u);
+#pragma unroll
+                    for (int j = 0; j < GQ; ++j) {
+                        const float pj = myP[j * 32 + t];
+                        const float w = pj * s;
+                        zacc[j] = fmaf(pj, z, zacc[j]);
+#pragma unroll
+                        for (int c = 0; c < CPL; ++c) acc[j][c] = fmaf(w, cf[c], acc[j][c]);
+                    }
+                }
+                __syncwarp();
+            }
+            // ---- write the segment partial at its first chunk slot ----
+            const int64_t slot0 = (int64_t)b * P.max_chunks + c_first;
+#pragma unroll
+            for (int j = 0; j < GQ; ++j) {
+                if (j >= P.g) break;
+                const int hq = hk * P.g + j;
+                if (lane == 0) P.ml[slot0 * P.Hq + hq] = make_float2(m[j], l[j]);
+                float* o = P.po + (slot0 * P.Hq + hq) * D + lane * CPL;
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) o[c] = acc[j][c] + zacc[j];
+            }
+            // other chunks of the segment: marker (empty partial)
+            for (int64_t ff = f + 1 + lane; ff < fe; ff += 32) {
+                const int64_t sl = (int64_t)b * P.max_chunks + (int)(ff - P.cprefix[b]);
+                for (int j = 0; j < P.g; ++j) P.ml[sl * P.Hq + hk * P.g + j] = make_float2(-INFINITY, 0.f);
+            }
+        }
+        f = fe;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// combine: one block per (KV head, request).  BF16 windows attended directly
+// (fp32), history partials merged by log-sum-exp, R_Vᵀ applied to the merged
+// rotated-domain sum, the two domains merged and normalised.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(DecodeParams P) {
+    extern __shared__ __align__(16) float s_c[];
+    const int hk = blockIdx.x, b = blockIdx.y;
+    const int g = P.g, S = P.S, W = P.W;
+    const int nwin = S + W;
+    float* sq = s_c;                   // [g][D] unrotated q · qscale
+    float* slog = sq + g * D;          // [g][nwin] window logits -> probabilities
+    float* sorot = slog + g * nwin;    // [g][D] merged rotated-domain sum
+    float* sred = sorot + g * D;       // [g][4]: m_plain, l_plain, m_rot, l_rot
+    const int tid = threadIdx.x;
+    const int L = P.len[b];
+    const int rq = P.req[b];
+    float* outp = P.out + ((int64_t)b * P.Hq + hk * g) * D;
+    if (L <= 0) {
+        for (int i = tid; i < g * D; i += blockDim.x) outp[i] = 0.f;
+        return;
+    }
+    for (int i = tid; i < g * D; i += blockDim.x)
+        sq[i] = load_elem(P.q, ((int64_t)b * P.Hq + hk * g) * D + i, P.q_dtype) * P.qscale;
+    const int sink_end = min(S, L);
+    const int rec_lo = d_hist_hi(L, S, W);
+    const int n_rec = max(0, L - rec_lo);
+    const int nplain = sink_end + n_rec;
+    __syncthreads();
+    // window logits: thread per (token, head)
+    for (int i = tid; i < nplain * g; i += blockDim.x) {
+        const int t = i / g, j = i % g;
+        const uint16_t* kr = (t < sink_end)
+            ? P.sink + (((int64_t)rq * S + t) * P.Hkv + hk) * 2 * D
+            : P.recent + (((int64_t)rq * W + (rec_lo + t - sink_end) % W) * P.Hkv + hk) * 2 * D;
+        float acc = 0.f;
+        for (int c = 0; c < D; c += 2) {
+            const uint32_t two = *reinterpret_cast<const uint32_t*>(kr + c);
+            acc = fmaf(sq[j * D + c], __uint_as_float(two << 16), acc);
+            acc = fmaf(sq[j * D + c + 1], __uint_as_float(two & 0xFFFF0000u), acc);
+        }
+        slog[j * nwin + t] = acc;
+    }
+    __syncthreads();
+    const int warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+    // per head: window max/sum (warp j), and the LSE merge of the history partials
+    for (int j = warp; j < g; j += nw) {
+        float mx = -INFINITY;
+        for (int t = lane; t < nplain; t += 32) mx = fmaxf(mx, slog[j * nwin + t]);
+        for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        float sum = 0.f;
+        for (int t = lane; t < nplain; t += 32) {
+            const float p = exp2f(slog[j * nwin + t] - mx);
+            slog[j * nwin + t] = p;
+            sum += p;
+        }
+        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        const int nch = (d_hist_hi(L, S, W) - S + P.chunk - 1) / P.chunk;
+        const int hq = hk * g + j;
+        float M = -INFINITY;
+        for (int c = lane; c < max(nch, 0); c += 32)
+            M = fmaxf(M, P.ml[((int64_t)b * P.max_chunks + c) * P.Hq + hq].x);
+        for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float lr = 0.f;
+        for (int c = lane; c < max(nch, 0); c += 32) {
+            const float2 ml = P.ml[((int64_t)b * P.max_chunks + c) * P.Hq + hq];
+            if (ml.x != -INFINITY) lr += exp2f(ml.x - M) * ml.y;
+        }
+        for (int off = 16; off; off >>= 1) lr += __shfl_xor_sync(0xffffffffu, lr, off);
+        if (lane == 0) {
+            sred[j * 4 + 0] = mx;
+            sred[j * 4 + 1] = sum;
+            sred[j * 4 + 2] = M;
+            sred[j * 4 + 3] = lr;
+        }
+    }
+    __syncthreads();
+    // merged rotated sum: thread per (head, channel)
+    const int nch = max(0, (d_hist_hi(L, S, W) - S + P.chunk - 1) / P.chunk);
+    for (int i = tid; i < g * D; i += blockDim.x) {
+        const int j = i / D, c = i % D;
+        const int hq = hk * g + j;
+        const float M = sred[j * 4 + 2];
+        float acc = 0.f;
+        for (int ch = 0; ch < nch; ++ch) {
+            const int64_t sl = (int64_t)b * P.max_chunks + ch;
+            const float2 ml = P.ml[sl * P.Hq + hq];
+            if (ml.x == -INFINITY) continue;
+            acc = fmaf(exp2f(ml.x - M), P.po[(sl * P.Hq + hq) * D + c], acc);
+        }
+        sorot[i] = acc;
+    }
+    __syncthreads();
+    // out = (e^{m_p-M}·Σ p v + e^{m_r-M}·(Σ_rot)·R_Vᵀ) / (e^{m_p-M} l_p + e^{m_r-M} l_r)
+    for (int i = tid; i < g * D; i += blockDim.x) {
+        const int j = i / D, c = i % D;
+        const float mp = sred[j * 4 + 0], lp = sred[j * 4 + 1], mr = sred[j * 4 + 2], lr = sred[j * 4 + 3];
+        const float Mx = fmaxf(mp, mr);
+        const float wp = (mp == -INFINITY) ? 0.f : exp2f(mp - Mx);
+        const float wr = (mr == -INFINITY) ? 0.f : exp2f(mr - Mx);
+        float plain = 0.f;
+        for (int t = 0; t < nplain; ++t) {
+            const uint16_t* vr = (t < sink_end)
+                ? P.sink + (((int64_t)rq * S + t) * P.Hkv + hk) * 2 * D + D
+                : P.recent + (((int64_t)rq * W + (rec_lo + t - sink_end) % W) * P.Hkv + hk) * 2 * D + D;
+            plain = fmaf(slog[j * nwin + t], bf16_bits_to_f32(vr[c]), plain);
+        }
+        float rot = 0.f;
+        if (wr != 0.f) {
+            const float* rrow = P.rot_v + (int64_t)c * D;   // (x·R_Vᵀ)[c] = Σ_k x[k]·R_V[c][k]
+            for (int k = 0; k < D; ++k) rot = fmaf(sorot[j * D + k], rrow[k], rot);
+        }
+        const float den = wp * lp + wr * lr;
+        outp[j * D + c] = (wp * plain + wr * rot) / den;
+    }
+}
+
+}  // namespace oscar
+
+using namespace oscar;
+
+static int decode_validate(const oscar_config* cfg, const oscar_layer_cache* cache, int32_t batch,
+                           int32_t max_seq_len, int64_t pt_stride) {
+    int rc = validate_config(cfg);
+    if (rc) return rc;
+    rc = validate_cache(cfg, cache);
+    if (rc) return rc;
+    if (batch < 0 || batch > kMaxDecodeBatch)
+        return fail(OSCAR_ERR_ARG, "batch must be in [0, %d] (got %d)", kMaxDecodeBatch, batch);
+    if (max_seq_len < 1) return fail(OSCAR_ERR_ARG, "max_seq_len must be >= 1");
+    if (pt_stride < max_seq_len) return fail(OSCAR_ERR_ARG, "pt_stride (%lld) must be >= max_seq_len (%d)",
+                                             (long long)pt_stride, max_seq_len);
+    if ((int64_t)cfg->num_q_heads * cfg->head_dim > 16384)
+        return fail(OSCAR_ERR_ARG, "num_q_heads * head_dim must be <= 16384");
+    return OSCAR_OK;
+}
+
+extern "C" int oscar_decode_workspace_bytes(const oscar_config* cfg, int32_t batch, int32_t max_seq_len,
+                                            size_t* bytes) {
+    clear_error();
+    int rc = validate_config(cfg);
+    if (rc) return rc;
+    if (!bytes) return fail(OSCAR_ERR_NULL, "bytes is NULL");
+    if (batch < 0 || batch > kMaxDecodeBatch || max_seq_len < 1)
+        return fail(OSCAR_ERR_ARG, "batch in [0, %d] and max_seq_len >= 1 required", kMaxDecodeBatch);
+    const int nsm = sm_count();
+    if (nsm <= 0) return OSCAR_ERR_CUDA;
+    *bytes = make_plan(cfg, batch, max_seq_len, nsm).total;
+    return OSCAR_OK;
+}
+
+namespace oscar {
+int launch_history_mma(const DecodeParams& P, int head_dim, cudaStream_t st, bool* launched);
+}
+
+template <int D>
+static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
+    prep_kernel<D><<<P.batch, 256, 0, st>>>(P);
+    int rc = check_cuda("prep_kernel launch");
+    if (rc) return rc;
+    bool done = false;
+    const int prof = prof_begin(0, st);
+    if (impl != 1) {
+        rc = launch_history_mma(P, D, st, &done);
+        if (rc) return rc;
+    }
+    if (!done) {
+        const int nwarps = std::min(16, P.Hkv);
+        const int threads = 32 * nwarps;
+        const int gq = P.g <= 4 ? 4 : (P.g <= 8 ? 8 : 16);
+        const size_t smem = ((size_t)P.Hq * D + (size_t)nwarps * gq * 32) * 4;
+        auto pick = [&](auto kern) -> int {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+                return check_cuda("cudaFuncSetAttribute(history_simt_kernel)");
+            int per_sm = 0;
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+            const int grid = std::max(1, sm_count() * std::max(1, per_sm));
+            kern<<<grid, threads, smem, st>>>(P);
+            return check_cuda("history_simt_kernel launch");
+        };
+        if (gq == 4) rc = pick(history_simt_kernel<D, 4>);
+        else if (gq == 8) rc = pick(history_simt_kernel<D, 8>);
+        else rc = pick(history_simt_kernel<D, 16>);
+        if (rc) return rc;
+    }
+    prof_end(prof, st);
+    const size_t csmem = ((size_t)P.g * D * 2 + (size_t)P.g * (P.S + P.W) + (size_t)P.g * 4) * 4;
+    if (cudaFuncSetAttribute(combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem) != cudaSuccess)
+        return check_cuda("cudaFuncSetAttribute(combine_kernel)");
+    combine_kernel<D><<<dim3(P.Hkv, P.batch), 256, csmem, st>>>(P);
+    return check_cuda("combine_kernel launch");
+}
+
+static int decode_impl(const oscar_config* cfg, const oscar_layer_cache* cache, const void* q,
+                       const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens,
+                       const int32_t* req_idx, int32_t batch, int32_t max_seq_len, float* out,
+                       void* workspace, size_t workspace_bytes, void* stream, int impl) {
+    clear_error();
+    int rc = decode_validate(cfg, cache, batch, max_seq_len, pt_stride);
+    if (rc) return rc;
+    if (batch == 0) return OSCAR_OK;
+    if (!q || !page_table || !seq_lens || !out) return fail(OSCAR_ERR_NULL, "q, page_table, seq_lens and out are required");
+    const int nsm = sm_count();
+    if (nsm <= 0) return OSCAR_ERR_CUDA;
+    const DecodePlan plan = make_plan(cfg, batch, max_seq_len, nsm);
+    if (!workspace) return fail(OSCAR_ERR_WORKSPACE, "workspace is NULL");
+    if (workspace_bytes < plan.total)
+        return fail(OSCAR_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", workspace_bytes, plan.total);
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+        return fail(OSCAR_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    DecodeParams P;
+    P.q = q;
+    P.q_dtype = cfg->q_dtype;
+    P.page_table = page_table;
+    P.pt_stride = pt_stride;
+    P.seq_lens = seq_lens;
+    P.req_idx = req_idx;
+    P.batch = batch;
+    P.max_seq_len = max_seq_len;
+    P.out = out;
+    P.records = cache->records;
+    P.sink = cache->sink;
+    P.recent = cache->recent;
+    P.rot_k = cache->rot_k;
+    P.rot_v = cache->rot_v;
+    P.num_slots = cache->num_slots;
+    P.max_reqs = cache->max_reqs;
+    P.Hq = cfg->num_q_heads;
+    P.Hkv = cfg->num_kv_heads;
+    P.g = P.Hq / P.Hkv;
+    P.S = cfg->sink;
+    P.W = cfg->recent;
+    P.G = cfg->group_size;
+    P.ng = cfg->head_dim / cfg->group_size;
+    P.rec_bytes = record_layout(cfg->head_dim, cfg->group_size).bytes;
+    P.chunk = plan.chunk;
+    P.max_chunks = plan.max_chunks;
+    P.n_frag_tiles = plan.n_frag_tiles;
+    P.qscale = (float)(1.4426950408889634 / std::sqrt((double)cfg->head_dim));
+    char* ws = reinterpret_cast<char*>(workspace);
+    P.len = reinterpret_cast<int32_t*>(ws + plan.off_len);
+    P.req = reinterpret_cast<int32_t*>(ws + plan.off_req);
+    P.cprefix = reinterpret_cast<int32_t*>(ws + plan.off_cprefix);
+    P.qt = reinterpret_cast<float*>(ws + plan.off_qt);
+    P.qsum = reinterpret_cast<float*>(ws + plan.off_qsum);
+    P.qfrag = reinterpret_cast<uint2*>(ws + plan.off_qfrag);
+    P.ml = reinterpret_cast<float2*>(ws + plan.off_ml);
+    P.po = reinterpret_cast<float*>(ws + plan.off_o);
+    P.status = status_word();
+    if (!P.status) return OSCAR_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    switch (cfg->head_dim) {
+        case 64: return launch_decode<64>(P, st, impl);
+        case 128: return launch_decode<128>(P, st, impl);
+        default: return launch_decode<256>(P, st, impl);
+    }
+}
+
+extern "C" int oscar_decode_attention(const oscar_config* cfg, const oscar_layer_cache* cache, const void* q,
+                                      const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens,
+                                      const int32_t* req_idx, int32_t batch, int32_t max_seq_len, float* out,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+    return decode_impl(cfg, cache, q, page_table, pt_stride, seq_lens, req_idx, batch, max_seq_len, out,
+                       workspace, workspace_bytes, stream, 0);
+}
+
+extern "C" int oscar_decode_attention_simt(const oscar_config* cfg, const oscar_layer_cache* cache, const void* q,
+                                           const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens,
+                                           const int32_t* req_idx, int32_t batch, int32_t max_seq_len, float* out,
+                                           void* workspace, size_t workspace_bytes, void* stream) {
+    return decode_impl(cfg, cache, q, page_table, pt_stride, seq_lens, req_idx, batch, max_seq_len, out,
+                       workspace, workspace_bytes, stream, 1);
+}

@@ -1,0 +1,55 @@
+// Internal declarations shared by the host and CUDA translation units of
+// liboscar.so.  Not part of the public ABI (include/oscar.h is).
+#pragma once
+
+#include <stdint.h>
+#include <stddef.h>
+
+#include <cuda_runtime.h>
+
+#include "oscar.h"
+
+namespace oscar {
+
+// Record geometry of one (slot, KV head) entry of the INT2 pool:
+// [K codes d/4][V codes d/4][K (s,z) fp16 pairs x d/G][V (s,z) x d/G], padded to 16.
+struct RecordLayout {
+    int d, G, ng;
+    int k_codes, v_codes, k_sz, v_sz, bytes;
+};
+
+inline RecordLayout record_layout(int d, int G) {
+    RecordLayout r;
+    r.d = d;
+    r.G = G;
+    r.ng = d / G;
+    r.k_codes = 0;
+    r.v_codes = d / 4;
+    r.k_sz = d / 2;
+    r.v_sz = d / 2 + 4 * r.ng;
+    r.bytes = (d / 2 + 8 * r.ng + 15) / 16 * 16;
+    return r;
+}
+
+// Thread-local error message; returns `code` for convenient `return fail(...)`.
+int fail(int code, const char* fmt, ...);
+void clear_error();
+
+// Host-side validation of a layer configuration (sets the error message).
+int validate_config(const oscar_config* cfg);
+int validate_cache(const oscar_config* cfg, const oscar_layer_cache* cache);
+
+// Per-device address of the device status word (OSCAR_DEV_* bits).
+int* status_word();
+
+// Number of SMs of the current device (cached).
+int sm_count();
+
+// Converts the pending CUDA error (if any) into OSCAR_ERR_CUDA.
+int check_cuda(const char* what);
+
+// Benchmark timing of the dominant kernels (see oscar_profile_enable).
+int prof_begin(int kind, cudaStream_t st);   // returns a slot or -1 when disabled
+void prof_end(int slot, cudaStream_t st);
+
+}  // namespace oscar

@@ -1,0 +1,150 @@
+// Runtime helpers of liboscar.so: the per-device status word written by the
+// kernels' bounds checks, the SM count used to size persistent grids, and the
+// mapping of CUDA runtime errors to OSCAR_ERR_CUDA.
+#include <cuda_runtime.h>
+
+#include "oscar_internal.h"
+
+namespace oscar {
+
+// OR of OSCAR_DEV_* bits; one instance per device (module-scope variable).
+__device__ int g_status_word;
+
+static constexpr int kMaxDevices = 64;
+static int* g_status_ptr[kMaxDevices];
+static int g_sm_count[kMaxDevices];
+
+static int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+int* status_word() {
+    const int dev = current_device();
+    if (dev < 0) {
+        fail(OSCAR_ERR_CUDA, "no current CUDA device");
+        return nullptr;
+    }
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
+        if (e != cudaSuccess) {
+            fail(OSCAR_ERR_CUDA, "cudaGetSymbolAddress(status word): %s", cudaGetErrorString(e));
+            return nullptr;
+        }
+        g_status_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+int sm_count() {
+    const int dev = current_device();
+    if (dev < 0) {
+        fail(OSCAR_ERR_CUDA, "no current CUDA device");
+        return 0;
+    }
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            fail(OSCAR_ERR_CUDA, "cannot query the SM count");
+            return 0;
+        }
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+int check_cuda(const char* what) {
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) return OSCAR_OK;
+    return fail(OSCAR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace oscar
+
+extern "C" int oscar_device_status(int32_t* flags, int32_t clear) {
+    using namespace oscar;
+    clear_error();
+    if (!flags) return fail(OSCAR_ERR_NULL, "flags is NULL");
+    int v = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int));
+    if (e == cudaSuccess && clear) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int));
+    }
+    if (e != cudaSuccess) return fail(OSCAR_ERR_CUDA, "reading the device status: %s", cudaGetErrorString(e));
+    *flags = v;
+    return OSCAR_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Kernel timing for benchmarks: when enabled, the entry points record a CUDA
+// event pair around their dominant kernel on the call's stream (kind 0: the
+// decode history kernel, kind 1: the append quantise kernel).
+// ---------------------------------------------------------------------------
+#include <vector>
+#include <mutex>
+
+namespace oscar {
+
+struct ProfSlot { cudaEvent_t a, b; int kind; };
+static std::mutex g_prof_mu;
+static bool g_prof_on = false;
+static std::vector<ProfSlot> g_prof_slots;
+static size_t g_prof_used = 0;
+
+int prof_begin(int kind, cudaStream_t st) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_on) return -1;
+    if (g_prof_used == g_prof_slots.size()) {
+        if (g_prof_slots.size() >= 65536) return -1;
+        ProfSlot s;
+        if (cudaEventCreate(&s.a) != cudaSuccess) return -1;
+        if (cudaEventCreate(&s.b) != cudaSuccess) { cudaEventDestroy(s.a); return -1; }
+        g_prof_slots.push_back(s);
+    }
+    const int idx = (int)g_prof_used++;
+    g_prof_slots[idx].kind = kind;
+    cudaEventRecord(g_prof_slots[idx].a, st);
+    return idx;
+}
+
+void prof_end(int idx, cudaStream_t st) {
+    if (idx < 0) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    cudaEventRecord(g_prof_slots[idx].b, st);
+}
+
+}  // namespace oscar
+
+extern "C" int oscar_profile_enable(int32_t enable) {
+    using namespace oscar;
+    clear_error();
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_on = enable != 0;
+    g_prof_used = 0;
+    return OSCAR_OK;
+}
+
+extern "C" int oscar_profile_read(int32_t kind, double* total_ms, int64_t* launches) {
+    using namespace oscar;
+    clear_error();
+    if (!total_ms || !launches) return fail(OSCAR_ERR_NULL, "outputs must be non-NULL");
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    double ms = 0.0;
+    int64_t n = 0;
+    for (size_t i = 0; i < g_prof_used; ++i) {
+        if (g_prof_slots[i].kind != kind) continue;
+        float t = 0.f;
+        cudaError_t e = cudaEventSynchronize(g_prof_slots[i].b);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&t, g_prof_slots[i].a, g_prof_slots[i].b);
+        if (e != cudaSuccess) return fail(OSCAR_ERR_CUDA, "event timing: %s", cudaGetErrorString(e));
+        ms += t;
+        ++n;
+    }
+    *total_ms = ms;
+    *launches = n;
+    return OSCAR_OK;
+}

@@ -1,0 +1,280 @@
+"""ctypes binding of liboscar.so (include/oscar.h): argument marshalling only.
+
+Every step of the append and decode paths runs in the library's CUDA kernels;
+this module only checks tensor shapes / dtypes / devices, passes raw pointers
+and the current CUDA stream, and turns error codes into exceptions.  There is
+no fallback: if liboscar.so is missing the import of the library fails loudly.
+"""
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liboscar.so")
+
+OSCAR_OK = 0
+ERR_NAMES = {-1: "OSCAR_ERR_ARG", -2: "OSCAR_ERR_NULL", -3: "OSCAR_ERR_WORKSPACE",
+             -4: "OSCAR_ERR_CUDA", -5: "OSCAR_ERR_NUMERIC"}
+DTYPE_BF16 = 0
+DTYPE_F32 = 1
+DEV_BAD_SLOT, DEV_BAD_LEN, DEV_BAD_REQ, DEV_TIMEOUT = 1, 2, 4, 8
+
+
+class OscarError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("%s (%d): %s" % (ERR_NAMES.get(code, "?"), code, msg))
+        self.code = code
+
+
+class CConfig(ctypes.Structure):
+    _fields_ = [("head_dim", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("group_size", ctypes.c_int32),
+                ("sink", ctypes.c_int32), ("recent", ctypes.c_int32),
+                ("clip_ratio", ctypes.c_float), ("kv_dtype", ctypes.c_int32),
+                ("q_dtype", ctypes.c_int32)]
+
+
+class CLayerCache(ctypes.Structure):
+    _fields_ = [("records", ctypes.c_void_p), ("sink", ctypes.c_void_p),
+                ("recent", ctypes.c_void_p), ("rot_k", ctypes.c_void_p),
+                ("rot_v", ctypes.c_void_p), ("num_slots", ctypes.c_int64),
+                ("max_reqs", ctypes.c_int32)]
+
+
+_lib = None
+
+_SIGS = {
+    "oscar_version": ([], ctypes.c_char_p),
+    "oscar_last_error": ([], ctypes.c_char_p),
+    "oscar_record_bytes": ([ctypes.POINTER(CConfig), ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+    "oscar_cache_bytes_per_token": ([ctypes.POINTER(CConfig), ctypes.POINTER(ctypes.c_int64),
+                                     ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+    "oscar_covariance": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
+    "oscar_value_covariance": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
+    "oscar_build_rotation": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                              ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "oscar_quantize_append": ([ctypes.POINTER(CConfig), ctypes.POINTER(CLayerCache), ctypes.c_void_p,
+                               ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                               ctypes.c_void_p], ctypes.c_int),
+    "oscar_decode_workspace_bytes": ([ctypes.POINTER(CConfig), ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+    "oscar_decode_attention": ([ctypes.POINTER(CConfig), ctypes.POINTER(CLayerCache), ctypes.c_void_p,
+                                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
+    "oscar_decode_attention_simt": ([ctypes.POINTER(CConfig), ctypes.POINTER(CLayerCache), ctypes.c_void_p,
+                                     ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
+    "oscar_device_status": ([ctypes.POINTER(ctypes.c_int32), ctypes.c_int32], ctypes.c_int),
+    "oscar_profile_enable": ([ctypes.c_int32], ctypes.c_int),
+    "oscar_profile_read": ([ctypes.c_int32, ctypes.POINTER(ctypes.c_double),
+                            ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+}
+
+
+def lib():
+    """The loaded liboscar.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError("liboscar.so is not built (run __graft_entry__.build() or "
+                               "python rotated_int2_kv_gb300/build.py)")
+        L = ctypes.CDLL(_LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(rc):
+    if rc != OSCAR_OK:
+        raise OscarError(rc, lib().oscar_last_error().decode())
+
+
+def last_error():
+    return lib().oscar_last_error().decode()
+
+
+@dataclass
+class Config:
+    head_dim: int
+    num_q_heads: int
+    num_kv_heads: int
+    group_size: int = 64
+    sink: int = 64
+    recent: int = 256
+    clip_ratio: float = 0.9
+    kv_dtype: torch.dtype = torch.bfloat16
+    q_dtype: torch.dtype = torch.bfloat16
+
+    def c(self):
+        def code(dt):
+            if dt == torch.bfloat16:
+                return DTYPE_BF16
+            if dt == torch.float32:
+                return DTYPE_F32
+            raise ValueError("dtype must be torch.bfloat16 or torch.float32")
+        return CConfig(self.head_dim, self.num_q_heads, self.num_kv_heads, self.group_size,
+                       self.sink, self.recent, self.clip_ratio, code(self.kv_dtype),
+                       code(self.q_dtype))
+
+    @property
+    def gqa(self):
+        return self.num_q_heads // self.num_kv_heads
+
+
+def version():
+    return lib().oscar_version().decode()
+
+
+def record_bytes(cfg):
+    out = ctypes.c_int64()
+    _check(lib().oscar_record_bytes(ctypes.byref(cfg.c()), ctypes.byref(out)))
+    return out.value
+
+
+def cache_bytes_per_token(cfg):
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().oscar_cache_bytes_per_token(ctypes.byref(cfg.c()), ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+# -- host rotation construction ---------------------------------------------
+
+def covariance(samples):
+    X = np.ascontiguousarray(samples, dtype=np.float64)
+    n, d = X.shape
+    C = np.empty((d, d), np.float64)
+    _check(lib().oscar_covariance(X.ctypes.data, n, d, C.ctypes.data))
+    return C
+
+
+def value_covariance(scores, values):
+    S = np.ascontiguousarray(scores, dtype=np.float64)
+    V = np.ascontiguousarray(values, dtype=np.float64)
+    C = np.empty((V.shape[1], V.shape[1]), np.float64)
+    _check(lib().oscar_value_covariance(S.ctypes.data, V.ctypes.data, S.shape[0], S.shape[1],
+                                        V.shape[1], C.ctypes.data))
+    return C
+
+
+def build_rotation(cov, d, use_bitrev=True):
+    """Returns (R fp32, R fp64, eigenvalues) as NumPy arrays (host)."""
+    R32 = np.empty((d, d), np.float32)
+    R64 = np.empty((d, d), np.float64)
+    w = np.empty(d, np.float64)
+    cp = None
+    if cov is not None:
+        cov = np.ascontiguousarray(cov, dtype=np.float64)
+        cp = cov.ctypes.data
+    _check(lib().oscar_build_rotation(cp, d, int(bool(use_bitrev)), R32.ctypes.data,
+                                      R64.ctypes.data, w.ctypes.data))
+    return R32, R64, w
+
+
+# -- device cache -------------------------------------------------------------
+
+class LayerCache:
+    """Device buffers of one layer (allocated with PyTorch, owned here)."""
+
+    def __init__(self, cfg, num_slots, max_reqs, rot_k, rot_v, device="cuda"):
+        self.cfg = cfg
+        rb = record_bytes(cfg)
+        H, d = cfg.num_kv_heads, cfg.head_dim
+        self.records = torch.zeros((num_slots, H, rb), dtype=torch.uint8, device=device)
+        self.sink = torch.zeros((max_reqs, max(cfg.sink, 1), H, 2, d), dtype=torch.bfloat16, device=device)
+        self.recent = torch.zeros((max_reqs, cfg.recent, H, 2, d), dtype=torch.bfloat16, device=device)
+        self.rot_k = torch.as_tensor(np.ascontiguousarray(rot_k, np.float32)).to(device)
+        self.rot_v = torch.as_tensor(np.ascontiguousarray(rot_v, np.float32)).to(device)
+        self.num_slots = num_slots
+        self.max_reqs = max_reqs
+
+    def c(self):
+        return CLayerCache(self.records.data_ptr(), self.sink.data_ptr(), self.recent.data_ptr(),
+                           self.rot_k.data_ptr(), self.rot_v.data_ptr(), self.num_slots, self.max_reqs)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s (got %s)" % (name, dtype, t.dtype))
+    return t.data_ptr()
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def quantize_append(cache, k, v, cu_new, start_pos, page_table, req_idx=None, stream=None):
+    """Appends new rows k, v: (T, Hkv, d) for a batch; see oscar_quantize_append."""
+    cfg = cache.cfg
+    T = k.shape[0]
+    if k.shape != v.shape or k.dim() != 3:
+        raise ValueError("k and v must both be (T, Hkv, d)")
+    B = start_pos.shape[0]
+    if cu_new.shape[0] != B + 1:
+        raise ValueError("cu_new must have batch + 1 entries")
+    _check(lib().oscar_quantize_append(
+        ctypes.byref(cfg.c()), ctypes.byref(cache.c()), _ptr(k, cfg.kv_dtype, "k"),
+        _ptr(v, cfg.kv_dtype, "v"), T, _ptr(cu_new, torch.int32, "cu_new"),
+        _ptr(start_pos, torch.int32, "start_pos"), _ptr(req_idx, torch.int32, "req_idx"),
+        _ptr(page_table, torch.int32, "page_table"), page_table.shape[1], B, _stream(stream)))
+
+
+def decode_workspace_bytes(cfg, batch, max_seq_len):
+    out = ctypes.c_size_t()
+    _check(lib().oscar_decode_workspace_bytes(ctypes.byref(cfg.c()), batch, max_seq_len, ctypes.byref(out)))
+    return out.value
+
+
+def alloc_workspace(cfg, batch, max_seq_len, device="cuda"):
+    n = decode_workspace_bytes(cfg, batch, max_seq_len)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def decode_attention(cache, q, page_table, seq_lens, max_seq_len, workspace, req_idx=None, out=None,
+                     stream=None, impl="auto"):
+    """One decode step: q (B, Hq, d) -> out (B, Hq, d) fp32.  impl: 'auto' or 'simt'."""
+    cfg = cache.cfg
+    B = q.shape[0]
+    if out is None:
+        out = torch.empty((B, cfg.num_q_heads, cfg.head_dim), dtype=torch.float32, device=q.device)
+    fn = lib().oscar_decode_attention if impl == "auto" else lib().oscar_decode_attention_simt
+    _check(fn(ctypes.byref(cfg.c()), ctypes.byref(cache.c()), _ptr(q, cfg.q_dtype, "q"),
+              _ptr(page_table, torch.int32, "page_table"), page_table.shape[1],
+              _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(req_idx, torch.int32, "req_idx"), B,
+              max_seq_len, _ptr(out, torch.float32, "out"), _ptr(workspace, torch.uint8, "workspace"),
+              workspace.numel(), _stream(stream)))
+    return out
+
+
+def device_status(clear=True):
+    f = ctypes.c_int32()
+    _check(lib().oscar_device_status(ctypes.byref(f), int(bool(clear))))
+    return f.value
+
+
+def profile_enable(on=True):
+    """Start (or stop) event timing of the dominant kernels; clears old records."""
+    _check(lib().oscar_profile_enable(int(bool(on))))
+
+
+def profile_read(kind):
+    """(total milliseconds, launches) of kernel `kind` (0: decode history, 1: append quantise)."""
+    ms, n = ctypes.c_double(), ctypes.c_int64()
+    _check(lib().oscar_profile_read(kind, ctypes.byref(ms), ctypes.byref(n)))
+    return ms.value, n.value

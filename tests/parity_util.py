@@ -1,0 +1,116 @@
+"""Helpers for the GPU parity tests: moving an oracle cache to the device,
+and classifying INT2 record mismatches against the acceptance rule
+
+    codes are bit-exact except where the oracle's pre-rounding value
+    u = (y - z)/s lies within 1e-6·max(1, |u|) of a rounding boundary, and
+    (s, z) are exact except where the fp32 value rounded to fp16 lies within
+    1e-6 relative of an fp16 rounding tie (all codes of such a group excused).
+"""
+
+import numpy as np
+import torch
+
+import oracle
+from oracle import quant as oq
+
+REL_TIE = 1e-6
+
+
+def fp16_near_tie(x):
+    """True where fp32 x is within REL_TIE (relative) of a midpoint between fp16 neighbours."""
+    x = np.asarray(x, np.float32)
+    h = x.astype(np.float16)
+    up = np.nextafter(h, np.float16(np.inf)).astype(np.float32)
+    dn = np.nextafter(h, np.float16(-np.inf)).astype(np.float32)
+    hf = h.astype(np.float32)
+    mid = np.where(x >= hf, (hf + up) / 2, (hf + dn) / 2)
+    return np.abs(x.astype(np.float64) - mid) <= REL_TIE * np.maximum(np.abs(x), 1e-30)
+
+
+def classify_records(gpu_rec, ora_cache, slots, ora_y=None):
+    """Compare GPU records with the oracle's for the given slots (all heads).
+
+    Returns dict(exact, code_ties, sz_ties, bad) counted over (slot, head, K|V, group).
+    `ora_y` (optional): dict slot -> (ky (Hkv, d), vy (Hkv, d)) fp32 rotated rows of the oracle.
+    """
+    cfg = ora_cache.cfg
+    d, G, H = cfg.head_dim, cfg.group_size, cfg.num_kv_heads
+    ng = d // G
+    r = np.float32(cfg.clip_ratio)
+    slots = np.asarray(slots, dtype=np.int64)
+    want = ora_cache.records()[slots]
+    got = np.asarray(gpu_rec)[slots]
+    stats = dict(exact=0, code_ties=0, sz_ties=0, bad=0, bad_examples=[])
+    diff = (want != got).any(axis=-1)               # (n, H)
+    stats["exact"] = int((~diff).sum()) * 2 * ng
+    for i, h in zip(*np.nonzero(diff)):
+        s = int(slots[i])
+        gk = oq.unpack_record(got[i, h], d, G)
+        wk = oq.unpack_record(want[i, h], d, G)
+        for mat in (0, 1):
+            gc, gs, gz = gk[3 * mat: 3 * mat + 3]
+            wc, ws, wz = wk[3 * mat: 3 * mat + 3]
+            y = None
+            if ora_y is not None:
+                y = ora_y[s][mat][h]
+            elif s in (ora_cache.ky if mat == 0 else ora_cache.vy):
+                y = (ora_cache.ky if mat == 0 else ora_cache.vy)[s][h]
+            for gi in range(ng):
+                sl = slice(gi * G, (gi + 1) * G)
+                same_sz = gs[gi] == ws[gi] and gz[gi] == wz[gi]
+                if same_sz and np.array_equal(gc[sl], wc[sl]):
+                    stats["exact"] += 1
+                    continue
+                if y is None:
+                    stats["bad"] += 1
+                    continue
+                yg = y[sl].astype(np.float32)
+                lo = np.float32(r * yg.min())
+                hi = np.float32(r * yg.max())
+                s32 = np.float32(np.float32(hi - lo) / np.float32(3.0))
+                if not same_sz:
+                    if fp16_near_tie(s32) or fp16_near_tie(lo):
+                        stats["sz_ties"] += 1
+                    else:
+                        stats["bad"] += 1
+                        stats["bad_examples"].append(("sz", s, int(h), mat, gi))
+                    continue
+                sf = np.float32(ws[gi])
+                zf = np.float32(wz[gi])
+                u = (np.float32(yg - zf) / sf).astype(np.float32)
+                bad_here = False
+                for j in np.nonzero(gc[sl] != wc[sl])[0]:
+                    uj = float(u[j])
+                    near = min(abs(uj - (k + 0.5)) for k in range(3))
+                    if near > REL_TIE * max(1.0, abs(uj)):
+                        bad_here = True
+                if bad_here:
+                    stats["bad"] += 1
+                    stats["bad_examples"].append(("code", s, int(h), mat, gi))
+                else:
+                    stats["code_ties"] += 1
+    return stats
+
+
+def device_cache_from_oracle(ops, ocache, cfg, device="cuda"):
+    """A LayerCache holding exactly the oracle cache's records and windows."""
+    dc = ops.LayerCache(cfg, ocache.num_slots, ocache.max_reqs, ocache.rot_k.astype(np.float32),
+                        ocache.rot_v.astype(np.float32), device=device)
+    dc.records.copy_(torch.from_numpy(ocache.records()))
+    sink_bits, ring_bits = ocache.window_bits()
+    if cfg.sink > 0:
+        dc.sink.copy_(torch.from_numpy(sink_bits.view(np.int16)).view(torch.bfloat16))
+    dc.recent.copy_(torch.from_numpy(ring_bits.view(np.int16)).view(torch.bfloat16))
+    return dc
+
+
+def attn_errors(got, want):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    err = float(np.abs(got - want).max())
+    rel = float(np.linalg.norm(got - want) / max(np.linalg.norm(want), 1e-30))
+    return err, rel
+
+
+ATOL = 2e-3      # max-abs bound on attention outputs
+RTOL_L2 = 1e-3   # relative-L2 bound on attention outputs

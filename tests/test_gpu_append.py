@@ -1,0 +1,147 @@
+"""GPU parity of oscar_quantize_append against the fp64 oracle.
+
+INT2 records: bit-exact except counted rounding-boundary cases (see
+parity_util).  BF16 windows: bit-exact.  Slots outside the history: untouched.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from rotated_int2_kv_gb300 import synth
+from parity_util import classify_records
+
+pytestmark = pytest.mark.gpu
+
+SEED = 1234
+
+
+def _rotations(d, seed=SEED):
+    Rk, _ = oracle.build_rotation(oracle.covariance(synth.calib_samples(seed, 0, d)), d)
+    Rv, _ = oracle.build_rotation(oracle.covariance(synth.calib_samples(seed, 1, d)), d)
+    return Rk.astype(np.float32), Rv.astype(np.float32)
+
+
+def run_append_scenario(d, Hq, Hkv, G, S, W, kv_dtype, calls, clip=0.9, mode="fixed4", pool_extra=37,
+                        seed=SEED):
+    from rotated_int2_kv_gb300 import ops
+    B = len(calls[0])
+    Lfin = [sum(c[b] for c in calls) for b in range(B)]
+    maxL = max(max(Lfin), 1)
+    pool = B * maxL + pool_extra
+    cfg = ops.Config(d, Hq, Hkv, G, S, W, clip, kv_dtype=kv_dtype)
+    Rk, Rv = _rotations(d, seed)
+    pt = synth.page_table(seed, B, maxL, pool, shuffled=True)
+    req = torch.tensor(list(reversed(range(B))), dtype=torch.int32)   # window rows permuted
+    max_reqs = B + 2
+    dev = torch.device("cuda")
+    dc = ops.LayerCache(cfg, pool, max_reqs, Rk, Rv, device=dev)
+    oc = oracle.OracleCache(oracle.OracleConfig(d, Hq, Hkv, G, S, W, clip), pool, max_reqs, Rk, Rv)
+    scales = synth.outlier_scales(seed, Hkv, d, mode)
+    pos = [0] * B
+    for call in calls:
+        ks, vs = [], []
+        for b in range(B):
+            k, v = synth.kv_tokens(seed, b, pos[b], call[b], Hkv, d, scales, dtype=kv_dtype)
+            ks.append(k)
+            vs.append(v)
+        k = torch.cat(ks)
+        v = torch.cat(vs)
+        cu = np.concatenate([[0], np.cumsum(call)]).astype(np.int32)
+        ops.quantize_append(dc, k.to(dev), v.to(dev), torch.from_numpy(cu).to(dev),
+                            torch.tensor(pos, dtype=torch.int32, device=dev), pt.to(dev), req_idx=req.to(dev))
+        oc.append(k.float().numpy(), v.float().numpy(), cu, pos, req.numpy(), pt.numpy(), keep_y=True)
+        pos = [pos[b] + call[b] for b in range(B)]
+    torch.cuda.synchronize()
+    assert ops.device_status() == 0
+    gpu_rec = dc.records.cpu().numpy()
+    hist_slots = []
+    for b in range(B):
+        _, lo, hi, rlo, rhi = oracle.regions(Lfin[b], S, W)
+        hist_slots += list(pt[b, lo:hi].numpy())
+    hist_slots = np.array(sorted(hist_slots), dtype=np.int64)
+    stats = classify_records(gpu_rec, oc, hist_slots)
+    assert stats["bad"] == 0, stats
+    others = np.setdiff1d(np.arange(pool), hist_slots)
+    assert not gpu_rec[others].any(), "records outside the history were written"
+    # windows: bit-exact bf16
+    sink_bits, ring_bits = oc.window_bits()
+    gs = dc.sink.view(torch.int16).cpu().numpy().view(np.uint16)
+    gr = dc.recent.view(torch.int16).cpu().numpy().view(np.uint16)
+    for b in range(B):
+        rq = int(req[b])
+        se, lo, hi, rlo, rhi = oracle.regions(Lfin[b], S, W)
+        if S > 0:
+            assert np.array_equal(gs[rq, :se], sink_bits[rq, :se])
+        idx = np.arange(rlo, rhi) % W
+        assert np.array_equal(gr[rq, idx], ring_bits[rq, idx])
+    return stats
+
+
+def test_tiny_config_single_fill_fp32():
+    # 1 layer, 4 q / 1 KV head, d 128, 64 + 704 + 256 tokens, fp32 K/V, group 64
+    st = run_append_scenario(128, 4, 1, 64, 64, 256, torch.float32, [[1024]], pool_extra=0)
+    assert st["exact"] > 0
+
+
+def test_spill_heavy_small_windows_ragged():
+    calls = [[5, 0, 17], [1, 1, 1], [20, 3, 0], [1, 30, 2], [9, 9, 9], [0, 0, 1], [40, 1, 64]]
+    run_append_scenario(64, 12, 2, 32, 4, 8, torch.bfloat16, calls)
+
+
+def test_wide_head_gqa6_chunks_then_decode_steps():
+    calls = [[700, 400], [1, 1], [300, 0], [1, 1], [0, 513], [1, 1]]
+    run_append_scenario(256, 24, 4, 128, 64, 256, torch.bfloat16, calls, mode="fixed4")
+
+
+def test_gqa8_per_head_outliers():
+    calls = [[2000, 333, 1], [1, 1, 1], [1, 1, 1], [257, 1, 300]]
+    run_append_scenario(128, 64, 8, 64, 64, 256, torch.bfloat16, calls, mode="per_head")
+
+
+@pytest.mark.parametrize("d,G", [(256, 256), (256, 32), (128, 128), (64, 64), (128, 32)])
+def test_group_sizes(d, G):
+    run_append_scenario(d, 2, 1, G, 16, 32, torch.bfloat16, [[300], [1], [77]])
+
+
+def test_decode_step_appends_spill_every_step():
+    calls = [[330, 330, 400, 64]] + [[1, 1, 1, 1]] * 12
+    run_append_scenario(128, 32, 8, 64, 64, 256, torch.bfloat16, calls)
+
+
+def test_sink_only_and_no_history():
+    # lengths that never reach the history: everything stays in the windows
+    st = run_append_scenario(128, 8, 2, 64, 64, 256, torch.bfloat16, [[10, 64, 320], [5, 0, 0]])
+    assert st["exact"] == 0 and st["bad"] == 0
+
+
+def test_clip_ratio_one_and_empty_calls():
+    from rotated_int2_kv_gb300 import ops
+    run_append_scenario(128, 4, 2, 64, 8, 16, torch.bfloat16, [[0, 0], [100, 50], [0, 0], [3, 0]], clip=1.0)
+    # an empty batch and an all-empty call are no-ops
+    cfg = ops.Config(128, 4, 2, 64, 8, 16)
+    Rk, Rv = _rotations(128)
+    dc = ops.LayerCache(cfg, 64, 2, Rk, Rv)
+    z = torch.zeros((0, 2, 128), dtype=torch.bfloat16, device="cuda")
+    ops.quantize_append(dc, z, z, torch.zeros(1, dtype=torch.int32, device="cuda"),
+                        torch.zeros(0, dtype=torch.int32, device="cuda"),
+                        torch.zeros((0, 16), dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert not dc.records.any()
+
+
+def test_device_checks_flag_bad_slots_without_faulting():
+    from rotated_int2_kv_gb300 import ops
+    cfg = ops.Config(64, 2, 1, 32, 4, 8)
+    Rk, Rv = _rotations(64)
+    dc = ops.LayerCache(cfg, 32, 1, Rk, Rv)
+    ops.device_status(clear=True)
+    k = torch.randn((40, 1, 64), device="cuda").to(torch.bfloat16)
+    pt = torch.arange(40, dtype=torch.int32, device="cuda").reshape(1, 40)
+    pt[0, 20] = 10 ** 6            # slot outside the pool: skipped and flagged
+    ops.quantize_append(dc, k, k, torch.tensor([0, 40], dtype=torch.int32, device="cuda"),
+                        torch.zeros(1, dtype=torch.int32, device="cuda"), pt)
+    torch.cuda.synchronize()
+    assert ops.device_status(clear=True) & ops.DEV_BAD_SLOT
+    assert ops.device_status(clear=True) == 0

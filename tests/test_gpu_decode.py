@@ -1,0 +1,178 @@
+"""GPU parity of oscar_decode_attention against the fp64 oracle.
+
+The cache is built by the oracle and copied to the device, so both sides
+evaluate attention on the same dequantised values; the bar is max-abs 2e-3
+and relative-L2 1e-3 on the fp32 outputs.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from rotated_int2_kv_gb300 import synth
+from parity_util import ATOL, RTOL_L2, attn_errors, device_cache_from_oracle
+
+pytestmark = pytest.mark.gpu
+
+SEED = 1234
+
+
+def _rotations(d, seed=SEED):
+    Rk, _ = oracle.build_rotation(oracle.covariance(synth.calib_samples(seed, 0, d)), d)
+    Rv, _ = oracle.build_rotation(oracle.covariance(synth.calib_samples(seed, 1, d)), d)
+    return Rk.astype(np.float32), Rv.astype(np.float32)
+
+
+def build_oracle_cache(d, Hq, Hkv, G, S, W, lens, kv_dtype=torch.bfloat16, mode="fixed4", clip=0.9,
+                       seed=SEED, shuffled=True, pt_width=None):
+    B = len(lens)
+    maxL = max(pt_width or 0, max(lens))
+    pool = B * maxL + 11
+    Rk, Rv = _rotations(d, seed)
+    pt = synth.page_table(seed, B, maxL, pool, shuffled=shuffled)
+    req = np.array(list(reversed(range(B))), np.int32)
+    oc = oracle.OracleCache(oracle.OracleConfig(d, Hq, Hkv, G, S, W, clip), pool, B + 1, Rk, Rv)
+    scales = synth.outlier_scales(seed, Hkv, d, mode)
+    ks, vs = [], []
+    for b in range(B):
+        k, v = synth.kv_tokens(seed, b, 0, lens[b], Hkv, d, scales, dtype=kv_dtype)
+        ks.append(k.float().numpy())
+        vs.append(v.float().numpy())
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    oc.append(np.concatenate(ks), np.concatenate(vs), cu, [0] * B, req, pt.numpy())
+    return oc, pt, req
+
+
+def run_decode_case(d, Hq, Hkv, G, S, W, lens, q_dtype=torch.bfloat16, impl="auto", mode="fixed4",
+                    max_seq_len=None, step=0):
+    from rotated_int2_kv_gb300 import ops
+    oc, pt, req = build_oracle_cache(d, Hq, Hkv, G, S, W, lens, mode=mode, pt_width=max_seq_len)
+    cfg = ops.Config(d, Hq, Hkv, G, S, W, 0.9, q_dtype=q_dtype)
+    dc = device_cache_from_oracle(ops, oc, cfg)
+    B = len(lens)
+    q = synth.queries(SEED, step, B, Hq, d, dtype=q_dtype)
+    msl = max_seq_len or max(lens)
+    ws = ops.alloc_workspace(cfg, B, msl)
+    dev = torch.device("cuda")
+    out = ops.decode_attention(dc, q.to(dev), pt.to(dev), torch.tensor(lens, dtype=torch.int32, device=dev),
+                               msl, ws, req_idx=torch.from_numpy(req).to(dev), impl=impl)
+    torch.cuda.synchronize()
+    assert ops.device_status() == 0
+    want = oracle.decode_attention(oc, q.float().numpy(), pt.numpy(), lens, req)
+    err, rel = attn_errors(out.cpu().numpy(), want)
+    assert err <= ATOL and rel <= RTOL_L2, (err, rel)
+    return err, rel
+
+
+@pytest.mark.parametrize("impl", ["auto", "simt"])
+def test_tiny_config(impl):
+    # 4 q / 1 KV head, d 128, L 1024 = 64 + 704 + 256, fp32 q, group 64
+    run_decode_case(128, 4, 1, 64, 64, 256, [1024], q_dtype=torch.float32, impl=impl)
+
+
+@pytest.mark.parametrize("impl", ["auto", "simt"])
+def test_edge_lengths_qwen8b_heads(impl):
+    # L = 1 (sink only), 50 (< S), 320 (= S + W, no history), 321 (one history token), 3000
+    run_decode_case(128, 32, 8, 64, 64, 256, [1, 50, 320, 321, 3000], impl=impl)
+
+
+@pytest.mark.parametrize("impl", ["auto", "simt"])
+def test_gqa6_wide_heads(impl):
+    run_decode_case(256, 24, 4, 128, 64, 256, [2500, 777], impl=impl)
+
+
+@pytest.mark.parametrize("impl", ["auto", "simt"])
+def test_gqa8_ragged(impl):
+    run_decode_case(128, 64, 8, 64, 64, 256, [4100, 1300, 2222], impl=impl, mode="per_head")
+
+
+def test_small_windows_d64():
+    run_decode_case(64, 12, 2, 32, 4, 8, [60, 13, 200])
+
+
+@pytest.mark.parametrize("G", [32, 128])
+def test_group_sizes(G):
+    run_decode_case(128, 8, 2, G, 64, 256, [1500, 900])
+
+
+def test_many_chunks_and_ctas():
+    # long enough that the history spans many chunks and persistent CTAs
+    run_decode_case(128, 32, 8, 64, 64, 256, [20000, 7000, 15001], max_seq_len=20000)
+
+
+def test_max_seq_len_larger_than_lengths():
+    run_decode_case(128, 32, 8, 64, 64, 256, [900, 2000], max_seq_len=8192)
+
+
+def test_workspace_and_length_errors():
+    from rotated_int2_kv_gb300 import ops
+    cfg = ops.Config(128, 4, 1, 64)
+    Rk, Rv = _rotations(128)
+    dc = ops.LayerCache(cfg, 64, 1, Rk, Rv)
+    q = torch.zeros((1, 4, 128), dtype=torch.bfloat16, device="cuda")
+    pt = torch.zeros((1, 64), dtype=torch.int32, device="cuda")
+    lens = torch.tensor([64], dtype=torch.int32, device="cuda")
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ops.OscarError) as ei:
+        ops.decode_attention(dc, q, pt, lens, 64, small)
+    assert ei.value.code == -3
+    # a length beyond max_seq_len is flagged on the device and yields zeros
+    ws = ops.alloc_workspace(cfg, 1, 64)
+    ops.device_status(clear=True)
+    out = ops.decode_attention(dc, q, pt, torch.tensor([65], dtype=torch.int32, device="cuda"), 64, ws)
+    torch.cuda.synchronize()
+    assert ops.device_status(clear=True) & ops.DEV_BAD_LEN
+    assert not out.any()
+
+
+def test_end_to_end_gpu_append_then_decode():
+    """Chunked GPU appends followed by decode steps, checked at every step:
+    the GPU-built records against the oracle's (bit-exact except counted
+    rounding ties), decode parity on identical cache contents, and the
+    decode over the GPU-built cache against the oracle in relative L2 (a
+    tie-flipped code may move single outputs by more than the max-abs bound)."""
+    from rotated_int2_kv_gb300 import ops
+    from parity_util import classify_records
+    d, Hq, Hkv, G, S, W = 128, 32, 8, 64, 64, 256
+    lens0 = [3000, 1200]
+    B = 2
+    maxL = 3100
+    pool = B * maxL
+    Rk, Rv = _rotations(d)
+    pt = synth.page_table(SEED, B, maxL, pool)
+    cfg = ops.Config(d, Hq, Hkv, G, S, W)
+    dev = torch.device("cuda")
+    dc = ops.LayerCache(cfg, pool, B, Rk, Rv)
+    oc = oracle.OracleCache(oracle.OracleConfig(d, Hq, Hkv, G, S, W), pool, B, Rk, Rv)
+    scales = synth.outlier_scales(SEED, Hkv, d)
+    pos = [0, 0]
+    req = np.arange(B, dtype=np.int32)
+    ws = ops.alloc_workspace(cfg, B, maxL)
+    ties = 0
+    for step, call in enumerate([lens0, [1, 1], [1, 1], [1, 1]]):
+        kk, vv = zip(*[synth.kv_tokens(SEED, b, pos[b], call[b], Hkv, d, scales) for b in range(B)])
+        k = torch.cat(kk)
+        v = torch.cat(vv)
+        cu = np.concatenate([[0], np.cumsum(call)]).astype(np.int32)
+        ops.quantize_append(dc, k.to(dev), v.to(dev), torch.from_numpy(cu).to(dev),
+                            torch.tensor(pos, dtype=torch.int32, device=dev), pt.to(dev))
+        oc.append(k.float().numpy(), v.float().numpy(), cu, pos, req, pt.numpy(), keep_y=True)
+        pos = [pos[b] + call[b] for b in range(B)]
+        hist = np.concatenate([pt[b, S:max(S, pos[b] - W)].numpy() for b in range(B)])
+        st = classify_records(dc.records.cpu().numpy(), oc, hist)
+        assert st["bad"] == 0, st
+        ties += st["code_ties"] + st["sz_ties"]
+        q = synth.queries(SEED, step, B, Hq, d).to(dev)
+        lens_t = torch.tensor(pos, dtype=torch.int32, device=dev)
+        want = oracle.decode_attention(oc, q.float().cpu().numpy(), pt.numpy(), pos, req)
+        same = device_cache_from_oracle(ops, oc, cfg)
+        out = ops.decode_attention(same, q, pt.to(dev), lens_t, maxL, ws)
+        err, rel = attn_errors(out.cpu().numpy(), want)
+        assert err <= ATOL and rel <= RTOL_L2, ("identical cache", step, err, rel)
+        out = ops.decode_attention(dc, q, pt.to(dev), lens_t, maxL, ws)
+        err, rel = attn_errors(out.cpu().numpy(), want)
+        assert rel <= RTOL_L2, ("gpu-built cache", step, err, rel, ties)
+        if ties == 0:
+            assert err <= ATOL, ("gpu-built cache", step, err)
+    assert ops.device_status() == 0
