@@ -156,6 +156,11 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
     }
 }
 
+// True when CTA i of an n-CTA history grid owns at least one of N chunks.
+__device__ __forceinline__ bool cta_has_work(int64_t i, int64_t N, int64_t n) {
+    return i * N / n < (i + 1) * N / n;
+}
+
 // Maps flattened chunk index f to (request, chunk-in-request) by binary search
 // over the exclusive prefix cprefix[0..batch].
 __device__ __forceinline__ int chunk_request(const int32_t* cprefix, int batch, int64_t f) {
@@ -321,8 +326,8 @@ __global__ void __launch_bounds__(512) history_simt_kernel(DecodeParams P) {
                 }
                 __syncwarp();
             }
-            // ---- write the segment partial at its first chunk slot ----
-            const int64_t slot0 = (int64_t)b * P.max_chunks + c_first;
+            // ---- write the segment partial at slot (CTA + request) ----
+            const int64_t slot0 = (int64_t)blockIdx.x + b;
 #pragma unroll
             for (int j = 0; j < GQ; ++j) {
                 if (j >= P.g) break;
@@ -331,11 +336,6 @@ __global__ void __launch_bounds__(512) history_simt_kernel(DecodeParams P) {
                 float* o = P.po + (slot0 * P.Hq + hq) * D + lane * CPL;
 #pragma unroll
                 for (int c = 0; c < CPL; ++c) o[c] = acc[j][c] + zacc[j];
-            }
-            // other chunks of the segment: marker (empty partial)
-            for (int64_t ff = f + 1 + lane; ff < fe; ff += 32) {
-                const int64_t sl = (int64_t)b * P.max_chunks + (int)(ff - P.cprefix[b]);
-                for (int j = 0; j < P.g; ++j) P.ml[sl * P.Hq + hk * P.g + j] = make_float2(-INFINITY, 0.f);
             }
         }
         f = fe;
@@ -388,6 +388,11 @@ __global__ void __launch_bounds__(256) combine_kernel(DecodeParams P) {
     }
     __syncthreads();
     const int warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+    // history partials of request b: CTAs owning chunks [cprefix[b], cprefix[b+1])
+    const int64_t N = P.cprefix[P.batch];
+    const int64_t c0 = P.cprefix[b], c1 = P.cprefix[b + 1];
+    const int64_t i_lo = c1 > c0 ? chunk_owner(c0, N, P.n_ctas) : 0;
+    const int64_t i_hi = c1 > c0 ? chunk_owner(c1 - 1, N, P.n_ctas) : -1;
     // per head: window max/sum (warp j), and the LSE merge of the history partials
     for (int j = warp; j < g; j += nw) {
         float mx = -INFINITY;
@@ -400,15 +405,17 @@ __global__ void __launch_bounds__(256) combine_kernel(DecodeParams P) {
             sum += p;
         }
         for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        const int nch = (d_hist_hi(L, S, W) - S + P.chunk - 1) / P.chunk;
         const int hq = hk * g + j;
         float M = -INFINITY;
-        for (int c = lane; c < max(nch, 0); c += 32)
-            M = fmaxf(M, P.ml[((int64_t)b * P.max_chunks + c) * P.Hq + hq].x);
+        for (int i = i_lo + lane; i <= i_hi; i += 32) {
+            if (!cta_has_work(i, N, P.n_ctas)) continue;
+            M = fmaxf(M, P.ml[((int64_t)i + b) * P.Hq + hq].x);
+        }
         for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
         float lr = 0.f;
-        for (int c = lane; c < max(nch, 0); c += 32) {
-            const float2 ml = P.ml[((int64_t)b * P.max_chunks + c) * P.Hq + hq];
+        for (int i = i_lo + lane; i <= i_hi; i += 32) {
+            if (!cta_has_work(i, N, P.n_ctas)) continue;
+            const float2 ml = P.ml[((int64_t)i + b) * P.Hq + hq];
             if (ml.x != -INFINITY) lr += exp2f(ml.x - M) * ml.y;
         }
         for (int off = 16; off; off >>= 1) lr += __shfl_xor_sync(0xffffffffu, lr, off);
@@ -421,14 +428,14 @@ __global__ void __launch_bounds__(256) combine_kernel(DecodeParams P) {
     }
     __syncthreads();
     // merged rotated sum: thread per (head, channel)
-    const int nch = max(0, (d_hist_hi(L, S, W) - S + P.chunk - 1) / P.chunk);
     for (int i = tid; i < g * D; i += blockDim.x) {
         const int j = i / D, c = i % D;
         const int hq = hk * g + j;
         const float M = sred[j * 4 + 2];
         float acc = 0.f;
-        for (int ch = 0; ch < nch; ++ch) {
-            const int64_t sl = (int64_t)b * P.max_chunks + ch;
+        for (int64_t ci = i_lo; ci <= i_hi; ++ci) {
+            if (!cta_has_work(ci, N, P.n_ctas)) continue;
+            const int64_t sl = ci + b;
             const float2 ml = P.ml[sl * P.Hq + hq];
             if (ml.x == -INFINITY) continue;
             acc = fmaf(exp2f(ml.x - M), P.po[(sl * P.Hq + hq) * D + c], acc);
@@ -519,7 +526,8 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
                 return check_cuda("cudaFuncSetAttribute(history_simt_kernel)");
             int per_sm = 0;
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
-            const int grid = std::max(1, sm_count() * std::max(1, per_sm));
+            const int grid = std::min(P.n_ctas, std::max(1, sm_count() * std::max(1, per_sm)));
+            P.n_ctas = grid;
             kern<<<grid, threads, smem, st>>>(P);
             return check_cuda("history_simt_kernel launch");
         };
@@ -579,7 +587,7 @@ static int decode_impl(const oscar_config* cfg, const oscar_layer_cache* cache, 
     P.ng = cfg->head_dim / cfg->group_size;
     P.rec_bytes = record_layout(cfg->head_dim, cfg->group_size).bytes;
     P.chunk = plan.chunk;
-    P.max_chunks = plan.max_chunks;
+    P.n_ctas = plan.max_ctas;          // set by the history launcher
     P.n_frag_tiles = plan.n_frag_tiles;
     P.qscale = (float)(1.4426950408889634 / std::sqrt((double)cfg->head_dim));
     char* ws = reinterpret_cast<char*>(workspace);

@@ -4,17 +4,23 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <algorithm>
+
 #include "oscar_internal.h"
 
 namespace oscar {
 
-// The history of each request is cut into chunks of `chunk` tokens; a
-// persistent history grid takes contiguous runs of the flattened chunk list,
-// and each run inside one request produces one (m, l, o) partial, stored at
-// the slot of its first chunk (the other chunks of the run get a marker).
+// The history of each request is cut into chunks of `chunk` tokens.  A
+// persistent history grid of at most `max_ctas` CTAs splits the flattened
+// chunk list into contiguous runs (CTA i owns [i·N/n, (i+1)·N/n)), and each
+// CTA writes one (m, l, o) partial per request it touches, at partial slot
+// i + b.  The slot is unique: if CTAs i < i' both touch requests b and b' with
+// i + b = i' + b', then b' < b, but runs are ordered so b' >= b.  So
+// max_ctas + batch slots suffice, whatever the lengths.
 struct DecodePlan {
     int chunk;        // tokens per chunk (multiple of 32)
-    int max_chunks;   // chunk slots per request
+    int max_ctas;     // upper bound of the history grid
+    int part_slots;   // max_ctas + batch
     int n_frag_tiles; // n-tiles of 8 columns for the fragment-packed queries
     // workspace offsets (bytes, 256-aligned)
     size_t off_len, off_req, off_cprefix, off_qt, off_qsum, off_qfrag, off_ml, off_o, total;
@@ -27,14 +33,15 @@ inline DecodePlan make_plan(const oscar_config* cfg, int batch, int max_seq_len,
     const int d = cfg->head_dim, Hq = cfg->num_q_heads, Hkv = cfg->num_kv_heads;
     const int g = Hq / Hkv, ng = d / cfg->group_size;
     const int64_t max_hist = std::max<int64_t>(0, (int64_t)max_seq_len - cfg->sink - cfg->recent);
-    // aim for ~16 chunks per CTA-slot of a 2-per-SM grid, 32..1024 tokens each
-    const int64_t target = (int64_t)std::max(1, n_sm) * 32;
+    // ~64 chunks per SM of work for balance, 32..1024 tokens each
+    const int64_t target = (int64_t)std::max(1, n_sm) * 64;
     int64_t c = ((int64_t)batch * max_hist + target - 1) / target;
     c = (c + 31) / 32 * 32;
     if (c < 32) c = 32;
     if (c > 1024) c = 1024;
     p.chunk = (int)c;
-    p.max_chunks = (int)std::max<int64_t>(1, (max_hist + c - 1) / c);
+    p.max_ctas = std::max(1, n_sm) * 4;
+    p.part_slots = p.max_ctas + batch;
     p.n_frag_tiles = (2 * g + 7) / 8;
     size_t off = 0;
     p.off_len = off;      off = align256(off + (size_t)batch * 4);
@@ -43,8 +50,8 @@ inline DecodePlan make_plan(const oscar_config* cfg, int batch, int max_seq_len,
     p.off_qt = off;       off = align256(off + (size_t)batch * Hq * d * 4);
     p.off_qsum = off;     off = align256(off + (size_t)batch * Hq * ng * 4);
     p.off_qfrag = off;    off = align256(off + (size_t)batch * Hkv * p.n_frag_tiles * (d / 16) * 32 * 8);
-    p.off_ml = off;       off = align256(off + (size_t)batch * p.max_chunks * Hq * 8);
-    p.off_o = off;        off = align256(off + (size_t)batch * p.max_chunks * Hq * d * 4);
+    p.off_ml = off;       off = align256(off + (size_t)p.part_slots * Hq * 8);
+    p.off_o = off;        off = align256(off + (size_t)p.part_slots * Hq * d * 4);
     p.total = off;
     return p;
 }
@@ -67,7 +74,8 @@ struct DecodeParams {
     int64_t num_slots;
     int max_reqs;
     int Hq, Hkv, g, S, W, G, ng, rec_bytes;
-    int chunk, max_chunks, n_frag_tiles;
+    int chunk, n_frag_tiles;
+    int n_ctas;        // history grid actually launched (<= plan.max_ctas)
     float qscale;      // log2(e) / sqrt(d)
     // workspace
     int32_t* len;      // effective L per request (0 when invalid)
@@ -76,9 +84,18 @@ struct DecodeParams {
     float* qt;         // q·R_K·qscale, [batch][Hq][d]
     float* qsum;       // per-group sums of the fragment-packed q̃, [batch][Hq][ng]
     uint2* qfrag;      // fp16 hi/lo B fragments, [batch][Hkv][n_tiles][d/16][32]
-    float2* ml;        // (m, l) per chunk slot, [batch][max_chunks][Hq]
-    float* po;         // unnormalised o per chunk slot, [batch][max_chunks][Hq][d]
+    float2* ml;        // (m, l) per partial slot, [part_slots][Hq]
+    float* po;         // unnormalised o per partial slot, [part_slots][Hq][d]
     int* status;
 };
+
+}  // namespace oscar
+
+namespace oscar {
+
+// CTA of the history grid that owns flattened chunk f (N chunks over n CTAs).
+__host__ __device__ __forceinline__ int64_t chunk_owner(int64_t f, int64_t N, int64_t n) {
+    return ((f + 1) * n - 1) / N;
+}
 
 }  // namespace oscar
