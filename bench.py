@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-append", action="store_true")
+    ap.add_argument("--workload", choices=["qwen8b-100k", "small"], default="qwen8b-100k",
+                    help="small: batch 4 at 65,536 tokens (168 MB of INT2 records, > L2), for ncu captures")
     return ap.parse_args()
 
 
@@ -289,11 +291,11 @@ def run_reference(args, rank, ws):
 
 
 def workload_config():
-    return {"workload": "Qwen3-8B-shaped decode step (append 1 token + attention), batch 32, "
-                        "context 100,000 (64 sink + 99,680 INT2 + 256 recent), 32 q / 8 KV heads, d 128, "
-                        "group 64, clip 0.9, shuffled page table, page_size 1",
+    return {"workload": "Qwen3-8B-shaped decode step (append 1 token + attention), batch %d, "
+                        "context %d (64 sink + %d INT2 + 256 recent), 32 q / 8 KV heads, d 128, "
+                        "group 64, clip 0.9, shuffled page table, page_size 1" % (B, L_BASE, L_BASE - 320),
             "batch": B, "context": L_BASE, "q_heads": HQ, "kv_heads": HKV, "head_dim": D, "group_size": G,
-            "l2": "inputs larger than L2 (2.05 GB INT2 history per step)",
+            "l2": "inputs larger than L2 (%.2f GB INT2 history per step)" % (B * (L_BASE - 320) * 640 / 1e9),
             "parallelism": "replicas (independent requests per GPU)"}
 
 
@@ -304,6 +306,9 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank, ws)
         return
+    global B, L_BASE
+    if args.workload == "small":
+        B, L_BASE = 4, 65536
     import torch
     from rotated_int2_kv_gb300 import ops
     if not os.path.exists(ops._LIB_PATH):
