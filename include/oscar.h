@@ -231,6 +231,29 @@ int oscar_decode_attention_simt(const oscar_config* cfg, const oscar_layer_cache
                                 int32_t batch, int32_t max_seq_len, float* out,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* Allocation-free variant of oscar_decode_attention (no counterpart on the
+ * pages: an interface addition of this library).  Same arguments and result
+ * minus the workspace: the scratch lives in a 16 MiB array compiled into the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  It serves callers that cannot allocate device memory -- host
+ * runtimes that reserve almost all of the GPU for their own pool and give
+ * plug-in kernels no allocation rights, or code paths where a cudaMalloc
+ * (which may synchronise the device) is not allowed.  This call allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *  - Sizes whose scratch need (oscar_decode_workspace_bytes) exceeds 16 MiB
+ *    are rejected with OSCAR_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array and it keeps the previous
+ *    call's contents; every byte a call reads is written earlier in the same
+ *    call, so nothing needs clearing.  Calls that overlap on the GPU (e.g.
+ *    on two streams) race on the array: order them on one stream. */
+int oscar_decode_attention_noalloc(const oscar_config* cfg, const oscar_layer_cache* cache,
+                                   const void* q, const int32_t* page_table, int64_t pt_stride,
+                                   const int32_t* seq_lens, const int32_t* req_idx,
+                                   int32_t batch, int32_t max_seq_len, float* out, void* stream);
+
 /* ---- kernel timing (benchmarks) ----------------------------------------- */
 
 /* Enables (1) or disables (0) event timing of the dominant kernels and

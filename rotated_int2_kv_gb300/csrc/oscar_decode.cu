@@ -624,3 +624,62 @@ extern "C" int oscar_decode_attention_simt(const oscar_config* cfg, const oscar_
     return decode_impl(cfg, cache, q, page_table, pt_stride, seq_lens, req_idx, batch, max_seq_len, out,
                        workspace, workspace_bytes, stream, 1);
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode.  Some callers cannot allocate device memory for a
+// workspace: host runtimes that reserve nearly all of the GPU for their own
+// pool at start-up and hand plug-in kernels no allocation rights, and code
+// paths where a cudaMalloc, which may synchronise the device, is not allowed.
+// For them the decode below uses a fixed scratch area compiled into the
+// library instead of a caller-provided workspace.  Every GPU that loads the
+// library holds this array until the process exits.
+// ---------------------------------------------------------------------------
+namespace oscar {
+
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;   // 16 MiB per device
+__device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+static void* g_scratch_ptr[64];
+
+// Device address of the scratch array for the current device.  Host code may
+// not use g_decode_scratch's name as an address (it is a host-side stand-in),
+// so the address is queried once per device with that device current.
+static int static_scratch(void** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64)
+        return fail(OSCAR_ERR_CUDA, "no current CUDA device: %s", cudaGetErrorString(e));
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(OSCAR_ERR_CUDA, "cudaGetSymbolAddress(decode scratch): %s", cudaGetErrorString(e));
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return OSCAR_OK;
+}
+
+}  // namespace oscar
+
+extern "C" int oscar_decode_attention_noalloc(const oscar_config* cfg, const oscar_layer_cache* cache,
+                                              const void* q, const int32_t* page_table, int64_t pt_stride,
+                                              const int32_t* seq_lens, const int32_t* req_idx, int32_t batch,
+                                              int32_t max_seq_len, float* out, void* stream) {
+    clear_error();
+    int rc = decode_validate(cfg, cache, batch, max_seq_len, pt_stride);
+    if (rc) return rc;
+    const int nsm = sm_count();
+    if (nsm <= 0) return OSCAR_ERR_CUDA;
+    const size_t need = make_plan(cfg, batch, max_seq_len, nsm).total;
+    if (need > kStaticScratchBytes)
+        return fail(OSCAR_ERR_WORKSPACE,
+                    "batch %d with max_seq_len %d needs %zu bytes of scratch; the built-in scratch holds %zu "
+                    "(use oscar_decode_attention with a caller workspace)",
+                    batch, max_seq_len, need, kStaticScratchBytes);
+    void* ws = nullptr;
+    rc = static_scratch(&ws);
+    if (rc) return rc;
+    return decode_impl(cfg, cache, q, page_table, pt_stride, seq_lens, req_idx, batch, max_seq_len, out, ws,
+                       kStaticScratchBytes, stream, 0);
+}

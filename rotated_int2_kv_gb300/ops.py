@@ -71,6 +71,10 @@ _SIGS = {
                                      ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                      ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
+    "oscar_decode_attention_noalloc": ([ctypes.POINTER(CConfig), ctypes.POINTER(CLayerCache), ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p],
+                                       ctypes.c_int),
     "oscar_device_status": ([ctypes.POINTER(ctypes.c_int32), ctypes.c_int32], ctypes.c_int),
     "oscar_profile_enable": ([ctypes.c_int32], ctypes.c_int),
     "oscar_profile_read": ([ctypes.c_int32, ctypes.POINTER(ctypes.c_double),
@@ -278,3 +282,17 @@ def profile_read(kind):
     ms, n = ctypes.c_double(), ctypes.c_int64()
     _check(lib().oscar_profile_read(kind, ctypes.byref(ms), ctypes.byref(n)))
     return ms.value, n.value
+
+
+def decode_attention_noalloc(cache, q, page_table, seq_lens, max_seq_len, req_idx=None, out=None, stream=None):
+    """Decode step with the library's built-in scratch (no workspace, nothing allocated by the library)."""
+    cfg = cache.cfg
+    B = q.shape[0]
+    if out is None:
+        out = torch.empty((B, cfg.num_q_heads, cfg.head_dim), dtype=torch.float32, device=q.device)
+    _check(lib().oscar_decode_attention_noalloc(
+        ctypes.byref(cfg.c()), ctypes.byref(cache.c()), _ptr(q, cfg.q_dtype, "q"),
+        _ptr(page_table, torch.int32, "page_table"), page_table.shape[1],
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(req_idx, torch.int32, "req_idx"), B, max_seq_len,
+        _ptr(out, torch.float32, "out"), _stream(stream)))
+    return out
