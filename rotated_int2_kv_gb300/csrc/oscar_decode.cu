@@ -41,7 +41,7 @@ __device__ __forceinline__ bool request_valid(const DecodeParams& P, int b, int*
 
 // ---------------------------------------------------------------------------
 // prep: per request, q̃ = q·R_K·(log2 e/√d) for every query head (fp32), its
-// fp16 hi/lo split packed as mma B fragments, the per-group sums of hi+lo,
+// fp16 hi/lo split (of q̃/α) packed as mma B fragments, the per-group sums,
 // the effective length / window row, and (block 0) the chunk prefix.
 // ---------------------------------------------------------------------------
 template <int D>
@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
     __shared__ int scan[256];
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
-    if (b == 0) {
+    if (b == 0 && blockIdx.y == 0) {
         // chunk prefix over all requests (re-derives validity locally)
         const int per = (P.batch + 255) / 256;
         const int b0 = min(P.batch, tid * per), b1 = min(P.batch, b0 + per);
@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
     }
     int L, rq;
     const bool ok = request_valid(P, b, &L, &rq);
-    if (tid == 0) {
+    if (tid == 0 && blockIdx.y == 0) {
         P.len[b] = ok ? L : 0;
         P.req[b] = ok ? rq : 0;
         if (!ok) {
@@ -89,7 +89,8 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
             set_status(P.status, bits);
         }
     }
-    for (int h0 = 0; h0 < P.Hq; h0 += 16) {
+    {
+        const int h0 = blockIdx.y * 16;
         const int nh = min(16, P.Hq - h0);
         __syncthreads();
         for (int i = tid; i < nh * D; i += 256)
@@ -111,17 +112,27 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
             }
         }
         __syncthreads();
-        // per-group sums of the fp16 hi + lo parts
-        for (int i = tid; i < nh * P.ng; i += 256) {
+        // Per group, from the fp16 hi + lo parts actually fed to the MMA: Q = Σ q̃
+        // and Q' = Σ q̃/α, where α = 1/16 for even and 1/4 for odd channels (the
+        // weights with which the MMA path encodes a code c as 1 + α·c).
+        const int lane = tid & 31, warp = tid >> 5;
+        for (int i = warp; i < nh * P.ng; i += 8) {
             const int j = i / P.ng, gi = i % P.ng;
-            float s = 0.f;
-            for (int c = gi * P.G; c < (gi + 1) * P.G; ++c) {
-                const float x = sqt[j][c];
+            float sq_ = 0.f, sqa = 0.f;
+            for (int c = gi * P.G + lane; c < (gi + 1) * P.G; c += 32) {
+                const float inv = (c & 1) ? 4.f : 16.f;
+                const float x = sqt[j][c] * inv;
                 const __half hi = __float2half_rn(x);
                 const __half lo = __float2half_rn(x - __half2float(hi));
-                s += __half2float(hi) + __half2float(lo);
+                const float v = __half2float(hi) + __half2float(lo);
+                sqa += v;
+                sq_ += v / inv;
             }
-            P.qsum[((int64_t)b * P.Hq + h0 + j) * P.ng + gi] = s;
+            for (int off = 16; off; off >>= 1) {
+                sq_ += __shfl_xor_sync(0xffffffffu, sq_, off);
+                sqa += __shfl_xor_sync(0xffffffffu, sqa, off);
+            }
+            if (lane == 0) P.qsum[((int64_t)b * P.Hq + h0 + j) * P.ng + gi] = make_float2(sq_, sqa);
         }
         // B fragments: [Hkv][n_tiles][D/16][32 lanes] of (b0b1, b2b3);
         // column n of tile nt is (head 4nt + n/2 of the KV group, part n%2).
@@ -135,17 +146,19 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
             const int head = hk * P.g + 4 * nt + (n >> 1);
             const int part = n & 1;
             if (4 * nt + (n >> 1) >= P.g) {         // padding column: zero, written once
-                if (h0 == 0)
+                if (blockIdx.y == 0)
                     P.qfrag[(((int64_t)b * P.Hkv + hk) * P.n_frag_tiles + nt) * (D / 16) * 32 + kk * 32 + lane] =
                         make_uint2(0u, 0u);
                 continue;
             }
             if (head < h0 || head >= h0 + nh) continue;
+            // k-cols (2j, 2j+1) <- channels (16kk+2j, 16kk+2j+8), even: scaled by 16;
+            // k-cols (2j+8, 2j+9) <- channels (16kk+2j+1, 16kk+2j+9), odd: scaled by 4
             const int chans[4] = {16 * kk + 2 * j, 16 * kk + 2 * j + 8, 16 * kk + 2 * j + 1, 16 * kk + 2 * j + 9};
             uint16_t hv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float x = sqt[head - h0][chans[e]];
+                const float x = sqt[head - h0][chans[e]] * (e < 2 ? 16.f : 4.f);
                 const __half hi = __float2half_rn(x);
                 const __half v = part ? __float2half_rn(x - __half2float(hi)) : hi;
                 hv[e] = *reinterpret_cast<const uint16_t*>(&v);
@@ -268,7 +281,7 @@ __global__ void __launch_bounds__(512) history_simt_kernel(DecodeParams P) {
 #pragma unroll
                         for (int j = 0; j < GQ; ++j) {
                             if (j < P.g) {
-                                const float Q = P.qsum[((int64_t)b * P.Hq + hk * P.g + j) * ng + gi];
+                                const float Q = P.qsum[((int64_t)b * P.Hq + hk * P.g + j) * ng + gi].x;
                                 // Σ q̃(1 + c/4) = Q + Σq̃c/4  =>  s·Σq̃c + z·Q = 4s·(dot - Q) + z·Q
                                 logit[j] += 4.f * s * (dot[j] - Q) + z * Q;
                             }
@@ -343,127 +356,204 @@ __global__ void __launch_bounds__(512) history_simt_kernel(DecodeParams P) {
 }
 
 // ---------------------------------------------------------------------------
-// combine: one block per (KV head, request).  BF16 windows attended directly
-// (fp32), history partials merged by log-sum-exp, R_Vᵀ applied to the merged
-// rotated-domain sum, the two domains merged and normalised.
+// window: one block of 128 threads per (KV head, request, 64-token tile of the
+// BF16 sink + recent tokens).  K and V rows are staged in shared memory (rows
+// padded to an odd number of words), logits in fp32 against the unrotated q,
+// and the tile's (m, l, o) partial is written for the combine.
 // ---------------------------------------------------------------------------
+constexpr int kCombThreads = 128;
+constexpr int kWinTile = 64;
+
 template <int D>
-__global__ void __launch_bounds__(256) combine_kernel(DecodeParams P) {
-    extern __shared__ __align__(16) float s_c[];
-    const int hk = blockIdx.x, b = blockIdx.y;
+__global__ void __launch_bounds__(kCombThreads) window_kernel(DecodeParams P) {
+    constexpr int kRowW = D / 2 + 1;               // words per staged bf16 row (odd: conflict-free)
+    extern __shared__ __align__(16) float s_w[];
+    const int hk = blockIdx.x, b = blockIdx.y, wt = blockIdx.z;
     const int g = P.g, S = P.S, W = P.W;
-    const int nwin = S + W;
-    float* sq = s_c;                   // [g][D] unrotated q · qscale
-    float* slog = sq + g * D;          // [g][nwin] window logits -> probabilities
-    float* sorot = slog + g * nwin;    // [g][D] merged rotated-domain sum
-    float* sred = sorot + g * D;       // [g][4]: m_plain, l_plain, m_rot, l_rot
-    const int tid = threadIdx.x;
+    float* sq = s_w;                               // [g][D] q · qscale
+    float* sp = sq + g * D;                        // [g][kWinTile] logits -> probabilities
+    float* sml = sp + g * kWinTile;                // [g][2] (m, l)
+    uint32_t* sk = reinterpret_cast<uint32_t*>(sml + 2 * g);   // [kWinTile][kRowW] K tile
+    uint32_t* sv = sk + kWinTile * kRowW;                      // [kWinTile][kRowW] V tile
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = P.len[b];
     const int rq = P.req[b];
-    float* outp = P.out + ((int64_t)b * P.Hq + hk * g) * D;
-    if (L <= 0) {
-        for (int i = tid; i < g * D; i += blockDim.x) outp[i] = 0.f;
-        return;
-    }
-    for (int i = tid; i < g * D; i += blockDim.x)
-        sq[i] = load_elem(P.q, ((int64_t)b * P.Hq + hk * g) * D + i, P.q_dtype) * P.qscale;
     const int sink_end = min(S, L);
     const int rec_lo = d_hist_hi(L, S, W);
-    const int n_rec = max(0, L - rec_lo);
-    const int nplain = sink_end + n_rec;
-    __syncthreads();
-    // window logits: thread per (token, head)
-    for (int i = tid; i < nplain * g; i += blockDim.x) {
-        const int t = i / g, j = i % g;
-        const uint16_t* kr = (t < sink_end)
-            ? P.sink + (((int64_t)rq * S + t) * P.Hkv + hk) * 2 * D
-            : P.recent + (((int64_t)rq * W + (rec_lo + t - sink_end) % W) * P.Hkv + hk) * 2 * D;
-        float acc = 0.f;
-        for (int c = 0; c < D; c += 2) {
-            const uint32_t two = *reinterpret_cast<const uint32_t*>(kr + c);
-            acc = fmaf(sq[j * D + c], __uint_as_float(two << 16), acc);
-            acc = fmaf(sq[j * D + c + 1], __uint_as_float(two & 0xFFFF0000u), acc);
-        }
-        slog[j * nwin + t] = acc;
+    const int nplain = L > 0 ? sink_end + max(0, L - rec_lo) : 0;
+    const int t0 = wt * kWinTile;
+    const int nt = min(kWinTile, nplain - t0);
+    const int64_t pbase = ((int64_t)b * P.Hq + hk * g) * P.n_win_tiles + wt;   // + j * n_win_tiles
+    if (nt <= 0) {                                 // empty tile: neutral partial
+        for (int j = tid; j < g; j += kCombThreads) P.wml[pbase + (int64_t)j * P.n_win_tiles] = make_float2(-1e30f, 0.f);
+        return;
+    }
+    for (int i = tid; i < g * D; i += kCombThreads)
+        sq[i] = load_elem(P.q, ((int64_t)b * P.Hq + hk * g) * D + i, P.q_dtype) * P.qscale;
+    for (int i = tid; i < nt * (D / 8); i += kCombThreads) {
+        const int t = i / (D / 8), c8 = i % (D / 8);
+        const int tt = t0 + t;
+        const uint16_t* base = (tt < sink_end)
+            ? P.sink + (((int64_t)rq * S + tt) * P.Hkv + hk) * 2 * D
+            : P.recent + (((int64_t)rq * W + (rec_lo + tt - sink_end) % W) * P.Hkv + hk) * 2 * D;
+        const uint4 kq = *reinterpret_cast<const uint4*>(base + c8 * 8);
+        const uint4 vq = *reinterpret_cast<const uint4*>(base + D + c8 * 8);
+        uint32_t* kd = sk + t * kRowW + c8 * 4;
+        uint32_t* vd = sv + t * kRowW + c8 * 4;
+        kd[0] = kq.x; kd[1] = kq.y; kd[2] = kq.z; kd[3] = kq.w;
+        vd[0] = vq.x; vd[1] = vq.y; vd[2] = vq.z; vd[3] = vq.w;
     }
     __syncthreads();
-    const int warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
-    // history partials of request b: CTAs owning chunks [cprefix[b], cprefix[b+1])
+    for (int i = tid; i < nt * g; i += kCombThreads) {     // logits: thread per (token, head)
+        const int t = i % nt, j = i / nt;
+        const uint32_t* kr = sk + t * kRowW;
+        const float* qj = sq + j * D;
+        float acc = 0.f;
+#pragma unroll 8
+        for (int w = 0; w < D / 2; ++w) {
+            const uint32_t two = kr[w];
+            acc = fmaf(qj[2 * w], __uint_as_float(two << 16), acc);
+            acc = fmaf(qj[2 * w + 1], __uint_as_float(two & 0xFFFF0000u), acc);
+        }
+        sp[j * kWinTile + t] = acc;
+    }
+    __syncthreads();
+    for (int j = warp; j < g; j += kCombThreads / 32) {    // softmax of the tile, per head
+        float mx = -INFINITY;
+        for (int t = lane; t < nt; t += 32) mx = fmaxf(mx, sp[j * kWinTile + t]);
+        for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        float sum = 0.f;
+        for (int t = lane; t < nt; t += 32) {
+            const float pv = exp2f(sp[j * kWinTile + t] - mx);
+            sp[j * kWinTile + t] = pv;
+            sum += pv;
+        }
+        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if (lane == 0) {
+            sml[2 * j] = mx;
+            sml[2 * j + 1] = sum;
+            P.wml[pbase + (int64_t)j * P.n_win_tiles] = make_float2(mx, sum);
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < g * (D / 2); i += kCombThreads) {   // P·V: thread per (head, channel pair)
+        const int j = i / (D / 2), w = i % (D / 2);
+        float x0 = 0.f, x1 = 0.f;
+        const float* pj = sp + j * kWinTile;
+        for (int t = 0; t < nt; ++t) {
+            const uint32_t two = sv[t * kRowW + w];
+            x0 = fmaf(pj[t], __uint_as_float(two << 16), x0);
+            x1 = fmaf(pj[t], __uint_as_float(two & 0xFFFF0000u), x1);
+        }
+        float* o = P.wo + (pbase + (int64_t)j * P.n_win_tiles) * D;
+        o[2 * w] = x0;
+        o[2 * w + 1] = x1;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// combine: one block of 128 threads per (KV head, request).  Merges the BF16
+// window tiles and, separately, the history partials by log-sum-exp, applies
+// R_Vᵀ once to the merged rotated-domain sum, and merges the two domains:
+//   out = (e^{m_p-M}·Σ_bf16 p v + e^{m_r-M}·(Σ_hist p v̂)·R_Vᵀ) / (e^{m_p-M} l_p + e^{m_r-M} l_r).
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams P) {
+    extern __shared__ __align__(16) float s_c[];
+    const int hk = blockIdx.x, b = blockIdx.y;
+    const int g = P.g;
+    float* srot = s_c;                             // [g][D] merged rotated sum
+    float* spl = srot + g * D;                     // [g][D] merged window sum
+    float* sst = spl + g * D;                      // [g][4]: m_p, l_p, m_r, l_r
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int L = P.len[b];
+    float* outp = P.out + ((int64_t)b * P.Hq + hk * g) * D;
+    if (L <= 0) {
+        for (int i = tid; i < g * D; i += kCombThreads) outp[i] = 0.f;
+        return;
+    }
     const int64_t N = P.cprefix[P.batch];
     const int64_t c0 = P.cprefix[b], c1 = P.cprefix[b + 1];
     const int64_t i_lo = c1 > c0 ? chunk_owner(c0, N, P.n_ctas) : 0;
     const int64_t i_hi = c1 > c0 ? chunk_owner(c1 - 1, N, P.n_ctas) : -1;
-    // per head: window max/sum (warp j), and the LSE merge of the history partials
-    for (int j = warp; j < g; j += nw) {
-        float mx = -INFINITY;
-        for (int t = lane; t < nplain; t += 32) mx = fmaxf(mx, slog[j * nwin + t]);
-        for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        float sum = 0.f;
-        for (int t = lane; t < nplain; t += 32) {
-            const float p = exp2f(slog[j * nwin + t] - mx);
-            slog[j * nwin + t] = p;
-            sum += p;
-        }
-        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    const int nwt = P.n_win_tiles;
+    for (int j = warp; j < g; j += kCombThreads / 32) {
         const int hq = hk * g + j;
-        float M = -INFINITY;
-        for (int i = i_lo + lane; i <= i_hi; i += 32) {
-            if (!cta_has_work(i, N, P.n_ctas)) continue;
-            M = fmaxf(M, P.ml[((int64_t)i + b) * P.Hq + hq].x);
+        const float2* wml = P.wml + ((int64_t)b * P.Hq + hq) * nwt;
+        float Mp = -INFINITY, Mr = -INFINITY;
+        for (int t = lane; t < nwt; t += 32) Mp = fmaxf(Mp, wml[t].x);
+        for (int64_t i = i_lo + lane; i <= i_hi; i += 32)
+            if (cta_has_work(i, N, P.n_ctas)) Mr = fmaxf(Mr, P.ml[(i + b) * P.Hq + hq].x);
+        for (int off = 16; off; off >>= 1) {
+            Mp = fmaxf(Mp, __shfl_xor_sync(0xffffffffu, Mp, off));
+            Mr = fmaxf(Mr, __shfl_xor_sync(0xffffffffu, Mr, off));
         }
-        for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        float lr = 0.f;
-        for (int i = i_lo + lane; i <= i_hi; i += 32) {
+        float lp = 0.f, lr = 0.f;
+        for (int t = lane; t < nwt; t += 32)
+            if (wml[t].y > 0.f) lp += exp2f(wml[t].x - Mp) * wml[t].y;
+        for (int64_t i = i_lo + lane; i <= i_hi; i += 32) {
             if (!cta_has_work(i, N, P.n_ctas)) continue;
-            const float2 ml = P.ml[((int64_t)i + b) * P.Hq + hq];
-            if (ml.x != -INFINITY) lr += exp2f(ml.x - M) * ml.y;
+            const float2 ml = P.ml[(i + b) * P.Hq + hq];
+            if (ml.y > 0.f) lr += exp2f(ml.x - Mr) * ml.y;
         }
-        for (int off = 16; off; off >>= 1) lr += __shfl_xor_sync(0xffffffffu, lr, off);
+        for (int off = 16; off; off >>= 1) {
+            lp += __shfl_xor_sync(0xffffffffu, lp, off);
+            lr += __shfl_xor_sync(0xffffffffu, lr, off);
+        }
         if (lane == 0) {
-            sred[j * 4 + 0] = mx;
-            sred[j * 4 + 1] = sum;
-            sred[j * 4 + 2] = M;
-            sred[j * 4 + 3] = lr;
+            sst[j * 4 + 0] = Mp;
+            sst[j * 4 + 1] = lp;
+            sst[j * 4 + 2] = Mr;
+            sst[j * 4 + 3] = lr;
         }
     }
     __syncthreads();
-    // merged rotated sum: thread per (head, channel)
-    for (int i = tid; i < g * D; i += blockDim.x) {
+    for (int i = tid; i < g * D; i += kCombThreads) {
         const int j = i / D, c = i % D;
         const int hq = hk * g + j;
-        const float M = sred[j * 4 + 2];
-        float acc = 0.f;
+        const float Mp = sst[j * 4 + 0], Mr = sst[j * 4 + 2];
+        float ap = 0.f;
+        const int64_t wb = ((int64_t)b * P.Hq + hq) * nwt;
+        for (int t = 0; t < nwt; ++t) {
+            const float2 ml = P.wml[wb + t];
+            if (ml.y > 0.f) ap = fmaf(exp2f(ml.x - Mp), P.wo[(wb + t) * D + c], ap);
+        }
+        spl[i] = ap;
+        float ar = 0.f;
         for (int64_t ci = i_lo; ci <= i_hi; ++ci) {
             if (!cta_has_work(ci, N, P.n_ctas)) continue;
             const int64_t sl = ci + b;
             const float2 ml = P.ml[sl * P.Hq + hq];
-            if (ml.x == -INFINITY) continue;
-            acc = fmaf(exp2f(ml.x - M), P.po[(sl * P.Hq + hq) * D + c], acc);
+            if (ml.y > 0.f) ar = fmaf(exp2f(ml.x - Mr), P.po[(sl * P.Hq + hq) * D + c], ar);
         }
-        sorot[i] = acc;
+        srot[i] = ar;
     }
     __syncthreads();
-    // out = (e^{m_p-M}·Σ p v + e^{m_r-M}·(Σ_rot)·R_Vᵀ) / (e^{m_p-M} l_p + e^{m_r-M} l_r)
-    for (int i = tid; i < g * D; i += blockDim.x) {
-        const int j = i / D, c = i % D;
-        const float mp = sred[j * 4 + 0], lp = sred[j * 4 + 1], mr = sred[j * 4 + 2], lr = sred[j * 4 + 3];
-        const float Mx = fmaxf(mp, mr);
-        const float wp = (mp == -INFINITY) ? 0.f : exp2f(mp - Mx);
-        const float wr = (mr == -INFINITY) ? 0.f : exp2f(mr - Mx);
-        float plain = 0.f;
-        for (int t = 0; t < nplain; ++t) {
-            const uint16_t* vr = (t < sink_end)
-                ? P.sink + (((int64_t)rq * S + t) * P.Hkv + hk) * 2 * D + D
-                : P.recent + (((int64_t)rq * W + (rec_lo + t - sink_end) % W) * P.Hkv + hk) * 2 * D + D;
-            plain = fmaf(slog[j * nwin + t], bf16_bits_to_f32(vr[c]), plain);
+    // (Σ_hist p v̂)·R_Vᵀ : (x·R_Vᵀ)[c] = Σ_k x[k]·R_V[c][k]; thread per channel c
+    for (int c = tid; c < D; c += kCombThreads) {
+        float accj[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) accj[j] = 0.f;
+        const float4* rrow = reinterpret_cast<const float4*>(P.rot_v + (int64_t)c * D);
+        for (int k4 = 0; k4 < D / 4; ++k4) {
+            const float4 rv = rrow[k4];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (j < g) {
+                    const float* x = srot + j * D + 4 * k4;
+                    accj[j] = fmaf(x[0], rv.x, fmaf(x[1], rv.y, fmaf(x[2], rv.z, fmaf(x[3], rv.w, accj[j]))));
+                }
+            }
         }
-        float rot = 0.f;
-        if (wr != 0.f) {
-            const float* rrow = P.rot_v + (int64_t)c * D;   // (x·R_Vᵀ)[c] = Σ_k x[k]·R_V[c][k]
-            for (int k = 0; k < D; ++k) rot = fmaf(sorot[j * D + k], rrow[k], rot);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (j >= g) break;
+            const float mp = sst[j * 4 + 0], lp = sst[j * 4 + 1], mr = sst[j * 4 + 2], lr = sst[j * 4 + 3];
+            const float Mx = fmaxf(mp, mr);
+            const float wp = lp > 0.f ? exp2f(mp - Mx) : 0.f;
+            const float wr = lr > 0.f ? exp2f(mr - Mx) : 0.f;
+            outp[j * D + c] = (wp * spl[j * D + c] + wr * accj[j]) / (wp * lp + wr * lr);
         }
-        const float den = wp * lp + wr * lr;
-        outp[j * D + c] = (wp * plain + wr * rot) / den;
     }
 }
 
@@ -502,13 +592,20 @@ extern "C" int oscar_decode_workspace_bytes(const oscar_config* cfg, int32_t bat
 }
 
 namespace oscar {
-int launch_history_mma(const DecodeParams& P, int head_dim, cudaStream_t st, bool* launched);
+int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* launched);
 }
 
 template <int D>
 static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
-    prep_kernel<D><<<P.batch, 256, 0, st>>>(P);
+    prep_kernel<D><<<dim3(P.batch, (P.Hq + 15) / 16), 256, 0, st>>>(P);
     int rc = check_cuda("prep_kernel launch");
+    if (rc) return rc;
+    const size_t wsmem = ((size_t)P.g * D + (size_t)P.g * kWinTile + 2 * P.g) * 4 +
+                         (size_t)2 * kWinTile * (D / 2 + 1) * 4;
+    if (cudaFuncSetAttribute(window_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsmem) != cudaSuccess)
+        return check_cuda("cudaFuncSetAttribute(window_kernel)");
+    window_kernel<D><<<dim3(P.Hkv, P.batch, P.n_win_tiles), kCombThreads, wsmem, st>>>(P);
+    rc = check_cuda("window_kernel launch");
     if (rc) return rc;
     bool done = false;
     const int prof = prof_begin(0, st);
@@ -537,10 +634,10 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
         if (rc) return rc;
     }
     prof_end(prof, st);
-    const size_t csmem = ((size_t)P.g * D * 2 + (size_t)P.g * (P.S + P.W) + (size_t)P.g * 4) * 4;
+    const size_t csmem = ((size_t)P.g * D * 2 + (size_t)P.g * 4) * 4;
     if (cudaFuncSetAttribute(combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem) != cudaSuccess)
         return check_cuda("cudaFuncSetAttribute(combine_kernel)");
-    combine_kernel<D><<<dim3(P.Hkv, P.batch), 256, csmem, st>>>(P);
+    combine_kernel<D><<<dim3(P.Hkv, P.batch), kCombThreads, csmem, st>>>(P);
     return check_cuda("combine_kernel launch");
 }
 
@@ -589,16 +686,19 @@ static int decode_impl(const oscar_config* cfg, const oscar_layer_cache* cache, 
     P.chunk = plan.chunk;
     P.n_ctas = plan.max_ctas;          // set by the history launcher
     P.n_frag_tiles = plan.n_frag_tiles;
+    P.n_win_tiles = plan.n_win_tiles;
     P.qscale = (float)(1.4426950408889634 / std::sqrt((double)cfg->head_dim));
     char* ws = reinterpret_cast<char*>(workspace);
     P.len = reinterpret_cast<int32_t*>(ws + plan.off_len);
     P.req = reinterpret_cast<int32_t*>(ws + plan.off_req);
     P.cprefix = reinterpret_cast<int32_t*>(ws + plan.off_cprefix);
     P.qt = reinterpret_cast<float*>(ws + plan.off_qt);
-    P.qsum = reinterpret_cast<float*>(ws + plan.off_qsum);
+    P.qsum = reinterpret_cast<float2*>(ws + plan.off_qsum);
     P.qfrag = reinterpret_cast<uint2*>(ws + plan.off_qfrag);
     P.ml = reinterpret_cast<float2*>(ws + plan.off_ml);
     P.po = reinterpret_cast<float*>(ws + plan.off_o);
+    P.wml = reinterpret_cast<float2*>(ws + plan.off_wml);
+    P.wo = reinterpret_cast<float*>(ws + plan.off_wo);
     P.status = status_word();
     if (!P.status) return OSCAR_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

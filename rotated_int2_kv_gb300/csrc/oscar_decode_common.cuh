@@ -22,8 +22,9 @@ struct DecodePlan {
     int max_ctas;     // upper bound of the history grid
     int part_slots;   // max_ctas + batch
     int n_frag_tiles; // n-tiles of 8 columns for the fragment-packed queries
+    int n_win_tiles;  // 64-token tiles of the BF16 sink + recent windows
     // workspace offsets (bytes, 256-aligned)
-    size_t off_len, off_req, off_cprefix, off_qt, off_qsum, off_qfrag, off_ml, off_o, total;
+    size_t off_len, off_req, off_cprefix, off_qt, off_qsum, off_qfrag, off_ml, off_o, off_wml, off_wo, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -43,15 +44,18 @@ inline DecodePlan make_plan(const oscar_config* cfg, int batch, int max_seq_len,
     p.max_ctas = std::max(1, n_sm) * 4;
     p.part_slots = p.max_ctas + batch;
     p.n_frag_tiles = (2 * g + 7) / 8;
+    p.n_win_tiles = (cfg->sink + cfg->recent + 63) / 64;
     size_t off = 0;
     p.off_len = off;      off = align256(off + (size_t)batch * 4);
     p.off_req = off;      off = align256(off + (size_t)batch * 4);
     p.off_cprefix = off;  off = align256(off + (size_t)(batch + 1) * 4);
     p.off_qt = off;       off = align256(off + (size_t)batch * Hq * d * 4);
-    p.off_qsum = off;     off = align256(off + (size_t)batch * Hq * ng * 4);
+    p.off_qsum = off;     off = align256(off + (size_t)batch * Hq * ng * 8);
     p.off_qfrag = off;    off = align256(off + (size_t)batch * Hkv * p.n_frag_tiles * (d / 16) * 32 * 8);
     p.off_ml = off;       off = align256(off + (size_t)p.part_slots * Hq * 8);
     p.off_o = off;        off = align256(off + (size_t)p.part_slots * Hq * d * 4);
+    p.off_wml = off;      off = align256(off + (size_t)batch * Hq * p.n_win_tiles * 8);
+    p.off_wo = off;       off = align256(off + (size_t)batch * Hq * p.n_win_tiles * d * 4);
     p.total = off;
     return p;
 }
@@ -74,7 +78,7 @@ struct DecodeParams {
     int64_t num_slots;
     int max_reqs;
     int Hq, Hkv, g, S, W, G, ng, rec_bytes;
-    int chunk, n_frag_tiles;
+    int chunk, n_frag_tiles, n_win_tiles;
     int n_ctas;        // history grid actually launched (<= plan.max_ctas)
     float qscale;      // log2(e) / sqrt(d)
     // workspace
@@ -82,10 +86,13 @@ struct DecodeParams {
     int32_t* req;      // window row per request
     int32_t* cprefix;  // exclusive prefix of history chunk counts, [batch + 1]
     float* qt;         // q·R_K·qscale, [batch][Hq][d]
-    float* qsum;       // per-group sums of the fragment-packed q̃, [batch][Hq][ng]
+    float2* qsum;      // per group of the fp16 hi+lo parts of q̃: (Σ q̃, Σ q̃/α) with α the
+                       // per-channel code weight of the MMA path, [batch][Hq][ng]
     uint2* qfrag;      // fp16 hi/lo B fragments, [batch][Hkv][n_tiles][d/16][32]
     float2* ml;        // (m, l) per partial slot, [part_slots][Hq]
     float* po;         // unnormalised o per partial slot, [part_slots][Hq][d]
+    float2* wml;       // (m, l) per BF16 window tile, [batch][Hq][n_win_tiles]
+    float* wo;         // unnormalised o per BF16 window tile, [batch][Hq][n_win_tiles][d]
     int* status;
 };
 

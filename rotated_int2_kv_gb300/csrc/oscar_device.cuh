@@ -24,6 +24,14 @@ __device__ __forceinline__ float load_elem(const void* base, int64_t i, int dtyp
     return reinterpret_cast<const float*>(base)[i];
 }
 
+// 2^x with the hardware approximation (ex2.approx.ftz.f32: relative error
+// about 2^-22, subnormal results flushed to zero); 2^-inf = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void set_status(int* word, int bits) {
     if (word) atomicOr(word, bits);
 }
@@ -55,22 +63,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity), "r"(1000000u) : "memory");
+        : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete.  Gives up after
-// `limit` polls (each poll suspends for up to ~1 ms), sets OSCAR_DEV_TIMEOUT
-// in the status word and returns false; callers then drain and exit.
+// Waits for the phase with the given parity to complete, for at most
+// `budget` SM clock cycles.  On giving up it sets OSCAR_DEV_TIMEOUT in the
+// status word, drops the caller's budget to zero (every later wait makes a
+// single attempt) and returns false.  Callers carry on regardless (every
+// address they use derives from indices, not from the awaited data), so warps
+// that share named barriers stay matched and the kernel ends quickly.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status,
-                                                  uint32_t limit = 4000u) {
-    for (uint32_t i = 0; i < limit; ++i)
+                                                  long long& budget) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && clock64() - t0 > budget) break;
+    }
     set_status(status, 8 /* OSCAR_DEV_TIMEOUT */);
+    budget = 0;
     return false;
 }
+
+// 4-byte asynchronous copy global -> shared (cp.async, completion by groups).
+__device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(smem_addr(dst_smem)), "l"(src) : "memory");
+}
+// 16-byte asynchronous copy global -> shared (both addresses 16-byte aligned).
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_addr(dst_smem)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
 // both addresses 16-byte aligned).
