@@ -50,8 +50,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-append", action="store_true")
-    ap.add_argument("--workload", choices=["qwen8b-100k", "small"], default="qwen8b-100k",
-                    help="small: batch 4 at 65,536 tokens (168 MB of INT2 records, > L2), for ncu captures")
+    ap.add_argument("--workload", choices=["qwen8b-100k", "mid", "small"], default="qwen8b-100k",
+                    help="small: batch 4 at 65,536 tokens (168 MB of INT2 records, > L2), for ncu captures; "
+                         "mid: batch 8 at 100,000 tokens (0.51 GB)")
     return ap.parse_args()
 
 
@@ -309,6 +310,8 @@ def main():
     global B, L_BASE
     if args.workload == "small":
         B, L_BASE = 4, 65536
+    elif args.workload == "mid":
+        B, L_BASE = 8, 100_000
     import torch
     from rotated_int2_kv_gb300 import ops
     if not os.path.exists(ops._LIB_PATH):

@@ -10,12 +10,16 @@
 //
 // Structure (persistent CTAs, one per SM; CTA i owns flattened history chunks
 // [i·N/n, (i+1)·N/n)):
-//  * every warp owns one KV head (two warps per head: token-interleaved
-//    16-token tiles for d <= 128, channel halves for d = 256) and runs its own
-//    gather pipeline: page-table entries are fetched 2·kNPF tiles ahead and the
-//    head's records (rec bytes per token, a slot-major pool) kNPF tiles ahead,
-//    both with cp.async into a private shared-memory ring; waits are
-//    cp.async.wait_group, so warps never block on one another's loads;
+//  * the CTA walks its chunk run in stages of 32·TI tokens through a ring of 4
+//    or 8 shared-memory stages.  Every warp copies, with 16-byte cp.async, a
+//    contiguous run of the stage's token records (all KV heads of a token are
+//    one contiguous slot-major record, so one copy instruction touches one or
+//    two records: few address translations per byte) and arrives on the
+//    stage's full mbarrier when its copies land; slot ids come from a table
+//    that warp 0 fills one ring-depth ahead;
+//  * every warp then consumes its own KV head (and 32-token half when two
+//    warps share a head: token halves for d <= 128, channel halves for
+//    d = 256) of the stage, and releases it on the stage's empty mbarrier;
 //  * each tile runs mma.sync.m16n8k16 f16 → f32.  A code c enters the MMA as
 //    the exact fp16 value 1 + α·c, α = 1/4 for odd and 1/16 for even channels
 //    (one funnel shift exposes two adjacent code positions at bits 8-9 and
@@ -38,8 +42,7 @@ namespace oscar {
 
 namespace mma_detail {
 
-constexpr int kNPF = 8;     // 16-token tiles in flight per warp
-constexpr int kTile = 16;
+constexpr int kTT = 32;     // tokens per consumer tile
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
@@ -95,57 +98,6 @@ __host__ __device__ constexpr int row_bytes(int rec) {
     return ((rec + 15) / 16) % 2 == 1 ? (rec + 15) / 16 * 16 : (rec + 15) / 16 * 16 + 16;
 }
 
-// Walks the segments (one per request) of a CTA's chunk run [f, f1) and, in
-// each, the 16-token tiles first, first + step, ... that belong to one warp.
-struct TileIter {
-    int64_t f, f1, fe;
-    int b, t_seg, t_end, t0, step16;
-    bool valid;
-
-    __device__ void seg(const DecodeParams& P) {
-        valid = f < f1;
-        if (!valid) return;
-        int lo = 0, hi = P.batch - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (P.cprefix[mid] <= f) lo = mid; else hi = mid - 1;
-        }
-        b = lo;
-        fe = min(f1, (int64_t)P.cprefix[b + 1]);
-        const int L = P.len[b];
-        const int h_end = max(P.S, L - P.W);
-        t_seg = P.S + (int)(f - P.cprefix[b]) * P.chunk;
-        t_end = min(h_end, P.S + (int)(fe - P.cprefix[b]) * P.chunk);
-    }
-    // segment iteration (consumers)
-    __device__ void init_seg(const DecodeParams& P, int64_t f0_, int64_t f1_) {
-        f = f0_;
-        f1 = f1_;
-        seg(P);
-    }
-    __device__ void next_seg(const DecodeParams& P) {
-        f = fe;
-        seg(P);
-    }
-    // tile iteration (producers): skips segments with no tile for this warp
-    __device__ void skip_empty(const DecodeParams& P, int first) {
-        while (valid && t_seg + first * mma_detail::kTile >= t_end) next_seg(P);
-        if (valid) t0 = t_seg + first * mma_detail::kTile;
-    }
-    __device__ void init_tiles(const DecodeParams& P, int64_t f0_, int64_t f1_, int first, int step) {
-        step16 = step * mma_detail::kTile;
-        init_seg(P, f0_, f1_);
-        skip_empty(P, first);
-    }
-    __device__ void next_tile(const DecodeParams& P, int first) {
-        t0 += step16;
-        if (t0 >= t_end) {
-            next_seg(P);
-            skip_empty(P, first);
-        }
-    }
-};
-
 // D: head_dim; G: group size; NT: n8 tiles of (head, hi/lo) columns; WPH:
 // warps per head along channels (2 for d = 256); TI: token-interleaved warps
 // per (head, channel slice).
@@ -161,106 +113,189 @@ struct MmaCfg {
     static_assert(WPH * TI <= 2, "at most two warps share a KV head");
 };
 
-// Shared-memory layout: per warp [kNPF][16][row] records, [2·kNPF][16] slot
-// ids, [kNPF] tile masks (warp_bytes apiece), then per head the logit
-// exchange / merge area at x_off.
+// Stage iterator over a CTA's chunk run [f, f1): stages of TT tokens that never
+// cross a request boundary (the last stage of a segment may be partial).
+struct StageIter {
+    int64_t f, f1, fe;
+    int b, t0, t_seg, t_end, tt;
+    bool valid;
+
+    __device__ void seg(const DecodeParams& P) {
+        valid = f < f1;
+        if (!valid) return;
+        int lo = 0, hi = P.batch - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (P.cprefix[mid] <= f) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        fe = min(f1, (int64_t)P.cprefix[b + 1]);
+        const int L = P.len[b];
+        const int h_end = max(P.S, L - P.W);
+        t_seg = P.S + (int)(f - P.cprefix[b]) * P.chunk;
+        t0 = t_seg;
+        t_end = min(h_end, P.S + (int)(fe - P.cprefix[b]) * P.chunk);
+    }
+    __device__ void init(const DecodeParams& P, int64_t f0_, int64_t f1_, int tokens) {
+        f = f0_;
+        f1 = f1_;
+        tt = tokens;
+        seg(P);
+    }
+    __device__ bool seg_first() const { return t0 == t_seg; }
+    __device__ bool seg_last() const { return t0 + tt >= t_end; }
+    __device__ void next(const DecodeParams& P) {
+        t0 += tt;
+        if (t0 >= t_end) {
+            f = fe;
+            seg(P);
+        }
+    }
+};
+
+// Shared-memory layout (byte offsets): [0, 64) full[8] and [64, 128) empty[8]
+// mbarriers, [128, 192) stage masks [16][... ]; the slot table [8][64] at 256;
+// then per warp the fp32 scale table of its current tile (SF bytes each), per
+// head the logit exchange / merge area, and the stage ring at stages_off.
+template <int D, int G, int NT, int WPH, int TI>
+struct MmaSmemCfg {
+    static constexpr int REC = (D / 2 + 8 * (D / G) + 15) / 16 * 16;   // record bytes
+    static constexpr int NG = D / G;
+    static constexpr int SFW = 4 * NG + 2;                              // words per scale row (≡ 2 mod 8)
+    static constexpr int SF = mma_detail::kTT * SFW * 4;
+    static constexpr int TT = mma_detail::kTT * TI;                     // tokens per stage
+    static constexpr int XCH = WPH == 2 ? 2 * 32 * 2 * NT * 4 : 0;     // logit exchange (2 buffers x 2 slices)
+    static constexpr int MRG = TI == 2 ? 32 * NT * MmaCfg<D, G, NT, WPH, TI>::kMT * 2 + 16 * NT : 0;
+    static constexpr int X_FLOATS = XCH + MRG + 4;
+    static constexpr int kBar = 0, kMask = 128, kSlots = 256;
+    static constexpr int kSF = kSlots + 8 * 64 * 4;                     // 2304
+};
+
 template <int D, int G, int NT, int WPH, int TI>
 __global__ void __launch_bounds__(32 * (D == 256 ? 4 : 8) * WPH * TI, 1)
-history_mma_kernel(DecodeParams P, int x_off) {
+history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_log2) {
     using namespace mma_detail;
     using C = MmaCfg<D, G, NT, WPH, TI>;
+    using SC = MmaSmemCfg<D, G, NT, WPH, TI>;
     constexpr int KS = C::kKS, GW = C::kGW, MT = C::kMT, MTG = C::kMTG;
-    constexpr int kXFloats = 2 * 32 * 2 * NT * 2 + 32 * NT * MT * 2 + 64;  // logits x2 buffers + merge
-    constexpr int REC = (D / 2 + 8 * (D / G) + 15) / 16 * 16;   // record bytes (== P.rec_bytes)
-    constexpr int row = row_bytes(REC);         // shared row stride of one token's record
-    constexpr int warp_bytes = (kNPF * kTile * row + 2 * kNPF * kTile * 4 + kNPF * 4 + 127) / 128 * 128;
+    constexpr int REC = SC::REC, NG = SC::NG, SFW = SC::SFW, TT = SC::TT;
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int Hkv = P.Hkv;
+    const int nwarps = blockDim.x >> 5;
     const int h = warp / (WPH * TI);            // KV head
     const int sub = warp % (WPH * TI);
     const int wsl = (WPH == 2) ? sub : 0;       // channel slice
-    const int ti = (TI == 2) ? sub : 0;         // token interleave index
+    const int ti = (TI == 2) ? sub : 0;         // which 32-token half of a stage this warp consumes
     const int r = lane >> 2, j = lane & 3;
     const int g = P.g;
-    unsigned char* ring = smem + warp * warp_bytes;                             // [kNPF][16][row]
-    int32_t* pts = reinterpret_cast<int32_t*>(ring + kNPF * kTile * row);      // [2 kNPF][16]
-    uint32_t* tmask = reinterpret_cast<uint32_t*>(pts + 2 * kNPF * kTile);     // [kNPF]
-    float* xb = reinterpret_cast<float*>(smem + x_off) + h * kXFloats;
+    const uint32_t NS = 1u << ns_log2;
+    const int row = trow;                       // stage row stride of one token (all heads)
+    const int tok_bytes = Hkv * REC;
+    const int cpt = tok_bytes / 16;             // 16-byte chunks per token
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + SC::kBar);
+    uint64_t* empty = full + 8;
+    uint32_t* smask = reinterpret_cast<uint32_t*>(smem + SC::kMask);     // [16 stages][2 halves]
+    int32_t* slots = reinterpret_cast<int32_t*>(smem + SC::kSlots);      // [8][64]
+    float* sf = reinterpret_cast<float*>(smem + SC::kSF + warp * SC::SF);  // [32][SFW]
+    float* xb = reinterpret_cast<float*>(smem + x_off) + h * SC::X_FLOATS;
+    unsigned char* stages = smem + stages_off;
+    const uint32_t stage_bytes = (uint32_t)TT * (uint32_t)row;
     const int bar_id = 1 + h;
 
     const int64_t N = P.cprefix[P.batch];
     const int64_t f0 = (int64_t)blockIdx.x * N / gridDim.x;
     const int64_t f1 = (int64_t)(blockIdx.x + 1) * N / gridDim.x;
     if (f0 >= f1) return;
-    const int first = ti;
-    constexpr int CPR = REC / 16;               // 16-byte chunks per record
-    constexpr int CPH = (CPR + 1) / 2;          // chunks per half-warp lane
-    const uint8_t* recbase = P.records + (int64_t)h * REC;
-    // zero the ring once: rows of invalid tokens then always hold finite values
-    for (int i = lane; i < warp_bytes / 16; i += 32)
-        *reinterpret_cast<uint4*>(ring + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
-    __syncwarp();
 
-    // ---- gather pipeline of this warp ----
-    TileIter itp, itr;
-    itp.init_tiles(P, f0, f1, first, TI);
-    itr = itp;
-    uint32_t kp = 0, kr = 0;
-    auto issue_pt = [&]() {                     // slot ids of tile kp -> pts[kp % 2kNPF]
-        if (itp.valid) {
-            const int p = itp.t0 + lane;
-            if (lane < kTile && p < itp.t_end)
-                cp_async4(pts + (kp % (2 * kNPF)) * kTile + lane, P.page_table + (int64_t)itp.b * P.pt_stride + p);
-            itp.next_tile(P, first);
+    // ---- stage pipeline shared by the whole CTA ----
+    // Warp 0 writes the slot ids (and validity masks) of stage k + NS while the
+    // CTA is at stage k, before it releases stage k; every warp then copies a
+    // contiguous run of 16-byte chunks of whole token records of the stages it
+    // issues (stage k + NS - 1 at iteration k), so a copy instruction touches
+    // one or two records, and arrives on the stage's full barrier when its
+    // copies have landed.
+    long long budget = 4000000000LL;            // cycles per pipeline wait (~2 s); 0 after a timeout
+    const int chunks = TT * cpt;
+    const int cpw = (chunks + nwarps - 1) / nwarps;
+    const int cbeg = warp * cpw, cend = min(chunks, cbeg + cpw);
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < NS; ++s) {
+            mbar_init(&full[s], blockDim.x);
+            mbar_init(&empty[s], nwarps);
         }
-        ++kp;
-    };
-    auto issue_rec = [&]() {                    // records of tile kr -> ring[kr % kNPF]; commits a group
-        if (itr.valid) {
-            const int ntok = min(kTile, itr.t_end - itr.t0);
-            const int32_t* ps = pts + (kr % (2 * kNPF)) * kTile;
-            unsigned char* dst = ring + (kr % kNPF) * kTile * row;
-            // lanes t and t+16 copy token t: chunks [0, CPH) and [CPH, CPR)
-            const int t = lane & 15, c0 = (lane >> 4) * CPH;
-            bool ok = false;
-            int sl = 0;
-            if (t < ntok) {
-                sl = ps[t];
-                ok = sl >= 0 && sl < P.num_slots;
-                if (!ok && lane < 16) set_status(P.status, OSCAR_DEV_BAD_SLOT);
-            }
-            if (ok) {
-                const uint8_t* src = recbase + (int64_t)sl * (Hkv * REC);
-#pragma unroll
-                for (int c = 0; c < CPH; ++c)
-                    if (c0 + c < CPR) cp_async16(dst + t * row + (c0 + c) * 16, src + (c0 + c) * 16);
-            }
-            const uint32_t vm = __ballot_sync(0xffffffffu, ok) & 0xFFFFu;
-            if (lane == 0) tmask[kr % kNPF] = vm;
-            itr.next_tile(P, first);
-        }
-        cp_async_commit();
-        ++kr;
-    };
-    for (int i = 0; i < kNPF; ++i) issue_pt();  // slot ids of the first kNPF tiles
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncwarp();
-    for (int i = 0; i < kNPF; ++i) {            // their records, and the next kNPF slot-id tiles
-        issue_pt();
-        issue_rec();
+        fence_mbar_init();
     }
+    // zero the stage ring once: rows of invalid tokens then always hold finite values
+    for (uint32_t i = threadIdx.x; i < NS * stage_bytes / 16; i += blockDim.x)
+        *reinterpret_cast<uint4*>(stages + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+    // slot ids of stage `it` -> slots[si], mask -> smask[mi] (warp 0)
+    auto put_slots = [&](const StageIter& it, int v0, int v1, uint32_t si, uint32_t mi) {
+        bool ok0 = false, ok1 = false;
+        if (it.valid) {
+            ok0 = it.t0 + lane < it.t_end && v0 >= 0 && v0 < P.num_slots;
+            ok1 = TT > 32 && it.t0 + 32 + lane < it.t_end && v1 >= 0 && v1 < P.num_slots;
+            if ((it.t0 + lane < it.t_end && !ok0) || (TT > 32 && it.t0 + 32 + lane < it.t_end && !ok1))
+                set_status(P.status, OSCAR_DEV_BAD_SLOT);
+        }
+        slots[si * 64 + lane] = ok0 ? v0 : -1;
+        if (TT > 32) slots[si * 64 + 32 + lane] = ok1 ? v1 : -1;
+        const uint32_t m0 = __ballot_sync(0xffffffffu, ok0), m1 = __ballot_sync(0xffffffffu, ok1);
+        if (lane == 0) { smask[mi * 2] = m0; smask[mi * 2 + 1] = m1; }
+    };
+    auto get_slots = [&](const StageIter& it, int* v0, int* v1) {
+        *v0 = -1;
+        *v1 = -1;
+        if (!it.valid) return;
+        const int32_t* pt = P.page_table + (int64_t)it.b * P.pt_stride;
+        if (it.t0 + lane < it.t_end) *v0 = pt[it.t0 + lane];
+        if (TT > 32 && it.t0 + 32 + lane < it.t_end) *v1 = pt[it.t0 + 32 + lane];
+    };
+    StageIter wit;                               // warp 0: stage whose slot ids come next
+    int nv0 = -1, nv1 = -1;                      // warp 0: prefetched slot ids of stage wk
+    uint32_t wk = 0;
+    if (warp == 0) {
+        wit.init(P, f0, f1, TT);
+        for (; wk < NS; ++wk) {
+            int v0, v1;
+            get_slots(wit, &v0, &v1);
+            put_slots(wit, v0, v1, wk % NS, wk % (2 * NS));
+            if (wit.valid) wit.next(P);
+        }
+        get_slots(wit, &nv0, &nv1);              // stage NS
+    }
+    __syncthreads();
+
+    // copies of stage (iterator `it`, global index k) by this warp
+    auto issue = [&](const StageIter& it, uint32_t k) {
+        const uint32_t s = k & (NS - 1);
+        if (k >= NS) mbar_wait_bounded(&empty[s], ((k >> ns_log2) - 1) & 1, P.status, budget);
+        unsigned char* dst = stages + s * stage_bytes;
+        int c = cbeg + lane;
+        int t = c / cpt, piece = c - t * cpt;
+        for (; c < cend; c += 32) {
+            const int sl = slots[s * 64 + t];
+            if (sl >= 0)
+                cp_async16(dst + t * row + piece * 16, P.records + (int64_t)sl * tok_bytes + piece * 16);
+            piece += 32;
+            while (piece >= cpt) { piece -= cpt; ++t; }
+        }
+        cp_async_mbar_arrive(&full[s]);
+    };
+    StageIter pit;                               // stage to issue next (NS - 1 ahead)
+    pit.init(P, f0, f1, TT);
+    uint32_t pk = 0;
+    for (; pk < NS - 1 && pit.valid; ++pk, pit.next(P)) issue(pit, pk);
 
     // funnel shift for the K extraction: code position 2j+1 to bits 8-9 (2j to 6-7)
     const uint32_t rotK = (uint32_t)(4 * j - 6) & 31u;
     int xpar = 0;   // logit-exchange buffer parity; continuous across segments
-    uint32_t k = 0; // tiles consumed
+    uint32_t k = 0; // stages consumed
 
-    TileIter sg;
-    sg.init_seg(P, f0, f1);
-    while (sg.valid) {
-        const int b = sg.b;
+    StageIter it;
+    it.init(P, f0, f1, TT);
+    while (it.valid) {
+        const int b = it.b;
         // ---- per-segment query state ----
         uint32_t bq[NT][KS][2];
         {
@@ -298,94 +333,129 @@ history_mma_kernel(DecodeParams P, int x_off) {
             for (int gi = 0; gi < GW; ++gi) { Wsum[nt][gi] = 0.f; Zsum[nt][gi] = 0.f; }
         }
 
-        for (int t0 = sg.t_seg + first * kTile; t0 < sg.t_end; t0 += TI * kTile, ++k) {
-            cp_async_wait<kNPF - 1>();          // records of tile k have landed
-            __syncwarp();
-            const uint32_t vmask = tmask[k % kNPF];
-            const unsigned char* tb = ring + (k % kNPF) * kTile * row;
-            {
-                const bool v_r = (vmask >> r) & 1u;
-                const bool v_r8 = (vmask >> (r + 8)) & 1u;
-            // ---------------- QK ----------------
-            float sc[GW][NT][4];
+        bool seg_done = false;
+        for (; !seg_done; ++k) {
+            seg_done = it.seg_last();
+            if (pit.valid) {                     // keep NS - 1 stages in flight
+                issue(pit, pk);
+                ++pk;
+                pit.next(P);
+            }
+            const uint32_t s = k & (NS - 1);
+            mbar_wait_bounded(&full[s], (k >> ns_log2) & 1, P.status, budget);
+            if (warp == 0) {
+                // Every thread has issued stage k (its full barrier completed), so the
+                // slot row of stage k is free: it receives the slot ids of stage k + NS,
+                // which the other warps read after waiting for stage k's release.
+                put_slots(wit, nv0, nv1, k & (NS - 1), (k + NS) % (2 * NS));
+                if (wit.valid) wit.next(P);
+                get_slots(wit, &nv0, &nv1);
+            }
+            const uint32_t vmask = smask[(k % (2 * NS)) * 2 + ti];
+            const unsigned char* tb = stages + s * stage_bytes + (ti * 32) * row + h * REC;
+            {   // this tile's (s, z) pairs as fp32: lane t converts token t's K and V pairs
+                const uint32_t* src = reinterpret_cast<const uint32_t*>(tb + lane * row + D / 2);
+                float* dst = sf + lane * SFW;
 #pragma unroll
-            for (int gi = 0; gi < GW; ++gi)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) sc[gi][nt][e] = 0.f;
-            const uint32_t* krow0 = reinterpret_cast<const uint32_t*>(tb + r * row) + wsl * KS;
-            const uint32_t* krow1 = reinterpret_cast<const uint32_t*>(tb + (r + 8) * row) + wsl * KS;
-#pragma unroll
-            for (int k4 = 0; k4 < KS; k4 += 4) {
-                const uint4 w0 = *reinterpret_cast<const uint4*>(krow0 + k4);
-                const uint4 w1 = *reinterpret_cast<const uint4*>(krow1 + k4);
-                const uint32_t a0s[4] = {w0.x, w0.y, w0.z, w0.w};
-                const uint32_t a1s[4] = {w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int kk = k4 + q;
-                    const int gi = (kk * 16) / G;
-                    const uint32_t y0 = rotr(a0s[q], rotK), y1 = rotr(a1s[q], rotK);
-                    const uint32_t x0 = code_q16(y0), x1 = code_q16(y1);   // channels 2j, 2j+8
-                    const uint32_t x2 = code_q4(y0), x3 = code_q4(y1);     // channels 2j+1, 2j+9
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        mma16816(sc[gi][nt], x0, x1, x2, x3, bq[nt][kk][0], bq[nt][kk][1]);
+                for (int e = 0; e < 2 * NG; ++e) {
+                    const float2 v = h2f(src[e]);
+                    *reinterpret_cast<float2*>(dst + 2 * e) = v;
                 }
             }
-            // logits (log2 units) for rows r, r+8 and head 4nt + j
-            float lg[NT][2];
+            __syncwarp();
+            // ---------------- QK: two m16 tiles (tokens 0-15, 16-31) ----------------
+            float sc[2][GW][NT][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) { lg[nt][0] = 0.f; lg[nt][1] = 0.f; }
+            for (int mq = 0; mq < 2; ++mq)
 #pragma unroll
-            for (int gi = 0; gi < GW; ++gi) {
-                const int gg = wsl * GW + gi;
-                const float2 sz0 = h2f(*reinterpret_cast<const uint32_t*>(tb + r * row + D / 2 + 4 * gg));
-                const float2 sz1 = h2f(*reinterpret_cast<const uint32_t*>(tb + (r + 8) * row + D / 2 + 4 * gg));
+                for (int gi = 0; gi < GW; ++gi)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const float2 Q = qs[nt][gi];       // (Σ q̃, Σ q̃/α)
-                    lg[nt][0] += sz0.x * (sc[gi][nt][0] + sc[gi][nt][1] - Q.y) + sz0.y * Q.x;
-                    lg[nt][1] += sz1.x * (sc[gi][nt][2] + sc[gi][nt][3] - Q.y) + sz1.y * Q.x;
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sc[mq][gi][nt][e] = 0.f;
+#pragma unroll
+            for (int k4 = 0; k4 < KS; k4 += 4) {
+#pragma unroll
+                for (int mq = 0; mq < 2; ++mq) {
+                    const uint4 w0 = *reinterpret_cast<const uint4*>(
+                        reinterpret_cast<const uint32_t*>(tb + (16 * mq + r) * row) + wsl * KS + k4);
+                    const uint4 w1 = *reinterpret_cast<const uint4*>(
+                        reinterpret_cast<const uint32_t*>(tb + (16 * mq + r + 8) * row) + wsl * KS + k4);
+                    const uint32_t a0s[4] = {w0.x, w0.y, w0.z, w0.w};
+                    const uint32_t a1s[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int kk = k4 + q;
+                        const int gi = (kk * 16) / G;
+                        const uint32_t y0 = rotr(a0s[q], rotK), y1 = rotr(a1s[q], rotK);
+                        const uint32_t x0 = code_q16(y0), x1 = code_q16(y1);   // channels 2j, 2j+8
+                        const uint32_t x2 = code_q4(y0), x3 = code_q4(y1);     // channels 2j+1, 2j+9
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma16816(sc[mq][gi][nt], x0, x1, x2, x3, bq[nt][kk][0], bq[nt][kk][1]);
+                    }
+                }
+            }
+            // logits (log2 units) of head 4nt + j for tokens r, r+8, r+16, r+24 (index i = 2mq + half)
+            float lg[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) lg[nt][i] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = 8 * i + r;         // 16·mq + 8·half + r
+                const int mq = i >> 1, hf = i & 1;
+#pragma unroll
+                for (int gi = 0; gi < GW; ++gi) {
+                    const int gg = wsl * GW + gi;
+                    const float2 sz = *reinterpret_cast<const float2*>(sf + t * SFW + 2 * gg);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const float2 Q = qs[nt][gi];       // (Σ q̃, Σ q̃/α)
+                        lg[nt][i] += sz.x * (sc[mq][gi][nt][2 * hf] + sc[mq][gi][nt][2 * hf + 1] - Q.y) + sz.y * Q.x;
+                    }
                 }
             }
             if (WPH == 2) {   // add the other channel slice's partial logits
-                float* my = xb + xpar * (2 * 32 * 2 * NT) + wsl * (32 * 2 * NT);
-                float* ot = xb + xpar * (2 * 32 * 2 * NT) + (1 - wsl) * (32 * 2 * NT);
+                float* my = xb + xpar * (2 * 32 * 4 * NT) + wsl * (32 * 4 * NT);
+                float* ot = xb + xpar * (2 * 32 * 4 * NT) + (1 - wsl) * (32 * 4 * NT);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    my[(nt * 2 + 0) * 32 + lane] = lg[nt][0];
-                    my[(nt * 2 + 1) * 32 + lane] = lg[nt][1];
-                }
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) my[(nt * 4 + i) * 32 + lane] = lg[nt][i];
                 named_bar(bar_id, 64);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    lg[nt][0] += ot[(nt * 2 + 0) * 32 + lane];
-                    lg[nt][1] += ot[(nt * 2 + 1) * 32 + lane];
-                }
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) lg[nt][i] += ot[(nt * 4 + i) * 32 + lane];
                 xpar ^= 1;
             }
-            // ---------------- online softmax ----------------
-            float pr[NT][2];
+            // ---------------- online softmax over the 32 tokens ----------------
+            float pr[NT][4];
             bool grew = false;
             float alpha[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const bool hv = (4 * nt + j) < g;
-                const float x0 = (v_r && hv) ? lg[nt][0] : -INFINITY;
-                const float x1 = (v_r8 && hv) ? lg[nt][1] : -INFINITY;
-                float tm = fmaxf(x0, x1);
+                float x[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) x[i] = (hv && ((vmask >> (8 * i + r)) & 1u)) ? lg[nt][i] : -INFINITY;
+                float tm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
                 tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
                 tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
                 tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
                 const float mn = fmaxf(m_run[nt], tm);
                 grew |= mn > m_run[nt];
-                alpha[nt] = fast_exp2(m_run[nt] - mn);           // m_run starts at a finite -1e30
+                alpha[nt] = fast_exp2(m_run[nt] - mn);
                 m_run[nt] = mn;
-                pr[nt][0] = fast_exp2(x0 - mn);                  // masked tokens: 2^-inf = 0
-                pr[nt][1] = fast_exp2(x1 - mn);
-                l_run[nt] = l_run[nt] * alpha[nt] + pr[nt][0] + pr[nt][1];
+                float ps = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    pr[nt][i] = fast_exp2(x[i] - mn);              // masked tokens: 2^-inf = 0
+                    ps += pr[nt][i];
+                }
+                l_run[nt] = l_run[nt] * alpha[nt] + ps;
             }
             if (__any_sync(0xffffffffu, grew)) {
 #pragma unroll
@@ -399,79 +469,52 @@ history_mma_kernel(DecodeParams P, int x_off) {
                     for (int gi = 0; gi < GW; ++gi) { Wsum[nt][gi] *= ab; Zsum[nt][gi] *= ab; }
                 }
             }
-            // ---------------- P·V ----------------
-            // p of tokens 2j, 2j+1, 2j+8, 2j+9 for head 4nt + r/2
+            // ---------------- P·V: two k16 steps (tokens 0-15, 16-31) ----------------
             const int srcA = 8 * j + (r >> 1), srcB = srcA + 4;
-            float pb[NT][4];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                pb[nt][0] = __shfl_sync(0xffffffffu, pr[nt][0], srcA);
-                pb[nt][1] = __shfl_sync(0xffffffffu, pr[nt][0], srcB);
-                pb[nt][2] = __shfl_sync(0xffffffffu, pr[nt][1], srcA);
-                pb[nt][3] = __shfl_sync(0xffffffffu, pr[nt][1], srcB);
-            }
-            const int tk[4] = {2 * j, 2 * j + 1, 2 * j + 8, 2 * j + 9};
             const bool lo_part = r & 1;
 #pragma unroll
-            for (int gi = 0; gi < GW; ++gi) {
-                const int gg = wsl * GW + gi;
-                float sv[4], zv[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    // rows of invalid tokens hold finite stale data and get p = 0
-                    const float2 sz = h2f(*reinterpret_cast<const uint32_t*>(
-                        tb + tk[e] * row + D / 2 + 4 * (D / G) + 4 * gg));
-                    sv[e] = sz.x;
-                    zv[e] = sz.y;
-                }
-                uint32_t bv[NT][2];
+            for (int ks = 0; ks < 2; ++ks) {
+                // p of tokens 16ks + {2j, 2j+1, 2j+8, 2j+9} for head 4nt + r/2
+                float pb[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    float w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        w[e] = pb[nt][e] * sv[e];
-                        Wsum[nt][gi] += w[e];
-                        Zsum[nt][gi] = fmaf(pb[nt][e], zv[e], Zsum[nt][gi]);
-                    }
-                    bv[nt][0] = pack_part(w[0], w[1], lo_part);
-                    bv[nt][1] = pack_part(w[2], w[3], lo_part);
+                    pb[nt][0] = __shfl_sync(0xffffffffu, pr[nt][2 * ks], srcA);
+                    pb[nt][1] = __shfl_sync(0xffffffffu, pr[nt][2 * ks], srcB);
+                    pb[nt][2] = __shfl_sync(0xffffffffu, pr[nt][2 * ks + 1], srcA);
+                    pb[nt][3] = __shfl_sync(0xffffffffu, pr[nt][2 * ks + 1], srcB);
                 }
-                // this thread's V code slice of group gg: G/32 bytes per token
-                const int vb = D / 4 + gg * (G / 4) + r * (G / 32);   // byte offset in the record
-                if constexpr (G == 32) {
-                    const uint32_t* w0p = reinterpret_cast<const uint32_t*>(tb + tk[0] * row + (vb & ~3));
-                    const uint32_t* w1p = reinterpret_cast<const uint32_t*>(tb + tk[1] * row + (vb & ~3));
-                    const uint32_t* w2p = reinterpret_cast<const uint32_t*>(tb + tk[2] * row + (vb & ~3));
-                    const uint32_t* w3p = reinterpret_cast<const uint32_t*>(tb + tk[3] * row + (vb & ~3));
-                    const uint32_t bsel = (uint32_t)(vb & 3);
-                    const uint32_t sel = bsel | ((4u + bsel) << 8) | (bsel << 4) | ((4u + bsel) << 12);
-                    const uint32_t u01 = prmt(*w0p, *w1p, sel);
-                    const uint32_t u23 = prmt(*w2p, *w3p, sel);
+                const int tk[4] = {16 * ks + 2 * j, 16 * ks + 2 * j + 1, 16 * ks + 2 * j + 8, 16 * ks + 2 * j + 9};
 #pragma unroll
-                    for (int mu = 0; mu < 2; ++mu) {
-                        const int mt = gi * MTG + mu;
-                        const uint32_t rb = (uint32_t)(4 * mu - 6) & 31u;   // position 2mu+1 -> bits 8-9
-                        const uint32_t y01 = rotr(u01, rb), y23 = rotr(u23, rb);
-                        const uint32_t a0 = code_q16(y01), a1 = code_q4(y01);
-                        const uint32_t a2 = code_q16(y23), a3 = code_q4(y23);
+                for (int gi = 0; gi < GW; ++gi) {
+                    const int gg = wsl * GW + gi;
+                    uint32_t bv[NT][2];
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            mma16816(acc[nt][mt], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
+                    for (int nt = 0; nt < NT; ++nt) {
+                        float w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            // rows of invalid tokens hold finite stale data and get p = 0
+                            const float2 sz = *reinterpret_cast<const float2*>(sf + tk[e] * SFW + 2 * (NG + gg));
+                            w[e] = pb[nt][e] * sz.x;
+                            Wsum[nt][gi] += w[e];
+                            Zsum[nt][gi] = fmaf(pb[nt][e], sz.y, Zsum[nt][gi]);
+                        }
+                        bv[nt][0] = pack_part(w[0], w[1], lo_part);
+                        bv[nt][1] = pack_part(w[2], w[3], lo_part);
                     }
-                } else {
-#pragma unroll
-                    for (int hw = 0; hw < G / 64; ++hw) {
-                        const int off = vb + 2 * hw;
-                        const uint32_t wsel = (off & 2) ? 0x7632u : 0x5410u;
-                        const int wo = off & ~3;
+                    // this thread's V code slice of group gg: G/32 bytes per token
+                    const int vb = D / 4 + gg * (G / 4) + r * (G / 32);   // byte offset in the record
+                    if constexpr (G == 32) {
+                        const int wo = vb & ~3;
+                        const uint32_t bsel = (uint32_t)(vb & 3);
+                        const uint32_t sel = bsel | ((4u + bsel) << 8) | (bsel << 4) | ((4u + bsel) << 12);
                         const uint32_t u01 = prmt(*reinterpret_cast<const uint32_t*>(tb + tk[0] * row + wo),
-                                                  *reinterpret_cast<const uint32_t*>(tb + tk[1] * row + wo), wsel);
+                                                  *reinterpret_cast<const uint32_t*>(tb + tk[1] * row + wo), sel);
                         const uint32_t u23 = prmt(*reinterpret_cast<const uint32_t*>(tb + tk[2] * row + wo),
-                                                  *reinterpret_cast<const uint32_t*>(tb + tk[3] * row + wo), wsel);
+                                                  *reinterpret_cast<const uint32_t*>(tb + tk[3] * row + wo), sel);
 #pragma unroll
-                        for (int mu = 0; mu < 4; ++mu) {
-                            const int mt = gi * MTG + hw * 4 + mu;
+                        for (int mu = 0; mu < 2; ++mu) {
+                            const int mt = gi * MTG + mu;
                             const uint32_t rb = (uint32_t)(4 * mu - 6) & 31u;   // position 2mu+1 -> bits 8-9
                             const uint32_t y01 = rotr(u01, rb), y23 = rotr(u23, rb);
                             const uint32_t a0 = code_q16(y01), a1 = code_q4(y01);
@@ -480,13 +523,34 @@ history_mma_kernel(DecodeParams P, int x_off) {
                             for (int nt = 0; nt < NT; ++nt)
                                 mma16816(acc[nt][mt], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
                         }
+                    } else {
+#pragma unroll
+                        for (int hw = 0; hw < G / 64; ++hw) {
+                            const int off = vb + 2 * hw;
+                            const uint32_t wsel = (off & 2) ? 0x7632u : 0x5410u;
+                            const int wo = off & ~3;
+                            const uint32_t u01 = prmt(*reinterpret_cast<const uint32_t*>(tb + tk[0] * row + wo),
+                                                      *reinterpret_cast<const uint32_t*>(tb + tk[1] * row + wo), wsel);
+                            const uint32_t u23 = prmt(*reinterpret_cast<const uint32_t*>(tb + tk[2] * row + wo),
+                                                      *reinterpret_cast<const uint32_t*>(tb + tk[3] * row + wo), wsel);
+#pragma unroll
+                            for (int mu = 0; mu < 4; ++mu) {
+                                const int mt = gi * MTG + hw * 4 + mu;
+                                const uint32_t rb = (uint32_t)(4 * mu - 6) & 31u;   // position 2mu+1 -> bits 8-9
+                                const uint32_t y01 = rotr(u01, rb), y23 = rotr(u23, rb);
+                                const uint32_t a0 = code_q16(y01), a1 = code_q4(y01);
+                                const uint32_t a2 = code_q16(y23), a3 = code_q4(y23);
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt)
+                                    mma16816(acc[nt][mt], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
+                            }
+                        }
                     }
                 }
             }
-            }
-            __syncwarp();                       // ring slot k % kNPF is free again
-            issue_pt();
-            issue_rec();
+            __syncwarp();                       // this warp is done with stage k and its scale table
+            if (lane == 0) mbar_arrive(&empty[s]);
+            it.next(P);
         }
 
         // ---------------- segment end: reduce, merge, write the partial ----------------
@@ -521,7 +585,7 @@ history_mma_kernel(DecodeParams P, int x_off) {
             }
         }
         if (TI == 2) {   // merge the two token-interleaved warps of this head
-            float* mb = xb + 2 * 32 * 2 * NT;
+            float* mb = xb;
             if (ti == 1) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
@@ -580,36 +644,41 @@ history_mma_kernel(DecodeParams P, int x_off) {
                 }
             }
         }
-        sg.next_seg(P);
     }
-    cp_async_wait<0>();
 }
 
-// Shared-memory plan: (offset of the exchange areas, total bytes).
+// Stage row stride of one token (all KV heads): rounded up to an odd multiple
+// of 16 bytes so that 8 consecutive rows start in 8 different 4-bank groups.
+static int token_row_bytes(int tok_bytes) { return row_bytes(tok_bytes); }
+
+// Shared-memory plan: (x_off, stages_off, ring depth log2, total bytes).
 template <int D, int G, int NT, int WPH, int TI>
-static void mma_smem_plan(int Hkv, int* x_off, size_t* total) {
-    using namespace mma_detail;
-    constexpr int kXFloats = 2 * 32 * 2 * NT * 2 + 32 * NT * MmaCfg<D, G, NT, WPH, TI>::kMT * 2 + 64;
-    constexpr int REC = (D / 2 + 8 * (D / G) + 15) / 16 * 16;
-    constexpr int row = row_bytes(REC);
-    constexpr int warp_bytes = (kNPF * kTile * row + 2 * kNPF * kTile * 4 + kNPF * 4 + 127) / 128 * 128;
-    *x_off = Hkv * WPH * TI * warp_bytes;
-    *total = (size_t)*x_off + (size_t)Hkv * kXFloats * 4;
+static bool mma_smem_plan(int Hkv, int* x_off, int* stages_off, int* ns_log2, size_t* total) {
+    using SC = MmaSmemCfg<D, G, NT, WPH, TI>;
+    const int nwarps = Hkv * WPH * TI;
+    *x_off = SC::kSF + nwarps * SC::SF;
+    *stages_off = (*x_off + Hkv * SC::X_FLOATS * 4 + 127) / 128 * 128;
+    const size_t stage = (size_t)SC::TT * token_row_bytes(Hkv * SC::REC);
+    int lg = 3;                                  // 8 stages when they fit, else 4
+    if (*stages_off + (stage << 3) > 224 * 1024) lg = 2;
+    *ns_log2 = lg;
+    *total = *stages_off + (stage << lg);
+    return *total <= 225 * 1024;
 }
 
 template <int D, int G, int NT, int WPH, int TI>
 static int launch_mma(DecodeParams P, cudaStream_t st) {
     const int threads = 32 * P.Hkv * WPH * TI;
-    int x_off;
+    int x_off, stages_off, ns_log2;
     size_t smem;
-    mma_smem_plan<D, G, NT, WPH, TI>(P.Hkv, &x_off, &smem);
-    if (smem > 225 * 1024) return OSCAR_ERR_ARG;
+    if (!mma_smem_plan<D, G, NT, WPH, TI>(P.Hkv, &x_off, &stages_off, &ns_log2, &smem)) return OSCAR_ERR_ARG;
     auto kern = history_mma_kernel<D, G, NT, WPH, TI>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return check_cuda("cudaFuncSetAttribute(history_mma_kernel)");
     const int grid = std::min(P.n_ctas, sm_count());
     P.n_ctas = grid;
-    kern<<<grid, threads, smem, st>>>(P, x_off);
+    const int trow = token_row_bytes(P.Hkv * MmaSmemCfg<D, G, NT, WPH, TI>::REC);
+    kern<<<grid, threads, smem, st>>>(P, x_off, stages_off, trow, ns_log2);
     return check_cuda("history_mma_kernel launch");
 }
 
@@ -622,10 +691,9 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
     const int nt = (2 * P.g + 7) / 8;
     int rc = OSCAR_OK;
     auto go = [&](auto plan, auto fn) {
-        int xo;
+        int xo, so, lg;
         size_t smem;
-        plan(P.Hkv, &xo, &smem);
-        if (smem > 225 * 1024) return;           // does not fit: CUDA-core kernel instead
+        if (!plan(P.Hkv, &xo, &so, &lg, &smem)) return;   // does not fit: CUDA-core kernel instead
         rc = fn(P, st);
         *launched = true;
     };
