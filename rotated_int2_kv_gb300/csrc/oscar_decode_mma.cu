@@ -10,27 +10,29 @@
 //
 // Structure (persistent CTAs, one per SM; CTA i owns flattened history chunks
 // [i·N/n, (i+1)·N/n)):
-//  * the CTA walks its chunk run in stages of 32·TI tokens through a ring of 4
-//    or 8 shared-memory stages.  Every warp copies, with 16-byte cp.async, a
-//    contiguous run of the stage's token records (all KV heads of a token are
-//    one contiguous slot-major record, so one copy instruction touches one or
-//    two records: few address translations per byte) and arrives on the
-//    stage's full mbarrier when its copies land; slot ids come from a table
-//    that warp 0 fills one ring-depth ahead;
-//  * every warp then consumes its own KV head (and 32-token half when two
-//    warps share a head: token halves for d <= 128, channel halves for
-//    d = 256) of the stage, and releases it on the stage's empty mbarrier;
-//  * each tile runs mma.sync.m16n8k16 f16 → f32.  A code c enters the MMA as
-//    the exact fp16 value 1 + α·c, α = 1/4 for odd and 1/16 for even channels
-//    (one funnel shift exposes two adjacent code positions at bits 8-9 and
-//    6-7, and one LOP3 each turns them into fp16); the channel weights 1/α
-//    sit in the other operand or in the epilogue, and the per-group scale s
-//    and zero z are applied in fp32 afterwards:
+//  * the CTA walks its chunk run in stages of TTOK tokens (64, or 32 when a
+//    warp carries two n8 column tiles) through a ring of 4 or 8 shared-memory
+//    stages.  Every warp copies, with 16-byte cp.async, a contiguous run of
+//    the stage's token records (all KV heads of a token are one contiguous
+//    slot-major record, so one copy instruction touches one or two records:
+//    few address translations per byte) and arrives on the stage's full
+//    mbarrier when its copies land; slot ids come from a table that warp 0
+//    fills one ring-depth ahead;
+//  * every warp then consumes its own KV head of the stage (its channel half
+//    for d = 256, where two warps share a head) and releases the stage on its
+//    empty mbarrier;
+//  * each 16-token sub-tile runs mma.sync.m16n8k16 f16 → f32.  A code c
+//    enters the MMA as the exact fp16 value 1 + α·c, α = 1/4 for odd and 1/16
+//    for even channels (one funnel shift exposes two adjacent code positions
+//    at bits 8-9 and 6-7, and one LOP3 each turns them into fp16); the
+//    channel weights 1/α sit in the other operand or in the epilogue, and the
+//    per-group scale s and zero z are applied in fp32 afterwards:
 //        logit = Σ_g [s_g·(Σ (q̃/α)(1 + α c) − Σ q̃/α) + z_g·Σ q̃]
 //        o_rot[ch] = (Σ_t w_t (1 + α_ch c_t) − Σ_t w_t)/α_ch + Σ_t p_t z_t,   w = p·s
 //    q̃/α and p·s are split into fp16 hi + lo parts that occupy the n8 columns
 //    (head, part), so the products carry ~22 bits;
-//  * online softmax in log2 units, partials (m, l, o) per (CTA, request).
+//  * online softmax in log2 units, one running-max update per stage;
+//    partials (m, l, o) per (CTA, request).
 #include <algorithm>
 #include <cmath>
 
@@ -42,23 +44,22 @@ namespace oscar {
 
 namespace mma_detail {
 
-constexpr int kTT = 32;     // tokens per consumer tile
-
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
     return d;
 }
 
-// From x (the word rotated so that code position m sits at bits 8-9 and
-// m-1 at bits 6-7 of each half): half2 of 1 + c/4 for position m, and of
-// 1 + c/16 for position m-1.  Both values are exact in fp16.
 // (x & mask) | one as a single LOP3 (look-up table 0xEA = (a & b) | c).
 __device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t one) {
     uint32_t d;
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "r"(mask), "r"(one));
     return d;
 }
+
+// From x (the word rotated so that code position m sits at bits 8-9 and
+// m-1 at bits 6-7 of each half): half2 of 1 + c/4 for position m, and of
+// 1 + c/16 for position m-1.  Both values are exact in fp16.
 __device__ __forceinline__ uint32_t code_q4(uint32_t x) { return and_or(x, 0x03000300u, 0x3C003C00u); }
 __device__ __forceinline__ uint32_t code_q16(uint32_t x) { return and_or(x, 0x00C000C0u, 0x3C003C00u); }
 __device__ __forceinline__ uint32_t rotr(uint32_t w, uint32_t n) { return __funnelshift_r(w, w, n); }
@@ -92,28 +93,14 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
 
 }  // namespace mma_detail
 
-// Shared row stride of one token's record: rounded up to an odd multiple of
-// 16 B, so that 8 consecutive rows start in 8 different 4-bank groups.
-__host__ __device__ constexpr int row_bytes(int rec) {
-    return ((rec + 15) / 16) % 2 == 1 ? (rec + 15) / 16 * 16 : (rec + 15) / 16 * 16 + 16;
+// Row stride of one token's record in shared memory: rounded up to an odd
+// multiple of 16 bytes, so that 8 consecutive rows start in 8 different
+// 4-bank groups.
+__host__ __device__ constexpr int row_bytes(int bytes) {
+    return ((bytes + 15) / 16) % 2 == 1 ? (bytes + 15) / 16 * 16 : (bytes + 15) / 16 * 16 + 16;
 }
 
-// D: head_dim; G: group size; NT: n8 tiles of (head, hi/lo) columns; WPH:
-// warps per head along channels (2 for d = 256); TI: token-interleaved warps
-// per (head, channel slice).
-template <int D, int G, int NT, int WPH, int TI>
-struct MmaCfg {
-    static constexpr int kSliceCh = D / WPH;        // channels per warp
-    static constexpr int kKS = kSliceCh / 16;       // k-steps (words of 16 codes) per warp
-    static constexpr int kGW = kSliceCh / G > 0 ? kSliceCh / G : 1;  // groups per warp slice
-    static constexpr int kMT = kSliceCh / 16;       // P·V m-tiles per warp
-    static constexpr int kMTG = G / 16;             // m-tiles per group
-    static_assert(G <= kSliceCh, "a warp's channel slice must hold whole groups");
-    static_assert(G >= 32, "group size below 32 has no fast path");
-    static_assert(WPH * TI <= 2, "at most two warps share a KV head");
-};
-
-// Stage iterator over a CTA's chunk run [f, f1): stages of TT tokens that never
+// Stage iterator over a CTA's chunk run [f, f1): stages of tt tokens that never
 // cross a request boundary (the last stage of a segment may be partial).
 struct StageIter {
     int64_t f, f1, fe;
@@ -142,7 +129,6 @@ struct StageIter {
         tt = tokens;
         seg(P);
     }
-    __device__ bool seg_first() const { return t0 == t_seg; }
     __device__ bool seg_last() const { return t0 + tt >= t_end; }
     __device__ void next(const DecodeParams& P) {
         t0 += tt;
@@ -153,52 +139,58 @@ struct StageIter {
     }
 };
 
-// Shared-memory layout (byte offsets): [0, 64) full[8] and [64, 128) empty[8]
-// mbarriers, [128, 192) stage masks [16][... ]; the slot table [8][64] at 256;
-// then per warp the fp32 scale table of its current tile (SF bytes each), per
-// head the logit exchange / merge area, and the stage ring at stages_off.
-template <int D, int G, int NT, int WPH, int TI>
-struct MmaSmemCfg {
-    static constexpr int REC = (D / 2 + 8 * (D / G) + 15) / 16 * 16;   // record bytes
+// D: head_dim; G: group size; NT: n8 tiles of (head, hi/lo) columns; WPH:
+// warps per head along channels (2 for d = 256); TTOK: tokens per stage.
+template <int D, int G, int NT, int WPH, int TTOK>
+struct MmaCfg {
+    static constexpr int kSliceCh = D / WPH;        // channels per warp
+    static constexpr int kKS = kSliceCh / 16;       // k-steps (words of 16 codes) per warp
+    static constexpr int kGW = kSliceCh / G;        // groups per warp slice
+    static constexpr int kMT = kSliceCh / 16;       // P·V m-tiles per warp
+    static constexpr int kMTG = G / 16;             // m-tiles per group
+    static constexpr int kMQ = TTOK / 16;           // 16-token sub-tiles per stage
+    static constexpr int REC = (D / 2 + 8 * (D / G) + 15) / 16 * 16;   // record bytes per (slot, head)
     static constexpr int NG = D / G;
-    static constexpr int SFW = 4 * NG + 2;                              // words per scale row (≡ 2 mod 8)
-    static constexpr int SF = mma_detail::kTT * SFW * 4;
-    static constexpr int TT = mma_detail::kTT * TI;                     // tokens per stage
-    static constexpr int XCH = WPH == 2 ? 2 * 32 * 2 * NT * 4 : 0;     // logit exchange (2 buffers x 2 slices)
-    static constexpr int MRG = TI == 2 ? 32 * NT * MmaCfg<D, G, NT, WPH, TI>::kMT * 2 + 16 * NT : 0;
-    static constexpr int X_FLOATS = XCH + MRG + 4;
-    static constexpr int kBar = 0, kMask = 128, kSlots = 256;
-    static constexpr int kSF = kSlots + 8 * 64 * 4;                     // 2304
+    static constexpr int SFW = 4 * NG + 2;          // words per fp32 scale row (≡ 2 mod 8: conflict-free)
+    static constexpr int SF = TTOK * SFW * 4;       // bytes of a warp's scale table
+    static constexpr int NR = 2 * kMQ;              // token rows per thread per stage
+    static constexpr int XCH = WPH == 2 ? 2 * 2 * 32 * NT * NR : 0;   // logit exchange floats per head
+    static_assert(G <= kSliceCh, "a warp's channel slice must hold whole groups");
+    static_assert(G >= 32, "group size below 32 has no fast path");
+    static_assert(TTOK == 32 || TTOK == 64, "stages of 32 or 64 tokens");
 };
 
-template <int D, int G, int NT, int WPH, int TI>
-__global__ void __launch_bounds__(32 * (D == 256 ? 4 : 8) * WPH * TI, 1)
+// Shared-memory layout (byte offsets): [0, 64) full[8] and [64, 128) empty[8]
+// mbarriers; [128, 256) stage validity masks [16][2]; [256, 2304) slot-id
+// table [8][64]; then per warp its fp32 scale table, per head the logit
+// exchange area (d = 256), and the stage ring at stages_off.
+constexpr int kSmemMask = 128, kSmemSlots = 256, kSmemSF = 256 + 8 * 64 * 4;
+
+template <int D, int G, int NT, int WPH, int TTOK>
+__global__ void __launch_bounds__(256, 1)
 history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_log2) {
     using namespace mma_detail;
-    using C = MmaCfg<D, G, NT, WPH, TI>;
-    using SC = MmaSmemCfg<D, G, NT, WPH, TI>;
-    constexpr int KS = C::kKS, GW = C::kGW, MT = C::kMT, MTG = C::kMTG;
-    constexpr int REC = SC::REC, NG = SC::NG, SFW = SC::SFW, TT = SC::TT;
+    using C = MmaCfg<D, G, NT, WPH, TTOK>;
+    constexpr int KS = C::kKS, GW = C::kGW, MT = C::kMT, MTG = C::kMTG, MQ = C::kMQ;
+    constexpr int REC = C::REC, NG = C::NG, SFW = C::SFW, TT = TTOK, NR = C::NR;
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int Hkv = P.Hkv;
     const int nwarps = blockDim.x >> 5;
-    const int h = warp / (WPH * TI);            // KV head
-    const int sub = warp % (WPH * TI);
-    const int wsl = (WPH == 2) ? sub : 0;       // channel slice
-    const int ti = (TI == 2) ? sub : 0;         // which 32-token half of a stage this warp consumes
+    const int h = warp / WPH;                   // KV head
+    const int wsl = warp % WPH;                 // channel slice
     const int r = lane >> 2, j = lane & 3;
     const int g = P.g;
     const uint32_t NS = 1u << ns_log2;
     const int row = trow;                       // stage row stride of one token (all heads)
     const int tok_bytes = Hkv * REC;
-    const int cpt = tok_bytes / 16;             // 16-byte chunks per token
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + SC::kBar);
+    const int cpt = tok_bytes / 16;             // 16-byte chunks per token record
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + 8;
-    uint32_t* smask = reinterpret_cast<uint32_t*>(smem + SC::kMask);     // [16 stages][2 halves]
-    int32_t* slots = reinterpret_cast<int32_t*>(smem + SC::kSlots);      // [8][64]
-    float* sf = reinterpret_cast<float*>(smem + SC::kSF + warp * SC::SF);  // [32][SFW]
-    float* xb = reinterpret_cast<float*>(smem + x_off) + h * SC::X_FLOATS;
+    uint32_t* smask = reinterpret_cast<uint32_t*>(smem + kSmemMask);     // [16 stages][2 halves]
+    int32_t* slots = reinterpret_cast<int32_t*>(smem + kSmemSlots);      // [8][64]
+    float* sf = reinterpret_cast<float*>(smem + kSmemSF + warp * C::SF);  // [TT][SFW]
+    float* xb = reinterpret_cast<float*>(smem + x_off) + h * C::XCH;
     unsigned char* stages = smem + stages_off;
     const uint32_t stage_bytes = (uint32_t)TT * (uint32_t)row;
     const int bar_id = 1 + h;
@@ -209,16 +201,15 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     if (f0 >= f1) return;
 
     // ---- stage pipeline shared by the whole CTA ----
-    // Warp 0 writes the slot ids (and validity masks) of stage k + NS while the
-    // CTA is at stage k, before it releases stage k; every warp then copies a
-    // contiguous run of 16-byte chunks of whole token records of the stages it
-    // issues (stage k + NS - 1 at iteration k), so a copy instruction touches
-    // one or two records, and arrives on the stage's full barrier when its
-    // copies have landed.
+    // Warp 0 writes the slot ids (and validity masks) of stage k + NS once every
+    // thread has issued stage k; every warp copies a contiguous run of 16-byte
+    // chunks of whole token records of the stages it issues (stage k + NS - 1 at
+    // iteration k) and arrives on the stage's full barrier when they have landed.
     long long budget = 4000000000LL;            // cycles per pipeline wait (~2 s); 0 after a timeout
-    const int chunks = TT * cpt;
-    const int cpw = (chunks + nwarps - 1) / nwarps;
-    const int cbeg = warp * cpw, cend = min(chunks, cbeg + cpw);
+    const int tpw = (TT + nwarps - 1) / nwarps; // tokens whose records this warp copies per stage
+    const int tbeg = min(TT, warp * tpw), tend = min(TT, tbeg + tpw);
+    // chunk walk of the warp's run: lane starts at chunk `lane`, steps by 32 chunks
+    const int lt0 = lane / cpt, lp0 = lane % cpt, dq = 32 / cpt, dr = 32 % cpt;
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < NS; ++s) {
             mbar_init(&full[s], blockDim.x);
@@ -229,14 +220,15 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     // zero the stage ring once: rows of invalid tokens then always hold finite values
     for (uint32_t i = threadIdx.x; i < NS * stage_bytes / 16; i += blockDim.x)
         *reinterpret_cast<uint4*>(stages + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
-    // slot ids of stage `it` -> slots[si], mask -> smask[mi] (warp 0)
+    // slot ids of stage `it` -> slots[si], validity masks -> smask[mi] (warp 0)
     auto put_slots = [&](const StageIter& it, int v0, int v1, uint32_t si, uint32_t mi) {
         bool ok0 = false, ok1 = false;
         if (it.valid) {
-            ok0 = it.t0 + lane < it.t_end && v0 >= 0 && v0 < P.num_slots;
-            ok1 = TT > 32 && it.t0 + 32 + lane < it.t_end && v1 >= 0 && v1 < P.num_slots;
-            if ((it.t0 + lane < it.t_end && !ok0) || (TT > 32 && it.t0 + 32 + lane < it.t_end && !ok1))
-                set_status(P.status, OSCAR_DEV_BAD_SLOT);
+            const bool in0 = it.t0 + lane < it.t_end;
+            const bool in1 = TT > 32 && it.t0 + 32 + lane < it.t_end;
+            ok0 = in0 && v0 >= 0 && v0 < P.num_slots;
+            ok1 = in1 && v1 >= 0 && v1 < P.num_slots;
+            if ((in0 && !ok0) || (in1 && !ok1)) set_status(P.status, OSCAR_DEV_BAD_SLOT);
         }
         slots[si * 64 + lane] = ok0 ? v0 : -1;
         if (TT > 32) slots[si * 64 + 32 + lane] = ok1 ? v1 : -1;
@@ -252,40 +244,39 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         if (TT > 32 && it.t0 + 32 + lane < it.t_end) *v1 = pt[it.t0 + 32 + lane];
     };
     StageIter wit;                               // warp 0: stage whose slot ids come next
-    int nv0 = -1, nv1 = -1;                      // warp 0: prefetched slot ids of stage wk
-    uint32_t wk = 0;
+    int nv0 = -1, nv1 = -1;                      // warp 0: prefetched slot ids of stage wit
     if (warp == 0) {
         wit.init(P, f0, f1, TT);
-        for (; wk < NS; ++wk) {
+        for (uint32_t wk = 0; wk < NS; ++wk) {
             int v0, v1;
             get_slots(wit, &v0, &v1);
-            put_slots(wit, v0, v1, wk % NS, wk % (2 * NS));
+            put_slots(wit, v0, v1, wk, wk);
             if (wit.valid) wit.next(P);
         }
         get_slots(wit, &nv0, &nv1);              // stage NS
     }
     __syncthreads();
 
-    // copies of stage (iterator `it`, global index k) by this warp
-    auto issue = [&](const StageIter& it, uint32_t k) {
+    // copies of stage k by this warp
+    auto issue = [&](uint32_t k) {
         const uint32_t s = k & (NS - 1);
         if (k >= NS) mbar_wait_bounded(&empty[s], ((k >> ns_log2) - 1) & 1, P.status, budget);
         unsigned char* dst = stages + s * stage_bytes;
-        int c = cbeg + lane;
-        int t = c / cpt, piece = c - t * cpt;
-        for (; c < cend; c += 32) {
-            const int sl = slots[s * 64 + t];
-            if (sl >= 0)
-                cp_async16(dst + t * row + piece * 16, P.records + (int64_t)sl * tok_bytes + piece * 16);
-            piece += 32;
-            while (piece >= cpt) { piece -= cpt; ++t; }
+        const int32_t* srow = slots + s * 64;
+        int t = tbeg + lt0, pc = lp0;
+        while (t < tend) {
+            const int sl = srow[t];
+            if (sl >= 0) cp_async16(dst + t * row + pc * 16, P.records + (int64_t)sl * tok_bytes + pc * 16);
+            t += dq;
+            pc += dr;
+            if (pc >= cpt) { pc -= cpt; ++t; }
         }
         cp_async_mbar_arrive(&full[s]);
     };
     StageIter pit;                               // stage to issue next (NS - 1 ahead)
     pit.init(P, f0, f1, TT);
     uint32_t pk = 0;
-    for (; pk < NS - 1 && pit.valid; ++pk, pit.next(P)) issue(pit, pk);
+    for (; pk < NS - 1 && pit.valid; ++pk, pit.next(P)) issue(pk);
 
     // funnel shift for the K extraction: code position 2j+1 to bits 8-9 (2j to 6-7)
     const uint32_t rotK = (uint32_t)(4 * j - 6) & 31u;
@@ -337,7 +328,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         for (; !seg_done; ++k) {
             seg_done = it.seg_last();
             if (pit.valid) {                     // keep NS - 1 stages in flight
-                issue(pit, pk);
+                issue(pk);
                 ++pk;
                 pit.next(P);
             }
@@ -347,101 +338,116 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                 // Every thread has issued stage k (its full barrier completed), so the
                 // slot row of stage k is free: it receives the slot ids of stage k + NS,
                 // which the other warps read after waiting for stage k's release.
-                put_slots(wit, nv0, nv1, k & (NS - 1), (k + NS) % (2 * NS));
+                put_slots(wit, nv0, nv1, s, (k + NS) % (2 * NS));
                 if (wit.valid) wit.next(P);
                 get_slots(wit, &nv0, &nv1);
             }
-            const uint32_t vmask = smask[(k % (2 * NS)) * 2 + ti];
-            const unsigned char* tb = stages + s * stage_bytes + (ti * 32) * row + h * REC;
-            {   // this tile's (s, z) pairs as fp32: lane t converts token t's K and V pairs
-                const uint32_t* src = reinterpret_cast<const uint32_t*>(tb + lane * row + D / 2);
-                float* dst = sf + lane * SFW;
+            const uint32_t mrow = (k % (2 * NS)) * 2;
+            const uint64_t vmask = (uint64_t)smask[mrow] | ((uint64_t)smask[mrow + 1] << 32);
+            const unsigned char* tb = stages + s * stage_bytes + h * REC;
+            // this stage's (s, z) pairs as fp32: lane converts tokens lane (+ 32)
 #pragma unroll
-                for (int e = 0; e < 2 * NG; ++e) {
-                    const float2 v = h2f(src[e]);
-                    *reinterpret_cast<float2*>(dst + 2 * e) = v;
+            for (int tq = 0; tq < TT / 32; ++tq) {
+                const int t = lane + 32 * tq;
+                uint32_t w[2 * NG];
+                if constexpr (2 * NG % 4 == 0) {
+#pragma unroll
+                    for (int e = 0; e < 2 * NG; e += 4) {   // 16-byte loads, 8 rows per phase: no bank conflicts
+                        const uint4 q4 = *reinterpret_cast<const uint4*>(tb + t * row + D / 2 + 4 * e);
+                        w[e] = q4.x; w[e + 1] = q4.y; w[e + 2] = q4.z; w[e + 3] = q4.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 2 * NG; ++e) w[e] = *reinterpret_cast<const uint32_t*>(tb + t * row + D / 2 + 4 * e);
                 }
+                float* dst = sf + t * SFW;
+#pragma unroll
+                for (int e = 0; e < 2 * NG; ++e) *reinterpret_cast<float2*>(dst + 2 * e) = h2f(w[e]);
             }
             __syncwarp();
-            // ---------------- QK: two m16 tiles (tokens 0-15, 16-31) ----------------
-            float sc[2][GW][NT][4];
+            // ---------------- QK: MQ m16 tiles ----------------
+            float lg[NT][NR];        // logits (log2 units) of head 4nt + j, token 8i + r
+            {
+                float sc[MQ][GW][NT][4];
 #pragma unroll
-            for (int mq = 0; mq < 2; ++mq)
+                for (int mq = 0; mq < MQ; ++mq)
 #pragma unroll
-                for (int gi = 0; gi < GW; ++gi)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) sc[mq][gi][nt][e] = 0.f;
-#pragma unroll
-            for (int k4 = 0; k4 < KS; k4 += 4) {
-#pragma unroll
-                for (int mq = 0; mq < 2; ++mq) {
-                    const uint4 w0 = *reinterpret_cast<const uint4*>(
-                        reinterpret_cast<const uint32_t*>(tb + (16 * mq + r) * row) + wsl * KS + k4);
-                    const uint4 w1 = *reinterpret_cast<const uint4*>(
-                        reinterpret_cast<const uint32_t*>(tb + (16 * mq + r + 8) * row) + wsl * KS + k4);
-                    const uint32_t a0s[4] = {w0.x, w0.y, w0.z, w0.w};
-                    const uint32_t a1s[4] = {w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int kk = k4 + q;
-                        const int gi = (kk * 16) / G;
-                        const uint32_t y0 = rotr(a0s[q], rotK), y1 = rotr(a1s[q], rotK);
-                        const uint32_t x0 = code_q16(y0), x1 = code_q16(y1);   // channels 2j, 2j+8
-                        const uint32_t x2 = code_q4(y0), x3 = code_q4(y1);     // channels 2j+1, 2j+9
+                    for (int gi = 0; gi < GW; ++gi)
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
-                            mma16816(sc[mq][gi][nt], x0, x1, x2, x3, bq[nt][kk][0], bq[nt][kk][1]);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) sc[mq][gi][nt][e] = 0.f;
+#pragma unroll
+                for (int k4 = 0; k4 < KS; k4 += 4) {
+#pragma unroll
+                    for (int mq = 0; mq < MQ; ++mq) {
+                        const uint4 w0 = *reinterpret_cast<const uint4*>(
+                            reinterpret_cast<const uint32_t*>(tb + (16 * mq + r) * row) + wsl * KS + k4);
+                        const uint4 w1 = *reinterpret_cast<const uint4*>(
+                            reinterpret_cast<const uint32_t*>(tb + (16 * mq + r + 8) * row) + wsl * KS + k4);
+                        const uint32_t a0s[4] = {w0.x, w0.y, w0.z, w0.w};
+                        const uint32_t a1s[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int kk = k4 + q;
+                            const int gi = (kk * 16) / G;
+                            const uint32_t y0 = rotr(a0s[q], rotK), y1 = rotr(a1s[q], rotK);
+                            const uint32_t x0 = code_q16(y0), x1 = code_q16(y1);   // channels 2j, 2j+8
+                            const uint32_t x2 = code_q4(y0), x3 = code_q4(y1);     // channels 2j+1, 2j+9
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                mma16816(sc[mq][gi][nt], x0, x1, x2, x3, bq[nt][kk][0], bq[nt][kk][1]);
+                        }
                     }
                 }
-            }
-            // logits (log2 units) of head 4nt + j for tokens r, r+8, r+16, r+24 (index i = 2mq + half)
-            float lg[NT][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) lg[nt][i] = 0.f;
+                    for (int i = 0; i < NR; ++i) lg[nt][i] = 0.f;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = 8 * i + r;         // 16·mq + 8·half + r
-                const int mq = i >> 1, hf = i & 1;
+                for (int i = 0; i < NR; ++i) {
+                    const int t = 8 * i + r;     // 16·mq + 8·half + r
+                    const int mq = i >> 1, hf = i & 1;
 #pragma unroll
-                for (int gi = 0; gi < GW; ++gi) {
-                    const int gg = wsl * GW + gi;
-                    const float2 sz = *reinterpret_cast<const float2*>(sf + t * SFW + 2 * gg);
+                    for (int gi = 0; gi < GW; ++gi) {
+                        const int gg = wsl * GW + gi;
+                        const float2 sz = *reinterpret_cast<const float2*>(sf + t * SFW + 2 * gg);
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const float2 Q = qs[nt][gi];       // (Σ q̃, Σ q̃/α)
-                        lg[nt][i] += sz.x * (sc[mq][gi][nt][2 * hf] + sc[mq][gi][nt][2 * hf + 1] - Q.y) + sz.y * Q.x;
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const float2 Q = qs[nt][gi];       // (Σ q̃, Σ q̃/α)
+                            lg[nt][i] += sz.x * (sc[mq][gi][nt][2 * hf] + sc[mq][gi][nt][2 * hf + 1] - Q.y) + sz.y * Q.x;
+                        }
                     }
                 }
             }
             if (WPH == 2) {   // add the other channel slice's partial logits
-                float* my = xb + xpar * (2 * 32 * 4 * NT) + wsl * (32 * 4 * NT);
-                float* ot = xb + xpar * (2 * 32 * 4 * NT) + (1 - wsl) * (32 * 4 * NT);
+                float* my = xb + xpar * (2 * 32 * NT * NR) + wsl * (32 * NT * NR);
+                float* ot = xb + xpar * (2 * 32 * NT * NR) + (1 - wsl) * (32 * NT * NR);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) my[(nt * 4 + i) * 32 + lane] = lg[nt][i];
+                    for (int i = 0; i < NR; ++i) my[(nt * NR + i) * 32 + lane] = lg[nt][i];
                 named_bar(bar_id, 64);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) lg[nt][i] += ot[(nt * 4 + i) * 32 + lane];
+                    for (int i = 0; i < NR; ++i) lg[nt][i] += ot[(nt * NR + i) * 32 + lane];
                 xpar ^= 1;
             }
-            // ---------------- online softmax over the 32 tokens ----------------
-            float pr[NT][4];
+            // ---------------- online softmax over the stage ----------------
+            float pr[NT][NR];
             bool grew = false;
             float alpha[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const bool hv = (4 * nt + j) < g;
-                float x[4];
+                float x[NR];
+                float tm = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) x[i] = (hv && ((vmask >> (8 * i + r)) & 1u)) ? lg[nt][i] : -INFINITY;
-                float tm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+                for (int i = 0; i < NR; ++i) {
+                    x[i] = (hv && ((vmask >> (8 * i + r)) & 1u)) ? lg[nt][i] : -INFINITY;
+                    tm = fmaxf(tm, x[i]);
+                }
                 tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
                 tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
                 tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
@@ -451,7 +457,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                 m_run[nt] = mn;
                 float ps = 0.f;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < NR; ++i) {
                     pr[nt][i] = fast_exp2(x[i] - mn);              // masked tokens: 2^-inf = 0
                     ps += pr[nt][i];
                 }
@@ -469,11 +475,11 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                     for (int gi = 0; gi < GW; ++gi) { Wsum[nt][gi] *= ab; Zsum[nt][gi] *= ab; }
                 }
             }
-            // ---------------- P·V: two k16 steps (tokens 0-15, 16-31) ----------------
+            // ---------------- P·V: MQ k16 steps ----------------
             const int srcA = 8 * j + (r >> 1), srcB = srcA + 4;
             const bool lo_part = r & 1;
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
+            for (int ks = 0; ks < MQ; ++ks) {
                 // p of tokens 16ks + {2j, 2j+1, 2j+8, 2j+9} for head 4nt + r/2
                 float pb[NT][4];
 #pragma unroll
@@ -553,7 +559,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
             it.next(P);
         }
 
-        // ---------------- segment end: reduce, merge, write the partial ----------------
+        // ---------------- segment end: reduce and write the partial ----------------
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], 4);
@@ -569,77 +575,27 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         }
         // out[head 4nt+j][ch] = (acc_hi + acc_lo − W)/α_ch + Z, with α = 1/16 on the
         // rows r (even code positions) and 1/4 on the rows r+8; W, Z of head 4nt+j sit in lane 8j
-        float ov[NT][MT][2];
+        const int64_t slot = (int64_t)blockIdx.x + b;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
+            const int hh = 4 * nt + j;
+            const int hq = h * g + hh;
+            float* o = P.po + (slot * P.Hq + hq) * D;
+            if (r == 0 && wsl == 0 && hh < g) P.ml[slot * P.Hq + hq] = make_float2(m_run[nt], l_run[nt]);
 #pragma unroll
             for (int gi = 0; gi < GW; ++gi) {
                 const float Wh = __shfl_sync(0xffffffffu, Wsum[nt][gi], 8 * j);
                 const float Zh = __shfl_sync(0xffffffffu, Zsum[nt][gi], 8 * j);
+                const int gg = wsl * GW + gi;
 #pragma unroll
                 for (int mu = 0; mu < MTG; ++mu) {
                     const int mt = gi * MTG + mu;
-                    ov[nt][mt][0] = 16.f * (acc[nt][mt][0] + acc[nt][mt][1] - Wh) + Zh;
-                    ov[nt][mt][1] = 4.f * (acc[nt][mt][2] + acc[nt][mt][3] - Wh) + Zh;
-                }
-            }
-        }
-        if (TI == 2) {   // merge the two token-interleaved warps of this head
-            float* mb = xb;
-            if (ti == 1) {
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        mb[((nt * MT + mt) * 2 + 0) * 32 + lane] = ov[nt][mt][0];
-                        mb[((nt * MT + mt) * 2 + 1) * 32 + lane] = ov[nt][mt][1];
-                    }
-                    if (r == 0) {
-                        mb[NT * MT * 64 + nt * 8 + j] = m_run[nt];
-                        mb[NT * MT * 64 + nt * 8 + 4 + j] = l_run[nt];
-                    }
-                }
-            }
-            named_bar(bar_id, 64);
-            if (ti == 0) {
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const float m1 = mb[NT * MT * 64 + nt * 8 + j];
-                    const float l1 = mb[NT * MT * 64 + nt * 8 + 4 + j];
-                    const float M = fmaxf(m_run[nt], m1);
-                    const float a0 = fast_exp2(m_run[nt] - M);
-                    const float a1 = fast_exp2(m1 - M);
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        ov[nt][mt][0] = ov[nt][mt][0] * a0 + mb[((nt * MT + mt) * 2 + 0) * 32 + lane] * a1;
-                        ov[nt][mt][1] = ov[nt][mt][1] * a0 + mb[((nt * MT + mt) * 2 + 1) * 32 + lane] * a1;
-                    }
-                    l_run[nt] = l_run[nt] * a0 + l1 * a1;
-                    m_run[nt] = M;
-                }
-            }
-            named_bar(bar_id, 64);
-        }
-        if (ti == 0) {
-            const int64_t slot = (int64_t)blockIdx.x + b;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int hh = 4 * nt + j;
-                if (hh >= g) continue;
-                const int hq = h * g + hh;
-                if (r == 0 && wsl == 0) P.ml[slot * P.Hq + hq] = make_float2(m_run[nt], l_run[nt]);
-                float* o = P.po + (slot * P.Hq + hq) * D;
-#pragma unroll
-                for (int gi = 0; gi < GW; ++gi) {
-                    const int gg = wsl * GW + gi;
-#pragma unroll
-                    for (int mu = 0; mu < MTG; ++mu) {
-                        const int mt = gi * MTG + mu;
-                        int ch0;
-                        if constexpr (G == 32) ch0 = gg * G + 4 * r + 2 * mu;
-                        else ch0 = gg * G + r * (G / 8) + 8 * (mu / 4) + 2 * (mu % 4);
-                        o[ch0] = ov[nt][mt][0];
-                        o[ch0 + 1] = ov[nt][mt][1];
+                    int ch0;
+                    if constexpr (G == 32) ch0 = gg * G + 4 * r + 2 * mu;
+                    else ch0 = gg * G + r * (G / 8) + 8 * (mu / 4) + 2 * (mu % 4);
+                    if (hh < g) {
+                        o[ch0] = 16.f * (acc[nt][mt][0] + acc[nt][mt][1] - Wh) + Zh;
+                        o[ch0 + 1] = 4.f * (acc[nt][mt][2] + acc[nt][mt][3] - Wh) + Zh;
                     }
                 }
             }
@@ -647,18 +603,14 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     }
 }
 
-// Stage row stride of one token (all KV heads): rounded up to an odd multiple
-// of 16 bytes so that 8 consecutive rows start in 8 different 4-bank groups.
-static int token_row_bytes(int tok_bytes) { return row_bytes(tok_bytes); }
-
-// Shared-memory plan: (x_off, stages_off, ring depth log2, total bytes).
-template <int D, int G, int NT, int WPH, int TI>
+// Shared-memory plan: (x_off, stages_off, ring depth log2, total bytes); false if it does not fit.
+template <int D, int G, int NT, int WPH, int TTOK>
 static bool mma_smem_plan(int Hkv, int* x_off, int* stages_off, int* ns_log2, size_t* total) {
-    using SC = MmaSmemCfg<D, G, NT, WPH, TI>;
-    const int nwarps = Hkv * WPH * TI;
-    *x_off = SC::kSF + nwarps * SC::SF;
-    *stages_off = (*x_off + Hkv * SC::X_FLOATS * 4 + 127) / 128 * 128;
-    const size_t stage = (size_t)SC::TT * token_row_bytes(Hkv * SC::REC);
+    using C = MmaCfg<D, G, NT, WPH, TTOK>;
+    const int nwarps = Hkv * WPH;
+    *x_off = kSmemSF + nwarps * C::SF;
+    *stages_off = (*x_off + Hkv * C::XCH * 4 + 127) / 128 * 128;
+    const size_t stage = (size_t)TTOK * row_bytes(Hkv * C::REC);
     int lg = 3;                                  // 8 stages when they fit, else 4
     if (*stages_off + (stage << 3) > 224 * 1024) lg = 2;
     *ns_log2 = lg;
@@ -666,18 +618,17 @@ static bool mma_smem_plan(int Hkv, int* x_off, int* stages_off, int* ns_log2, si
     return *total <= 225 * 1024;
 }
 
-template <int D, int G, int NT, int WPH, int TI>
+template <int D, int G, int NT, int WPH, int TTOK>
 static int launch_mma(DecodeParams P, cudaStream_t st) {
-    const int threads = 32 * P.Hkv * WPH * TI;
+    const int threads = 32 * P.Hkv * WPH;
     int x_off, stages_off, ns_log2;
     size_t smem;
-    if (!mma_smem_plan<D, G, NT, WPH, TI>(P.Hkv, &x_off, &stages_off, &ns_log2, &smem)) return OSCAR_ERR_ARG;
-    auto kern = history_mma_kernel<D, G, NT, WPH, TI>;
+    if (!mma_smem_plan<D, G, NT, WPH, TTOK>(P.Hkv, &x_off, &stages_off, &ns_log2, &smem)) return OSCAR_ERR_ARG;
+    auto kern = history_mma_kernel<D, G, NT, WPH, TTOK>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return check_cuda("cudaFuncSetAttribute(history_mma_kernel)");
     const int grid = std::min(P.n_ctas, sm_count());
-    P.n_ctas = grid;
-    const int trow = token_row_bytes(P.Hkv * MmaSmemCfg<D, G, NT, WPH, TI>::REC);
+    const int trow = row_bytes(P.Hkv * MmaCfg<D, G, NT, WPH, TTOK>::REC);
     kern<<<grid, threads, smem, st>>>(P, x_off, stages_off, trow, ns_log2);
     return check_cuda("history_mma_kernel launch");
 }
@@ -697,14 +648,14 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
         rc = fn(P, st);
         *launched = true;
     };
-#define OSCAR_MMA(D_, G_, NT_, WPH_, TI_) go(mma_smem_plan<D_, G_, NT_, WPH_, TI_>, launch_mma<D_, G_, NT_, WPH_, TI_>)
+#define OSCAR_MMA(D_, G_, NT_, WPH_, TT_) go(mma_smem_plan<D_, G_, NT_, WPH_, TT_>, launch_mma<D_, G_, NT_, WPH_, TT_>)
     if (head_dim == 128) {
-        if (P.G == 64) { if (nt == 1) OSCAR_MMA(128, 64, 1, 1, 2); else OSCAR_MMA(128, 64, 2, 1, 1); }
-        else if (P.G == 128) { if (nt == 1) OSCAR_MMA(128, 128, 1, 1, 2); else OSCAR_MMA(128, 128, 2, 1, 1); }
-        else if (P.G == 32) { if (nt == 1) OSCAR_MMA(128, 32, 1, 1, 2); else OSCAR_MMA(128, 32, 2, 1, 1); }
+        if (P.G == 64) { if (nt == 1) OSCAR_MMA(128, 64, 1, 1, 64); else OSCAR_MMA(128, 64, 2, 1, 32); }
+        else if (P.G == 128) { if (nt == 1) OSCAR_MMA(128, 128, 1, 1, 64); else OSCAR_MMA(128, 128, 2, 1, 32); }
+        else if (P.G == 32) { if (nt == 1) OSCAR_MMA(128, 32, 1, 1, 64); else OSCAR_MMA(128, 32, 2, 1, 32); }
     } else if (head_dim == 256) {
-        if (P.G == 128) { if (nt == 1) OSCAR_MMA(256, 128, 1, 2, 1); else OSCAR_MMA(256, 128, 2, 2, 1); }
-        else if (P.G == 64) { if (nt == 1) OSCAR_MMA(256, 64, 1, 2, 1); else OSCAR_MMA(256, 64, 2, 2, 1); }
+        if (P.G == 128) { if (nt == 1) OSCAR_MMA(256, 128, 1, 2, 64); else OSCAR_MMA(256, 128, 2, 2, 32); }
+        else if (P.G == 64) { if (nt == 1) OSCAR_MMA(256, 64, 1, 2, 64); else OSCAR_MMA(256, 64, 2, 2, 32); }
     }
 #undef OSCAR_MMA
     if (*launched) P.n_ctas = std::min(P.n_ctas, sm_count());

@@ -59,13 +59,27 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
 }
 
+#ifndef OSCAR_MBAR_SUSPEND_NS
+#define OSCAR_MBAR_SUSPEND_NS 0   // 0: the hardware's default time slice per try_wait
+#endif
+
+// Tests the phase with the given parity (a waiting thread may be suspended
+// for a while before the test returns false).
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
+#if OSCAR_MBAR_SUSPEND_NS > 0
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity), "r"((unsigned)OSCAR_MBAR_SUSPEND_NS) : "memory");
+#else
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+#endif
     return ok != 0;
 }
 
@@ -81,7 +95,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     const long long t0 = clock64();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && clock64() - t0 > budget) break;
+        if ((i & 15u) == 0 && clock64() - t0 > budget) break;
     }
     set_status(status, 8 /* OSCAR_DEV_TIMEOUT */);
     budget = 0;
