@@ -229,8 +229,8 @@ def decode_step(w, i, kernel):
 
 
 def launches_per_step():
-    # quantize + window copy (append) ; prep + history + combine (decode)
-    return 5
+    # quantize + window copy (append) ; prep + window + history + combine (decode)
+    return 6
 
 
 def algorithmic_history_bytes(rec_bytes_per_token, L):
@@ -365,7 +365,12 @@ def main():
     traffic = None
     try:
         prof = json.load(open(os.path.join(ROOT, "profiles", "history_traffic.json")))
-        if prof.get("kernel") == "history_mma_kernel" and args.decode_kernel == "auto":
+        import hashlib
+        src = os.path.join(ROOT, "rotated_int2_kv_gb300", "csrc", "oscar_decode_mma.cu")
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        # counters taken on another version of the kernel do not describe this one
+        if (prof.get("kernel") == "history_mma_kernel" and prof.get("kernel_source_sha256") == sha
+                and args.decode_kernel == "auto" and args.workload == "qwen8b-100k"):
             traffic = prof.get("bytes_per_launch_full")
     except (OSError, ValueError):
         pass
