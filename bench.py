@@ -162,6 +162,14 @@ def sum_over_ranks(x, ws):
     return float(t.item())
 
 
+def job_throughput(units, ms, ws):
+    """Whole-job rate: the units all ranks processed over the slowest rank's time.
+
+    Returns (units per second, max-over-ranks milliseconds)."""
+    ms_max = max_over_ranks(ms, ws)
+    return sum_over_ranks(units, ws) / (ms_max / 1e3), ms_max
+
+
 # --------------------------------------------------------------------------
 # workload
 # --------------------------------------------------------------------------
@@ -344,7 +352,6 @@ def main():
     hist_ms, hist_n = ops.profile_read(0)
     ops.profile_enable(False)
     clk = clocks.stop()
-    ms = max_over_ranks(ms, ws)
 
     rec_tok, _ = ops.cache_bytes_per_token(w["cfg"])
     tokens = 0
@@ -353,8 +360,7 @@ def main():
         L = L_BASE + (args.warmup + i) % CYCLE + 1
         tokens += B * L
         hist_bytes += B * algorithmic_history_bytes(rec_tok, L)
-    tokens_all = sum_over_ranks(tokens, ws)
-    value = tokens_all / (ms / 1e3)
+    value, ms = job_throughput(tokens, ms, ws)
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -441,10 +447,9 @@ def e2e_measure(w, args, ws):
         tokens += B * (L_BASE + s + 1)
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1), ws)
-    tokens = sum_over_ranks(tokens, ws)
+    value, _ = job_throughput(tokens, e0.elapsed_time(e1), ws)
     h2d = dk.numel() * 2 + dv.numel() * 2 + dq.numel() * 2
-    return {"value": tokens / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": hout.numel() * 4, "steps": n}
 
 
