@@ -462,9 +462,6 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams P) {
     extern __shared__ __align__(16) float s_c[];
     const int hk = blockIdx.x, b = blockIdx.y;
     const int g = P.g;
-    float* srot = s_c;                             // [g][D] merged rotated sum
-    float* spl = srot + g * D;                     // [g][D] merged window sum
-    float* sst = spl + g * D;                      // [g][4]: m_p, l_p, m_r, l_r
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = P.len[b];
     float* outp = P.out + ((int64_t)b * P.Hq + hk * g) * D;
@@ -477,24 +474,44 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams P) {
     const int64_t i_lo = c1 > c0 ? chunk_owner(c0, N, P.n_ctas) : 0;
     const int64_t i_hi = c1 > c0 ? chunk_owner(c1 - 1, N, P.n_ctas) : -1;
     const int nwt = P.n_win_tiles;
+    const int psh = P.par == 2 ? 1 : 0;            // partial slots per (CTA, request) = 1 << psh
+    const int nsl = (int)(i_hi - i_lo + 1) << psh;  // this request's partial slots: (i_lo << psh) + b·par + u
+    const int64_t sl0 = (i_lo << psh) + ((int64_t)b << psh);
+    float* srot = s_c;                             // [g][D] merged rotated sum
+    float* spl = srot + g * D;                     // [g][D] merged window sum
+    float* sst = spl + g * D;                      // [g][4]: m_p, l_p, m_r, l_r
+    float* sww = sst + 4 * g;                      // [g][nwt] window tile weights
+    float* swr = sww + g * nwt;                    // [g][P.n_ctas·par + 2] history partial weights
+    const int swr_stride = (P.n_ctas << psh) + 2;
     for (int j = warp; j < g; j += kCombThreads / 32) {
         const int hq = hk * g + j;
         const float2* wml = P.wml + ((int64_t)b * P.Hq + hq) * nwt;
         float Mp = -INFINITY, Mr = -INFINITY;
-        for (int t = lane; t < nwt; t += 32) Mp = fmaxf(Mp, wml[t].x);
-        for (int64_t i = i_lo + lane; i <= i_hi; i += 32)
-            if (cta_has_work(i, N, P.n_ctas)) Mr = fmaxf(Mr, P.ml[(i + b) * P.Hq + hq].x);
+        for (int t = lane; t < nwt; t += 32)
+            if (wml[t].y > 0.f) Mp = fmaxf(Mp, wml[t].x);
+        // a partial counts when its CTA had a chunk run and its l is positive
+        for (int u = lane; u < nsl; u += 32) {
+            const float2 ml = P.ml[(sl0 + u) * P.Hq + hq];
+            const bool ok = cta_has_work(i_lo + (u >> psh), N, P.n_ctas) && ml.y > 0.f;
+            swr[j * swr_stride + u] = ok ? ml.x : -INFINITY;
+            if (ok) Mr = fmaxf(Mr, ml.x);
+        }
         for (int off = 16; off; off >>= 1) {
             Mp = fmaxf(Mp, __shfl_xor_sync(0xffffffffu, Mp, off));
             Mr = fmaxf(Mr, __shfl_xor_sync(0xffffffffu, Mr, off));
         }
         float lp = 0.f, lr = 0.f;
-        for (int t = lane; t < nwt; t += 32)
-            if (wml[t].y > 0.f) lp += exp2f(wml[t].x - Mp) * wml[t].y;
-        for (int64_t i = i_lo + lane; i <= i_hi; i += 32) {
-            if (!cta_has_work(i, N, P.n_ctas)) continue;
-            const float2 ml = P.ml[(i + b) * P.Hq + hq];
-            if (ml.y > 0.f) lr += exp2f(ml.x - Mr) * ml.y;
+        for (int t = lane; t < nwt; t += 32) {
+            const float2 ml = wml[t];
+            const float w = ml.y > 0.f ? exp2f(ml.x - Mp) : 0.f;
+            sww[j * nwt + t] = w;
+            lp += w * ml.y;
+        }
+        for (int u = lane; u < nsl; u += 32) {
+            const float m = swr[j * swr_stride + u];
+            const float w = m > -INFINITY ? exp2f(m - Mr) : 0.f;
+            swr[j * swr_stride + u] = w;
+            if (w > 0.f) lr += w * P.ml[(sl0 + u) * P.Hq + hq].y;
         }
         for (int off = 16; off; off >>= 1) {
             lp += __shfl_xor_sync(0xffffffffu, lp, off);
@@ -511,20 +528,17 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams P) {
     for (int i = tid; i < g * D; i += kCombThreads) {
         const int j = i / D, c = i % D;
         const int hq = hk * g + j;
-        const float Mp = sst[j * 4 + 0], Mr = sst[j * 4 + 2];
         float ap = 0.f;
         const int64_t wb = ((int64_t)b * P.Hq + hq) * nwt;
         for (int t = 0; t < nwt; ++t) {
-            const float2 ml = P.wml[wb + t];
-            if (ml.y > 0.f) ap = fmaf(exp2f(ml.x - Mp), P.wo[(wb + t) * D + c], ap);
+            const float w = sww[j * nwt + t];
+            if (w > 0.f) ap = fmaf(w, P.wo[(wb + t) * D + c], ap);
         }
         spl[i] = ap;
         float ar = 0.f;
-        for (int64_t ci = i_lo; ci <= i_hi; ++ci) {
-            if (!cta_has_work(ci, N, P.n_ctas)) continue;
-            const int64_t sl = ci + b;
-            const float2 ml = P.ml[sl * P.Hq + hq];
-            if (ml.y > 0.f) ar = fmaf(exp2f(ml.x - Mr), P.po[(sl * P.Hq + hq) * D + c], ar);
+        for (int u = 0; u < nsl; ++u) {
+            const float w = swr[j * swr_stride + u];
+            if (w > 0.f) ar = fmaf(w, P.po[((sl0 + u) * P.Hq + hq) * D + c], ar);
         }
         srot[i] = ar;
     }
@@ -634,7 +648,8 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
         if (rc) return rc;
     }
     prof_end(prof, st);
-    const size_t csmem = ((size_t)P.g * D * 2 + (size_t)P.g * 4) * 4;
+    const size_t csmem = ((size_t)P.g * D * 2 + (size_t)P.g * 4 + (size_t)P.g * P.n_win_tiles +
+                          (size_t)P.g * ((size_t)P.n_ctas * P.par + 2)) * 4;
     if (cudaFuncSetAttribute(combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem) != cudaSuccess)
         return check_cuda("cudaFuncSetAttribute(combine_kernel)");
     combine_kernel<D><<<dim3(P.Hkv, P.batch), kCombThreads, csmem, st>>>(P);
@@ -685,6 +700,7 @@ static int decode_impl(const oscar_config* cfg, const oscar_layer_cache* cache, 
     P.rec_bytes = record_layout(cfg->head_dim, cfg->group_size).bytes;
     P.chunk = plan.chunk;
     P.n_ctas = plan.max_ctas;          // set by the history launcher
+    P.par = 1;                         // set by the tensor-core history launcher
     P.n_frag_tiles = plan.n_frag_tiles;
     P.n_win_tiles = plan.n_win_tiles;
     P.qscale = (float)(1.4426950408889634 / std::sqrt((double)cfg->head_dim));

@@ -13,14 +13,17 @@ namespace oscar {
 // The history of each request is cut into chunks of `chunk` tokens.  A
 // persistent history grid of at most `max_ctas` CTAs splits the flattened
 // chunk list into contiguous runs (CTA i owns [i·N/n, (i+1)·N/n)), and each
-// CTA writes one (m, l, o) partial per request it touches, at partial slot
-// i + b.  The slot is unique: if CTAs i < i' both touch requests b and b' with
-// i + b = i' + b', then b' < b, but runs are ordered so b' >= b.  So
-// max_ctas + batch slots suffice, whatever the lengths.
+// CTA writes one (m, l, o) partial per request it touches and per stage parity
+// π < par (par = 1 or 2 warp sets consuming alternate stages), at partial slot
+// (i + b)·par + π.  i + b is unique: if CTAs i < i' both touch requests b and b'
+// with i + b = i' + b', then b' < b, but runs are ordered so b' >= b.  The
+// CUDA-core grid has up to max_ctas = 4·n_sm CTAs and par = 1; the tensor-core
+// grid has at most n_sm CTAs and par <= 2.  So max(max_ctas + batch,
+// 2·(n_sm + batch)) slots suffice, whatever the lengths.
 struct DecodePlan {
     int chunk;        // tokens per chunk (multiple of 32)
     int max_ctas;     // upper bound of the history grid
-    int part_slots;   // max_ctas + batch
+    int part_slots;   // max(max_ctas + batch, 2 * (n_sm + batch))
     int n_frag_tiles; // n-tiles of 8 columns for the fragment-packed queries
     int n_win_tiles;  // 64-token tiles of the BF16 sink + recent windows
     // workspace offsets (bytes, 256-aligned)
@@ -42,7 +45,7 @@ inline DecodePlan make_plan(const oscar_config* cfg, int batch, int max_seq_len,
     if (c > 1024) c = 1024;
     p.chunk = (int)c;
     p.max_ctas = std::max(1, n_sm) * 4;
-    p.part_slots = p.max_ctas + batch;
+    p.part_slots = std::max(p.max_ctas + batch, 2 * (std::max(1, n_sm) + batch));
     p.n_frag_tiles = (2 * g + 7) / 8;
     p.n_win_tiles = (cfg->sink + cfg->recent + 63) / 64;
     size_t off = 0;
@@ -80,6 +83,7 @@ struct DecodeParams {
     int Hq, Hkv, g, S, W, G, ng, rec_bytes;
     int chunk, n_frag_tiles, n_win_tiles;
     int n_ctas;        // history grid actually launched (<= plan.max_ctas)
+    int par;           // partial slots per (CTA, request): stage parities of the history kernel
     float qscale;      // log2(e) / sqrt(d)
     // workspace
     int32_t* len;      // effective L per request (0 when invalid)

@@ -151,10 +151,16 @@ struct MmaCfg {
     static constexpr int kMQ = TTOK / 16;           // 16-token sub-tiles per stage
     static constexpr int REC = (D / 2 + 8 * (D / G) + 15) / 16 * 16;   // record bytes per (slot, head)
     static constexpr int NG = D / G;
-    static constexpr int SFW = 4 * NG + 2;          // words per fp32 scale row (≡ 2 mod 8: conflict-free)
-    static constexpr int SF = TTOK * SFW * 4;       // bytes of a warp's scale table
     static constexpr int NR = 2 * kMQ;              // token rows per thread per stage
     static constexpr int XCH = WPH == 2 ? 2 * 2 * 32 * NT * NR : 0;   // logit exchange floats per head
+    // P·V operand table of a warp: w = p·s per (column head, token, group) as fp16,
+    // one table of hi parts and one of lo parts.  A row (head) holds TT tokens of
+    // kGW halves each; the row stride (words, ≡ 8 mod 32) and the lo-table offset
+    // (≡ 16 mod 32) make both the owner stores and the fragment loads conflict-free.
+    static constexpr int kWT = TTOK * kGW / 2;                       // words per table row
+    static constexpr int kWS = kWT + ((8 - kWT % 32) + 32) % 32;      // row stride in words
+    static constexpr int kWLO = NT * 4 * kWS + 16;                    // lo table offset in words
+    static constexpr int TBL = (kWLO + NT * 4 * kWS) * 4;             // bytes per warp
     static_assert(G <= kSliceCh, "a warp's channel slice must hold whole groups");
     static_assert(G >= 32, "group size below 32 has no fast path");
     static_assert(TTOK == 32 || TTOK == 64, "stages of 32 or 64 tokens");
@@ -162,23 +168,25 @@ struct MmaCfg {
 
 // Shared-memory layout (byte offsets): [0, 64) full[8] and [64, 128) empty[8]
 // mbarriers; [128, 256) stage validity masks [16][2]; [256, 2304) slot-id
-// table [8][64]; then per warp its fp32 scale table, per head the logit
-// exchange area (d = 256), and the stage ring at stages_off.
-constexpr int kSmemMask = 128, kSmemSlots = 256, kSmemSF = 256 + 8 * 64 * 4;
+// table [8][64]; then per warp its P·V operand table, per (head, parity) the
+// logit exchange area (d = 256), and the stage ring at stages_off.
+constexpr int kSmemMask = 128, kSmemSlots = 256, kSmemTab = 256 + 8 * 64 * 4;
 
-template <int D, int G, int NT, int WPH, int TTOK>
-__global__ void __launch_bounds__(256, 1)
+template <int D, int G, int NT, int WPH, int TTOK, int PAR>
+__global__ void __launch_bounds__(256 * PAR, 1)
 history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_log2) {
     using namespace mma_detail;
     using C = MmaCfg<D, G, NT, WPH, TTOK>;
     constexpr int KS = C::kKS, GW = C::kGW, MT = C::kMT, MTG = C::kMTG, MQ = C::kMQ;
-    constexpr int REC = C::REC, NG = C::NG, SFW = C::SFW, TT = TTOK, NR = C::NR;
+    constexpr int REC = C::REC, NG = C::NG, TT = TTOK, NR = C::NR;
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int Hkv = P.Hkv;
     const int nwarps = blockDim.x >> 5;
-    const int h = warp / WPH;                   // KV head
-    const int wsl = warp % WPH;                 // channel slice
+    const int pi = warp % PAR;                  // parity of the stages this warp consumes
+    const int hw = warp / PAR;
+    const int h = hw / WPH;                     // KV head
+    const int wsl = hw % WPH;                   // channel slice
     const int r = lane >> 2, j = lane & 3;
     const int g = P.g;
     const uint32_t NS = 1u << ns_log2;
@@ -189,11 +197,11 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     uint64_t* empty = full + 8;
     uint32_t* smask = reinterpret_cast<uint32_t*>(smem + kSmemMask);     // [16 stages][2 halves]
     int32_t* slots = reinterpret_cast<int32_t*>(smem + kSmemSlots);      // [8][64]
-    float* sf = reinterpret_cast<float*>(smem + kSmemSF + warp * C::SF);  // [TT][SFW]
-    float* xb = reinterpret_cast<float*>(smem + x_off) + h * C::XCH;
+    uint32_t* wtab = reinterpret_cast<uint32_t*>(smem + kSmemTab + warp * C::TBL);
+    float* xb = reinterpret_cast<float*>(smem + x_off) + (h * PAR + pi) * C::XCH;
     unsigned char* stages = smem + stages_off;
     const uint32_t stage_bytes = (uint32_t)TT * (uint32_t)row;
-    const int bar_id = 1 + h;
+    const int bar_id = 1 + h * PAR + pi;
 
     const int64_t N = P.cprefix[P.batch];
     const int64_t f0 = (int64_t)blockIdx.x * N / gridDim.x;
@@ -213,7 +221,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < NS; ++s) {
             mbar_init(&full[s], blockDim.x);
-            mbar_init(&empty[s], nwarps);
+            mbar_init(&empty[s], nwarps / PAR);
         }
         fence_mbar_init();
     }
@@ -243,17 +251,23 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         if (it.t0 + lane < it.t_end) *v0 = pt[it.t0 + lane];
         if (TT > 32 && it.t0 + 32 + lane < it.t_end) *v1 = pt[it.t0 + 32 + lane];
     };
-    StageIter wit;                               // warp 0: stage whose slot ids come next
-    int nv0 = -1, nv1 = -1;                      // warp 0: prefetched slot ids of stage wit
-    if (warp == 0) {
+    // Warp 0 writes the slot ids of stages 0 .. NS-1; afterwards the leader warp of
+    // each stage parity (hw == 0) writes those of stage k + NS while consuming stage k.
+    StageIter wit;                               // leader: stage whose slot ids come next
+    int nv0 = -1, nv1 = -1;                      // leader: prefetched slot ids of stage wit
+    if (hw == 0) {
         wit.init(P, f0, f1, TT);
         for (uint32_t wk = 0; wk < NS; ++wk) {
-            int v0, v1;
-            get_slots(wit, &v0, &v1);
-            put_slots(wit, v0, v1, wk, wk);
+            if (warp == 0) {
+                int v0, v1;
+                get_slots(wit, &v0, &v1);
+                put_slots(wit, v0, v1, wk, wk);
+            }
             if (wit.valid) wit.next(P);
         }
-        get_slots(wit, &nv0, &nv1);              // stage NS
+        for (int q = 0; q < pi; ++q)
+            if (wit.valid) wit.next(P);
+        get_slots(wit, &nv0, &nv1);              // stage NS + pi
     }
     __syncthreads();
 
@@ -273,10 +287,13 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         }
         cp_async_mbar_arrive(&full[s]);
     };
-    StageIter pit;                               // stage to issue next (NS - 1 ahead)
+    // Stage k + NS - PAR is issued at iteration k: it reuses the slot of stage
+    // k - PAR, which the warps of this iteration's parity released one round ago,
+    // so issuing never waits for the stage the other parity is consuming.
+    StageIter pit;                               // stage to issue next (NS - PAR ahead)
     pit.init(P, f0, f1, TT);
     uint32_t pk = 0;
-    for (; pk < NS - 1 && pit.valid; ++pk, pit.next(P)) issue(pk);
+    for (; pk < NS - PAR && pit.valid; ++pk, pit.next(P)) issue(pk);
 
     // funnel shift for the K extraction: code position 2j+1 to bits 8-9 (2j to 6-7)
     const uint32_t rotK = (uint32_t)(4 * j - 6) & 31u;
@@ -311,7 +328,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         }
         float m_run[NT], l_run[NT];
         float acc[NT][MT][4];
-        float Wsum[NT][GW], Zsum[NT][GW];   // for head 4nt + r/2 (B-fragment layout)
+        float Wsum[NT][GW], Zsum[NT][GW];   // Σ w and Σ p·z for head 4nt + j over this thread's tokens
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             m_run[nt] = -1e30f;     // finite: 2^(m_run - m) never sees -inf - -inf
@@ -327,44 +344,29 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         bool seg_done = false;
         for (; !seg_done; ++k) {
             seg_done = it.seg_last();
-            if (pit.valid) {                     // keep NS - 1 stages in flight
+            if (pit.valid) {                     // keep NS - PAR stages in flight
                 issue(pk);
                 ++pk;
                 pit.next(P);
             }
+            if ((k & (PAR - 1)) != (uint32_t)pi) {   // a stage of the other parity
+                it.next(P);
+                continue;
+            }
             const uint32_t s = k & (NS - 1);
             mbar_wait_bounded(&full[s], (k >> ns_log2) & 1, P.status, budget);
-            if (warp == 0) {
+            if (hw == 0) {
                 // Every thread has issued stage k (its full barrier completed), so the
-                // slot row of stage k is free: it receives the slot ids of stage k + NS,
-                // which the other warps read after waiting for stage k's release.
+                // slot row of stage k is free: it receives the slot ids of stage k + NS
+                // (same parity), which every warp reads after waiting for stage k's release.
                 put_slots(wit, nv0, nv1, s, (k + NS) % (2 * NS));
-                if (wit.valid) wit.next(P);
+                for (int q = 0; q < PAR; ++q)
+                    if (wit.valid) wit.next(P);
                 get_slots(wit, &nv0, &nv1);
             }
             const uint32_t mrow = (k % (2 * NS)) * 2;
             const uint64_t vmask = (uint64_t)smask[mrow] | ((uint64_t)smask[mrow + 1] << 32);
             const unsigned char* tb = stages + s * stage_bytes + h * REC;
-            // this stage's (s, z) pairs as fp32: lane converts tokens lane (+ 32)
-#pragma unroll
-            for (int tq = 0; tq < TT / 32; ++tq) {
-                const int t = lane + 32 * tq;
-                uint32_t w[2 * NG];
-                if constexpr (2 * NG % 4 == 0) {
-#pragma unroll
-                    for (int e = 0; e < 2 * NG; e += 4) {   // 16-byte loads, 8 rows per phase: no bank conflicts
-                        const uint4 q4 = *reinterpret_cast<const uint4*>(tb + t * row + D / 2 + 4 * e);
-                        w[e] = q4.x; w[e + 1] = q4.y; w[e + 2] = q4.z; w[e + 3] = q4.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 2 * NG; ++e) w[e] = *reinterpret_cast<const uint32_t*>(tb + t * row + D / 2 + 4 * e);
-                }
-                float* dst = sf + t * SFW;
-#pragma unroll
-                for (int e = 0; e < 2 * NG; ++e) *reinterpret_cast<float2*>(dst + 2 * e) = h2f(w[e]);
-            }
-            __syncwarp();
             // ---------------- QK: MQ m16 tiles ----------------
             float lg[NT][NR];        // logits (log2 units) of head 4nt + j, token 8i + r
             {
@@ -411,7 +413,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
 #pragma unroll
                     for (int gi = 0; gi < GW; ++gi) {
                         const int gg = wsl * GW + gi;
-                        const float2 sz = *reinterpret_cast<const float2*>(sf + t * SFW + 2 * gg);
+                        const float2 sz = h2f(*reinterpret_cast<const uint32_t*>(tb + t * row + D / 2 + 4 * gg));
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             const float2 Q = qs[nt][gi];       // (Σ q̃, Σ q̃/α)
@@ -435,79 +437,115 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                 xpar ^= 1;
             }
             // ---------------- online softmax over the stage ----------------
-            float pr[NT][NR];
-            bool grew = false;
-            float alpha[NT];
+            // The running max moves only when a logit exceeds it (rare after the first
+            // stages), so the common path is one vote and no max reduction.
+            float x[NT][NR];
+            bool over = false;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const bool hv = (4 * nt + j) < g;
-                float x[NR];
-                float tm = -INFINITY;
+                const uint64_t need = TT == 64 ? ~0ull : 0xffffffffull;
+                const uint64_t vm = (4 * nt + j) < g ? vmask : 0ull;
 #pragma unroll
-                for (int i = 0; i < NR; ++i) {
-                    x[i] = (hv && ((vmask >> (8 * i + r)) & 1u)) ? lg[nt][i] : -INFINITY;
-                    tm = fmaxf(tm, x[i]);
-                }
-                tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
-                tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
-                tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
-                const float mn = fmaxf(m_run[nt], tm);
-                grew |= mn > m_run[nt];
-                alpha[nt] = fast_exp2(m_run[nt] - mn);
-                m_run[nt] = mn;
-                float ps = 0.f;
+                for (int i = 0; i < NR; ++i) x[nt][i] = lg[nt][i];
+                if (vm != need) {
 #pragma unroll
-                for (int i = 0; i < NR; ++i) {
-                    pr[nt][i] = fast_exp2(x[i] - mn);              // masked tokens: 2^-inf = 0
-                    ps += pr[nt][i];
+                    for (int i = 0; i < NR; ++i)
+                        if (!((vm >> (8 * i + r)) & 1u)) x[nt][i] = -INFINITY;
                 }
-                l_run[nt] = l_run[nt] * alpha[nt] + ps;
+#pragma unroll
+                for (int i = 0; i < NR; ++i) over |= x[nt][i] > m_run[nt];
             }
-            if (__any_sync(0xffffffffu, grew)) {
+            if (__any_sync(0xffffffffu, over)) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const float ab = __shfl_sync(0xffffffffu, alpha[nt], r >> 1);  // head 4nt + r/2
+                    float tm = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < NR; ++i) tm = fmaxf(tm, x[nt][i]);
+                    tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
+                    tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
+                    tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+                    const float mn = fmaxf(m_run[nt], tm);
+                    const float alpha = fast_exp2(m_run[nt] - mn);
+                    m_run[nt] = mn;
+                    l_run[nt] *= alpha;
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) acc[nt][mt][e] *= alpha[nt];
+                        for (int e = 0; e < 4; ++e) acc[nt][mt][e] *= alpha;
 #pragma unroll
-                    for (int gi = 0; gi < GW; ++gi) { Wsum[nt][gi] *= ab; Zsum[nt][gi] *= ab; }
+                    for (int gi = 0; gi < GW; ++gi) { Wsum[nt][gi] *= alpha; Zsum[nt][gi] *= alpha; }
                 }
             }
+            // p, w = p·s of the V groups, and the fp16 hi / lo parts of w into the
+            // operand table (row = head 4nt + j, this thread's tokens 8i + r)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                uint32_t* th = wtab + (4 * nt + j) * C::kWS;
+#pragma unroll
+                for (int i = 0; i < NR; ++i) {
+                    const int t = 8 * i + r;
+                    const float pv = fast_exp2(x[nt][i] - m_run[nt]);   // masked tokens: 2^-inf = 0
+                    l_run[nt] += pv;
+                    float w[GW];
+#pragma unroll
+                    for (int gi = 0; gi < GW; ++gi) {
+                        // rows of invalid tokens hold finite stale data and get p = 0
+                        const float2 sz = h2f(*reinterpret_cast<const uint32_t*>(
+                            tb + t * row + D / 2 + 4 * (NG + wsl * GW + gi)));
+                        w[gi] = pv * sz.x;
+                        Wsum[nt][gi] += w[gi];
+                        Zsum[nt][gi] = fmaf(pv, sz.y, Zsum[nt][gi]);
+                    }
+                    if constexpr (GW == 1) {
+                        const __half hh = __float2half_rn(w[0]);
+                        const __half hl = __float2half_rn(w[0] - __half2float(hh));
+                        reinterpret_cast<__half*>(th)[t] = hh;
+                        reinterpret_cast<__half*>(th + C::kWLO)[t] = hl;
+                    } else {
+#pragma unroll
+                        for (int gp = 0; gp < GW / 2; ++gp) {
+                            const uint32_t hi = pack_part(w[2 * gp], w[2 * gp + 1], false);
+                            const float2 f = h2f(hi);
+                            const uint32_t lo = pack_part(w[2 * gp] - f.x, w[2 * gp + 1] - f.y, false);
+                            th[t * (GW / 2) + gp] = hi;
+                            th[C::kWLO + t * (GW / 2) + gp] = lo;
+                        }
+                    }
+                }
+            }
+            __syncwarp();
             // ---------------- P·V: MQ k16 steps ----------------
-            const int srcA = 8 * j + (r >> 1), srcB = srcA + 4;
-            const bool lo_part = r & 1;
+            // B fragment of column r (head 4nt + r/2, part r&1): tokens 16ks + {2j, 2j+1} and {2j+8, 2j+9}
+            const uint32_t* tr = wtab + (r & 1) * C::kWLO + (r >> 1) * C::kWS;
 #pragma unroll
             for (int ks = 0; ks < MQ; ++ks) {
-                // p of tokens 16ks + {2j, 2j+1, 2j+8, 2j+9} for head 4nt + r/2
-                float pb[NT][4];
+                uint32_t bvg[NT][GW][2];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    pb[nt][0] = __shfl_sync(0xffffffffu, pr[nt][2 * ks], srcA);
-                    pb[nt][1] = __shfl_sync(0xffffffffu, pr[nt][2 * ks], srcB);
-                    pb[nt][2] = __shfl_sync(0xffffffffu, pr[nt][2 * ks + 1], srcA);
-                    pb[nt][3] = __shfl_sync(0xffffffffu, pr[nt][2 * ks + 1], srcB);
+                    const uint32_t* tn = tr + 4 * nt * C::kWS;
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int t0 = 16 * ks + 2 * j + 8 * hf;   // even
+                        if constexpr (GW == 1) {
+                            bvg[nt][0][hf] = tn[t0 / 2];
+                        } else if constexpr (GW == 2) {
+                            const uint2 u = *reinterpret_cast<const uint2*>(tn + t0);
+                            bvg[nt][0][hf] = prmt(u.x, u.y, 0x5410u);
+                            bvg[nt][1][hf] = prmt(u.x, u.y, 0x7632u);
+                        } else {
+#pragma unroll
+                            for (int gp = 0; gp < GW / 2; ++gp) {
+                                const uint32_t u0 = tn[t0 * (GW / 2) + gp], u1 = tn[(t0 + 1) * (GW / 2) + gp];
+                                bvg[nt][2 * gp][hf] = prmt(u0, u1, 0x5410u);
+                                bvg[nt][2 * gp + 1][hf] = prmt(u0, u1, 0x7632u);
+                            }
+                        }
+                    }
                 }
                 const int tk[4] = {16 * ks + 2 * j, 16 * ks + 2 * j + 1, 16 * ks + 2 * j + 8, 16 * ks + 2 * j + 9};
 #pragma unroll
                 for (int gi = 0; gi < GW; ++gi) {
                     const int gg = wsl * GW + gi;
-                    uint32_t bv[NT][2];
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        float w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            // rows of invalid tokens hold finite stale data and get p = 0
-                            const float2 sz = *reinterpret_cast<const float2*>(sf + tk[e] * SFW + 2 * (NG + gg));
-                            w[e] = pb[nt][e] * sz.x;
-                            Wsum[nt][gi] += w[e];
-                            Zsum[nt][gi] = fmaf(pb[nt][e], sz.y, Zsum[nt][gi]);
-                        }
-                        bv[nt][0] = pack_part(w[0], w[1], lo_part);
-                        bv[nt][1] = pack_part(w[2], w[3], lo_part);
-                    }
                     // this thread's V code slice of group gg: G/32 bytes per token
                     const int vb = D / 4 + gg * (G / 4) + r * (G / 32);   // byte offset in the record
                     if constexpr (G == 32) {
@@ -527,7 +565,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                             const uint32_t a2 = code_q16(y23), a3 = code_q4(y23);
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt)
-                                mma16816(acc[nt][mt], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
+                                mma16816(acc[nt][mt], a0, a1, a2, a3, bvg[nt][gi][0], bvg[nt][gi][1]);
                         }
                     } else {
 #pragma unroll
@@ -548,7 +586,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                                 const uint32_t a2 = code_q16(y23), a3 = code_q4(y23);
 #pragma unroll
                                 for (int nt = 0; nt < NT; ++nt)
-                                    mma16816(acc[nt][mt], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
+                                    mma16816(acc[nt][mt], a0, a1, a2, a3, bvg[nt][gi][0], bvg[nt][gi][1]);
                             }
                         }
                     }
@@ -567,15 +605,16 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
             l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], 16);
 #pragma unroll
             for (int gi = 0; gi < GW; ++gi) {
-                Wsum[nt][gi] += __shfl_xor_sync(0xffffffffu, Wsum[nt][gi], 1);
-                Wsum[nt][gi] += __shfl_xor_sync(0xffffffffu, Wsum[nt][gi], 2);
-                Zsum[nt][gi] += __shfl_xor_sync(0xffffffffu, Zsum[nt][gi], 1);
-                Zsum[nt][gi] += __shfl_xor_sync(0xffffffffu, Zsum[nt][gi], 2);
+#pragma unroll
+                for (int sh = 4; sh < 32; sh <<= 1) {
+                    Wsum[nt][gi] += __shfl_xor_sync(0xffffffffu, Wsum[nt][gi], sh);
+                    Zsum[nt][gi] += __shfl_xor_sync(0xffffffffu, Zsum[nt][gi], sh);
+                }
             }
         }
         // out[head 4nt+j][ch] = (acc_hi + acc_lo − W)/α_ch + Z, with α = 1/16 on the
-        // rows r (even code positions) and 1/4 on the rows r+8; W, Z of head 4nt+j sit in lane 8j
-        const int64_t slot = (int64_t)blockIdx.x + b;
+        // rows r (even code positions) and 1/4 on the rows r+8
+        const int64_t slot = ((int64_t)blockIdx.x + b) * PAR + pi;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int hh = 4 * nt + j;
@@ -584,8 +623,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
             if (r == 0 && wsl == 0 && hh < g) P.ml[slot * P.Hq + hq] = make_float2(m_run[nt], l_run[nt]);
 #pragma unroll
             for (int gi = 0; gi < GW; ++gi) {
-                const float Wh = __shfl_sync(0xffffffffu, Wsum[nt][gi], 8 * j);
-                const float Zh = __shfl_sync(0xffffffffu, Zsum[nt][gi], 8 * j);
+                const float Wh = Wsum[nt][gi], Zh = Zsum[nt][gi];
                 const int gg = wsl * GW + gi;
 #pragma unroll
                 for (int mu = 0; mu < MTG; ++mu) {
@@ -603,28 +641,30 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     }
 }
 
-// Shared-memory plan: (x_off, stages_off, ring depth log2, total bytes); false if it does not fit.
-template <int D, int G, int NT, int WPH, int TTOK>
+// Shared-memory plan: (x_off, stages_off, ring depth log2, total bytes); false if it
+// does not fit.  Two stage parities need at least 4 stages (2 in flight).
+template <int D, int G, int NT, int WPH, int TTOK, int PAR>
 static bool mma_smem_plan(int Hkv, int* x_off, int* stages_off, int* ns_log2, size_t* total) {
     using C = MmaCfg<D, G, NT, WPH, TTOK>;
-    const int nwarps = Hkv * WPH;
-    *x_off = kSmemSF + nwarps * C::SF;
-    *stages_off = (*x_off + Hkv * C::XCH * 4 + 127) / 128 * 128;
+    const int nwarps = Hkv * WPH * PAR;
+    *x_off = kSmemTab + nwarps * C::TBL;
+    *stages_off = (*x_off + Hkv * PAR * C::XCH * 4 + 127) / 128 * 128;
     const size_t stage = (size_t)TTOK * row_bytes(Hkv * C::REC);
-    int lg = 3;                                  // 8 stages when they fit, else 4
-    if (*stages_off + (stage << 3) > 224 * 1024) lg = 2;
+    int lg = 3;                                  // 8 stages when they fit, else 4, else 2
+    while (lg > PAR && *stages_off + (stage << lg) > 224 * 1024) --lg;
     *ns_log2 = lg;
     *total = *stages_off + (stage << lg);
     return *total <= 225 * 1024;
 }
 
-template <int D, int G, int NT, int WPH, int TTOK>
+template <int D, int G, int NT, int WPH, int TTOK, int PAR>
 static int launch_mma(DecodeParams P, cudaStream_t st) {
-    const int threads = 32 * P.Hkv * WPH;
+    const int threads = 32 * P.Hkv * WPH * PAR;
     int x_off, stages_off, ns_log2;
     size_t smem;
-    if (!mma_smem_plan<D, G, NT, WPH, TTOK>(P.Hkv, &x_off, &stages_off, &ns_log2, &smem)) return OSCAR_ERR_ARG;
-    auto kern = history_mma_kernel<D, G, NT, WPH, TTOK>;
+    if (!mma_smem_plan<D, G, NT, WPH, TTOK, PAR>(P.Hkv, &x_off, &stages_off, &ns_log2, &smem))
+        return OSCAR_ERR_ARG;
+    auto kern = history_mma_kernel<D, G, NT, WPH, TTOK, PAR>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return check_cuda("cudaFuncSetAttribute(history_mma_kernel)");
     const int grid = std::min(P.n_ctas, sm_count());
@@ -641,21 +681,39 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
     if (P.Hkv > (head_dim == 256 ? 4 : 8) || P.g > 8) return OSCAR_OK;
     const int nt = (2 * P.g + 7) / 8;
     int rc = OSCAR_OK;
-    auto go = [&](auto plan, auto fn) {
+    // a variant is taken when its shared-memory plan fits; otherwise the next one is tried
+    auto go = [&](auto plan, auto fn, int par) {
+        if (*launched) return;
         int xo, so, lg;
         size_t smem;
-        if (!plan(P.Hkv, &xo, &so, &lg, &smem)) return;   // does not fit: CUDA-core kernel instead
+        if (!plan(P.Hkv, &xo, &so, &lg, &smem)) return;
+        P.par = par;
         rc = fn(P, st);
         *launched = true;
     };
-#define OSCAR_MMA(D_, G_, NT_, WPH_, TT_) go(mma_smem_plan<D_, G_, NT_, WPH_, TT_>, launch_mma<D_, G_, NT_, WPH_, TT_>)
+#define OSCAR_MMA(D_, G_, NT_, WPH_, TT_, PAR_) \
+    go(mma_smem_plan<D_, G_, NT_, WPH_, TT_, PAR_>, launch_mma<D_, G_, NT_, WPH_, TT_, PAR_>, PAR_)
+    // one n8 column tile (g <= 4): two warps per (head, slice) on alternate stages;
+    // two tiles: one warp, 32-token stages (register budget)
     if (head_dim == 128) {
-        if (P.G == 64) { if (nt == 1) OSCAR_MMA(128, 64, 1, 1, 64); else OSCAR_MMA(128, 64, 2, 1, 32); }
-        else if (P.G == 128) { if (nt == 1) OSCAR_MMA(128, 128, 1, 1, 64); else OSCAR_MMA(128, 128, 2, 1, 32); }
-        else if (P.G == 32) { if (nt == 1) OSCAR_MMA(128, 32, 1, 1, 64); else OSCAR_MMA(128, 32, 2, 1, 32); }
+        if (P.G == 64) {
+            if (nt == 1) { OSCAR_MMA(128, 64, 1, 1, 64, 2); OSCAR_MMA(128, 64, 1, 1, 64, 1); }
+            else OSCAR_MMA(128, 64, 2, 1, 32, 1);
+        } else if (P.G == 128) {
+            if (nt == 1) { OSCAR_MMA(128, 128, 1, 1, 64, 2); OSCAR_MMA(128, 128, 1, 1, 64, 1); }
+            else OSCAR_MMA(128, 128, 2, 1, 32, 1);
+        } else if (P.G == 32) {
+            if (nt == 1) { OSCAR_MMA(128, 32, 1, 1, 64, 2); OSCAR_MMA(128, 32, 1, 1, 64, 1); }
+            else OSCAR_MMA(128, 32, 2, 1, 32, 1);
+        }
     } else if (head_dim == 256) {
-        if (P.G == 128) { if (nt == 1) OSCAR_MMA(256, 128, 1, 2, 64); else OSCAR_MMA(256, 128, 2, 2, 32); }
-        else if (P.G == 64) { if (nt == 1) OSCAR_MMA(256, 64, 1, 2, 64); else OSCAR_MMA(256, 64, 2, 2, 32); }
+        if (P.G == 128) {
+            if (nt == 1) { OSCAR_MMA(256, 128, 1, 2, 64, 2); OSCAR_MMA(256, 128, 1, 2, 64, 1); }
+            else OSCAR_MMA(256, 128, 2, 2, 32, 1);
+        } else if (P.G == 64) {
+            if (nt == 1) { OSCAR_MMA(256, 64, 1, 2, 64, 2); OSCAR_MMA(256, 64, 1, 2, 64, 1); }
+            else OSCAR_MMA(256, 64, 2, 2, 32, 1);
+        }
     }
 #undef OSCAR_MMA
     if (*launched) P.n_ctas = std::min(P.n_ctas, sm_count());
