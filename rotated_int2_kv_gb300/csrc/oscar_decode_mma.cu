@@ -100,41 +100,38 @@ __host__ __device__ constexpr int row_bytes(int bytes) {
     return ((bytes + 15) / 16) % 2 == 1 ? (bytes + 15) / 16 * 16 : (bytes + 15) / 16 * 16 + 16;
 }
 
-// Stage iterator over a CTA's chunk run [f, f1): stages of tt tokens that never
-// cross a request boundary (the last stage of a segment may be partial).
+// Stage iterator over a CTA's chunk run [f, f1): stages of TT tokens that never
+// cross a request boundary (the last stage of a segment may be partial).  Chunk
+// indices fit in 32 bits (the chunk prefix is int32); f1 is held by the caller.
+template <int TT>
 struct StageIter {
-    int64_t f, f1, fe;
-    int b, t0, t_seg, t_end, tt;
-    bool valid;
+    int f, fe;          // current chunk; end of the current segment's chunks
+    int b, t0, t_end;   // request, first token of the stage, end of the segment's tokens
 
-    __device__ void seg(const DecodeParams& P) {
-        valid = f < f1;
-        if (!valid) return;
+    __device__ bool valid(int f1) const { return f < f1; }
+    __device__ void seg(const DecodeParams& P, int f1) {
+        if (f >= f1) return;
         int lo = 0, hi = P.batch - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (P.cprefix[mid] <= f) lo = mid; else hi = mid - 1;
         }
         b = lo;
-        fe = min(f1, (int64_t)P.cprefix[b + 1]);
-        const int L = P.len[b];
-        const int h_end = max(P.S, L - P.W);
-        t_seg = P.S + (int)(f - P.cprefix[b]) * P.chunk;
-        t0 = t_seg;
-        t_end = min(h_end, P.S + (int)(fe - P.cprefix[b]) * P.chunk);
+        fe = min(f1, P.cprefix[b + 1]);
+        const int h_end = max(P.S, P.len[b] - P.W);
+        t0 = P.S + (f - P.cprefix[b]) * P.chunk;
+        t_end = min(h_end, P.S + (fe - P.cprefix[b]) * P.chunk);
     }
-    __device__ void init(const DecodeParams& P, int64_t f0_, int64_t f1_, int tokens) {
-        f = f0_;
-        f1 = f1_;
-        tt = tokens;
-        seg(P);
+    __device__ void init(const DecodeParams& P, int f0, int f1) {
+        f = f0;
+        seg(P, f1);
     }
-    __device__ bool seg_last() const { return t0 + tt >= t_end; }
-    __device__ void next(const DecodeParams& P) {
-        t0 += tt;
+    __device__ bool seg_last() const { return t0 + TT >= t_end; }
+    __device__ void next(const DecodeParams& P, int f1) {
+        t0 += TT;
         if (t0 >= t_end) {
             f = fe;
-            seg(P);
+            seg(P, f1);
         }
     }
 };
@@ -204,8 +201,8 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     const int bar_id = 1 + h * PAR + pi;
 
     const int64_t N = P.cprefix[P.batch];
-    const int64_t f0 = (int64_t)blockIdx.x * N / gridDim.x;
-    const int64_t f1 = (int64_t)(blockIdx.x + 1) * N / gridDim.x;
+    const int f0 = (int)((int64_t)blockIdx.x * N / gridDim.x);
+    const int f1 = (int)((int64_t)(blockIdx.x + 1) * N / gridDim.x);
     if (f0 >= f1) return;
 
     // ---- stage pipeline shared by the whole CTA ----
@@ -214,14 +211,17 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     // chunks of whole token records of the stages it issues (stage k + NS - 1 at
     // iteration k) and arrives on the stage's full barrier when they have landed.
     long long budget = 4000000000LL;            // cycles per pipeline wait (~2 s); 0 after a timeout
-    const int tpw = (TT + nwarps - 1) / nwarps; // tokens whose records this warp copies per stage
-    const int tbeg = min(TT, warp * tpw), tend = min(TT, tbeg + tpw);
+    // The warps of one parity copy and consume the stages of that parity: two
+    // independent pipelines over even and odd stages when PAR = 2.
+    const int npw = nwarps / PAR;               // warps per parity
+    const int tpw = (TT + npw - 1) / npw;       // tokens whose records this warp copies per stage
+    const int tbeg = min(TT, hw * tpw), tend = min(TT, tbeg + tpw);
     // chunk walk of the warp's run: lane starts at chunk `lane`, steps by 32 chunks
     const int lt0 = lane / cpt, lp0 = lane % cpt, dq = 32 / cpt, dr = 32 % cpt;
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < NS; ++s) {
-            mbar_init(&full[s], blockDim.x);
-            mbar_init(&empty[s], nwarps / PAR);
+            mbar_init(&full[s], blockDim.x / PAR);
+            mbar_init(&empty[s], npw);
         }
         fence_mbar_init();
     }
@@ -229,9 +229,9 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     for (uint32_t i = threadIdx.x; i < NS * stage_bytes / 16; i += blockDim.x)
         *reinterpret_cast<uint4*>(stages + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
     // slot ids of stage `it` -> slots[si], validity masks -> smask[mi] (warp 0)
-    auto put_slots = [&](const StageIter& it, int v0, int v1, uint32_t si, uint32_t mi) {
+    auto put_slots = [&](const StageIter<TT>& it, int v0, int v1, uint32_t si, uint32_t mi) {
         bool ok0 = false, ok1 = false;
-        if (it.valid) {
+        if (it.valid(f1)) {
             const bool in0 = it.t0 + lane < it.t_end;
             const bool in1 = TT > 32 && it.t0 + 32 + lane < it.t_end;
             ok0 = in0 && v0 >= 0 && v0 < P.num_slots;
@@ -243,30 +243,30 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         const uint32_t m0 = __ballot_sync(0xffffffffu, ok0), m1 = __ballot_sync(0xffffffffu, ok1);
         if (lane == 0) { smask[mi * 2] = m0; smask[mi * 2 + 1] = m1; }
     };
-    auto get_slots = [&](const StageIter& it, int* v0, int* v1) {
+    auto get_slots = [&](const StageIter<TT>& it, int* v0, int* v1) {
         *v0 = -1;
         *v1 = -1;
-        if (!it.valid) return;
+        if (!it.valid(f1)) return;
         const int32_t* pt = P.page_table + (int64_t)it.b * P.pt_stride;
         if (it.t0 + lane < it.t_end) *v0 = pt[it.t0 + lane];
         if (TT > 32 && it.t0 + 32 + lane < it.t_end) *v1 = pt[it.t0 + 32 + lane];
     };
     // Warp 0 writes the slot ids of stages 0 .. NS-1; afterwards the leader warp of
     // each stage parity (hw == 0) writes those of stage k + NS while consuming stage k.
-    StageIter wit;                               // leader: stage whose slot ids come next
+    StageIter<TT> wit;                               // leader: stage whose slot ids come next
     int nv0 = -1, nv1 = -1;                      // leader: prefetched slot ids of stage wit
     if (hw == 0) {
-        wit.init(P, f0, f1, TT);
+        wit.init(P, f0, f1);
         for (uint32_t wk = 0; wk < NS; ++wk) {
             if (warp == 0) {
                 int v0, v1;
                 get_slots(wit, &v0, &v1);
                 put_slots(wit, v0, v1, wk, wk);
             }
-            if (wit.valid) wit.next(P);
+            if (wit.valid(f1)) wit.next(P, f1);
         }
         for (int q = 0; q < pi; ++q)
-            if (wit.valid) wit.next(P);
+            if (wit.valid(f1)) wit.next(P, f1);
         get_slots(wit, &nv0, &nv1);              // stage NS + pi
     }
     __syncthreads();
@@ -287,22 +287,28 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         }
         cp_async_mbar_arrive(&full[s]);
     };
-    // Stage k + NS - PAR is issued at iteration k: it reuses the slot of stage
-    // k - PAR, which the warps of this iteration's parity released one round ago,
-    // so issuing never waits for the stage the other parity is consuming.
-    StageIter pit;                               // stage to issue next (NS - PAR ahead)
-    pit.init(P, f0, f1, TT);
-    uint32_t pk = 0;
-    for (; pk < NS - PAR && pit.valid; ++pk, pit.next(P)) issue(pk);
+    // Stage k + NS - PAR is issued at iteration k by the warps of k's parity: it
+    // reuses the slot of stage k - PAR, which those warps released one round ago.
+    StageIter<TT> pit;                               // next stage of this parity to issue
+    pit.init(P, f0, f1);
+    uint32_t pk = pi;
+    for (int q = 0; q < pi; ++q)
+        if (pit.valid(f1)) pit.next(P, f1);
+    auto pit_step = [&]() {
+        pk += PAR;
+        for (int q = 0; q < PAR; ++q)
+            if (pit.valid(f1)) pit.next(P, f1);
+    };
+    for (; pk < NS - PAR && pit.valid(f1); pit_step()) issue(pk);
 
     // funnel shift for the K extraction: code position 2j+1 to bits 8-9 (2j to 6-7)
     const uint32_t rotK = (uint32_t)(4 * j - 6) & 31u;
     int xpar = 0;   // logit-exchange buffer parity; continuous across segments
     uint32_t k = 0; // stages consumed
 
-    StageIter it;
-    it.init(P, f0, f1, TT);
-    while (it.valid) {
+    StageIter<TT> it;
+    it.init(P, f0, f1);
+    while (it.valid(f1)) {
         const int b = it.b;
         // ---- per-segment query state ----
         uint32_t bq[NT][KS][2];
@@ -344,14 +350,13 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         bool seg_done = false;
         for (; !seg_done; ++k) {
             seg_done = it.seg_last();
-            if (pit.valid) {                     // keep NS - PAR stages in flight
-                issue(pk);
-                ++pk;
-                pit.next(P);
-            }
             if ((k & (PAR - 1)) != (uint32_t)pi) {   // a stage of the other parity
-                it.next(P);
+                it.next(P, f1);
                 continue;
+            }
+            if (pit.valid(f1)) {                 // stage k + NS - PAR (this parity)
+                issue(pk);
+                pit_step();
             }
             const uint32_t s = k & (NS - 1);
             mbar_wait_bounded(&full[s], (k >> ns_log2) & 1, P.status, budget);
@@ -361,7 +366,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                 // (same parity), which every warp reads after waiting for stage k's release.
                 put_slots(wit, nv0, nv1, s, (k + NS) % (2 * NS));
                 for (int q = 0; q < PAR; ++q)
-                    if (wit.valid) wit.next(P);
+                    if (wit.valid(f1)) wit.next(P, f1);
                 get_slots(wit, &nv0, &nv1);
             }
             const uint32_t mrow = (k % (2 * NS)) * 2;
@@ -369,20 +374,23 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
             const unsigned char* tb = stages + s * stage_bytes + h * REC;
             // ---------------- QK: MQ m16 tiles ----------------
             float lg[NT][NR];        // logits (log2 units) of head 4nt + j, token 8i + r
-            {
-                float sc[MQ][GW][NT][4];
 #pragma unroll
-                for (int mq = 0; mq < MQ; ++mq)
+            for (int mh = 0; mh < MQ; mh += 2) {   // two m16 tiles at a time (register budget)
+                constexpr int MB = MQ < 2 ? MQ : 2;
+                float sc[MB][GW][NT][4];
+#pragma unroll
+                for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
                     for (int gi = 0; gi < GW; ++gi)
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) sc[mq][gi][nt][e] = 0.f;
+                            for (int e = 0; e < 4; ++e) sc[mb][gi][nt][e] = 0.f;
 #pragma unroll
                 for (int k4 = 0; k4 < KS; k4 += 4) {
 #pragma unroll
-                    for (int mq = 0; mq < MQ; ++mq) {
+                    for (int mb = 0; mb < MB; ++mb) {
+                        const int mq = mh + mb;
                         const uint4 w0 = *reinterpret_cast<const uint4*>(
                             reinterpret_cast<const uint32_t*>(tb + (16 * mq + r) * row) + wsl * KS + k4);
                         const uint4 w1 = *reinterpret_cast<const uint4*>(
@@ -398,18 +406,17 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                             const uint32_t x2 = code_q4(y0), x3 = code_q4(y1);     // channels 2j+1, 2j+9
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt)
-                                mma16816(sc[mq][gi][nt], x0, x1, x2, x3, bq[nt][kk][0], bq[nt][kk][1]);
+                                mma16816(sc[mb][gi][nt], x0, x1, x2, x3, bq[nt][kk][0], bq[nt][kk][1]);
                         }
                     }
                 }
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                for (int ib = 0; ib < 2 * MB; ++ib) {
+                    const int i = 2 * mh + ib;       // token row 8i + r = 16·mq + 8·half + r
+                    const int t = 8 * i + r;
+                    const int mb = ib >> 1, hf = ib & 1;
 #pragma unroll
-                    for (int i = 0; i < NR; ++i) lg[nt][i] = 0.f;
-#pragma unroll
-                for (int i = 0; i < NR; ++i) {
-                    const int t = 8 * i + r;     // 16·mq + 8·half + r
-                    const int mq = i >> 1, hf = i & 1;
+                    for (int nt = 0; nt < NT; ++nt) lg[nt][i] = 0.f;
 #pragma unroll
                     for (int gi = 0; gi < GW; ++gi) {
                         const int gg = wsl * GW + gi;
@@ -417,7 +424,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             const float2 Q = qs[nt][gi];       // (Σ q̃, Σ q̃/α)
-                            lg[nt][i] += sz.x * (sc[mq][gi][nt][2 * hf] + sc[mq][gi][nt][2 * hf + 1] - Q.y) + sz.y * Q.x;
+                            lg[nt][i] += sz.x * (sc[mb][gi][nt][2 * hf] + sc[mb][gi][nt][2 * hf + 1] - Q.y) + sz.y * Q.x;
                         }
                     }
                 }
@@ -594,7 +601,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
             }
             __syncwarp();                       // this warp is done with stage k and its scale table
             if (lane == 0) mbar_arrive(&empty[s]);
-            it.next(P);
+            it.next(P, f1);
         }
 
         // ---------------- segment end: reduce and write the partial ----------------
