@@ -113,14 +113,16 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
         }
         __syncthreads();
         // Per group, from the fp16 hi + lo parts actually fed to the MMA: Q = Σ q̃
-        // and Q' = Σ q̃/α, where α = 1/16 for even and 1/4 for odd channels (the
-        // weights with which the MMA path encodes a code c as 1 + α·c).
+        // and Q' = Σ q̃/α, where α is the weight with which the tensor-core path
+        // encodes a code c of that channel as 1 + α·c: by code position within a
+        // 16-code word (pos_inv_alpha) for groups >= 64, 1/16 on even and 1/4 on
+        // odd channels for group size 32.
         const int lane = tid & 31, warp = tid >> 5;
         for (int i = warp; i < nh * P.ng; i += 8) {
             const int j = i / P.ng, gi = i % P.ng;
             float sq_ = 0.f, sqa = 0.f;
             for (int c = gi * P.G + lane; c < (gi + 1) * P.G; c += 32) {
-                const float inv = (c & 1) ? 4.f : 16.f;
+                const float inv = P.G >= 64 ? pos_inv_alpha(c & 7) : ((c & 1) ? 4.f : 16.f);
                 const float x = sqt[j][c] * inv;
                 const __half hi = __float2half_rn(x);
                 const __half lo = __float2half_rn(x - __half2float(hi));
@@ -152,13 +154,29 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
                 continue;
             }
             if (head < h0 || head >= h0 + nh) continue;
-            // k-cols (2j, 2j+1) <- channels (16kk+2j, 16kk+2j+8), even: scaled by 16;
-            // k-cols (2j+8, 2j+9) <- channels (16kk+2j+1, 16kk+2j+9), odd: scaled by 4
-            const int chans[4] = {16 * kk + 2 * j, 16 * kk + 2 * j + 8, 16 * kk + 2 * j + 1, 16 * kk + 2 * j + 9};
+            // Group size 32: k-cols (2j, 2j+1) <- channels (16kk+2j, 16kk+2j+8), even:
+            // scaled by 16; k-cols (2j+8, 2j+9) <- channels (16kk+2j+1, 16kk+2j+9), odd:
+            // scaled by 4.  Groups >= 64: lane j owns word w = 4(kk/4) + j; k-step kk
+            // takes slot kk%4 of it: k-cols (2j, 2j+1) <- first position p of both
+            // halves (channels 16w + p, 16w + 8 + p), (2j+8, 2j+9) <- second position.
+            int chans[4];
+            float scl[4];
+            if (P.G >= 64) {
+                const int w = 4 * (kk / 4) + j, p0 = slot_pos(kk % 4, 0), p1 = slot_pos(kk % 4, 1);
+                chans[0] = 16 * w + p0; chans[1] = 16 * w + 8 + p0;
+                chans[2] = 16 * w + p1; chans[3] = 16 * w + 8 + p1;
+                scl[0] = scl[1] = pos_inv_alpha(p0);
+                scl[2] = scl[3] = pos_inv_alpha(p1);
+            } else {
+                chans[0] = 16 * kk + 2 * j; chans[1] = 16 * kk + 2 * j + 8;
+                chans[2] = 16 * kk + 2 * j + 1; chans[3] = 16 * kk + 2 * j + 9;
+                scl[0] = scl[1] = 16.f;
+                scl[2] = scl[3] = 4.f;
+            }
             uint16_t hv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float x = sqt[head - h0][chans[e]] * (e < 2 ? 16.f : 4.f);
+                const float x = sqt[head - h0][chans[e]] * scl[e];
                 const __half hi = __float2half_rn(x);
                 const __half v = part ? __float2half_rn(x - __half2float(hi)) : hi;
                 hv[e] = *reinterpret_cast<const uint16_t*>(&v);

@@ -64,6 +64,15 @@ __device__ __forceinline__ uint32_t code_q4(uint32_t x) { return and_or(x, 0x030
 __device__ __forceinline__ uint32_t code_q16(uint32_t x) { return and_or(x, 0x00C000C0u, 0x3C003C00u); }
 __device__ __forceinline__ uint32_t rotr(uint32_t w, uint32_t n) { return __funnelshift_r(w, w, n); }
 
+// half2 (1 + α_p·c) of position p from the three variants (y = w, w >> 6, w << 4)
+template <int POS>
+__device__ __forceinline__ uint32_t code_pos(uint32_t yd, uint32_t yr, uint32_t yl) {
+    constexpr int bit = POS <= 1 ? 2 * POS + 4 : (POS <= 4 ? 2 * POS : 2 * POS - 6);
+    constexpr uint32_t mask = (3u << bit) | (3u << (bit + 16));
+    const uint32_t y = POS <= 1 ? yl : (POS <= 4 ? yd : yr);
+    return and_or(y, mask, 0x3C003C00u);
+}
+
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -302,7 +311,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     for (; pk < NS - PAR && pit.valid(f1); pit_step()) issue(pk);
 
     // funnel shift for the K extraction: code position 2j+1 to bits 8-9 (2j to 6-7)
-    const uint32_t rotK = (uint32_t)(4 * j - 6) & 31u;
+    const uint32_t rotK = (uint32_t)(4 * j - 6) & 31u;   // (group size 32)
     int xpar = 0;   // logit-exchange buffer parity; continuous across segments
     uint32_t k = 0; // stages consumed
 
@@ -391,22 +400,52 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
 #pragma unroll
                     for (int mb = 0; mb < MB; ++mb) {
                         const int mq = mh + mb;
-                        const uint4 w0 = *reinterpret_cast<const uint4*>(
-                            reinterpret_cast<const uint32_t*>(tb + (16 * mq + r) * row) + wsl * KS + k4);
-                        const uint4 w1 = *reinterpret_cast<const uint4*>(
-                            reinterpret_cast<const uint32_t*>(tb + (16 * mq + r + 8) * row) + wsl * KS + k4);
-                        const uint32_t a0s[4] = {w0.x, w0.y, w0.z, w0.w};
-                        const uint32_t a1s[4] = {w1.x, w1.y, w1.z, w1.w};
+                        const uint32_t* w_r = reinterpret_cast<const uint32_t*>(tb + (16 * mq + r) * row) + wsl * KS + k4;
+                        const uint32_t* w_r8 = reinterpret_cast<const uint32_t*>(tb + (16 * mq + r + 8) * row) + wsl * KS + k4;
+                        if constexpr (G >= 64) {
+                            // lane j owns word k4 + j of its rows: k-step k4 + q takes its
+                            // slot q, (k 2j, 2j+1) <- first position of both halves and
+                            // (2j+8, 2j+9) <- second position; all 4 words in one group
+                            const int gi = (k4 * 16) / G;
+                            const uint32_t u0 = w_r[j], u1 = w_r8[j];
+                            const uint32_t d0 = u0, r0 = u0 >> 6, l0 = u0 << 4;
+                            const uint32_t d1 = u1, r1 = u1 >> 6, l1 = u1 << 4;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int kk = k4 + q;
-                            const int gi = (kk * 16) / G;
-                            const uint32_t y0 = rotr(a0s[q], rotK), y1 = rotr(a1s[q], rotK);
-                            const uint32_t x0 = code_q16(y0), x1 = code_q16(y1);   // channels 2j, 2j+8
-                            const uint32_t x2 = code_q4(y0), x3 = code_q4(y1);     // channels 2j+1, 2j+9
+                            for (int q = 0; q < 4; ++q) {
+                                uint32_t x0, x1, x2, x3;
+                                if (q == 0) {
+                                    x0 = code_pos<slot_pos(0, 0)>(d0, r0, l0); x1 = code_pos<slot_pos(0, 0)>(d1, r1, l1);
+                                    x2 = code_pos<slot_pos(0, 1)>(d0, r0, l0); x3 = code_pos<slot_pos(0, 1)>(d1, r1, l1);
+                                } else if (q == 1) {
+                                    x0 = code_pos<slot_pos(1, 0)>(d0, r0, l0); x1 = code_pos<slot_pos(1, 0)>(d1, r1, l1);
+                                    x2 = code_pos<slot_pos(1, 1)>(d0, r0, l0); x3 = code_pos<slot_pos(1, 1)>(d1, r1, l1);
+                                } else if (q == 2) {
+                                    x0 = code_pos<slot_pos(2, 0)>(d0, r0, l0); x1 = code_pos<slot_pos(2, 0)>(d1, r1, l1);
+                                    x2 = code_pos<slot_pos(2, 1)>(d0, r0, l0); x3 = code_pos<slot_pos(2, 1)>(d1, r1, l1);
+                                } else {
+                                    x0 = code_pos<slot_pos(3, 0)>(d0, r0, l0); x1 = code_pos<slot_pos(3, 0)>(d1, r1, l1);
+                                    x2 = code_pos<slot_pos(3, 1)>(d0, r0, l0); x3 = code_pos<slot_pos(3, 1)>(d1, r1, l1);
+                                }
 #pragma unroll
-                            for (int nt = 0; nt < NT; ++nt)
-                                mma16816(sc[mb][gi][nt], x0, x1, x2, x3, bq[nt][kk][0], bq[nt][kk][1]);
+                                for (int nt = 0; nt < NT; ++nt)
+                                    mma16816(sc[mb][gi][nt], x0, x1, x2, x3, bq[nt][k4 + q][0], bq[nt][k4 + q][1]);
+                            }
+                        } else {
+                            const uint4 w0 = *reinterpret_cast<const uint4*>(w_r);
+                            const uint4 w1 = *reinterpret_cast<const uint4*>(w_r8);
+                            const uint32_t a0s[4] = {w0.x, w0.y, w0.z, w0.w};
+                            const uint32_t a1s[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const int kk = k4 + q;
+                                const int gi = (kk * 16) / G;
+                                const uint32_t y0 = rotr(a0s[q], rotK), y1 = rotr(a1s[q], rotK);
+                                const uint32_t x0 = code_q16(y0), x1 = code_q16(y1);   // channels 2j, 2j+8
+                                const uint32_t x2 = code_q4(y0), x3 = code_q4(y1);     // channels 2j+1, 2j+9
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt)
+                                    mma16816(sc[mb][gi][nt], x0, x1, x2, x3, bq[nt][kk][0], bq[nt][kk][1]);
+                            }
                         }
                     }
                 }
@@ -584,13 +623,26 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                                                       *reinterpret_cast<const uint32_t*>(tb + tk[1] * row + wo), wsel);
                             const uint32_t u23 = prmt(*reinterpret_cast<const uint32_t*>(tb + tk[2] * row + wo),
                                                       *reinterpret_cast<const uint32_t*>(tb + tk[3] * row + wo), wsel);
+                            // m-tile slot mu: row r <- first, row r+8 <- second position of slot mu
+                            const uint32_t d01 = u01, r01 = u01 >> 6, l01 = u01 << 4;
+                            const uint32_t d23 = u23, r23 = u23 >> 6, l23 = u23 << 4;
 #pragma unroll
                             for (int mu = 0; mu < 4; ++mu) {
                                 const int mt = gi * MTG + hw * 4 + mu;
-                                const uint32_t rb = (uint32_t)(4 * mu - 6) & 31u;   // position 2mu+1 -> bits 8-9
-                                const uint32_t y01 = rotr(u01, rb), y23 = rotr(u23, rb);
-                                const uint32_t a0 = code_q16(y01), a1 = code_q4(y01);
-                                const uint32_t a2 = code_q16(y23), a3 = code_q4(y23);
+                                uint32_t a0, a1, a2, a3;
+                                if (mu == 0) {
+                                    a0 = code_pos<slot_pos(0, 0)>(d01, r01, l01); a1 = code_pos<slot_pos(0, 1)>(d01, r01, l01);
+                                    a2 = code_pos<slot_pos(0, 0)>(d23, r23, l23); a3 = code_pos<slot_pos(0, 1)>(d23, r23, l23);
+                                } else if (mu == 1) {
+                                    a0 = code_pos<slot_pos(1, 0)>(d01, r01, l01); a1 = code_pos<slot_pos(1, 1)>(d01, r01, l01);
+                                    a2 = code_pos<slot_pos(1, 0)>(d23, r23, l23); a3 = code_pos<slot_pos(1, 1)>(d23, r23, l23);
+                                } else if (mu == 2) {
+                                    a0 = code_pos<slot_pos(2, 0)>(d01, r01, l01); a1 = code_pos<slot_pos(2, 1)>(d01, r01, l01);
+                                    a2 = code_pos<slot_pos(2, 0)>(d23, r23, l23); a3 = code_pos<slot_pos(2, 1)>(d23, r23, l23);
+                                } else {
+                                    a0 = code_pos<slot_pos(3, 0)>(d01, r01, l01); a1 = code_pos<slot_pos(3, 1)>(d01, r01, l01);
+                                    a2 = code_pos<slot_pos(3, 0)>(d23, r23, l23); a3 = code_pos<slot_pos(3, 1)>(d23, r23, l23);
+                                }
 #pragma unroll
                                 for (int nt = 0; nt < NT; ++nt)
                                     mma16816(acc[nt][mt], a0, a1, a2, a3, bvg[nt][gi][0], bvg[nt][gi][1]);
@@ -635,12 +687,22 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
 #pragma unroll
                 for (int mu = 0; mu < MTG; ++mu) {
                     const int mt = gi * MTG + mu;
-                    int ch0;
-                    if constexpr (G == 32) ch0 = gg * G + 4 * r + 2 * mu;
-                    else ch0 = gg * G + r * (G / 8) + 8 * (mu / 4) + 2 * (mu % 4);
-                    if (hh < g) {
-                        o[ch0] = 16.f * (acc[nt][mt][0] + acc[nt][mt][1] - Wh) + Zh;
-                        o[ch0 + 1] = 4.f * (acc[nt][mt][2] + acc[nt][mt][3] - Wh) + Zh;
+                    if (hh >= g) continue;
+                    const float v0 = acc[nt][mt][0] + acc[nt][mt][1] - Wh;   // row r
+                    const float v1 = acc[nt][mt][2] + acc[nt][mt][3] - Wh;   // row r + 8
+                    if constexpr (G == 32) {
+                        // rows r / r+8: even / odd code position of the pair, α = 1/16, 1/4
+                        const int ch0 = gg * G + 4 * r + 2 * mu;
+                        o[ch0] = 16.f * v0 + Zh;
+                        o[ch0 + 1] = 4.f * v1 + Zh;
+                    } else {
+                        // the 16-bit chunk r (and half-word mu / 4) of the group; slot mu % 4
+                        const int base = gg * G + r * (G / 8) + 8 * (mu / 4);
+                        const int s4 = mu % 4;
+                        const int p0 = s4 == 0 ? slot_pos(0, 0) : s4 == 1 ? slot_pos(1, 0) : s4 == 2 ? slot_pos(2, 0) : slot_pos(3, 0);
+                        const int p1 = s4 == 0 ? slot_pos(0, 1) : s4 == 1 ? slot_pos(1, 1) : s4 == 2 ? slot_pos(2, 1) : slot_pos(3, 1);
+                        o[base + p0] = pos_inv_alpha(p0) * v0 + Zh;
+                        o[base + p1] = pos_inv_alpha(p1) * v1 + Zh;
                     }
                 }
             }
