@@ -11,28 +11,32 @@
 // Structure (persistent CTAs, one per SM; CTA i owns flattened history chunks
 // [i·N/n, (i+1)·N/n)):
 //  * the CTA walks its chunk run in stages of TTOK tokens (64, or 32 when a
-//    warp carries two n8 column tiles) through a ring of 4 or 8 shared-memory
-//    stages.  Every warp copies, with 16-byte cp.async, a contiguous run of
-//    the stage's token records (all KV heads of a token are one contiguous
-//    slot-major record, so one copy instruction touches one or two records:
-//    few address translations per byte) and arrives on the stage's full
-//    mbarrier when its copies land; slot ids come from a table that warp 0
-//    fills one ring-depth ahead;
-//  * every warp then consumes its own KV head of the stage (its channel half
-//    for d = 256, where two warps share a head) and releases the stage on its
+//    warp carries two n8 column tiles).  With PAR = 2 two sets of warps (one
+//    warp per KV head each) take the even and the odd stages: two independent
+//    pipelines over a shared ring of 4 or 8 shared-memory stages, so each SM
+//    scheduler has 4 warps to interleave.  The warps of a set copy the
+//    records of their stages with one bulk (TMA engine) copy per token: all
+//    KV heads of a token are one contiguous slot-major record, so one copy
+//    moves 640 B of one page (few address translations per byte), completing
+//    on the stage's full mbarrier; slot ids come from a table that the set's
+//    leader warp fills one ring-depth ahead;
+//  * every warp consumes its own KV head of its stages (its channel half for
+//    d = 256, where two warps share a head) and releases each stage on its
 //    empty mbarrier;
 //  * each 16-token sub-tile runs mma.sync.m16n8k16 f16 → f32.  A code c
-//    enters the MMA as the exact fp16 value 1 + α·c, α = 1/4 for odd and 1/16
-//    for even channels (one funnel shift exposes two adjacent code positions
-//    at bits 8-9 and 6-7, and one LOP3 each turns them into fp16); the
-//    channel weights 1/α sit in the other operand or in the epilogue, and the
-//    per-group scale s and zero z are applied in fp32 afterwards:
+//    enters the MMA as the exact fp16 value 1 + α·c: one LOP3 masks a code
+//    position of both 16-bit halves of a word and ORs in 0x3C00, after at most
+//    one shift of the word (see pos_inv_alpha / slot_pos; group size 32 uses
+//    one funnel shift per word and α = 1/16, 1/4).  The channel weights 1/α sit
+//    in the query operand or in the epilogue, and the per-group scale s and
+//    zero z are applied in fp32 afterwards:
 //        logit = Σ_g [s_g·(Σ (q̃/α)(1 + α c) − Σ q̃/α) + z_g·Σ q̃]
 //        o_rot[ch] = (Σ_t w_t (1 + α_ch c_t) − Σ_t w_t)/α_ch + Σ_t p_t z_t,   w = p·s
 //    q̃/α and p·s are split into fp16 hi + lo parts that occupy the n8 columns
 //    (head, part), so the products carry ~22 bits;
-//  * online softmax in log2 units, one running-max update per stage;
-//    partials (m, l, o) per (CTA, request).
+//  * online softmax in log2 units; the running max moves only when a logit
+//    exceeds it (one warp vote per stage otherwise); partials (m, l, o) per
+//    (CTA, request, stage parity).
 #include <algorithm>
 #include <cmath>
 
@@ -198,7 +202,6 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     const uint32_t NS = 1u << ns_log2;
     const int row = trow;                       // stage row stride of one token (all heads)
     const int tok_bytes = Hkv * REC;
-    const int cpt = tok_bytes / 16;             // 16-byte chunks per token record
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + 8;
     uint32_t* smask = reinterpret_cast<uint32_t*>(smem + kSmemMask);     // [16 stages][2 halves]
@@ -215,21 +218,18 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     if (f0 >= f1) return;
 
     // ---- stage pipeline shared by the whole CTA ----
-    // Warp 0 writes the slot ids (and validity masks) of stage k + NS once every
-    // thread has issued stage k; every warp copies a contiguous run of 16-byte
-    // chunks of whole token records of the stages it issues (stage k + NS - 1 at
-    // iteration k) and arrives on the stage's full barrier when they have landed.
+    // The leader warp of a set writes the slot ids (and validity masks) of stage
+    // k + NS once every warp of the set has issued stage k; every warp of the set
+    // copies its share of the token records of the stages it issues.
     long long budget = 4000000000LL;            // cycles per pipeline wait (~2 s); 0 after a timeout
     // The warps of one parity copy and consume the stages of that parity: two
     // independent pipelines over even and odd stages when PAR = 2.
     const int npw = nwarps / PAR;               // warps per parity
     const int tpw = (TT + npw - 1) / npw;       // tokens whose records this warp copies per stage
     const int tbeg = min(TT, hw * tpw), tend = min(TT, tbeg + tpw);
-    // chunk walk of the warp's run: lane starts at chunk `lane`, steps by 32 chunks
-    const int lt0 = lane / cpt, lp0 = lane % cpt, dq = 32 / cpt, dr = 32 % cpt;
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < NS; ++s) {
-            mbar_init(&full[s], blockDim.x / PAR);
+            mbar_init(&full[s], npw);
             mbar_init(&empty[s], npw);
         }
         fence_mbar_init();
@@ -284,17 +284,19 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     auto issue = [&](uint32_t k) {
         const uint32_t s = k & (NS - 1);
         if (k >= NS) mbar_wait_bounded(&empty[s], ((k >> ns_log2) - 1) & 1, P.status, budget);
+        // one bulk copy (TMA engine) per token record; the warp's lane 0 posts the
+        // byte count of its copies on the stage's full barrier before they are issued
         unsigned char* dst = stages + s * stage_bytes;
         const int32_t* srow = slots + s * 64;
-        int t = tbeg + lt0, pc = lp0;
-        while (t < tend) {
+        int nvalid = 0;
+        for (int t = tbeg + lane; t < tend; t += 32) nvalid += srow[t] >= 0;
+        for (int off = 16; off; off >>= 1) nvalid += __shfl_xor_sync(0xffffffffu, nvalid, off);
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(nvalid * tok_bytes));
+        __syncwarp();
+        for (int t = tbeg + lane; t < tend; t += 32) {
             const int sl = srow[t];
-            if (sl >= 0) cp_async16(dst + t * row + pc * 16, P.records + (int64_t)sl * tok_bytes + pc * 16);
-            t += dq;
-            pc += dr;
-            if (pc >= cpt) { pc -= cpt; ++t; }
+            if (sl >= 0) bulk_g2s(dst + t * row, P.records + (int64_t)sl * tok_bytes, (uint32_t)tok_bytes, &full[s]);
         }
-        cp_async_mbar_arrive(&full[s]);
     };
     // Stage k + NS - PAR is issued at iteration k by the warps of k's parity: it
     // reuses the slot of stage k - PAR, which those warps released one round ago.
@@ -772,7 +774,7 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
             if (nt == 1) { OSCAR_MMA(128, 128, 1, 1, 64, 2); OSCAR_MMA(128, 128, 1, 1, 64, 1); }
             else OSCAR_MMA(128, 128, 2, 1, 32, 1);
         } else if (P.G == 32) {
-            if (nt == 1) { OSCAR_MMA(128, 32, 1, 1, 64, 2); OSCAR_MMA(128, 32, 1, 1, 64, 1); }
+            if (nt == 1) OSCAR_MMA(128, 32, 1, 1, 64, 1);   // two sets would spill registers
             else OSCAR_MMA(128, 32, 2, 1, 32, 1);
         }
     } else if (head_dim == 256) {
