@@ -18,8 +18,8 @@
 //    records of their stages with one bulk (TMA engine) copy per token: all
 //    KV heads of a token are one contiguous slot-major record, so one copy
 //    moves 640 B of one page (few address translations per byte), completing
-//    on the stage's full mbarrier; slot ids come from a table that the set's
-//    leader warp fills one ring-depth ahead;
+//    on the stage's full mbarrier; each warp fetches the slot ids of its
+//    tokens from the page table one stage ahead;
 //  * every warp consumes its own KV head of its stages (its channel half for
 //    d = 256, where two warps share a head) and releases each stage on its
 //    empty mbarrier;
@@ -177,10 +177,10 @@ struct MmaCfg {
 };
 
 // Shared-memory layout (byte offsets): [0, 64) full[8] and [64, 128) empty[8]
-// mbarriers; [128, 256) stage validity masks [16][2]; [256, 2304) slot-id
-// table [8][64]; then per warp its P·V operand table, per (head, parity) the
-// logit exchange area (d = 256), and the stage ring at stages_off.
-constexpr int kSmemMask = 128, kSmemSlots = 256, kSmemTab = 256 + 8 * 64 * 4;
+// mbarriers; [128, 256) stage validity masks, two 64-bit words per ring slot;
+// then per warp its P·V operand table, per (head, parity) the logit exchange
+// area (d = 256), and the stage ring at stages_off.
+constexpr int kSmemMask = 128, kSmemTab = 256;
 
 template <int D, int G, int NT, int WPH, int TTOK, int PAR>
 __global__ void __launch_bounds__(256 * PAR, 1)
@@ -204,8 +204,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     const int tok_bytes = Hkv * REC;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + 8;
-    uint32_t* smask = reinterpret_cast<uint32_t*>(smem + kSmemMask);     // [16 stages][2 halves]
-    int32_t* slots = reinterpret_cast<int32_t*>(smem + kSmemSlots);      // [8][64]
+    uint64_t* vmw = reinterpret_cast<uint64_t*>(smem + kSmemMask);      // [8 slots][2] validity masks
     uint32_t* wtab = reinterpret_cast<uint32_t*>(smem + kSmemTab + warp * C::TBL);
     float* xb = reinterpret_cast<float*>(smem + x_off) + (h * PAR + pi) * C::XCH;
     unsigned char* stages = smem + stages_off;
@@ -218,9 +217,8 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     if (f0 >= f1) return;
 
     // ---- stage pipeline shared by the whole CTA ----
-    // The leader warp of a set writes the slot ids (and validity masks) of stage
-    // k + NS once every warp of the set has issued stage k; every warp of the set
-    // copies its share of the token records of the stages it issues.
+    // Every warp of a set copies its share (tokens [tbeg, tend)) of the token
+    // records of the stages it issues.
     long long budget = 4000000000LL;            // cycles per pipeline wait (~2 s); 0 after a timeout
     // The warps of one parity copy and consume the stages of that parity: two
     // independent pipelines over even and odd stages when PAR = 2.
@@ -237,70 +235,52 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     // zero the stage ring once: rows of invalid tokens then always hold finite values
     for (uint32_t i = threadIdx.x; i < NS * stage_bytes / 16; i += blockDim.x)
         *reinterpret_cast<uint4*>(stages + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
-    // slot ids of stage `it` -> slots[si], validity masks -> smask[mi] (warp 0)
-    auto put_slots = [&](const StageIter<TT>& it, int v0, int v1, uint32_t si, uint32_t mi) {
-        bool ok0 = false, ok1 = false;
-        if (it.valid(f1)) {
-            const bool in0 = it.t0 + lane < it.t_end;
-            const bool in1 = TT > 32 && it.t0 + 32 + lane < it.t_end;
-            ok0 = in0 && v0 >= 0 && v0 < P.num_slots;
-            ok1 = in1 && v1 >= 0 && v1 < P.num_slots;
-            if ((in0 && !ok0) || (in1 && !ok1)) set_status(P.status, OSCAR_DEV_BAD_SLOT);
-        }
-        slots[si * 64 + lane] = ok0 ? v0 : -1;
-        if (TT > 32) slots[si * 64 + 32 + lane] = ok1 ? v1 : -1;
-        const uint32_t m0 = __ballot_sync(0xffffffffu, ok0), m1 = __ballot_sync(0xffffffffu, ok1);
-        if (lane == 0) { smask[mi * 2] = m0; smask[mi * 2 + 1] = m1; }
+    // Every warp fetches the page-table entries of its tokens of the next stage it
+    // issues one iteration ahead (nsl0, nsl1: tokens tbeg + lane, tbeg + 32 + lane;
+    // kNoTok when the position lies outside the history).  At issue it posts the
+    // validity bits of its tokens into the stage's mask word: two words per ring
+    // slot, alternating with the slot's use, the next one cleared by the set's
+    // first warp once the slot's previous consumers are done with it.
+    constexpr int kNoTok = -2147483647 - 1;
+    int nsl0 = kNoTok, nsl1 = kNoTok;
+    StageIter<TT> pit;                               // next stage of this parity to issue
+    auto load_slots = [&]() {
+        nsl0 = kNoTok;
+        nsl1 = kNoTok;
+        if (!pit.valid(f1)) return;
+        const int32_t* pt = P.page_table + (int64_t)pit.b * P.pt_stride + pit.t0;
+        const int ta = tbeg + lane, tc = tbeg + 32 + lane;
+        if (ta < tend && pit.t0 + ta < pit.t_end) nsl0 = pt[ta];
+        if (tc < tend && pit.t0 + tc < pit.t_end) nsl1 = pt[tc];
     };
-    auto get_slots = [&](const StageIter<TT>& it, int* v0, int* v1) {
-        *v0 = -1;
-        *v1 = -1;
-        if (!it.valid(f1)) return;
-        const int32_t* pt = P.page_table + (int64_t)it.b * P.pt_stride;
-        if (it.t0 + lane < it.t_end) *v0 = pt[it.t0 + lane];
-        if (TT > 32 && it.t0 + 32 + lane < it.t_end) *v1 = pt[it.t0 + 32 + lane];
-    };
-    // Warp 0 writes the slot ids of stages 0 .. NS-1; afterwards the leader warp of
-    // each stage parity (hw == 0) writes those of stage k + NS while consuming stage k.
-    StageIter<TT> wit;                               // leader: stage whose slot ids come next
-    int nv0 = -1, nv1 = -1;                      // leader: prefetched slot ids of stage wit
-    if (hw == 0) {
-        wit.init(P, f0, f1);
-        for (uint32_t wk = 0; wk < NS; ++wk) {
-            if (warp == 0) {
-                int v0, v1;
-                get_slots(wit, &v0, &v1);
-                put_slots(wit, v0, v1, wk, wk);
-            }
-            if (wit.valid(f1)) wit.next(P, f1);
-        }
-        for (int q = 0; q < pi; ++q)
-            if (wit.valid(f1)) wit.next(P, f1);
-        get_slots(wit, &nv0, &nv1);              // stage NS + pi
-    }
+    for (uint32_t i = threadIdx.x; i < 2 * NS; i += blockDim.x) vmw[i] = 0ull;
     __syncthreads();
 
-    // copies of stage k by this warp
+    // copies of stage k (the stage at pit) by this warp
     auto issue = [&](uint32_t k) {
         const uint32_t s = k & (NS - 1);
-        if (k >= NS) mbar_wait_bounded(&empty[s], ((k >> ns_log2) - 1) & 1, P.status, budget);
-        // one bulk copy (TMA engine) per token record; the warp's lane 0 posts the
-        // byte count of its copies on the stage's full barrier before they are issued
-        unsigned char* dst = stages + s * stage_bytes;
-        const int32_t* srow = slots + s * 64;
-        int nvalid = 0;
-        for (int t = tbeg + lane; t < tend; t += 32) nvalid += srow[t] >= 0;
-        for (int off = 16; off; off >>= 1) nvalid += __shfl_xor_sync(0xffffffffu, nvalid, off);
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(nvalid * tok_bytes));
-        __syncwarp();
-        for (int t = tbeg + lane; t < tend; t += 32) {
-            const int sl = srow[t];
-            if (sl >= 0) bulk_g2s(dst + t * row, P.records + (int64_t)sl * tok_bytes, (uint32_t)tok_bytes, &full[s]);
+        const uint32_t use = k >> ns_log2;
+        if (k >= NS) mbar_wait_bounded(&empty[s], (use - 1) & 1, P.status, budget);
+        const bool ok0 = nsl0 >= 0 && nsl0 < P.num_slots;
+        const bool ok1 = nsl1 >= 0 && nsl1 < P.num_slots;
+        if ((nsl0 != kNoTok && !ok0) || (nsl1 != kNoTok && !ok1)) set_status(P.status, OSCAR_DEV_BAD_SLOT);
+        const uint32_t b0 = __ballot_sync(0xffffffffu, ok0), b1 = __ballot_sync(0xffffffffu, ok1);
+        if (lane == 0) {
+            if (hw == 0) vmw[2 * s + ((use + 1) & 1)] = 0ull;
+            const uint64_t bits = ((uint64_t)b0 | ((uint64_t)b1 << 32)) << tbeg;
+            if (bits) atomicOr(reinterpret_cast<unsigned long long*>(&vmw[2 * s + (use & 1)]),
+                               (unsigned long long)bits);
+            // one bulk copy (TMA engine) per token record; the byte count is posted
+            // on the stage's full barrier before the copies are issued
+            mbar_arrive_expect_tx(&full[s], (uint32_t)((__popc(b0) + __popc(b1)) * tok_bytes));
         }
+        __syncwarp();
+        unsigned char* dst = stages + s * stage_bytes;
+        if (ok0) bulk_g2s(dst + (tbeg + lane) * row, P.records + (int64_t)nsl0 * tok_bytes, (uint32_t)tok_bytes, &full[s]);
+        if (ok1) bulk_g2s(dst + (tbeg + 32 + lane) * row, P.records + (int64_t)nsl1 * tok_bytes, (uint32_t)tok_bytes, &full[s]);
     };
     // Stage k + NS - PAR is issued at iteration k by the warps of k's parity: it
     // reuses the slot of stage k - PAR, which those warps released one round ago.
-    StageIter<TT> pit;                               // next stage of this parity to issue
     pit.init(P, f0, f1);
     uint32_t pk = pi;
     for (int q = 0; q < pi; ++q)
@@ -309,7 +289,9 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         pk += PAR;
         for (int q = 0; q < PAR; ++q)
             if (pit.valid(f1)) pit.next(P, f1);
+        load_slots();
     };
+    load_slots();
     for (; pk < NS - PAR && pit.valid(f1); pit_step()) issue(pk);
 
     // funnel shift for the K extraction: code position 2j+1 to bits 8-9 (2j to 6-7)
@@ -371,17 +353,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
             }
             const uint32_t s = k & (NS - 1);
             mbar_wait_bounded(&full[s], (k >> ns_log2) & 1, P.status, budget);
-            if (hw == 0) {
-                // Every thread has issued stage k (its full barrier completed), so the
-                // slot row of stage k is free: it receives the slot ids of stage k + NS
-                // (same parity), which every warp reads after waiting for stage k's release.
-                put_slots(wit, nv0, nv1, s, (k + NS) % (2 * NS));
-                for (int q = 0; q < PAR; ++q)
-                    if (wit.valid(f1)) wit.next(P, f1);
-                get_slots(wit, &nv0, &nv1);
-            }
-            const uint32_t mrow = (k % (2 * NS)) * 2;
-            const uint64_t vmask = (uint64_t)smask[mrow] | ((uint64_t)smask[mrow + 1] << 32);
+            const uint64_t vmask = vmw[2 * s + ((k >> ns_log2) & 1)];
             const unsigned char* tb = stages + s * stage_bytes + h * REC;
             // ---------------- QK: MQ m16 tiles ----------------
             float lg[NT][NR];        // logits (log2 units) of head 4nt + j, token 8i + r
