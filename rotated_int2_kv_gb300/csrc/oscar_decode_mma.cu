@@ -104,6 +104,15 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier that also returns the OR of v over the participating threads.
+__device__ __forceinline__ int named_bar_or(int id, int nthreads, int v) {
+    int r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\t"
+                 "bar.red.or.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r) : "r"(v), "r"(id), "r"(nthreads) : "memory");
+    return r;
+}
+
 }  // namespace mma_detail
 
 // Row stride of one token's record in shared memory: rounded up to an odd
@@ -178,11 +187,12 @@ struct MmaCfg {
 
 // Shared-memory layout (byte offsets): [0, 64) full[8] and [64, 128) empty[8]
 // mbarriers; [128, 256) stage validity masks, two 64-bit words per ring slot;
-// then per warp its P·V operand table, per (head, parity) the logit exchange
+// [256, 260) the abort flag; from 384 per warp its P·V operand table, per (head, parity) the logit exchange
 // area (d = 256), and the stage ring at stages_off.
-constexpr int kSmemMask = 128, kSmemTab = 256;
+constexpr int kSmemMask = 128, kSmemAbort = 256, kSmemTab = 384;
 
-template <int D, int G, int NT, int WPH, int TTOK, int PAR>
+// HKV > 0 fixes the KV head count (and so the stage row stride) at compile time.
+template <int D, int G, int NT, int WPH, int TTOK, int PAR, int HKV>
 __global__ void __launch_bounds__(256 * PAR, 1)
 history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_log2) {
     using namespace mma_detail;
@@ -191,7 +201,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     constexpr int REC = C::REC, NG = C::NG, TT = TTOK, NR = C::NR;
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int Hkv = P.Hkv;
+    const int Hkv = HKV > 0 ? HKV : P.Hkv;
     const int nwarps = blockDim.x >> 5;
     const int pi = warp % PAR;                  // parity of the stages this warp consumes
     const int hw = warp / PAR;
@@ -200,11 +210,12 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     const int r = lane >> 2, j = lane & 3;
     const int g = P.g;
     const uint32_t NS = 1u << ns_log2;
-    const int row = trow;                       // stage row stride of one token (all heads)
+    const int row = HKV > 0 ? row_bytes(HKV * REC) : trow;   // stage row stride of one token (all heads)
     const int tok_bytes = Hkv * REC;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + 8;
     uint64_t* vmw = reinterpret_cast<uint64_t*>(smem + kSmemMask);      // [8 slots][2] validity masks
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemAbort);
     uint32_t* wtab = reinterpret_cast<uint32_t*>(smem + kSmemTab + warp * C::TBL);
     float* xb = reinterpret_cast<float*>(smem + x_off) + (h * PAR + pi) * C::XCH;
     unsigned char* stages = smem + stages_off;
@@ -254,13 +265,14 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         if (tc < tend && pit.t0 + tc < pit.t_end) nsl1 = pt[tc];
     };
     for (uint32_t i = threadIdx.x; i < 2 * NS; i += blockDim.x) vmw[i] = 0ull;
+    if (threadIdx.x == 0) *abort_flag = 0;
     __syncthreads();
 
     // copies of stage k (the stage at pit) by this warp
     auto issue = [&](uint32_t k) {
         const uint32_t s = k & (NS - 1);
         const uint32_t use = k >> ns_log2;
-        if (k >= NS) mbar_wait_bounded(&empty[s], (use - 1) & 1, P.status, budget);
+        if (k >= NS && !mbar_wait_bounded(&empty[s], (use - 1) & 1, P.status, budget)) *abort_flag = 1;
         const bool ok0 = nsl0 >= 0 && nsl0 < P.num_slots;
         const bool ok1 = nsl1 >= 0 && nsl1 < P.num_slots;
         if ((nsl0 != kNoTok && !ok0) || (nsl1 != kNoTok && !ok1)) set_status(P.status, OSCAR_DEV_BAD_SLOT);
@@ -299,9 +311,14 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     int xpar = 0;   // logit-exchange buffer parity; continuous across segments
     uint32_t k = 0; // stages consumed
 
+    // A pipeline wait that runs out of time sets the abort flag (and the device
+    // status).  Every warp checks the flag before each of its stages, the two
+    // channel-slice warps of a head agreeing on it through their named barrier;
+    // it then waits (bounded) for the copies it has issued and returns.
+    bool aborted = false;
     StageIter<TT> it;
     it.init(P, f0, f1);
-    while (it.valid(f1)) {
+    while (it.valid(f1) && !aborted) {
         const int b = it.b;
         // ---- per-segment query state ----
         uint32_t bq[NT][KS][2];
@@ -347,12 +364,18 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                 it.next(P, f1);
                 continue;
             }
+            int ab = *abort_flag;
+            if (WPH == 2) ab = named_bar_or(bar_id, 64, ab);
+            if (ab) {
+                aborted = true;
+                break;
+            }
             if (pit.valid(f1)) {                 // stage k + NS - PAR (this parity)
                 issue(pk);
                 pit_step();
             }
             const uint32_t s = k & (NS - 1);
-            mbar_wait_bounded(&full[s], (k >> ns_log2) & 1, P.status, budget);
+            if (!mbar_wait_bounded(&full[s], (k >> ns_log2) & 1, P.status, budget)) *abort_flag = 1;
             const uint64_t vmask = vmw[2 * s + ((k >> ns_log2) & 1)];
             const unsigned char* tb = stages + s * stage_bytes + h * REC;
             // ---------------- QK: MQ m16 tiles ----------------
@@ -630,6 +653,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
             it.next(P, f1);
         }
 
+        if (aborted) break;
         // ---------------- segment end: reduce and write the partial ----------------
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -682,6 +706,11 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
             }
         }
     }
+    if (aborted) {   // stages this warp issued but did not consume: k, k + PAR, ..., pk - PAR
+        long long drain = 2000000000LL;
+        for (uint32_t kk = k; kk < pk; kk += PAR)
+            mbar_wait_bounded(&full[kk & (NS - 1)], (kk >> ns_log2) & 1, P.status, drain);
+    }
 }
 
 // Shared-memory plan: (x_off, stages_off, ring depth log2, total bytes); false if it
@@ -700,14 +729,14 @@ static bool mma_smem_plan(int Hkv, int* x_off, int* stages_off, int* ns_log2, si
     return *total <= 225 * 1024;
 }
 
-template <int D, int G, int NT, int WPH, int TTOK, int PAR>
+template <int D, int G, int NT, int WPH, int TTOK, int PAR, int HKV>
 static int launch_mma(DecodeParams P, cudaStream_t st) {
     const int threads = 32 * P.Hkv * WPH * PAR;
     int x_off, stages_off, ns_log2;
     size_t smem;
     if (!mma_smem_plan<D, G, NT, WPH, TTOK, PAR>(P.Hkv, &x_off, &stages_off, &ns_log2, &smem))
         return OSCAR_ERR_ARG;
-    auto kern = history_mma_kernel<D, G, NT, WPH, TTOK, PAR>;
+    auto kern = history_mma_kernel<D, G, NT, WPH, TTOK, PAR, HKV>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return check_cuda("cudaFuncSetAttribute(history_mma_kernel)");
     const int grid = std::min(P.n_ctas, sm_count());
@@ -725,8 +754,8 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
     const int nt = (2 * P.g + 7) / 8;
     int rc = OSCAR_OK;
     // a variant is taken when its shared-memory plan fits; otherwise the next one is tried
-    auto go = [&](auto plan, auto fn, int par) {
-        if (*launched) return;
+    auto go = [&](auto plan, auto fn, int par, int hkv) {
+        if (*launched || (hkv > 0 && hkv != P.Hkv)) return;
         int xo, so, lg;
         size_t smem;
         if (!plan(P.Hkv, &xo, &so, &lg, &smem)) return;
@@ -734,13 +763,15 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
         rc = fn(P, st);
         *launched = true;
     };
-#define OSCAR_MMA(D_, G_, NT_, WPH_, TT_, PAR_) \
-    go(mma_smem_plan<D_, G_, NT_, WPH_, TT_, PAR_>, launch_mma<D_, G_, NT_, WPH_, TT_, PAR_>, PAR_)
+#define OSCAR_MMA_H(D_, G_, NT_, WPH_, TT_, PAR_, HKV_) \
+    go(mma_smem_plan<D_, G_, NT_, WPH_, TT_, PAR_>, launch_mma<D_, G_, NT_, WPH_, TT_, PAR_, HKV_>, PAR_, HKV_)
+#define OSCAR_MMA(D_, G_, NT_, WPH_, TT_, PAR_) OSCAR_MMA_H(D_, G_, NT_, WPH_, TT_, PAR_, 0)
     // one n8 column tile (g <= 4): two warps per (head, slice) on alternate stages;
     // two tiles: one warp, 32-token stages (register budget)
     if (head_dim == 128) {
         if (P.G == 64) {
-            if (nt == 1) { OSCAR_MMA(128, 64, 1, 1, 64, 2); OSCAR_MMA(128, 64, 1, 1, 64, 1); }
+            // 8 KV heads (Qwen3-8B-like layers): compile-time stage row stride
+            if (nt == 1) { OSCAR_MMA_H(128, 64, 1, 1, 64, 2, 8); OSCAR_MMA(128, 64, 1, 1, 64, 2); OSCAR_MMA(128, 64, 1, 1, 64, 1); }
             else OSCAR_MMA(128, 64, 2, 1, 32, 1);
         } else if (P.G == 128) {
             if (nt == 1) { OSCAR_MMA(128, 128, 1, 1, 64, 2); OSCAR_MMA(128, 128, 1, 1, 64, 1); }
@@ -759,6 +790,7 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
         }
     }
 #undef OSCAR_MMA
+#undef OSCAR_MMA_H
     if (*launched) P.n_ctas = std::min(P.n_ctas, sm_count());
     return rc;
 }
