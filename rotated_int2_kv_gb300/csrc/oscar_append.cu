@@ -101,6 +101,56 @@ __device__ __forceinline__ int find_request(const int* prefix, int batch, int u)
     return lo;
 }
 
+// Quantises one rotated head vector held by a warp (lane: channels lane·CPL ..
+// lane·CPL + CPL - 1) and writes its codes and (s, z) pairs into the record.
+template <int D>
+__device__ __forceinline__ void quantize_store(const AppendParams& P, const float (&y)[D / 32], int slot, int h,
+                                               int mat, int lane) {
+    constexpr int CPL = D / 32;
+    const int lpg = P.G / CPL;       // lanes per group (4..32)
+    const float r = P.clip;
+    const int rec_off_codes = mat ? D / 4 : 0;
+    const int ng = D / P.G;
+    const int rec_off_sz = D / 2 + (mat ? 4 * ng : 0);
+    float mn = y[0], mx = y[0];
+#pragma unroll
+    for (int j = 1; j < CPL; ++j) { mn = fminf(mn, y[j]); mx = fmaxf(mx, y[j]); }
+    for (int off = 1; off < lpg; off <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    const float lo = __fmul_rn(r, mn);
+    const float hi = __fmul_rn(r, mx);
+    const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 3.0f));
+    const __half z16 = __float2half_rn(lo);
+    const float s = __half2float(s16), z = __half2float(z16);
+    uint32_t bits = 0;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        uint32_t c = 0;
+        if (s != 0.0f) {
+            const float u = __fdiv_rn(__fsub_rn(y[j], z), s);
+            const float cr = fminf(fmaxf(rintf(u), 0.0f), 3.0f);
+            c = (uint32_t)cr;
+        }
+        bits |= c << (2 * j);
+    }
+    uint8_t* rec = P.records + ((int64_t)slot * P.Hkv + h) * P.rec_bytes;
+    if (CPL >= 4) {
+#pragma unroll
+        for (int bj = 0; bj < CPL / 4; ++bj)
+            rec[rec_off_codes + lane * (CPL / 4) + bj] = (uint8_t)(bits >> (8 * bj));
+    } else {  // CPL == 2: two lanes share a byte
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, bits, 1);
+        if ((lane & 1) == 0) rec[rec_off_codes + lane / 2] = (uint8_t)(bits | (other << 4));
+    }
+    if ((lane % lpg) == 0) {
+        const int gi = lane / lpg;
+        __half2 sz = __halves2half2(s16, z16);
+        *reinterpret_cast<__half2*>(rec + rec_off_sz + 4 * gi) = sz;
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads)
 quantize_kernel(AppendParams P) {
@@ -133,10 +183,6 @@ quantize_kernel(AppendParams P) {
         for (int i = tid * 4; i < D * D; i += kAppendThreads * 4)
             *reinterpret_cast<float4*>(sR + i) = *reinterpret_cast<const float4*>(R + i);
     }
-    const int rec_off_codes = mat ? D / 4 : 0;
-    const int ng = D / P.G;
-    const int rec_off_sz = D / 2 + (mat ? 4 * ng : 0);
-
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int64_t e0 = tile * kTileVec;
         const int nvec = (int)(total_vec - e0 < kTileVec ? total_vec - e0 : kTileVec);
@@ -271,8 +317,6 @@ quantize_kernel(AppendParams P) {
         __syncthreads();
         // ---- quantise: one warp per vector, D/32 contiguous channels per lane ----
         constexpr int CPL = D / 32;
-        const int lpg = P.G / CPL;       // lanes per group (4..32)
-        const float r = P.clip;
         for (int v = warp; v < nvec; v += kAppendThreads / 32) {
             const int slot = s_meta[v][3];
             if (slot < 0) continue;      // warp-uniform
@@ -280,83 +324,151 @@ quantize_kernel(AppendParams P) {
             float y[CPL];
 #pragma unroll
             for (int j = 0; j < CPL; ++j) y[j] = sY[v * kYStride + lane * CPL + j];
-            float mn = y[0], mx = y[0];
-#pragma unroll
-            for (int j = 1; j < CPL; ++j) { mn = fminf(mn, y[j]); mx = fmaxf(mx, y[j]); }
-            for (int off = 1; off < lpg; off <<= 1) {
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            }
-            const float lo = __fmul_rn(r, mn);
-            const float hi = __fmul_rn(r, mx);
-            const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 3.0f));
-            const __half z16 = __float2half_rn(lo);
-            const float s = __half2float(s16), z = __half2float(z16);
-            uint32_t bits = 0;
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-                uint32_t c = 0;
-                if (s != 0.0f) {
-                    const float u = __fdiv_rn(__fsub_rn(y[j], z), s);
-                    const float cr = fminf(fmaxf(rintf(u), 0.0f), 3.0f);
-                    c = (uint32_t)cr;
-                }
-                bits |= c << (2 * j);
-            }
-            uint8_t* rec = P.records + ((int64_t)slot * P.Hkv + h) * P.rec_bytes;
-            if (CPL >= 4) {
-#pragma unroll
-                for (int bj = 0; bj < CPL / 4; ++bj)
-                    rec[rec_off_codes + lane * (CPL / 4) + bj] = (uint8_t)(bits >> (8 * bj));
-            } else {  // CPL == 2: two lanes share a byte
-                const uint32_t other = __shfl_xor_sync(0xffffffffu, bits, 1);
-                if ((lane & 1) == 0) rec[rec_off_codes + lane / 2] = (uint8_t)(bits | (other << 4));
-            }
-            if ((lane % lpg) == 0) {
-                const int gi = lane / lpg;
-                __half2 sz = __halves2half2(s16, z16);
-                *reinterpret_cast<__half2*>(rec + rec_off_sz + 4 * gi) = sz;
-            }
+            quantize_store<D>(P, y, slot, h, mat, lane);
         }
         __syncthreads();
     }
 }
 
-// Copies each new row to the sink or the recent ring (bf16).  One block per row.
+// Small appends (decode steps): one warp per head vector entering the history,
+// 8 per block, so that a few hundred vectors still spread over many SMs.  The
+// warp rotates its vector with the same sequential fp32 FMA order over k as
+// quantize_kernel (bit-identical y), reading R through the L1 cache.
+constexpr int kSmallVec = kAppendThreads / 32;
+
+template <int D>
+__global__ void __launch_bounds__(kAppendThreads)
+quantize_small_kernel(AppendParams P) {
+    // R is staged in shared memory when it fits in 64 KB (d <= 128): every
+    // thread issues all of its loads at once, ahead of the request prefix
+    constexpr bool kResidentR = (D * D * 4 <= 64 * 1024);
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ float sx[kSmallVec][D];
+    float* sR = reinterpret_cast<float*>(smem);
+    int* prefix = reinterpret_cast<int*>(smem + (kResidentR ? D * D * 4 : 0));
+    int* scratch = prefix + P.batch + 1;
+    constexpr int CPL = D / 32;
+    const int mat = blockIdx.y;
+    const float* R = mat ? P.rot_v : P.rot_k;
+    const void* src_new = mat ? P.v : P.k;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (kResidentR) {
+        constexpr int NU = D * D / 4 / kAppendThreads;   // 16-byte copies per thread
+#pragma unroll
+        for (int u = 0; u < NU; ++u)
+            cp_async16(sR + 4 * (tid + kAppendThreads * u), R + 4 * (tid + kAppendThreads * u));
+        cp_async_commit();
+    }
+    build_prefix(P, prefix, scratch);
+    if (kResidentR) {
+        cp_async_wait<0>();
+        __syncthreads();
+    }
+    const float* Rs = kResidentR ? sR : R;
+    const int64_t total_vec = (int64_t)prefix[P.batch] * P.Hkv;
+    for (int64_t e = (int64_t)blockIdx.x * kSmallVec + warp; e < total_vec; e += (int64_t)gridDim.x * kSmallVec) {
+        // ---- resolve the vector (every lane, warp-uniform) ----
+        const int u = (int)(e / P.Hkv), h = (int)(e % P.Hkv);
+        const int b = find_request(prefix, P.batch, u);
+        const int L0 = P.start_pos[b];
+        const int p = hist_hi(L0, P.S, P.W) + (u - prefix[b]);
+        int slot = -1;
+        int bits = 0;
+        if (p >= P.pt_stride) {
+            bits |= OSCAR_DEV_BAD_LEN;
+        } else {
+            const int sl = P.page_table[(int64_t)b * P.pt_stride + p];
+            if (sl < 0 || sl >= P.num_slots) bits |= OSCAR_DEV_BAD_SLOT;
+            else slot = sl;
+        }
+        const int rq = P.req_idx ? P.req_idx[b] : b;
+        if (p < L0 && (rq < 0 || rq >= P.max_reqs)) {
+            bits |= OSCAR_DEV_BAD_REQ;
+            slot = -1;
+        }
+        const int64_t t = (int64_t)P.cu_new[b] + (p - L0);
+        if (p >= L0 && t >= P.total_new) {
+            bits |= OSCAR_DEV_BAD_LEN;
+            slot = -1;
+        }
+        if (bits && lane == 0) set_status(P.status, bits);
+        if (slot < 0) continue;
+        // ---- x (bf16-rounded): lane holds channels lane·CPL .. ----
+        float x[CPL];
+        if (p < L0) {
+            const uint16_t* rowp = P.recent + ((((int64_t)rq * P.W + p % P.W) * P.Hkv + h) * 2 + mat) * D + lane * CPL;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) x[j] = bf16_bits_to_f32(rowp[j]);
+        } else {
+            const int64_t base = (t * P.Hkv + h) * D + lane * CPL;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) x[j] = bf16_bits_to_f32(f32_to_bf16_bits(load_elem(src_new, base + j, P.kv_dtype)));
+        }
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) sx[warp][lane * CPL + j] = x[j];
+        __syncwarp();
+        // ---- y = x · R, sequential over k ----
+        float y[CPL];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) y[j] = 0.f;
+#pragma unroll 8
+        for (int k = 0; k < D; ++k) {
+            const float xk = sx[warp][k];
+            const float* rr = Rs + (int64_t)k * D + lane * CPL;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) y[j] = fmaf(xk, rr[j], y[j]);
+        }
+        __syncwarp();
+        quantize_store<D>(P, y, slot, h, mat, lane);
+    }
+}
+
+// Copies each new row to the sink or the recent ring (bf16).  Block (b, y)
+// handles rows y, y + gridDim.y, ... of request b; every thread issues a batch
+// of loads before its stores.
 template <int D>
 __global__ void __launch_bounds__(128)
-window_copy_kernel(AppendParams P, int64_t total_new) {
-    __shared__ int s_b;
-    for (int64_t t = blockIdx.x; t < total_new; t += gridDim.x) {
-        if (threadIdx.x == 0) {
-            int lo = 0, hi = P.batch - 1;  // last b with cu_new[b] <= t
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (P.cu_new[mid] <= t) lo = mid; else hi = mid - 1;
-            }
-            s_b = lo;
+window_copy_kernel(AppendParams P) {
+    const int b = blockIdx.x;
+    const int L0 = P.start_pos[b];
+    const int c0 = P.cu_new[b], c1 = P.cu_new[b + 1];
+    const int n = c1 - c0;
+    if (L0 < 0 || n <= 0) return;
+    const int rq = P.req_idx ? P.req_idx[b] : b;
+    if (rq < 0 || rq >= P.max_reqs) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) set_status(P.status, OSCAR_DEV_BAD_REQ);
+        return;
+    }
+    const int L1 = L0 + n;
+    const int hh = hist_hi(L1, P.S, P.W);
+    const int nel = P.Hkv * 2 * D;
+    constexpr int kU = 8;
+    for (int r = blockIdx.y; r < n; r += gridDim.y) {
+        const int64_t t = (int64_t)c0 + r;
+        if (t >= P.total_new) {
+            if (threadIdx.x == 0) set_status(P.status, OSCAR_DEV_BAD_LEN);
+            break;
         }
-        __syncthreads();
-        const int b = s_b;
-        __syncthreads();
-        const int L0 = P.start_pos[b];
-        const int n = P.cu_new[b + 1] - P.cu_new[b];
-        if (L0 < 0 || n < 0) continue;
-        const int p = L0 + (int)(t - P.cu_new[b]);
-        const int L1 = L0 + n;
+        const int p = L0 + r;
         uint16_t* dst = nullptr;
-        const int rq = P.req_idx ? P.req_idx[b] : b;
-        if (rq < 0 || rq >= P.max_reqs) {
-            if (threadIdx.x == 0) set_status(P.status, OSCAR_DEV_BAD_REQ);
-            continue;
-        }
-        if (p < P.S) dst = P.sink + ((int64_t)rq * P.S + p) * P.Hkv * 2 * D;
-        else if (p >= hist_hi(L1, P.S, P.W)) dst = P.recent + ((int64_t)rq * P.W + p % P.W) * P.Hkv * 2 * D;
+        if (p < P.S) dst = P.sink + ((int64_t)rq * P.S + p) * nel;
+        else if (p >= hh) dst = P.recent + ((int64_t)rq * P.W + p % P.W) * nel;
         if (!dst) continue;
-        for (int i = threadIdx.x; i < P.Hkv * 2 * D; i += blockDim.x) {
-            const int h = i / (2 * D), mat = (i / D) & 1, c = i % D;
-            const void* src = mat ? P.v : P.k;
-            dst[i] = f32_to_bf16_bits(load_elem(src, (t * P.Hkv + h) * D + c, P.kv_dtype));
+        for (int i0 = 0; i0 < nel; i0 += 128 * kU) {
+            float x[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = i0 + threadIdx.x + 128 * u;
+                if (i < nel) {
+                    const int h = i / (2 * D), mat = (i / D) & 1, c = i % D;
+                    x[u] = load_elem(mat ? P.v : P.k, (t * P.Hkv + h) * D + c, P.kv_dtype);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = i0 + threadIdx.x + 128 * u;
+                if (i < nel) dst[i] = f32_to_bf16_bits(x[u]);
+            }
         }
     }
 }
@@ -372,15 +484,27 @@ static int launch_append(const AppendParams& P, int64_t total_new, cudaStream_t 
     auto kern = quantize_kernel<D>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return check_cuda("cudaFuncSetAttribute(quantize_kernel)");
-    // Upper bound of the vectors entering the history: every new row plus
-    // every row that can leave the ring.
-    const int64_t max_units = total_new + (int64_t)P.batch * P.W;
+    // Upper bound of the vectors entering the history: a request of L0 cached
+    // and n new tokens moves max(S, L0+n-W) - max(S, L0-W) <= n positions.
+    const int64_t max_units = total_new;
     const int64_t max_tiles = (max_units * P.Hkv + kTileVec - 1) / kTileVec;
     // blockIdx.y selects K or V, so the two halves together fill every SM
     // with its resident CTAs (2 per SM when R stays in shared memory).
     const int per_sm = kResidentR ? 2 : 1;
     const int64_t grid_x = std::max<int64_t>(1, std::min<int64_t>(max_tiles, (int64_t)sm_count() * per_sm / 2));
-    if (max_tiles > 0) {
+    const int64_t max_vec = max_units * P.Hkv;
+    if (max_vec > 0 && max_vec <= (int64_t)sm_count() * kTileVec) {
+        // few vectors (decode steps): one warp per vector over many blocks
+        const size_t ssmem = (size_t)(P.batch + 1 + kAppendThreads) * 4 + (D * D * 4 <= 64 * 1024 ? D * D * 4 : 0);
+        if (cudaFuncSetAttribute(quantize_small_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem) != cudaSuccess)
+            return check_cuda("cudaFuncSetAttribute(quantize_small_kernel)");
+        const int64_t gs = std::min<int64_t>((max_vec + kSmallVec - 1) / kSmallVec, (int64_t)sm_count() * 4);
+        const int prof = prof_begin(1, stream);
+        quantize_small_kernel<D><<<dim3((unsigned)gs, 2), kAppendThreads, ssmem, stream>>>(P);
+        prof_end(prof, stream);
+        int rc = check_cuda("quantize_small_kernel launch");
+        if (rc) return rc;
+    } else if (max_tiles > 0) {
         const int prof = prof_begin(1, stream);
         kern<<<dim3((unsigned)grid_x, 2), kAppendThreads, smem, stream>>>(P);
         prof_end(prof, stream);
@@ -388,8 +512,10 @@ static int launch_append(const AppendParams& P, int64_t total_new, cudaStream_t 
         if (rc) return rc;
     }
     if (total_new > 0) {
-        const int64_t grid = std::min<int64_t>(total_new, (int64_t)sm_count() * 8);
-        window_copy_kernel<D><<<(unsigned)grid, 128, 0, stream>>>(P, total_new);
+        // rows per request are not known on the host: spread each request over up
+        // to ceil(total_new / batch) blocks (at least 1, at most 64)
+        const int64_t gy = std::max<int64_t>(1, std::min<int64_t>(64, (total_new + P.batch - 1) / P.batch));
+        window_copy_kernel<D><<<dim3((unsigned)P.batch, (unsigned)gy), 128, 0, stream>>>(P);
         int rc = check_cuda("window_copy_kernel launch");
         if (rc) return rc;
     }

@@ -46,11 +46,21 @@ __device__ __forceinline__ bool request_valid(const DecodeParams& P, int b, int*
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
+    // R_K is staged in shared memory (all 16-byte copies in flight at once)
+    // when it fits in 64 KB (d <= 128)
+    constexpr bool kResidentR = (D * D * 4 <= 64 * 1024);
+    extern __shared__ __align__(16) float s_rk[];
     __shared__ float sq[16][D];
     __shared__ float sqt[16][D];
     __shared__ int scan[256];
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
+    if (kResidentR) {
+#pragma unroll
+        for (int u = 0; u < D * D / 4 / 256; ++u)
+            cp_async16(s_rk + 4 * (tid + 256 * u), P.rot_k + 4 * (tid + 256 * u));
+        cp_async_commit();
+    }
     if (b == 0 && blockIdx.y == 0) {
         // chunk prefix over all requests (re-derives validity locally)
         const int per = (P.batch + 255) / 256;
@@ -95,20 +105,30 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
         __syncthreads();
         for (int i = tid; i < nh * D; i += 256)
             sq[i / D][i % D] = load_elem(P.q, ((int64_t)b * P.Hq + h0 + i / D) * D + i % D, P.q_dtype);
+        if (kResidentR) cp_async_wait<0>();
         __syncthreads();
-        for (int col = tid; col < D; col += 256) {
-            float acc[16];
+        const float* RK = kResidentR ? s_rk : P.rot_k;
+        // thread (column, head half): 16 loads of R_K in flight per batch of k
+        constexpr int kHalves = 256 / D > 1 ? 256 / D : 1;   // threads per column
+        constexpr int kHPT = 16 / kHalves;                   // heads per thread
+        for (int ci = tid; ci < D * kHalves; ci += 256) {
+            const int col = ci % D, hb = (ci / D) * kHPT;
+            float acc[kHPT];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-            for (int k = 0; k < D; ++k) {
-                const float r = P.rot_k[(int64_t)k * D + col];
+            for (int j = 0; j < kHPT; ++j) acc[j] = 0.f;
+            for (int k0 = 0; k0 < D; k0 += 16) {
+                float r[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc[j] = fmaf(sq[j][k], r, acc[j]);
+                for (int u = 0; u < 16; ++u) r[u] = RK[(int64_t)(k0 + u) * D + col];
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+#pragma unroll
+                    for (int j = 0; j < kHPT; ++j) acc[j] = fmaf(sq[hb + j][k0 + u], r[u], acc[j]);
             }
-            for (int j = 0; j < nh; ++j) {
+            for (int j = 0; j < kHPT && hb + j < nh; ++j) {
                 const float v = acc[j] * P.qscale;
-                sqt[j][col] = v;
-                P.qt[((int64_t)b * P.Hq + h0 + j) * D + col] = v;
+                sqt[hb + j][col] = v;
+                P.qt[((int64_t)b * P.Hq + h0 + hb + j) * D + col] = v;
             }
         }
         __syncthreads();
@@ -408,18 +428,34 @@ __global__ void __launch_bounds__(kCombThreads) window_kernel(DecodeParams P) {
     }
     for (int i = tid; i < g * D; i += kCombThreads)
         sq[i] = load_elem(P.q, ((int64_t)b * P.Hq + hk * g) * D + i, P.q_dtype) * P.qscale;
-    for (int i = tid; i < nt * (D / 8); i += kCombThreads) {
-        const int t = i / (D / 8), c8 = i % (D / 8);
-        const int tt = t0 + t;
-        const uint16_t* base = (tt < sink_end)
-            ? P.sink + (((int64_t)rq * S + tt) * P.Hkv + hk) * 2 * D
-            : P.recent + (((int64_t)rq * W + (rec_lo + tt - sink_end) % W) * P.Hkv + hk) * 2 * D;
-        const uint4 kq = *reinterpret_cast<const uint4*>(base + c8 * 8);
-        const uint4 vq = *reinterpret_cast<const uint4*>(base + D + c8 * 8);
-        uint32_t* kd = sk + t * kRowW + c8 * 4;
-        uint32_t* vd = sv + t * kRowW + c8 * 4;
-        kd[0] = kq.x; kd[1] = kq.y; kd[2] = kq.z; kd[3] = kq.w;
-        vd[0] = vq.x; vd[1] = vq.y; vd[2] = vq.z; vd[3] = vq.w;
+    {   // stage the tile: every thread issues all of its 16-byte loads before storing
+        constexpr int C8 = D / 8;                       // 16-byte chunks per K (or V) row
+        constexpr int NU = kWinTile * C8 / kCombThreads;
+        uint4 kq[NU], vq[NU];
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+            const int i = tid + kCombThreads * u;
+            const int t = i / C8, c8 = i % C8;
+            const int tt = t0 + t;
+            if (t < nt) {
+                const uint16_t* base = (tt < sink_end)
+                    ? P.sink + (((int64_t)rq * S + tt) * P.Hkv + hk) * 2 * D
+                    : P.recent + (((int64_t)rq * W + (rec_lo + tt - sink_end) % W) * P.Hkv + hk) * 2 * D;
+                kq[u] = *reinterpret_cast<const uint4*>(base + c8 * 8);
+                vq[u] = *reinterpret_cast<const uint4*>(base + D + c8 * 8);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+            const int i = tid + kCombThreads * u;
+            const int t = i / C8, c8 = i % C8;
+            if (t < nt) {
+                uint32_t* kd = sk + t * kRowW + c8 * 4;
+                uint32_t* vd = sv + t * kRowW + c8 * 4;
+                kd[0] = kq[u].x; kd[1] = kq[u].y; kd[2] = kq[u].z; kd[3] = kq[u].w;
+                vd[0] = vq[u].x; vd[1] = vq[u].y; vd[2] = vq[u].z; vd[3] = vq[u].w;
+            }
+        }
     }
     __syncthreads();
     for (int i = tid; i < nt * g; i += kCombThreads) {     // logits: thread per (token, head)
@@ -546,17 +582,30 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams P) {
     for (int i = tid; i < g * D; i += kCombThreads) {
         const int j = i / D, c = i % D;
         const int hq = hk * g + j;
+        // batches of 8 predicated loads in flight (a zero weight skips its load)
         float ap = 0.f;
         const int64_t wb = ((int64_t)b * P.Hq + hq) * nwt;
-        for (int t = 0; t < nwt; ++t) {
-            const float w = sww[j * nwt + t];
-            if (w > 0.f) ap = fmaf(w, P.wo[(wb + t) * D + c], ap);
+        for (int t0 = 0; t0 < nwt; t0 += 8) {
+            float x[8], w[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                w[u] = t0 + u < nwt ? sww[j * nwt + t0 + u] : 0.f;
+                x[u] = w[u] > 0.f ? P.wo[(wb + t0 + u) * D + c] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) ap = fmaf(w[u], x[u], ap);
         }
         spl[i] = ap;
         float ar = 0.f;
-        for (int u = 0; u < nsl; ++u) {
-            const float w = swr[j * swr_stride + u];
-            if (w > 0.f) ar = fmaf(w, P.po[((sl0 + u) * P.Hq + hq) * D + c], ar);
+        for (int u0 = 0; u0 < nsl; u0 += 8) {
+            float x[8], w[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                w[u] = u0 + u < nsl ? swr[j * swr_stride + u0 + u] : 0.f;
+                x[u] = w[u] > 0.f ? P.po[((sl0 + u0 + u) * P.Hq + hq) * D + c] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) ar = fmaf(w[u], x[u], ar);
         }
         srot[i] = ar;
     }
@@ -567,13 +616,19 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams P) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) accj[j] = 0.f;
         const float4* rrow = reinterpret_cast<const float4*>(P.rot_v + (int64_t)c * D);
-        for (int k4 = 0; k4 < D / 4; ++k4) {
-            const float4 rv = rrow[k4];
+        constexpr int kB = D / 4 < 8 ? D / 4 : 8;      // row loads in flight per batch
+        for (int k0 = 0; k0 < D / 4; k0 += kB) {
+            float4 rv[kB];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                if (j < g) {
-                    const float* x = srot + j * D + 4 * k4;
-                    accj[j] = fmaf(x[0], rv.x, fmaf(x[1], rv.y, fmaf(x[2], rv.z, fmaf(x[3], rv.w, accj[j]))));
+            for (int u = 0; u < kB; ++u) rv[u] = rrow[k0 + u];
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    if (j < g) {
+                        const float* x = srot + j * D + 4 * (k0 + u);
+                        accj[j] = fmaf(x[0], rv[u].x, fmaf(x[1], rv[u].y, fmaf(x[2], rv[u].z, fmaf(x[3], rv[u].w, accj[j]))));
+                    }
                 }
             }
         }
@@ -629,7 +684,10 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
 
 template <int D>
 static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
-    prep_kernel<D><<<dim3(P.batch, (P.Hq + 15) / 16), 256, 0, st>>>(P);
+    const size_t psmem = D * D * 4 <= 64 * 1024 ? (size_t)D * D * 4 : 0;
+    if (psmem && cudaFuncSetAttribute(prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem) != cudaSuccess)
+        return check_cuda("cudaFuncSetAttribute(prep_kernel)");
+    prep_kernel<D><<<dim3(P.batch, (P.Hq + 15) / 16), 256, psmem, st>>>(P);
     int rc = check_cuda("prep_kernel launch");
     if (rc) return rc;
     const size_t wsmem = ((size_t)P.g * D + (size_t)P.g * kWinTile + 2 * P.g) * 4 +
