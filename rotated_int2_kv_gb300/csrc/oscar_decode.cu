@@ -44,14 +44,16 @@ __device__ __forceinline__ bool request_valid(const DecodeParams& P, int b, int*
 // fp16 hi/lo split (of q̃/α) packed as mma B fragments, the per-group sums,
 // the effective length / window row, and (block 0) the chunk prefix.
 // ---------------------------------------------------------------------------
+constexpr int kPrepHeads = 8;     // query heads per prep block
+
 template <int D>
 __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
     // R_K is staged in shared memory (all 16-byte copies in flight at once)
     // when it fits in 64 KB (d <= 128)
     constexpr bool kResidentR = (D * D * 4 <= 64 * 1024);
     extern __shared__ __align__(16) float s_rk[];
-    __shared__ float sq[16][D];
-    __shared__ float sqt[16][D];
+    __shared__ float sq[kPrepHeads][D];
+    __shared__ float sqt[kPrepHeads][D];
     __shared__ int scan[256];
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
@@ -100,8 +102,8 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
         }
     }
     {
-        const int h0 = blockIdx.y * 16;
-        const int nh = min(16, P.Hq - h0);
+        const int h0 = blockIdx.y * kPrepHeads;
+        const int nh = min(kPrepHeads, P.Hq - h0);
         __syncthreads();
         for (int i = tid; i < nh * D; i += 256)
             sq[i / D][i % D] = load_elem(P.q, ((int64_t)b * P.Hq + h0 + i / D) * D + i % D, P.q_dtype);
@@ -110,7 +112,7 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
         const float* RK = kResidentR ? s_rk : P.rot_k;
         // thread (column, head half): 16 loads of R_K in flight per batch of k
         constexpr int kHalves = 256 / D > 1 ? 256 / D : 1;   // threads per column
-        constexpr int kHPT = 16 / kHalves;                   // heads per thread
+        constexpr int kHPT = kPrepHeads / kHalves;           // heads per thread
         for (int ci = tid; ci < D * kHalves; ci += 256) {
             const int col = ci % D, hb = (ci / D) * kHPT;
             float acc[kHPT];
@@ -399,7 +401,8 @@ __global__ void __launch_bounds__(512) history_simt_kernel(DecodeParams P) {
 // padded to an odd number of words), logits in fp32 against the unrotated q,
 // and the tile's (m, l, o) partial is written for the combine.
 // ---------------------------------------------------------------------------
-constexpr int kCombThreads = 128;
+constexpr int kCombThreads = 128;      // window kernel
+constexpr int kMergeThreads = 512;     // combine kernel
 constexpr int kWinTile = 64;
 
 template <int D>
@@ -458,18 +461,29 @@ __global__ void __launch_bounds__(kCombThreads) window_kernel(DecodeParams P) {
         }
     }
     __syncthreads();
-    for (int i = tid; i < nt * g; i += kCombThreads) {     // logits: thread per (token, head)
-        const int t = i % nt, j = i / nt;
-        const uint32_t* kr = sk + t * kRowW;
-        const float* qj = sq + j * D;
-        float acc = 0.f;
+    // logits: thread per (token, head pair j, j + hs); two heads share the K row
+    // loads and each dot product runs as two independent chains
+    {
+        const int hs = (g + 1) / 2;
+        for (int i = tid; i < nt * hs; i += kCombThreads) {
+            const int t = i % nt, j = i / nt;
+            const bool two_h = j + hs < g;
+            const uint32_t* kr = sk + t * kRowW;
+            const float* qa = sq + j * D;
+            const float* qb = sq + (two_h ? j + hs : j) * D;
+            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll 8
-        for (int w = 0; w < D / 2; ++w) {
-            const uint32_t two = kr[w];
-            acc = fmaf(qj[2 * w], __uint_as_float(two << 16), acc);
-            acc = fmaf(qj[2 * w + 1], __uint_as_float(two & 0xFFFF0000u), acc);
+            for (int w = 0; w < D / 2; ++w) {
+                const uint32_t two = kr[w];
+                const float k0 = __uint_as_float(two << 16), k1 = __uint_as_float(two & 0xFFFF0000u);
+                a0 = fmaf(qa[2 * w], k0, a0);
+                a1 = fmaf(qa[2 * w + 1], k1, a1);
+                b0 = fmaf(qb[2 * w], k0, b0);
+                b1 = fmaf(qb[2 * w + 1], k1, b1);
+            }
+            sp[j * kWinTile + t] = a0 + a1;
+            if (two_h) sp[(j + hs) * kWinTile + t] = b0 + b1;
         }
-        sp[j * kWinTile + t] = acc;
     }
     __syncthreads();
     for (int j = warp; j < g; j += kCombThreads / 32) {    // softmax of the tile, per head
@@ -490,18 +504,32 @@ __global__ void __launch_bounds__(kCombThreads) window_kernel(DecodeParams P) {
         }
     }
     __syncthreads();
-    for (int i = tid; i < g * (D / 2); i += kCombThreads) {   // P·V: thread per (head, channel pair)
-        const int j = i / (D / 2), w = i % (D / 2);
-        float x0 = 0.f, x1 = 0.f;
-        const float* pj = sp + j * kWinTile;
-        for (int t = 0; t < nt; ++t) {
-            const uint32_t two = sv[t * kRowW + w];
-            x0 = fmaf(pj[t], __uint_as_float(two << 16), x0);
-            x1 = fmaf(pj[t], __uint_as_float(two & 0xFFFF0000u), x1);
+    {   // P·V: thread per (head pair j, j + hs; channel pair), sharing the V loads
+        const int hs = (g + 1) / 2;
+        for (int i = tid; i < hs * (D / 2); i += kCombThreads) {
+            const int j = i / (D / 2), w = i % (D / 2);
+            const bool two_h = j + hs < g;
+            float x0 = 0.f, x1 = 0.f, y0 = 0.f, y1 = 0.f;
+            const float* pa = sp + j * kWinTile;
+            const float* pb = sp + (two_h ? j + hs : j) * kWinTile;
+#pragma unroll 4
+            for (int t = 0; t < nt; ++t) {
+                const uint32_t two = sv[t * kRowW + w];
+                const float v0 = __uint_as_float(two << 16), v1 = __uint_as_float(two & 0xFFFF0000u);
+                x0 = fmaf(pa[t], v0, x0);
+                x1 = fmaf(pa[t], v1, x1);
+                y0 = fmaf(pb[t], v0, y0);
+                y1 = fmaf(pb[t], v1, y1);
+            }
+            float* o = P.wo + (pbase + (int64_t)j * P.n_win_tiles) * D;
+            o[2 * w] = x0;
+            o[2 * w + 1] = x1;
+            if (two_h) {
+                float* o2 = P.wo + (pbase + (int64_t)(j + hs) * P.n_win_tiles) * D;
+                o2[2 * w] = y0;
+                o2[2 * w + 1] = y1;
+            }
         }
-        float* o = P.wo + (pbase + (int64_t)j * P.n_win_tiles) * D;
-        o[2 * w] = x0;
-        o[2 * w + 1] = x1;
     }
 }
 
@@ -512,7 +540,7 @@ __global__ void __launch_bounds__(kCombThreads) window_kernel(DecodeParams P) {
 //   out = (e^{m_p-M}·Σ_bf16 p v + e^{m_r-M}·(Σ_hist p v̂)·R_Vᵀ) / (e^{m_p-M} l_p + e^{m_r-M} l_r).
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams P) {
+__global__ void __launch_bounds__(kMergeThreads) combine_kernel(DecodeParams P) {
     extern __shared__ __align__(16) float s_c[];
     const int hk = blockIdx.x, b = blockIdx.y;
     const int g = P.g;
@@ -520,7 +548,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams P) {
     const int L = P.len[b];
     float* outp = P.out + ((int64_t)b * P.Hq + hk * g) * D;
     if (L <= 0) {
-        for (int i = tid; i < g * D; i += kCombThreads) outp[i] = 0.f;
+        for (int i = tid; i < g * D; i += kMergeThreads) outp[i] = 0.f;
         return;
     }
     const int64_t N = P.cprefix[P.batch];
@@ -537,7 +565,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams P) {
     float* sww = sst + 4 * g;                      // [g][nwt] window tile weights
     float* swr = sww + g * nwt;                    // [g][P.n_ctas·par + 2] history partial weights
     const int swr_stride = (P.n_ctas << psh) + 2;
-    for (int j = warp; j < g; j += kCombThreads / 32) {
+    for (int j = warp; j < g; j += kMergeThreads / 32) {
         const int hq = hk * g + j;
         const float2* wml = P.wml + ((int64_t)b * P.Hq + hq) * nwt;
         float Mp = -INFINITY, Mr = -INFINITY;
@@ -579,7 +607,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams P) {
         }
     }
     __syncthreads();
-    for (int i = tid; i < g * D; i += kCombThreads) {
+    for (int i = tid; i < g * D; i += kMergeThreads) {
         const int j = i / D, c = i % D;
         const int hq = hk * g + j;
         // batches of 8 predicated loads in flight (a zero weight skips its load)
@@ -610,12 +638,13 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams P) {
         srot[i] = ar;
     }
     __syncthreads();
-    // (Σ_hist p v̂)·R_Vᵀ : (x·R_Vᵀ)[c] = Σ_k x[k]·R_V[c][k]; thread per channel c
-    for (int c = tid; c < D; c += kCombThreads) {
-        float accj[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) accj[j] = 0.f;
+    // (Σ_hist p v̂)·R_Vᵀ : (x·R_Vᵀ)[c] = Σ_k x[k]·R_V[c][k]; thread per (channel c,
+    // head j): the threads of one channel share its R_V row through L1
+    for (int i = tid; i < g * D; i += kMergeThreads) {
+        const int c = i % D, j = i / D;
         const float4* rrow = reinterpret_cast<const float4*>(P.rot_v + (int64_t)c * D);
+        const float* x = srot + j * D;
+        float a0 = 0.f, a1 = 0.f;
         constexpr int kB = D / 4 < 8 ? D / 4 : 8;      // row loads in flight per batch
         for (int k0 = 0; k0 < D / 4; k0 += kB) {
             float4 rv[kB];
@@ -623,24 +652,16 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams P) {
             for (int u = 0; u < kB; ++u) rv[u] = rrow[k0 + u];
 #pragma unroll
             for (int u = 0; u < kB; ++u) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    if (j < g) {
-                        const float* x = srot + j * D + 4 * (k0 + u);
-                        accj[j] = fmaf(x[0], rv[u].x, fmaf(x[1], rv[u].y, fmaf(x[2], rv[u].z, fmaf(x[3], rv[u].w, accj[j]))));
-                    }
-                }
+                const float* xk = x + 4 * (k0 + u);
+                a0 = fmaf(xk[0], rv[u].x, fmaf(xk[1], rv[u].y, a0));
+                a1 = fmaf(xk[2], rv[u].z, fmaf(xk[3], rv[u].w, a1));
             }
         }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            if (j >= g) break;
-            const float mp = sst[j * 4 + 0], lp = sst[j * 4 + 1], mr = sst[j * 4 + 2], lr = sst[j * 4 + 3];
-            const float Mx = fmaxf(mp, mr);
-            const float wp = lp > 0.f ? exp2f(mp - Mx) : 0.f;
-            const float wr = lr > 0.f ? exp2f(mr - Mx) : 0.f;
-            outp[j * D + c] = (wp * spl[j * D + c] + wr * accj[j]) / (wp * lp + wr * lr);
-        }
+        const float mp = sst[j * 4 + 0], lp = sst[j * 4 + 1], mr = sst[j * 4 + 2], lr = sst[j * 4 + 3];
+        const float Mx = fmaxf(mp, mr);
+        const float wp = lp > 0.f ? exp2f(mp - Mx) : 0.f;
+        const float wr = lr > 0.f ? exp2f(mr - Mx) : 0.f;
+        outp[j * D + c] = (wp * spl[j * D + c] + wr * (a0 + a1)) / (wp * lp + wr * lr);
     }
 }
 
@@ -687,7 +708,7 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
     const size_t psmem = D * D * 4 <= 64 * 1024 ? (size_t)D * D * 4 : 0;
     if (psmem && cudaFuncSetAttribute(prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem) != cudaSuccess)
         return check_cuda("cudaFuncSetAttribute(prep_kernel)");
-    prep_kernel<D><<<dim3(P.batch, (P.Hq + 15) / 16), 256, psmem, st>>>(P);
+    prep_kernel<D><<<dim3(P.batch, (P.Hq + kPrepHeads - 1) / kPrepHeads), 256, psmem, st>>>(P);
     int rc = check_cuda("prep_kernel launch");
     if (rc) return rc;
     const size_t wsmem = ((size_t)P.g * D + (size_t)P.g * kWinTile + 2 * P.g) * 4 +
@@ -728,7 +749,7 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
                           (size_t)P.g * ((size_t)P.n_ctas * P.par + 2)) * 4;
     if (cudaFuncSetAttribute(combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem) != cudaSuccess)
         return check_cuda("cudaFuncSetAttribute(combine_kernel)");
-    combine_kernel<D><<<dim3(P.Hkv, P.batch), kCombThreads, csmem, st>>>(P);
+    combine_kernel<D><<<dim3(P.Hkv, P.batch), kMergeThreads, csmem, st>>>(P);
     return check_cuda("combine_kernel launch");
 }
 

@@ -86,6 +86,16 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// c = A·B (no accumulator input: the zero C operand needs no register moves).
+__device__ __forceinline__ void mma16816_first(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
 // Packs (x0, x1) as fp16 hi parts, or as the lo parts x - fp16(x) when lo is set.
 __device__ __forceinline__ uint32_t pack_part(float x0, float x1, bool lo) {
     __half2 h = __floats2half2_rn(x0, x1);
@@ -383,15 +393,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
 #pragma unroll
             for (int mh = 0; mh < MQ; mh += 2) {   // two m16 tiles at a time (register budget)
                 constexpr int MB = MQ < 2 ? MQ : 2;
-                float sc[MB][GW][NT][4];
-#pragma unroll
-                for (int mb = 0; mb < MB; ++mb)
-#pragma unroll
-                    for (int gi = 0; gi < GW; ++gi)
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) sc[mb][gi][nt][e] = 0.f;
+                float sc[MB][GW][NT][4];     // set by the first k-step of each group
 #pragma unroll
                 for (int k4 = 0; k4 < KS; k4 += 4) {
 #pragma unroll
@@ -424,8 +426,12 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                                     x2 = code_pos<slot_pos(3, 1)>(d0, r0, l0); x3 = code_pos<slot_pos(3, 1)>(d1, r1, l1);
                                 }
 #pragma unroll
-                                for (int nt = 0; nt < NT; ++nt)
-                                    mma16816(sc[mb][gi][nt], x0, x1, x2, x3, bq[nt][k4 + q][0], bq[nt][k4 + q][1]);
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    if ((k4 + q) * 16 % G == 0)
+                                        mma16816_first(sc[mb][gi][nt], x0, x1, x2, x3, bq[nt][k4 + q][0], bq[nt][k4 + q][1]);
+                                    else
+                                        mma16816(sc[mb][gi][nt], x0, x1, x2, x3, bq[nt][k4 + q][0], bq[nt][k4 + q][1]);
+                                }
                             }
                         } else {
                             const uint4 w0 = *reinterpret_cast<const uint4*>(w_r);
@@ -440,8 +446,12 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                                 const uint32_t x0 = code_q16(y0), x1 = code_q16(y1);   // channels 2j, 2j+8
                                 const uint32_t x2 = code_q4(y0), x3 = code_q4(y1);     // channels 2j+1, 2j+9
 #pragma unroll
-                                for (int nt = 0; nt < NT; ++nt)
-                                    mma16816(sc[mb][gi][nt], x0, x1, x2, x3, bq[nt][kk][0], bq[nt][kk][1]);
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    if (kk * 16 % G == 0)
+                                        mma16816_first(sc[mb][gi][nt], x0, x1, x2, x3, bq[nt][kk][0], bq[nt][kk][1]);
+                                    else
+                                        mma16816(sc[mb][gi][nt], x0, x1, x2, x3, bq[nt][kk][0], bq[nt][kk][1]);
+                                }
                             }
                         }
                     }
