@@ -248,7 +248,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     const int tbeg = min(TT, hw * tpw), tend = min(TT, tbeg + tpw);
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < NS; ++s) {
-            mbar_init(&full[s], npw);
+            mbar_init(&full[s], npw * 32);
             mbar_init(&empty[s], npw);
         }
         fence_mbar_init();
@@ -292,14 +292,40 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
             const uint64_t bits = ((uint64_t)b0 | ((uint64_t)b1 << 32)) << tbeg;
             if (bits) atomicOr(reinterpret_cast<unsigned long long*>(&vmw[2 * s + (use & 1)]),
                                (unsigned long long)bits);
-            // one bulk copy (TMA engine) per token record; the byte count is posted
-            // on the stage's full barrier before the copies are issued
-            mbar_arrive_expect_tx(&full[s], (uint32_t)((__popc(b0) + __popc(b1)) * tok_bytes));
         }
-        __syncwarp();
         unsigned char* dst = stages + s * stage_bytes;
-        if (ok0) bulk_g2s(dst + (tbeg + lane) * row, P.records + (int64_t)nsl0 * tok_bytes, (uint32_t)tok_bytes, &full[s]);
-        if (ok1) bulk_g2s(dst + (tbeg + 32 + lane) * row, P.records + (int64_t)nsl1 * tok_bytes, (uint32_t)tok_bytes, &full[s]);
+        // 16-byte cp.async of whole token records, completing on the stage's full
+        // barrier through every thread's no-increment arrival
+        if constexpr (HKV > 0 && (HKV * REC) % 128 == 0 && TT == 64) {
+            // 8 tokens per warp: lane l copies chunks (l & 7) + 8u of tokens
+            // tbeg + (l >> 3) and tbeg + 4 + (l >> 3) (4 records per instruction)
+            constexpr int kTB = HKV * REC;
+            const int sa = ok0 ? nsl0 : -1;
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+                const int tt = (lane >> 3) + 4 * v;
+                const int sl = __shfl_sync(0xffffffffu, sa, tt);
+                if (tbeg + tt < tend && sl >= 0) {
+                    const uint8_t* src = P.records + (int64_t)sl * kTB + (lane & 7) * 16;
+                    unsigned char* d = dst + (tbeg + tt) * row + (lane & 7) * 16;
+#pragma unroll
+                    for (int u = 0; u < kTB / 128; ++u) cp_async16(d + 128 * u, src + 128 * u);
+                }
+            }
+        } else {
+            // any shape: the warp's tokens one at a time, lanes over 16-byte chunks
+            const int cpt = tok_bytes / 16;
+            for (int q = 0; q < tend - tbeg; ++q) {
+                const int sl = __shfl_sync(0xffffffffu, q < 32 ? nsl0 : nsl1, q & 31);
+                const bool okq = q < 32 ? ((b0 >> q) & 1u) : ((b1 >> (q - 32)) & 1u);
+                if (okq) {
+                    const uint8_t* src = P.records + (int64_t)sl * tok_bytes;
+                    unsigned char* d = dst + (tbeg + q) * row;
+                    for (int pc = lane; pc < cpt; pc += 32) cp_async16(d + 16 * pc, src + 16 * pc);
+                }
+            }
+        }
+        cp_async_mbar_arrive(&full[s]);
     };
     // Stage k + NS - PAR is issued at iteration k by the warps of k's parity: it
     // reuses the slot of stage k - PAR, which those warps released one round ago.
