@@ -23,15 +23,17 @@
 //  * every warp consumes its own KV head of its stages (its channel half for
 //    d = 256, where two warps share a head) and releases each stage on its
 //    empty mbarrier;
-//  * each 16-token sub-tile runs mma.sync.m16n8k16 f16 → f32.  A code c
-//    enters the MMA as the exact fp16 value 1 + α·c: one LOP3 masks a code
-//    position of both 16-bit halves of a word and ORs in 0x3C00, after at most
-//    one shift of the word (see pos_inv_alpha / slot_pos; group size 32 uses
-//    one funnel shift per word and α = 1/16, 1/4).  The channel weights 1/α sit
-//    in the query operand or in the epilogue, and the per-group scale s and
-//    zero z are applied in fp32 afterwards:
+//  * each 16-token sub-tile runs mma.sync.m16n8k16 f16 → f32.  One LOP3 masks
+//    a code position of both 16-bit halves of a word, after at most one shift
+//    of the word.  For QK a K code c enters as the exact fp16 value 1 + α·c
+//    (0x3C00 ORed in; see pos_inv_alpha / slot_pos; group size 32 uses one
+//    funnel shift per word and α = 1/16, 1/4), the query carries 1/α, and the
+//    short sum over channels subtracts Σ q̃/α.  For P·V a V code enters as the
+//    exact fp16 subnormal c·2^(bit-24) (see sub_bit), so the long sum over tokens
+//    has no offset to cancel.  The per-group scale s and zero z are applied in
+//    fp32:
 //        logit = Σ_g [s_g·(Σ (q̃/α)(1 + α c) − Σ q̃/α) + z_g·Σ q̃]
-//        o_rot[ch] = (Σ_t w_t (1 + α_ch c_t) − Σ_t w_t)/α_ch + Σ_t p_t z_t,   w = p·s
+//        o_rot[ch] = 2^(24-bit_ch)·Σ_t w_t·c_t·2^(bit_ch-24) + Σ_t p_t z_t,   w = p·s
 //    q̃/α and p·s are split into fp16 hi + lo parts that occupy the n8 columns
 //    (head, part), so the products carry ~22 bits;
 //  * online softmax in log2 units; the running max moves only when a logit
@@ -67,6 +69,21 @@ __device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t o
 __device__ __forceinline__ uint32_t code_q4(uint32_t x) { return and_or(x, 0x03000300u, 0x3C003C00u); }
 __device__ __forceinline__ uint32_t code_q16(uint32_t x) { return and_or(x, 0x00C000C0u, 0x3C003C00u); }
 __device__ __forceinline__ uint32_t rotr(uint32_t w, uint32_t n) { return __funnelshift_r(w, w, n); }
+
+// V side: the code enters the MMA as the exact fp16 subnormal c·2^(bit - 24)
+// (exponent field 0), so P·V accumulates Σ w·c itself with no offset to cancel
+// over thousands of tokens.  Position p of a 16-code word sits at bit 2p of each
+// half for p <= 4 and at bit 2p - 6 of the word >> 6 for p = 5, 6, 7.
+__host__ __device__ constexpr int sub_bit(int p) { return p <= 4 ? 2 * p : 2 * p - 6; }
+__host__ __device__ constexpr float sub_inv(int bit) {   // 2^(24 - bit)
+    return (float)(1u << (24 - bit));
+}
+template <int POS>
+__device__ __forceinline__ uint32_t code_sub(uint32_t yd, uint32_t yr) {
+    constexpr int bit = sub_bit(POS);
+    constexpr uint32_t mask = (3u << bit) | (3u << (bit + 16));
+    return (POS <= 4 ? yd : yr) & mask;
+}
 
 // half2 (1 + α_p·c) of position p from the three variants (y = w, w >> 6, w << 4)
 template <int POS>
@@ -380,7 +397,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         }
         float m_run[NT], l_run[NT];
         float acc[NT][MT][4];
-        float Wsum[NT][GW], Zsum[NT][GW];   // Σ w and Σ p·z for head 4nt + j over this thread's tokens
+        float Zsum[NT][GW];                 // Σ p·z for head 4nt + j over this thread's tokens
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             m_run[nt] = -1e30f;     // finite: 2^(m_run - m) never sees -inf - -inf
@@ -390,7 +407,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[nt][mt][e] = 0.f;
 #pragma unroll
-            for (int gi = 0; gi < GW; ++gi) { Wsum[nt][gi] = 0.f; Zsum[nt][gi] = 0.f; }
+            for (int gi = 0; gi < GW; ++gi) Zsum[nt][gi] = 0.f;
         }
 
         bool seg_done = false;
@@ -552,7 +569,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
 #pragma unroll
                         for (int e = 0; e < 4; ++e) acc[nt][mt][e] *= alpha;
 #pragma unroll
-                    for (int gi = 0; gi < GW; ++gi) { Wsum[nt][gi] *= alpha; Zsum[nt][gi] *= alpha; }
+                    for (int gi = 0; gi < GW; ++gi) Zsum[nt][gi] *= alpha;
                 }
             }
             // p, w = p·s of the V groups, and the fp16 hi / lo parts of w into the
@@ -572,7 +589,6 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                         const float2 sz = h2f(*reinterpret_cast<const uint32_t*>(
                             tb + t * row + D / 2 + 4 * (NG + wsl * GW + gi)));
                         w[gi] = pv * sz.x;
-                        Wsum[nt][gi] += w[gi];
                         Zsum[nt][gi] = fmaf(pv, sz.y, Zsum[nt][gi]);
                     }
                     if constexpr (GW == 1) {
@@ -636,12 +652,12 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                         const uint32_t u23 = prmt(*reinterpret_cast<const uint32_t*>(tb + tk[2] * row + wo),
                                                   *reinterpret_cast<const uint32_t*>(tb + tk[3] * row + wo), sel);
 #pragma unroll
-                        for (int mu = 0; mu < 2; ++mu) {
+                        for (int mu = 0; mu < 2; ++mu) {   // rows r / r+8: positions 2mu / 2mu+1 of the byte
                             const int mt = gi * MTG + mu;
-                            const uint32_t rb = (uint32_t)(4 * mu - 6) & 31u;   // position 2mu+1 -> bits 8-9
-                            const uint32_t y01 = rotr(u01, rb), y23 = rotr(u23, rb);
-                            const uint32_t a0 = code_q16(y01), a1 = code_q4(y01);
-                            const uint32_t a2 = code_q16(y23), a3 = code_q4(y23);
+                            const uint32_t m0 = (3u << (4 * mu)) | (3u << (4 * mu + 16));
+                            const uint32_t m1 = m0 << 2;
+                            const uint32_t a0 = u01 & m0, a1 = u01 & m1;
+                            const uint32_t a2 = u23 & m0, a3 = u23 & m1;
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt)
                                 mma16816(acc[nt][mt], a0, a1, a2, a3, bvg[nt][gi][0], bvg[nt][gi][1]);
@@ -657,24 +673,24 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                             const uint32_t u23 = prmt(*reinterpret_cast<const uint32_t*>(tb + tk[2] * row + wo),
                                                       *reinterpret_cast<const uint32_t*>(tb + tk[3] * row + wo), wsel);
                             // m-tile slot mu: row r <- first, row r+8 <- second position of slot mu
-                            const uint32_t d01 = u01, r01 = u01 >> 6, l01 = u01 << 4;
-                            const uint32_t d23 = u23, r23 = u23 >> 6, l23 = u23 << 4;
+                            const uint32_t d01 = u01, r01 = u01 >> 6;
+                            const uint32_t d23 = u23, r23 = u23 >> 6;
 #pragma unroll
                             for (int mu = 0; mu < 4; ++mu) {
                                 const int mt = gi * MTG + hw * 4 + mu;
                                 uint32_t a0, a1, a2, a3;
                                 if (mu == 0) {
-                                    a0 = code_pos<slot_pos(0, 0)>(d01, r01, l01); a1 = code_pos<slot_pos(0, 1)>(d01, r01, l01);
-                                    a2 = code_pos<slot_pos(0, 0)>(d23, r23, l23); a3 = code_pos<slot_pos(0, 1)>(d23, r23, l23);
+                                    a0 = code_sub<slot_pos(0, 0)>(d01, r01); a1 = code_sub<slot_pos(0, 1)>(d01, r01);
+                                    a2 = code_sub<slot_pos(0, 0)>(d23, r23); a3 = code_sub<slot_pos(0, 1)>(d23, r23);
                                 } else if (mu == 1) {
-                                    a0 = code_pos<slot_pos(1, 0)>(d01, r01, l01); a1 = code_pos<slot_pos(1, 1)>(d01, r01, l01);
-                                    a2 = code_pos<slot_pos(1, 0)>(d23, r23, l23); a3 = code_pos<slot_pos(1, 1)>(d23, r23, l23);
+                                    a0 = code_sub<slot_pos(1, 0)>(d01, r01); a1 = code_sub<slot_pos(1, 1)>(d01, r01);
+                                    a2 = code_sub<slot_pos(1, 0)>(d23, r23); a3 = code_sub<slot_pos(1, 1)>(d23, r23);
                                 } else if (mu == 2) {
-                                    a0 = code_pos<slot_pos(2, 0)>(d01, r01, l01); a1 = code_pos<slot_pos(2, 1)>(d01, r01, l01);
-                                    a2 = code_pos<slot_pos(2, 0)>(d23, r23, l23); a3 = code_pos<slot_pos(2, 1)>(d23, r23, l23);
+                                    a0 = code_sub<slot_pos(2, 0)>(d01, r01); a1 = code_sub<slot_pos(2, 1)>(d01, r01);
+                                    a2 = code_sub<slot_pos(2, 0)>(d23, r23); a3 = code_sub<slot_pos(2, 1)>(d23, r23);
                                 } else {
-                                    a0 = code_pos<slot_pos(3, 0)>(d01, r01, l01); a1 = code_pos<slot_pos(3, 1)>(d01, r01, l01);
-                                    a2 = code_pos<slot_pos(3, 0)>(d23, r23, l23); a3 = code_pos<slot_pos(3, 1)>(d23, r23, l23);
+                                    a0 = code_sub<slot_pos(3, 0)>(d01, r01); a1 = code_sub<slot_pos(3, 1)>(d01, r01);
+                                    a2 = code_sub<slot_pos(3, 0)>(d23, r23); a3 = code_sub<slot_pos(3, 1)>(d23, r23);
                                 }
 #pragma unroll
                                 for (int nt = 0; nt < NT; ++nt)
@@ -700,7 +716,6 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
             for (int gi = 0; gi < GW; ++gi) {
 #pragma unroll
                 for (int sh = 4; sh < 32; sh <<= 1) {
-                    Wsum[nt][gi] += __shfl_xor_sync(0xffffffffu, Wsum[nt][gi], sh);
                     Zsum[nt][gi] += __shfl_xor_sync(0xffffffffu, Zsum[nt][gi], sh);
                 }
             }
@@ -716,27 +731,27 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
             if (r == 0 && wsl == 0 && hh < g) P.ml[slot * P.Hq + hq] = make_float2(m_run[nt], l_run[nt]);
 #pragma unroll
             for (int gi = 0; gi < GW; ++gi) {
-                const float Wh = Wsum[nt][gi], Zh = Zsum[nt][gi];
+                const float Zh = Zsum[nt][gi];
                 const int gg = wsl * GW + gi;
 #pragma unroll
                 for (int mu = 0; mu < MTG; ++mu) {
                     const int mt = gi * MTG + mu;
                     if (hh >= g) continue;
-                    const float v0 = acc[nt][mt][0] + acc[nt][mt][1] - Wh;   // row r
-                    const float v1 = acc[nt][mt][2] + acc[nt][mt][3] - Wh;   // row r + 8
+                    const float v0 = acc[nt][mt][0] + acc[nt][mt][1];   // row r  (hi + lo columns)
+                    const float v1 = acc[nt][mt][2] + acc[nt][mt][3];   // row r + 8
                     if constexpr (G == 32) {
-                        // rows r / r+8: even / odd code position of the pair, α = 1/16, 1/4
+                        // rows r / r+8: positions 2mu / 2mu+1 of the byte r (bits 4mu, 4mu+2)
                         const int ch0 = gg * G + 4 * r + 2 * mu;
-                        o[ch0] = 16.f * v0 + Zh;
-                        o[ch0 + 1] = 4.f * v1 + Zh;
+                        o[ch0] = (mu == 0 ? sub_inv(0) : sub_inv(4)) * v0 + Zh;
+                        o[ch0 + 1] = (mu == 0 ? sub_inv(2) : sub_inv(6)) * v1 + Zh;
                     } else {
                         // the 16-bit chunk r (and half-word mu / 4) of the group; slot mu % 4
                         const int base = gg * G + r * (G / 8) + 8 * (mu / 4);
                         const int s4 = mu % 4;
                         const int p0 = s4 == 0 ? slot_pos(0, 0) : s4 == 1 ? slot_pos(1, 0) : s4 == 2 ? slot_pos(2, 0) : slot_pos(3, 0);
                         const int p1 = s4 == 0 ? slot_pos(0, 1) : s4 == 1 ? slot_pos(1, 1) : s4 == 2 ? slot_pos(2, 1) : slot_pos(3, 1);
-                        o[base + p0] = pos_inv_alpha(p0) * v0 + Zh;
-                        o[base + p1] = pos_inv_alpha(p1) * v1 + Zh;
+                        o[base + p0] = sub_inv(sub_bit(p0)) * v0 + Zh;
+                        o[base + p1] = sub_inv(sub_bit(p1)) * v1 + Zh;
                     }
                 }
             }
