@@ -135,16 +135,16 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
         }
         __syncthreads();
         // Per group, from the fp16 hi + lo parts actually fed to the MMA: Q = Σ q̃
-        // and Q' = Σ q̃/α, where α is the weight with which the tensor-core path
-        // encodes a code c of that channel as 1 + α·c: by code position within a
-        // 16-code word (pos_inv_alpha) for groups >= 64, 1/16 on even and 1/4 on
-        // odd channels for group size 32.
+        // and Q' = Σ (fed value).  The fed value of channel c is q̃·2^(kQkExp - bit)
+        // for groups >= 64 (subnormal codes; Q' unused there) and q̃/α for group
+        // size 32, whose codes enter as 1 + α·c with α = 1/16 on even and 1/4 on
+        // odd channels (Q' is subtracted from the accumulator).
         const int lane = tid & 31, warp = tid >> 5;
         for (int i = warp; i < nh * P.ng; i += 8) {
             const int j = i / P.ng, gi = i % P.ng;
             float sq_ = 0.f, sqa = 0.f;
             for (int c = gi * P.G + lane; c < (gi + 1) * P.G; c += 32) {
-                const float inv = P.G >= 64 ? pos_inv_alpha(c & 7) : ((c & 1) ? 4.f : 16.f);
+                const float inv = P.G >= 64 ? (float)(1u << (kQkExp - sub_bit(c & 7))) : ((c & 1) ? 4.f : 16.f);
                 const float x = sqt[j][c] * inv;
                 const __half hi = __float2half_rn(x);
                 const __half lo = __float2half_rn(x - __half2float(hi));
@@ -187,8 +187,8 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
                 const int w = 4 * (kk / 4) + j, p0 = slot_pos(kk % 4, 0), p1 = slot_pos(kk % 4, 1);
                 chans[0] = 16 * w + p0; chans[1] = 16 * w + 8 + p0;
                 chans[2] = 16 * w + p1; chans[3] = 16 * w + 8 + p1;
-                scl[0] = scl[1] = pos_inv_alpha(p0);
-                scl[2] = scl[3] = pos_inv_alpha(p1);
+                scl[0] = scl[1] = (float)(1u << (kQkExp - sub_bit(p0)));
+                scl[2] = scl[3] = (float)(1u << (kQkExp - sub_bit(p1)));
             } else {
                 chans[0] = 16 * kk + 2 * j; chans[1] = 16 * kk + 2 * j + 8;
                 chans[2] = 16 * kk + 2 * j + 1; chans[3] = 16 * kk + 2 * j + 9;

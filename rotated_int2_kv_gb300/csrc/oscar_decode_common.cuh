@@ -104,19 +104,18 @@ struct DecodeParams {
 
 namespace oscar {
 
-// Tensor-core code encoding for group sizes >= 64.  Position p of a 32-bit word
-// of 16 codes (bits 2p, 2p+1 of each 16-bit half) enters the MMA as the exact fp16 value
-// 1 + α_p·c after one LOP3 on one of three variants of the word: the word itself
-// (p = 2, 3, 4 at bits 4-9), the word >> 6 (p = 5, 6, 7) or the word << 4 (p = 0, 1).
-// Neither shift moves bits across the 16-bit halves into the masked bits.
-// α_p = 2^-6, 2^-4, 2^-2 at bits 4-5, 6-7, 8-9; 1/α_p by position:
-__host__ __device__ constexpr float pos_inv_alpha(int p) {
-    return (p == 4 || p == 7) ? 4.f : ((p == 1 || p == 3 || p == 6) ? 16.f : 64.f);
-}
+// Tensor-core code encoding for group sizes >= 64.  A code at position p of a
+// 32-bit word of 16 codes (bits 2p, 2p+1 of each 16-bit half) enters the MMA as
+// the exact fp16 subnormal c·2^(bit - 24) after one AND, on the word itself for
+// p <= 4 (bit = 2p) or on the word >> 6 for p = 5, 6, 7 (bit = 2p - 6).
+__host__ __device__ constexpr int sub_bit(int p) { return p <= 4 ? 2 * p : 2 * p - 6; }
 // The four register slots of a word: (first, second) position of slot s.
 __host__ __device__ constexpr int slot_pos(int s, int second) {
     return s == 0 ? (second ? 4 : 3) : s == 1 ? (second ? 5 : 2) : s == 2 ? (second ? 7 : 6) : (second ? 1 : 0);
 }
+// The query operand of channel at position p is q̃·2^(kQkExp - bit) (at most 256·q̃,
+// inside the fp16 range), so a QK product is q̃·c·2^(kQkExp - 24).
+constexpr int kQkExp = 8;
 
 // CTA of the history grid that owns flattened chunk f (N chunks over n CTAs).
 __host__ __device__ __forceinline__ int64_t chunk_owner(int64_t f, int64_t N, int64_t n) {

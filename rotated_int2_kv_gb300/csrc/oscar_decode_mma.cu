@@ -23,18 +23,17 @@
 //  * every warp consumes its own KV head of its stages (its channel half for
 //    d = 256, where two warps share a head) and releases each stage on its
 //    empty mbarrier;
-//  * each 16-token sub-tile runs mma.sync.m16n8k16 f16 → f32.  One LOP3 masks
-//    a code position of both 16-bit halves of a word, after at most one shift
-//    of the word.  For QK a K code c enters as the exact fp16 value 1 + α·c
-//    (0x3C00 ORed in; see pos_inv_alpha / slot_pos; group size 32 uses one
-//    funnel shift per word and α = 1/16, 1/4), the query carries 1/α, and the
-//    short sum over channels subtracts Σ q̃/α.  For P·V a V code enters as the
-//    exact fp16 subnormal c·2^(bit-24) (see sub_bit), so the long sum over tokens
-//    has no offset to cancel.  The per-group scale s and zero z are applied in
-//    fp32:
-//        logit = Σ_g [s_g·(Σ (q̃/α)(1 + α c) − Σ q̃/α) + z_g·Σ q̃]
+//  * each 16-token sub-tile runs mma.sync.m16n8k16 f16 → f32.  One AND masks a
+//    code position of both 16-bit halves of a word, after at most one shift of
+//    the word, and the code enters the MMA as the exact fp16 subnormal
+//    c·2^(bit-24) (see sub_bit / slot_pos), so neither sum carries an offset to
+//    cancel.  The query operand of a channel is q̃·2^(kQkExp - bit); the per-group
+//    scale s and zero z are applied in fp32:
+//        logit    = 2^(24-kQkExp)·Σ_g s_g·Σ_ch (q̃ 2^(kQkExp-bit))(c 2^(bit-24)) + Σ_g z_g·Σ q̃
 //        o_rot[ch] = 2^(24-bit_ch)·Σ_t w_t·c_t·2^(bit_ch-24) + Σ_t p_t z_t,   w = p·s
-//    q̃/α and p·s are split into fp16 hi + lo parts that occupy the n8 columns
+//    (group size 32 keeps the older 1 + α·c encoding of the K codes, α = 1/16,
+//    1/4, with one funnel shift per word and Σ q̃/α subtracted);
+//    the query operand and p·s are split into fp16 hi + lo parts that occupy the n8 columns
 //    (head, part), so the products carry ~22 bits;
 //  * online softmax in log2 units; the running max moves only when a logit
 //    exceeds it (one warp vote per stage otherwise); partials (m, l, o) per
@@ -74,7 +73,6 @@ __device__ __forceinline__ uint32_t rotr(uint32_t w, uint32_t n) { return __funn
 // (exponent field 0), so P·V accumulates Σ w·c itself with no offset to cancel
 // over thousands of tokens.  Position p of a 16-code word sits at bit 2p of each
 // half for p <= 4 and at bit 2p - 6 of the word >> 6 for p = 5, 6, 7.
-__host__ __device__ constexpr int sub_bit(int p) { return p <= 4 ? 2 * p : 2 * p - 6; }
 __host__ __device__ constexpr float sub_inv(int bit) {   // 2^(24 - bit)
     return (float)(1u << (24 - bit));
 }
@@ -85,14 +83,6 @@ __device__ __forceinline__ uint32_t code_sub(uint32_t yd, uint32_t yr) {
     return (POS <= 4 ? yd : yr) & mask;
 }
 
-// half2 (1 + α_p·c) of position p from the three variants (y = w, w >> 6, w << 4)
-template <int POS>
-__device__ __forceinline__ uint32_t code_pos(uint32_t yd, uint32_t yr, uint32_t yl) {
-    constexpr int bit = POS <= 1 ? 2 * POS + 4 : (POS <= 4 ? 2 * POS : 2 * POS - 6);
-    constexpr uint32_t mask = (3u << bit) | (3u << (bit + 16));
-    const uint32_t y = POS <= 1 ? yl : (POS <= 4 ? yd : yr);
-    return and_or(y, mask, 0x3C003C00u);
-}
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -450,23 +440,23 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                             // (2j+8, 2j+9) <- second position; all 4 words in one group
                             const int gi = (k4 * 16) / G;
                             const uint32_t u0 = w_r[j], u1 = w_r8[j];
-                            const uint32_t d0 = u0, r0 = u0 >> 6, l0 = u0 << 4;
-                            const uint32_t d1 = u1, r1 = u1 >> 6, l1 = u1 << 4;
+                            const uint32_t d0 = u0, r0 = u0 >> 6;
+                            const uint32_t d1 = u1, r1 = u1 >> 6;
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
                                 uint32_t x0, x1, x2, x3;
                                 if (q == 0) {
-                                    x0 = code_pos<slot_pos(0, 0)>(d0, r0, l0); x1 = code_pos<slot_pos(0, 0)>(d1, r1, l1);
-                                    x2 = code_pos<slot_pos(0, 1)>(d0, r0, l0); x3 = code_pos<slot_pos(0, 1)>(d1, r1, l1);
+                                    x0 = code_sub<slot_pos(0, 0)>(d0, r0); x1 = code_sub<slot_pos(0, 0)>(d1, r1);
+                                    x2 = code_sub<slot_pos(0, 1)>(d0, r0); x3 = code_sub<slot_pos(0, 1)>(d1, r1);
                                 } else if (q == 1) {
-                                    x0 = code_pos<slot_pos(1, 0)>(d0, r0, l0); x1 = code_pos<slot_pos(1, 0)>(d1, r1, l1);
-                                    x2 = code_pos<slot_pos(1, 1)>(d0, r0, l0); x3 = code_pos<slot_pos(1, 1)>(d1, r1, l1);
+                                    x0 = code_sub<slot_pos(1, 0)>(d0, r0); x1 = code_sub<slot_pos(1, 0)>(d1, r1);
+                                    x2 = code_sub<slot_pos(1, 1)>(d0, r0); x3 = code_sub<slot_pos(1, 1)>(d1, r1);
                                 } else if (q == 2) {
-                                    x0 = code_pos<slot_pos(2, 0)>(d0, r0, l0); x1 = code_pos<slot_pos(2, 0)>(d1, r1, l1);
-                                    x2 = code_pos<slot_pos(2, 1)>(d0, r0, l0); x3 = code_pos<slot_pos(2, 1)>(d1, r1, l1);
+                                    x0 = code_sub<slot_pos(2, 0)>(d0, r0); x1 = code_sub<slot_pos(2, 0)>(d1, r1);
+                                    x2 = code_sub<slot_pos(2, 1)>(d0, r0); x3 = code_sub<slot_pos(2, 1)>(d1, r1);
                                 } else {
-                                    x0 = code_pos<slot_pos(3, 0)>(d0, r0, l0); x1 = code_pos<slot_pos(3, 0)>(d1, r1, l1);
-                                    x2 = code_pos<slot_pos(3, 1)>(d0, r0, l0); x3 = code_pos<slot_pos(3, 1)>(d1, r1, l1);
+                                    x0 = code_sub<slot_pos(3, 0)>(d0, r0); x1 = code_sub<slot_pos(3, 0)>(d1, r1);
+                                    x2 = code_sub<slot_pos(3, 1)>(d0, r0); x3 = code_sub<slot_pos(3, 1)>(d1, r1);
                                 }
 #pragma unroll
                                 for (int nt = 0; nt < NT; ++nt) {
@@ -504,16 +494,35 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                     const int i = 2 * mh + ib;       // token row 8i + r = 16·mq + 8·half + r
                     const int t = 8 * i + r;
                     const int mb = ib >> 1, hf = ib & 1;
+                    if constexpr (G >= 64) {
+                        // lg = 2^(24 - kQkExp) Σ_g s_g·acc_g + Σ_g z_g·Σ q̃  (subnormal K codes)
+                        float ts[NT], tz[NT];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) lg[nt][i] = 0.f;
+                        for (int nt = 0; nt < NT; ++nt) { ts[nt] = 0.f; tz[nt] = 0.f; }
 #pragma unroll
-                    for (int gi = 0; gi < GW; ++gi) {
-                        const int gg = wsl * GW + gi;
-                        const float2 sz = h2f(*reinterpret_cast<const uint32_t*>(tb + t * row + D / 2 + 4 * gg));
+                        for (int gi = 0; gi < GW; ++gi) {
+                            const int gg = wsl * GW + gi;
+                            const float2 sz = h2f(*reinterpret_cast<const uint32_t*>(tb + t * row + D / 2 + 4 * gg));
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            const float2 Q = qs[nt][gi];       // (Σ q̃, Σ q̃/α)
-                            lg[nt][i] += sz.x * (sc[mb][gi][nt][2 * hf] + sc[mb][gi][nt][2 * hf + 1] - Q.y) + sz.y * Q.x;
+                            for (int nt = 0; nt < NT; ++nt) {
+                                ts[nt] = fmaf(sz.x, sc[mb][gi][nt][2 * hf] + sc[mb][gi][nt][2 * hf + 1], ts[nt]);
+                                tz[nt] = fmaf(sz.y, qs[nt][gi].x, tz[nt]);
+                            }
+                        }
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) lg[nt][i] = fmaf(ts[nt], (float)(1u << (24 - kQkExp)), tz[nt]);
+                    } else {
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) lg[nt][i] = 0.f;
+#pragma unroll
+                        for (int gi = 0; gi < GW; ++gi) {
+                            const int gg = wsl * GW + gi;
+                            const float2 sz = h2f(*reinterpret_cast<const uint32_t*>(tb + t * row + D / 2 + 4 * gg));
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                const float2 Q = qs[nt][gi];       // (Σ q̃, Σ q̃/α)
+                                lg[nt][i] += sz.x * (sc[mb][gi][nt][2 * hf] + sc[mb][gi][nt][2 * hf + 1] - Q.y) + sz.y * Q.x;
+                            }
                         }
                     }
                 }
