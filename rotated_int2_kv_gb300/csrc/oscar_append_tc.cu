@@ -6,40 +6,51 @@
 // z = fp16(lo), c = clamp(rint((y-z)/s), 0, 3)).
 //
 // y = x·R is a dense (vectors × d) · (d × d) contraction, so it runs on the
-// tensor cores with mma.sync.m16n8k16 in bf16: x is exactly bf16 (every input
-// is rounded to bf16 first), and R (fp32) is split into three bf16 parts
-// hi + mid + lo, which hold its 24-bit significand.  Products are exact; for
-// every k-step of 16 channels the three parts are chained from lo to hi from a
-// zero accumulator, and the k-steps are summed in fp32 registers (round to
-// nearest).  Measured against the exact product this is more accurate than a
-// sequential fp32 FMA chain, which matters because a code decided near a
-// rounding boundary must agree with the oracle.  The quantisation then uses
-// the same IEEE fp32 operations as the CUDA-core kernels.
+// fifth-generation tensor cores (tcgen05.mma, kind::f16, bf16 operands, fp32
+// accumulators in tensor memory).  x is exactly bf16 (every input is rounded
+// to bf16 first), and R (fp32) is split into three bf16 parts hi + mid + lo,
+// which hold its 24-bit significand, so every product is exact.  One
+// accumulator takes the lo parts of all k-steps first, then the mid parts,
+// then the hi parts.  Measured against the exact product this is more
+// accurate than a sequential fp32 FMA chain (largest error about 5.5e-7 of
+// the row's largest |y|, against 1.2e-6), which matters because a code
+// decided near a rounding boundary must agree with the oracle.
 //
-// One CTA of 8 warps takes tiles of 128 vectors of one matrix (K or V:
-// blockIdx.y); warp w owns vectors 16w .. 16w+15 of the tile and all d output
-// channels, so a group's min / max is a reduction over its own registers and 4
-// lanes.  The B fragments of the three parts of R are built once per CTA in
-// shared memory.
+// One CTA per SM, persistent over tiles of 128 vectors of one matrix (K or V:
+// blockIdx.y).  R's three parts stay in shared memory as the B operand (N = d
+// output channels × K = d, K-major, 128-byte swizzle).  Three warpgroups take
+// the tiles in turn, each with its own x tile (the A operand, M = 128
+// vectors), its own accumulator in tensor memory and its own mbarrier; one
+// thread of the group issues the group's MMAs.  A group's flow per tile: wait for its
+// rows, issue the MMAs, finish resolving the next tile's vectors and start the
+// page-table loads of the one after, wait for the MMAs, start copying the next
+// tile's rows (16-byte cp.async), then quantise: thread
+// i of the group owns tensor-memory lane i, that is vector i of the tile and
+// all its d channels, so a group's min / max is a reduction in registers.
+//
+// The code decision uses the correctly rounded reciprocal of 3s: q = 3·sat(a ·
+// (1/3s)) with a = y - z is within 2^-21 of the correctly rounded quotient a/s
+// for q in [0, 3] (three roundings), so rint(q) is the oracle's code unless q
+// lies within 2^-19 of a half-integer; a warp in which some thread meets such a
+// q in a group decides that group again with correctly rounded division.
+// Tensor-memory loads (tcgen05.ld) are warp-collective, so every branch around
+// them is warp-uniform.
 #include <algorithm>
 
 #include "oscar_append_common.cuh"
+#include "oscar_tcgen05.cuh"
 
 namespace oscar {
 
 namespace {
 
-constexpr int kTcVec = 128;          // vectors per tile (8 warps x 16 rows)
-constexpr int kTcThreads = 256;
-
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
+constexpr int kTcRows = 128;               // vectors per tile (the MMA's M; one tensor-memory lane each)
+constexpr int kSlots = 3;                  // warpgroups, each with its own tile in flight
+constexpr int kTcThreads = 128 * kSlots;
+constexpr uint32_t kTmemCols = 512;        // slot e's accumulator: columns 128·e .. 128·e + d
+constexpr int kMetaInts = 4;               // per vector: slot, head | kind << 16, source offset (int64)
+constexpr float kMagic = 12582912.0f;      // 1.5·2^23: x + kMagic rounds x to an integer in the low bits
+constexpr float kTieBand = 0.5f - 1.0f / 524288.0f;   // |q - rint(q)| above this: within 2^-19 of a tie
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
@@ -55,245 +66,376 @@ __device__ __forceinline__ float bf16_part(float x, int p) {
     return r1 - m;
 }
 
+__device__ __forceinline__ void group_bar(int e) {
+    asm volatile("bar.sync %0, 128;" :: "r"(1 + e) : "memory");
+}
+
+// Group barrier that also returns the OR of v over the group.
+__device__ __forceinline__ bool group_bar_or(int e, bool v) {
+    int r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\t"
+                 "bar.red.or.pred q, %2, 128, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r) : "r"((int)v), "r"(1 + e) : "memory");
+    return r != 0;
+}
+
+// 32 channels of y for this thread's vector.
+__device__ __forceinline__ void load_y(uint32_t taddr, float (&y)[32]) {
+    tc5::ld32(taddr, y);
+    tc5::wait_ld();
+}
+
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// min and max of 32 values folded into (mn, mx): four independent chains of
+// three-input min / max, then a short combine.
+__device__ __forceinline__ void minmax32(const float (&y)[32], float& mn, float& mx) {
+    float a[4], b[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float* v = y + 8 * k;
+        a[k] = fminf(min3f(min3f(v[0], v[1], v[2]), v[3], v[4]), min3f(v[5], v[6], v[7]));
+        b[k] = fmaxf(max3f(max3f(v[0], v[1], v[2]), v[3], v[4]), max3f(v[5], v[6], v[7]));
+    }
+    mn = min3f(mn, min3f(a[0], a[1], a[2]), a[3]);
+    mx = max3f(mx, max3f(b[0], b[1], b[2]), b[3]);
+}
+
+// Codes of 32 channels as two words of 16 (channel i at bits 2i).  EXACT:
+// correctly rounded division (the same codes as the reciprocal path wherever
+// that one is not near a tie).  Otherwise the reciprocal path on channel pairs
+// (paired fp32 operations), and bit 31 of `tie` is cleared when some
+// |q - rint(q)| reaches kTieBand.  s = 0 (a flat group) gives codes 0 either way.
+template <bool EXACT>
+__device__ __forceinline__ void codes32(const float (&y)[32], float zc, float sc, float r3, uint32_t& w0, uint32_t& w1,
+                                        uint32_t& tie) {
+    float2 c[16];                         // codes of channels (2j, 2j+1) as floats
+    if (EXACT) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            float v[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float a = __fsub_rn(y[2 * j + h], zc);
+                v[h] = sc != 0.0f ? fminf(fmaxf(rintf(__fdiv_rn(a, sc)), 0.0f), 3.0f) : 0.0f;
+            }
+            c[j] = make_float2(v[0], v[1]);
+        }
+    } else {
+        const float2 nz = make_float2(-zc, -zc), three = make_float2(3.0f, 3.0f);
+        const float2 mg = make_float2(kMagic, kMagic), nmg = make_float2(-kMagic, -kMagic);
+        const float2 m1 = make_float2(-1.0f, -1.0f);
+        const float2 nb = make_float2(-kTieBand * kTieBand, -kTieBand * kTieBand);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float2 a = __fadd2_rn(make_float2(y[2 * j], y[2 * j + 1]), nz);                 // y - z
+            const float2 t = make_float2(__saturatef(__fmul_rn(a.x, r3)), __saturatef(__fmul_rn(a.y, r3)));
+            const float2 q = __fmul2_rn(t, three);                                               // in [0, 3]
+            c[j] = __fadd2_rn(__fadd2_rn(q, mg), nmg);                                          // rint(q)
+            const float2 d = __ffma2_rn(c[j], m1, q);                                           // q - rint(q)
+            const float2 e = __ffma2_rn(d, d, nb);                                              // >= 0: near a tie
+            tie &= __float_as_uint(e.x) & __float_as_uint(e.y);
+        }
+    }
+    // Σ c_i 4^i over 8 channels per value, as a depth-3 tree of exact integer FMAs
+    const float2 k16 = make_float2(16.0f, 16.0f), k256 = make_float2(256.0f, 256.0f);
+    float2 A[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) A[k] = __ffma2_rn(c[2 * k + 1], k16, c[2 * k]);      // c_4k + 16 c_4k+2 | odd
+    uint32_t u[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const float2 B = __ffma2_rn(A[2 * m + 1], k256, A[2 * m]);
+        const float v = __fmaf_rn(B.y, 4.0f, B.x);                                    // channels 8m .. 8m+7
+        u[m] = __float_as_uint(__fadd_rn(v, kMagic));                                 // low 16 bits = v
+    }
+    w0 = __byte_perm(u[0], u[1], 0x5410);
+    w1 = __byte_perm(u[2], u[3], 0x5410);
+}
+
+template <int D>
+struct TcCfg {
+    static constexpr int KS = D / 16;               // k-steps of 16
+    static constexpr int A_BYTES = kTcRows * D * 2; // one x tile
+    static constexpr int B_PART = D * D * 2;        // one part of R
+    static constexpr int CPR = D / 8;               // 16-byte chunks per row
+    static constexpr int RPI = 32 / CPR;            // rows per warp instruction in the copy
+    static constexpr size_t SMEM = 1024 + 3 * (size_t)B_PART + kSlots * (size_t)A_BYTES +
+                                   (size_t)kSlots * 2 * kTcRows * kMetaInts * 4 + 64;   // + prefix, scratch
+};
+
 }  // namespace
 
 template <int D, int G>
 __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(AppendParams P) {
-    constexpr int KS = D / 16;           // k-steps
-    constexpr int NTL = D / 8;           // n8 tiles of output channels
-    constexpr int XS = D + 8;            // bf16 row stride of the X tile (≡ 4 words mod 32)
-    constexpr int CB = D / 4;            // code bytes per vector
-    extern __shared__ __align__(16) unsigned char smem[];
-    uint2* fragB = reinterpret_cast<uint2*>(smem);                                   // [3][KS][NTL][32]
-    uint16_t* sX = reinterpret_cast<uint16_t*>(smem + 3 * KS * NTL * 32 * 8);        // [2][kTcVec][XS]
-    uint8_t* sC = reinterpret_cast<uint8_t*>(sX + 2 * kTcVec * XS);                  // [kTcVec][CB]
-    int* prefix = reinterpret_cast<int*>(sC + kTcVec * CB);                          // batch + 1
-    int* scratch = prefix + P.batch + 1;                                              // blockDim.x
-    __shared__ int s_meta[2][kTcVec][4];                                              // b, p, h, slot
+    using C = TcCfg<D>;
+    constexpr int ng = D / G;
+    constexpr int NW = D / 16;                      // code words per vector
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* sB = smem;                                               // [3 parts][D rows][D] swizzled
+    unsigned char* sA = smem + 3 * C::B_PART;                               // [slots][128 rows][D] swizzled
+    int* meta = reinterpret_cast<int*>(sA + kSlots * C::A_BYTES);          // [slots][2 buffers][128][4]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(meta + kSlots * 2 * kTcRows * kMetaInts);   // [slots]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kSlots);
+    int* prefix = reinterpret_cast<int*>(tslot + 2);                       // batch + 1
+    int* scratch = prefix + P.batch + 1;                                    // kTcThreads
 
     const int mat = blockIdx.y;
     const float* R = mat ? P.rot_v : P.rot_k;
     const void* src_new = mat ? P.v : P.k;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int r = lane >> 2, j = lane & 3;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int e = warp >> 2;           // warpgroup = tile slot
+    const int gw = warp & 3;           // warp of the group = tensor-memory lane quarter
+    const int gt = tid & 127;          // thread of the group = tile row of the epilogue
 
     build_prefix(P, prefix, scratch);
     const int64_t total_vec = (int64_t)prefix[P.batch] * P.Hkv;
-    const int64_t ntiles = (total_vec + kTcVec - 1) / kTcVec;
-    if ((int64_t)blockIdx.x >= ntiles) return;
+    const int64_t ntiles = (total_vec + kTcRows - 1) / kTcRows;
+    if ((int64_t)blockIdx.x >= ntiles) return;    // uniform over the CTA, before any allocation
 
-    // B fragments of R's three parts: lane (n, j) of k-step kk, n-tile nt holds
-    // (R[16kk+2j][8nt+n], R[16kk+2j+1][8nt+n]) and (R[16kk+2j+8][..], R[16kk+2j+9][..])
-    for (int i = tid; i < 3 * KS * NTL * 32; i += kTcThreads) {
-        const int ln = i & 31, nt = (i >> 5) % NTL, kk = (i / (32 * NTL)) % KS, p = i / (32 * NTL * KS);
-        const int n = ln >> 2, jj = ln & 3;
-        const int col = 8 * nt + n, k0 = 16 * kk + 2 * jj;
-        const float* Rc = R + col;
-        fragB[i] = make_uint2(pack_bf16(bf16_part(Rc[(int64_t)k0 * D], p), bf16_part(Rc[(int64_t)(k0 + 1) * D], p)),
-                              pack_bf16(bf16_part(Rc[(int64_t)(k0 + 8) * D], p), bf16_part(Rc[(int64_t)(k0 + 9) * D], p)));
+    if (tid == 0) {
+        for (int q = 0; q < kSlots; ++q) mbar_init(&bars[q], 1);
+        fence_mbar_init();
     }
-    constexpr int ng = D / G;
-    constexpr int lpg = G / 8;           // n-tiles per group
-    const float rclip = P.clip;
-    // 16-byte loads of the new rows when the input is 16-byte aligned (rows of d
-    // elements then stay aligned: d·2 and d·4 bytes are multiples of 16)
+    if (warp == 0) {
+        tc5::alloc(tslot, kTmemCols);
+        tc5::relinquish();
+    }
+    // B: part p of R as D rows n (column n of R) × D k, consecutive threads on
+    // consecutive n (coalesced reads of R; the swizzle spreads the stores)
+    for (int i = tid; i < 3 * D * C::CPR; i += kTcThreads) {
+        const int n = i % D, j = (i / D) % C::CPR, p = i / (D * C::CPR);
+        const float* Rc = R + (int64_t)(8 * j) * D + n;
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) w[q] = pack_bf16(bf16_part(Rc[(2 * q) * D], p), bf16_part(Rc[(2 * q + 1) * D], p));
+        *reinterpret_cast<uint4*>(sB + p * C::B_PART + tc5::sw128_offset(D, n, j)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    tc5::fence_proxy_async();
+    tc5::fence_before();
+    __syncthreads();
+    tc5::fence_after();
+    const uint32_t tmem = *tslot;
+
     const bool vec_in = (reinterpret_cast<uintptr_t>(src_new) & 15) == 0;
+    const float rclip = P.clip;
     const int rec_off_codes = mat ? D / 4 : 0;
     const int rec_off_sz = D / 2 + (mat ? 4 * ng : 0);
+    unsigned char* A = sA + e * C::A_BYTES;
+    int* gmeta = meta + e * 2 * kTcRows * kMetaInts;
+    uint64_t* bar = &bars[e];
+    const uint32_t tacc = tmem + (uint32_t)(128 * e) + ((uint32_t)(32 * gw) << 16);
 
-    // Tiles are pipelined over two buffers: while the warps multiply tile t, the
-    // vectors of tile t + gridDim.x are resolved and their rows copied (16-byte
-    // cp.async for bf16 sources) into the other buffer.
-    auto resolve = [&](int64_t tile, int buf) {
-        const int64_t e0 = tile * kTcVec;
-        const int nvec = (int)(total_vec - e0 < kTcVec ? total_vec - e0 : kTcVec);
-        if (tid < kTcVec) {
-            int b = -1, p = 0, h = 0, slot = -1;
-            if (tid < nvec) {
-                const int64_t e = e0 + tid;
-                const int u = (int)(e / P.Hkv);
-                h = (int)(e % P.Hkv);
-                b = find_request(prefix, P.batch, u);
-                const int L0 = P.start_pos[b];
-                p = hist_hi(L0, P.S, P.W) + (u - prefix[b]);
-                if (p >= P.pt_stride) {
-                    set_status(P.status, OSCAR_DEV_BAD_LEN);
+    // Vector gt of a tile is resolved in two stages one loop iteration apart, so
+    // that its page-table load is in flight while the group quantises: locate()
+    // finds the request and position and starts that load; publish() checks the
+    // slot and writes the entry (slot, -1 when there is nothing to write; head;
+    // source kind, 1 recent ring, 2 new input; element offset of the row).
+    struct Loc {
+        int b, p, h, sl;
+        bool valid;
+    };
+    auto locate = [&](int64_t tile) {
+        Loc L{0, 0, 0, -1, false};
+        const int64_t ev = tile * kTcRows + gt;
+        if (tile < ntiles && ev < total_vec) {
+            const int u = (int)(ev / P.Hkv);
+            L.h = (int)(ev % P.Hkv);
+            L.b = find_request(prefix, P.batch, u);
+            L.p = hist_hi(P.start_pos[L.b], P.S, P.W) + (u - prefix[L.b]);
+            L.valid = true;
+            if (L.p < P.pt_stride) L.sl = P.page_table[(int64_t)L.b * P.pt_stride + L.p];
+        }
+        return L;
+    };
+    auto publish = [&](const Loc& L, int buf) {
+        int slot = -1, kind = 0;
+        int64_t off = 0;
+        if (L.valid) {
+            const int b = L.b, p = L.p, h = L.h;
+            const int L0 = P.start_pos[b];
+            if (p >= P.pt_stride) set_status(P.status, OSCAR_DEV_BAD_LEN);
+            else if (L.sl < 0 || L.sl >= P.num_slots) set_status(P.status, OSCAR_DEV_BAD_SLOT);
+            else slot = L.sl;
+            const int rq = P.req_idx ? P.req_idx[b] : b;
+            if (p < L0 && (rq < 0 || rq >= P.max_reqs)) {
+                set_status(P.status, OSCAR_DEV_BAD_REQ);
+                slot = -1;
+            }
+            if (p >= L0 && (int64_t)P.cu_new[b] + (p - L0) >= P.total_new) {
+                set_status(P.status, OSCAR_DEV_BAD_LEN);
+                slot = -1;
+            }
+            if (slot >= 0) {
+                if (p < L0) {
+                    kind = 1;
+                    off = ((((int64_t)rq * P.W + p % P.W) * P.Hkv + h) * 2 + mat) * D;
                 } else {
-                    const int sl = P.page_table[(int64_t)b * P.pt_stride + p];
-                    if (sl < 0 || sl >= P.num_slots) set_status(P.status, OSCAR_DEV_BAD_SLOT);
-                    else slot = sl;
-                }
-                const int rq = P.req_idx ? P.req_idx[b] : b;
-                if (p < L0 && (rq < 0 || rq >= P.max_reqs)) {
-                    set_status(P.status, OSCAR_DEV_BAD_REQ);
-                    slot = -1;
-                }
-                if (p >= L0 && (int64_t)P.cu_new[b] + (p - L0) >= P.total_new) {
-                    set_status(P.status, OSCAR_DEV_BAD_LEN);
-                    slot = -1;
+                    kind = 2;
+                    off = ((int64_t)(P.cu_new[b] + (p - L0)) * P.Hkv + h) * D;
                 }
             }
-            s_meta[buf][tid][0] = b;
-            s_meta[buf][tid][1] = p;
-            s_meta[buf][tid][2] = h;
-            s_meta[buf][tid][3] = slot;
         }
+        int* m = gmeta + (buf * kTcRows + gt) * kMetaInts;
+        m[0] = slot;
+        m[1] = L.h | (kind << 16);
+        *reinterpret_cast<int64_t*>(m + 2) = off;
     };
-    auto gather = [&](int64_t tile, int buf) {
-        const int64_t e0 = tile * kTcVec;
-        const int nvec = (int)(total_vec - e0 < kTcVec ? total_vec - e0 : kTcVec);
-        uint16_t* xb = sX + buf * kTcVec * XS;
-        for (int idx = tid; idx < kTcVec * (D / 8); idx += kTcThreads) {
-            const int v = idx / (D / 8), c8 = idx % (D / 8);
-            uint32_t* dst = reinterpret_cast<uint32_t*>(xb + v * XS + c8 * 8);   // 16-byte aligned: XS·2 ≡ 0 mod 16
-            if (v < nvec && s_meta[buf][v][3] >= 0) {
-                const int b = s_meta[buf][v][0], p = s_meta[buf][v][1], h = s_meta[buf][v][2];
-                const int L0 = P.start_pos[b];
-                if (p < L0) {
-                    const int rq = P.req_idx ? P.req_idx[b] : b;
-                    const uint16_t* rowp = P.recent + ((((int64_t)rq * P.W + p % P.W) * P.Hkv + h) * 2 + mat) * D;
-                    cp_async16(dst, rowp + c8 * 8);
-                } else {
-                    const int64_t t = P.cu_new[b] + (p - L0);
-                    const int64_t base = (t * P.Hkv + h) * D + c8 * 8;
-                    if (vec_in && P.kv_dtype == OSCAR_DTYPE_BF16) {
-                        cp_async16(dst, reinterpret_cast<const uint16_t*>(src_new) + base);
-                    } else if (vec_in) {
-                        const float4 f0 = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src_new) + base);
-                        const float4 f1 = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src_new) + base + 4);
-                        *reinterpret_cast<uint4*>(dst) =
-                            make_uint4(pack_bf16(f0.x, f0.y), pack_bf16(f0.z, f0.w), pack_bf16(f1.x, f1.y), pack_bf16(f1.z, f1.w));
-                    } else {
-                        uint32_t w[4];
+    // rows 32·gw .. +31 of a tile into the group's x tile; RPI rows per warp instruction
+    auto gather = [&](int buf) {
+#pragma unroll 4
+        for (int rr = 0; rr < 32; rr += C::RPI) {
+            const int row = 32 * gw + rr + lane / C::CPR, j = lane % C::CPR;
+            unsigned char* dst = A + tc5::sw128_offset(kTcRows, row, j);
+            const int* m = gmeta + (buf * kTcRows + row) * kMetaInts;
+            const int kind = m[1] >> 16;
+            const int64_t off = *reinterpret_cast<const int64_t*>(m + 2) + 8 * j;
+            if (kind == 1) {
+                cp_async16(dst, P.recent + off);
+            } else if (kind == 2 && vec_in && P.kv_dtype == OSCAR_DTYPE_BF16) {
+                cp_async16(dst, reinterpret_cast<const uint16_t*>(src_new) + off);
+            } else if (kind == 2 && vec_in) {
+                const float4 f0 = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src_new) + off);
+                const float4 f1 = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src_new) + off + 4);
+                *reinterpret_cast<uint4*>(dst) =
+                    make_uint4(pack_bf16(f0.x, f0.y), pack_bf16(f0.z, f0.w), pack_bf16(f1.x, f1.y), pack_bf16(f1.z, f1.w));
+            } else if (kind == 2) {
+                uint32_t w[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = (uint32_t)f32_to_bf16_bits(load_elem(src_new, base + 2 * e, P.kv_dtype)) |
-                                   ((uint32_t)f32_to_bf16_bits(load_elem(src_new, base + 2 * e + 1, P.kv_dtype)) << 16);
-                        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                }
+                for (int q = 0; q < 4; ++q)
+                    w[q] = pack_bf16(load_elem(src_new, off + 2 * q, P.kv_dtype), load_elem(src_new, off + 2 * q + 1, P.kv_dtype));
+                *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
             } else {
                 *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
         cp_async_commit();
     };
-    int buf = 0;
-    resolve(blockIdx.x, 0);
-    __syncthreads();
-    gather(blockIdx.x, 0);
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, buf ^= 1) {
-        const int64_t e0 = tile * kTcVec;
-        const int nvec = (int)(total_vec - e0 < kTcVec ? total_vec - e0 : kTcVec);
-        const int64_t nxt = tile + gridDim.x;
-        if (nxt < ntiles) resolve(nxt, buf ^ 1);
+
+    long long budget = 2000000000LL;            // cycles per MMA wait (~1 s); 0 after a timeout
+    bool aborted = false;
+    uint32_t it = 0;
+    const int64_t step = kSlots * (int64_t)gridDim.x;
+    int64_t tile = blockIdx.x + (int64_t)e * gridDim.x;
+    publish(locate(tile), 0);
+    group_bar(e);
+    if (tile < ntiles) gather(0);
+    Loc pend = locate(tile + step);             // the tile after the current one
+    for (; tile < ntiles; tile += step, ++it) {
+        const int buf = it & 1;
         cp_async_wait<0>();
-        __syncthreads();                 // tile's rows landed; next tile's vectors resolved
-        if (nxt < ntiles) gather(nxt, buf ^ 1);
-        const uint16_t* sXb = sX + buf * kTcVec * XS;
-        int (*meta)[4] = s_meta[buf];
-        // ---- y = x·R for rows 16·warp .. +15: per k-step the parts lo, mid, hi ----
-        const int row0 = 16 * warp;
-        uint32_t a[KS][4];
+        tc5::fence_proxy_async();
+        tc5::fence_before();
+        group_bar(e);                           // the tile's rows are in place; last epilogue's loads done
+        if (gt == 0) {
+            tc5::fence_after();
+            constexpr uint32_t idesc = tc5::idesc_bf16_f32(kTcRows, D);
+            const uint32_t sa = smem_addr(A), sb = smem_addr(sB);
+            const uint32_t dcol = tmem + (uint32_t)(128 * e);
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-            const uint32_t* x0 = reinterpret_cast<const uint32_t*>(sXb + (row0 + r) * XS + 16 * kk);
-            const uint32_t* x8 = reinterpret_cast<const uint32_t*>(sXb + (row0 + r + 8) * XS + 16 * kk);
-            a[kk][0] = x0[j];
-            a[kk][1] = x8[j];
-            a[kk][2] = x0[j + 4];
-            a[kk][3] = x8[j + 4];
+            for (int p = 2; p >= 0; --p)          // lo parts first, hi parts last
+#pragma unroll
+                for (int kk = 0; kk < C::KS; ++kk) {
+                    const uint32_t ao = (uint32_t)((kk >> 2) * kTcRows * 128 + (kk & 3) * 32);
+                    const uint32_t bo = (uint32_t)(p * C::B_PART + (kk >> 2) * D * 128 + (kk & 3) * 32);
+                    tc5::mma_bf16(dcol, tc5::sw128_desc(sa + ao), tc5::sw128_desc(sb + bo), idesc, !(p == 2 && kk == 0));
+                }
+            tc5::commit(bar);
         }
-        // one group of output channels at a time keeps only its G/8 n-tiles live
-        const int v0 = row0 + r;
-        const int slot0 = v0 < nvec ? meta[v0][3] : -1;
-        const int slot1 = v0 + 8 < nvec ? meta[v0 + 8][3] : -1;
-#pragma unroll 1
+        const int64_t nxt = tile + step;
+        publish(pend, buf ^ 1);                 // tile nxt: its page-table load was started one iteration ago
+        pend = locate(nxt + step);
+        bool to = !mbar_wait_bounded(bar, it & 1, P.status, budget);
+        tc5::fence_after();
+        if (group_bar_or(e, to)) {              // MMAs done (A free); next tile's vectors resolved
+            aborted = true;
+            break;
+        }
+        if (nxt < ntiles) gather(buf ^ 1);
+
+        // ---- quantise vector gt of the tile ----
+        const int* m = gmeta + (buf * kTcRows + gt) * kMetaInts;
+        const int slot = m[0];
+        uint8_t* rec = P.records + ((int64_t)(slot < 0 ? 0 : slot) * P.Hkv + (m[1] & 0xFFFF)) * P.rec_bytes;
+        uint32_t words[NW];
+        constexpr int NC = G / 32;                // 32-channel chunks per group
+        constexpr bool kKeep = G <= 64;           // the group's y stays in registers between the passes
+#pragma unroll
         for (int gi = 0; gi < ng; ++gi) {
-            float y[lpg][4];
+            float yk[kKeep ? NC : 1][32];
+            float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
-            for (int t = 0; t < lpg; ++t) {
-                const int nt = gi * lpg + t;
+            for (int c = 0; c < NC; ++c) {
+                float (&y)[32] = yk[kKeep ? c : 0];
+                load_y(tacc + gi * G + 32 * c, y);
+                minmax32(y, mn, mx);
+            }
+            const float lo = __fmul_rn(rclip, mn);
+            const float hi = __fmul_rn(rclip, mx);
+            const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 3.0f));
+            const __half z16 = __float2half_rn(lo);
+            const float sc = __half2float(s16), zc = __half2float(z16);
+            // tcgen05.ld is warp-collective: every lane runs the same loads.  A flat
+            // group (s = 0) takes r3 = 0, so its fast-path codes are all 0.
+            const float r3 = sc != 0.0f ? __frcp_rn(3.0f * sc) : 0.0f;   // 3·sc is exact (11-bit significand × 3)
+            uint32_t tie = 0xFFFFFFFFu;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) y[t][e] = 0.f;
+            for (int c = 0; c < NC; ++c) {
+                if (!kKeep) load_y(tacc + gi * G + 32 * c, yk[0]);
+                codes32<false>(yk[kKeep ? c : 0], zc, sc, r3, words[gi * (G / 16) + 2 * c],
+                               words[gi * (G / 16) + 2 * c + 1], tie);
+            }
+            if (__any_sync(0xffffffffu, !(tie >> 31))) {   // a quotient near a tie: decide the group exactly
 #pragma unroll
-                for (int kk = 0; kk < KS; ++kk) {
-                    float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int p = 2; p >= 0; --p) {
-                        const uint2 bb = fragB[((p * KS + kk) * NTL + nt) * 32 + lane];
-                        mma_bf16(d, a[kk][0], a[kk][1], a[kk][2], a[kk][3], bb.x, bb.y);
-                    }
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) y[t][e] += d[e];
+                for (int c = 0; c < NC; ++c) {
+                    if (!kKeep) load_y(tacc + gi * G + 32 * c, yk[0]);
+                    codes32<true>(yk[kKeep ? c : 0], zc, sc, r3, words[gi * (G / 16) + 2 * c],
+                                  words[gi * (G / 16) + 2 * c + 1], tie);
                 }
             }
-            // ---- quantise rows r (values y[.][0..1]) and r + 8 (y[.][2..3]) ----
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int v = v0 + 8 * hf;
-                const int slot = hf ? slot1 : slot0;
-                float mn = INFINITY, mx = -INFINITY;
-#pragma unroll
-                for (int t = 0; t < lpg; ++t) {
-                    mn = fminf(mn, fminf(y[t][2 * hf], y[t][2 * hf + 1]));
-                    mx = fmaxf(mx, fmaxf(y[t][2 * hf], y[t][2 * hf + 1]));
-                }
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float lo = __fmul_rn(rclip, mn);
-                const float hi = __fmul_rn(rclip, mx);
-                const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 3.0f));
-                const __half z16 = __float2half_rn(lo);
-                const float sc = __half2float(s16), zc = __half2float(z16);
-#pragma unroll
-                for (int t = 0; t < lpg; ++t) {
-                    uint32_t nib = 0;
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        uint32_t c = 0;
-                        if (sc != 0.0f) {
-                            const float u = __fdiv_rn(__fsub_rn(y[t][2 * hf + e], zc), sc);
-                            c = (uint32_t)fminf(fmaxf(rintf(u), 0.0f), 3.0f);
-                        }
-                        nib |= c << (2 * e);
-                    }
-                    // channels 8nt + 2j, +1: bits 4·(j & 1) of byte 2nt + j/2
-                    const uint32_t other = __shfl_xor_sync(0xffffffffu, nib, 1);
-                    if ((j & 1) == 0) sC[v * CB + 2 * (gi * lpg + t) + (j >> 1)] = (uint8_t)(nib | (other << 4));
-                }
-                if (j == 0 && slot >= 0) {
-                    uint8_t* rec = P.records + ((int64_t)slot * P.Hkv + meta[v][2]) * P.rec_bytes;
-                    *reinterpret_cast<__half2*>(rec + rec_off_sz + 4 * gi) = __halves2half2(s16, z16);
-                }
-            }
+            if (slot >= 0) *reinterpret_cast<__half2*>(rec + rec_off_sz + 4 * gi) = __halves2half2(s16, z16);
         }
-        __syncwarp();
-        // ---- codes of the warp's 16 rows: 16-byte stores ----
-        for (int i = lane; i < 16 * (CB / 16); i += 32) {
-            const int v = row0 + i / (CB / 16), q = i % (CB / 16);
-            const int slot = v < nvec ? meta[v][3] : -1;
-            if (slot >= 0) {
-                uint8_t* rec = P.records + ((int64_t)slot * P.Hkv + meta[v][2]) * P.rec_bytes;
-                *reinterpret_cast<uint4*>(rec + rec_off_codes + 16 * q) = *reinterpret_cast<const uint4*>(sC + v * CB + 16 * q);
-            }
+        if (slot >= 0) {
+#pragma unroll
+            for (int q = 0; q < NW / 4; ++q)
+                *reinterpret_cast<uint4*>(rec + rec_off_codes + 16 * q) =
+                    make_uint4(words[4 * q], words[4 * q + 1], words[4 * q + 2], words[4 * q + 3]);
         }
-        __syncthreads();
+    }
+    if (aborted) {                                // the group's last MMAs may still run: bounded drain
+        long long drain = 2000000000LL;
+        mbar_wait_bounded(bar, it & 1, P.status, drain);
+    }
+    cp_async_wait<0>();
+    tc5::fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc5::fence_after();
+        tc5::dealloc(tmem, kTmemCols);
     }
 }
 
 template <int D, int G>
 static int launch_tc(const AppendParams& P, int64_t max_vec, cudaStream_t stream) {
-    constexpr int KS = D / 16, NTL = D / 8, XS = D + 8, CB = D / 4;
-    const size_t smem = (size_t)3 * KS * NTL * 32 * 8 + (size_t)2 * kTcVec * XS * 2 + (size_t)kTcVec * CB +
-                        (size_t)(P.batch + 1 + kTcThreads) * 4;
+    using C = TcCfg<D>;
+    // at least 116 KB, so that one CTA (and one tensor-memory allocation) sits on each SM
+    const size_t smem = std::max<size_t>(C::SMEM + (size_t)(P.batch + 1 + kTcThreads) * 4, 116 * 1024);
     auto kern = quantize_tc_kernel<D, G>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return check_cuda("cudaFuncSetAttribute(quantize_tc_kernel)");
-    const int64_t tiles = (max_vec + kTcVec - 1) / kTcVec;
-    const int64_t grid_x = std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)sm_count() / 2));
+    const int64_t tiles = (max_vec + kTcRows - 1) / kTcRows;
+    const int64_t grid_x = std::max<int64_t>(1, std::min<int64_t>((tiles + kSlots - 1) / kSlots, (int64_t)sm_count() / 2));
     kern<<<dim3((unsigned)grid_x, 2), kTcThreads, smem, stream>>>(P);
     return check_cuda("quantize_tc_kernel launch");
 }

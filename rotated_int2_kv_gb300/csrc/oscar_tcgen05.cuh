@@ -1,0 +1,100 @@
+// Fifth-generation tensor core primitives (tcgen05, sm_100 family) as inline
+// PTX: tensor-memory allocation, the shared-memory and instruction descriptors
+// of kind::f16 MMAs with bf16 operands and fp32 accumulators, the MMA itself,
+// its completion on an mbarrier, and tensor-memory loads.
+//
+// Operand layout used throughout: K-major tiles with the 128-byte swizzle.  A
+// tile of R rows × K bf16 elements is stored as K/64 blocks of R rows × 128 B
+// (block b holds elements 64b .. 64b+63 of every row); row r of a block starts
+// at 128·r and its 16-byte chunk j sits at chunk position j ^ (r mod 8).  Each
+// block starts on a 1024-byte boundary, so the hardware's address-based
+// swizzle matches this placement, and 8-row groups are 1024 B apart (the
+// descriptor's stride offset).  The k-step kk (16 elements, 32 B) of a tile
+// starts at block kk/4, byte 32·(kk mod 4).
+#pragma once
+
+#include <stdint.h>
+
+#include "oscar_device.cuh"
+
+namespace oscar {
+namespace tc5 {
+
+// Byte offset of the 16-byte chunk j (elements 8j .. 8j+7) of row r in a
+// swizzled K-major tile of `rows` rows.
+__host__ __device__ constexpr uint32_t sw128_offset(int rows, int r, int j) {
+    return (uint32_t)(j >> 3) * (uint32_t)rows * 128u + (uint32_t)r * 128u +
+           (uint32_t)(((j & 7) ^ (r & 7)) << 4);
+}
+
+// Shared-memory matrix descriptor: start address, leading byte offset 16 (not
+// used by swizzled K-major tiles), stride byte offset 1024, descriptor version
+// 1, base offset 0, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(16u >> 4) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, no negation or sparsity, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] · B[smem]ᵀ (one thread issues it for the CTA).
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate) : "memory");
+}
+
+// Arrives once on `bar` when every MMA this thread issued before has completed.
+__device__ __forceinline__ void commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(smem_addr(bar)) : "memory");
+}
+
+// Tensor-memory allocation by one whole warp; the column base is written to
+// *dst (shared memory).  ncols: a power of two >= 32.
+__device__ __forceinline__ void alloc(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_addr(dst)), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy reads (the tensor core's operand fetches).
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane (the warp
+// reads lanes 32·(warp mod 4) .. +31; taddr carries the lane in bits 16-31).
+__device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t* u = reinterpret_cast<uint32_t*>(v);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15]),
+          "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]),
+          "=r"(u[24]), "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]), "=r"(u[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+}  // namespace tc5
+}  // namespace oscar

@@ -23,8 +23,17 @@ def _rotations(d, seed=SEED):
     return Rk.astype(np.float32), Rv.astype(np.float32)
 
 
+def _misaligned(t):
+    """A copy of t whose data pointer is one element past a 16-byte boundary."""
+    buf = torch.empty(t.numel() + 8, dtype=t.dtype, device=t.device)
+    out = buf[1:1 + t.numel()].view(t.shape)
+    out.copy_(t)
+    assert out.data_ptr() % 16 != 0
+    return out
+
+
 def run_append_scenario(d, Hq, Hkv, G, S, W, kv_dtype, calls, clip=0.9, mode="fixed4", pool_extra=37,
-                        seed=SEED):
+                        seed=SEED, unaligned=False):
     from rotated_int2_kv_gb300 import ops
     B = len(calls[0])
     Lfin = [sum(c[b] for c in calls) for b in range(B)]
@@ -49,7 +58,10 @@ def run_append_scenario(d, Hq, Hkv, G, S, W, kv_dtype, calls, clip=0.9, mode="fi
         k = torch.cat(ks)
         v = torch.cat(vs)
         cu = np.concatenate([[0], np.cumsum(call)]).astype(np.int32)
-        ops.quantize_append(dc, k.to(dev), v.to(dev), torch.from_numpy(cu).to(dev),
+        kd, vd = k.to(dev), v.to(dev)
+        if unaligned:
+            kd, vd = _misaligned(kd), _misaligned(vd)
+        ops.quantize_append(dc, kd, vd, torch.from_numpy(cu).to(dev),
                             torch.tensor(pos, dtype=torch.int32, device=dev), pt.to(dev), req_idx=req.to(dev))
         oc.append(k.float().numpy(), v.float().numpy(), cu, pos, req.numpy(), pt.numpy(), keep_y=True)
         pos = [pos[b] + call[b] for b in range(B)]
@@ -103,6 +115,19 @@ def test_gqa8_per_head_outliers():
 @pytest.mark.parametrize("d,G", [(256, 256), (256, 32), (128, 128), (64, 64), (128, 32)])
 def test_group_sizes(d, G):
     run_append_scenario(d, 2, 1, G, 16, 32, torch.bfloat16, [[300], [1], [77]])
+
+
+@pytest.mark.parametrize("d,G,dtype,unaligned", [
+    (128, 64, torch.bfloat16, False), (128, 32, torch.bfloat16, False), (128, 128, torch.float32, False),
+    (64, 64, torch.bfloat16, False), (64, 32, torch.float32, False), (128, 64, torch.bfloat16, True),
+    (256, 128, torch.bfloat16, False)])
+def test_large_appends_tiled_path(d, G, dtype, unaligned):
+    # the second call moves 12,600+ vectors into the history (the tiled kernels:
+    # tensor cores for d <= 128, fp32 FMA for d = 256): the ring's spilled tokens
+    # and new ones, a ragged last tile
+    calls = [[300, 290, 13], [2600, 2700, 1001]]
+    st = run_append_scenario(d, 8, 2, G, 64, 256, dtype, calls, unaligned=unaligned)
+    assert st["exact"] > 0
 
 
 def test_decode_step_appends_spill_every_step():
