@@ -23,8 +23,9 @@
 // vectors), its own accumulator in tensor memory and its own mbarrier; one
 // thread of the group issues the group's MMAs.  A group's flow per tile: wait for its
 // rows, issue the MMAs, finish resolving the next tile's vectors and start the
-// page-table loads of the one after, wait for the MMAs, start copying the next
-// tile's rows (16-byte cp.async), then quantise: thread
+// page-table loads of the one after, wait for the MMAs, start the next tile's
+// rows (one tensor-map TMA load when they are a contiguous block of the bf16
+// input, else 16-byte cp.async per chunk), then quantise: thread
 // i of the group owns tensor-memory lane i, that is vector i of the tile and
 // all its d channels, so a group's min / max is a reduction in registers.
 //
@@ -36,6 +37,9 @@
 // Tensor-memory loads (tcgen05.ld) are warp-collective, so every branch around
 // them is warp-uniform.
 #include <algorithm>
+#include <cstring>
+
+#include <cuda.h>
 
 #include "oscar_append_common.cuh"
 #include "oscar_tcgen05.cuh"
@@ -170,13 +174,15 @@ struct TcCfg {
     static constexpr int CPR = D / 8;               // 16-byte chunks per row
     static constexpr int RPI = 32 / CPR;            // rows per warp instruction in the copy
     static constexpr size_t SMEM = 1024 + 3 * (size_t)B_PART + kSlots * (size_t)A_BYTES +
-                                   (size_t)kSlots * 2 * kTcRows * kMetaInts * 4 + 64;   // + prefix, scratch
+                                   (size_t)kSlots * 2 * kTcRows * kMetaInts * 4 + 128;   // + prefix, scratch
 };
 
 }  // namespace
 
 template <int D, int G>
-__global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(AppendParams P) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   int use_tma) {
     using C = TcCfg<D>;
     constexpr int ng = D / G;
     constexpr int NW = D / 16;                      // code words per vector
@@ -186,8 +192,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(AppendParams
     unsigned char* sB = smem;                                               // [3 parts][D rows][D] swizzled
     unsigned char* sA = smem + 3 * C::B_PART;                               // [slots][128 rows][D] swizzled
     int* meta = reinterpret_cast<int*>(sA + kSlots * C::A_BYTES);          // [slots][2 buffers][128][4]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(meta + kSlots * 2 * kTcRows * kMetaInts);   // [slots]
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kSlots);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(meta + kSlots * 2 * kTcRows * kMetaInts);   // [slots] MMAs done
+    uint64_t* fulls = bars + kSlots;                                        // [slots] TMA rows landed
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(fulls + kSlots);
     int* prefix = reinterpret_cast<int*>(tslot + 2);                       // batch + 1
     int* scratch = prefix + P.batch + 1;                                    // kTcThreads
 
@@ -205,7 +212,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(AppendParams
     if ((int64_t)blockIdx.x >= ntiles) return;    // uniform over the CTA, before any allocation
 
     if (tid == 0) {
-        for (int q = 0; q < kSlots; ++q) mbar_init(&bars[q], 1);
+        for (int q = 0; q < kSlots; ++q) {
+            mbar_init(&bars[q], 1);
+            mbar_init(&fulls[q], 1);
+        }
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -235,6 +245,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(AppendParams
     unsigned char* A = sA + e * C::A_BYTES;
     int* gmeta = meta + e * 2 * kTcRows * kMetaInts;
     uint64_t* bar = &bars[e];
+    uint64_t* full = &fulls[e];
+    const CUtensorMap* tmap = mat ? &tm_v : &tm_k;
     const uint32_t tacc = tmem + (uint32_t)(128 * e) + ((uint32_t)(32 * gw) << 16);
 
     // Vector gt of a tile is resolved in two stages one loop iteration apart, so
@@ -250,8 +262,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(AppendParams
         Loc L{0, 0, 0, -1, false};
         const int64_t ev = tile * kTcRows + gt;
         if (tile < ntiles && ev < total_vec) {
-            const int u = (int)(ev / P.Hkv);
-            L.h = (int)(ev % P.Hkv);
+            int u;
+            if (total_vec <= 0x7FFFFFFF) {       // 32-bit index arithmetic (uniform branch)
+                u = (int)((uint32_t)ev / (uint32_t)P.Hkv);
+                L.h = (int)((uint32_t)ev - (uint32_t)u * (uint32_t)P.Hkv);
+            } else {
+                u = (int)(ev / P.Hkv);
+                L.h = (int)(ev % P.Hkv);
+            }
             L.b = find_request(prefix, P.batch, u);
             L.p = hist_hi(P.start_pos[L.b], P.S, P.W) + (u - prefix[L.b]);
             L.valid = true;
@@ -298,9 +316,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(AppendParams
         for (int rr = 0; rr < 32; rr += C::RPI) {
             const int row = 32 * gw + rr + lane / C::CPR, j = lane % C::CPR;
             unsigned char* dst = A + tc5::sw128_offset(kTcRows, row, j);
-            const int* m = gmeta + (buf * kTcRows + row) * kMetaInts;
-            const int kind = m[1] >> 16;
-            const int64_t off = *reinterpret_cast<const int64_t*>(m + 2) + 8 * j;
+            const int4 m = *reinterpret_cast<const int4*>(gmeta + (buf * kTcRows + row) * kMetaInts);
+            const int kind = m.y >> 16;
+            const int64_t off = (int64_t)(((uint64_t)(uint32_t)m.w << 32) | (uint32_t)m.z) + 8 * j;
             if (kind == 1) {
                 cp_async16(dst, P.recent + off);
             } else if (kind == 2 && vec_in && P.kv_dtype == OSCAR_DTYPE_BF16) {
@@ -323,46 +341,101 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(AppendParams
         cp_async_commit();
     };
 
+    // A tile whose valid rows are all new input, row r at row 0's offset + r·d,
+    // is one 128 × d block of the input: a tensor-map (TMA) load of two 64-wide
+    // boxes lands it in the swizzled layout directly.  Called after the group
+    // barrier that follows publish(buf); uniform over the group.
+    auto contiguous = [&](int buf) -> bool {
+        const int4 m0 = *reinterpret_cast<const int4*>(gmeta + buf * kTcRows * kMetaInts);
+        const int4 m = *reinterpret_cast<const int4*>(gmeta + (buf * kTcRows + gt) * kMetaInts);
+        const int64_t off0 = (int64_t)(((uint64_t)(uint32_t)m0.w << 32) | (uint32_t)m0.z);
+        const int64_t off = (int64_t)(((uint64_t)(uint32_t)m.w << 32) | (uint32_t)m.z);
+        const bool row_ok = m.x < 0 || ((m.y >> 16) == 2 && off == off0 + (int64_t)gt * D);
+        const bool head_ok = m0.x >= 0 && (m0.y >> 16) == 2;
+        return !group_bar_or(e, !(row_ok && head_ok));
+    };
+    auto issue_tma = [&](int buf) {
+        if (gt == 0) {
+            const int4 m0 = *reinterpret_cast<const int4*>(gmeta + buf * kTcRows * kMetaInts);
+            const int64_t off0 = (int64_t)(((uint64_t)(uint32_t)m0.w << 32) | (uint32_t)m0.z);
+            mbar_arrive_expect_tx(full, (uint32_t)C::A_BYTES);
+#pragma unroll
+            for (int xb = 0; xb < D / 64; ++xb)
+                tc5::tma_load_2d(A + xb * kTcRows * 128, tmap, 64 * xb, (int)(off0 / D), full);
+        }
+    };
+
     long long budget = 2000000000LL;            // cycles per MMA wait (~1 s); 0 after a timeout
     bool aborted = false;
     uint32_t it = 0;
     const int64_t step = kSlots * (int64_t)gridDim.x;
     int64_t tile = blockIdx.x + (int64_t)e * gridDim.x;
+    uint32_t tma_n = 0;                         // TMA tiles of this slot so far (parity of `full`)
+    bool cur_tma = false;                       // the current tile's rows come by TMA
+    int drain_full = -1, drain_mma = -1;        // parities still to wait for after an abort
     publish(locate(tile), 0);
     group_bar(e);
-    if (tile < ntiles) gather(0);
+    if (tile < ntiles) {
+        cur_tma = use_tma && contiguous(0);
+        if (cur_tma) issue_tma(0);
+        else gather(0);
+    }
     Loc pend = locate(tile + step);             // the tile after the current one
     for (; tile < ntiles; tile += step, ++it) {
         const int buf = it & 1;
-        cp_async_wait<0>();
-        tc5::fence_proxy_async();
+        bool to = false;
+        if (cur_tma) {
+            if (gt == 0 && !mbar_wait_bounded(full, tma_n & 1, P.status, budget)) {
+                to = true;
+                drain_full = (int)(tma_n & 1);
+            }
+            ++tma_n;
+        } else {
+            cp_async_wait<0>();
+            tc5::fence_proxy_async();
+        }
         tc5::fence_before();
-        group_bar(e);                           // the tile's rows are in place; last epilogue's loads done
+        if (group_bar_or(e, to)) {              // the tile's rows are in place; last epilogue's loads done
+            aborted = true;
+            break;
+        }
         if (gt == 0) {
             tc5::fence_after();
             constexpr uint32_t idesc = tc5::idesc_bf16_f32(kTcRows, D);
-            const uint32_t sa = smem_addr(A), sb = smem_addr(sB);
+            const uint64_t ad0 = tc5::sw128_desc(smem_addr(A)), bd0 = tc5::sw128_desc(smem_addr(sB));
             const uint32_t dcol = tmem + (uint32_t)(128 * e);
 #pragma unroll
             for (int p = 2; p >= 0; --p)          // lo parts first, hi parts last
 #pragma unroll
                 for (int kk = 0; kk < C::KS; ++kk) {
+                    // the start address (bits 0-13, in 16-byte units) advances by the
+                    // k-step's byte offset; it stays below 2^14, so no carry leaves the field
                     const uint32_t ao = (uint32_t)((kk >> 2) * kTcRows * 128 + (kk & 3) * 32);
                     const uint32_t bo = (uint32_t)(p * C::B_PART + (kk >> 2) * D * 128 + (kk & 3) * 32);
-                    tc5::mma_bf16(dcol, tc5::sw128_desc(sa + ao), tc5::sw128_desc(sb + bo), idesc, !(p == 2 && kk == 0));
+                    tc5::mma_bf16(dcol, ad0 + (ao >> 4), bd0 + (bo >> 4), idesc, !(p == 2 && kk == 0));
                 }
             tc5::commit(bar);
         }
         const int64_t nxt = tile + step;
         publish(pend, buf ^ 1);                 // tile nxt: its page-table load was started one iteration ago
         pend = locate(nxt + step);
-        bool to = !mbar_wait_bounded(bar, it & 1, P.status, budget);
-        tc5::fence_after();
+        // one thread observes the MMAs' completion; the group barrier passes it on
+        to = false;
+        if (gt == 0 && !mbar_wait_bounded(bar, it & 1, P.status, budget)) {
+            to = true;
+            drain_mma = (int)(it & 1);
+        }
         if (group_bar_or(e, to)) {              // MMAs done (A free); next tile's vectors resolved
             aborted = true;
             break;
         }
-        if (nxt < ntiles) gather(buf ^ 1);
+        tc5::fence_after();
+        cur_tma = false;
+        if (nxt < ntiles) {
+            cur_tma = use_tma && contiguous(buf ^ 1);
+            if (cur_tma) issue_tma(buf ^ 1);
+            else gather(buf ^ 1);
+        }
 
         // ---- quantise vector gt of the tile ----
         const int* m = gmeta + (buf * kTcRows + gt) * kMetaInts;
@@ -413,9 +486,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(AppendParams
                     make_uint4(words[4 * q], words[4 * q + 1], words[4 * q + 2], words[4 * q + 3]);
         }
     }
-    if (aborted) {                                // the group's last MMAs may still run: bounded drain
+    if (aborted && gt == 0) {                     // copies or MMAs of the slot may still run: bounded drain
         long long drain = 2000000000LL;
-        mbar_wait_bounded(bar, it & 1, P.status, drain);
+        if (drain_full >= 0) mbar_wait_bounded(full, (uint32_t)drain_full, P.status, drain);
+        if (drain_mma >= 0) mbar_wait_bounded(bar, (uint32_t)drain_mma, P.status, drain);
     }
     cp_async_wait<0>();
     tc5::fence_before();
@@ -425,6 +499,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(AppendParams
         tc5::dealloc(tmem, kTmemCols);
     }
 }
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, fetched through the runtime (null if absent).
+EncodeTiledFn encode_fn() {
+    static const EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return (EncodeTiledFn) nullptr;
+        }
+        return (EncodeTiledFn)p;
+    }();
+    return fn;
+}
+
+// 2-D map of a [rows][d] bf16 input: boxes of 64 channels × 128 rows with the
+// 128-byte swizzle (the MMA's operand layout); rows past the end read as zero.
+bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int d) {
+    const EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kTcRows};
+    const cuuint32_t es[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
 
 template <int D, int G>
 static int launch_tc(const AppendParams& P, int64_t max_vec, cudaStream_t stream) {
@@ -436,7 +547,15 @@ static int launch_tc(const AppendParams& P, int64_t max_vec, cudaStream_t stream
         return check_cuda("cudaFuncSetAttribute(quantize_tc_kernel)");
     const int64_t tiles = (max_vec + kTcRows - 1) / kTcRows;
     const int64_t grid_x = std::max<int64_t>(1, std::min<int64_t>((tiles + kSlots - 1) / kSlots, (int64_t)sm_count() / 2));
-    kern<<<dim3((unsigned)grid_x, 2), kTcThreads, smem, stream>>>(P);
+    // bf16 inputs on 16-byte boundaries: contiguous tiles arrive by TMA
+    CUtensorMap tk, tv;
+    memset(&tk, 0, sizeof tk);
+    memset(&tv, 0, sizeof tv);
+    const int64_t rows = P.total_new * P.Hkv;
+    const int use_tma = P.kv_dtype == OSCAR_DTYPE_BF16 && rows > 0 && rows < 0x7FFFFFFF &&
+                        (reinterpret_cast<uintptr_t>(P.k) & 15) == 0 && (reinterpret_cast<uintptr_t>(P.v) & 15) == 0 &&
+                        encode_rows(&tk, P.k, rows, D) && encode_rows(&tv, P.v, rows, D);
+    kern<<<dim3((unsigned)grid_x, 2), kTcThreads, smem, stream>>>(P, tk, tv, use_tma);
     return check_cuda("quantize_tc_kernel launch");
 }
 

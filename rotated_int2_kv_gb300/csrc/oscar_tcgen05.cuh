@@ -96,5 +96,14 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
 }
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Tiled TMA load of the box at element coordinates (x, y) of a 2-D tensor map
+// into shared memory, completing (with its byte count) on `bar`.  x·element
+// size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(smem_addr(dst)), "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar)) : "memory");
+}
+
 }  // namespace tc5
 }  // namespace oscar
