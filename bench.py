@@ -475,11 +475,14 @@ def append_measure():
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
+    h0 = time.perf_counter()
     for _ in range(reps):
         ops.quantize_append(cache, k, v, cu, st, pt)
+    host_ms = (time.perf_counter() - h0) * 1e3 / reps     # host time to issue one call
     e1.record()
     torch.cuda.synchronize()
     qms, qn = ops.profile_read(1)
+    wms, wn = ops.profile_read(2)
     ops.profile_enable(False)
     call_ms = e0.elapsed_time(e1) / reps
     hist = L - S_SINK - W_RECENT
@@ -499,6 +502,7 @@ def append_measure():
     return {"workload": "one 32,768-token request appended at once (32,448 INT2 + 320 BF16), "
                         "Qwen3-8B-shaped layer", "value": alg_bytes / (call_ms / 1e3) / 1e9, "unit": "GB/s",
             "ms_per_call": call_ms, "quantize_kernel_ms": kern_ms,
+            "window_copy_kernel_ms": wms / max(wn, 1), "host_ms_per_call": host_ms,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "kernel": "quantize_tc_kernel (tcgen05 rotation + INT2)",
                          "peak_source": "measured hbm_gbs",

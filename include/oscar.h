@@ -259,8 +259,9 @@ int oscar_decode_attention_noalloc(const oscar_config* cfg, const oscar_layer_ca
 /* Enables (1) or disables (0) event timing of the dominant kernels and
  * forgets earlier records.  While enabled, every oscar_decode_attention call
  * records a CUDA event pair around its history kernel (kind 0) and every
- * oscar_quantize_append call around its quantise kernel (kind 1), on the
- * call's stream.  Host-side cost: two cudaEventRecord per call. */
+ * oscar_quantize_append call around its quantise kernel (kind 1) and its
+ * window-copy kernel (kind 2), on the call's stream.  Host-side cost: two
+ * cudaEventRecord per timed kernel. */
 int oscar_profile_enable(int32_t enable);
 
 /* Waits for the recorded events of `kind` and returns their summed duration

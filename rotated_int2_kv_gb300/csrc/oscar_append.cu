@@ -345,9 +345,12 @@ quantize_small_kernel(AppendParams P) {
     }
 }
 
-// Copies each new row to the sink or the recent ring (bf16).  Block (b, y)
-// handles rows y, y + gridDim.y, ... of request b; every thread issues a batch
-// of loads before its stores.
+// Copies the new rows that land in a BF16 window: positions below S go to the
+// sink, positions at or after max(S, L1 - W) to the ring slot p % W; the rows in
+// between enter the history and are the quantise kernel's.  Block (b, y)
+// takes window rows y, y + gridDim.y, ... of request b (sink rows first), so a
+// 32K-token prefill visits its 320 window rows, not all of its rows.  bf16
+// inputs on 16-byte boundaries move in 16-byte chunks (8 channels).
 template <int D>
 __global__ void __launch_bounds__(128)
 window_copy_kernel(AppendParams P) {
@@ -363,33 +366,32 @@ window_copy_kernel(AppendParams P) {
     }
     const int L1 = L0 + n;
     const int hh = hist_hi(L1, P.S, P.W);
-    const int nel = P.Hkv * 2 * D;
-    constexpr int kU = 8;
-    for (int r = blockIdx.y; r < n; r += gridDim.y) {
+    const int s_end = min(n, max(0, P.S - L0));        // rows [0, s_end): sink
+    const int r_beg = min(n, max(s_end, hh - L0));     // rows [r_beg, n): ring
+    const int nwin = s_end + (n - r_beg);
+    const int nel = P.Hkv * 2 * D;                      // one position: [Hkv][K|V][d]
+    const bool vec = P.kv_dtype == OSCAR_DTYPE_BF16 &&
+                     ((reinterpret_cast<uintptr_t>(P.k) | reinterpret_cast<uintptr_t>(P.v)) & 15) == 0;
+    for (int w = blockIdx.y; w < nwin; w += gridDim.y) {
+        const int r = w < s_end ? w : r_beg + (w - s_end);
         const int64_t t = (int64_t)c0 + r;
         if (t >= P.total_new) {
             if (threadIdx.x == 0) set_status(P.status, OSCAR_DEV_BAD_LEN);
             break;
         }
         const int p = L0 + r;
-        uint16_t* dst = nullptr;
-        if (p < P.S) dst = P.sink + ((int64_t)rq * P.S + p) * nel;
-        else if (p >= hh) dst = P.recent + ((int64_t)rq * P.W + p % P.W) * nel;
-        if (!dst) continue;
-        for (int i0 = 0; i0 < nel; i0 += 128 * kU) {
-            float x[kU];
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int i = i0 + threadIdx.x + 128 * u;
-                if (i < nel) {
-                    const int h = i / (2 * D), mat = (i / D) & 1, c = i % D;
-                    x[u] = load_elem(mat ? P.v : P.k, (t * P.Hkv + h) * D + c, P.kv_dtype);
-                }
+        uint16_t* dst = p < P.S ? P.sink + ((int64_t)rq * P.S + p) * nel
+                                : P.recent + ((int64_t)rq * P.W + p % P.W) * nel;
+        if (vec) {
+            for (int ci = threadIdx.x; ci < nel / 8; ci += blockDim.x) {
+                const int h = ci / (D / 4), mat = (ci / (D / 8)) & 1, c8 = ci % (D / 8);
+                const uint16_t* src = reinterpret_cast<const uint16_t*>(mat ? P.v : P.k) + (t * P.Hkv + h) * D + 8 * c8;
+                *reinterpret_cast<uint4*>(dst + 8 * ci) = *reinterpret_cast<const uint4*>(src);
             }
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int i = i0 + threadIdx.x + 128 * u;
-                if (i < nel) dst[i] = f32_to_bf16_bits(x[u]);
+        } else {
+            for (int i = threadIdx.x; i < nel; i += blockDim.x) {
+                const int h = i / (2 * D), mat = (i / D) & 1, c = i % D;
+                dst[i] = f32_to_bf16_bits(load_elem(mat ? P.v : P.k, (t * P.Hkv + h) * D + c, P.kv_dtype));
             }
         }
     }
@@ -404,8 +406,8 @@ static int launch_append(const AppendParams& P, int64_t total_new, cudaStream_t 
     smem += kResidentR ? std::max(xt, y) : xt + y;
     smem += (size_t)(P.batch + 1 + kAppendThreads) * 4;
     auto kern = quantize_kernel<D>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return check_cuda("cudaFuncSetAttribute(quantize_kernel)");
+    if (const int rc_ = ensure_dynamic_smem((const void*)kern, smem, "cudaFuncSetAttribute(quantize_kernel)"))
+        return rc_;
     // Upper bound of the vectors entering the history: a request of L0 cached
     // and n new tokens moves max(S, L0+n-W) - max(S, L0-W) <= n positions.
     const int64_t max_units = total_new;
@@ -418,8 +420,8 @@ static int launch_append(const AppendParams& P, int64_t total_new, cudaStream_t 
     if (max_vec > 0 && max_vec <= (int64_t)sm_count() * kTileVec) {
         // few vectors (decode steps): one warp per vector over many blocks
         const size_t ssmem = (size_t)(P.batch + 1 + kAppendThreads) * 4 + (D * D * 4 <= 64 * 1024 ? D * D * 4 : 0);
-        if (cudaFuncSetAttribute(quantize_small_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem) != cudaSuccess)
-            return check_cuda("cudaFuncSetAttribute(quantize_small_kernel)");
+        if (const int rc_ = ensure_dynamic_smem((const void*)quantize_small_kernel<D>, ssmem, "cudaFuncSetAttribute(quantize_small_kernel)"))
+            return rc_;
         const int64_t gs = std::min<int64_t>((max_vec + kSmallVec - 1) / kSmallVec, (int64_t)sm_count() * 4);
         const int prof = prof_begin(1, stream);
         quantize_small_kernel<D><<<dim3((unsigned)gs, 2), kAppendThreads, ssmem, stream>>>(P);
@@ -440,10 +442,13 @@ static int launch_append(const AppendParams& P, int64_t total_new, cudaStream_t 
         if (rc) return rc;
     }
     if (total_new > 0) {
-        // rows per request are not known on the host: spread each request over up
-        // to ceil(total_new / batch) blocks (at least 1, at most 64)
-        const int64_t gy = std::max<int64_t>(1, std::min<int64_t>(64, (total_new + P.batch - 1) / P.batch));
+        // window rows per request (at most S + W; one per new token for decode
+        // steps) are not known on the host: up to one block per window row
+        const int64_t win = std::min<int64_t>((int64_t)P.S + P.W, (total_new + P.batch - 1) / P.batch);
+        const int64_t gy = std::max<int64_t>(1, win);
+        const int prof = prof_begin(2, stream);
         window_copy_kernel<D><<<dim3((unsigned)P.batch, (unsigned)gy), 128, 0, stream>>>(P);
+        prof_end(prof, stream);
         int rc = check_cuda("window_copy_kernel launch");
         if (rc) return rc;
     }

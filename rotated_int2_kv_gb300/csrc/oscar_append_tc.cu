@@ -222,15 +222,35 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
         tc5::alloc(tslot, kTmemCols);
         tc5::relinquish();
     }
-    // B: part p of R as D rows n (column n of R) × D k, consecutive threads on
-    // consecutive n (coalesced reads of R; the swizzle spreads the stores)
-    for (int i = tid; i < 3 * D * C::CPR; i += kTcThreads) {
-        const int n = i % D, j = (i / D) % C::CPR, p = i / (D * C::CPR);
-        const float* Rc = R + (int64_t)(8 * j) * D + n;
-        uint32_t w[4];
+    // B: the three parts of R as D rows n (column n of R) × D k.  Item (n, j)
+    // reads R[8j .. 8j+7][n] once and stores its 16-byte chunk of every part;
+    // consecutive threads take consecutive n (coalesced reads; the swizzle
+    // spreads the stores), two items in flight per thread.
+    constexpr int NB = D * C::CPR;
+#pragma unroll 1
+    for (int i0 = tid; i0 < NB; i0 += 2 * kTcThreads) {
+        float v[2][8];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) w[q] = pack_bf16(bf16_part(Rc[(2 * q) * D], p), bf16_part(Rc[(2 * q + 1) * D], p));
-        *reinterpret_cast<uint4*>(sB + p * C::B_PART + tc5::sw128_offset(D, n, j)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int u = 0; u < 2; ++u) {
+            const int i = i0 + u * kTcThreads;
+            const int n = i % D, j = i / D;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[u][q] = i < NB ? R[(int64_t)(8 * j + q) * D + n] : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = i0 + u * kTcThreads;
+            if (i >= NB) continue;
+            const int n = i % D, j = i / D;
+#pragma unroll
+            for (int p = 0; p < 3; ++p) {
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) w[q] = pack_bf16(bf16_part(v[u][2 * q], p), bf16_part(v[u][2 * q + 1], p));
+                *reinterpret_cast<uint4*>(sB + p * C::B_PART + tc5::sw128_offset(D, n, j)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
     }
     tc5::fence_proxy_async();
     tc5::fence_before();
@@ -543,8 +563,8 @@ static int launch_tc(const AppendParams& P, int64_t max_vec, cudaStream_t stream
     // at least 116 KB, so that one CTA (and one tensor-memory allocation) sits on each SM
     const size_t smem = std::max<size_t>(C::SMEM + (size_t)(P.batch + 1 + kTcThreads) * 4, 116 * 1024);
     auto kern = quantize_tc_kernel<D, G>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return check_cuda("cudaFuncSetAttribute(quantize_tc_kernel)");
+    if (const int rc_ = ensure_dynamic_smem((const void*)kern, smem, "cudaFuncSetAttribute(quantize_tc_kernel)"))
+        return rc_;
     const int64_t tiles = (max_vec + kTcRows - 1) / kTcRows;
     const int64_t grid_x = std::max<int64_t>(1, std::min<int64_t>((tiles + kSlots - 1) / kSlots, (int64_t)sm_count() / 2));
     // bf16 inputs on 16-byte boundaries: contiguous tiles arrive by TMA

@@ -706,15 +706,17 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
 template <int D>
 static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
     const size_t psmem = D * D * 4 <= 64 * 1024 ? (size_t)D * D * 4 : 0;
-    if (psmem && cudaFuncSetAttribute(prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem) != cudaSuccess)
-        return check_cuda("cudaFuncSetAttribute(prep_kernel)");
+    if (psmem) {
+        if (const int rc_ = ensure_dynamic_smem((const void*)prep_kernel<D>, psmem, "cudaFuncSetAttribute(prep_kernel)"))
+            return rc_;
+    }
     prep_kernel<D><<<dim3(P.batch, (P.Hq + kPrepHeads - 1) / kPrepHeads), 256, psmem, st>>>(P);
     int rc = check_cuda("prep_kernel launch");
     if (rc) return rc;
     const size_t wsmem = ((size_t)P.g * D + (size_t)P.g * kWinTile + 2 * P.g) * 4 +
                          (size_t)2 * kWinTile * (D / 2 + 1) * 4;
-    if (cudaFuncSetAttribute(window_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsmem) != cudaSuccess)
-        return check_cuda("cudaFuncSetAttribute(window_kernel)");
+    if (const int rc_ = ensure_dynamic_smem((const void*)window_kernel<D>, wsmem, "cudaFuncSetAttribute(window_kernel)"))
+        return rc_;
     window_kernel<D><<<dim3(P.Hkv, P.batch, P.n_win_tiles), kCombThreads, wsmem, st>>>(P);
     rc = check_cuda("window_kernel launch");
     if (rc) return rc;
@@ -730,8 +732,8 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
         const int gq = P.g <= 4 ? 4 : (P.g <= 8 ? 8 : 16);
         const size_t smem = ((size_t)P.Hq * D + (size_t)nwarps * gq * 32) * 4;
         auto pick = [&](auto kern) -> int {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-                return check_cuda("cudaFuncSetAttribute(history_simt_kernel)");
+            if (const int rc_ = ensure_dynamic_smem((const void*)kern, smem, "cudaFuncSetAttribute(history_simt_kernel)"))
+                return rc_;
             int per_sm = 0;
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
             const int grid = std::min(P.n_ctas, std::max(1, sm_count() * std::max(1, per_sm)));
@@ -747,8 +749,8 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
     prof_end(prof, st);
     const size_t csmem = ((size_t)P.g * D * 2 + (size_t)P.g * 4 + (size_t)P.g * P.n_win_tiles +
                           (size_t)P.g * ((size_t)P.n_ctas * P.par + 2)) * 4;
-    if (cudaFuncSetAttribute(combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem) != cudaSuccess)
-        return check_cuda("cudaFuncSetAttribute(combine_kernel)");
+    if (const int rc_ = ensure_dynamic_smem((const void*)combine_kernel<D>, csmem, "cudaFuncSetAttribute(combine_kernel)"))
+        return rc_;
     combine_kernel<D><<<dim3(P.Hkv, P.batch), kMergeThreads, csmem, st>>>(P);
     return check_cuda("combine_kernel launch");
 }

@@ -797,8 +797,8 @@ static int launch_mma(DecodeParams P, cudaStream_t st) {
     if (!mma_smem_plan<D, G, NT, WPH, TTOK, PAR>(P.Hkv, &x_off, &stages_off, &ns_log2, &smem))
         return OSCAR_ERR_ARG;
     auto kern = history_mma_kernel<D, G, NT, WPH, TTOK, PAR, HKV>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return check_cuda("cudaFuncSetAttribute(history_mma_kernel)");
+    if (const int rc_ = ensure_dynamic_smem((const void*)kern, smem, "cudaFuncSetAttribute(history_mma_kernel)"))
+        return rc_;
     const int grid = std::min(P.n_ctas, sm_count());
     const int trow = row_bytes(P.Hkv * MmaCfg<D, G, NT, WPH, TTOK>::REC);
     kern<<<grid, threads, smem, st>>>(P, x_off, stages_off, trow, ns_log2);

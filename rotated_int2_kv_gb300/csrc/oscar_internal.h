@@ -47,6 +47,9 @@ int sm_count();
 
 // Converts the pending CUDA error (if any) into OSCAR_ERR_CUDA.
 int check_cuda(const char* what);
+// Sets the kernel's dynamic shared-memory limit to at least `bytes` (once per
+// device and size); OSCAR_OK or the CUDA error, reported as `what`.
+int ensure_dynamic_smem(const void* kernel, size_t bytes, const char* what);
 
 // Benchmark timing of the dominant kernels (see oscar_profile_enable).
 int prof_begin(int kind, cudaStream_t st);   // returns a slot or -1 when disabled

@@ -1,6 +1,9 @@
 // Runtime helpers of liboscar.so: the per-device status word written by the
 // kernels' bounds checks, the SM count used to size persistent grids, and the
 // mapping of CUDA runtime errors to OSCAR_ERR_CUDA.
+#include <mutex>
+#include <unordered_map>
+
 #include <cuda_runtime.h>
 
 #include "oscar_internal.h"
@@ -18,6 +21,26 @@ static int current_device() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
     return dev;
+}
+
+// Largest dynamic shared-memory size already granted per (device, kernel): the
+// attribute is set only when a launch needs more, not on every call.
+int ensure_dynamic_smem(const void* kernel, size_t bytes, const char* what) {
+    const int dev = current_device();
+    if (dev < 0) return fail(OSCAR_ERR_CUDA, "no current CUDA device");
+    static std::mutex mu;
+    static std::unordered_map<const void*, size_t> granted[kMaxDevices];
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = granted[dev].find(kernel);
+        if (it != granted[dev].end() && it->second >= bytes) return OSCAR_OK;
+    }
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+        return check_cuda(what);
+    std::lock_guard<std::mutex> lock(mu);
+    size_t& g = granted[dev][kernel];
+    if (bytes > g) g = bytes;
+    return OSCAR_OK;
 }
 
 int* status_word() {
