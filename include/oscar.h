@@ -275,6 +275,16 @@ int oscar_profile_read(int32_t kind, double* total_ms, int64_t* launches);
  * `clear` is non-zero.  Returns OSCAR_ERR_CUDA if the device cannot be read. */
 int oscar_device_status(int32_t* flags, int32_t clear);
 
+/* Self-test of the bounded pipeline wait that the kernels use on their
+ * mbarriers.  One warp waits for phase 0 of a shared-memory mbarrier for at
+ * most `budget_cycles` SM clock cycles (clamped to [1,000, 4e9]).  With
+ * `complete` = 0 nothing ever arrives, so the wait runs out: it sets
+ * OSCAR_DEV_TIMEOUT in the device status word and the kernel returns, leaving
+ * the context usable.  With `complete` = 1 the barrier is completed first and
+ * no bit is set.  Asynchronous on `stream`; read the result with
+ * oscar_device_status. */
+int oscar_selftest_bounded_wait(int64_t budget_cycles, int32_t complete, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

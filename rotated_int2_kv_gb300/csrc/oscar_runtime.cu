@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "oscar_internal.h"
+#include "oscar_device.cuh"
 
 namespace oscar {
 
@@ -170,4 +171,33 @@ extern "C" int oscar_profile_read(int32_t kind, double* total_ms, int64_t* launc
     *total_ms = ms;
     *launches = n;
     return OSCAR_OK;
+}
+
+namespace oscar {
+
+// One warp waits (bounded) for phase 0 of an mbarrier that receives its single
+// arrival only when `complete` is set.
+__global__ void __launch_bounds__(32) selftest_wait_kernel(int* status, long long budget, int complete) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (complete && threadIdx.x == 0) mbar_arrive(&bar);
+    __syncwarp();
+    long long b = budget;
+    mbar_wait_bounded(&bar, 0, status, b);
+}
+
+}  // namespace oscar
+
+extern "C" int oscar_selftest_bounded_wait(int64_t budget_cycles, int32_t complete, void* stream) {
+    using namespace oscar;
+    clear_error();
+    int* st = status_word();
+    if (!st) return OSCAR_ERR_CUDA;
+    const long long budget = budget_cycles < 1000 ? 1000 : (budget_cycles > 4000000000LL ? 4000000000LL : budget_cycles);
+    selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(st, budget, complete ? 1 : 0);
+    return check_cuda("selftest_wait_kernel launch");
 }

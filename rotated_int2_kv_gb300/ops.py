@@ -76,6 +76,7 @@ _SIGS = {
                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p],
                                        ctypes.c_int),
     "oscar_device_status": ([ctypes.POINTER(ctypes.c_int32), ctypes.c_int32], ctypes.c_int),
+    "oscar_selftest_bounded_wait": ([ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
     "oscar_profile_enable": ([ctypes.c_int32], ctypes.c_int),
     "oscar_profile_read": ([ctypes.c_int32, ctypes.POINTER(ctypes.c_double),
                             ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
@@ -270,6 +271,11 @@ def device_status(clear=True):
     f = ctypes.c_int32()
     _check(lib().oscar_device_status(ctypes.byref(f), int(bool(clear))))
     return f.value
+
+
+def selftest_bounded_wait(budget_cycles, complete, stream=None):
+    """Runs the bounded mbarrier wait once (see oscar_selftest_bounded_wait)."""
+    _check(lib().oscar_selftest_bounded_wait(int(budget_cycles), int(bool(complete)), _stream(stream)))
 
 
 def profile_enable(on=True):
