@@ -15,11 +15,12 @@
 //    warp per KV head each) take the even and the odd stages: two independent
 //    pipelines over a shared ring of 4 or 8 shared-memory stages, so each SM
 //    scheduler has 4 warps to interleave.  The warps of a set copy the
-//    records of their stages with one bulk (TMA engine) copy per token: all
-//    KV heads of a token are one contiguous slot-major record, so one copy
-//    moves 640 B of one page (few address translations per byte), completing
-//    on the stage's full mbarrier; each warp fetches the slot ids of its
-//    tokens from the page table one stage ahead;
+//    records of their stages with 16-byte cp.async: all KV heads of a token
+//    are one contiguous slot-major record (640 B at d 128 / 8 heads), and one
+//    warp instruction moves 16-byte chunks of four records; every thread's
+//    copies complete on the stage's full mbarrier (cp.async.mbarrier.arrive);
+//    each warp fetches the slot ids of its tokens from the page table one
+//    stage ahead;
 //  * every warp consumes its own KV head of its stages (its channel half for
 //    d = 256, where two warps share a head) and releases each stage on its
 //    empty mbarrier;
