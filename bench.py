@@ -337,7 +337,7 @@ def main():
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     time.sleep(0.3)
-    ops.profile_enable(True)
+    ops.profile_enable([ops.PROF_HISTORY])
     barrier(ws)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -349,9 +349,23 @@ def main():
     torch.cuda.synchronize()
     barrier(ws)
     ms = e0.elapsed_time(e1)
-    hist_ms, hist_n = ops.profile_read(0)
-    ops.profile_enable(False)
+    hist_ms, hist_n = ops.profile_read(ops.PROF_HISTORY)
+    ops.profile_enable(None)
     clk = clocks.stop()
+    # per-kernel breakdown from a separate pass (every launch between event pairs,
+    # which costs the step some time, so it is not the timed region)
+    nb = min(args.steps, 200)
+    kinds = ((ops.PROF_HISTORY, "history"), (ops.PROF_QUANTIZE, "quantize"), (ops.PROF_WINDOW_COPY, "window_copy"),
+             (ops.PROF_PREP, "prep"), (ops.PROF_WINDOW, "window"), (ops.PROF_COMBINE, "combine"))
+    ops.profile_enable([k for k, _ in kinds])
+    for i in range(nb):
+        decode_step(w, args.warmup + i, args.decode_kernel)
+    torch.cuda.synchronize()
+    kernel_ms = {}
+    for kind, name in kinds:
+        kms, kn = ops.profile_read(kind)
+        kernel_ms[name] = kms / nb if kn else 0.0
+    ops.profile_enable(None)
 
     rec_tok, _ = ops.cache_bytes_per_token(w["cfg"])
     tokens = 0
@@ -390,6 +404,7 @@ def main():
                          "kernel": "history kernel (INT2 split-K)", "peak_source": "measured hbm_gbs",
                          "history_ms_per_step": hist_ms / max(hist_n, 1),
                          "pct_of_8TBs": (achieved / 8000.0) if achieved else None},
+            "kernel_ms_per_step": kernel_ms,
             "gpu_launches": launches_per_step() * args.steps,
             "bits_per_kv_element": (16.0 * 320 + (2 + 32.0 / G) * (L_BASE - 320)) / L_BASE,
             "clocks": clk}
@@ -470,7 +485,7 @@ def append_measure():
     for _ in range(3):
         ops.quantize_append(cache, k, v, cu, st, pt)
     torch.cuda.synchronize()
-    ops.profile_enable(True)
+    ops.profile_enable([ops.PROF_QUANTIZE, ops.PROF_WINDOW_COPY])
     reps = 20
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -483,7 +498,7 @@ def append_measure():
     torch.cuda.synchronize()
     qms, qn = ops.profile_read(1)
     wms, wn = ops.profile_read(2)
-    ops.profile_enable(False)
+    ops.profile_enable(None)
     call_ms = e0.elapsed_time(e1) / reps
     hist = L - S_SINK - W_RECENT
     rec_tok, _ = ops.cache_bytes_per_token(cfg)

@@ -256,12 +256,12 @@ int oscar_decode_attention_noalloc(const oscar_config* cfg, const oscar_layer_ca
 
 /* ---- kernel timing (benchmarks) ----------------------------------------- */
 
-/* Enables (1) or disables (0) event timing of the dominant kernels and
- * forgets earlier records.  While enabled, every oscar_decode_attention call
- * records a CUDA event pair around its history kernel (kind 0) and every
- * oscar_quantize_append call around its quantise kernel (kind 1) and its
- * window-copy kernel (kind 2), on the call's stream.  Host-side cost: two
- * cudaEventRecord per timed kernel. */
+/* Event timing of the kernels: `enable` is a bit mask of kinds (bit k times
+ * kind k; 0 disables) and earlier records are forgotten.  Kinds: 0 the
+ * history kernel, 3 the query preparation, 4 the window and 5 the combine
+ * kernel of oscar_decode_attention; 1 the quantise and 2 the window-copy kernel of
+ * oscar_quantize_append.  A timed launch gets a CUDA event pair on the call's
+ * stream (two cudaEventRecord, which also separate it from its neighbours). */
 int oscar_profile_enable(int32_t enable);
 
 /* Waits for the recorded events of `kind` and returns their summed duration

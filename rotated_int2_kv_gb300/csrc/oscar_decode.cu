@@ -710,14 +710,22 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
         if (const int rc_ = ensure_dynamic_smem((const void*)prep_kernel<D>, psmem, "cudaFuncSetAttribute(prep_kernel)"))
             return rc_;
     }
-    prep_kernel<D><<<dim3(P.batch, (P.Hq + kPrepHeads - 1) / kPrepHeads), 256, psmem, st>>>(P);
+    {
+        const int prof_k = prof_begin(3, st);
+        prep_kernel<D><<<dim3(P.batch, (P.Hq + kPrepHeads - 1) / kPrepHeads), 256, psmem, st>>>(P);
+        prof_end(prof_k, st);
+    }
     int rc = check_cuda("prep_kernel launch");
     if (rc) return rc;
     const size_t wsmem = ((size_t)P.g * D + (size_t)P.g * kWinTile + 2 * P.g) * 4 +
                          (size_t)2 * kWinTile * (D / 2 + 1) * 4;
     if (const int rc_ = ensure_dynamic_smem((const void*)window_kernel<D>, wsmem, "cudaFuncSetAttribute(window_kernel)"))
         return rc_;
-    window_kernel<D><<<dim3(P.Hkv, P.batch, P.n_win_tiles), kCombThreads, wsmem, st>>>(P);
+    {
+        const int prof_k = prof_begin(4, st);
+        window_kernel<D><<<dim3(P.Hkv, P.batch, P.n_win_tiles), kCombThreads, wsmem, st>>>(P);
+        prof_end(prof_k, st);
+    }
     rc = check_cuda("window_kernel launch");
     if (rc) return rc;
     bool done = false;
@@ -751,7 +759,11 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
                           (size_t)P.g * ((size_t)P.n_ctas * P.par + 2)) * 4;
     if (const int rc_ = ensure_dynamic_smem((const void*)combine_kernel<D>, csmem, "cudaFuncSetAttribute(combine_kernel)"))
         return rc_;
-    combine_kernel<D><<<dim3(P.Hkv, P.batch), kMergeThreads, csmem, st>>>(P);
+    {
+        const int prof_k = prof_begin(5, st);
+        combine_kernel<D><<<dim3(P.Hkv, P.batch), kMergeThreads, csmem, st>>>(P);
+        prof_end(prof_k, st);
+    }
     return check_cuda("combine_kernel launch");
 }
 

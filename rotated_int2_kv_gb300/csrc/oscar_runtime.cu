@@ -115,13 +115,13 @@ namespace oscar {
 
 struct ProfSlot { cudaEvent_t a, b; int kind; };
 static std::mutex g_prof_mu;
-static bool g_prof_on = false;
+static uint32_t g_prof_mask = 0;   // bit k: time launches of kind k
 static std::vector<ProfSlot> g_prof_slots;
 static size_t g_prof_used = 0;
 
 int prof_begin(int kind, cudaStream_t st) {
     std::lock_guard<std::mutex> lk(g_prof_mu);
-    if (!g_prof_on) return -1;
+    if (kind < 0 || kind > 31 || !((g_prof_mask >> kind) & 1u)) return -1;
     if (g_prof_used == g_prof_slots.size()) {
         if (g_prof_slots.size() >= 65536) return -1;
         ProfSlot s;
@@ -147,7 +147,7 @@ extern "C" int oscar_profile_enable(int32_t enable) {
     using namespace oscar;
     clear_error();
     std::lock_guard<std::mutex> lk(g_prof_mu);
-    g_prof_on = enable != 0;
+    g_prof_mask = (uint32_t)enable;
     g_prof_used = 0;
     return OSCAR_OK;
 }

@@ -278,9 +278,15 @@ def selftest_bounded_wait(budget_cycles, complete, stream=None):
     _check(lib().oscar_selftest_bounded_wait(int(budget_cycles), int(bool(complete)), _stream(stream)))
 
 
-def profile_enable(on=True):
-    """Start (or stop) event timing of the dominant kernels; clears old records."""
-    _check(lib().oscar_profile_enable(int(bool(on))))
+PROF_HISTORY, PROF_QUANTIZE, PROF_WINDOW_COPY, PROF_PREP, PROF_WINDOW, PROF_COMBINE = 0, 1, 2, 3, 4, 5
+
+
+def profile_enable(kinds=(PROF_HISTORY,)):
+    """Start event timing of the given kernel kinds (None or () stops it); clears old records."""
+    mask = 0
+    for k in kinds or ():
+        mask |= 1 << int(k)
+    _check(lib().oscar_profile_enable(mask))
 
 
 def profile_read(kind):
