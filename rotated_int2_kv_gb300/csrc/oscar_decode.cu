@@ -406,7 +406,7 @@ constexpr int kMergeThreads = 512;     // combine kernel
 constexpr int kWinTile = 64;
 
 template <int D>
-__global__ void __launch_bounds__(kCombThreads) window_kernel(DecodeParams P) {
+__global__ void __launch_bounds__(kCombThreads, D >= 256 ? 2 : 6) window_kernel(DecodeParams P) {
     constexpr int kRowW = D / 2 + 1;               // words per staged bf16 row (odd: conflict-free)
     extern __shared__ __align__(16) float s_w[];
     const int hk = blockIdx.x, b = blockIdx.y, wt = blockIdx.z;
@@ -429,8 +429,15 @@ __global__ void __launch_bounds__(kCombThreads) window_kernel(DecodeParams P) {
         for (int j = tid; j < g; j += kCombThreads) P.wml[pbase + (int64_t)j * P.n_win_tiles] = make_float2(-1e30f, 0.f);
         return;
     }
-    for (int i = tid; i < g * D; i += kCombThreads)
-        sq[i] = load_elem(P.q, ((int64_t)b * P.Hq + hk * g) * D + i, P.q_dtype) * P.qscale;
+    // q of the g heads (at most 8): its loads are issued with the tile's, in one round
+    constexpr int NQ = 8 * D / kCombThreads;
+    float qv[NQ];
+    const int64_t qb = ((int64_t)b * P.Hq + hk * g) * D;
+#pragma unroll
+    for (int u = 0; u < NQ; ++u) {
+        const int i = tid + kCombThreads * u;
+        qv[u] = i < g * D ? load_elem(P.q, qb + i, P.q_dtype) : 0.f;
+    }
     {   // stage the tile: every thread issues all of its 16-byte loads before storing
         constexpr int C8 = D / 8;                       // 16-byte chunks per K (or V) row
         constexpr int NU = kWinTile * C8 / kCombThreads;
@@ -459,6 +466,11 @@ __global__ void __launch_bounds__(kCombThreads) window_kernel(DecodeParams P) {
                 vd[0] = vq[u].x; vd[1] = vq[u].y; vd[2] = vq[u].z; vd[3] = vq[u].w;
             }
         }
+    }
+#pragma unroll
+    for (int u = 0; u < NQ; ++u) {
+        const int i = tid + kCombThreads * u;
+        if (i < g * D) sq[i] = qv[u] * P.qscale;
     }
     __syncthreads();
     // logits: thread per (token, head pair j, j + hs); two heads share the K row
@@ -534,13 +546,39 @@ __global__ void __launch_bounds__(kCombThreads) window_kernel(DecodeParams P) {
 }
 
 // ---------------------------------------------------------------------------
-// combine: one block of 128 threads per (KV head, request).  Merges the BF16
+// combine: one block of 512 threads per (KV head, request).  Merges the BF16
 // window tiles and, separately, the history partials by log-sum-exp, applies
 // R_Vᵀ once to the merged rotated-domain sum, and merges the two domains:
 //   out = (e^{m_p-M}·Σ_bf16 p v + e^{m_r-M}·(Σ_hist p v̂)·R_Vᵀ) / (e^{m_p-M} l_p + e^{m_r-M} l_r).
+// The kernel is latency-bound, so it is organised around few rounds of global
+// loads: every thread issues the (m, l) pairs and o values of all partials of
+// its (head, channel) items together and merges them with a running maximum;
+// R_Vᵀ is applied with one warp per row of R_V (coalesced row loads, all rows
+// of the warp in flight) and warp reductions.
 // ---------------------------------------------------------------------------
 template <int D>
+struct CombCfg {
+    static constexpr int NV = (8 * D + kMergeThreads - 1) / kMergeThreads;   // (head, channel) items per thread, g <= 8
+    static constexpr int RPW = D / (kMergeThreads / 32);                     // R_V rows per warp
+    static constexpr int F4 = (D / 4 + 31) / 32;                             // float4 of a row per lane
+};
+
+// Running log-sum-exp merge of one (m, l) partial and its o value into (M, l, a).
+__device__ __forceinline__ void lse_merge(float m, float lv, float x, float& M, float& l, float& a) {
+    if (m > M) {
+        const float sc = M > -INFINITY ? exp2f(M - m) : 0.f;
+        l *= sc;
+        a *= sc;
+        M = m;
+    }
+    const float w = exp2f(m - M);
+    l = fmaf(w, lv, l);
+    a = fmaf(w, x, a);
+}
+
+template <int D>
 __global__ void __launch_bounds__(kMergeThreads) combine_kernel(DecodeParams P) {
+    using C = CombCfg<D>;
     extern __shared__ __align__(16) float s_c[];
     const int hk = blockIdx.x, b = blockIdx.y;
     const int g = P.g;
@@ -561,107 +599,104 @@ __global__ void __launch_bounds__(kMergeThreads) combine_kernel(DecodeParams P) 
     const int64_t sl0 = (i_lo << psh) + ((int64_t)b << psh);
     float* srot = s_c;                             // [g][D] merged rotated sum
     float* spl = srot + g * D;                     // [g][D] merged window sum
-    float* sst = spl + g * D;                      // [g][4]: m_p, l_p, m_r, l_r
-    float* sww = sst + 4 * g;                      // [g][nwt] window tile weights
-    float* swr = sww + g * nwt;                    // [g][P.n_ctas·par + 2] history partial weights
-    const int swr_stride = (P.n_ctas << psh) + 2;
-    for (int j = warp; j < g; j += kMergeThreads / 32) {
-        const int hq = hk * g + j;
-        const float2* wml = P.wml + ((int64_t)b * P.Hq + hq) * nwt;
-        float Mp = -INFINITY, Mr = -INFINITY;
-        for (int t = lane; t < nwt; t += 32)
-            if (wml[t].y > 0.f) Mp = fmaxf(Mp, wml[t].x);
-        // a partial counts when its CTA had a chunk run and its l is positive
-        for (int u = lane; u < nsl; u += 32) {
-            const float2 ml = P.ml[(sl0 + u) * P.Hq + hq];
-            const bool ok = cta_has_work(i_lo + (u >> psh), N, P.n_ctas) && ml.y > 0.f;
-            swr[j * swr_stride + u] = ok ? ml.x : -INFINITY;
-            if (ok) Mr = fmaxf(Mr, ml.x);
+    float* sst = spl + g * D;                      // [g][4]: weights of the two domains and 1 / denominator
+    uint8_t* sval = reinterpret_cast<uint8_t*>(sst + 4 * g);   // [nsl]: slot's CTA had a chunk run
+    for (int u = tid; u < nsl; u += kMergeThreads) {
+        const int64_t ci = i_lo + (u >> psh);
+        bool has;
+        if ((ci + 1) * N < 0x7FFFFFFF) {            // 32-bit division when the products fit
+            const uint32_t n = (uint32_t)P.n_ctas;
+            has = (uint32_t)(ci * N) / n < (uint32_t)((ci + 1) * N) / n;
+        } else {
+            has = cta_has_work(ci, N, P.n_ctas);
         }
-        for (int off = 16; off; off >>= 1) {
-            Mp = fmaxf(Mp, __shfl_xor_sync(0xffffffffu, Mp, off));
-            Mr = fmaxf(Mr, __shfl_xor_sync(0xffffffffu, Mr, off));
-        }
-        float lp = 0.f, lr = 0.f;
-        for (int t = lane; t < nwt; t += 32) {
-            const float2 ml = wml[t];
-            const float w = ml.y > 0.f ? exp2f(ml.x - Mp) : 0.f;
-            sww[j * nwt + t] = w;
-            lp += w * ml.y;
-        }
-        for (int u = lane; u < nsl; u += 32) {
-            const float m = swr[j * swr_stride + u];
-            const float w = m > -INFINITY ? exp2f(m - Mr) : 0.f;
-            swr[j * swr_stride + u] = w;
-            if (w > 0.f) lr += w * P.ml[(sl0 + u) * P.Hq + hq].y;
-        }
-        for (int off = 16; off; off >>= 1) {
-            lp += __shfl_xor_sync(0xffffffffu, lp, off);
-            lr += __shfl_xor_sync(0xffffffffu, lr, off);
-        }
-        if (lane == 0) {
-            sst[j * 4 + 0] = Mp;
-            sst[j * 4 + 1] = lp;
-            sst[j * 4 + 2] = Mr;
-            sst[j * 4 + 3] = lr;
-        }
+        sval[u] = has ? 1 : 0;
     }
     __syncthreads();
-    for (int i = tid; i < g * D; i += kMergeThreads) {
+    // ---- one round of loads per 8 partials: thread items (head j, channel c) ----
+#pragma unroll
+    for (int v = 0; v < C::NV; ++v) {
+        const int i = tid + kMergeThreads * v;
+        if (i >= g * D) break;
         const int j = i / D, c = i % D;
         const int hq = hk * g + j;
-        // batches of 8 predicated loads in flight (a zero weight skips its load)
-        float ap = 0.f;
+        float Mp = -INFINITY, lp = 0.f, ap = 0.f;
         const int64_t wb = ((int64_t)b * P.Hq + hq) * nwt;
         for (int t0 = 0; t0 < nwt; t0 += 8) {
-            float x[8], w[8];
+            float2 ml[8];
+            float x[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                w[u] = t0 + u < nwt ? sww[j * nwt + t0 + u] : 0.f;
-                x[u] = w[u] > 0.f ? P.wo[(wb + t0 + u) * D + c] : 0.f;
+                const bool in = t0 + u < nwt;
+                ml[u] = in ? P.wml[wb + t0 + u] : make_float2(-INFINITY, 0.f);
+                x[u] = in ? P.wo[(wb + t0 + u) * D + c] : 0.f;
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) ap = fmaf(w[u], x[u], ap);
+            for (int u = 0; u < 8; ++u)
+                if (ml[u].y > 0.f) lse_merge(ml[u].x, ml[u].y, x[u], Mp, lp, ap);
         }
-        spl[i] = ap;
-        float ar = 0.f;
+        float Mr = -INFINITY, lr = 0.f, ar = 0.f;
         for (int u0 = 0; u0 < nsl; u0 += 8) {
-            float x[8], w[8];
+            float2 ml[8];
+            float x[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                w[u] = u0 + u < nsl ? swr[j * swr_stride + u0 + u] : 0.f;
-                x[u] = w[u] > 0.f ? P.po[((sl0 + u0 + u) * P.Hq + hq) * D + c] : 0.f;
+                const bool in = u0 + u < nsl;
+                const int64_t sl = sl0 + u0 + u;
+                ml[u] = in ? P.ml[sl * P.Hq + hq] : make_float2(-INFINITY, 0.f);
+                x[u] = in ? P.po[(sl * P.Hq + hq) * D + c] : 0.f;
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) ar = fmaf(w[u], x[u], ar);
+            for (int u = 0; u < 8; ++u)
+                if (u0 + u < nsl && sval[u0 + u] && ml[u].y > 0.f) lse_merge(ml[u].x, ml[u].y, x[u], Mr, lr, ar);
         }
         srot[i] = ar;
+        spl[i] = ap;
+        if (c == 0) {                              // every item of head j merged the same (m, l) sequence
+            const float Mx = fmaxf(Mp, Mr);
+            const float wp = lp > 0.f ? exp2f(Mp - Mx) : 0.f;
+            const float wr = lr > 0.f ? exp2f(Mr - Mx) : 0.f;
+            sst[4 * j + 0] = wp;
+            sst[4 * j + 1] = wr;
+            sst[4 * j + 2] = 1.0f / (wp * lp + wr * lr);
+        }
     }
     __syncthreads();
-    // (Σ_hist p v̂)·R_Vᵀ : (x·R_Vᵀ)[c] = Σ_k x[k]·R_V[c][k]; thread per (channel c,
-    // head j): the threads of one channel share its R_V row through L1
-    for (int i = tid; i < g * D; i += kMergeThreads) {
-        const int c = i % D, j = i / D;
-        const float4* rrow = reinterpret_cast<const float4*>(P.rot_v + (int64_t)c * D);
-        const float* x = srot + j * D;
-        float a0 = 0.f, a1 = 0.f;
-        constexpr int kB = D / 4 < 8 ? D / 4 : 8;      // row loads in flight per batch
-        for (int k0 = 0; k0 < D / 4; k0 += kB) {
-            float4 rv[kB];
+    // ---- (Σ_hist p v̂)·R_Vᵀ: y[j][c] = Σ_k x[j][k]·R_V[c][k], one warp per row c ----
+    constexpr int RB = C::F4 > 1 ? 4 : 8;          // rows whose loads are in flight together
+#pragma unroll 1
+    for (int r0 = 0; r0 < C::RPW; r0 += RB) {
+        float4 rv[RB][C::F4];
 #pragma unroll
-            for (int u = 0; u < kB; ++u) rv[u] = rrow[k0 + u];
+        for (int r = 0; r < RB; ++r) {
+            const int c = warp + (kMergeThreads / 32) * (r0 + r);
+            const float4* row = reinterpret_cast<const float4*>(P.rot_v + (int64_t)c * D);
 #pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const float* xk = x + 4 * (k0 + u);
-                a0 = fmaf(xk[0], rv[u].x, fmaf(xk[1], rv[u].y, a0));
-                a1 = fmaf(xk[2], rv[u].z, fmaf(xk[3], rv[u].w, a1));
+            for (int f = 0; f < C::F4; ++f) {
+                const int k4 = lane + 32 * f;
+                rv[r][f] = (r0 + r < C::RPW && k4 < D / 4) ? row[k4] : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        const float mp = sst[j * 4 + 0], lp = sst[j * 4 + 1], mr = sst[j * 4 + 2], lr = sst[j * 4 + 3];
-        const float Mx = fmaxf(mp, mr);
-        const float wp = lp > 0.f ? exp2f(mp - Mx) : 0.f;
-        const float wr = lr > 0.f ? exp2f(mr - Mx) : 0.f;
-        outp[j * D + c] = (wp * spl[j * D + c] + wr * (a0 + a1)) / (wp * lp + wr * lr);
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            if (r0 + r >= C::RPW) break;
+            const int c = warp + (kMergeThreads / 32) * (r0 + r);
+            for (int j = 0; j < g; ++j) {
+                float y = 0.f;
+#pragma unroll
+                for (int f = 0; f < C::F4; ++f) {
+                    const int k4 = lane + 32 * f;
+                    if (k4 < D / 4) {
+                        const float4 xv = *reinterpret_cast<const float4*>(srot + j * D + 4 * k4);
+                        y = fmaf(xv.x, rv[r][f].x, fmaf(xv.y, rv[r][f].y, fmaf(xv.z, rv[r][f].z, fmaf(xv.w, rv[r][f].w, y))));
+                    }
+                }
+#pragma unroll
+                for (int off = 16; off; off >>= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
+                if (lane == j)
+                    outp[j * D + c] = fmaf(sst[4 * j + 0], spl[j * D + c], sst[4 * j + 1] * y) * sst[4 * j + 2];
+            }
+        }
     }
 }
 
@@ -755,8 +790,7 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
         if (rc) return rc;
     }
     prof_end(prof, st);
-    const size_t csmem = ((size_t)P.g * D * 2 + (size_t)P.g * 4 + (size_t)P.g * P.n_win_tiles +
-                          (size_t)P.g * ((size_t)P.n_ctas * P.par + 2)) * 4;
+    const size_t csmem = ((size_t)P.g * D * 2 + (size_t)P.g * 4) * 4 + (size_t)P.n_ctas * P.par + 16;
     if (const int rc_ = ensure_dynamic_smem((const void*)combine_kernel<D>, csmem, "cudaFuncSetAttribute(combine_kernel)"))
         return rc_;
     {
