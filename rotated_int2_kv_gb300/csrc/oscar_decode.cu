@@ -577,7 +577,7 @@ __device__ __forceinline__ void lse_merge(float m, float lv, float x, float& M, 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) combine_kernel(DecodeParams P) {
+__global__ void __launch_bounds__(kMergeThreads, D == 128 ? 2 : 1) combine_kernel(DecodeParams P) {
     using C = CombCfg<D>;
     extern __shared__ __align__(16) float s_c[];
     const int hk = blockIdx.x, b = blockIdx.y;
@@ -663,7 +663,7 @@ __global__ void __launch_bounds__(kMergeThreads) combine_kernel(DecodeParams P) 
     }
     __syncthreads();
     // ---- (Σ_hist p v̂)·R_Vᵀ: y[j][c] = Σ_k x[j][k]·R_V[c][k], one warp per row c ----
-    constexpr int RB = C::F4 > 1 ? 4 : 8;          // rows whose loads are in flight together
+    constexpr int RB = C::F4 > 1 ? 2 : 4;          // rows whose loads are in flight together
 #pragma unroll 1
     for (int r0 = 0; r0 < C::RPW; r0 += RB) {
         float4 rv[RB][C::F4];
