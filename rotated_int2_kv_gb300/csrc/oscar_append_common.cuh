@@ -55,21 +55,14 @@ __device__ __forceinline__ void build_prefix(const AppendParams& P, int* prefix,
         prefix[b] = cnt;  // temporarily the count
         local += cnt;
     }
-    scratch[tid] = local;
-    __syncthreads();
-    for (int off = 1; off < blockDim.x; off <<= 1) {  // inclusive Hillis-Steele scan
-        const int x = tid >= off ? scratch[tid - off] : 0;
-        __syncthreads();
-        scratch[tid] += x;
-        __syncthreads();
-    }
-    int run = tid ? scratch[tid - 1] : 0;
+    int total;
+    int run = block_exclusive_scan(local, scratch, &total);
     for (int b = b0; b < b1; ++b) {
         const int c = prefix[b];
         prefix[b] = run;
         run += c;
     }
-    if (tid == blockDim.x - 1) prefix[P.batch] = scratch[tid];
+    if (tid == 0) prefix[P.batch] = total;
     __syncthreads();
 }
 

@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
     extern __shared__ __align__(16) float s_rk[];
     __shared__ float sq[kPrepHeads][D];
     __shared__ float sqt[kPrepHeads][D];
-    __shared__ int scan[256];
+    __shared__ int scan[8];
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
     if (kResidentR) {
@@ -72,21 +72,14 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
             int L, rq;
             if (request_valid(P, r, &L, &rq)) local += n_chunks(L, P);
         }
-        scan[tid] = local;
-        __syncthreads();
-        for (int off = 1; off < 256; off <<= 1) {
-            const int x = tid >= off ? scan[tid - off] : 0;
-            __syncthreads();
-            scan[tid] += x;
-            __syncthreads();
-        }
-        int run = tid ? scan[tid - 1] : 0;
+        int total;
+        int run = block_exclusive_scan(local, scan, &total);
         for (int r = b0; r < b1; ++r) {
             P.cprefix[r] = run;
             int L, rq;
             if (request_valid(P, r, &L, &rq)) run += n_chunks(L, P);
         }
-        if (tid == 255) P.cprefix[P.batch] = scan[255];
+        if (tid == 0) P.cprefix[P.batch] = total;
         __syncthreads();
     }
     int L, rq;

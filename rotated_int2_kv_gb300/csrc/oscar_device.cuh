@@ -32,6 +32,33 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Block-wide exclusive scan of one int per thread (warp shuffles, then the
+// warp totals); *total receives the sum.  scratch: one int per warp.  All
+// threads of the block participate.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nw ? scratch[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += y;
+        }
+        if (lane < nw) scratch[lane] = w;
+    }
+    __syncthreads();
+    *total = scratch[nw - 1];
+    return (warp ? scratch[warp - 1] : 0) + x - v;
+}
+
 __device__ __forceinline__ void set_status(int* word, int bits) {
     if (word) atomicOr(word, bits);
 }
