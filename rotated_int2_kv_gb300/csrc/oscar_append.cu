@@ -76,6 +76,7 @@ __device__ __forceinline__ void quantize_store(const AppendParams& P, const floa
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads)
 quantize_kernel(AppendParams P) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     constexpr bool kResidentR = (D * D * 4 <= 64 * 1024);
     constexpr int kNB = D / kColBlock;           // column blocks of R
     constexpr int kYStride = D + 4;
@@ -261,6 +262,7 @@ constexpr int kSmallVec = kAppendThreads / 32;
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads)
 quantize_small_kernel(AppendParams P) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     // R is staged in shared memory when it fits in 64 KB (d <= 128): every
     // thread issues all of its loads at once, ahead of the request prefix
     constexpr bool kResidentR = (D * D * 4 <= 64 * 1024);
@@ -354,6 +356,7 @@ quantize_small_kernel(AppendParams P) {
 template <int D>
 __global__ void __launch_bounds__(128)
 window_copy_kernel(AppendParams P) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     const int b = blockIdx.x;
     const int L0 = P.start_pos[b];
     const int c0 = P.cu_new[b], c1 = P.cu_new[b + 1];
@@ -424,7 +427,7 @@ static int launch_append(const AppendParams& P, int64_t total_new, cudaStream_t 
             return rc_;
         const int64_t gs = std::min<int64_t>((max_vec + kSmallVec - 1) / kSmallVec, (int64_t)sm_count() * 4);
         const int prof = prof_begin(1, stream);
-        quantize_small_kernel<D><<<dim3((unsigned)gs, 2), kAppendThreads, ssmem, stream>>>(P);
+        launch_dependent(quantize_small_kernel<D>, dim3((unsigned)gs, 2), dim3(kAppendThreads), ssmem, stream, P);
         prof_end(prof, stream);
         int rc = check_cuda("quantize_small_kernel launch");
         if (rc) return rc;
@@ -435,7 +438,7 @@ static int launch_append(const AppendParams& P, int64_t total_new, cudaStream_t 
             // large appends, d <= 128: rotation on the tensor cores
             rc = launch_quantize_tc<D>(P, max_vec, stream);
         } else {
-            kern<<<dim3((unsigned)grid_x, 2), kAppendThreads, smem, stream>>>(P);
+            launch_dependent(kern, dim3((unsigned)grid_x, 2), dim3(kAppendThreads), smem, stream, P);
             rc = check_cuda("quantize_kernel launch");
         }
         prof_end(prof, stream);
@@ -447,7 +450,7 @@ static int launch_append(const AppendParams& P, int64_t total_new, cudaStream_t 
         const int64_t win = std::min<int64_t>((int64_t)P.S + P.W, (total_new + P.batch - 1) / P.batch);
         const int64_t gy = std::max<int64_t>(1, win);
         const int prof = prof_begin(2, stream);
-        window_copy_kernel<D><<<dim3((unsigned)P.batch, (unsigned)gy), 128, 0, stream>>>(P);
+        launch_dependent(window_copy_kernel<D>, dim3((unsigned)P.batch, (unsigned)gy), dim3(128), 0, stream, P);
         prof_end(prof, stream);
         int rc = check_cuda("window_copy_kernel launch");
         if (rc) return rc;

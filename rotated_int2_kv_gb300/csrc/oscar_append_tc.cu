@@ -183,6 +183,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(kTcThreads, 1)
 quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    int use_tma) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     using C = TcCfg<D>;
     constexpr int ng = D / G;
     constexpr int NW = D / 16;                      // code words per vector
@@ -575,7 +576,7 @@ static int launch_tc(const AppendParams& P, int64_t max_vec, cudaStream_t stream
     const int use_tma = P.kv_dtype == OSCAR_DTYPE_BF16 && rows > 0 && rows < 0x7FFFFFFF &&
                         (reinterpret_cast<uintptr_t>(P.k) & 15) == 0 && (reinterpret_cast<uintptr_t>(P.v) & 15) == 0 &&
                         encode_rows(&tk, P.k, rows, D) && encode_rows(&tv, P.v, rows, D);
-    kern<<<dim3((unsigned)grid_x, 2), kTcThreads, smem, stream>>>(P, tk, tv, use_tma);
+    launch_dependent(kern, dim3((unsigned)grid_x, 2), dim3(kTcThreads), smem, stream, P, tk, tv, use_tma);
     return check_cuda("quantize_tc_kernel launch");
 }
 

@@ -48,6 +48,7 @@ constexpr int kPrepHeads = 8;     // query heads per prep block
 
 template <int D>
 __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     // R_K is staged in shared memory (all 16-byte copies in flight at once)
     // when it fits in 64 KB (d <= 128)
     constexpr bool kResidentR = (D * D * 4 <= 64 * 1024);
@@ -229,6 +230,7 @@ __device__ __forceinline__ int chunk_request(const int32_t* cprefix, int batch, 
 // ---------------------------------------------------------------------------
 template <int D, int GQ>
 __global__ void __launch_bounds__(512) history_simt_kernel(DecodeParams P) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     constexpr int CPL = D / 32;                 // channels per lane in P·V
     extern __shared__ __align__(16) float s_dyn[];
     float* sQ = s_dyn;                          // [Hq][D] q̃ of the current request
@@ -400,6 +402,7 @@ constexpr int kWinTile = 64;
 
 template <int D>
 __global__ void __launch_bounds__(kCombThreads, D >= 256 ? 2 : 6) window_kernel(DecodeParams P) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     constexpr int kRowW = D / 2 + 1;               // words per staged bf16 row (odd: conflict-free)
     extern __shared__ __align__(16) float s_w[];
     const int hk = blockIdx.x, b = blockIdx.y, wt = blockIdx.z;
@@ -571,6 +574,7 @@ __device__ __forceinline__ void lse_merge(float m, float lv, float x, float& M, 
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads, D == 128 ? 2 : 1) combine_kernel(DecodeParams P) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     using C = CombCfg<D>;
     extern __shared__ __align__(16) float s_c[];
     const int hk = blockIdx.x, b = blockIdx.y;
@@ -740,7 +744,7 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
     }
     {
         const int prof_k = prof_begin(3, st);
-        prep_kernel<D><<<dim3(P.batch, (P.Hq + kPrepHeads - 1) / kPrepHeads), 256, psmem, st>>>(P);
+        launch_dependent(prep_kernel<D>, dim3(P.batch, (P.Hq + kPrepHeads - 1) / kPrepHeads), dim3(256), psmem, st, P);
         prof_end(prof_k, st);
     }
     int rc = check_cuda("prep_kernel launch");
@@ -751,7 +755,7 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
         return rc_;
     {
         const int prof_k = prof_begin(4, st);
-        window_kernel<D><<<dim3(P.Hkv, P.batch, P.n_win_tiles), kCombThreads, wsmem, st>>>(P);
+        launch_dependent(window_kernel<D>, dim3(P.Hkv, P.batch, P.n_win_tiles), dim3(kCombThreads), wsmem, st, P);
         prof_end(prof_k, st);
     }
     rc = check_cuda("window_kernel launch");
@@ -774,7 +778,7 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
             const int grid = std::min(P.n_ctas, std::max(1, sm_count() * std::max(1, per_sm)));
             P.n_ctas = grid;
-            kern<<<grid, threads, smem, st>>>(P);
+            launch_dependent(kern, dim3(grid), dim3(threads), smem, st, P);
             return check_cuda("history_simt_kernel launch");
         };
         if (gq == 4) rc = pick(history_simt_kernel<D, 4>);
@@ -788,7 +792,7 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
         return rc_;
     {
         const int prof_k = prof_begin(5, st);
-        combine_kernel<D><<<dim3(P.Hkv, P.batch), kMergeThreads, csmem, st>>>(P);
+        launch_dependent(combine_kernel<D>, dim3(P.Hkv, P.batch), dim3(kMergeThreads), csmem, st, P);
         prof_end(prof_k, st);
     }
     return check_cuda("combine_kernel launch");

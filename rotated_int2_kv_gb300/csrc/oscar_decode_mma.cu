@@ -213,6 +213,7 @@ constexpr int kSmemMask = 128, kSmemAbort = 256, kSmemTab = 384;
 template <int D, int G, int NT, int WPH, int TTOK, int PAR, int HKV>
 __global__ void __launch_bounds__(256 * PAR, 1)
 history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_log2) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     using namespace mma_detail;
     using C = MmaCfg<D, G, NT, WPH, TTOK>;
     constexpr int KS = C::kKS, GW = C::kGW, MT = C::kMT, MTG = C::kMTG, MQ = C::kMQ;
@@ -802,7 +803,7 @@ static int launch_mma(DecodeParams P, cudaStream_t st) {
         return rc_;
     const int grid = std::min(P.n_ctas, sm_count());
     const int trow = row_bytes(P.Hkv * MmaCfg<D, G, NT, WPH, TTOK>::REC);
-    kern<<<grid, threads, smem, st>>>(P, x_off, stages_off, trow, ns_log2);
+    launch_dependent(kern, dim3(grid), dim3(threads), smem, st, P, x_off, stages_off, trow, ns_log2);
     return check_cuda("history_mma_kernel launch");
 }
 

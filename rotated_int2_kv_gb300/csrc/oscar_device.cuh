@@ -59,6 +59,14 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* to
     return (warp ? scratch[warp - 1] : 0) + x - v;
 }
 
+// Programmatic dependent launch: wait for the previous grid of the stream (its
+// completion and memory), then let the next grid be scheduled.  Both are no-ops
+// for a grid launched without the programmatic attribute.
+__device__ __forceinline__ void grid_dep_sync() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void set_status(int* word, int bits) {
     if (word) atomicOr(word, bits);
 }

@@ -51,6 +51,27 @@ int check_cuda(const char* what);
 // device and size); OSCAR_OK or the CUDA error, reported as `what`.
 int ensure_dynamic_smem(const void* kernel, size_t bytes, const char* what);
 
+// Launches `kern` on `st` as a programmatic dependent of the stream's previous
+// kernel: the grid may be scheduled while that kernel drains.  Every kernel of
+// the library begins with grid_dep_wait() (griddepcontrol.wait) before it
+// touches global memory, which waits for the previous grid to complete and its
+// writes to be visible, so the relaxed launch changes timing, not results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Benchmark timing of the dominant kernels (see oscar_profile_enable).
 int prof_begin(int kind, cudaStream_t st);   // returns a slot or -1 when disabled
 void prof_end(int slot, cudaStream_t st);
