@@ -50,9 +50,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-append", action="store_true")
-    ap.add_argument("--workload", choices=["qwen8b-100k", "mid", "small"], default="qwen8b-100k",
+    ap.add_argument("--workload", choices=["qwen8b-100k", "mid", "small", "b1-32k"], default="qwen8b-100k",
                     help="small: batch 4 at 65,536 tokens (168 MB of INT2 records, > L2), for ncu captures; "
-                         "mid: batch 8 at 100,000 tokens (0.51 GB)")
+                         "mid: batch 8 at 100,000 tokens (0.51 GB); b1-32k: one request at 32,768 tokens "
+                         "(launch-bound)")
     return ap.parse_args()
 
 
@@ -304,7 +305,10 @@ def workload_config():
                         "context %d (64 sink + %d INT2 + 256 recent), 32 q / 8 KV heads, d 128, "
                         "group 64, clip 0.9, shuffled page table, page_size 1" % (B, L_BASE, L_BASE - 320),
             "batch": B, "context": L_BASE, "q_heads": HQ, "kv_heads": HKV, "head_dim": D, "group_size": G,
-            "l2": "inputs larger than L2 (%.2f GB INT2 history per step)" % (B * (L_BASE - 320) * 640 / 1e9),
+            "l2": ("inputs larger than L2 (%.2f GB INT2 history per step)" % (B * (L_BASE - 320) * 640 / 1e9)
+                   if B * (L_BASE - 320) * 640 > 129e6 else
+                   "inputs smaller than L2 (%.3f GB INT2 history, not flushed): a latency figure, not a "
+                   "bandwidth one" % (B * (L_BASE - 320) * 640 / 1e9)),
             "parallelism": "replicas (independent requests per GPU)"}
 
 
@@ -320,6 +324,8 @@ def main():
         B, L_BASE = 4, 65536
     elif args.workload == "mid":
         B, L_BASE = 8, 100_000
+    elif args.workload == "b1-32k":
+        B, L_BASE = 1, 32_767
     import torch
     from rotated_int2_kv_gb300 import ops
     if not os.path.exists(ops._LIB_PATH):
