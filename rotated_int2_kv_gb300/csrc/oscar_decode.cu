@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
     const bool ok = request_valid(P, b, &L, &rq);
     if (tid == 0 && blockIdx.y == 0) {
         P.len[b] = ok ? L : 0;
+        for (int h = 0; h < P.Hkv; ++h) P.comb_count[(int64_t)b * P.Hkv + h] = 0;
         P.req[b] = ok ? rq : 0;
         if (!ok) {
             int bits = 0;
@@ -572,59 +573,60 @@ __device__ __forceinline__ void lse_merge(float m, float lv, float x, float& M, 
     a = fmaf(w, x, a);
 }
 
-template <int D>
-__global__ void __launch_bounds__(kMergeThreads, D == 128 ? 2 : 1) combine_kernel(DecodeParams P) {
-    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
+// A request with more than kCombSlice history partials (few requests over
+// many CTAs: a single request splits over every CTA) is merged in slices:
+// blocks z, z + gridDim.z, ... each merge kCombSlice partials of the request
+// in place into the slice's first slot, and the block whose arrival completes
+// the count (an atomic per request and KV head, zeroed by prep) merges the
+// slices and finishes.
+constexpr int kCombSlice = 32;
+
+// Per-block facts of one (KV head, request) of the combine.
+struct CombReq {
+    int hk, b, nwt, psh, nsl;
+    int64_t N, i_lo, sl0;
+    float* outp;
+};
+
+// Whether history partial slot u of the request belongs to a CTA with a chunk run.
+__device__ __forceinline__ uint8_t comb_slot_valid(const DecodeParams& P, const CombReq& R, int u) {
+    const int64_t ci = R.i_lo + (u >> R.psh);
+    if ((ci + 1) * R.N < 0x7FFFFFFF) {              // 32-bit division when the products fit
+        const uint32_t n = (uint32_t)P.n_ctas;
+        return (uint32_t)(ci * R.N) / n < (uint32_t)((ci + 1) * R.N) / n;
+    }
+    return cta_has_work(ci, R.N, P.n_ctas);
+}
+
+// Final merge of the window partials and of the history partials at slots
+// sl0 + stride·u, u < hn (SLICED: slice results written by other blocks, valid
+// when l > 0, read past L1; otherwise the raw partials with their validity in
+// sval), then R_Vᵀ and the output.
+template <int D, bool SLICED>
+__device__ __forceinline__ void combine_finish(const DecodeParams& P, const CombReq& R, float* s_c,
+                                               const uint8_t* sval, int hn) {
     using C = CombCfg<D>;
-    extern __shared__ __align__(16) float s_c[];
-    const int hk = blockIdx.x, b = blockIdx.y;
     const int g = P.g;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int L = P.len[b];
-    float* outp = P.out + ((int64_t)b * P.Hq + hk * g) * D;
-    if (L <= 0) {
-        for (int i = tid; i < g * D; i += kMergeThreads) outp[i] = 0.f;
-        return;
-    }
-    const int64_t N = P.cprefix[P.batch];
-    const int64_t c0 = P.cprefix[b], c1 = P.cprefix[b + 1];
-    const int64_t i_lo = c1 > c0 ? chunk_owner(c0, N, P.n_ctas) : 0;
-    const int64_t i_hi = c1 > c0 ? chunk_owner(c1 - 1, N, P.n_ctas) : -1;
-    const int nwt = P.n_win_tiles;
-    const int psh = P.par == 2 ? 1 : 0;            // partial slots per (CTA, request) = 1 << psh
-    const int nsl = (int)(i_hi - i_lo + 1) << psh;  // this request's partial slots: (i_lo << psh) + b·par + u
-    const int64_t sl0 = (i_lo << psh) + ((int64_t)b << psh);
+    const int64_t stride = SLICED ? kCombSlice : 1;
     float* srot = s_c;                             // [g][D] merged rotated sum
     float* spl = srot + g * D;                     // [g][D] merged window sum
     float* sst = spl + g * D;                      // [g][4]: weights of the two domains and 1 / denominator
-    uint8_t* sval = reinterpret_cast<uint8_t*>(sst + 4 * g);   // [nsl]: slot's CTA had a chunk run
-    for (int u = tid; u < nsl; u += kMergeThreads) {
-        const int64_t ci = i_lo + (u >> psh);
-        bool has;
-        if ((ci + 1) * N < 0x7FFFFFFF) {            // 32-bit division when the products fit
-            const uint32_t n = (uint32_t)P.n_ctas;
-            has = (uint32_t)(ci * N) / n < (uint32_t)((ci + 1) * N) / n;
-        } else {
-            has = cta_has_work(ci, N, P.n_ctas);
-        }
-        sval[u] = has ? 1 : 0;
-    }
-    __syncthreads();
     // ---- one round of loads per 8 partials: thread items (head j, channel c) ----
 #pragma unroll
     for (int v = 0; v < C::NV; ++v) {
         const int i = tid + kMergeThreads * v;
         if (i >= g * D) break;
         const int j = i / D, c = i % D;
-        const int hq = hk * g + j;
+        const int hq = R.hk * g + j;
         float Mp = -INFINITY, lp = 0.f, ap = 0.f;
-        const int64_t wb = ((int64_t)b * P.Hq + hq) * nwt;
-        for (int t0 = 0; t0 < nwt; t0 += 8) {
+        const int64_t wb = ((int64_t)R.b * P.Hq + hq) * R.nwt;
+        for (int t0 = 0; t0 < R.nwt; t0 += 8) {
             float2 ml[8];
             float x[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const bool in = t0 + u < nwt;
+                const bool in = t0 + u < R.nwt;
                 ml[u] = in ? P.wml[wb + t0 + u] : make_float2(-INFINITY, 0.f);
                 x[u] = in ? P.wo[(wb + t0 + u) * D + c] : 0.f;
             }
@@ -633,19 +635,24 @@ __global__ void __launch_bounds__(kMergeThreads, D == 128 ? 2 : 1) combine_kerne
                 if (ml[u].y > 0.f) lse_merge(ml[u].x, ml[u].y, x[u], Mp, lp, ap);
         }
         float Mr = -INFINITY, lr = 0.f, ar = 0.f;
-        for (int u0 = 0; u0 < nsl; u0 += 8) {
+        for (int u0 = 0; u0 < hn; u0 += 8) {
             float2 ml[8];
             float x[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const bool in = u0 + u < nsl;
-                const int64_t sl = sl0 + u0 + u;
-                ml[u] = in ? P.ml[sl * P.Hq + hq] : make_float2(-INFINITY, 0.f);
-                x[u] = in ? P.po[(sl * P.Hq + hq) * D + c] : 0.f;
+                const bool in = u0 + u < hn;
+                const int64_t sl = R.sl0 + stride * (u0 + u);
+                if (SLICED) {
+                    ml[u] = in ? __ldcg(P.ml + sl * P.Hq + hq) : make_float2(-INFINITY, 0.f);
+                    x[u] = in ? __ldcg(P.po + (sl * P.Hq + hq) * D + c) : 0.f;
+                } else {
+                    ml[u] = in ? P.ml[sl * P.Hq + hq] : make_float2(-INFINITY, 0.f);
+                    x[u] = in ? P.po[(sl * P.Hq + hq) * D + c] : 0.f;
+                }
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                if (u0 + u < nsl && sval[u0 + u] && ml[u].y > 0.f) lse_merge(ml[u].x, ml[u].y, x[u], Mr, lr, ar);
+                if (u0 + u < hn && (SLICED || sval[u0 + u]) && ml[u].y > 0.f) lse_merge(ml[u].x, ml[u].y, x[u], Mr, lr, ar);
         }
         srot[i] = ar;
         spl[i] = ap;
@@ -691,10 +698,105 @@ __global__ void __launch_bounds__(kMergeThreads, D == 128 ? 2 : 1) combine_kerne
 #pragma unroll
                 for (int off = 16; off; off >>= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
                 if (lane == j)
-                    outp[j * D + c] = fmaf(sst[4 * j + 0], spl[j * D + c], sst[4 * j + 1] * y) * sst[4 * j + 2];
+                    R.outp[j * D + c] = fmaf(sst[4 * j + 0], spl[j * D + c], sst[4 * j + 1] * y) * sst[4 * j + 2];
             }
         }
     }
+}
+
+// The sliced merge of a request with more than kCombSlice history partials
+// (kept out of line: the common path's registers stay as they are).
+template <int D>
+__device__ __noinline__ void combine_sliced(const DecodeParams& P, const CombReq& R, float* s_c, int nslice) {
+    using C = CombCfg<D>;
+    __shared__ int s_last;
+    const int g = P.g;
+    const int tid = threadIdx.x;
+    uint8_t* sval = reinterpret_cast<uint8_t*>(s_c + (2 * g * D + 4 * g));
+    for (int sc = blockIdx.z; sc < nslice; sc += gridDim.z) {
+        const int u_lo = sc * kCombSlice, u_n = min(kCombSlice, R.nsl - u_lo);
+        for (int u = tid; u < u_n; u += kMergeThreads) sval[u] = comb_slot_valid(P, R, u_lo + u);
+        __syncthreads();
+        float ar[C::NV], Mr[C::NV], lr[C::NV];
+#pragma unroll
+        for (int v = 0; v < C::NV; ++v) {
+            const int i = tid + kMergeThreads * v;
+            ar[v] = 0.f; Mr[v] = -INFINITY; lr[v] = 0.f;
+            if (i >= g * D) continue;
+            const int j = i / D, c = i % D;
+            const int hq = R.hk * g + j;
+            for (int u0 = 0; u0 < u_n; u0 += 8) {
+                float2 ml[8];
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const bool in = u0 + u < u_n;
+                    const int64_t sl = R.sl0 + u_lo + u0 + u;
+                    ml[u] = in ? P.ml[sl * P.Hq + hq] : make_float2(-INFINITY, 0.f);
+                    x[u] = in ? P.po[(sl * P.Hq + hq) * D + c] : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (u0 + u < u_n && sval[u0 + u] && ml[u].y > 0.f) lse_merge(ml[u].x, ml[u].y, x[u], Mr[v], lr[v], ar[v]);
+            }
+        }
+        __syncthreads();                           // every read of the slice's first slot is done
+        const int64_t slw = R.sl0 + u_lo;          // the slice's result replaces its first slot
+#pragma unroll
+        for (int v = 0; v < C::NV; ++v) {
+            const int i = tid + kMergeThreads * v;
+            if (i >= g * D) continue;
+            const int j = i / D, c = i % D;
+            const int hq = R.hk * g + j;
+            P.po[(slw * P.Hq + hq) * D + c] = ar[v];
+            if (c == 0) P.ml[slw * P.Hq + hq] = lr[v] > 0.f ? make_float2(Mr[v], lr[v]) : make_float2(-INFINITY, 0.f);
+        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) s_last = atomicAdd(P.comb_count + (int64_t)R.b * P.Hkv + R.hk, 1) == nslice - 1;
+        __syncthreads();
+        if (s_last) {                              // every slice is merged: finish the request
+            __threadfence();
+            combine_finish<D, true>(P, R, s_c, sval, nslice);
+            return;
+        }
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads, D == 128 ? 2 : 1) combine_kernel(DecodeParams P) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
+    extern __shared__ __align__(16) float s_c[];
+    const int g = P.g;
+    const int tid = threadIdx.x;
+    CombReq R;
+    R.hk = blockIdx.x;
+    R.b = blockIdx.y;
+    const int L = P.len[R.b];
+    R.outp = P.out + ((int64_t)R.b * P.Hq + R.hk * g) * D;
+    if (L <= 0) {
+        if (blockIdx.z == 0)
+            for (int i = tid; i < g * D; i += kMergeThreads) R.outp[i] = 0.f;
+        return;
+    }
+    R.N = P.cprefix[P.batch];
+    const int64_t c0 = P.cprefix[R.b], c1 = P.cprefix[R.b + 1];
+    R.i_lo = c1 > c0 ? chunk_owner(c0, R.N, P.n_ctas) : 0;
+    const int64_t i_hi = c1 > c0 ? chunk_owner(c1 - 1, R.N, P.n_ctas) : -1;
+    R.nwt = P.n_win_tiles;
+    R.psh = P.par == 2 ? 1 : 0;                    // partial slots per (CTA, request) = 1 << psh
+    R.nsl = (int)(i_hi - R.i_lo + 1) << R.psh;     // this request's partial slots: (i_lo << psh) + b·par + u
+    R.sl0 = (R.i_lo << R.psh) + ((int64_t)R.b << R.psh);
+    const int nslice = R.nsl > kCombSlice ? (R.nsl + kCombSlice - 1) / kCombSlice : 1;
+    if ((int)blockIdx.z >= nslice) return;
+    if (nslice > 1) {
+        combine_sliced<D>(P, R, s_c, nslice);
+        return;
+    }
+    uint8_t* sval = reinterpret_cast<uint8_t*>(s_c + (2 * g * D + 4 * g));   // [nsl]: slot's CTA had a chunk run
+    for (int u = tid; u < R.nsl; u += kMergeThreads) sval[u] = comb_slot_valid(P, R, u);
+    __syncthreads();
+    combine_finish<D, false>(P, R, s_c, sval, R.nsl);
 }
 
 }  // namespace oscar
@@ -788,11 +890,14 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
     }
     prof_end(prof, st);
     const size_t csmem = ((size_t)P.g * D * 2 + (size_t)P.g * 4) * 4 + (size_t)P.n_ctas * P.par + 16;
+    // blocks per (request, KV head) for slice merging: about the slices an even split
+    // over the history grid gives each request (any count is correct)
+    const int nz = std::max(1, std::min(16, (P.n_ctas * P.par / std::max(1, P.batch) + kCombSlice - 1) / kCombSlice));
     if (const int rc_ = ensure_dynamic_smem((const void*)combine_kernel<D>, csmem, "cudaFuncSetAttribute(combine_kernel)"))
         return rc_;
     {
         const int prof_k = prof_begin(5, st);
-        launch_dependent(combine_kernel<D>, dim3(P.Hkv, P.batch), dim3(kMergeThreads), csmem, st, P);
+        launch_dependent(combine_kernel<D>, dim3(P.Hkv, P.batch, nz), dim3(kMergeThreads), csmem, st, P);
         prof_end(prof_k, st);
     }
     return check_cuda("combine_kernel launch");
@@ -855,6 +960,7 @@ static int decode_impl(const oscar_config* cfg, const oscar_layer_cache* cache, 
     P.qfrag = reinterpret_cast<uint2*>(ws + plan.off_qfrag);
     P.ml = reinterpret_cast<float2*>(ws + plan.off_ml);
     P.po = reinterpret_cast<float*>(ws + plan.off_o);
+    P.comb_count = reinterpret_cast<int*>(ws + plan.off_cnt);
     P.wml = reinterpret_cast<float2*>(ws + plan.off_wml);
     P.wo = reinterpret_cast<float*>(ws + plan.off_wo);
     P.status = status_word();

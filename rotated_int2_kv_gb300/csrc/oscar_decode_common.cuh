@@ -27,7 +27,7 @@ struct DecodePlan {
     int n_frag_tiles; // n-tiles of 8 columns for the fragment-packed queries
     int n_win_tiles;  // 64-token tiles of the BF16 sink + recent windows
     // workspace offsets (bytes, 256-aligned)
-    size_t off_len, off_req, off_cprefix, off_qt, off_qsum, off_qfrag, off_ml, off_o, off_wml, off_wo, total;
+    size_t off_len, off_req, off_cprefix, off_qt, off_qsum, off_qfrag, off_ml, off_o, off_wml, off_wo, off_cnt, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -57,6 +57,7 @@ inline DecodePlan make_plan(const oscar_config* cfg, int batch, int max_seq_len,
     p.off_qfrag = off;    off = align256(off + (size_t)batch * Hkv * p.n_frag_tiles * (d / 16) * 32 * 8);
     p.off_ml = off;       off = align256(off + (size_t)p.part_slots * Hq * 8);
     p.off_o = off;        off = align256(off + (size_t)p.part_slots * Hq * d * 4);
+    p.off_cnt = off;      off = align256(off + (size_t)batch * Hkv * 4);
     p.off_wml = off;      off = align256(off + (size_t)batch * Hq * p.n_win_tiles * 8);
     p.off_wo = off;       off = align256(off + (size_t)batch * Hq * p.n_win_tiles * d * 4);
     p.total = off;
@@ -95,6 +96,7 @@ struct DecodeParams {
     uint2* qfrag;      // fp16 hi/lo B fragments, [batch][Hkv][n_tiles][d/16][32]
     float2* ml;        // (m, l) per partial slot, [part_slots][Hq]
     float* po;         // unnormalised o per partial slot, [part_slots][Hq][d]
+    int* comb_count;   // combine: merged slices per (request, KV head), [batch][Hkv]; zeroed by prep
     float2* wml;       // (m, l) per BF16 window tile, [batch][Hq][n_win_tiles]
     float* wo;         // unnormalised o per BF16 window tile, [batch][Hq][n_win_tiles][d]
     int* status;

@@ -101,6 +101,18 @@ def test_many_chunks_and_ctas():
     run_decode_case(128, 32, 8, 64, 64, 256, [20000, 7000, 15001], max_seq_len=20000)
 
 
+@pytest.mark.parametrize("impl", ["auto", "simt"])
+def test_single_request_over_every_cta(impl):
+    # one request: its history splits over the whole grid, so the combine merges
+    # its partials in slices (several blocks, last-arrival finish)
+    run_decode_case(128, 32, 8, 64, 64, 256, [12000], impl=impl)
+
+
+def test_one_long_request_among_short_ones():
+    # more slices than the combine's blocks per request: blocks loop over slices
+    run_decode_case(128, 16, 4, 64, 64, 256, [24000, 400, 350, 900])
+
+
 def test_max_seq_len_larger_than_lengths():
     run_decode_case(128, 32, 8, 64, 64, 256, [900, 2000], max_seq_len=8192)
 
