@@ -7,7 +7,7 @@ stored in INT2 after the OSCAR rotation and clipping.  [Escha log] part 2,
 settings table: one scale per group of 64 channels ("--kv-cache-quant-group-size
 64"); fix 1: INT2 codes take 0.25 byte per element.
 
-Readings where the pages are silent (listed again in the design doc):
+Readings where the pages are silent:
 * every K/V vector is first rounded to bf16 (round to nearest even), the
   storage type of the unquantised windows; the quantiser reads that bf16
   vector, so a token's codes do not depend on whether it reached the history

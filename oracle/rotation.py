@@ -14,7 +14,7 @@ importance level across the quantisation groups.
 Hadamard matrix divided by sqrt(head_dim), built by repeated doubling
 [[h, h], [h, -h]], identical in every layer.
 
-Readings where the pages are silent (listed again in the design doc):
+Readings where the pages are silent:
 * row-vector convention: a head vector x is rotated as x · R, so that
   (q R)(k R)ᵀ = q kᵀ for orthogonal R;
 * the Hadamard factor has the full size d (the page builds it at head_dim);
