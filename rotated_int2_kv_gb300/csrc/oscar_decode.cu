@@ -543,6 +543,204 @@ __global__ void __launch_bounds__(kCombThreads, D >= 256 ? 2 : 6) window_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// window on the tensor cores (d <= 128, g <= 8): the same per-tile partials as
+// window_kernel, one block of 4 warps per (KV head, request, 64-token tile).
+// The block issues every load of its tile at once (16-byte cp.async of the K
+// and V rows, rows past the tile's end read as zero; q with them), then:
+//  * warp w computes the logits of tokens 16w .. 16w+15 with
+//    mma.sync.m16n8k16 bf16 → fp32: q is the A operand (rows 0..7 the bf16
+//    parts of the g heads, rows 8..15 their lo parts q - bf16(q), zero for
+//    bf16 q), K enters through ldmatrix; products are exact and
+//    S = row h + row h + 8, times log2(e)/√d;
+//  * the tile's max and sum per head are combined across the warps in shared
+//    memory; p = 2^(S - m) goes to shared memory as A fragments (rows 0..7
+//    bf16(p), rows 8..15 the lo parts p - bf16(p));
+//  * warp w computes P·V for channels [d/4·w, d/4·(w+1)) over all 64 tokens,
+//    V entering through ldmatrix.trans; o = row h + row h + 8.
+// ---------------------------------------------------------------------------
+namespace wmma_detail {
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&d)[4], uint32_t saddr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]) : "r"(saddr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&d)[4], uint32_t saddr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]) : "r"(saddr));
+}
+// 16-byte cp.async that copies src_bytes (16 or 0) and fills the rest with zeros
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+// bf16 pair (lower element in the low half) and the pair of lo parts x - bf16(x)
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const uint16_t h0 = f32_to_bf16_bits(x0), h1 = f32_to_bf16_bits(x1);
+    hi = (uint32_t)h0 | ((uint32_t)h1 << 16);
+    lo = (uint32_t)f32_to_bf16_bits(x0 - bf16_bits_to_f32(h0)) |
+         ((uint32_t)f32_to_bf16_bits(x1 - bf16_bits_to_f32(h1)) << 16);
+}
+
+}  // namespace wmma_detail
+
+template <int D>
+struct WinMmaCfg {
+    static constexpr int KS = D / 16;          // k-steps of the logits
+    static constexpr int RW = D / 2 + 4;       // words per staged row (≡ 4 mod 32: ldmatrix rows in distinct banks)
+    static constexpr int CPR = D / 8;          // 16-byte chunks per row
+    static constexpr int NTW = D / 32;         // n-tiles of 8 channels per warp in P·V
+    // shared words: K and V tiles, q fragments [KS][32][4], P fragments [4][32][4], max / sum [4][8] each
+    static constexpr int SMEM_WORDS = 2 * kWinTile * RW + KS * 128 + 4 * 128 + 2 * 32;
+};
+
+template <int D>
+__global__ void __launch_bounds__(128) window_mma_kernel(DecodeParams P) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
+    using namespace wmma_detail;
+    using C = WinMmaCfg<D>;
+    constexpr int KS = C::KS, RW = C::RW, CPR = C::CPR, NTW = C::NTW;
+    extern __shared__ __align__(16) uint32_t s_wm[];
+    uint32_t* sk = s_wm;                               // [64][RW] K rows
+    uint32_t* sv = sk + kWinTile * RW;                 // [64][RW] V rows
+    uint32_t* sqa = sv + kWinTile * RW;                // [KS][32 lanes][4] q fragments
+    uint32_t* spa = sqa + KS * 128;                    // [4 sub-tiles][32 lanes][4] P fragments
+    float* smx = reinterpret_cast<float*>(spa + 4 * 128);   // [4 warps][8 heads] sub-tile max
+    float* ssm = smx + 32;                                   // [4 warps][8 heads] sub-tile sum
+    const int hk = blockIdx.x, b = blockIdx.y, wt = blockIdx.z;
+    const int g = P.g, S = P.S, W = P.W;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = lane >> 2, j = lane & 3;
+    const int L = P.len[b];
+    const int rq = P.req[b];
+    const int sink_end = min(S, L);
+    const int rec_lo = d_hist_hi(L, S, W);
+    const int nplain = L > 0 ? sink_end + max(0, L - rec_lo) : 0;
+    const int t0 = wt * kWinTile;
+    const int nt = min(kWinTile, nplain - t0);
+    const int nwt = P.n_win_tiles;
+    const int64_t pbase = ((int64_t)b * P.Hq + hk * g) * nwt + wt;   // + head · nwt
+    if (nt <= 0) {                                     // empty tile: neutral partial
+        if (tid < g) P.wml[pbase + (int64_t)tid * nwt] = make_float2(-1e30f, 0.f);
+        return;
+    }
+    // ---- every load of the tile in one round: K / V rows (cp.async) and q ----
+#pragma unroll
+    for (int u = 0; u < 2 * kWinTile * CPR / 128; ++u) {
+        const int i = tid + 128 * u;
+        const int mat = i / (kWinTile * CPR), t = (i / CPR) % kWinTile, c = i % CPR;
+        const bool ok = t < nt;
+        const int tt = t0 + (ok ? t : 0);
+        const uint16_t* row = (tt < sink_end)
+            ? P.sink + (((int64_t)rq * S + tt) * P.Hkv + hk) * 2 * D
+            : P.recent + (((int64_t)rq * W + (rec_lo + tt - sink_end) % W) * P.Hkv + hk) * 2 * D;
+        cp_async16_zfill((mat ? sv : sk) + t * RW + 4 * c, row + mat * D + 8 * c, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+    {   // q A fragments: entry (kk, lane l, reg e): row (l>>2) + 8·(e&1) (bf16 part / lo part),
+        // channels 16kk + 8·(e>>1) + 2·(l&3), +1
+        const int64_t qb = ((int64_t)b * P.Hq + hk * g) * D;
+        for (int x = tid; x < KS * 64; x += 128) {      // pairs (e = 2h, 2h+1) share their loads
+            const int kk = x / 64, l = (x / 2) % 32, h = x % 2;
+            const int hr = l >> 2, ch = 16 * kk + 8 * h + 2 * (l & 3);
+            float q0 = 0.f, q1 = 0.f;
+            if (hr < g) {
+                q0 = load_elem(P.q, qb + (int64_t)hr * D + ch, P.q_dtype);
+                q1 = load_elem(P.q, qb + (int64_t)hr * D + ch + 1, P.q_dtype);
+            }
+            uint32_t hi, lo;
+            split_bf16x2(q0, q1, hi, lo);
+            sqa[(kk * 32 + l) * 4 + 2 * h] = hi;
+            sqa[(kk * 32 + l) * 4 + 2 * h + 1] = lo;
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    // ---- logits of sub-tile `warp`: n-tiles tokens 0..7 and 8..15 of it ----
+    const int ts = 16 * warp;                          // first token of the sub-tile
+    float sv4[4];
+    {
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+        const int mi = lane >> 3;                      // matrix: tokens +8·(mi >> 1), channels +8·(mi & 1)
+        const uint32_t rowa = smem_addr(sk + (ts + (mi >> 1) * 8 + (lane & 7)) * RW) + (mi & 1) * 16;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            const uint4 a = *reinterpret_cast<const uint4*>(sqa + (kk * 32 + lane) * 4);
+            uint32_t bk[4];
+            ldsm_x4(bk, rowa + kk * 32);
+            mma_bf16(c0, a.x, a.y, a.z, a.w, bk[0], bk[1]);
+            mma_bf16(c1, a.x, a.y, a.z, a.w, bk[2], bk[3]);
+        }
+        // head r: tokens 2j, 2j+1 (n-tile 0) and 8+2j, 9+2j (n-tile 1) of the sub-tile
+        sv4[0] = (c0[0] + c0[2]) * P.qscale;
+        sv4[1] = (c0[1] + c0[3]) * P.qscale;
+        sv4[2] = (c1[0] + c1[2]) * P.qscale;
+        sv4[3] = (c1[1] + c1[3]) * P.qscale;
+        const int tk = ts + 2 * j;
+        if (tk >= nt) sv4[0] = -INFINITY;
+        if (tk + 1 >= nt) sv4[1] = -INFINITY;
+        if (tk + 8 >= nt) sv4[2] = -INFINITY;
+        if (tk + 9 >= nt) sv4[3] = -INFINITY;
+    }
+    float mx = fmaxf(fmaxf(sv4[0], sv4[1]), fmaxf(sv4[2], sv4[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (j == 0) smx[warp * 8 + r] = mx;
+    __syncthreads();
+    const float m = fmaxf(fmaxf(smx[r], smx[8 + r]), fmaxf(smx[16 + r], smx[24 + r]));   // token 0 is valid: finite
+    float pv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pv[e] = exp2f(sv4[e] - m);   // masked: 2^-inf = 0
+    float sum = (pv[0] + pv[1]) + (pv[2] + pv[3]);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    if (j == 0) ssm[warp * 8 + r] = sum;
+    {
+        uint32_t pa[4];
+        split_bf16x2(pv[0], pv[1], pa[0], pa[1]);      // rows r (bf16 p) and r + 8 (lo parts), tokens 2j, 2j+1
+        split_bf16x2(pv[2], pv[3], pa[2], pa[3]);      // tokens 8+2j, 9+2j
+        *reinterpret_cast<uint4*>(spa + (warp * 32 + lane) * 4) = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+    }
+    __syncthreads();
+    // ---- P·V: channels [d/4·warp, d/4·(warp+1)), all sub-tiles with tokens ----
+    float o[NTW][4];
+#pragma unroll
+    for (int n = 0; n < NTW; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    {
+        const int mi = lane >> 3;                      // matrix: tokens +8·(mi & 1), channels +8·(mi >> 1)
+        const uint32_t rowv = smem_addr(sv + ((mi & 1) * 8 + (lane & 7)) * RW) + (mi >> 1) * 16 + warp * (D / 4) * 2;
+        const int nsub = (nt + 15) / 16;
+        for (int ks = 0; ks < nsub; ++ks) {
+            const uint4 a = *reinterpret_cast<const uint4*>(spa + (ks * 32 + lane) * 4);
+#pragma unroll
+            for (int q2 = 0; q2 < NTW / 2; ++q2) {
+                uint32_t bv[4];
+                ldsm_x4_trans(bv, rowv + ks * 16 * RW * 4 + q2 * 32);
+                mma_bf16(o[2 * q2], a.x, a.y, a.z, a.w, bv[0], bv[1]);
+                mma_bf16(o[2 * q2 + 1], a.x, a.y, a.z, a.w, bv[2], bv[3]);
+            }
+        }
+    }
+    // ---- the tile's partial: m, l per head and o = row r + row r + 8 ----
+    if (r < g) {
+        const int64_t slot = pbase + (int64_t)r * nwt;
+        if (warp == 0 && j == 0)
+            P.wml[slot] = make_float2(m, (ssm[r] + ssm[8 + r]) + (ssm[16 + r] + ssm[24 + r]));
+        float* op = P.wo + slot * D + warp * (D / 4);
+#pragma unroll
+        for (int n = 0; n < NTW; ++n)
+            *reinterpret_cast<float2*>(op + 8 * n + 2 * j) = make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // combine: one block of 512 threads per (KV head, request).  Merges the BF16
 // window tiles and, separately, the history partials by log-sum-exp, applies
 // R_Vᵀ once to the merged rotated-domain sum, and merges the two domains:
@@ -851,16 +1049,26 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
     }
     int rc = check_cuda("prep_kernel launch");
     if (rc) return rc;
-    const size_t wsmem = ((size_t)P.g * D + (size_t)P.g * kWinTile + 2 * P.g) * 4 +
-                         (size_t)2 * kWinTile * (D / 2 + 1) * 4;
-    if (const int rc_ = ensure_dynamic_smem((const void*)window_kernel<D>, wsmem, "cudaFuncSetAttribute(window_kernel)"))
-        return rc_;
-    {
+    if (D <= 128 && P.g <= 8) {
+        // tensor-core window: one block of 4 warps per (KV head, request, 64-token tile)
+        constexpr int DW = D <= 128 ? D : 128;
+        const size_t wsmem = (size_t)WinMmaCfg<DW>::SMEM_WORDS * 4;
+        if (const int rc_ = ensure_dynamic_smem((const void*)window_mma_kernel<DW>, wsmem,
+                                                "cudaFuncSetAttribute(window_mma_kernel)"))
+            return rc_;
+        const int prof_k = prof_begin(4, st);
+        launch_dependent(window_mma_kernel<DW>, dim3(P.Hkv, P.batch, P.n_win_tiles), dim3(128), wsmem, st, P);
+        prof_end(prof_k, st);
+    } else {
+        const size_t wsmem = ((size_t)P.g * D + (size_t)P.g * kWinTile + 2 * P.g) * 4 +
+                             (size_t)2 * kWinTile * (D / 2 + 1) * 4;
+        if (const int rc_ = ensure_dynamic_smem((const void*)window_kernel<D>, wsmem, "cudaFuncSetAttribute(window_kernel)"))
+            return rc_;
         const int prof_k = prof_begin(4, st);
         launch_dependent(window_kernel<D>, dim3(P.Hkv, P.batch, P.n_win_tiles), dim3(kCombThreads), wsmem, st, P);
         prof_end(prof_k, st);
     }
-    rc = check_cuda("window_kernel launch");
+    rc = check_cuda("window kernel launch");
     if (rc) return rc;
     bool done = false;
     const int prof = prof_begin(0, st);
