@@ -796,6 +796,57 @@ __device__ __forceinline__ uint8_t comb_slot_valid(const DecodeParams& P, const 
     return cta_has_work(ci, R.N, P.n_ctas);
 }
 
+// Row c of R_V against the merged rotated sums of heads j0 .. j0 + g - 1: the
+// lane's partial dot products of the (up to) NH heads are summed over the warp by a butterfly
+// that halves the values a lane carries at each of the first log2(NH) steps
+// (NH - 1 shuffles), then a plain reduction over the remaining lane bits; head
+// h = bits 4, 3, ... of the lane then holds its total, and the first lane of
+// each head's group writes the output.
+template <int D, int NH>
+__device__ __forceinline__ void row_heads(const CombReq& R, const float4 (&rv)[CombCfg<D>::F4], const float* srot,
+                                          const float* spl, const float* sst, int g, int c, int lane, int j0 = 0) {
+    srot += j0 * D;
+    spl += j0 * D;
+    sst += 4 * j0;
+    float* outp = R.outp + j0 * D;
+    float v[NH];
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+        float y = 0.f;
+        if (j < g) {
+#pragma unroll
+            for (int f = 0; f < CombCfg<D>::F4; ++f) {
+                const int k4 = lane + 32 * f;
+                if (k4 < D / 4) {
+                    const float4 xv = *reinterpret_cast<const float4*>(srot + j * D + 4 * k4);
+                    y = fmaf(xv.x, rv[f].x, fmaf(xv.y, rv[f].y, fmaf(xv.z, rv[f].z, fmaf(xv.w, rv[f].w, y))));
+                }
+            }
+        }
+        v[j] = y;
+    }
+    int off = 16;
+#pragma unroll
+    for (int cnt = NH; cnt > 1; cnt >>= 1, off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int k = 0; k < cnt / 2; ++k) {
+            const float send = upper ? v[k] : v[k + cnt / 2];
+            const float keep = upper ? v[k + cnt / 2] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+#pragma unroll
+    for (int o2 = off; o2 >= 1; o2 >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o2);
+    // head of this lane: bit 4 of the lane selects the upper half, bit 3 the upper quarter, ...
+    int h = 0;
+#pragma unroll
+    for (int cnt = NH, bit = 16; cnt > 1; cnt >>= 1, bit >>= 1) h += (lane & bit) ? cnt / 2 : 0;
+    const int first = (lane & ~(2 * off - 1)) == lane;     // lowest lane of the head's group
+    if (first && h < g)
+        outp[h * D + c] = fmaf(sst[4 * h + 0], spl[h * D + c], sst[4 * h + 1] * v[0]) * sst[4 * h + 2];
+}
+
 // Final merge of the window partials and of the history partials at slots
 // sl0 + stride·u, u < hn (SLICED: slice results written by other blocks, valid
 // when l > 0, read past L1; otherwise the raw partials with their validity in
@@ -883,21 +934,8 @@ __device__ __forceinline__ void combine_finish(const DecodeParams& P, const Comb
         for (int r = 0; r < RB; ++r) {
             if (r0 + r >= C::RPW) break;
             const int c = warp + (kMergeThreads / 32) * (r0 + r);
-            for (int j = 0; j < g; ++j) {
-                float y = 0.f;
-#pragma unroll
-                for (int f = 0; f < C::F4; ++f) {
-                    const int k4 = lane + 32 * f;
-                    if (k4 < D / 4) {
-                        const float4 xv = *reinterpret_cast<const float4*>(srot + j * D + 4 * k4);
-                        y = fmaf(xv.x, rv[r][f].x, fmaf(xv.y, rv[r][f].y, fmaf(xv.z, rv[r][f].z, fmaf(xv.w, rv[r][f].w, y))));
-                    }
-                }
-#pragma unroll
-                for (int off = 16; off; off >>= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
-                if (lane == j)
-                    R.outp[j * D + c] = fmaf(sst[4 * j + 0], spl[j * D + c], sst[4 * j + 1] * y) * sst[4 * j + 2];
-            }
+            for (int j0 = 0; j0 < g; j0 += 4)   // four heads at a time
+                row_heads<D, 4>(R, rv[r], srot, spl, sst, min(4, g - j0), c, lane, j0);
         }
     }
 }
