@@ -296,6 +296,28 @@ quantize_small_kernel(AppendParams P) {
         const int b = find_request(prefix, P.batch, u);
         const int L0 = P.start_pos[b];
         const int p = hist_hi(L0, P.S, P.W) + (u - prefix[b]);
+        const int rq = P.req_idx ? P.req_idx[b] : b;
+        const int64_t t = (int64_t)P.cu_new[b] + (p - L0);
+        // ---- x (bf16-rounded): lane holds channels lane·CPL ..; loaded when its
+        // address is valid, in the same round as the page-table entry ----
+        const bool from_ring = p < L0;
+        const bool src_ok = from_ring ? (rq >= 0 && rq < P.max_reqs) : (t < P.total_new);
+        float x[CPL];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) x[j] = 0.f;
+        if (src_ok) {
+            if (from_ring) {
+                const uint16_t* rowp =
+                    P.recent + ((((int64_t)rq * P.W + p % P.W) * P.Hkv + h) * 2 + mat) * D + lane * CPL;
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) x[j] = bf16_bits_to_f32(rowp[j]);
+            } else {
+                const int64_t base = (t * P.Hkv + h) * D + lane * CPL;
+#pragma unroll
+                for (int j = 0; j < CPL; ++j)
+                    x[j] = bf16_bits_to_f32(f32_to_bf16_bits(load_elem(src_new, base + j, P.kv_dtype)));
+            }
+        }
         int slot = -1;
         int bits = 0;
         if (p >= P.pt_stride) {
@@ -305,29 +327,12 @@ quantize_small_kernel(AppendParams P) {
             if (sl < 0 || sl >= P.num_slots) bits |= OSCAR_DEV_BAD_SLOT;
             else slot = sl;
         }
-        const int rq = P.req_idx ? P.req_idx[b] : b;
-        if (p < L0 && (rq < 0 || rq >= P.max_reqs)) {
-            bits |= OSCAR_DEV_BAD_REQ;
-            slot = -1;
-        }
-        const int64_t t = (int64_t)P.cu_new[b] + (p - L0);
-        if (p >= L0 && t >= P.total_new) {
-            bits |= OSCAR_DEV_BAD_LEN;
+        if (!src_ok) {
+            bits |= from_ring ? OSCAR_DEV_BAD_REQ : OSCAR_DEV_BAD_LEN;
             slot = -1;
         }
         if (bits && lane == 0) set_status(P.status, bits);
         if (slot < 0) continue;
-        // ---- x (bf16-rounded): lane holds channels lane·CPL .. ----
-        float x[CPL];
-        if (p < L0) {
-            const uint16_t* rowp = P.recent + ((((int64_t)rq * P.W + p % P.W) * P.Hkv + h) * 2 + mat) * D + lane * CPL;
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) x[j] = bf16_bits_to_f32(rowp[j]);
-        } else {
-            const int64_t base = (t * P.Hkv + h) * D + lane * CPL;
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) x[j] = bf16_bits_to_f32(f32_to_bf16_bits(load_elem(src_new, base + j, P.kv_dtype)));
-        }
 #pragma unroll
         for (int j = 0; j < CPL; ++j) sx[warp][lane * CPL + j] = x[j];
         __syncwarp();

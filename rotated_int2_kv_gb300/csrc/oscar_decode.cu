@@ -100,8 +100,20 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
         const int h0 = blockIdx.y * kPrepHeads;
         const int nh = min(kPrepHeads, P.Hq - h0);
         __syncthreads();
-        for (int i = tid; i < nh * D; i += 256)
-            sq[i / D][i % D] = load_elem(P.q, ((int64_t)b * P.Hq + h0 + i / D) * D + i % D, P.q_dtype);
+        {   // every thread's q loads in flight together
+            constexpr int NQ = (kPrepHeads * D + 255) / 256;
+            float qv[NQ];
+#pragma unroll
+            for (int u = 0; u < NQ; ++u) {
+                const int i = tid + 256 * u;
+                qv[u] = i < nh * D ? load_elem(P.q, ((int64_t)b * P.Hq + h0 + i / D) * D + i % D, P.q_dtype) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < NQ; ++u) {
+                const int i = tid + 256 * u;
+                if (i < nh * D) sq[i / D][i % D] = qv[u];
+            }
+        }
         if (kResidentR) cp_async_wait<0>();
         __syncthreads();
         const float* RK = kResidentR ? s_rk : P.rot_k;
@@ -645,18 +657,30 @@ __global__ void __launch_bounds__(128) window_mma_kernel(DecodeParams P) {
     }
     cp_async_commit();
     {   // q A fragments: entry (kk, lane l, reg e): row (l>>2) + 8·(e&1) (bf16 part / lo part),
-        // channels 16kk + 8·(e>>1) + 2·(l&3), +1
+        // channels 16kk + 8·(e>>1) + 2·(l&3), +1.  Pairs (e = 2h, 2h+1) share their
+        // loads, and every thread's loads are issued before the first is used.
+        constexpr int NQ = KS * 64 / 128;
+        static_assert(KS % 2 == 0, "whole rounds of 128 fragment pairs");
         const int64_t qb = ((int64_t)b * P.Hq + hk * g) * D;
-        for (int x = tid; x < KS * 64; x += 128) {      // pairs (e = 2h, 2h+1) share their loads
+        float q0[NQ], q1[NQ];
+#pragma unroll
+        for (int u = 0; u < NQ; ++u) {
+            const int x = tid + 128 * u;
             const int kk = x / 64, l = (x / 2) % 32, h = x % 2;
             const int hr = l >> 2, ch = 16 * kk + 8 * h + 2 * (l & 3);
-            float q0 = 0.f, q1 = 0.f;
+            q0[u] = 0.f;
+            q1[u] = 0.f;
             if (hr < g) {
-                q0 = load_elem(P.q, qb + (int64_t)hr * D + ch, P.q_dtype);
-                q1 = load_elem(P.q, qb + (int64_t)hr * D + ch + 1, P.q_dtype);
+                q0[u] = load_elem(P.q, qb + (int64_t)hr * D + ch, P.q_dtype);
+                q1[u] = load_elem(P.q, qb + (int64_t)hr * D + ch + 1, P.q_dtype);
             }
+        }
+#pragma unroll
+        for (int u = 0; u < NQ; ++u) {
+            const int x = tid + 128 * u;
+            const int kk = x / 64, l = (x / 2) % 32, h = x % 2;
             uint32_t hi, lo;
-            split_bf16x2(q0, q1, hi, lo);
+            split_bf16x2(q0[u], q1[u], hi, lo);
             sqa[(kk * 32 + l) * 4 + 2 * h] = hi;
             sqa[(kk * 32 + l) * 4 + 2 * h + 1] = lo;
         }
