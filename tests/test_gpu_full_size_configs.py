@@ -1,0 +1,188 @@
+"""Full-size parity of the two other large workload shapes, on sampled requests
+that the oracle rebuilds from the same seeded tokens, in the launch
+configuration the library picks for each shape:
+
+* Qwen3-32B-shaped ragged batch: 64 query / 8 KV heads (GQA 8), d 128, group
+  64, batch 8, lengths uniform in [65,536, 131,072], K outlier channels drawn
+  per KV head, shuffled token-granular page table;
+* GQA-6 wide-head shard: 24 query / 4 KV heads, d 256, group 128, batch 5 at
+  112,000 tokens, filled by 8,192-token chunks (13 full chunks and one of
+  5,504) with a decode call for all 5 requests after every chunk round.
+
+Both end with a decode-step append (one token per request) and a decode at the
+final lengths.  Per sampled request: the INT2 records the GPU wrote equal the
+oracle's (bit-exact except counted rounding ties); then the oracle's records
+and windows replace that request's in the device cache, and its decode
+outputs match the oracle's decode of the same cache contents (max-abs 2e-3,
+relative L2 1e-3).  The other requests keep their GPU-built records.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from rotated_int2_kv_gb300 import synth
+from parity_util import ATOL, RTOL_L2, attn_errors, classify_records, fp32_rotation_bound
+
+pytestmark = pytest.mark.gpu
+
+SEED = 1234
+CHUNK = 8192
+CLIP = 0.9
+
+
+def _rotations(d):
+    Rk, _ = oracle.build_rotation(oracle.covariance(synth.calib_samples(SEED, 0, d)), d)
+    Rv, _ = oracle.build_rotation(oracle.covariance(synth.calib_samples(SEED, 1, d)), d)
+    return Rk.astype(np.float32), Rv.astype(np.float32)
+
+
+def _oracle_request(shape, b, L, Rk, Rv, scales):
+    """The oracle's cache of request b alone (slot = position, window row 0)."""
+    d, hq, hkv, G, S, W = shape
+    oc = oracle.OracleCache(oracle.OracleConfig(d, hq, hkv, G, S, W, CLIP), L, 1, Rk, Rv)
+    pt = np.arange(L, dtype=np.int64)[None, :]
+    for pos in range(0, L, CHUNK):
+        n = min(CHUNK, L - pos)
+        k, v = synth.kv_tokens(SEED, b, pos, n, hkv, d, scales)
+        oc.append(k.float().numpy(), v.float().numpy(), [0, n], [pos], [0], pt)
+    return oc
+
+
+def _rotated_rows(shape, b, positions, Rk, Rv, scales):
+    """Rotated rows y = bf16(x)·R of request b at the given positions (tie
+    classification), and bounds on the kernel's fp32 error in them (every one of
+    the 3d products of the three-part R split may round once into the sum):
+    ({position: (y_k, y_v)}, {position: (bound_k, bound_v)}), each (Hkv, d); one
+    draw per block."""
+    d, _, hkv, _, _, _ = shape
+    out, bnd = {}, {}
+    positions = np.asarray(positions, dtype=np.int64)
+    for blk in np.unique(positions // synth.BLOCK):
+        p0 = int(blk) * synth.BLOCK
+        k, v = synth.kv_tokens(SEED, b, p0, synth.BLOCK, hkv, d, scales)
+        sel = positions[positions // synth.BLOCK == blk]
+        xk = oracle.bf16_round(k.float().numpy()[sel - p0])
+        xv = oracle.bf16_round(v.float().numpy()[sel - p0])
+        yk = oracle.quant.rotate_rows(xk.reshape(-1, d), Rk.astype(np.float64)).reshape(len(sel), hkv, d)
+        yv = oracle.quant.rotate_rows(xv.reshape(-1, d), Rv.astype(np.float64)).reshape(len(sel), hkv, d)
+        bk = fp32_rotation_bound(xk, Rk, 3 * d)
+        bv = fp32_rotation_bound(xv, Rv, 3 * d)
+        for i, p in enumerate(sel):
+            out[int(p)] = (yk[i], yv[i])
+            bnd[int(p)] = (bk[i], bv[i])
+    return out, bnd
+
+
+def _run(shape, lens, sampled, heads, outliers, chunk_sizes=None, decode_every_round=False):
+    """Fills every request b to lens[b] - 1 tokens in rounds of chunk appends,
+    appends one token per request, decodes at lens, and checks the sampled
+    requests against the oracle."""
+    from rotated_int2_kv_gb300 import ops
+    d, hq, hkv, G, S, W = shape
+    dev = torch.device("cuda")
+    B = len(lens)
+    lens = np.asarray(lens, dtype=np.int64)
+    max_len = int(lens.max())
+    Rk, Rv = _rotations(d)
+    pool = B * max_len
+    pt = synth.page_table(SEED, B, max_len, pool)                 # shuffled, page_size 1
+    cfg = ops.Config(d, hq, hkv, G, S, W, CLIP)
+    dc = ops.LayerCache(cfg, pool, B, Rk, Rv, device=dev)
+    scales = synth.outlier_scales(SEED, hkv, d, outliers)
+    pt_d = pt.to(dev)
+    ws = ops.alloc_workspace(cfg, B, max_len)
+
+    def tokens(b, pos, n):
+        # the sampled requests draw on the host, like the oracle (the device
+        # generator gives other values); the rest draw on the device
+        if b in sampled:
+            return [t.to(dev) for t in synth.kv_tokens(SEED, b, pos, n, hkv, d, scales)]
+        return synth.kv_tokens(SEED, b, pos, n, hkv, d, scales, device=dev)
+
+    # ---- fill: request b takes min(chunk, remaining) tokens per round ----
+    fill = lens - 1
+    sizes = chunk_sizes or [CHUNK] * ((int(fill.max()) + CHUNK - 1) // CHUNK)
+    cur = np.zeros(B, dtype=np.int64)
+    for rnd, csz in enumerate(sizes):
+        n = np.minimum(csz, fill - cur).clip(min=0)
+        if not n.any():
+            break
+        kk, vv = zip(*[tokens(b, int(cur[b]), int(n[b])) for b in range(B)])
+        cu = torch.from_numpy(np.concatenate([[0], np.cumsum(n)]).astype(np.int32)).to(dev)
+        start = torch.from_numpy(cur.astype(np.int32)).to(dev)
+        ops.quantize_append(dc, torch.cat(kk), torch.cat(vv), cu, start, pt_d)
+        cur += n
+        if decode_every_round:
+            q = synth.queries(SEED, 1000 + rnd, B, hq, d).to(dev)
+            lens_now = torch.from_numpy(cur.astype(np.int32)).to(dev)
+            o = ops.decode_attention(dc, q, pt_d, lens_now, max_len, ws)
+            torch.cuda.synchronize()
+            assert ops.device_status() == 0
+            assert torch.isfinite(o).all()
+    assert (cur == fill).all()
+    # ---- decode step: one token per request, then attention at lens ----
+    kk, vv = zip(*[tokens(b, int(fill[b]), 1) for b in range(B)])
+    ops.quantize_append(dc, torch.cat(kk), torch.cat(vv), torch.arange(0, B + 1, dtype=torch.int32, device=dev),
+                        torch.from_numpy(fill.astype(np.int32)).to(dev), pt_d)
+    torch.cuda.synchronize()
+    assert ops.device_status() == 0
+
+    q = synth.queries(SEED, 0, B, hq, d)
+    lens_d = torch.from_numpy(lens.astype(np.int32)).to(dev)
+    caches = {}
+    for b0 in sampled:
+        L = int(lens[b0])
+        hist = np.arange(S, L - W)
+        oc = caches[b0] = _oracle_request(shape, b0, L, Rk, Rv, scales)
+        # ---- append parity of the GPU-built records of request b0 ----
+        got = np.zeros((L, hkv, dc.records.shape[-1]), np.uint8)
+        idx = pt[b0, hist].to(dev).long()
+        got[hist] = dc.records[idx].cpu().numpy()
+        want = oc.records()
+        diff_pos = hist[(got[hist] != want[hist]).any(axis=(1, 2))]
+        # a token differs when any of its (head, K|V, group) records holds a
+        # rounding tie; far more than a few percent would be a systematic error
+        assert len(diff_pos) <= 0.05 * len(hist), (b0, len(diff_pos))
+        ora_y, ora_yb = _rotated_rows(shape, b0, diff_pos, Rk, Rv, scales) if len(diff_pos) else ({}, {})
+        st = classify_records(got, oc, diff_pos, ora_y=ora_y, ora_yb=ora_yb) if len(diff_pos) else dict(bad=0)
+        summary = (b0, {k: v for k, v in st.items() if k != "bad_examples"}, st.get("bad_examples", [])[:5])
+        assert st["bad"] == 0, summary
+        # mismatches excused only by the fp32 bound are rare; many would be a real error
+        assert st.get("fp32_ties", 0) <= 16, summary
+        # ---- the oracle's cache contents for request b0 ----
+        dc.records[idx] = torch.from_numpy(want[hist]).to(dev)
+        sink_bits, ring_bits = oc.window_bits()
+        dc.sink[b0].copy_(torch.from_numpy(sink_bits[0].view(np.int16)).view(torch.bfloat16))
+        dc.recent[b0].copy_(torch.from_numpy(ring_bits[0].view(np.int16)).view(torch.bfloat16))
+    out = ops.decode_attention(dc, q.to(dev), pt_d, lens_d, max_len, ws)
+    torch.cuda.synchronize()
+    assert ops.device_status() == 0
+    out = out.cpu().numpy()
+    assert np.isfinite(out).all()
+    for b0 in sampled:
+        L = int(lens[b0])
+        pairs = [(0, h) for h in heads]
+        want = oracle.decode_attention(caches[b0], q[b0:b0 + 1].float().numpy(), np.arange(L)[None, :], [L], [0],
+                                       pairs=pairs)
+        for _, h in pairs:
+            err, rel = attn_errors(out[b0, h], want[0, h])
+            assert err <= ATOL and rel <= RTOL_L2, (b0, h, err, rel)
+
+
+def test_full_size_qwen32b_ragged_gqa8():
+    lens = synth.ragged_lengths(SEED, 8, 65_536, 131_072)
+    sampled = (int(np.argmax(lens)), int(np.argmin(lens)))     # the longest and the shortest request
+    # query heads of the first, two middle and the last KV head (8 query heads each)
+    _run((128, 64, 8, 64, 64, 256), lens, sampled, heads=(0, 7, 8, 35, 56, 63), outliers="per_head")
+
+
+def test_full_size_gqa6_wide_chunked_prefill_with_decode_rounds():
+    L0 = 112_000
+    sizes = [CHUNK] * 13 + [5_504]
+    assert sum(sizes) == L0
+    # fill to L0 (the decode step then appends token L0 + 1)
+    # query heads of every KV head (6 query heads each)
+    _run((256, 24, 4, 128, 64, 256), [L0 + 1] * 5, sampled=(0, 4), heads=(0, 5, 6, 13, 18, 23),
+         outliers="fixed4", chunk_sizes=sizes, decode_every_round=True)
