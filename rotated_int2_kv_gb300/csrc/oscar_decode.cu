@@ -908,11 +908,12 @@ __device__ __forceinline__ void combine_finish(const DecodeParams& P, const Comb
                 if (ml[u].y > 0.f) lse_merge(ml[u].x, ml[u].y, x[u], Mp, lp, ap);
         }
         float Mr = -INFINITY, lr = 0.f, ar = 0.f;
-        for (int u0 = 0; u0 < hn; u0 += 8) {
-            float2 ml[8];
-            float x[8];
+        constexpr int UB = 8;                      // partials per round of loads (register budget)
+        for (int u0 = 0; u0 < hn; u0 += UB) {
+            float2 ml[UB];
+            float x[UB];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < UB; ++u) {
                 const bool in = u0 + u < hn;
                 const int64_t sl = R.sl0 + stride * (u0 + u);
                 if (SLICED) {
@@ -924,7 +925,7 @@ __device__ __forceinline__ void combine_finish(const DecodeParams& P, const Comb
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
+            for (int u = 0; u < UB; ++u)
                 if (u0 + u < hn && (SLICED || sval[u0 + u]) && ml[u].y > 0.f) lse_merge(ml[u].x, ml[u].y, x[u], Mr, lr, ar);
         }
         srot[i] = ar;
@@ -966,50 +967,74 @@ __device__ __forceinline__ void combine_finish(const DecodeParams& P, const Comb
 
 // The sliced merge of a request with more than kCombSlice history partials
 // (kept out of line: the common path's registers stay as they are).
+// The sliced request's finish, out of line like the slice merge itself.
+template <int D>
+__device__ __noinline__ void combine_finish_sliced(const DecodeParams& P, const CombReq& R, float* s_c,
+                                                   const uint8_t* sval, int nslice) {
+    combine_finish<D, true>(P, R, s_c, sval, nslice);
+}
+
 template <int D>
 __device__ __noinline__ void combine_sliced(const DecodeParams& P, const CombReq& R, float* s_c, int nslice) {
     using C = CombCfg<D>;
     __shared__ int s_last;
+    __shared__ float s_w[8][kCombSlice];           // per (head, slot of the slice): weight e^{m - M_head}
+    __shared__ float s_ml[8][2];                   // per head: M and Σ weight·l over the slice
     const int g = P.g;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint8_t* sval = reinterpret_cast<uint8_t*>(s_c + (2 * g * D + 4 * g));
     for (int sc = blockIdx.z; sc < nslice; sc += gridDim.z) {
         const int u_lo = sc * kCombSlice, u_n = min(kCombSlice, R.nsl - u_lo);
-        for (int u = tid; u < u_n; u += kMergeThreads) sval[u] = comb_slot_valid(P, R, u_lo + u);
-        __syncthreads();
-        float ar[C::NV], Mr[C::NV], lr[C::NV];
+        const int64_t sl0 = R.sl0 + u_lo;
+        // first (m, l) of the slice through one warp per head (lane = slot) into
+        // weights e^{m - M} in shared memory; then every o value of the thread's
+        // item in one round of loads
+        if (warp < g) {
+            const int hq = R.hk * g + warp;
+            float m = -INFINITY, l = 0.f;
+            if (lane < u_n && comb_slot_valid(P, R, u_lo + lane)) {
+                const float2 ml = P.ml[(sl0 + lane) * P.Hq + hq];
+                if (ml.y > 0.f) { m = ml.x; l = ml.y; }
+            }
+            float M = m;
 #pragma unroll
+            for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            const float w = l > 0.f ? exp2f(m - M) : 0.f;
+            float lw = w * l;
+#pragma unroll
+            for (int o = 16; o; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+            s_w[warp][lane] = w;
+            if (lane == 0) { s_ml[warp][0] = M; s_ml[warp][1] = lw; }
+        }
+        __syncthreads();
+#pragma unroll 1
         for (int v = 0; v < C::NV; ++v) {
             const int i = tid + kMergeThreads * v;
-            ar[v] = 0.f; Mr[v] = -INFINITY; lr[v] = 0.f;
-            if (i >= g * D) continue;
-            const int j = i / D, c = i % D;
+            const int j = min(i / D, g - 1), c = i % D;
             const int hq = R.hk * g + j;
-            for (int u0 = 0; u0 < u_n; u0 += 8) {
-                float2 ml[8];
-                float x[8];
+            const float* px = P.po + (sl0 * P.Hq + hq) * D + c;
+            const int64_t step = (int64_t)P.Hq * D;  // one slot further
+            const int un = i < g * D ? u_n : 0;
+            // slots of CTAs without a chunk run were never written: weight 0, not loaded
+            float x[kCombSlice];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const bool in = u0 + u < u_n;
-                    const int64_t sl = R.sl0 + u_lo + u0 + u;
-                    ml[u] = in ? P.ml[sl * P.Hq + hq] : make_float2(-INFINITY, 0.f);
-                    x[u] = in ? P.po[(sl * P.Hq + hq) * D + c] : 0.f;
-                }
+            for (int u = 0; u < kCombSlice; ++u) x[u] = (u < un && s_w[j][u] != 0.f) ? px[u * step] : 0.f;
+            float a = 0.f;
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (u0 + u < u_n && sval[u0 + u] && ml[u].y > 0.f) lse_merge(ml[u].x, ml[u].y, x[u], Mr[v], lr[v], ar[v]);
-            }
+            for (int u = 0; u < kCombSlice; ++u) a = fmaf(s_w[j][u], x[u], a);
+            if (i < g * D) s_c[i] = a;             // the finish's scratch is free until the last slice
         }
         __syncthreads();                           // every read of the slice's first slot is done
-        const int64_t slw = R.sl0 + u_lo;          // the slice's result replaces its first slot
+        const int64_t slw = sl0;                   // the slice's result replaces its first slot
 #pragma unroll
         for (int v = 0; v < C::NV; ++v) {
             const int i = tid + kMergeThreads * v;
             if (i >= g * D) continue;
             const int j = i / D, c = i % D;
             const int hq = R.hk * g + j;
-            P.po[(slw * P.Hq + hq) * D + c] = ar[v];
-            if (c == 0) P.ml[slw * P.Hq + hq] = lr[v] > 0.f ? make_float2(Mr[v], lr[v]) : make_float2(-INFINITY, 0.f);
+            P.po[(slw * P.Hq + hq) * D + c] = s_c[i];
+            if (c == 0) P.ml[slw * P.Hq + hq] = s_ml[j][1] > 0.f ? make_float2(s_ml[j][0], s_ml[j][1])
+                                                                  : make_float2(-INFINITY, 0.f);
         }
         __threadfence();
         __syncthreads();
@@ -1017,7 +1042,7 @@ __device__ __noinline__ void combine_sliced(const DecodeParams& P, const CombReq
         __syncthreads();
         if (s_last) {                              // every slice is merged: finish the request
             __threadfence();
-            combine_finish<D, true>(P, R, s_c, sval, nslice);
+            combine_finish_sliced<D>(P, R, s_c, sval, nslice);
             return;
         }
     }
