@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
     const bool ok = request_valid(P, b, &L, &rq);
     if (tid == 0 && blockIdx.y == 0) {
         P.len[b] = ok ? L : 0;
-        for (int h = 0; h < P.Hkv; ++h) P.comb_count[(int64_t)b * P.Hkv + h] = 0;
+        for (int h = 0; h < P.Hkv * kCombGroups; ++h) P.comb_count[(int64_t)b * P.Hkv * kCombGroups + h] = 0;
         P.req[b] = ok ? rq : 0;
         if (!ok) {
             int bits = 0;
@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(kCombThreads, D >= 256 ? 2 : 6) window_kernel(
         for (int j = tid; j < g; j += kCombThreads) P.wml[pbase + (int64_t)j * P.n_win_tiles] = make_float2(-1e30f, 0.f);
         return;
     }
-    // q of the g heads (at most 8): its loads are issued with the tile's, in one round
+    // q of the first 8 heads: its loads are issued with the tile's, in one round
     constexpr int NQ = 8 * D / kCombThreads;
     float qv[NQ];
     const int64_t qb = ((int64_t)b * P.Hq + hk * g) * D;
@@ -481,6 +481,8 @@ __global__ void __launch_bounds__(kCombThreads, D >= 256 ? 2 : 6) window_kernel(
         const int i = tid + kCombThreads * u;
         if (i < g * D) sq[i] = qv[u] * P.qscale;
     }
+    // heads 8 .. g-1 of larger query groups (up to 16): one more round
+    for (int i = 8 * D + tid; i < g * D; i += kCombThreads) sq[i] = load_elem(P.q, qb + i, P.q_dtype) * P.qscale;
     __syncthreads();
     // logits: thread per (token, head pair j, j + hs); two heads share the K row
     // loads and each dot product runs as two independent chains
@@ -777,7 +779,7 @@ __global__ void __launch_bounds__(128) window_mma_kernel(DecodeParams P) {
 // ---------------------------------------------------------------------------
 template <int D>
 struct CombCfg {
-    static constexpr int NV = (8 * D + kMergeThreads - 1) / kMergeThreads;   // (head, channel) items per thread, g <= 8
+    static constexpr int NV = (kCombHeads * D + kMergeThreads - 1) / kMergeThreads;   // (head, channel) items per thread
     static constexpr int RPW = D / (kMergeThreads / 32);                     // R_V rows per warp
     static constexpr int F4 = (D / 4 + 31) / 32;                             // float4 of a row per lane
 };
@@ -806,6 +808,7 @@ constexpr int kCombSlice = 32;
 // Per-block facts of one (KV head, request) of the combine.
 struct CombReq {
     int hk, b, nwt, psh, nsl;
+    int hq0, gh, grp;                           // first query head of the block, heads in it, head group
     int64_t N, i_lo, sl0;
     float* outp;
 };
@@ -879,7 +882,7 @@ template <int D, bool SLICED>
 __device__ __forceinline__ void combine_finish(const DecodeParams& P, const CombReq& R, float* s_c,
                                                const uint8_t* sval, int hn) {
     using C = CombCfg<D>;
-    const int g = P.g;
+    const int g = R.gh;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t stride = SLICED ? kCombSlice : 1;
     float* srot = s_c;                             // [g][D] merged rotated sum
@@ -891,7 +894,7 @@ __device__ __forceinline__ void combine_finish(const DecodeParams& P, const Comb
         const int i = tid + kMergeThreads * v;
         if (i >= g * D) break;
         const int j = i / D, c = i % D;
-        const int hq = R.hk * g + j;
+        const int hq = R.hq0 + j;
         float Mp = -INFINITY, lp = 0.f, ap = 0.f;
         const int64_t wb = ((int64_t)R.b * P.Hq + hq) * R.nwt;
         for (int t0 = 0; t0 < R.nwt; t0 += 8) {
@@ -978,9 +981,9 @@ template <int D>
 __device__ __noinline__ void combine_sliced(const DecodeParams& P, const CombReq& R, float* s_c, int nslice) {
     using C = CombCfg<D>;
     __shared__ int s_last;
-    __shared__ float s_w[8][kCombSlice];           // per (head, slot of the slice): weight e^{m - M_head}
-    __shared__ float s_ml[8][2];                   // per head: M and Σ weight·l over the slice
-    const int g = P.g;
+    __shared__ float s_w[kCombHeads][kCombSlice];  // per (head, slot of the slice): weight e^{m - M_head}
+    __shared__ float s_ml[kCombHeads][2];          // per head: M and Σ weight·l over the slice
+    const int g = R.gh;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint8_t* sval = reinterpret_cast<uint8_t*>(s_c + (2 * g * D + 4 * g));
     for (int sc = blockIdx.z; sc < nslice; sc += gridDim.z) {
@@ -990,7 +993,7 @@ __device__ __noinline__ void combine_sliced(const DecodeParams& P, const CombReq
         // weights e^{m - M} in shared memory; then every o value of the thread's
         // item in one round of loads
         if (warp < g) {
-            const int hq = R.hk * g + warp;
+            const int hq = R.hq0 + warp;
             float m = -INFINITY, l = 0.f;
             if (lane < u_n && comb_slot_valid(P, R, u_lo + lane)) {
                 const float2 ml = P.ml[(sl0 + lane) * P.Hq + hq];
@@ -1011,7 +1014,7 @@ __device__ __noinline__ void combine_sliced(const DecodeParams& P, const CombReq
         for (int v = 0; v < C::NV; ++v) {
             const int i = tid + kMergeThreads * v;
             const int j = min(i / D, g - 1), c = i % D;
-            const int hq = R.hk * g + j;
+            const int hq = R.hq0 + j;
             const float* px = P.po + (sl0 * P.Hq + hq) * D + c;
             const int64_t step = (int64_t)P.Hq * D;  // one slot further
             const int un = i < g * D ? u_n : 0;
@@ -1031,14 +1034,14 @@ __device__ __noinline__ void combine_sliced(const DecodeParams& P, const CombReq
             const int i = tid + kMergeThreads * v;
             if (i >= g * D) continue;
             const int j = i / D, c = i % D;
-            const int hq = R.hk * g + j;
+            const int hq = R.hq0 + j;
             P.po[(slw * P.Hq + hq) * D + c] = s_c[i];
             if (c == 0) P.ml[slw * P.Hq + hq] = s_ml[j][1] > 0.f ? make_float2(s_ml[j][0], s_ml[j][1])
                                                                   : make_float2(-INFINITY, 0.f);
         }
         __threadfence();
         __syncthreads();
-        if (tid == 0) s_last = atomicAdd(P.comb_count + (int64_t)R.b * P.Hkv + R.hk, 1) == nslice - 1;
+        if (tid == 0) s_last = atomicAdd(P.comb_count + ((int64_t)R.b * P.Hkv + R.hk) * kCombGroups + R.grp, 1) == nslice - 1;
         __syncthreads();
         if (s_last) {                              // every slice is merged: finish the request
             __threadfence();
@@ -1055,13 +1058,18 @@ __global__ void __launch_bounds__(kMergeThreads, D == 128 ? 2 : 1) combine_kerne
     const int g = P.g;
     const int tid = threadIdx.x;
     CombReq R;
-    R.hk = blockIdx.x;
+    const int ngrp = (g + kCombHeads - 1) / kCombHeads;
+    R.hk = blockIdx.x / ngrp;
+    const int grp = blockIdx.x % ngrp;
     R.b = blockIdx.y;
+    R.gh = min(kCombHeads, g - grp * kCombHeads);
+    R.hq0 = R.hk * g + grp * kCombHeads;
+    R.grp = grp;
     const int L = P.len[R.b];
-    R.outp = P.out + ((int64_t)R.b * P.Hq + R.hk * g) * D;
+    R.outp = P.out + ((int64_t)R.b * P.Hq + R.hq0) * D;
     if (L <= 0) {
         if (blockIdx.z == 0)
-            for (int i = tid; i < g * D; i += kMergeThreads) R.outp[i] = 0.f;
+            for (int i = tid; i < R.gh * D; i += kMergeThreads) R.outp[i] = 0.f;
         return;
     }
     R.N = P.cprefix[P.batch];
@@ -1078,7 +1086,7 @@ __global__ void __launch_bounds__(kMergeThreads, D == 128 ? 2 : 1) combine_kerne
         combine_sliced<D>(P, R, s_c, nslice);
         return;
     }
-    uint8_t* sval = reinterpret_cast<uint8_t*>(s_c + (2 * g * D + 4 * g));   // [nsl]: slot's CTA had a chunk run
+    uint8_t* sval = reinterpret_cast<uint8_t*>(s_c + (2 * R.gh * D + 4 * R.gh));   // [nsl]: slot's CTA had a chunk run
     for (int u = tid; u < R.nsl; u += kMergeThreads) sval[u] = comb_slot_valid(P, R, u);
     __syncthreads();
     combine_finish<D, false>(P, R, s_c, sval, R.nsl);
@@ -1184,7 +1192,8 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
         if (rc) return rc;
     }
     prof_end(prof, st);
-    const size_t csmem = ((size_t)P.g * D * 2 + (size_t)P.g * 4) * 4 + (size_t)P.n_ctas * P.par + 16;
+    const int gh = std::min(P.g, kCombHeads);   // query heads per combine block
+    const size_t csmem = ((size_t)gh * D * 2 + (size_t)gh * 4) * 4 + (size_t)P.n_ctas * P.par + 16;
     // blocks per (request, KV head) for slice merging: about the slices an even split
     // over the history grid gives each request (any count is correct)
     const int nz = std::max(1, std::min(16, (P.n_ctas * P.par / std::max(1, P.batch) + kCombSlice - 1) / kCombSlice));
@@ -1192,7 +1201,8 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
         return rc_;
     {
         const int prof_k = prof_begin(5, st);
-        launch_dependent(combine_kernel<D>, dim3(P.Hkv, P.batch, nz), dim3(kMergeThreads), csmem, st, P);
+        launch_dependent(combine_kernel<D>, dim3(P.Hkv * ((P.g + kCombHeads - 1) / kCombHeads), P.batch, nz),
+                         dim3(kMergeThreads), csmem, st, P);
         prof_end(prof_k, st);
     }
     return check_cuda("combine_kernel launch");

@@ -20,6 +20,11 @@ namespace oscar {
 // CUDA-core grid has up to max_ctas = 4·n_sm CTAs and par = 1; the tensor-core
 // grid has at most n_sm CTAs and par <= 2.  So max(max_ctas + batch,
 // 2·(n_sm + batch)) slots suffice, whatever the lengths.
+// A combine block takes at most kCombHeads query heads of one KV head; larger
+// query groups (up to 16) take ceil(g / kCombHeads) blocks per KV head.
+constexpr int kCombHeads = 8;
+constexpr int kCombGroups = 2;   // combine blocks per KV head at g = 16
+
 struct DecodePlan {
     int chunk;        // tokens per chunk (multiple of 32)
     int max_ctas;     // upper bound of the history grid
@@ -57,7 +62,7 @@ inline DecodePlan make_plan(const oscar_config* cfg, int batch, int max_seq_len,
     p.off_qfrag = off;    off = align256(off + (size_t)batch * Hkv * p.n_frag_tiles * (d / 16) * 32 * 8);
     p.off_ml = off;       off = align256(off + (size_t)p.part_slots * Hq * 8);
     p.off_o = off;        off = align256(off + (size_t)p.part_slots * Hq * d * 4);
-    p.off_cnt = off;      off = align256(off + (size_t)batch * Hkv * 4);
+    p.off_cnt = off;      off = align256(off + (size_t)batch * Hkv * kCombGroups * 4);
     p.off_wml = off;      off = align256(off + (size_t)batch * Hq * p.n_win_tiles * 8);
     p.off_wo = off;       off = align256(off + (size_t)batch * Hq * p.n_win_tiles * d * 4);
     p.total = off;
@@ -96,7 +101,7 @@ struct DecodeParams {
     uint2* qfrag;      // fp16 hi/lo B fragments, [batch][Hkv][n_tiles][d/16][32]
     float2* ml;        // (m, l) per partial slot, [part_slots][Hq]
     float* po;         // unnormalised o per partial slot, [part_slots][Hq][d]
-    int* comb_count;   // combine: merged slices per (request, KV head), [batch][Hkv]; zeroed by prep
+    int* comb_count;   // combine: merged slices per (request, KV head, head group), [batch][Hkv][kCombGroups]; zeroed by prep
     float2* wml;       // (m, l) per BF16 window tile, [batch][Hq][n_win_tiles]
     float* wo;         // unnormalised o per BF16 window tile, [batch][Hq][n_win_tiles][d]
     int* status;

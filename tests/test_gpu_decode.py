@@ -113,6 +113,20 @@ def test_one_long_request_among_short_ones():
     run_decode_case(128, 16, 4, 64, 64, 256, [24000, 400, 350, 900])
 
 
+def test_gqa16_two_combine_blocks_per_kv_head():
+    # 16 query heads per KV head: the combine takes them in two blocks of 8
+    run_decode_case(128, 32, 2, 64, 64, 256, [3000, 700])
+
+
+def test_gqa16_single_request_sliced_merge():
+    # one long request over the whole history grid: slices merged per head group
+    run_decode_case(128, 16, 1, 64, 64, 256, [12000])
+
+
+def test_gqa16_wide_heads():
+    run_decode_case(256, 16, 1, 128, 64, 256, [2600])
+
+
 def test_max_seq_len_larger_than_lengths():
     run_decode_case(128, 32, 8, 64, 64, 256, [900, 2000], max_seq_len=8192)
 
