@@ -127,6 +127,22 @@ def test_gqa16_wide_heads():
     run_decode_case(256, 16, 1, 128, 64, 256, [2600])
 
 
+@pytest.mark.parametrize("G", [32, 64, 256])
+def test_wide_heads_group_sizes(G):
+    # d 256: group 64 takes a tensor-core history variant (two warps per head),
+    # groups 32 and 256 the CUDA-core kernel
+    run_decode_case(256, 8, 2, G, 64, 256, [1500, 700])
+
+
+def test_many_kv_heads():
+    # 32 KV heads, one query head each: more heads than the warps of a history block
+    run_decode_case(128, 32, 32, 64, 64, 256, [1100, 450])
+
+
+def test_no_sink_tokens():
+    run_decode_case(128, 8, 2, 64, 0, 256, [700, 300, 256, 1])
+
+
 def test_max_seq_len_larger_than_lengths():
     run_decode_case(128, 32, 8, 64, 64, 256, [900, 2000], max_seq_len=8192)
 
