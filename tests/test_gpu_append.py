@@ -130,6 +130,20 @@ def test_large_appends_tiled_path(d, G, dtype, unaligned):
     assert st["exact"] > 0
 
 
+def test_many_kv_heads():
+    # 32 KV heads: a large call through the tiled kernel, then decode steps
+    run_append_scenario(128, 32, 32, 64, 64, 256, torch.bfloat16, [[300, 290], [1500, 1300], [1, 1], [1, 1]])
+
+
+def test_large_windows():
+    # sink 128 and a 1,024-token recent ring: spills start only past 1,152 tokens
+    run_append_scenario(64, 4, 1, 64, 128, 1024, torch.bfloat16, [[1500], [1], [700], [1]])
+
+
+def test_no_sink_tokens():
+    run_append_scenario(128, 8, 2, 64, 0, 256, torch.bfloat16, [[600, 100], [1, 1], [300, 0], [1, 1]])
+
+
 def test_decode_step_appends_spill_every_step():
     calls = [[330, 330, 400, 64]] + [[1, 1, 1, 1]] * 12
     run_append_scenario(128, 32, 8, 64, 64, 256, torch.bfloat16, calls)
