@@ -143,6 +143,13 @@ def test_no_sink_tokens():
     run_decode_case(128, 8, 2, 64, 0, 256, [700, 300, 256, 1])
 
 
+def test_large_batch_short_ragged():
+    # 700 requests of 1..600 tokens (several per thread in the chunk-prefix scan),
+    # many with no history at all
+    lens = [int(x) for x in synth.ragged_lengths(SEED, 700, 1, 600)]
+    run_decode_case(64, 4, 1, 64, 16, 32, lens)
+
+
 def test_max_seq_len_larger_than_lengths():
     run_decode_case(128, 32, 8, 64, 64, 256, [900, 2000], max_seq_len=8192)
 
