@@ -208,12 +208,15 @@ int oscar_decode_workspace_bytes(const oscar_config* cfg, int32_t batch,
  *  page_table   int32 [batch][pt_stride]
  *  seq_lens     int32 [batch], 1 <= L <= max_seq_len
  *  req_idx      int32 [batch] window row, or NULL for b
- *  batch        host, >= 0; max_seq_len host, >= 1, <= pt_stride
+ *  batch        host, 0 <= batch <= 4096; max_seq_len host, >= 1, <= pt_stride
  *  out          fp32 [batch][Hq][d]
  *  workspace    device, >= oscar_decode_workspace_bytes(cfg, batch,
  *               max_seq_len) bytes, 256-byte aligned; the library writes it
  *               and reads it back within the call's stream order.
- * Returns OSCAR_ERR_WORKSPACE if workspace is NULL or too small. */
+ * Returns OSCAR_ERR_ARG if batch or max_seq_len is out of range or
+ * num_q_heads·head_dim exceeds 16384 (one request's rotated queries are
+ * staged in shared memory), OSCAR_ERR_WORKSPACE if workspace is NULL, too
+ * small or misaligned. */
 int oscar_decode_attention(const oscar_config* cfg, const oscar_layer_cache* cache,
                            const void* q, const int32_t* page_table, int64_t pt_stride,
                            const int32_t* seq_lens, const int32_t* req_idx,
