@@ -52,8 +52,8 @@ def _oracle_request(shape, b, L, Rk, Rv, scales):
 
 def _rotated_rows(shape, b, positions, Rk, Rv, scales):
     """Rotated rows y = bf16(x)·R of request b at the given positions (tie
-    classification), and bounds on the kernel's fp32 error in them (every one of
-    the 3d products of the three-part R split may round once into the sum):
+    classification), and bounds on the kernel's fp32 error in them (the 3d
+    products of the three-part R split are exact; each addition may round once):
     ({position: (y_k, y_v)}, {position: (bound_k, bound_v)}), each (Hkv, d); one
     draw per block."""
     d, _, hkv, _, _, _ = shape
