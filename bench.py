@@ -36,6 +36,8 @@ SEED = 1234
 
 B, HQ, HKV, D, G = 32, 32, 8, 128, 64
 L_BASE = 100_000          # tokens cached before the first decode step
+LB = np.full(B, L_BASE, dtype=np.int64)   # per-request cached tokens; uniform unless a workload sets it
+OUTLIERS = "fixed4"       # K/V outlier-channel recipe of the synthetic inputs
 CYCLE = 100               # decode steps of the sequence
 S_SINK, W_RECENT = 64, 256
 
@@ -50,10 +52,13 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-append", action="store_true")
-    ap.add_argument("--workload", choices=["qwen8b-100k", "mid", "small", "b1-32k"], default="qwen8b-100k",
+    ap.add_argument("--workload", choices=["qwen8b-100k", "mid", "small", "b1-32k", "qwen32b-ragged", "gqa6-wide"],
+                    default="qwen8b-100k",
                     help="small: batch 4 at 65,536 tokens (168 MB of INT2 records, > L2), for ncu captures; "
                          "mid: batch 8 at 100,000 tokens (0.51 GB); b1-32k: one request at 32,768 tokens "
-                         "(launch-bound)")
+                         "(launch-bound); qwen32b-ragged: 64 q / 8 KV heads, batch 8, lengths uniform in "
+                         "[65,536, 131,072], per-head K outliers, 50-step cycle; gqa6-wide: 24 q / 4 KV heads, "
+                         "d 256, group 128, batch 5 at 112,000 tokens")
     return ap.parse_args()
 
 
@@ -190,38 +195,39 @@ def build_decode_workload(rank, steps_total):
     seed = SEED + 7919 * rank
     cfg = ops.Config(D, HQ, HKV, G, S_SINK, W_RECENT, 0.9)
     Rk, Rv = rotations(D)
-    max_len = L_BASE + CYCLE
+    max_len = int(LB.max()) + CYCLE
     pool = B * max_len
     pt = synth.page_table(seed, B, max_len, pool).to(dev)
     cache = ops.LayerCache(cfg, pool, B, Rk, Rv, device=dev)
-    scales = synth.outlier_scales(seed, HKV, D, "fixed4")
-    # fill every request to L_BASE tokens with chunked appends
+    scales = synth.outlier_scales(seed, HKV, D, OUTLIERS)
+    # fill request b to LB[b] tokens with chunked appends (rounds of up to 8,192
+    # tokens per request; a request that is full takes no tokens)
     chunk = 8192
     pos = 0
-    while pos < L_BASE:
-        n = min(chunk, L_BASE - pos)
+    while pos < int(LB.max()):
+        n = np.clip(LB - pos, 0, chunk)
         kk, vv = [], []
         for b in range(B):
-            k, v = synth.kv_tokens(seed, b, pos, n, HKV, D, scales, device=dev)
+            k, v = synth.kv_tokens(seed, b, pos, int(n[b]), HKV, D, scales, device=dev)
             kk.append(k)
             vv.append(v)
         k = torch.cat(kk)
         v = torch.cat(vv)
-        cu = torch.arange(0, (B + 1) * n, n, dtype=torch.int32, device=dev)
-        start = torch.full((B,), pos, dtype=torch.int32, device=dev)
+        cu = torch.from_numpy(np.concatenate([[0], np.cumsum(n)]).astype(np.int32)).to(dev)
+        start = torch.from_numpy(np.minimum(LB, pos).astype(np.int32)).to(dev)
         ops.quantize_append(cache, k, v, cu, start, pt)
-        pos += n
+        pos += chunk
         del k, v, kk, vv
     torch.cuda.synchronize()
-    # per-step inputs of the 100-step cycle (device-resident)
+    # per-step inputs of the decode cycle (device-resident)
     newk, newv, qs = [], [], []
     for s in range(CYCLE):
-        kk, vv = zip(*[synth.kv_tokens(seed, b, L_BASE + s, 1, HKV, D, scales, device=dev) for b in range(B)])
+        kk, vv = zip(*[synth.kv_tokens(seed, b, int(LB[b]) + s, 1, HKV, D, scales, device=dev) for b in range(B)])
         newk.append(torch.cat(kk))
         newv.append(torch.cat(vv))
         qs.append(synth.queries(seed, s, B, HQ, D, device=dev))
-    starts = [torch.full((B,), L_BASE + s, dtype=torch.int32, device=dev) for s in range(CYCLE)]
-    lens = [torch.full((B,), L_BASE + s + 1, dtype=torch.int32, device=dev) for s in range(CYCLE)]
+    starts = [torch.from_numpy((LB + s).astype(np.int32)).to(dev) for s in range(CYCLE)]
+    lens = [torch.from_numpy((LB + s + 1).astype(np.int32)).to(dev) for s in range(CYCLE)]
     cu1 = torch.arange(0, B + 1, dtype=torch.int32, device=dev)
     ws = ops.alloc_workspace(cfg, B, max_len, device=dev)
     out = torch.empty((B, HQ, D), dtype=torch.float32, device=dev)
@@ -250,17 +256,18 @@ def algorithmic_history_bytes(rec_bytes_per_token, L):
 # --------------------------------------------------------------------------
 # the oracle as CPU baseline / reference arm
 # --------------------------------------------------------------------------
-def oracle_sample(seed, L=L_BASE + 1):
+def oracle_sample(seed, L=None):
     """Builds (untimed) an oracle cache of one request at L tokens; returns a closure timing one decode."""
     import torch
     import oracle
     from rotated_int2_kv_gb300 import synth
+    L = int(LB.max()) + 1 if L is None else L
     Ck = oracle.covariance(synth.calib_samples(SEED, 0, D))
     Cv = oracle.covariance(synth.calib_samples(SEED, 1, D))
     Rk = oracle.build_rotation(Ck, D)[0].astype(np.float32)
     Rv = oracle.build_rotation(Cv, D)[0].astype(np.float32)
     oc = oracle.OracleCache(oracle.OracleConfig(D, HQ, HKV, G, S_SINK, W_RECENT, 0.9), L, 1, Rk, Rv)
-    scales = synth.outlier_scales(seed, HKV, D, "fixed4")
+    scales = synth.outlier_scales(seed, HKV, D, OUTLIERS)
     k, v = synth.kv_tokens(seed, 0, 0, L, HKV, D, scales)
     pt = np.arange(L, dtype=np.int64)[None, :]
     oc.append(k.float().numpy(), v.float().numpy(), [0, L], [0], [0], pt)
@@ -300,15 +307,20 @@ def run_reference(args, rank, ws):
     print(json.dumps(line), flush=True)
 
 
-def workload_config():
-    return {"workload": "Qwen3-8B-shaped decode step (append 1 token + attention), batch %d, "
-                        "context %d (64 sink + %d INT2 + 256 recent), 32 q / 8 KV heads, d 128, "
-                        "group 64, clip 0.9, shuffled page table, page_size 1" % (B, L_BASE, L_BASE - 320),
-            "batch": B, "context": L_BASE, "q_heads": HQ, "kv_heads": HKV, "head_dim": D, "group_size": G,
-            "l2": ("inputs larger than L2 (%.2f GB INT2 history per step)" % (B * (L_BASE - 320) * 640 / 1e9)
-                   if B * (L_BASE - 320) * 640 > 129e6 else
+def workload_config(rec_tok=640):
+    hist_gb = float(np.maximum(LB - S_SINK - W_RECENT, 0).sum()) * rec_tok / 1e9
+    uniform = bool((LB == LB[0]).all())
+    ctx = ("context %d (64 sink + %d INT2 + 256 recent)" % (int(LB[0]), int(LB[0]) - 320) if uniform else
+           "contexts %d..%d (ragged)" % (int(LB.min()), int(LB.max())))
+    shape = ("Qwen3-8B-shaped" if (HQ, HKV, D) == (32, 8, 128) else
+             "Qwen3-32B-shaped" if (HQ, HKV, D) == (64, 8, 128) else "GQA-%d wide-head" % (HQ // HKV))
+    return {"workload": "%s decode step (append 1 token + attention), batch %d, %s, %d q / %d KV heads, "
+                        "d %d, group %d, clip 0.9, shuffled page table, page_size 1"
+                        % (shape, B, ctx, HQ, HKV, D, G),
+            "batch": B, "context": int(LB.max()), "q_heads": HQ, "kv_heads": HKV, "head_dim": D, "group_size": G,
+            "l2": ("inputs larger than L2 (%.2f GB INT2 history per step)" % hist_gb if hist_gb * 1e9 > 129e6 else
                    "inputs smaller than L2 (%.3f GB INT2 history, not flushed): a latency figure, not a "
-                   "bandwidth one" % (B * (L_BASE - 320) * 640 / 1e9)),
+                   "bandwidth one" % hist_gb),
             "parallelism": "replicas (independent requests per GPU)"}
 
 
@@ -319,13 +331,22 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank, ws)
         return
-    global B, L_BASE
+    global B, HQ, HKV, D, G, L_BASE, LB, OUTLIERS, CYCLE
     if args.workload == "small":
         B, L_BASE = 4, 65536
     elif args.workload == "mid":
         B, L_BASE = 8, 100_000
     elif args.workload == "b1-32k":
         B, L_BASE = 1, 32_767
+    elif args.workload == "qwen32b-ragged":
+        from rotated_int2_kv_gb300 import synth
+        B, HQ, HKV, D, G = 8, 64, 8, 128, 64
+        OUTLIERS, CYCLE = "per_head", 50
+        LB = synth.ragged_lengths(SEED, B, 65_536, 131_072).astype(np.int64) - 1
+    elif args.workload == "gqa6-wide":
+        B, HQ, HKV, D, G, L_BASE = 5, 24, 4, 256, 128, 112_000
+    if args.workload != "qwen32b-ragged":
+        LB = np.full(B, L_BASE, dtype=np.int64)
     import torch
     from rotated_int2_kv_gb300 import ops
     if not os.path.exists(ops._LIB_PATH):
@@ -377,9 +398,9 @@ def main():
     tokens = 0
     hist_bytes = 0
     for i in range(args.steps):
-        L = L_BASE + (args.warmup + i) % CYCLE + 1
-        tokens += B * L
-        hist_bytes += B * algorithmic_history_bytes(rec_tok, L)
+        Ls = LB + (args.warmup + i) % CYCLE + 1
+        tokens += int(Ls.sum())
+        hist_bytes += sum(algorithmic_history_bytes(rec_tok, int(L)) for L in Ls)
     value, ms = job_throughput(tokens, ms, ws)
     peaks = {}
     try:
@@ -404,7 +425,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": "f32" if args.decode_kernel == "simt" else "f16 mma / f32 accumulate",
-            "data": "synthetic", "config": workload_config(),
+            "data": "synthetic", "config": workload_config(rec_tok),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": (achieved / hbm_peak) if achieved else None, "traffic": traffic,
                          "kernel": "history kernel (INT2 split-K)", "peak_source": "measured hbm_gbs",
@@ -412,7 +433,7 @@ def main():
                          "pct_of_8TBs": (achieved / 8000.0) if achieved else None},
             "kernel_ms_per_step": kernel_ms,
             "gpu_launches": launches_per_step() * args.steps,
-            "bits_per_kv_element": (16.0 * 320 + (2 + 32.0 / G) * (L_BASE - 320)) / L_BASE,
+            "bits_per_kv_element": float(np.mean((16.0 * 320 + (2 + 32.0 / G) * (LB - 320)) / LB)),
             "clocks": clk}
     # ---- end to end through the C ABI with host buffers ----------------------
     if not args.no_e2e:
@@ -428,8 +449,8 @@ def main():
             t += run()
             n += 1
         line["cpu_baseline"] = {"value": n * L / t, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                                "sample": "%d x oracle fp64 decode of 1 request x 32 q heads at L=%d "
-                                          "(cache built untimed)" % (n, L)}
+                                "sample": "%d x oracle fp64 decode of 1 request x %d q heads at L=%d "
+                                          "(cache built untimed)" % (n, HQ, L)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -465,7 +486,7 @@ def e2e_measure(w, args, ws):
         ops.quantize_append(w["cache"], dk, dv, w["cu1"], w["starts"][s], w["pt"])
         ops.decode_attention(w["cache"], dq, w["pt"], w["lens"][s], w["max_len"], w["ws"], out=w["out"])
         hout.copy_(w["out"], non_blocking=True)
-        tokens += B * (L_BASE + s + 1)
+        tokens += int((LB + s + 1).sum())
     e1.record(stream)
     torch.cuda.synchronize()
     value, _ = job_throughput(tokens, e0.elapsed_time(e1), ws)
