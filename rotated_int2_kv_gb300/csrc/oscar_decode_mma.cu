@@ -210,9 +210,8 @@ struct MmaCfg {
 constexpr int kSmemMask = 128, kSmemAbort = 256, kSmemTab = 384;
 
 // HKV > 0 fixes the KV head count (and so the stage row stride) at compile time.
-// Blocks hold up to 8 (d 128) or 4 (d 256) KV heads × WPH warps × PAR sets.
 template <int D, int G, int NT, int WPH, int TTOK, int PAR, int HKV>
-__global__ void __launch_bounds__(32 * (D == 256 ? 4 : 8) * WPH * PAR, 1)
+__global__ void __launch_bounds__(256 * PAR, 1)
 history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_log2) {
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     using namespace mma_detail;
@@ -835,11 +834,7 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
         if (P.G == 64) {
             // 8 KV heads (Qwen3-8B-like layers): compile-time stage row stride
             if (nt == 1) { OSCAR_MMA_H(128, 64, 1, 1, 64, 2, 8); OSCAR_MMA(128, 64, 1, 1, 64, 2); OSCAR_MMA(128, 64, 1, 1, 64, 1); }
-            else {
-                // g 5..8: two warps per KV head on channel halves (16 warps at 8 KV
-                // heads) when the shared-memory plan fits, else one
-                OSCAR_MMA(128, 64, 2, 2, 32, 1); OSCAR_MMA(128, 64, 2, 2, 64, 1); OSCAR_MMA(128, 64, 2, 1, 32, 1);
-            }
+            else OSCAR_MMA(128, 64, 2, 1, 32, 1);
         } else if (P.G == 128) {
             if (nt == 1) { OSCAR_MMA(128, 128, 1, 1, 64, 2); OSCAR_MMA(128, 128, 1, 1, 64, 1); }
             else OSCAR_MMA(128, 128, 2, 1, 32, 1);
