@@ -352,6 +352,129 @@ quantize_small_kernel(AppendParams P) {
     }
 }
 
+// 32 consecutive rows of one column of a 256-wide fp32 matrix (row stride 1024
+// bytes), all loads issued back to back in one statement.
+__device__ __forceinline__ void ld32_col256(const float* p, float (&r)[32]) {
+    asm volatile(
+        "ld.global.nc.f32 %0, [%32+0];\n\t"
+        "ld.global.nc.f32 %1, [%32+1024];\n\t"
+        "ld.global.nc.f32 %2, [%32+2048];\n\t"
+        "ld.global.nc.f32 %3, [%32+3072];\n\t"
+        "ld.global.nc.f32 %4, [%32+4096];\n\t"
+        "ld.global.nc.f32 %5, [%32+5120];\n\t"
+        "ld.global.nc.f32 %6, [%32+6144];\n\t"
+        "ld.global.nc.f32 %7, [%32+7168];\n\t"
+        "ld.global.nc.f32 %8, [%32+8192];\n\t"
+        "ld.global.nc.f32 %9, [%32+9216];\n\t"
+        "ld.global.nc.f32 %10, [%32+10240];\n\t"
+        "ld.global.nc.f32 %11, [%32+11264];\n\t"
+        "ld.global.nc.f32 %12, [%32+12288];\n\t"
+        "ld.global.nc.f32 %13, [%32+13312];\n\t"
+        "ld.global.nc.f32 %14, [%32+14336];\n\t"
+        "ld.global.nc.f32 %15, [%32+15360];\n\t"
+        "ld.global.nc.f32 %16, [%32+16384];\n\t"
+        "ld.global.nc.f32 %17, [%32+17408];\n\t"
+        "ld.global.nc.f32 %18, [%32+18432];\n\t"
+        "ld.global.nc.f32 %19, [%32+19456];\n\t"
+        "ld.global.nc.f32 %20, [%32+20480];\n\t"
+        "ld.global.nc.f32 %21, [%32+21504];\n\t"
+        "ld.global.nc.f32 %22, [%32+22528];\n\t"
+        "ld.global.nc.f32 %23, [%32+23552];\n\t"
+        "ld.global.nc.f32 %24, [%32+24576];\n\t"
+        "ld.global.nc.f32 %25, [%32+25600];\n\t"
+        "ld.global.nc.f32 %26, [%32+26624];\n\t"
+        "ld.global.nc.f32 %27, [%32+27648];\n\t"
+        "ld.global.nc.f32 %28, [%32+28672];\n\t"
+        "ld.global.nc.f32 %29, [%32+29696];\n\t"
+        "ld.global.nc.f32 %30, [%32+30720];\n\t"
+        "ld.global.nc.f32 %31, [%32+31744];\n\t"
+        : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7]), "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]), "=f"(r[14]), "=f"(r[15]), "=f"(r[16]), "=f"(r[17]), "=f"(r[18]), "=f"(r[19]), "=f"(r[20]), "=f"(r[21]), "=f"(r[22]), "=f"(r[23]), "=f"(r[24]), "=f"(r[25]), "=f"(r[26]), "=f"(r[27]), "=f"(r[28]), "=f"(r[29]), "=f"(r[30]), "=f"(r[31])
+        : "l"(p));
+}
+
+// Decode-step appends at d = 256, where R (256 KB) does not fit the shared-memory
+// staging: one block of D threads per head vector, thread c forming output
+// channel c with the same sequential fp32 FMA order over k as the other
+// kernels (bit-identical y).  A warp reads rows of R as coalesced 128-byte
+// lines, 32 of them in flight, and the few vectors of a decode step spread
+// over as many SMs, instead of a warp streaming all of R for its vector.
+template <int D>
+__global__ void __launch_bounds__(D, 2)   // a minimum residency, so that the 32 loads stay in flight
+quantize_vec_kernel(AppendParams P) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
+    constexpr int CPL = D / 32;
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ float sx[D];
+    __shared__ float sy[D];
+    int* prefix = reinterpret_cast<int*>(smem);
+    int* scratch = prefix + P.batch + 1;
+    const int mat = blockIdx.y;
+    const float* R = mat ? P.rot_v : P.rot_k;
+    const void* src_new = mat ? P.v : P.k;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    build_prefix(P, prefix, scratch);
+    const int64_t total_vec = (int64_t)prefix[P.batch] * P.Hkv;
+    for (int64_t e = blockIdx.x; e < total_vec; e += gridDim.x) {
+        // ---- resolve the vector (every thread, block-uniform) ----
+        const int u = (int)(e / P.Hkv), h = (int)(e % P.Hkv);
+        const int b = find_request(prefix, P.batch, u);
+        const int L0 = P.start_pos[b];
+        const int p = hist_hi(L0, P.S, P.W) + (u - prefix[b]);
+        const int rq = P.req_idx ? P.req_idx[b] : b;
+        const int64_t t = (int64_t)P.cu_new[b] + (p - L0);
+        const bool from_ring = p < L0;
+        const bool src_ok = from_ring ? (rq >= 0 && rq < P.max_reqs) : (t < P.total_new);
+        // x (bf16-rounded), channel tid, loaded in the page-table entry's round
+        float x = 0.f;
+        if (src_ok) {
+            if (from_ring)
+                x = bf16_bits_to_f32(P.recent[((((int64_t)rq * P.W + p % P.W) * P.Hkv + h) * 2 + mat) * D + tid]);
+            else
+                x = bf16_bits_to_f32(f32_to_bf16_bits(load_elem(src_new, (t * P.Hkv + h) * D + tid, P.kv_dtype)));
+        }
+        int slot = -1;
+        int bits = 0;
+        if (p >= P.pt_stride) {
+            bits |= OSCAR_DEV_BAD_LEN;
+        } else {
+            const int sl = P.page_table[(int64_t)b * P.pt_stride + p];
+            if (sl < 0 || sl >= P.num_slots) bits |= OSCAR_DEV_BAD_SLOT;
+            else slot = sl;
+        }
+        if (!src_ok) {
+            bits |= from_ring ? OSCAR_DEV_BAD_REQ : OSCAR_DEV_BAD_LEN;
+            slot = -1;
+        }
+        if (bits && tid == 0) set_status(P.status, bits);
+        if (slot < 0) continue;                    // the same decision in every thread
+        sx[tid] = x;
+        __syncthreads();
+        // ---- y[c] = Σ_k x_k·R[k][c], k sequential ----
+        float y = 0.f;
+        const float* rc = R + tid;
+        for (int k0 = 0; k0 < D; k0 += 32) {      // 32 rows of R in flight, then their FMAs in order
+            float r[32];
+            if constexpr (D == 256) {
+                ld32_col256(rc + (int64_t)k0 * D, r);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 32; ++u) r[u] = __ldg(rc + (int64_t)(k0 + u) * D);
+            }
+#pragma unroll
+            for (int u = 0; u < 32; ++u) y = fmaf(sx[k0 + u], r[u], y);
+        }
+        sy[tid] = y;
+        __syncthreads();
+        if (warp == 0) {                           // lane: channels lane·CPL .. + CPL - 1
+            float yv[CPL];
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) yv[j] = sy[lane * CPL + j];
+            quantize_store<D>(P, yv, slot, h, mat, lane);
+        }
+        __syncthreads();                           // sx and sy are reused by the next vector
+    }
+}
+
 // Copies the new rows that land in a BF16 window: positions below S go to the
 // sink, positions at or after max(S, L1 - W) to the ring slot p % W; the rows in
 // between enter the history and are the quantise kernel's.  Block (b, y)
@@ -425,7 +548,18 @@ static int launch_append(const AppendParams& P, int64_t total_new, cudaStream_t 
     const int per_sm = kResidentR ? 2 : 1;
     const int64_t grid_x = std::max<int64_t>(1, std::min<int64_t>(max_tiles, (int64_t)sm_count() * per_sm / 2));
     const int64_t max_vec = max_units * P.Hkv;
-    if (max_vec > 0 && max_vec <= (int64_t)sm_count() * kTileVec) {
+    if (D * D * 4 > 64 * 1024 && max_vec > 0 && max_vec <= 2 * (int64_t)sm_count()) {
+        // few vectors with R too large for shared memory (d 256): one block per vector
+        const size_t vsmem = (size_t)(P.batch + 1 + D) * 4;
+        if (const int rc_ = ensure_dynamic_smem((const void*)quantize_vec_kernel<D>, vsmem,
+                                                "cudaFuncSetAttribute(quantize_vec_kernel)"))
+            return rc_;
+        const int prof = prof_begin(1, stream);
+        launch_dependent(quantize_vec_kernel<D>, dim3((unsigned)max_vec, 2), dim3(D), vsmem, stream, P);
+        prof_end(prof, stream);
+        int rc = check_cuda("quantize_vec_kernel launch");
+        if (rc) return rc;
+    } else if (max_vec > 0 && max_vec <= (int64_t)sm_count() * kTileVec) {
         // few vectors (decode steps): one warp per vector over many blocks
         const size_t ssmem = (size_t)(P.batch + 1 + kAppendThreads) * 4 + (D * D * 4 <= 64 * 1024 ? D * D * 4 : 0);
         if (const int rc_ = ensure_dynamic_smem((const void*)quantize_small_kernel<D>, ssmem, "cudaFuncSetAttribute(quantize_small_kernel)"))

@@ -125,12 +125,13 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
             float acc[kHPT];
 #pragma unroll
             for (int j = 0; j < kHPT; ++j) acc[j] = 0.f;
-            for (int k0 = 0; k0 < D; k0 += 16) {
-                float r[16];
+            constexpr int KB = kResidentR ? 16 : 32;   // rows of R_K in flight (from L2 when not staged)
+            for (int k0 = 0; k0 < D; k0 += KB) {
+                float r[KB];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) r[u] = RK[(int64_t)(k0 + u) * D + col];
+                for (int u = 0; u < KB; ++u) r[u] = RK[(int64_t)(k0 + u) * D + col];
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
+                for (int u = 0; u < KB; ++u)
 #pragma unroll
                     for (int j = 0; j < kHPT; ++j) acc[j] = fmaf(sq[hb + j][k0 + u], r[u], acc[j]);
             }
