@@ -249,7 +249,7 @@ def launches_per_step():
 
 
 def algorithmic_history_bytes(rec_bytes_per_token, L):
-    hist = max(0, L - W_RECENT) - S_SINK
+    hist = max(S_SINK, L - W_RECENT) - S_SINK      # history [S, max(S, L - W))
     return hist * (rec_bytes_per_token + 4)   # records + page-table entry
 
 
