@@ -244,8 +244,10 @@ def decode_step(w, i, kernel):
 
 
 def launches_per_step():
-    # quantize + window copy (append) ; prep + window + history + combine (decode)
-    return 6
+    # append: one launch when the step appends at most W tokens (the window row
+    # writes ride with the quantisation), else quantise + window copy;
+    # decode: window (with the query preparation) + history + combine
+    return (1 if B <= W_RECENT else 2) + 3
 
 
 def algorithmic_history_bytes(rec_bytes_per_token, L):
@@ -278,6 +280,33 @@ def oracle_sample(seed, L=None):
         oracle.decode_attention(oc, q, pt, [L], [0])
         return time.perf_counter() - t0
     return run, L
+
+
+def boundary_cases(w, n_hist=8192):
+    """INT2 records of request 0's first n_hist history tokens (written by the
+    chunked fill) against the oracle's: exact, rounding ties (codes within 1e-6
+    of a boundary, (s, z) at an fp16 tie) and other mismatches, counted over
+    (token, KV head, K|V, group)."""
+    import torch
+    import oracle
+    from rotated_int2_kv_gb300 import synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from parity_util import classify_records
+    L = S_SINK + n_hist + W_RECENT
+    k, v = synth.kv_tokens(w["seed"], 0, 0, L, HKV, D, w["scales"], device="cuda")
+    oc = oracle.OracleCache(oracle.OracleConfig(D, HQ, HKV, G, S_SINK, W_RECENT, 0.9), L, 1, w["Rk"], w["Rv"])
+    oc.append(k.float().cpu().numpy(), v.float().cpu().numpy(), [0, L], [0], [0],
+              np.arange(L, dtype=np.int64)[None, :], keep_y=True)
+    hist = np.arange(S_SINK, S_SINK + n_hist)
+    got = np.zeros((L, HKV, w["cache"].records.shape[-1]), np.uint8)
+    got[hist] = w["cache"].records[w["pt"][0, S_SINK:S_SINK + n_hist].long()].cpu().numpy()
+    st = classify_records(got, oc, hist)
+    return {"sample": "request 0, history tokens %d..%d (chunked-fill path), all KV heads, K and V"
+                      % (S_SINK, S_SINK + n_hist - 1),
+            "group_records": int(n_hist * HKV * 2 * (D // G)), "exact": st["exact"], "code_ties": st["code_ties"],
+            "sz_ties": st["sz_ties"], "other_mismatches": st["bad"],
+            "rule": "codes bit-exact except (y-z)/s within 1e-6*max(1,|u|) of a rounding boundary; (s, z) exact "
+                    "except the fp32 value within 1e-6 relative of an fp16 tie"}
 
 
 def cpu_cores():
@@ -382,8 +411,9 @@ def main():
     # per-kernel breakdown from a separate pass (every launch between event pairs,
     # which costs the step some time, so it is not the timed region)
     nb = min(args.steps, 200)
-    kinds = ((ops.PROF_HISTORY, "history"), (ops.PROF_QUANTIZE, "quantize"), (ops.PROF_WINDOW_COPY, "window_copy"),
-             (ops.PROF_PREP, "prep"), (ops.PROF_WINDOW, "window"), (ops.PROF_COMBINE, "combine"))
+    kinds = ((ops.PROF_HISTORY, "history"), (ops.PROF_QUANTIZE, "append (quantise + window rows)"),
+             (ops.PROF_WINDOW_COPY, "window_copy"), (ops.PROF_WINDOW, "window + query prep"),
+             (ops.PROF_COMBINE, "combine"))
     ops.profile_enable([k for k, _ in kinds])
     for i in range(nb):
         decode_step(w, args.warmup + i, args.decode_kernel)
@@ -391,7 +421,8 @@ def main():
     kernel_ms = {}
     for kind, name in kinds:
         kms, kn = ops.profile_read(kind)
-        kernel_ms[name] = kms / nb if kn else 0.0
+        if kn:                                   # kinds that launched in this step
+            kernel_ms[name] = kms / nb
     ops.profile_enable(None)
 
     rec_tok, _ = ops.cache_bytes_per_token(w["cfg"])
@@ -451,6 +482,7 @@ def main():
         line["cpu_baseline"] = {"value": n * L / t, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                                 "sample": "%d x oracle fp64 decode of 1 request x %d q heads at L=%d "
                                           "(cache built untimed)" % (n, HQ, L)}
+        line["boundary_cases"] = boundary_cases(w)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

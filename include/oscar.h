@@ -137,6 +137,37 @@ int oscar_covariance(const double* samples, int64_t n, int32_t d, double* cov);
 int oscar_value_covariance(const double* scores, const double* values, int64_t n_q,
                            int64_t n_k, int32_t d, double* cov);
 
+/* ---- calibration statistics on the device ------------------------------ */
+
+/* Workspace bytes of oscar_covariance_device for n rows of width d (host output). */
+int oscar_covariance_workspace_bytes(int64_t n, int32_t d, size_t* bytes);
+
+/* C = (1/n) Σ_i x_iᵀ x_i over the rows of x, the query covariance C_Q of
+ * [OSCAR news] "OSCARの違い", on the device.
+ *  x          device, row-major n×d in x_dtype (OSCAR_DTYPE_BF16 or _F32)
+ *  cov        device, d×d fp64 output (symmetric, both triangles written)
+ *  workspace  device, >= oscar_covariance_workspace_bytes(n, d), 256-byte aligned
+ * Accumulated in fp64 (every product of bf16 or fp32 inputs is exact; the
+ * additions round) over row slices added in a fixed order, so repeated calls
+ * give identical results.  n >= 1, 1 <= d <= 4096.  Asynchronous on stream. */
+int oscar_covariance_device(const void* x, int32_t x_dtype, int64_t n, int32_t d, double* cov,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of oscar_value_covariance_device (host output). */
+int oscar_value_covariance_workspace_bytes(int64_t n_q, int64_t n_k, int32_t d, size_t* bytes);
+
+/* C_S = (1/n_q) Vᵀ Sᵀ S V, the score-weighted value covariance of
+ * [OSCAR news] "OSCARの違い", on the device: Y = S·V (fp64 accumulation),
+ * then C_S = (1/n_q) YᵀY as in oscar_covariance_device.
+ *  scores     device fp32 n_q×n_k (row-major attention scores of the calibration queries)
+ *  values     device n_k×d in v_dtype (OSCAR_DTYPE_BF16 or _F32)
+ *  cov        device d×d fp64 output
+ *  workspace  device, >= oscar_value_covariance_workspace_bytes(n_q, n_k, d), 256-byte aligned
+ * 1 <= n_q <= 4,194,240, n_k >= 1, 1 <= d <= 4096.  Asynchronous on stream. */
+int oscar_value_covariance_device(const float* scores, const void* values, int32_t v_dtype, int64_t n_q,
+                                  int64_t n_k, int32_t d, double* cov, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
 /* R = U · (H_d/√d) · P_br  ([OSCAR news] "OSCARの違い"; [Escha log] fix 3).
  *  cov       host d×d fp64 symmetric covariance, or NULL for U = I (the
  *            calibration-free Hadamard rotation, identical in every layer).
@@ -245,9 +276,10 @@ int oscar_decode_attention_simt(const oscar_config* cfg, const oscar_layer_cache
  * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
  *  - Sizes whose scratch need (oscar_decode_workspace_bytes) exceeds 16 MiB
  *    are rejected with OSCAR_ERR_WORKSPACE before anything is launched.
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *  - Every call looks up the array's device address in the current context
+ *    (cudaGetSymbolAddress, with the caller's device current), which
+ *    allocates nothing; the first call on a device may also load the
+ *    library's module there, so make it before any stream capture.
  *  - All calls on a device share the one array and it keeps the previous
  *    call's contents; every byte a call reads is written earlier in the same
  *    call, so nothing needs clearing.  Calls that overlap on the GPU (e.g.
@@ -261,10 +293,13 @@ int oscar_decode_attention_noalloc(const oscar_config* cfg, const oscar_layer_ca
 
 /* Event timing of the kernels: `enable` is a bit mask of kinds (bit k times
  * kind k; 0 disables) and earlier records are forgotten.  Kinds: 0 the
- * history kernel, 3 the query preparation, 4 the window and 5 the combine
- * kernel of oscar_decode_attention; 1 the quantise and 2 the window-copy kernel of
- * oscar_quantize_append.  A timed launch gets a CUDA event pair on the call's
- * stream (two cudaEventRecord, which also separate it from its neighbours). */
+ * history kernel, 4 the window kernel (which also prepares the rotated
+ * queries) and 5 the combine kernel of oscar_decode_attention; 1 the quantise
+ * kernel (for appends of at most W tokens it also writes the window rows) and
+ * 2 the window-copy kernel (larger appends) of oscar_quantize_append.  Kind 3
+ * is reserved and never recorded.  A timed launch gets a CUDA event pair on
+ * the call's stream (two cudaEventRecord, which also separate it from its
+ * neighbours). */
 int oscar_profile_enable(int32_t enable);
 
 /* Waits for the recorded events of `kind` and returns their summed duration

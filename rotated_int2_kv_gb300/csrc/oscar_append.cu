@@ -25,36 +25,68 @@ namespace oscar {
 
 // Quantises one rotated head vector held by a warp (lane: channels lane·CPL ..
 // lane·CPL + CPL - 1) and writes its codes and (s, z) pairs into the record.
-template <int D>
-__device__ __forceinline__ void quantize_store(const AppendParams& P, const float (&y)[D / 32], int slot, int h,
-                                               int mat, int lane) {
+// y came from a sequential fp32 FMA chain and lies within e of x·R rounded to
+// fp32; every (s, z) or code decision that y ± e could change is taken again on
+// y values formed by the compensated dot product of xk (the vector's bf16
+// elements) with the columns of R (row-major, row stride D).
+template <int D, class XF>
+__device__ __forceinline__ void quantize_store(const AppendParams& P, float (&y)[D / 32], int slot, int h, int mat,
+                                               int lane, float e, XF xk, const float* R) {
     constexpr int CPL = D / 32;
     const int lpg = P.G / CPL;       // lanes per group (4..32)
     const float r = P.clip;
     const int rec_off_codes = mat ? D / 4 : 0;
     const int ng = D / P.G;
     const int rec_off_sz = D / 2 + (mat ? 4 * ng : 0);
-    float mn = y[0], mx = y[0];
+    auto group_extremes = [&](float& mn, float& mx) {
+        mn = y[0];
+        mx = y[0];
 #pragma unroll
-    for (int j = 1; j < CPL; ++j) { mn = fminf(mn, y[j]); mx = fmaxf(mx, y[j]); }
-    for (int off = 1; off < lpg; off <<= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        for (int j = 1; j < CPL; ++j) { mn = fminf(mn, y[j]); mx = fmaxf(mx, y[j]); }
+        for (int off = 1; off < lpg; off <<= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        }
+    };
+    float mn, mx;
+    group_extremes(mn, mx);
+    uint32_t exact = 0;              // channels j of this lane whose y is already the compensated one
+    const bool unc = sz_uncertain(mn, mx, r, e);
+    if (__any_sync(0xffffffffu, unc)) {
+        // the extremes of an uncertain group lie among its channels within 2e of
+        // the computed ones: form those exactly and take the extremes again
+        const float tlo = __fadd_ru(mn, __fmul_ru(2.0f, e)), thi = __fsub_rd(mx, __fmul_ru(2.0f, e));
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            uint32_t m = __ballot_sync(0xffffffffu, unc && (y[j] <= tlo || y[j] >= thi));
+            while (m) {
+                const int L = __ffs(m) - 1;
+                m &= m - 1;
+                const float ye = dot2_warp<D>(xk, R, D, L * CPL + j, lane);
+                if (lane == L) {
+                    y[j] = ye;
+                    exact |= 1u << j;
+                }
+            }
+        }
+        group_extremes(mn, mx);
     }
-    const float lo = __fmul_rn(r, mn);
-    const float hi = __fmul_rn(r, mx);
-    const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 3.0f));
-    const __half z16 = __float2half_rn(lo);
+    __half s16, z16;
+    sz_decide(mn, mx, r, s16, z16);
     const float s = __half2float(s16), z = __half2float(z16);
+    const float band = code_band(e, s);
     uint32_t bits = 0;
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
-        uint32_t c = 0;
-        if (s != 0.0f) {
-            const float u = __fdiv_rn(__fsub_rn(y[j], z), s);
-            const float cr = fminf(fmaxf(rintf(u), 0.0f), 3.0f);
-            c = (uint32_t)cr;
+        float u = s != 0.0f ? __fdiv_rn(__fsub_rn(y[j], z), s) : 0.0f;
+        uint32_t m = __ballot_sync(0xffffffffu, s != 0.0f && !((exact >> j) & 1u) && code_near_boundary(u, band));
+        while (m) {
+            const int L = __ffs(m) - 1;
+            m &= m - 1;
+            const float ye = dot2_warp<D>(xk, R, D, L * CPL + j, lane);
+            if (lane == L) u = __fdiv_rn(__fsub_rn(ye, z), s);
         }
+        const uint32_t c = s != 0.0f ? (uint32_t)fminf(fmaxf(rintf(u), 0.0f), 3.0f) : 0u;
         bits |= c << (2 * j);
     }
     uint8_t* rec = P.records + ((int64_t)slot * P.Hkv + h) * P.rec_bytes;
@@ -73,6 +105,17 @@ __device__ __forceinline__ void quantize_store(const AppendParams& P, const floa
     }
 }
 
+// Σ x² of a vector, summed over the warp (lane: channels lane·CPL ..).
+template <int CPL>
+__device__ __forceinline__ float warp_sum_sq(const float (&x)[CPL]) {
+    float q = 0.0f;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) q = fmaf(x[j], x[j], q);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) q += __shfl_xor_sync(0xffffffffu, q, off);
+    return q;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads)
 quantize_kernel(AppendParams P) {
@@ -84,10 +127,10 @@ quantize_kernel(AppendParams P) {
     constexpr int kRCols = kResidentR ? D : kColBlock;
     constexpr int kXT = D * kTileVec;                   // transposed X tile, floats
     constexpr int kY = kTileVec * kYStride;             // Y tile, floats
-    constexpr int kXY = kResidentR ? (kXT > kY ? kXT : kY) : kXT + kY;
+    constexpr int kXY = kXT + kY;                       // x stays in place for the exact re-decisions
     float* sR = reinterpret_cast<float*>(smem);         // D x kRCols
     float* sXT = sR + D * kRCols;                       // D x 64
-    float* sY = kResidentR ? sXT : sXT + kXT;           // 64 x (D + 4); aliases sXT if R is resident
+    float* sY = sXT + kXT;                              // 64 x (D + 4)
     int* prefix = reinterpret_cast<int*>(sR + D * kRCols + kXY);   // batch + 1
     int* scratch = prefix + P.batch + 1;                // blockDim.x
     __shared__ int s_meta[kTileVec][4];                               // b, p, h, slot (-1: skip)
@@ -228,7 +271,6 @@ quantize_kernel(AppendParams P) {
             }
         }
         if (kResidentR) {
-            __syncthreads();  // sY aliases sXT
 #pragma unroll
             for (int cb = 0; cb < kNB; ++cb)
 #pragma unroll
@@ -244,10 +286,14 @@ quantize_kernel(AppendParams P) {
             const int slot = s_meta[v][3];
             if (slot < 0) continue;      // warp-uniform
             const int h = s_meta[v][2];
-            float y[CPL];
+            float y[CPL], xv[CPL];
 #pragma unroll
-            for (int j = 0; j < CPL; ++j) y[j] = sY[v * kYStride + lane * CPL + j];
-            quantize_store<D>(P, y, slot, h, mat, lane);
+            for (int j = 0; j < CPL; ++j) {
+                y[j] = sY[v * kYStride + lane * CPL + j];
+                xv[j] = sXT[(lane * CPL + j) * kTileVec + v];
+            }
+            const float e = fma_chain_bound<D>(warp_sum_sq<CPL>(xv));
+            quantize_store<D>(P, y, slot, h, mat, lane, e, [&](int k) { return sXT[k * kTileVec + v]; }, R);
         }
         __syncthreads();
     }
@@ -348,7 +394,10 @@ quantize_small_kernel(AppendParams P) {
             for (int j = 0; j < CPL; ++j) y[j] = fmaf(xk, rr[j], y[j]);
         }
         __syncwarp();
-        quantize_store<D>(P, y, slot, h, mat, lane);
+        const float eb = fma_chain_bound<D>(warp_sum_sq<CPL>(x));
+        const float* xw = sx[warp];
+        quantize_store<D>(P, y, slot, h, mat, lane, eb, [&](int k) { return xw[k]; }, Rs);
+        __syncwarp();   // sx[warp] is rewritten by the warp's next vector
     }
 }
 
@@ -466,12 +515,189 @@ quantize_vec_kernel(AppendParams P) {
         sy[tid] = y;
         __syncthreads();
         if (warp == 0) {                           // lane: channels lane·CPL .. + CPL - 1
-            float yv[CPL];
+            float yv[CPL], xv[CPL];
 #pragma unroll
-            for (int j = 0; j < CPL; ++j) yv[j] = sy[lane * CPL + j];
-            quantize_store<D>(P, yv, slot, h, mat, lane);
+            for (int j = 0; j < CPL; ++j) {
+                yv[j] = sy[lane * CPL + j];
+                xv[j] = sx[lane * CPL + j];
+            }
+            const float e = fma_chain_bound<D>(warp_sum_sq<CPL>(xv));
+            quantize_store<D>(P, yv, slot, h, mat, lane, e, [&](int k) { return sx[k]; }, R);
         }
         __syncthreads();                           // sx and sy are reused by the next vector
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Decode-step appends in one launch.  When a call appends at most W tokens in
+// total, every request's new tokens all land in a BF16 window (sink below S,
+// else the ring), and the tokens leaving the window are exactly the positions
+// q = p - W >= S of the new positions p: position q's ring row p % W is the one
+// that new position p overwrites.  So one warp per (new token, KV head) reads
+// the leaving row, writes the new row over it, and quantises the leaving row
+// into its history record (each lane reads and then writes the same elements,
+// which orders the two), in place of the quantise kernel followed by the
+// window copy.
+// ---------------------------------------------------------------------------
+
+// Resolves new row t (K or V of head h) of a decode-step append: request b,
+// position p, window row rq; false (with status bits) when the row is invalid.
+__device__ __forceinline__ bool resolve_new_row(const AppendParams& P, int64_t t, int& b, int& p, int& rq, int& bits) {
+    b = find_request(P.cu_new, P.batch, (int)t);
+    const int L0 = P.start_pos[b];
+    const int c0 = P.cu_new[b], n = P.cu_new[b + 1] - c0;
+    p = L0 + (int)(t - c0);
+    rq = P.req_idx ? P.req_idx[b] : b;
+    bits = 0;
+    if (L0 < 0 || t - c0 >= n) bits |= OSCAR_DEV_BAD_LEN;
+    if (rq < 0 || rq >= P.max_reqs) bits |= OSCAR_DEV_BAD_REQ;
+    return bits == 0;
+}
+
+// Row of position p (K or V of head h) in the sink or the recent ring of window row rq.
+__device__ __forceinline__ int64_t window_row(const AppendParams& P, int rq, int p, int h, int mat, int D) {
+    return p < P.S ? ((((int64_t)rq * P.S + p) * P.Hkv + h) * 2 + mat) * D
+                   : ((((int64_t)rq * P.W + p % P.W) * P.Hkv + h) * 2 + mat) * D;
+}
+
+// Slot of the history record of position q of request b, or -1 (with status bits).
+__device__ __forceinline__ int history_slot(const AppendParams& P, int b, int q, int& bits) {
+    if (q >= P.pt_stride) {
+        bits |= OSCAR_DEV_BAD_LEN;
+        return -1;
+    }
+    const int sl = P.page_table[(int64_t)b * P.pt_stride + q];
+    if (sl < 0 || sl >= P.num_slots) {
+        bits |= OSCAR_DEV_BAD_SLOT;
+        return -1;
+    }
+    return sl;
+}
+
+// d <= 128: one warp per (new token, KV head), R staged in shared memory.
+template <int D>
+__global__ void __launch_bounds__(kAppendThreads)
+append_step_kernel(AppendParams P) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
+    static_assert(D * D * 4 <= 64 * 1024, "R staged in shared memory");
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ float sx[kSmallVec][D];
+    float* sR = reinterpret_cast<float*>(smem);
+    constexpr int CPL = D / 32;
+    const int mat = blockIdx.y;
+    const float* R = mat ? P.rot_v : P.rot_k;
+    const void* src_new = mat ? P.v : P.k;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NU = D * D / 4 / kAppendThreads;   // 16-byte copies of R per thread
+#pragma unroll
+    for (int u = 0; u < NU; ++u)
+        cp_async16(sR + 4 * (tid + kAppendThreads * u), R + 4 * (tid + kAppendThreads * u));
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    const int64_t total = P.total_new * P.Hkv;
+    for (int64_t e = (int64_t)blockIdx.x * kSmallVec + warp; e < total; e += (int64_t)gridDim.x * kSmallVec) {
+        const int64_t t = e / P.Hkv;
+        const int h = (int)(e % P.Hkv);
+        int b, p, rq, bits;
+        const bool ok = resolve_new_row(P, t, b, p, rq, bits);
+        const int q = p - P.W;                       // the position leaving the window, if any
+        const bool spill = ok && q >= P.S;
+        int slot = spill ? history_slot(P, b, q, bits) : -1;
+        float xs[CPL], xn[CPL];
+        if (spill) {
+            const uint16_t* row = P.recent + window_row(P, rq, q, h, mat, D) + lane * CPL;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) xs[j] = bf16_bits_to_f32(row[j]);
+        }
+        const int64_t base = (t * P.Hkv + h) * D + lane * CPL;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) xn[j] = ok ? load_elem(src_new, base + j, P.kv_dtype) : 0.f;
+        if (ok) {   // the new row over the leaving one (this lane read its elements above)
+            uint16_t* dst = (p < P.S ? P.sink : P.recent) + window_row(P, rq, p, h, mat, D) + lane * CPL;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) dst[j] = f32_to_bf16_bits(xn[j]);
+        }
+        if (bits && lane == 0) set_status(P.status, bits);
+        if (slot < 0) continue;                      // warp-uniform
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) sx[warp][lane * CPL + j] = xs[j];
+        __syncwarp();
+        // ---- y = x · R, sequential over k (the order of the other CUDA-core kernels) ----
+        float y[CPL];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) y[j] = 0.f;
+#pragma unroll 8
+        for (int k = 0; k < D; ++k) {
+            const float xk = sx[warp][k];
+            const float* rr = sR + k * D + lane * CPL;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) y[j] = fmaf(xk, rr[j], y[j]);
+        }
+        const float eb = fma_chain_bound<D>(warp_sum_sq<CPL>(xs));
+        const float* xw = sx[warp];
+        quantize_store<D>(P, y, slot, h, mat, lane, eb, [&](int k) { return xw[k]; }, sR);
+        __syncwarp();   // sx[warp] is rewritten by the warp's next item
+    }
+}
+
+// d = 256 (R does not fit in shared memory): one block of D threads per (new
+// token, KV head); thread c owns element c of the rows and output channel c.
+template <int D>
+__global__ void __launch_bounds__(D, 2)
+append_step_vec_kernel(AppendParams P) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
+    constexpr int CPL = D / 32;
+    __shared__ float sx[D];
+    __shared__ float sy[D];
+    const int mat = blockIdx.y;
+    const float* R = mat ? P.rot_v : P.rot_k;
+    const void* src_new = mat ? P.v : P.k;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t total = P.total_new * P.Hkv;
+    for (int64_t e = blockIdx.x; e < total; e += gridDim.x) {
+        const int64_t t = e / P.Hkv;
+        const int h = (int)(e % P.Hkv);
+        int b, p, rq, bits;
+        const bool ok = resolve_new_row(P, t, b, p, rq, bits);
+        const int q = p - P.W;
+        const bool spill = ok && q >= P.S;
+        const int slot = spill ? history_slot(P, b, q, bits) : -1;
+        const float xs = spill ? bf16_bits_to_f32(P.recent[window_row(P, rq, q, h, mat, D) + tid]) : 0.f;
+        if (ok) {   // the new element over the leaving one (this thread read it above)
+            const float xn = load_elem(src_new, (t * P.Hkv + h) * D + tid, P.kv_dtype);
+            (p < P.S ? P.sink : P.recent)[window_row(P, rq, p, h, mat, D) + tid] = f32_to_bf16_bits(xn);
+        }
+        if (bits && tid == 0) set_status(P.status, bits);
+        if (slot < 0) continue;                      // the same decision in every thread
+        sx[tid] = xs;
+        __syncthreads();
+        float y = 0.f;
+        const float* rc = R + tid;
+        for (int k0 = 0; k0 < D; k0 += 32) {         // 32 rows of R in flight, then their FMAs in order
+            float r[32];
+            if constexpr (D == 256) {
+                ld32_col256(rc + (int64_t)k0 * D, r);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 32; ++u) r[u] = __ldg(rc + (int64_t)(k0 + u) * D);
+            }
+#pragma unroll
+            for (int u = 0; u < 32; ++u) y = fmaf(sx[k0 + u], r[u], y);
+        }
+        sy[tid] = y;
+        __syncthreads();
+        if (warp == 0) {
+            float yv[CPL], xv[CPL];
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                yv[j] = sy[lane * CPL + j];
+                xv[j] = sx[lane * CPL + j];
+            }
+            const float eb = fma_chain_bound<D>(warp_sum_sq<CPL>(xv));
+            quantize_store<D>(P, yv, slot, h, mat, lane, eb, [&](int k) { return sx[k]; }, R);
+        }
+        __syncthreads();                             // sx and sy are reused by the next item
     }
 }
 
@@ -534,7 +760,7 @@ static int launch_append(const AppendParams& P, int64_t total_new, cudaStream_t 
     const int r_cols = kResidentR ? D : kColBlock;
     size_t smem = (size_t)D * r_cols * 4;  // must match the carve-up in quantize_kernel
     const size_t xt = (size_t)D * kTileVec * 4, y = (size_t)kTileVec * (D + 4) * 4;
-    smem += kResidentR ? std::max(xt, y) : xt + y;
+    smem += xt + y;
     smem += (size_t)(P.batch + 1 + kAppendThreads) * 4;
     auto kern = quantize_kernel<D>;
     if (const int rc_ = ensure_dynamic_smem((const void*)kern, smem, "cudaFuncSetAttribute(quantize_kernel)"))
@@ -548,6 +774,26 @@ static int launch_append(const AppendParams& P, int64_t total_new, cudaStream_t 
     const int per_sm = kResidentR ? 2 : 1;
     const int64_t grid_x = std::max<int64_t>(1, std::min<int64_t>(max_tiles, (int64_t)sm_count() * per_sm / 2));
     const int64_t max_vec = max_units * P.Hkv;
+    // at most W new tokens in the call: every new row lands in a window, and the
+    // rows leaving the ring are quantised by the same launch (see append_step_kernel)
+    const bool step = total_new > 0 && total_new <= P.W &&
+                      (D * D * 4 > 64 * 1024 ? max_vec <= 2 * (int64_t)sm_count()
+                                             : max_vec <= (int64_t)sm_count() * kTileVec);
+    if (step) {
+        const int prof = prof_begin(1, stream);
+        if constexpr (D * D * 4 > 64 * 1024) {
+            launch_dependent(append_step_vec_kernel<D>, dim3((unsigned)max_vec, 2), dim3(D), 0, stream, P);
+        } else {
+            const size_t ssmem = (size_t)D * D * 4;
+            if (const int rc_ = ensure_dynamic_smem((const void*)append_step_kernel<D>, ssmem,
+                                                    "cudaFuncSetAttribute(append_step_kernel)"))
+                return rc_;
+            const int64_t gs = std::min<int64_t>((max_vec + kSmallVec - 1) / kSmallVec, (int64_t)sm_count() * 4);
+            launch_dependent(append_step_kernel<D>, dim3((unsigned)gs, 2), dim3(kAppendThreads), ssmem, stream, P);
+        }
+        prof_end(prof, stream);
+        return check_cuda("append_step_kernel launch");
+    }
     if (D * D * 4 > 64 * 1024 && max_vec > 0 && max_vec <= 2 * (int64_t)sm_count()) {
         // few vectors with R too large for shared memory (d 256): one block per vector
         const size_t vsmem = (size_t)(P.batch + 1 + D) * 4;

@@ -76,6 +76,93 @@ __device__ __forceinline__ int find_request(const int* prefix, int batch, int u)
     return lo;
 }
 
+// ---- exact code decisions -------------------------------------------------
+//
+// The codes and (s, z) of a vector are a function of y = x·R rounded to fp32.
+// The kernels form y with fp32 accumulation, so their y may differ from that
+// value by a bounded amount e.  Every decision below is a monotone function of
+// the y values it reads (fp32 operations and fp16 rounding are monotone), so a
+// decision taken at both ends of [y - e, y + e] that comes out the same is the
+// decision of the exact y.  Where the two ends disagree, the y values that
+// decide it are formed again with a compensated dot product (Ogita, Rump and
+// Oishi's Dot2: error-free products and sums carried in a second fp32 word),
+// which is faithful to the exact product, and the decision is taken on them.
+
+// The fp16 (scale, zero) of a group from its extremes, in the order the
+// quantiser defines: lo = r·min, hi = r·max, s = fp16((hi - lo)/3), z = fp16(lo).
+__device__ __forceinline__ void sz_decide(float mn, float mx, float r, __half& s16, __half& z16) {
+    const float lo = __fmul_rn(r, mn);
+    const float hi = __fmul_rn(r, mx);
+    s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 3.0f));
+    z16 = __float2half_rn(lo);
+}
+
+// True when extremes anywhere in [mn - e, mn + e] × [mx - e, mx + e] could give
+// another (s, z): s grows with mx and falls with mn, z grows with mn.
+__device__ __forceinline__ bool sz_uncertain(float mn, float mx, float r, float e) {
+    __half sa, za, sb, zb;
+    sz_decide(__fsub_rd(mn, e), __fadd_ru(mx, e), r, sa, za);   // widest range: largest s, smallest z
+    sz_decide(__fadd_ru(mn, e), __fsub_rd(mx, e), r, sb, zb);   // narrowest range: smallest s, largest z
+    return __half_as_ushort(sa) != __half_as_ushort(sb) || __half_as_ushort(za) != __half_as_ushort(zb);
+}
+
+// Half-width in units of the quotient u = (y - z)/s of the band around a
+// rounding boundary (0.5, 1.5, 2.5) inside which y ± e may decide another code:
+// e/s plus the roundings of y - z and of the division (2^-21 relative for |u|
+// up to 3), with margin.
+__device__ __forceinline__ float code_band(float e, float s) {
+    return s != 0.0f ? __fmaf_ru(__fdiv_ru(e, s), 1.0f + 1.0f / 1048576.0f, 1.0f / 524288.0f) : 0.0f;
+}
+
+// True when the correctly rounded quotient u lies within `band` of a rounding
+// boundary that changes the clamped code.
+__device__ __forceinline__ bool code_near_boundary(float u, float band) {
+    const float d = fminf(fminf(fabsf(u - 0.5f), fabsf(u - 1.5f)), fabsf(u - 2.5f));
+    return d <= band;
+}
+
+// Σ_k x_k·R[k][j] over k < D, faithfully rounded (compensated), by the whole
+// warp: lane l takes k = l, l + 32, ...; every lane returns the result.  xk(k)
+// returns the bf16-exact input element k; R is row-major with row stride ldr.
+template <int D, class XF>
+__device__ __noinline__ float dot2_warp(XF xk, const float* R, int ldr, int j, int lane) {
+    float s = 0.0f, c = 0.0f;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) {
+        const int k = lane + 32 * i;
+        const float a = xk(k), b = R[(int64_t)k * ldr + j];
+        const float p = __fmul_rn(a, b);
+        const float pe = __fmaf_rn(a, b, -p);                       // a·b = p + pe exactly
+        const float t = __fadd_rn(s, p);
+        const float bp = __fsub_rn(t, s);
+        const float er = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(p, bp));   // s + p = t + er
+        s = t;
+        c = __fadd_rn(c, __fadd_rn(er, pe));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float so = __shfl_xor_sync(0xffffffffu, s, off);
+        const float co = __shfl_xor_sync(0xffffffffu, c, off);
+        const float t = __fadd_rn(s, so);
+        const float bp = __fsub_rn(t, s);
+        const float er = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(so, bp));
+        s = t;
+        c = __fadd_rn(__fadd_rn(c, co), er);
+    }
+    return __fadd_rn(s, c);
+}
+
+// Bound on |y_j - fl(x·R_j)| for every channel j of a vector whose y was formed
+// by a sequential fp32 FMA chain over k < D (D roundings), given Σ x_k²:
+// γ_D·Σ_k |x_k||R_kj| <= γ_D·‖x‖₂·‖R_j‖₂ (R orthogonal: ‖R_j‖₂ = 1 up to
+// rounding), plus half an ulp of the rounded result (<= 2^-24·‖x‖₂), with a
+// 1% margin for R's rounding and the evaluation of the norm.
+template <int D>
+__device__ __forceinline__ float fma_chain_bound(float x_sq) {
+    constexpr float k = 1.01f * (float)(D + 2) / 16777216.0f;
+    return k * sqrtf(x_sq);
+}
+
 // Tensor-core rotation + quantisation of large appends (head_dim 64 or 128);
 // returns OSCAR_OK after launching, or a negative status.
 template <int D>

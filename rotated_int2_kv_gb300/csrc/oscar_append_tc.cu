@@ -31,9 +31,13 @@
 //
 // The code decision uses the correctly rounded reciprocal of 3s: q = 3·sat(a ·
 // (1/3s)) with a = y - z is within 2^-21 of the correctly rounded quotient a/s
-// for q in [0, 3] (three roundings), so rint(q) is the oracle's code unless q
-// lies within 2^-19 of a half-integer; a warp in which some thread meets such a
-// q in a group decides that group again with correctly rounded division.
+// for q in [0, 3] (three roundings).  The tensor cores' y differs from x·R
+// rounded to fp32 by at most e = kTcBound·‖y‖₂, so rint(q) is the code of the
+// exact y unless q lies within e/s + 2^-19 + 2^-21 of a half-integer; a warp
+// in which some thread meets such a q in a group decides that group again with
+// correctly rounded division, forming y exactly (compensated dot product of
+// the input row with R's column) wherever y ± e straddles a boundary.  The
+// group's (s, z) are checked the same way at its extremes ± e first.
 // Tensor-memory loads (tcgen05.ld) are warp-collective, so every branch around
 // them is warp-uniform.
 #include <algorithm>
@@ -54,7 +58,16 @@ constexpr int kTcThreads = 128 * kSlots;
 constexpr uint32_t kTmemCols = 512;        // slot e's accumulator: columns 128·e .. 128·e + d
 constexpr int kMetaInts = 4;               // per vector: slot, head | kind << 16, source offset (int64)
 constexpr float kMagic = 12582912.0f;      // 1.5·2^23: x + kMagic rounds x to an integer in the low bits
-constexpr float kTieBand = 0.5f - 1.0f / 524288.0f;   // |q - rint(q)| above this: within 2^-19 of a tie
+// Bound on |y - fl(x·R)| per channel, in units of 2^-24·‖y‖₂.  Measured on
+// GB300 (kind::f16, fp32 accumulator): within one MMA the terms are aligned to
+// the largest one at a resolution of 2^-25 of its binade and truncated, and the
+// sum is truncated to fp32 (1 - 2^-26 gives 1, 2^30 + 1 - 2^30 gives 0).  Over
+// rows of Gaussian, outlier-channel, wide-exponent and column-aligned inputs the
+// largest error of this kernel's order (lo, mid, hi parts) was 7.3·2^-24·‖x‖₂
+// (2.1 on outlier-channel rows); the bound takes twice the largest, and ‖x‖₂ =
+// ‖y‖₂ for an orthogonal R (1% margin).
+constexpr float kTcErr = 16.0f;
+constexpr float kTcBound = 1.01f * (kTcErr + 1.0f) / 16777216.0f;
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
@@ -114,31 +127,20 @@ __device__ __forceinline__ void minmax32(const float (&y)[32], float& mn, float&
     mx = max3f(mx, max3f(b[0], b[1], b[2]), b[3]);
 }
 
-// Codes of 32 channels as two words of 16 (channel i at bits 2i).  EXACT:
-// correctly rounded division (the same codes as the reciprocal path wherever
-// that one is not near a tie).  Otherwise the reciprocal path on channel pairs
-// (paired fp32 operations), and bit 31 of `tie` is cleared when some
-// |q - rint(q)| reaches kTieBand.  s = 0 (a flat group) gives codes 0 either way.
-template <bool EXACT>
-__device__ __forceinline__ void codes32(const float (&y)[32], float zc, float sc, float r3, uint32_t& w0, uint32_t& w1,
+__device__ __forceinline__ void pack_codes32(const float2 (&c)[16], uint32_t& w0, uint32_t& w1);
+
+// Codes of 32 channels as two words of 16 (channel i at bits 2i) by the
+// reciprocal path on channel pairs (paired fp32 operations); bit 31 of `tie` is
+// cleared when some |q - rint(q)|² reaches -nb2 (q within the group's band of a
+// half-integer).  s = 0 (a flat group) takes r3 = 0 and gives codes 0.
+__device__ __forceinline__ void codes32(const float (&y)[32], float zc, float r3, float nb2, uint32_t& w0, uint32_t& w1,
                                         uint32_t& tie) {
     float2 c[16];                         // codes of channels (2j, 2j+1) as floats
-    if (EXACT) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            float v[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float a = __fsub_rn(y[2 * j + h], zc);
-                v[h] = sc != 0.0f ? fminf(fmaxf(rintf(__fdiv_rn(a, sc)), 0.0f), 3.0f) : 0.0f;
-            }
-            c[j] = make_float2(v[0], v[1]);
-        }
-    } else {
+    {
         const float2 nz = make_float2(-zc, -zc), three = make_float2(3.0f, 3.0f);
         const float2 mg = make_float2(kMagic, kMagic), nmg = make_float2(-kMagic, -kMagic);
         const float2 m1 = make_float2(-1.0f, -1.0f);
-        const float2 nb = make_float2(-kTieBand * kTieBand, -kTieBand * kTieBand);
+        const float2 nb = make_float2(nb2, nb2);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const float2 a = __fadd2_rn(make_float2(y[2 * j], y[2 * j + 1]), nz);                 // y - z
@@ -150,7 +152,13 @@ __device__ __forceinline__ void codes32(const float (&y)[32], float zc, float sc
             tie &= __float_as_uint(e.x) & __float_as_uint(e.y);
         }
     }
-    // Σ c_i 4^i over 8 channels per value, as a depth-3 tree of exact integer FMAs
+    pack_codes32(c, w0, w1);
+}
+
+// Packs 32 codes held as floats (channels 2j, 2j+1 in c[j]) into two words of
+// 16 (channel i at bits 2i): Σ c_i 4^i over 8 channels per value, as a
+// depth-3 tree of exact integer FMAs.
+__device__ __forceinline__ void pack_codes32(const float2 (&c)[16], uint32_t& w0, uint32_t& w1) {
     const float2 k16 = make_float2(16.0f, 16.0f), k256 = make_float2(256.0f, 256.0f);
     float2 A[8];
 #pragma unroll
@@ -164,6 +172,24 @@ __device__ __forceinline__ void codes32(const float (&y)[32], float zc, float sc
     }
     w0 = __byte_perm(u[0], u[1], 0x5410);
     w1 = __byte_perm(u[2], u[3], 0x5410);
+}
+
+// fl(x·R[:, ch]) (compensated, faithful) for the vector of lane L, computed by
+// the whole warp; kind / off locate the vector's bf16 row (1: the recent ring,
+// 2: the new input, converted to bf16 as it is read; anything else: zeros).
+template <int D>
+__device__ __noinline__ float tc_exact_y(const uint16_t* recent, const void* src_new, int kv_dtype, const float* R,
+                                         int kind, int64_t off, int L, int ch, int lane) {
+    const int kd = __shfl_sync(0xffffffffu, kind, L);
+    const uint32_t olo = __shfl_sync(0xffffffffu, (uint32_t)(uint64_t)off, L);
+    const uint32_t ohi = __shfl_sync(0xffffffffu, (uint32_t)((uint64_t)off >> 32), L);
+    const int64_t o = (int64_t)(((uint64_t)ohi << 32) | olo);
+    auto xk = [&](int k) -> float {
+        if (kd == 1) return bf16_bits_to_f32(recent[o + k]);
+        if (kd == 2) return bf16_bits_to_f32(f32_to_bf16_bits(load_elem(src_new, o + k, kv_dtype)));
+        return 0.0f;
+    };
+    return dot2_warp<D>(xk, R, D, ch, lane);
 }
 
 template <int D>
@@ -461,10 +487,29 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
         // ---- quantise vector gt of the tile ----
         const int* m = gmeta + (buf * kTcRows + gt) * kMetaInts;
         const int slot = m[0];
+        const int mkind = m[1] >> 16;
+        const int64_t moff = *reinterpret_cast<const int64_t*>(m + 2);
         uint8_t* rec = P.records + ((int64_t)(slot < 0 ? 0 : slot) * P.Hkv + (m[1] & 0xFFFF)) * P.rec_bytes;
         uint32_t words[NW];
         constexpr int NC = G / 32;                // 32-channel chunks per group
         constexpr bool kKeep = G <= 64;           // the group's y stays in registers between the passes
+        // e bounds |y - fl(x·R)| on every channel of the vector (kTcBound·‖y‖₂)
+        float e;
+        {
+            float2 q2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                float yy[32];
+                load_y(tacc + 32 * c, yy);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float2 v = make_float2(yy[2 * q], yy[2 * q + 1]);
+                    q2 = __ffma2_rn(v, v, q2);
+                }
+            }
+            e = kTcBound * sqrtf(q2.x + q2.y);
+        }
+        const float e2 = __fmul_ru(2.0f, e);
 #pragma unroll
         for (int gi = 0; gi < ng; ++gi) {
             float yk[kKeep ? NC : 1][32];
@@ -475,27 +520,79 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
                 load_y(tacc + gi * G + 32 * c, y);
                 minmax32(y, mn, mx);
             }
-            const float lo = __fmul_rn(rclip, mn);
-            const float hi = __fmul_rn(rclip, mx);
-            const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 3.0f));
-            const __half z16 = __float2half_rn(lo);
+            // (s, z) that y ± e could change: the group's extremes lie among the
+            // channels within 2e of the computed ones; form those exactly
+            const bool unc = sz_uncertain(mn, mx, rclip, e);
+            if (__any_sync(0xffffffffu, unc)) {
+                const float tlo = __fadd_ru(mn, e2), thi = __fsub_rd(mx, e2);
+                float mne = INFINITY, mxe = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    if (!kKeep) load_y(tacc + gi * G + 32 * c, yk[0]);
+                    const float (&y)[32] = yk[kKeep ? c : 0];
+                    uint32_t cm = 0;
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) cm |= (unc && (y[q] <= tlo || y[q] >= thi)) ? (1u << q) : 0u;
+                    uint32_t bal;
+                    while ((bal = __ballot_sync(0xffffffffu, cm != 0u)) != 0u) {
+                        const int L = __ffs(bal) - 1;
+                        const int q = __shfl_sync(0xffffffffu, __ffs(cm) - 1, L);
+                        const float ye = tc_exact_y<D>(P.recent, src_new, P.kv_dtype, R, mkind, moff, L,
+                                                       gi * G + 32 * c + q, lane);
+                        if (lane == L) {
+                            cm &= cm - 1u;
+                            mne = fminf(mne, ye);
+                            mxe = fmaxf(mxe, ye);
+                        }
+                    }
+                }
+                if (unc) {
+                    mn = mne;
+                    mx = mxe;
+                }
+            }
+            __half s16, z16;
+            sz_decide(mn, mx, rclip, s16, z16);
             const float sc = __half2float(s16), zc = __half2float(z16);
             // tcgen05.ld is warp-collective: every lane runs the same loads.  A flat
             // group (s = 0) takes r3 = 0, so its fast-path codes are all 0.
             const float r3 = sc != 0.0f ? __frcp_rn(3.0f * sc) : 0.0f;   // 3·sc is exact (11-bit significand × 3)
+            // a code is certain when its quotient is farther from a half-integer than
+            // e/s plus the reciprocal path's 2^-21
+            const float be = code_band(e, sc);
+            const float hb = 0.5f - (be + 1.0f / 2097152.0f);
+            const float nb2 = hb > 0.0f ? -hb * hb : 0.0f;
             uint32_t tie = 0xFFFFFFFFu;
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
                 if (!kKeep) load_y(tacc + gi * G + 32 * c, yk[0]);
-                codes32<false>(yk[kKeep ? c : 0], zc, sc, r3, words[gi * (G / 16) + 2 * c],
-                               words[gi * (G / 16) + 2 * c + 1], tie);
+                codes32(yk[kKeep ? c : 0], zc, r3, nb2, words[gi * (G / 16) + 2 * c], words[gi * (G / 16) + 2 * c + 1],
+                        tie);
             }
-            if (__any_sync(0xffffffffu, !(tie >> 31))) {   // a quotient near a tie: decide the group exactly
+            if (__any_sync(0xffffffffu, !(tie >> 31))) {
+                // a quotient near a tie: decide the group by correctly rounded
+                // division, on the exact y where y ± e straddles a boundary
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
                     if (!kKeep) load_y(tacc + gi * G + 32 * c, yk[0]);
-                    codes32<true>(yk[kKeep ? c : 0], zc, sc, r3, words[gi * (G / 16) + 2 * c],
-                                  words[gi * (G / 16) + 2 * c + 1], tie);
+                    const float (&y)[32] = yk[kKeep ? c : 0];
+                    float2 cc[16];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        float u = sc != 0.0f ? __fdiv_rn(__fsub_rn(y[q], zc), sc) : 0.0f;
+                        uint32_t mm = __ballot_sync(0xffffffffu, sc != 0.0f && code_near_boundary(u, be));
+                        while (mm) {
+                            const int L = __ffs(mm) - 1;
+                            mm &= mm - 1u;
+                            const float ye = tc_exact_y<D>(P.recent, src_new, P.kv_dtype, R, mkind, moff, L,
+                                                           gi * G + 32 * c + q, lane);
+                            if (lane == L) u = __fdiv_rn(__fsub_rn(ye, zc), sc);
+                        }
+                        const float cv = sc != 0.0f ? fminf(fmaxf(rintf(u), 0.0f), 3.0f) : 0.0f;
+                        if (q & 1) cc[q >> 1].y = cv;
+                        else cc[q >> 1].x = cv;
+                    }
+                    pack_codes32(cc, words[gi * (G / 16) + 2 * c], words[gi * (G / 16) + 2 * c + 1]);
                 }
             }
             if (slot >= 0) *reinterpret_cast<__half2*>(rec + rec_off_sz + 4 * gi) = __halves2half2(s16, z16);

@@ -40,33 +40,27 @@ __device__ __forceinline__ bool request_valid(const DecodeParams& P, int b, int*
 }
 
 // ---------------------------------------------------------------------------
-// prep: per request, q̃ = q·R_K·(log2 e/√d) for every query head (fp32), its
-// fp16 hi/lo split (of q̃/α) packed as mma B fragments, the per-group sums,
-// the effective length / window row, and (block 0) the chunk prefix.
+// prep: per (KV head, request), q̃ = q·R_K·(log2 e/√d) for the KV head's query
+// heads (fp32), its fp16 hi/lo split (of q̃/α) packed as mma B fragments, the
+// per-group sums; block (0, b) also the effective length / window row of
+// request b, and block (0, 0) the chunk prefix.  It runs as the last z-slice of
+// the window kernel's grid (128 threads), so the two need one launch.
 // ---------------------------------------------------------------------------
-constexpr int kPrepHeads = 8;     // query heads per prep block
+constexpr int kPrepThreads = 128;
 
-template <int D>
-__global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
-    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
-    // R_K is staged in shared memory (all 16-byte copies in flight at once)
-    // when it fits in 64 KB (d <= 128)
-    constexpr bool kResidentR = (D * D * 4 <= 64 * 1024);
-    extern __shared__ __align__(16) float s_rk[];
-    __shared__ float sq[kPrepHeads][D];
-    __shared__ float sqt[kPrepHeads][D];
+// Shared floats the prep slice needs: q and q̃ of up to 16 query heads.
+__host__ __device__ constexpr int prep_smem_floats(int D, int g) { return 2 * g * D; }
+
+template <int D, int GQ>
+__device__ __forceinline__ void prep_slice(const DecodeParams& P, int hk, int b, float* sm) {
     __shared__ int scan[8];
-    const int b = blockIdx.x;
-    const int tid = threadIdx.x;
-    if (kResidentR) {
-#pragma unroll
-        for (int u = 0; u < D * D / 4 / 256; ++u)
-            cp_async16(s_rk + 4 * (tid + 256 * u), P.rot_k + 4 * (tid + 256 * u));
-        cp_async_commit();
-    }
-    if (b == 0 && blockIdx.y == 0) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = P.g;
+    float* sq = sm;              // [GQ][D] q (rows >= g zero)
+    float* sqt = sm + GQ * D;    // [g][D] q̃
+    if (hk == 0 && b == 0) {
         // chunk prefix over all requests (re-derives validity locally)
-        const int per = (P.batch + 255) / 256;
+        const int per = (P.batch + kPrepThreads - 1) / kPrepThreads;
         const int b0 = min(P.batch, tid * per), b1 = min(P.batch, b0 + per);
         int local = 0;
         for (int r = b0; r < b1; ++r) {
@@ -81,11 +75,10 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
             if (request_valid(P, r, &L, &rq)) run += n_chunks(L, P);
         }
         if (tid == 0) P.cprefix[P.batch] = total;
-        __syncthreads();
     }
     int L, rq;
     const bool ok = request_valid(P, b, &L, &rq);
-    if (tid == 0 && blockIdx.y == 0) {
+    if (hk == 0 && tid == 0) {
         P.len[b] = ok ? L : 0;
         for (int h = 0; h < P.Hkv * kCombGroups; ++h) P.comb_count[(int64_t)b * P.Hkv * kCombGroups + h] = 0;
         P.req[b] = ok ? rq : 0;
@@ -96,125 +89,122 @@ __global__ void __launch_bounds__(256) prep_kernel(DecodeParams P) {
             set_status(P.status, bits);
         }
     }
-    {
-        const int h0 = blockIdx.y * kPrepHeads;
-        const int nh = min(kPrepHeads, P.Hq - h0);
-        __syncthreads();
-        {   // every thread's q loads in flight together
-            constexpr int NQ = (kPrepHeads * D + 255) / 256;
-            float qv[NQ];
+    {   // the q rows of the KV head's query heads: every thread's loads in flight together
+        constexpr int NQ = GQ * D / kPrepThreads;
+        const int64_t qb = ((int64_t)b * P.Hq + hk * g) * D;
+        float qv[NQ];
 #pragma unroll
-            for (int u = 0; u < NQ; ++u) {
-                const int i = tid + 256 * u;
-                qv[u] = i < nh * D ? load_elem(P.q, ((int64_t)b * P.Hq + h0 + i / D) * D + i % D, P.q_dtype) : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < NQ; ++u) {
-                const int i = tid + 256 * u;
-                if (i < nh * D) sq[i / D][i % D] = qv[u];
-            }
+        for (int u = 0; u < NQ; ++u) {
+            const int i = tid + kPrepThreads * u;
+            qv[u] = i < g * D ? load_elem(P.q, qb + i, P.q_dtype) : 0.f;
         }
-        if (kResidentR) cp_async_wait<0>();
-        __syncthreads();
-        const float* RK = kResidentR ? s_rk : P.rot_k;
-        // thread (column, head half): 16 loads of R_K in flight per batch of k
-        constexpr int kHalves = 256 / D > 1 ? 256 / D : 1;   // threads per column
-        constexpr int kHPT = kPrepHeads / kHalves;           // heads per thread
-        for (int ci = tid; ci < D * kHalves; ci += 256) {
-            const int col = ci % D, hb = (ci / D) * kHPT;
-            float acc[kHPT];
 #pragma unroll
-            for (int j = 0; j < kHPT; ++j) acc[j] = 0.f;
-            constexpr int KB = kResidentR ? 16 : 32;   // rows of R_K in flight (from L2 when not staged)
-            for (int k0 = 0; k0 < D; k0 += KB) {
-                float r[KB];
+        for (int u = 0; u < NQ; ++u) sq[tid + kPrepThreads * u] = qv[u];   // rows >= g hold zeros
+    }
+    __syncthreads();
+    // thread (column, head subset): 32 rows of R_K in flight from L2 per batch of k
+    constexpr int kSplit = D < kPrepThreads ? kPrepThreads / D : 1;   // threads per column
+    constexpr int kHPT = GQ / kSplit;                                   // heads per thread
+    for (int ci = tid; ci < D * kSplit; ci += kPrepThreads) {
+        const int col = ci % D, hs = ci / D;
+        float acc[kHPT];
 #pragma unroll
-                for (int u = 0; u < KB; ++u) r[u] = RK[(int64_t)(k0 + u) * D + col];
+        for (int j = 0; j < kHPT; ++j) acc[j] = 0.f;
+        for (int k0 = 0; k0 < D; k0 += 32) {
+            float r[32];
 #pragma unroll
-                for (int u = 0; u < KB; ++u)
+            for (int u = 0; u < 32; ++u) r[u] = __ldg(P.rot_k + (int64_t)(k0 + u) * D + col);
 #pragma unroll
-                    for (int j = 0; j < kHPT; ++j) acc[j] = fmaf(sq[hb + j][k0 + u], r[u], acc[j]);
-            }
-            for (int j = 0; j < kHPT && hb + j < nh; ++j) {
+            for (int u = 0; u < 32; ++u)
+#pragma unroll
+                for (int j = 0; j < kHPT; ++j) acc[j] = fmaf(sq[(j * kSplit + hs) * D + k0 + u], r[u], acc[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < kHPT; ++j) {
+            const int h = j * kSplit + hs;
+            if (h < g) {
                 const float v = acc[j] * P.qscale;
-                sqt[hb + j][col] = v;
-                P.qt[((int64_t)b * P.Hq + h0 + hb + j) * D + col] = v;
+                sqt[h * D + col] = v;
+                P.qt[((int64_t)b * P.Hq + hk * g + h) * D + col] = v;
             }
-        }
-        __syncthreads();
-        // Per group, from the fp16 hi + lo parts actually fed to the MMA: Q = Σ q̃
-        // and Q' = Σ (fed value).  The fed value of channel c is q̃·2^(kQkExp - bit)
-        // for groups >= 64 (subnormal codes; Q' unused there) and q̃/α for group
-        // size 32, whose codes enter as 1 + α·c with α = 1/16 on even and 1/4 on
-        // odd channels (Q' is subtracted from the accumulator).
-        const int lane = tid & 31, warp = tid >> 5;
-        for (int i = warp; i < nh * P.ng; i += 8) {
-            const int j = i / P.ng, gi = i % P.ng;
-            float sq_ = 0.f, sqa = 0.f;
-            for (int c = gi * P.G + lane; c < (gi + 1) * P.G; c += 32) {
-                const float inv = P.G >= 64 ? (float)(1u << (kQkExp - sub_bit(c & 7))) : ((c & 1) ? 4.f : 16.f);
-                const float x = sqt[j][c] * inv;
-                const __half hi = __float2half_rn(x);
-                const __half lo = __float2half_rn(x - __half2float(hi));
-                const float v = __half2float(hi) + __half2float(lo);
-                sqa += v;
-                sq_ += v / inv;
-            }
-            for (int off = 16; off; off >>= 1) {
-                sq_ += __shfl_xor_sync(0xffffffffu, sq_, off);
-                sqa += __shfl_xor_sync(0xffffffffu, sqa, off);
-            }
-            if (lane == 0) P.qsum[((int64_t)b * P.Hq + h0 + j) * P.ng + gi] = make_float2(sq_, sqa);
-        }
-        // B fragments: [Hkv][n_tiles][D/16][32 lanes] of (b0b1, b2b3);
-        // column n of tile nt is (head 4nt + n/2 of the KV group, part n%2).
-        const int nfr = P.Hkv * P.n_frag_tiles * (D / 16) * 32;
-        for (int i = tid; i < nfr; i += 256) {
-            const int lane = i & 31;
-            const int kk = (i >> 5) % (D / 16);
-            const int nt = (i / (32 * (D / 16))) % P.n_frag_tiles;
-            const int hk = i / (32 * (D / 16) * P.n_frag_tiles);
-            const int n = lane >> 2, j = lane & 3;
-            const int head = hk * P.g + 4 * nt + (n >> 1);
-            const int part = n & 1;
-            if (4 * nt + (n >> 1) >= P.g) {         // padding column: zero, written once
-                if (blockIdx.y == 0)
-                    P.qfrag[(((int64_t)b * P.Hkv + hk) * P.n_frag_tiles + nt) * (D / 16) * 32 + kk * 32 + lane] =
-                        make_uint2(0u, 0u);
-                continue;
-            }
-            if (head < h0 || head >= h0 + nh) continue;
-            // Group size 32: k-cols (2j, 2j+1) <- channels (16kk+2j, 16kk+2j+8), even:
-            // scaled by 16; k-cols (2j+8, 2j+9) <- channels (16kk+2j+1, 16kk+2j+9), odd:
-            // scaled by 4.  Groups >= 64: lane j owns word w = 4(kk/4) + j; k-step kk
-            // takes slot kk%4 of it: k-cols (2j, 2j+1) <- first position p of both
-            // halves (channels 16w + p, 16w + 8 + p), (2j+8, 2j+9) <- second position.
-            int chans[4];
-            float scl[4];
-            if (P.G >= 64) {
-                const int w = 4 * (kk / 4) + j, p0 = slot_pos(kk % 4, 0), p1 = slot_pos(kk % 4, 1);
-                chans[0] = 16 * w + p0; chans[1] = 16 * w + 8 + p0;
-                chans[2] = 16 * w + p1; chans[3] = 16 * w + 8 + p1;
-                scl[0] = scl[1] = (float)(1u << (kQkExp - sub_bit(p0)));
-                scl[2] = scl[3] = (float)(1u << (kQkExp - sub_bit(p1)));
-            } else {
-                chans[0] = 16 * kk + 2 * j; chans[1] = 16 * kk + 2 * j + 8;
-                chans[2] = 16 * kk + 2 * j + 1; chans[3] = 16 * kk + 2 * j + 9;
-                scl[0] = scl[1] = 16.f;
-                scl[2] = scl[3] = 4.f;
-            }
-            uint16_t hv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float x = sqt[head - h0][chans[e]] * scl[e];
-                const __half hi = __float2half_rn(x);
-                const __half v = part ? __float2half_rn(x - __half2float(hi)) : hi;
-                hv[e] = *reinterpret_cast<const uint16_t*>(&v);
-            }
-            P.qfrag[(((int64_t)b * P.Hkv + hk) * P.n_frag_tiles + nt) * (D / 16) * 32 + kk * 32 + lane] =
-                make_uint2((uint32_t)hv[0] | ((uint32_t)hv[1] << 16), (uint32_t)hv[2] | ((uint32_t)hv[3] << 16));
         }
     }
+    __syncthreads();
+    // Per group, from the fp16 hi + lo parts actually fed to the MMA: Q = Σ q̃
+    // and Q' = Σ (fed value).  The fed value of channel c is q̃·2^(kQkExp - bit)
+    // for groups >= 64 (subnormal codes; Q' unused there) and q̃/α for group
+    // size 32, whose codes enter as 1 + α·c with α = 1/16 on even and 1/4 on
+    // odd channels (Q' is subtracted from the accumulator).
+    for (int i = warp; i < g * P.ng; i += kPrepThreads / 32) {
+        const int j = i / P.ng, gi = i % P.ng;
+        float sq_ = 0.f, sqa = 0.f;
+        for (int c = gi * P.G + lane; c < (gi + 1) * P.G; c += 32) {
+            const float inv = P.G >= 64 ? (float)(1u << (kQkExp - sub_bit(c & 7))) : ((c & 1) ? 4.f : 16.f);
+            const float x = sqt[j * D + c] * inv;
+            const __half hi = __float2half_rn(x);
+            const __half lo = __float2half_rn(x - __half2float(hi));
+            const float v = __half2float(hi) + __half2float(lo);
+            sqa += v;
+            sq_ += v / inv;
+        }
+        for (int off = 16; off; off >>= 1) {
+            sq_ += __shfl_xor_sync(0xffffffffu, sq_, off);
+            sqa += __shfl_xor_sync(0xffffffffu, sqa, off);
+        }
+        if (lane == 0) P.qsum[((int64_t)b * P.Hq + hk * g + j) * P.ng + gi] = make_float2(sq_, sqa);
+    }
+    // B fragments of KV head hk: [n_tiles][D/16][32 lanes] of (b0b1, b2b3);
+    // column n of tile nt is (head 4nt + n/2 of the KV group, part n%2).
+    const int nfr = P.n_frag_tiles * (D / 16) * 32;
+    uint2* qf = P.qfrag + ((int64_t)b * P.Hkv + hk) * nfr;
+    for (int i = tid; i < nfr; i += kPrepThreads) {
+        const int ln = i & 31;
+        const int kk = (i >> 5) % (D / 16);
+        const int nt = i / (32 * (D / 16));
+        const int n = ln >> 2, j = ln & 3;
+        const int hh = 4 * nt + (n >> 1);
+        const int part = n & 1;
+        if (hh >= g) {                               // padding column: zero
+            qf[i] = make_uint2(0u, 0u);
+            continue;
+        }
+        // Group size 32: k-cols (2j, 2j+1) <- channels (16kk+2j, 16kk+2j+8), even:
+        // scaled by 16; k-cols (2j+8, 2j+9) <- channels (16kk+2j+1, 16kk+2j+9), odd:
+        // scaled by 4.  Groups >= 64: lane j owns word w = 4(kk/4) + j; k-step kk
+        // takes slot kk%4 of it: k-cols (2j, 2j+1) <- first position p of both
+        // halves (channels 16w + p, 16w + 8 + p), (2j+8, 2j+9) <- second position.
+        int chans[4];
+        float scl[4];
+        if (P.G >= 64) {
+            const int w = 4 * (kk / 4) + j, p0 = slot_pos(kk % 4, 0), p1 = slot_pos(kk % 4, 1);
+            chans[0] = 16 * w + p0; chans[1] = 16 * w + 8 + p0;
+            chans[2] = 16 * w + p1; chans[3] = 16 * w + 8 + p1;
+            scl[0] = scl[1] = (float)(1u << (kQkExp - sub_bit(p0)));
+            scl[2] = scl[3] = (float)(1u << (kQkExp - sub_bit(p1)));
+        } else {
+            chans[0] = 16 * kk + 2 * j; chans[1] = 16 * kk + 2 * j + 8;
+            chans[2] = 16 * kk + 2 * j + 1; chans[3] = 16 * kk + 2 * j + 9;
+            scl[0] = scl[1] = 16.f;
+            scl[2] = scl[3] = 4.f;
+        }
+        uint16_t hv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float x = sqt[hh * D + chans[e]] * scl[e];
+            const __half hi = __float2half_rn(x);
+            const __half v = part ? __float2half_rn(x - __half2float(hi)) : hi;
+            hv[e] = *reinterpret_cast<const uint16_t*>(&v);
+        }
+        qf[i] = make_uint2((uint32_t)hv[0] | ((uint32_t)hv[1] << 16), (uint32_t)hv[2] | ((uint32_t)hv[3] << 16));
+    }
+}
+
+// Runs the prep slice with the smallest head bucket that holds the query group.
+template <int D>
+__device__ __forceinline__ void prep_dispatch(const DecodeParams& P, int hk, int b, float* sm) {
+    if (P.g <= 4) prep_slice<D, 4>(P, hk, b, sm);
+    else if (P.g <= 8) prep_slice<D, 8>(P, hk, b, sm);
+    else prep_slice<D, 16>(P, hk, b, sm);
 }
 
 // True when CTA i of an n-CTA history grid owns at least one of N chunks.
@@ -420,6 +410,10 @@ __global__ void __launch_bounds__(kCombThreads, D >= 256 ? 2 : 6) window_kernel(
     constexpr int kRowW = D / 2 + 1;               // words per staged bf16 row (odd: conflict-free)
     extern __shared__ __align__(16) float s_w[];
     const int hk = blockIdx.x, b = blockIdx.y, wt = blockIdx.z;
+    if (wt == P.n_win_tiles) {                     // the last z-slice: query preparation
+        prep_dispatch<D>(P, hk, b, s_w);
+        return;
+    }
     const int g = P.g, S = P.S, W = P.W;
     float* sq = s_w;                               // [g][D] q · qscale
     float* sp = sq + g * D;                        // [g][kWinTile] logits -> probabilities
@@ -427,8 +421,8 @@ __global__ void __launch_bounds__(kCombThreads, D >= 256 ? 2 : 6) window_kernel(
     uint32_t* sk = reinterpret_cast<uint32_t*>(sml + 2 * g);   // [kWinTile][kRowW] K tile
     uint32_t* sv = sk + kWinTile * kRowW;                      // [kWinTile][kRowW] V tile
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int L = P.len[b];
-    const int rq = P.req[b];
+    int L, rq;                                     // the prep slice of this grid writes the same to len / req
+    if (!request_valid(P, b, &L, &rq)) L = rq = 0;
     const int sink_end = min(S, L);
     const int rec_lo = d_hist_hi(L, S, W);
     const int nplain = L > 0 ? sink_end + max(0, L - rec_lo) : 0;
@@ -630,11 +624,15 @@ __global__ void __launch_bounds__(128) window_mma_kernel(DecodeParams P) {
     float* smx = reinterpret_cast<float*>(spa + 4 * 128);   // [4 warps][8 heads] sub-tile max
     float* ssm = smx + 32;                                   // [4 warps][8 heads] sub-tile sum
     const int hk = blockIdx.x, b = blockIdx.y, wt = blockIdx.z;
+    if (wt == P.n_win_tiles) {                     // the last z-slice: query preparation
+        prep_dispatch<D>(P, hk, b, reinterpret_cast<float*>(s_wm));
+        return;
+    }
     const int g = P.g, S = P.S, W = P.W;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = lane >> 2, j = lane & 3;
-    const int L = P.len[b];
-    const int rq = P.req[b];
+    int L, rq;                                     // the prep slice of this grid writes the same to len / req
+    if (!request_valid(P, b, &L, &rq)) L = rq = 0;
     const int sink_end = min(S, L);
     const int rec_lo = d_hist_hi(L, S, W);
     const int nplain = L > 0 ? sink_end + max(0, L - rec_lo) : 0;
@@ -1133,35 +1131,27 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
 
 template <int D>
 static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
-    const size_t psmem = D * D * 4 <= 64 * 1024 ? (size_t)D * D * 4 : 0;
-    if (psmem) {
-        if (const int rc_ = ensure_dynamic_smem((const void*)prep_kernel<D>, psmem, "cudaFuncSetAttribute(prep_kernel)"))
-            return rc_;
-    }
-    {
-        const int prof_k = prof_begin(3, st);
-        launch_dependent(prep_kernel<D>, dim3(P.batch, (P.Hq + kPrepHeads - 1) / kPrepHeads), dim3(256), psmem, st, P);
-        prof_end(prof_k, st);
-    }
-    int rc = check_cuda("prep_kernel launch");
-    if (rc) return rc;
+    // the window kernel's grid carries one more z-slice: the query preparation
+    // of every (KV head, request)
+    const size_t psmem = (size_t)prep_smem_floats(D, P.g <= 4 ? 4 : P.g <= 8 ? 8 : 16) * 4;
+    int rc = OSCAR_OK;
     if (D <= 128 && P.g <= 8) {
         // tensor-core window: one block of 4 warps per (KV head, request, 64-token tile)
         constexpr int DW = D <= 128 ? D : 128;
-        const size_t wsmem = (size_t)WinMmaCfg<DW>::SMEM_WORDS * 4;
+        const size_t wsmem = std::max((size_t)WinMmaCfg<DW>::SMEM_WORDS * 4, psmem);
         if (const int rc_ = ensure_dynamic_smem((const void*)window_mma_kernel<DW>, wsmem,
                                                 "cudaFuncSetAttribute(window_mma_kernel)"))
             return rc_;
         const int prof_k = prof_begin(4, st);
-        launch_dependent(window_mma_kernel<DW>, dim3(P.Hkv, P.batch, P.n_win_tiles), dim3(128), wsmem, st, P);
+        launch_dependent(window_mma_kernel<DW>, dim3(P.Hkv, P.batch, P.n_win_tiles + 1), dim3(128), wsmem, st, P);
         prof_end(prof_k, st);
     } else {
-        const size_t wsmem = ((size_t)P.g * D + (size_t)P.g * kWinTile + 2 * P.g) * 4 +
-                             (size_t)2 * kWinTile * (D / 2 + 1) * 4;
+        const size_t wsmem = std::max(((size_t)P.g * D + (size_t)P.g * kWinTile + 2 * P.g) * 4 +
+                                          (size_t)2 * kWinTile * (D / 2 + 1) * 4, psmem);
         if (const int rc_ = ensure_dynamic_smem((const void*)window_kernel<D>, wsmem, "cudaFuncSetAttribute(window_kernel)"))
             return rc_;
         const int prof_k = prof_begin(4, st);
-        launch_dependent(window_kernel<D>, dim3(P.Hkv, P.batch, P.n_win_tiles), dim3(kCombThreads), wsmem, st, P);
+        launch_dependent(window_kernel<D>, dim3(P.Hkv, P.batch, P.n_win_tiles + 1), dim3(kCombThreads), wsmem, st, P);
         prof_end(prof_k, st);
     }
     rc = check_cuda("window kernel launch");
@@ -1309,24 +1299,17 @@ namespace oscar {
 constexpr size_t kStaticScratchBytes = size_t(16) << 20;   // 16 MiB per device
 __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
-static void* g_scratch_ptr[64];
-
-// Device address of the scratch array for the current device.  Host code may
+// Device address of the scratch array in the current context.  Host code may
 // not use g_decode_scratch's name as an address (it is a host-side stand-in),
-// so the address is queried once per device with that device current.
+// so the address is asked for on every call, with the caller's device current:
+// the lookup allocates nothing, and a context created after a device reset
+// (which loads the module again, possibly elsewhere) gets its own address.
 static int static_scratch(void** out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64)
-        return fail(OSCAR_ERR_CUDA, "no current CUDA device: %s", cudaGetErrorString(e));
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (e != cudaSuccess || !p)
-            return fail(OSCAR_ERR_CUDA, "cudaGetSymbolAddress(decode scratch): %s", cudaGetErrorString(e));
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess || !p)
+        return fail(OSCAR_ERR_CUDA, "cudaGetSymbolAddress(decode scratch): %s", cudaGetErrorString(e));
+    *out = p;
     return OSCAR_OK;
 }
 

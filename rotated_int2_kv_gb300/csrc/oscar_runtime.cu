@@ -1,6 +1,7 @@
 // Runtime helpers of liboscar.so: the per-device status word written by the
 // kernels' bounds checks, the SM count used to size persistent grids, and the
 // mapping of CUDA runtime errors to OSCAR_ERR_CUDA.
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -15,8 +16,10 @@ namespace oscar {
 __device__ int g_status_word;
 
 static constexpr int kMaxDevices = 64;
-static int* g_status_ptr[kMaxDevices];
-static int g_sm_count[kMaxDevices];
+// SM count per device (a property of the device, not of a context); written
+// with relaxed atomics, so threads making their first call concurrently race
+// only to store the same value.
+static std::atomic<int> g_sm_count[kMaxDevices];
 
 static int current_device() {
     int dev = -1;
@@ -44,22 +47,17 @@ int ensure_dynamic_smem(const void* kernel, size_t bytes, const char* what) {
     return OSCAR_OK;
 }
 
+// Device address of the status word in the current context, asked for on
+// every call: the lookup allocates nothing and stays right after a device
+// reset reloads the module.
 int* status_word() {
-    const int dev = current_device();
-    if (dev < 0) {
-        fail(OSCAR_ERR_CUDA, "no current CUDA device");
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess || !p) {
+        fail(OSCAR_ERR_CUDA, "cudaGetSymbolAddress(status word): %s", cudaGetErrorString(e));
         return nullptr;
     }
-    if (!g_status_ptr[dev]) {
-        void* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
-        if (e != cudaSuccess) {
-            fail(OSCAR_ERR_CUDA, "cudaGetSymbolAddress(status word): %s", cudaGetErrorString(e));
-            return nullptr;
-        }
-        g_status_ptr[dev] = static_cast<int*>(p);
-    }
-    return g_status_ptr[dev];
+    return static_cast<int*>(p);
 }
 
 int sm_count() {
@@ -68,15 +66,15 @@ int sm_count() {
         fail(OSCAR_ERR_CUDA, "no current CUDA device");
         return 0;
     }
-    if (!g_sm_count[dev]) {
-        int n = 0;
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
             fail(OSCAR_ERR_CUDA, "cannot query the SM count");
             return 0;
         }
-        g_sm_count[dev] = n;
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
     }
-    return g_sm_count[dev];
+    return n;
 }
 
 int check_cuda(const char* what) {
@@ -109,6 +107,7 @@ extern "C" int oscar_device_status(int32_t* flags, int32_t clear) {
 // decode history kernel, kind 1: the append quantise kernel).
 // ---------------------------------------------------------------------------
 #include <vector>
+#include <atomic>
 #include <mutex>
 
 namespace oscar {

@@ -75,6 +75,15 @@ _SIGS = {
                                         ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p],
                                        ctypes.c_int),
+    "oscar_covariance_workspace_bytes": ([ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)],
+                                         ctypes.c_int),
+    "oscar_covariance_device": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
+                                 ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
+    "oscar_value_covariance_workspace_bytes": ([ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                               ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+    "oscar_value_covariance_device": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                       ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
     "oscar_device_status": ([ctypes.POINTER(ctypes.c_int32), ctypes.c_int32], ctypes.c_int),
     "oscar_selftest_bounded_wait": ([ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
     "oscar_profile_enable": ([ctypes.c_int32], ctypes.c_int),
@@ -185,6 +194,50 @@ def build_rotation(cov, d, use_bitrev=True):
     return R32, R64, w
 
 
+def _act_dtype(t, name):
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    raise ValueError("%s must be bfloat16 or float32" % name)
+
+
+def covariance_device(x, stream=None):
+    """C = XᵀX / n of the rows of x (n, d) on its CUDA device: (d, d) float64."""
+    if x.dim() != 2:
+        raise ValueError("x must be (n, d)")
+    n, d = x.shape
+    dt = _act_dtype(x, "x")
+    with torch.cuda.device(x.device):
+        nb = ctypes.c_size_t()
+        _check(lib().oscar_covariance_workspace_bytes(n, d, ctypes.byref(nb)))
+        ws = torch.empty(max(nb.value, 256), dtype=torch.uint8, device=x.device)
+        cov = torch.empty((d, d), dtype=torch.float64, device=x.device)
+        _check(lib().oscar_covariance_device(_ptr(x, None, "x"), dt, n, d, cov.data_ptr(), ws.data_ptr(),
+                                             ws.numel(), _stream(stream, x.device)))
+    return cov
+
+
+def value_covariance_device(scores, values, stream=None):
+    """C_S = (S V)ᵀ(S V) / n_q for scores (n_q, n_k) float32 and values (n_k, d): (d, d) float64."""
+    if scores.dim() != 2 or values.dim() != 2 or scores.shape[1] != values.shape[0]:
+        raise ValueError("scores (n_q, n_k) and values (n_k, d) required")
+    if values.device != scores.device:
+        raise ValueError("scores and values must be on one device")
+    n_q, n_k = scores.shape
+    d = values.shape[1]
+    dt = _act_dtype(values, "values")
+    with torch.cuda.device(scores.device):
+        nb = ctypes.c_size_t()
+        _check(lib().oscar_value_covariance_workspace_bytes(n_q, n_k, d, ctypes.byref(nb)))
+        ws = torch.empty(max(nb.value, 256), dtype=torch.uint8, device=scores.device)
+        cov = torch.empty((d, d), dtype=torch.float64, device=scores.device)
+        _check(lib().oscar_value_covariance_device(_ptr(scores, torch.float32, "scores"), _ptr(values, None, "values"),
+                                                   dt, n_q, n_k, d, cov.data_ptr(), ws.data_ptr(), ws.numel(),
+                                                   _stream(stream, scores.device)))
+    return cov
+
+
 # -- device cache -------------------------------------------------------------
 
 class LayerCache:
@@ -219,9 +272,19 @@ def _ptr(t, dtype=None, name="tensor"):
     return t.data_ptr()
 
 
-def _stream(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
+def _stream(stream, device=None):
+    s = torch.cuda.current_stream(device) if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _device_of(cache, *tensors):
+    """The one CUDA device that holds the cache and every given tensor; the
+    library launches on the current device, so the calls below make it current."""
+    dev = cache.records.device
+    for t in tensors:
+        if t is not None and t.device != dev:
+            raise ValueError("all tensors must be on the cache's device %s (got %s)" % (dev, t.device))
+    return dev
 
 
 def quantize_append(cache, k, v, cu_new, start_pos, page_table, req_idx=None, stream=None):
@@ -233,11 +296,13 @@ def quantize_append(cache, k, v, cu_new, start_pos, page_table, req_idx=None, st
     B = start_pos.shape[0]
     if cu_new.shape[0] != B + 1:
         raise ValueError("cu_new must have batch + 1 entries")
-    _check(lib().oscar_quantize_append(
-        ctypes.byref(cfg.c()), ctypes.byref(cache.c()), _ptr(k, cfg.kv_dtype, "k"),
-        _ptr(v, cfg.kv_dtype, "v"), T, _ptr(cu_new, torch.int32, "cu_new"),
-        _ptr(start_pos, torch.int32, "start_pos"), _ptr(req_idx, torch.int32, "req_idx"),
-        _ptr(page_table, torch.int32, "page_table"), page_table.shape[1], B, _stream(stream)))
+    dev = _device_of(cache, k, v, cu_new, start_pos, page_table, req_idx)
+    with torch.cuda.device(dev):
+        _check(lib().oscar_quantize_append(
+            ctypes.byref(cfg.c()), ctypes.byref(cache.c()), _ptr(k, cfg.kv_dtype, "k"),
+            _ptr(v, cfg.kv_dtype, "v"), T, _ptr(cu_new, torch.int32, "cu_new"),
+            _ptr(start_pos, torch.int32, "start_pos"), _ptr(req_idx, torch.int32, "req_idx"),
+            _ptr(page_table, torch.int32, "page_table"), page_table.shape[1], B, _stream(stream, dev)))
 
 
 def decode_workspace_bytes(cfg, batch, max_seq_len):
@@ -259,11 +324,13 @@ def decode_attention(cache, q, page_table, seq_lens, max_seq_len, workspace, req
     if out is None:
         out = torch.empty((B, cfg.num_q_heads, cfg.head_dim), dtype=torch.float32, device=q.device)
     fn = lib().oscar_decode_attention if impl == "auto" else lib().oscar_decode_attention_simt
-    _check(fn(ctypes.byref(cfg.c()), ctypes.byref(cache.c()), _ptr(q, cfg.q_dtype, "q"),
-              _ptr(page_table, torch.int32, "page_table"), page_table.shape[1],
-              _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(req_idx, torch.int32, "req_idx"), B,
-              max_seq_len, _ptr(out, torch.float32, "out"), _ptr(workspace, torch.uint8, "workspace"),
-              workspace.numel(), _stream(stream)))
+    dev = _device_of(cache, q, page_table, seq_lens, req_idx, out, workspace)
+    with torch.cuda.device(dev):
+        _check(fn(ctypes.byref(cfg.c()), ctypes.byref(cache.c()), _ptr(q, cfg.q_dtype, "q"),
+                  _ptr(page_table, torch.int32, "page_table"), page_table.shape[1],
+                  _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(req_idx, torch.int32, "req_idx"), B,
+                  max_seq_len, _ptr(out, torch.float32, "out"), _ptr(workspace, torch.uint8, "workspace"),
+                  workspace.numel(), _stream(stream, dev)))
     return out
 
 
@@ -297,14 +364,17 @@ def profile_read(kind):
 
 
 def decode_attention_noalloc(cache, q, page_table, seq_lens, max_seq_len, req_idx=None, out=None, stream=None):
-    """Decode step with the library's built-in scratch (no workspace, nothing allocated by the library)."""
+    """Decode step with the library's built-in scratch (no workspace, nothing
+    allocated by the library), on the device that holds q and the cache."""
     cfg = cache.cfg
     B = q.shape[0]
     if out is None:
         out = torch.empty((B, cfg.num_q_heads, cfg.head_dim), dtype=torch.float32, device=q.device)
-    _check(lib().oscar_decode_attention_noalloc(
-        ctypes.byref(cfg.c()), ctypes.byref(cache.c()), _ptr(q, cfg.q_dtype, "q"),
-        _ptr(page_table, torch.int32, "page_table"), page_table.shape[1],
-        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(req_idx, torch.int32, "req_idx"), B, max_seq_len,
-        _ptr(out, torch.float32, "out"), _stream(stream)))
+    dev = _device_of(cache, q, page_table, seq_lens, req_idx, out)
+    with torch.cuda.device(dev):
+        _check(lib().oscar_decode_attention_noalloc(
+            ctypes.byref(cfg.c()), ctypes.byref(cache.c()), _ptr(q, cfg.q_dtype, "q"),
+            _ptr(page_table, torch.int32, "page_table"), page_table.shape[1],
+            _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(req_idx, torch.int32, "req_idx"), B, max_seq_len,
+            _ptr(out, torch.float32, "out"), _stream(stream, dev)))
     return out

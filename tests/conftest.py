@@ -24,3 +24,21 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Reports the INT2 boundary cases (rounding ties excused by the parity
+    rule) that the GPU parity tests counted."""
+    try:
+        from parity_util import BOUNDARY_CASES
+    except Exception:
+        return
+    if not BOUNDARY_CASES:
+        return
+    tr = terminalreporter
+    tr.section("INT2 boundary cases (codes within 1e-6 of a rounding boundary; (s, z) at an fp16 tie)")
+    tc = ts = tn = 0
+    for name, c, z, n in BOUNDARY_CASES:
+        tr.write_line("%-40s code ties %4d   (s, z) ties %4d   of %d group records" % (name, c, z, n))
+        tc, ts, tn = tc + c, ts + z, tn + n
+    tr.write_line("%-40s code ties %4d   (s, z) ties %4d   of %d group records" % ("total", tc, ts, tn))

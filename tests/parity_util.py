@@ -6,13 +6,8 @@ and classifying INT2 record mismatches against the acceptance rule
     (s, z) are exact except where the fp32 value rounded to fp16 lies within
     1e-6 relative of an fp16 rounding tie (all codes of such a group excused).
 
-The rotation is an fp32 matrix applied in fp32 ([Escha log] part 2, fix 3
-builds and stores R as float32), while the oracle rotates in fp64.  The GPU's
-y therefore carries fp32 accumulation error, whose size follows the row's
-magnitude (Σ_k |x_k||R_kj|), not that of a group's minimum or of one code's
-distance to a boundary.  When per-element bounds on that error are supplied,
-a mismatch outside the 1e-6 bands but within the bound of a rounding boundary
-is counted separately as an fp32 tie; callers cap that count.
+Both kinds of boundary case are counted; `record_boundary_cases` keeps the
+counts of a test so that the session summary reports them.
 """
 
 import numpy as np
@@ -22,7 +17,6 @@ import oracle
 from oracle import quant as oq
 
 REL_TIE = 1e-6
-F32_U = 2.0 ** -24
 
 
 def fp16_near_tie(x, band=0.0):
@@ -37,22 +31,12 @@ def fp16_near_tie(x, band=0.0):
     return np.abs(x.astype(np.float64) - mid) <= np.maximum(REL_TIE * np.maximum(np.abs(x), 1e-30), band)
 
 
-def fp32_rotation_bound(x, R, n_round):
-    """Per-element bound on |y - x·R| for y = x·R evaluated in fp32 with at most
-    n_round rounded additions along each inner product: the standard a-priori
-    bound γ_n·Σ_k |x_k||R_kj|, γ_n = n·u / (1 - n·u), u = 2^-24.  x: (..., d)."""
-    g = n_round * F32_U / (1.0 - n_round * F32_U)
-    return g * (np.abs(np.asarray(x, np.float64)) @ np.abs(np.asarray(R, np.float64)))
-
-
-def classify_records(gpu_rec, ora_cache, slots, ora_y=None, ora_yb=None):
+def classify_records(gpu_rec, ora_cache, slots, ora_y=None):
     """Compare GPU records with the oracle's for the given slots (all heads).
 
-    Returns dict(exact, code_ties, sz_ties, fp32_ties, bad) counted over
+    Returns dict(exact, code_ties, sz_ties, bad) counted over
     (slot, head, K|V, group).
     `ora_y` (optional): dict slot -> (ky (Hkv, d), vy (Hkv, d)) fp32 rotated rows of the oracle.
-    `ora_yb` (optional): dict slot -> (bk, bv) per-element bounds on the GPU's fp32
-    rotation error (fp32_rotation_bound), same shapes.
     """
     cfg = ora_cache.cfg
     d, G, H = cfg.head_dim, cfg.group_size, cfg.num_kv_heads
@@ -61,7 +45,7 @@ def classify_records(gpu_rec, ora_cache, slots, ora_y=None, ora_yb=None):
     slots = np.asarray(slots, dtype=np.int64)
     want = ora_cache.records()[slots]
     got = np.asarray(gpu_rec)[slots]
-    stats = dict(exact=0, code_ties=0, sz_ties=0, fp32_ties=0, bad=0, bad_examples=[])
+    stats = dict(exact=0, code_ties=0, sz_ties=0, bad=0, bad_examples=[])
     diff = (want != got).any(axis=-1)               # (n, H)
     stats["exact"] = int((~diff).sum()) * 2 * ng
     for i, h in zip(*np.nonzero(diff)):
@@ -76,7 +60,6 @@ def classify_records(gpu_rec, ora_cache, slots, ora_y=None, ora_yb=None):
                 y = ora_y[s][mat][h]
             elif s in (ora_cache.ky if mat == 0 else ora_cache.vy):
                 y = (ora_cache.ky if mat == 0 else ora_cache.vy)[s][h]
-            yb = ora_yb[s][mat][h] if (ora_yb is not None and s in ora_yb) else None
             for gi in range(ng):
                 sl = slice(gi * G, (gi + 1) * G)
                 same_sz = gs[gi] == ws[gi] and gz[gi] == wz[gi]
@@ -94,16 +77,6 @@ def classify_records(gpu_rec, ora_cache, slots, ora_y=None, ora_yb=None):
                     if fp16_near_tie(s32) or fp16_near_tie(lo):
                         stats["sz_ties"] += 1
                         continue
-                    if yb is not None:
-                        # r·min and r·max move by at most r·max|Δy| (plus one
-                        # rounding of the product), s by their sum / 3 (plus the
-                        # roundings of the difference and the division)
-                        e = float(r) * float(yb[sl].max())
-                        dlo = e + F32_U * abs(float(lo))
-                        ds = 2.0 * e / 3.0 + 2.0 * F32_U * abs(float(s32))
-                        if fp16_near_tie(s32, ds) or fp16_near_tie(lo, dlo):
-                            stats["fp32_ties"] += 1
-                            continue
                     stats["bad"] += 1
                     stats["bad_examples"].append(("sz", s, int(h), mat, gi))
                     continue
@@ -111,22 +84,14 @@ def classify_records(gpu_rec, ora_cache, slots, ora_y=None, ora_yb=None):
                 zf = np.float32(wz[gi])
                 u = (np.float32(yg - zf) / sf).astype(np.float32)
                 bad_here = False
-                fp32_here = False
                 for j in np.nonzero(gc[sl] != wc[sl])[0]:
                     uj = float(u[j])
                     near = min(abs(uj - (k + 0.5)) for k in range(3))
-                    if near <= REL_TIE * max(1.0, abs(uj)):
-                        continue
-                    # with the same (s, z), u moves by |Δy| / s
-                    if yb is not None and near <= float(yb[sl][j]) / float(sf):
-                        fp32_here = True
-                    else:
+                    if near > REL_TIE * max(1.0, abs(uj)):
                         bad_here = True
                 if bad_here:
                     stats["bad"] += 1
                     stats["bad_examples"].append(("code", s, int(h), mat, gi))
-                elif fp32_here:
-                    stats["fp32_ties"] += 1
                 else:
                     stats["code_ties"] += 1
     return stats
@@ -154,3 +119,12 @@ def attn_errors(got, want):
 
 ATOL = 2e-3      # max-abs bound on attention outputs
 RTOL_L2 = 1e-3   # relative-L2 bound on attention outputs
+
+
+# Boundary-case counts of the tests in this session: (test, code ties, (s, z) ties, records compared).
+BOUNDARY_CASES = []
+
+
+def record_boundary_cases(name, stats, n_records):
+    """Keeps the tie counts of one comparison for the session summary."""
+    BOUNDARY_CASES.append((name, int(stats.get("code_ties", 0)), int(stats.get("sz_ties", 0)), int(n_records)))

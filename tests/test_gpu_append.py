@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from rotated_int2_kv_gb300 import synth
-from parity_util import classify_records
+from parity_util import classify_records, record_boundary_cases
 
 pytestmark = pytest.mark.gpu
 
@@ -33,14 +33,14 @@ def _misaligned(t):
 
 
 def run_append_scenario(d, Hq, Hkv, G, S, W, kv_dtype, calls, clip=0.9, mode="fixed4", pool_extra=37,
-                        seed=SEED, unaligned=False):
+                        seed=SEED, unaligned=False, rotations=None, keep=None):
     from rotated_int2_kv_gb300 import ops
     B = len(calls[0])
     Lfin = [sum(c[b] for c in calls) for b in range(B)]
     maxL = max(max(Lfin), 1)
     pool = B * maxL + pool_extra
     cfg = ops.Config(d, Hq, Hkv, G, S, W, clip, kv_dtype=kv_dtype)
-    Rk, Rv = _rotations(d, seed)
+    Rk, Rv = _rotations(d, seed) if rotations is None else rotations
     pt = synth.page_table(seed, B, maxL, pool, shuffled=True)
     req = torch.tensor(list(reversed(range(B))), dtype=torch.int32)   # window rows permuted
     max_reqs = B + 2
@@ -75,6 +75,7 @@ def run_append_scenario(d, Hq, Hkv, G, S, W, kv_dtype, calls, clip=0.9, mode="fi
     hist_slots = np.array(sorted(hist_slots), dtype=np.int64)
     stats = classify_records(gpu_rec, oc, hist_slots)
     assert stats["bad"] == 0, stats
+    record_boundary_cases("append d%d G%d Hkv%d" % (d, G, Hkv), stats, len(hist_slots) * Hkv * 2 * (d // G))
     others = np.setdiff1d(np.arange(pool), hist_slots)
     assert not gpu_rec[others].any(), "records outside the history were written"
     # windows: bit-exact bf16
@@ -88,6 +89,8 @@ def run_append_scenario(d, Hq, Hkv, G, S, W, kv_dtype, calls, clip=0.9, mode="fi
             assert np.array_equal(gs[rq, :se], sink_bits[rq, :se])
         idx = np.arange(rlo, rhi) % W
         assert np.array_equal(gr[rq, idx], ring_bits[rq, idx])
+    if keep is not None:
+        keep.update(cfg=cfg, dc=dc, oc=oc, pt=pt, req=req, lens=Lfin)
     return stats
 
 
@@ -184,3 +187,32 @@ def test_device_checks_flag_bad_slots_without_faulting():
     torch.cuda.synchronize()
     assert ops.device_status(clear=True) & ops.DEV_BAD_SLOT
     assert ops.device_status(clear=True) == 0
+
+
+def test_library_built_rotation_end_to_end():
+    # R_K, R_V from the library's own builder (oscar_build_rotation), not the
+    # oracle's: append parity, then decode against the oracle on the same R
+    from rotated_int2_kv_gb300 import ops
+    from parity_util import ATOL, RTOL_L2, attn_errors, device_cache_from_oracle
+    d = 128
+    Rk, _, _ = ops.build_rotation(ops.covariance(synth.calib_samples(SEED, 0, d)), d)
+    Rv, _, _ = ops.build_rotation(ops.covariance(synth.calib_samples(SEED, 1, d)), d)
+    keep = {}
+    calls = [[1500, 700], [1, 1], [1, 1], [1, 1]]
+    run_append_scenario(d, 32, 8, 64, 64, 256, torch.bfloat16, calls, rotations=(Rk, Rv), keep=keep)
+    cfg, dc, oc, pt, req, lens = keep["cfg"], keep["dc"], keep["oc"], keep["pt"], keep["req"], keep["lens"]
+    dev = torch.device("cuda")
+    B = len(lens)
+    q = synth.queries(SEED, 9, B, cfg.num_q_heads, d)
+    want = oracle.decode_attention(oc, q.float().numpy(), pt.numpy(), lens, req.numpy())
+    ws = ops.alloc_workspace(cfg, B, pt.shape[1])
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=dev)
+    same = device_cache_from_oracle(ops, oc, cfg)
+    out = ops.decode_attention(same, q.to(dev), pt.to(dev), lens_d, pt.shape[1], ws, req_idx=req.to(dev))
+    err, rel = attn_errors(out.cpu().numpy(), want)
+    assert err <= ATOL and rel <= RTOL_L2, ("identical cache", err, rel)
+    out = ops.decode_attention(dc, q.to(dev), pt.to(dev), lens_d, pt.shape[1], ws, req_idx=req.to(dev))
+    err, rel = attn_errors(out.cpu().numpy(), want)
+    assert rel <= RTOL_L2, ("gpu-built cache", err, rel)
+    torch.cuda.synchronize()
+    assert ops.device_status() == 0

@@ -19,7 +19,7 @@ import torch
 
 import oracle
 from rotated_int2_kv_gb300 import synth
-from parity_util import ATOL, RTOL_L2, attn_errors, classify_records
+from parity_util import ATOL, RTOL_L2, attn_errors, classify_records, record_boundary_cases
 
 pytestmark = pytest.mark.gpu
 
@@ -115,6 +115,7 @@ def test_full_size_batch32_100k_sampled_requests():
         ora_y = _rotated_rows(b0, diff_pos, Rk, Rv, scales) if len(diff_pos) else {}
         st = classify_records(got, oc, diff_pos, ora_y=ora_y) if len(diff_pos) else dict(bad=0)
         assert st["bad"] == 0, (b0, {k: v for k, v in st.items() if k != "bad_examples"}, st["bad_examples"][:5])
+        record_boundary_cases("qwen8b-100k request %d" % b0, st, len(hist) * HKV * 2 * (D // G))
         # ---- decode parity on the oracle's cache contents for request b0 ----
         dc.records[idx] = torch.from_numpy(want[hist]).to(dev)
         sink_bits, ring_bits = oc.window_bits()

@@ -2,26 +2,7 @@
 
 import numpy as np
 
-from parity_util import REL_TIE, fp16_near_tie, fp32_rotation_bound
-
-
-def test_fp32_rotation_bound_holds_for_an_fp32_product():
-    rng = np.random.default_rng(7)
-    for d in (64, 128, 256):
-        x = rng.standard_normal((64, d)) * np.where(rng.random(d) < 0.03, 20.0, 1.0)
-        R, _ = np.linalg.qr(rng.standard_normal((d, d)))
-        x32, R32 = x.astype(np.float32), R.astype(np.float32)
-        exact = x32.astype(np.float64) @ R32.astype(np.float64)
-        # a sequential fp32 inner product rounds once per addition: d - 1 roundings
-        y = np.zeros((64, d), np.float32)
-        for k in range(d):
-            y = (y + x32[:, k:k + 1] * R32[k:k + 1, :]).astype(np.float32)
-        err = np.abs(y.astype(np.float64) - exact)
-        # each product also rounds once: d products + d - 1 additions
-        bound = fp32_rotation_bound(x32, R32, 2 * d)
-        assert (err <= bound).all()
-        # and the bound is not vacuous: the typical error is far below it
-        assert np.median(err / bound) < 0.05
+from parity_util import REL_TIE, classify_records, fp16_near_tie
 
 
 def test_fp16_near_tie_bands():
@@ -33,3 +14,52 @@ def test_fp16_near_tie_bands():
     assert fp16_near_tie(off, band=5 * REL_TIE)     # inside an absolute band that covers it
     far = np.float32(1.0 + 2.0 ** -12)              # a quarter step from either neighbour
     assert not fp16_near_tie(far, band=1e-5)
+
+
+def _tie_cache():
+    """An oracle cache with one history token whose K group 0 holds a value at a
+    rounding boundary: R = I, clip 1, group min 0 and max 3 give s = 1 and
+    z = 0, so channel 1 (y = 0.5) sits exactly on the boundary between codes 0
+    and 1 and channel 2 (y = 1.203125) is far from any boundary."""
+    import oracle
+    d, G = 64, 64
+    cfg = oracle.OracleConfig(d, 1, 1, G, sink=0, recent=1, clip_ratio=1.0)
+    eye = np.eye(d)
+    oc = oracle.OracleCache(cfg, 4, 1, eye, eye)
+    rng = np.random.default_rng(3)
+    x = oracle.bf16_round(rng.uniform(0.25, 2.75, (2, 1, d)).astype(np.float32))
+    x[0, 0, 0], x[0, 0, 1], x[0, 0, 2], x[0, 0, 3] = 0.0, 0.5, 1.203125, 3.0
+    pt = np.arange(4, dtype=np.int32)[None, :]
+    oc.append(x, x, [0, 2], [0], [0], pt, keep_y=True)     # token 0 enters the history
+    return oc, d, G
+
+
+def test_classify_records_excuses_only_boundary_cases():
+    # planted on the host, in a copy of the oracle's own records
+    from oracle import quant as oq
+    oc, d, G = _tie_cache()
+    want = oc.records()
+    kc, ks, kz, vc, vs, vz = oq.unpack_record(want[0, 0], d, G)
+    assert float(ks[0]) == 1.0 and float(kz[0]) == 0.0 and kc[1] == 0 and kc[2] == 1
+    assert classify_records(want, oc, [0])["bad"] == 0
+    # the code of the tied channel flipped to the other side: a counted tie
+    tied = want.copy()
+    kc2 = kc.copy()
+    kc2[1] = 1
+    tied[0, 0] = oq.pack_record(kc2, ks, kz, vc, vs, vz, d, G)
+    st = classify_records(tied, oc, [0])
+    assert st["bad"] == 0 and st["code_ties"] == 1
+    # a code 0.2 away from a boundary flipped: not excused
+    wrong = want.copy()
+    kc3 = kc.copy()
+    kc3[2] = 2
+    wrong[0, 0] = oq.pack_record(kc3, ks, kz, vc, vs, vz, d, G)
+    st = classify_records(wrong, oc, [0])
+    assert st["bad"] == 1 and st["code_ties"] == 0
+    # a scale one fp16 step off, with no tie behind it: not excused
+    off = want.copy()
+    ks4 = ks.copy()
+    ks4[0] = np.nextafter(ks4[0], np.float16(2))
+    off[0, 0] = oq.pack_record(kc, ks4, kz, vc, vs, vz, d, G)
+    st = classify_records(off, oc, [0])
+    assert st["bad"] == 1 and st["sz_ties"] == 0

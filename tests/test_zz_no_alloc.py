@@ -56,6 +56,12 @@ def test_noalloc_matches_workspace_entry_point_twice():
         torch.cuda.synchronize()
         err, rel = attn_errors(out.cpu().numpy(), ref.cpu().numpy())
         assert err <= ATOL and rel <= RTOL_L2, (step, err, rel)
+        # the Python binding of the same entry point, into a caller-given output
+        out2 = torch.full_like(ref, float("nan"))
+        ops.decode_attention_noalloc(cache, q, pt, lens, L, out=out2)
+        torch.cuda.synchronize()
+        err, rel = attn_errors(out2.cpu().numpy(), ref.cpu().numpy())
+        assert err <= ATOL and rel <= RTOL_L2, ("binding", step, err, rel)
     assert ops.device_status() == 0
 
 
