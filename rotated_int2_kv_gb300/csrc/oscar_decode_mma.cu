@@ -210,8 +210,10 @@ struct MmaCfg {
 constexpr int kSmemMask = 128, kSmemAbort = 256, kSmemTab = 384;
 
 // HKV > 0 fixes the KV head count (and so the stage row stride) at compile time.
-template <int D, int G, int NT, int WPH, int TTOK, int PAR, int HKV>
-__global__ void __launch_bounds__(256 * PAR, 1)
+// HP splits a KV head's query group over HP warps (query heads 4·NT·hp ..),
+// each carrying NT n8 column tiles.
+template <int D, int G, int NT, int WPH, int TTOK, int PAR, int HKV, int HP>
+__global__ void __launch_bounds__(256 * PAR * HP, 1)
 history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_log2) {
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     using namespace mma_detail;
@@ -224,8 +226,10 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     const int nwarps = blockDim.x >> 5;
     const int pi = warp % PAR;                  // parity of the stages this warp consumes
     const int hw = warp / PAR;
-    const int h = hw / WPH;                     // KV head
     const int wsl = hw % WPH;                   // channel slice
+    const int hp = (hw / WPH) % HP;             // query-head part: head tiles hp·NT .. hp·NT + NT - 1
+    const int h = hw / (WPH * HP);              // KV head
+    const int hpx = h * HP + hp;                // (KV head, part)
     const int r = lane >> 2, j = lane & 3;
     const int g = P.g;
     const uint32_t NS = 1u << ns_log2;
@@ -236,10 +240,10 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     uint64_t* vmw = reinterpret_cast<uint64_t*>(smem + kSmemMask);      // [8 slots][2] validity masks
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemAbort);
     uint32_t* wtab = reinterpret_cast<uint32_t*>(smem + kSmemTab + warp * C::TBL);
-    float* xb = reinterpret_cast<float*>(smem + x_off) + (h * PAR + pi) * C::XCH;
+    float* xb = reinterpret_cast<float*>(smem + x_off) + (hpx * PAR + pi) * C::XCH;
     unsigned char* stages = smem + stages_off;
     const uint32_t stage_bytes = (uint32_t)TT * (uint32_t)row;
-    const int bar_id = 1 + h * PAR + pi;
+    const int bar_id = 1 + hpx * PAR + pi;
 
     const int64_t N = P.cprefix[P.batch];
     const int f0 = (int)((int64_t)blockIdx.x * N / gridDim.x);
@@ -373,15 +377,15 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
-                    const uint2 v = qf[((int64_t)nt * (D / 16) + wsl * KS + kk) * 32 + lane];
+                    const uint2 v = qf[((int64_t)(hp * NT + nt) * (D / 16) + wsl * KS + kk) * 32 + lane];
                     bq[nt][kk][0] = v.x;
                     bq[nt][kk][1] = v.y;
                 }
         }
-        float2 qs[NT][GW];          // (Σ q̃, Σ q̃/α) per group, head 4nt + j
+        float2 qs[NT][GW];          // (Σ q̃, Σ q̃/α) per group, head 4(hp·NT + nt) + j
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const int hh = 4 * nt + j;
+            const int hh = 4 * (hp * NT + nt) + j;
 #pragma unroll
             for (int gi = 0; gi < GW; ++gi)
                 qs[nt][gi] = hh < g ? P.qsum[((int64_t)b * P.Hq + h * g + hh) * P.ng + wsl * GW + gi]
@@ -551,7 +555,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const uint64_t need = TT == 64 ? ~0ull : 0xffffffffull;
-                const uint64_t vm = (4 * nt + j) < g ? vmask : 0ull;
+                const uint64_t vm = (4 * (hp * NT + nt) + j) < g ? vmask : 0ull;
 #pragma unroll
                 for (int i = 0; i < NR; ++i) x[nt][i] = lg[nt][i];
                 if (vm != need) {
@@ -736,7 +740,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         const int64_t slot = ((int64_t)blockIdx.x + b) * PAR + pi;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const int hh = 4 * nt + j;
+            const int hh = 4 * (hp * NT + nt) + j;
             const int hq = h * g + hh;
             float* o = P.po + (slot * P.Hq + hq) * D;
             if (r == 0 && wsl == 0 && hh < g) P.ml[slot * P.Hq + hq] = make_float2(m_run[nt], l_run[nt]);
@@ -777,12 +781,14 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
 
 // Shared-memory plan: (x_off, stages_off, ring depth log2, total bytes); false if it
 // does not fit.  Two stage parities need at least 4 stages (2 in flight).
-template <int D, int G, int NT, int WPH, int TTOK, int PAR>
+template <int D, int G, int NT, int WPH, int TTOK, int PAR, int HP>
 static bool mma_smem_plan(int Hkv, int* x_off, int* stages_off, int* ns_log2, size_t* total) {
     using C = MmaCfg<D, G, NT, WPH, TTOK>;
-    const int nwarps = Hkv * WPH * PAR;
+    const int nwarps = Hkv * WPH * PAR * HP;
+    // named barriers 1 .. Hkv·HP·PAR pair the channel-slice warps (ids up to 15)
+    if (WPH == 2 && Hkv * HP * PAR > 15) return false;
     *x_off = kSmemTab + nwarps * C::TBL;
-    *stages_off = (*x_off + Hkv * PAR * C::XCH * 4 + 127) / 128 * 128;
+    *stages_off = (*x_off + Hkv * HP * PAR * C::XCH * 4 + 127) / 128 * 128;
     const size_t stage = (size_t)TTOK * row_bytes(Hkv * C::REC);
     int lg = 3;                                  // 8 stages when they fit, else 4, else 2
     while (lg > PAR && *stages_off + (stage << lg) > 224 * 1024) --lg;
@@ -791,14 +797,14 @@ static bool mma_smem_plan(int Hkv, int* x_off, int* stages_off, int* ns_log2, si
     return *total <= 225 * 1024;
 }
 
-template <int D, int G, int NT, int WPH, int TTOK, int PAR, int HKV>
+template <int D, int G, int NT, int WPH, int TTOK, int PAR, int HKV, int HP>
 static int launch_mma(DecodeParams P, cudaStream_t st) {
-    const int threads = 32 * P.Hkv * WPH * PAR;
+    const int threads = 32 * P.Hkv * WPH * PAR * HP;
     int x_off, stages_off, ns_log2;
     size_t smem;
-    if (!mma_smem_plan<D, G, NT, WPH, TTOK, PAR>(P.Hkv, &x_off, &stages_off, &ns_log2, &smem))
+    if (!mma_smem_plan<D, G, NT, WPH, TTOK, PAR, HP>(P.Hkv, &x_off, &stages_off, &ns_log2, &smem))
         return OSCAR_ERR_ARG;
-    auto kern = history_mma_kernel<D, G, NT, WPH, TTOK, PAR, HKV>;
+    auto kern = history_mma_kernel<D, G, NT, WPH, TTOK, PAR, HKV, HP>;
     if (const int rc_ = ensure_dynamic_smem((const void*)kern, smem, "cudaFuncSetAttribute(history_mma_kernel)"))
         return rc_;
     const int grid = std::min(P.n_ctas, sm_count());
@@ -816,8 +822,9 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
     const int nt = (2 * P.g + 7) / 8;
     int rc = OSCAR_OK;
     // a variant is taken when its shared-memory plan fits; otherwise the next one is tried
-    auto go = [&](auto plan, auto fn, int par, int hkv) {
+    auto go = [&](auto plan, auto fn, int par, int hkv, int warps_per_head) {
         if (*launched || (hkv > 0 && hkv != P.Hkv)) return;
+        if (P.Hkv * warps_per_head > 32) return;     // at most 1,024 threads
         int xo, so, lg;
         size_t smem;
         if (!plan(P.Hkv, &xo, &so, &lg, &smem)) return;
@@ -825,19 +832,24 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
         rc = fn(P, st);
         *launched = true;
     };
-#define OSCAR_MMA_H(D_, G_, NT_, WPH_, TT_, PAR_, HKV_) \
-    go(mma_smem_plan<D_, G_, NT_, WPH_, TT_, PAR_>, launch_mma<D_, G_, NT_, WPH_, TT_, PAR_, HKV_>, PAR_, HKV_)
+#define OSCAR_MMA_X(D_, G_, NT_, WPH_, TT_, PAR_, HKV_, HP_) \
+    go(mma_smem_plan<D_, G_, NT_, WPH_, TT_, PAR_, HP_>, launch_mma<D_, G_, NT_, WPH_, TT_, PAR_, HKV_, HP_>, PAR_, HKV_, \
+       WPH_ * PAR_ * HP_)
+#define OSCAR_MMA_H(D_, G_, NT_, WPH_, TT_, PAR_, HKV_) OSCAR_MMA_X(D_, G_, NT_, WPH_, TT_, PAR_, HKV_, 1)
 #define OSCAR_MMA(D_, G_, NT_, WPH_, TT_, PAR_) OSCAR_MMA_H(D_, G_, NT_, WPH_, TT_, PAR_, 0)
+#define OSCAR_MMA_HP(D_, G_, WPH_, HKV_) OSCAR_MMA_X(D_, G_, 1, WPH_, 64, 1, HKV_, 2)
     // one n8 column tile (g <= 4): two warps per (head, slice) on alternate stages;
-    // two tiles: one warp, 32-token stages (register budget)
+    // two tiles (g = 5..8): two warps per (head, slice), each with four of the
+    // query heads, on every stage; failing that, one warp with both tiles and
+    // 32-token stages (register budget)
     if (head_dim == 128) {
         if (P.G == 64) {
             // 8 KV heads (Qwen3-8B-like layers): compile-time stage row stride
             if (nt == 1) { OSCAR_MMA_H(128, 64, 1, 1, 64, 2, 8); OSCAR_MMA(128, 64, 1, 1, 64, 2); OSCAR_MMA(128, 64, 1, 1, 64, 1); }
-            else OSCAR_MMA(128, 64, 2, 1, 32, 1);
+            else { OSCAR_MMA_HP(128, 64, 1, 8); OSCAR_MMA_HP(128, 64, 1, 0); OSCAR_MMA(128, 64, 2, 1, 32, 1); }
         } else if (P.G == 128) {
             if (nt == 1) { OSCAR_MMA(128, 128, 1, 1, 64, 2); OSCAR_MMA(128, 128, 1, 1, 64, 1); }
-            else OSCAR_MMA(128, 128, 2, 1, 32, 1);
+            else { OSCAR_MMA_HP(128, 128, 1, 0); OSCAR_MMA(128, 128, 2, 1, 32, 1); }
         } else if (P.G == 32) {
             if (nt == 1) OSCAR_MMA(128, 32, 1, 1, 64, 1);   // two sets would spill registers
             else OSCAR_MMA(128, 32, 2, 1, 32, 1);
@@ -845,14 +857,16 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
     } else if (head_dim == 256) {
         if (P.G == 128) {
             if (nt == 1) { OSCAR_MMA(256, 128, 1, 2, 64, 2); OSCAR_MMA(256, 128, 1, 2, 64, 1); }
-            else OSCAR_MMA(256, 128, 2, 2, 32, 1);
+            else { OSCAR_MMA_HP(256, 128, 2, 0); OSCAR_MMA(256, 128, 2, 2, 32, 1); }
         } else if (P.G == 64) {
             if (nt == 1) { OSCAR_MMA(256, 64, 1, 2, 64, 2); OSCAR_MMA(256, 64, 1, 2, 64, 1); }
-            else OSCAR_MMA(256, 64, 2, 2, 32, 1);
+            else { OSCAR_MMA_HP(256, 64, 2, 0); OSCAR_MMA(256, 64, 2, 2, 32, 1); }
         }
     }
 #undef OSCAR_MMA
 #undef OSCAR_MMA_H
+#undef OSCAR_MMA_HP
+#undef OSCAR_MMA_X
     if (*launched) P.n_ctas = std::min(P.n_ctas, sm_count());
     return rc;
 }
