@@ -578,7 +578,6 @@ __device__ __forceinline__ int history_slot(const AppendParams& P, int b, int q,
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads)
 append_step_kernel(AppendParams P) {
-    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     static_assert(D * D * 4 <= 64 * 1024, "R staged in shared memory");
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ float sx[kSmallVec][D];
@@ -588,11 +587,14 @@ append_step_kernel(AppendParams P) {
     const float* R = mat ? P.rot_v : P.rot_k;
     const void* src_new = mat ? P.v : P.k;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // R is no kernel's output, so its staging may start while the previous grid
+    // of the stream drains; everything else waits for that grid
     constexpr int NU = D * D / 4 / kAppendThreads;   // 16-byte copies of R per thread
 #pragma unroll
     for (int u = 0; u < NU; ++u)
         cp_async16(sR + 4 * (tid + kAppendThreads * u), R + 4 * (tid + kAppendThreads * u));
     cp_async_commit();
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     cp_async_wait<0>();
     __syncthreads();
     const int64_t total = P.total_new * P.Hkv;

@@ -174,22 +174,121 @@ __device__ __forceinline__ void pack_codes32(const float2 (&c)[16], uint32_t& w0
     w1 = __byte_perm(u[2], u[3], 0x5410);
 }
 
-// fl(x·R[:, ch]) (compensated, faithful) for the vector of lane L, computed by
-// the whole warp; kind / off locate the vector's bf16 row (1: the recent ring,
-// 2: the new input, converted to bf16 as it is read; anything else: zeros).
+// Where a vector's bf16 row lives: kind 1 the recent ring, kind 2 the new
+// input (converted to bf16 as it is read); anything else reads as zeros.
+struct ExactSrc {
+    const uint16_t* recent;
+    const void* src_new;
+    int kv_dtype;
+    int kind;
+    int64_t off;
+};
+
+// fl(x·R[:, ch]) (compensated, faithful to the exact product) for the vector of
+// lane L, by the whole warp: lane l takes k = l·D/32 .. + D/32 - 1, x from the
+// vector's row in global memory, R exactly as hi + mid + lo from the bf16 parts
+// in shared memory (B operand layout), then a compensated sum over the warp.
 template <int D>
-__device__ __noinline__ float tc_exact_y(const uint16_t* recent, const void* src_new, int kv_dtype, const float* R,
-                                         int kind, int64_t off, int L, int ch, int lane) {
-    const int kd = __shfl_sync(0xffffffffu, kind, L);
-    const uint32_t olo = __shfl_sync(0xffffffffu, (uint32_t)(uint64_t)off, L);
-    const uint32_t ohi = __shfl_sync(0xffffffffu, (uint32_t)((uint64_t)off >> 32), L);
-    const int64_t o = (int64_t)(((uint64_t)ohi << 32) | olo);
-    auto xk = [&](int k) -> float {
-        if (kd == 1) return bf16_bits_to_f32(recent[o + k]);
-        if (kd == 2) return bf16_bits_to_f32(f32_to_bf16_bits(load_elem(src_new, o + k, kv_dtype)));
-        return 0.0f;
-    };
-    return dot2_warp<D>(xk, R, D, ch, lane);
+__device__ __forceinline__ float tc_dot2(const unsigned char* sB, const ExactSrc& src, int L, int ch, int lane) {
+    constexpr int KPL = D / 32;                       // k per lane: 4 (d 128) or 2 (d 64)
+    constexpr int B_PART = D * D * 2;
+    const int kd = __shfl_sync(0xffffffffu, src.kind, L);
+    const uint32_t olo = __shfl_sync(0xffffffffu, (uint32_t)(uint64_t)src.off, L);
+    const uint32_t ohi = __shfl_sync(0xffffffffu, (uint32_t)((uint64_t)src.off >> 32), L);
+    const int64_t o = (int64_t)(((uint64_t)ohi << 32) | olo) + lane * KPL;
+    float x[KPL];
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+        x[i] = kd == 1 ? bf16_bits_to_f32(src.recent[o + i])
+             : kd == 2 ? bf16_bits_to_f32(f32_to_bf16_bits(load_elem(src.src_new, o + i, src.kv_dtype)))
+                       : 0.0f;
+    }
+    const int k0 = lane * KPL;
+    const uint32_t boff = tc5::sw128_offset(D, ch, k0 / 8) + (uint32_t)(k0 % 8) * 2;
+    float s = 0.0f, c = 0.0f;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+        float r = 0.0f;
+#pragma unroll
+        for (int p = 0; p < 3; ++p)                   // hi + mid + lo: exact in fp32
+            r += bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(sB + p * B_PART + boff + 2 * i));
+        const float pr = __fmul_rn(x[i], r);
+        const float pe = __fmaf_rn(x[i], r, -pr);
+        const float t = __fadd_rn(s, pr);
+        const float bp = __fsub_rn(t, s);
+        const float er = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(pr, bp));
+        s = t;
+        c = __fadd_rn(c, __fadd_rn(er, pe));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float so = __shfl_xor_sync(0xffffffffu, s, off);
+        const float co = __shfl_xor_sync(0xffffffffu, c, off);
+        const float t = __fadd_rn(s, so);
+        const float bp = __fsub_rn(t, s);
+        const float er = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(so, bp));
+        s = t;
+        c = __fadd_rn(__fadd_rn(c, co), er);
+    }
+    return __fadd_rn(s, c);
+}
+
+// Exact extremes of one group for the lanes whose (s, z) y ± e could change
+// (warp-collective; out of line, so the common path stays compact): the
+// extremes lie among the channels within 2e of the computed ones, which are
+// formed exactly.  Returns (min, max); meaningful for uncertain lanes.
+template <int D, int G>
+__device__ __noinline__ float2 tc_exact_extremes(uint32_t tgrp, const unsigned char* sB, ExactSrc src, bool unc,
+                                                 float mn, float mx, float e2, int ch0, int lane) {
+    const float tlo = __fadd_ru(mn, e2), thi = __fsub_rd(mx, e2);
+    float mne = INFINITY, mxe = -INFINITY;
+#pragma unroll 1
+    for (int c = 0; c < G / 32; ++c) {
+        float y[32];
+        load_y(tgrp + 32 * c, y);
+        uint32_t cm = 0;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) cm |= (unc && (y[q] <= tlo || y[q] >= thi)) ? (1u << q) : 0u;
+        uint32_t bal;
+        while ((bal = __ballot_sync(0xffffffffu, cm != 0u)) != 0u) {
+            const int L = __ffs(bal) - 1;
+            const int q = __shfl_sync(0xffffffffu, __ffs(cm) - 1, L);
+            const float ye = tc_dot2<D>(sB, src, L, ch0 + 32 * c + q, lane);
+            if (lane == L) {
+                cm &= cm - 1u;
+                mne = fminf(mne, ye);
+                mxe = fmaxf(mxe, ye);
+            }
+        }
+    }
+    return make_float2(mne, mxe);
+}
+
+// Codes of one 32-channel chunk by correctly rounded division, on the exact y
+// where y ± e straddles a boundary (warp-collective; out of line).
+template <int D>
+__device__ __noinline__ uint2 tc_exact_codes(uint32_t tchunk, const unsigned char* sB, ExactSrc src, float zc,
+                                             float sc, float be, int ch0, int lane) {
+    float y[32];
+    load_y(tchunk, y);
+    float2 cc[16];
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+        float u = sc != 0.0f ? __fdiv_rn(__fsub_rn(y[q], zc), sc) : 0.0f;
+        uint32_t mm = __ballot_sync(0xffffffffu, sc != 0.0f && code_near_boundary(u, be));
+        while (mm) {
+            const int L = __ffs(mm) - 1;
+            mm &= mm - 1u;
+            const float ye = tc_dot2<D>(sB, src, L, ch0 + q, lane);
+            if (lane == L) u = __fdiv_rn(__fsub_rn(ye, zc), sc);
+        }
+        const float cv = sc != 0.0f ? fminf(fmaxf(rintf(u), 0.0f), 3.0f) : 0.0f;
+        if (q & 1) cc[q >> 1].y = cv;
+        else cc[q >> 1].x = cv;
+    }
+    uint2 w;
+    pack_codes32(cc, w.x, w.y);
+    return w;
 }
 
 template <int D>
@@ -487,8 +586,7 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
         // ---- quantise vector gt of the tile ----
         const int* m = gmeta + (buf * kTcRows + gt) * kMetaInts;
         const int slot = m[0];
-        const int mkind = m[1] >> 16;
-        const int64_t moff = *reinterpret_cast<const int64_t*>(m + 2);
+        const ExactSrc xsrc{P.recent, src_new, P.kv_dtype, m[1] >> 16, *reinterpret_cast<const int64_t*>(m + 2)};
         uint8_t* rec = P.records + ((int64_t)(slot < 0 ? 0 : slot) * P.Hkv + (m[1] & 0xFFFF)) * P.rec_bytes;
         uint32_t words[NW];
         constexpr int NC = G / 32;                // 32-channel chunks per group
@@ -520,35 +618,13 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
                 load_y(tacc + gi * G + 32 * c, y);
                 minmax32(y, mn, mx);
             }
-            // (s, z) that y ± e could change: the group's extremes lie among the
-            // channels within 2e of the computed ones; form those exactly
+            // (s, z) that y ± e could change: the extremes formed exactly (out of line)
             const bool unc = sz_uncertain(mn, mx, rclip, e);
             if (__any_sync(0xffffffffu, unc)) {
-                const float tlo = __fadd_ru(mn, e2), thi = __fsub_rd(mx, e2);
-                float mne = INFINITY, mxe = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    if (!kKeep) load_y(tacc + gi * G + 32 * c, yk[0]);
-                    const float (&y)[32] = yk[kKeep ? c : 0];
-                    uint32_t cm = 0;
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) cm |= (unc && (y[q] <= tlo || y[q] >= thi)) ? (1u << q) : 0u;
-                    uint32_t bal;
-                    while ((bal = __ballot_sync(0xffffffffu, cm != 0u)) != 0u) {
-                        const int L = __ffs(bal) - 1;
-                        const int q = __shfl_sync(0xffffffffu, __ffs(cm) - 1, L);
-                        const float ye = tc_exact_y<D>(P.recent, src_new, P.kv_dtype, R, mkind, moff, L,
-                                                       gi * G + 32 * c + q, lane);
-                        if (lane == L) {
-                            cm &= cm - 1u;
-                            mne = fminf(mne, ye);
-                            mxe = fmaxf(mxe, ye);
-                        }
-                    }
-                }
+                const float2 ex = tc_exact_extremes<D, G>(tacc + gi * G, sB, xsrc, unc, mn, mx, e2, gi * G, lane);
                 if (unc) {
-                    mn = mne;
-                    mx = mxe;
+                    mn = ex.x;
+                    mx = ex.y;
                 }
             }
             __half s16, z16;
@@ -574,25 +650,9 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
                 // division, on the exact y where y ± e straddles a boundary
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
-                    if (!kKeep) load_y(tacc + gi * G + 32 * c, yk[0]);
-                    const float (&y)[32] = yk[kKeep ? c : 0];
-                    float2 cc[16];
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        float u = sc != 0.0f ? __fdiv_rn(__fsub_rn(y[q], zc), sc) : 0.0f;
-                        uint32_t mm = __ballot_sync(0xffffffffu, sc != 0.0f && code_near_boundary(u, be));
-                        while (mm) {
-                            const int L = __ffs(mm) - 1;
-                            mm &= mm - 1u;
-                            const float ye = tc_exact_y<D>(P.recent, src_new, P.kv_dtype, R, mkind, moff, L,
-                                                           gi * G + 32 * c + q, lane);
-                            if (lane == L) u = __fdiv_rn(__fsub_rn(ye, zc), sc);
-                        }
-                        const float cv = sc != 0.0f ? fminf(fmaxf(rintf(u), 0.0f), 3.0f) : 0.0f;
-                        if (q & 1) cc[q >> 1].y = cv;
-                        else cc[q >> 1].x = cv;
-                    }
-                    pack_codes32(cc, words[gi * (G / 16) + 2 * c], words[gi * (G / 16) + 2 * c + 1]);
+                    const uint2 w = tc_exact_codes<D>(tacc + gi * G + 32 * c, sB, xsrc, zc, sc, be, gi * G + 32 * c, lane);
+                    words[gi * (G / 16) + 2 * c] = w.x;
+                    words[gi * (G / 16) + 2 * c + 1] = w.y;
                 }
             }
             if (slot >= 0) *reinterpret_cast<__half2*>(rec + rec_off_sz + 4 * gi) = __halves2half2(s16, z16);

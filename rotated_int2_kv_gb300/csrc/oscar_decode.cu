@@ -43,8 +43,9 @@ __device__ __forceinline__ bool request_valid(const DecodeParams& P, int b, int*
 // prep: per (KV head, request), q̃ = q·R_K·(log2 e/√d) for the KV head's query
 // heads (fp32), its fp16 hi/lo split (of q̃/α) packed as mma B fragments, the
 // per-group sums; block (0, b) also the effective length / window row of
-// request b, and block (0, 0) the chunk prefix.  It runs as the last z-slice of
-// the window kernel's grid (128 threads), so the two need one launch.
+// request b, and block (0, 0) the chunk prefix.  It runs as the first z-slice
+// of the window kernel's grid (128 threads, scheduled ahead of the window
+// tiles), so the two need one launch.
 // ---------------------------------------------------------------------------
 constexpr int kPrepThreads = 128;
 
@@ -409,8 +410,8 @@ __global__ void __launch_bounds__(kCombThreads, D >= 256 ? 2 : 6) window_kernel(
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     constexpr int kRowW = D / 2 + 1;               // words per staged bf16 row (odd: conflict-free)
     extern __shared__ __align__(16) float s_w[];
-    const int hk = blockIdx.x, b = blockIdx.y, wt = blockIdx.z;
-    if (wt == P.n_win_tiles) {                     // the last z-slice: query preparation
+    const int hk = blockIdx.x, b = blockIdx.y, wt = (int)blockIdx.z - 1;
+    if (wt < 0) {                                  // the first z-slice: query preparation
         prep_dispatch<D>(P, hk, b, s_w);
         return;
     }
@@ -623,8 +624,8 @@ __global__ void __launch_bounds__(128) window_mma_kernel(DecodeParams P) {
     uint32_t* spa = sqa + KS * 128;                    // [4 sub-tiles][32 lanes][4] P fragments
     float* smx = reinterpret_cast<float*>(spa + 4 * 128);   // [4 warps][8 heads] sub-tile max
     float* ssm = smx + 32;                                   // [4 warps][8 heads] sub-tile sum
-    const int hk = blockIdx.x, b = blockIdx.y, wt = blockIdx.z;
-    if (wt == P.n_win_tiles) {                     // the last z-slice: query preparation
+    const int hk = blockIdx.x, b = blockIdx.y, wt = (int)blockIdx.z - 1;
+    if (wt < 0) {                                  // the first z-slice (scheduled first): query preparation
         prep_dispatch<D>(P, hk, b, reinterpret_cast<float*>(s_wm));
         return;
     }
