@@ -93,7 +93,11 @@ typedef struct {
  *            scale first.  Base address 16-byte aligned.
  *  sink      bf16 [max_reqs][S][Hkv][2][d]   (index 0 = K, 1 = V)
  *  recent    bf16 [max_reqs][W][Hkv][2][d]   ring: position p at p % W
- *  rot_k     fp32 [d][d] row-major R_K; rot_v likewise R_V (both orthogonal)
+ *  rot_k     fp32 [d][d] row-major R_K; rot_v likewise R_V (both orthogonal).
+ *            The append reads them before waiting for the stream's previous
+ *            kernel to finish (programmatic dependent launch), so write them
+ *            with a copy or with a kernel that does not signal its dependents
+ *            early.
  *  num_slots number of records in the pool; max_reqs rows of the windows.  */
 typedef struct {
     uint8_t*     records;
@@ -182,6 +186,16 @@ int oscar_value_covariance_device(const float* scores, const void* values, int32
  * Returns OSCAR_ERR_NUMERIC if the eigensolver does not converge. */
 int oscar_build_rotation(const double* cov, int32_t d, int32_t use_bitrev,
                          float* R_f32, double* R_f64, double* eigvals);
+
+/* As oscar_build_rotation, with the Hadamard factor block-diagonal: d/B copies
+ * of H_B/√B along the diagonal (B = hadamard_block, a power of two in [1, d];
+ * B = d is oscar_build_rotation).  [OSCAR news] "OSCARの違い" names the
+ * Hadamard factor without a size; with B < d each block mixes only B
+ * consecutive eigen-directions (channels of similar importance), and P_br then
+ * places every block's channels evenly over the quantisation groups: a group
+ * of G consecutive output channels takes G·B/d channels of each block. */
+int oscar_build_rotation_ex(const double* cov, int32_t d, int32_t use_bitrev, int32_t hadamard_block,
+                            float* R_f32, double* R_f64, double* eigvals);
 
 /* ---- append: rotate, clip, quantise, pack (device) ---------------------- */
 

@@ -34,7 +34,7 @@ Modules:
   accounting -- bytes and bits per token / element
 """
 
-from .rotation import (hadamard, bitrev_indices, eig_desc, build_rotation,
+from .rotation import (hadamard, block_hadamard, bitrev_indices, eig_desc, build_rotation,
                        covariance, value_covariance)
 from .quant import (bf16_round, quantize_rows, dequantize_rows, pack_codes,
                     unpack_codes)
@@ -44,7 +44,7 @@ from .accounting import (code_bytes_per_token, record_bytes, bits_per_element,
                          window_fraction)
 
 __all__ = [
-    "hadamard", "bitrev_indices", "eig_desc", "build_rotation", "covariance",
+    "hadamard", "block_hadamard", "bitrev_indices", "eig_desc", "build_rotation", "covariance",
     "value_covariance", "bf16_round", "quantize_rows", "dequantize_rows",
     "pack_codes", "unpack_codes", "OracleConfig", "OracleCache", "regions",
     "decode_attention", "decode_attention_split", "code_bytes_per_token",

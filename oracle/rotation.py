@@ -80,8 +80,28 @@ def eig_desc(C):
     return w, U
 
 
-def build_rotation(C, d, use_bitrev=True):
-    """R = U · (H_d / sqrt(d)) · P_br in fp64 (row-vector convention x · R).
+def block_hadamard(d, block):
+    """The d×d block-diagonal matrix with d/block copies of H_block / sqrt(block).
+
+    block = d gives the full normalised Hadamard.  [OSCAR news] "OSCARの違い"
+    names the Hadamard factor without a size; a block smaller than d confines
+    the mixing to channels of similar importance (consecutive eigen-directions),
+    which is the case in which P_br's spreading of each importance level over
+    the quantisation groups matters.
+    """
+    if block < 1 or (block & (block - 1)) != 0 or d % block != 0:
+        raise ValueError("block must be a power of two dividing d")
+    Hb = hadamard(block) / np.sqrt(block)
+    M = np.zeros((d, d))
+    for i in range(d // block):
+        M[i * block:(i + 1) * block, i * block:(i + 1) * block] = Hb
+    return M
+
+
+def build_rotation(C, d, use_bitrev=True, hadamard_block=None):
+    """R = U · H · P_br in fp64 (row-vector convention x · R), with H the
+    normalised Hadamard of size d, or block-diagonal with blocks of
+    hadamard_block (block_hadamard).
 
     C is the d×d covariance (C_Q for keys, C_S for values) or None for the
     calibration-free rotation U = I of [Escha log] fix 3.  With
@@ -97,7 +117,8 @@ def build_rotation(C, d, use_bitrev=True):
         if C.shape != (d, d):
             raise ValueError("covariance shape must be (d, d)")
         w, U = eig_desc(C)
-    M = U @ (hadamard(d) / np.sqrt(d))
+    block = d if hadamard_block is None else int(hadamard_block)
+    M = U @ block_hadamard(d, block)
     if use_bitrev:
         M = M[:, bitrev_indices(d)]  # column j takes column bitrev(j)
     return M, w

@@ -226,9 +226,16 @@ int oscar_value_covariance(const double* scores, const double* values, int64_t n
 
 int oscar_build_rotation(const double* cov, int32_t d, int32_t use_bitrev, float* R_f32,
                          double* R_f64, double* eigvals) {
+    return oscar_build_rotation_ex(cov, d, use_bitrev, d, R_f32, R_f64, eigvals);
+}
+
+int oscar_build_rotation_ex(const double* cov, int32_t d, int32_t use_bitrev, int32_t hadamard_block,
+                            float* R_f32, double* R_f64, double* eigvals) {
     clear_error();
     if (!R_f32) return fail(OSCAR_ERR_NULL, "R_f32 is NULL");
     if (d < 2 || d > 256 || (d & (d - 1)) != 0) return fail(OSCAR_ERR_ARG, "d must be a power of two in [2, 256]");
+    if (hadamard_block < 1 || hadamard_block > d || (hadamard_block & (hadamard_block - 1)) != 0)
+        return fail(OSCAR_ERR_ARG, "hadamard_block must be a power of two in [1, d]");
     const int n = d;
     std::vector<double> U((size_t)n * n, 0.0), w(n, 1.0);
     if (cov) {
@@ -260,15 +267,19 @@ int oscar_build_rotation(const double* cov, int32_t d, int32_t use_bitrev, float
     } else {
         for (int i = 0; i < n; ++i) U[(size_t)i * n + i] = 1.0;
     }
-    // M = U · H/√d with H[k][j] = (-1)^popcount(k & j) (Sylvester closed form).
-    const double inv = 1.0 / std::sqrt((double)n);
+    // M = U · H with H block-diagonal: blocks of B = hadamard_block channels,
+    // H[k][j] = (-1)^popcount(k & j)/√B when k and j share a block (Sylvester
+    // closed form within the block), else 0.  B = d is the full Hadamard.
+    const int B = hadamard_block;
+    const double inv = 1.0 / std::sqrt((double)B);
     std::vector<double> M((size_t)n * n, 0.0);
     for (int i = 0; i < n; ++i)
         for (int j = 0; j < n; ++j) {
             double acc = 0.0;
-            for (int k = 0; k < n; ++k) {
+            const int k0 = j / B * B;
+            for (int k = k0; k < k0 + B; ++k) {
                 const double u = U[(size_t)i * n + k];
-                acc += (popcount((unsigned)(k & j)) & 1) ? -u : u;
+                acc += (popcount((unsigned)(k & j & (B - 1))) & 1) ? -u : u;
             }
             M[(size_t)i * n + j] = acc * inv;
         }

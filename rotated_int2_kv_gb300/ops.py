@@ -84,6 +84,8 @@ _SIGS = {
     "oscar_value_covariance_device": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                                        ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
+    "oscar_build_rotation_ex": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                 ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "oscar_device_status": ([ctypes.POINTER(ctypes.c_int32), ctypes.c_int32], ctypes.c_int),
     "oscar_selftest_bounded_wait": ([ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
     "oscar_profile_enable": ([ctypes.c_int32], ctypes.c_int),
@@ -180,8 +182,9 @@ def value_covariance(scores, values):
     return C
 
 
-def build_rotation(cov, d, use_bitrev=True):
-    """Returns (R fp32, R fp64, eigenvalues) as NumPy arrays (host)."""
+def build_rotation(cov, d, use_bitrev=True, hadamard_block=None):
+    """Returns (R fp32, R fp64, eigenvalues) as NumPy arrays (host).
+    hadamard_block: block size of a block-diagonal Hadamard factor (None: d)."""
     R32 = np.empty((d, d), np.float32)
     R64 = np.empty((d, d), np.float64)
     w = np.empty(d, np.float64)
@@ -189,8 +192,9 @@ def build_rotation(cov, d, use_bitrev=True):
     if cov is not None:
         cov = np.ascontiguousarray(cov, dtype=np.float64)
         cp = cov.ctypes.data
-    _check(lib().oscar_build_rotation(cp, d, int(bool(use_bitrev)), R32.ctypes.data,
-                                      R64.ctypes.data, w.ctypes.data))
+    blk = d if hadamard_block is None else int(hadamard_block)
+    _check(lib().oscar_build_rotation_ex(cp, d, int(bool(use_bitrev)), blk, R32.ctypes.data,
+                                         R64.ctypes.data, w.ctypes.data))
     return R32, R64, w
 
 

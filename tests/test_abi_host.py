@@ -146,3 +146,18 @@ def test_rotation_argument_errors(ops):
     bad = np.full((4, 4), np.nan)
     out = np.zeros((4, 4), np.float32)
     assert L.oscar_build_rotation(bad.ctypes.data, 4, 1, out.ctypes.data, None, None) == -1
+
+
+@pytest.mark.parametrize("d,B", [(128, 16), (64, 8), (256, 64), (128, 1)])
+def test_block_hadamard_rotation_matches_oracle(ops, d, B):
+    import oracle
+    rng = np.random.default_rng(d + B)
+    X = rng.standard_normal((2048, d)) * (np.arange(1, d + 1) ** -0.75)
+    C = oracle.covariance(X)
+    R32, R64, w = ops.build_rotation(C, d, hadamard_block=B)
+    Ro, wo = oracle.build_rotation(C, d, hadamard_block=B)
+    assert np.abs(R64 - Ro).max() <= 1e-9
+    assert np.abs(R32 - Ro.astype(np.float32)).max() <= 1e-7
+    assert np.abs(R64 @ R64.T - np.eye(d)).max() <= 1e-12
+    with pytest.raises(ops.OscarError):
+        ops.build_rotation(C, d, hadamard_block=3)

@@ -189,14 +189,16 @@ def test_device_checks_flag_bad_slots_without_faulting():
     assert ops.device_status(clear=True) == 0
 
 
-def test_library_built_rotation_end_to_end():
-    # R_K, R_V from the library's own builder (oscar_build_rotation), not the
-    # oracle's: append parity, then decode against the oracle on the same R
+@pytest.mark.parametrize("block", [None, 16])
+def test_library_built_rotation_end_to_end(block):
+    # R_K, R_V from the library's own builder (oscar_build_rotation, and with a
+    # block-diagonal Hadamard factor), not the oracle's: append parity, then
+    # decode against the oracle on the same R
     from rotated_int2_kv_gb300 import ops
     from parity_util import ATOL, RTOL_L2, attn_errors, device_cache_from_oracle
     d = 128
-    Rk, _, _ = ops.build_rotation(ops.covariance(synth.calib_samples(SEED, 0, d)), d)
-    Rv, _, _ = ops.build_rotation(ops.covariance(synth.calib_samples(SEED, 1, d)), d)
+    Rk, _, _ = ops.build_rotation(ops.covariance(synth.calib_samples(SEED, 0, d)), d, hadamard_block=block)
+    Rv, _, _ = ops.build_rotation(ops.covariance(synth.calib_samples(SEED, 1, d)), d, hadamard_block=block)
     keep = {}
     calls = [[1500, 700], [1, 1], [1, 1], [1, 1]]
     run_append_scenario(d, 32, 8, 64, 64, 256, torch.bfloat16, calls, rotations=(Rk, Rv), keep=keep)

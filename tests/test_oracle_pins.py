@@ -127,6 +127,43 @@ def test_rotation_is_orthogonal_and_factorises():
     assert np.abs(C @ U - U * w).max() <= 1e-10 * np.abs(C).max()
 
 
+def test_block_hadamard_closed_form_and_orthogonality():
+    for d, B in ((128, 16), (64, 64), (256, 32), (8, 2), (8, 1)):
+        M = oracle.block_hadamard(d, B)
+        assert np.abs(M @ M.T - np.eye(d)).max() <= 1e-15
+        i, j = np.meshgrid(np.arange(d), np.arange(d), indexing="ij")
+        same = (i // B) == (j // B)
+        sign = np.array([[(-1.0) ** bin(a & b & (B - 1)).count("1") for b in range(d)] for a in range(d)])
+        assert np.array_equal(M, np.where(same, sign / math.sqrt(B), 0.0))
+    # the full size is the page's Hadamard
+    assert np.array_equal(oracle.block_hadamard(64, 64), oracle.hadamard(64) / 8.0)
+    R_full, _ = oracle.build_rotation(None, 128, hadamard_block=128)
+    R_def, _ = oracle.build_rotation(None, 128)
+    assert np.array_equal(R_full, R_def)
+
+
+def test_bitrev_spreads_every_importance_block_over_every_group():
+    # C = diag(lambda) descending: U = I, so input channel k is importance level
+    # k, and block b of H_B mixes levels [bB, (b+1)B).  After P_br, every group of
+    # G consecutive output channels takes G·B/d channels of every block; without
+    # P_br each group sees only G/B blocks.
+    d = 128
+    C = np.diag(np.arange(d, 0, -1, dtype=np.float64))
+    for B, G in ((16, 64), (8, 32), (32, 128), (128, 64)):
+        R, _ = oracle.build_rotation(C, d, hadamard_block=B)
+        for g in range(d // G):
+            cols = R[:, g * G:(g + 1) * G]
+            # output channels of the group fed by block b
+            per_block = np.array([(np.abs(cols[b * B:(b + 1) * B]).sum(axis=0) > 0).sum()
+                                  for b in range(d // B)])
+            assert (per_block == G * B // d).all(), (B, G, g, per_block)
+        if B < G:
+            Rn, _ = oracle.build_rotation(C, d, use_bitrev=False, hadamard_block=B)
+            cols = Rn[:, :G]
+            per_block = np.array([(np.abs(cols[b * B:(b + 1) * B]).sum(axis=0) > 0).sum() for b in range(d // B)])
+            assert (per_block[: G // B] == B).all() and (per_block[G // B:] == 0).all()
+
+
 def test_covariances_against_explicit_sums():
     rng = np.random.default_rng(4)
     X = rng.standard_normal((7, 5))
