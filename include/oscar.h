@@ -13,6 +13,8 @@
  *                per INT2 element), fix 3 (Hadamard / sqrt(head_dim)), fix 4
  *                (query head -> KV head mapping), settings table (group size 64).
  *  [Scheduler log] sglang scheduler article on 12 GB / 27B: page_size 1.
+ *  [Prefix log]  "KVプールが上限だった — hybrid GDN の長文キャッシュ…": the INT2
+ *                prefill path expands the cached prefix to fp16 before attention.
  *
  * Conventions shared by every entry point
  *  - Return value: OSCAR_OK (0) or a negative OSCAR_ERR_* code.  Nothing
@@ -303,6 +305,45 @@ int oscar_decode_attention_noalloc(const oscar_config* cfg, const oscar_layer_ca
                                    const int32_t* seq_lens, const int32_t* req_idx,
                                    int32_t batch, int32_t max_seq_len, float* out, void* stream);
 
+/* ---- prefill attention over the cached prefix (device) ------------------ */
+
+/* Workspace bytes of oscar_prefill_attention for `batch` requests and
+ * `total_q` chunk tokens in all (host output). */
+int oscar_prefill_workspace_bytes(const oscar_config* cfg, int32_t batch, int64_t total_q, size_t* bytes);
+
+/* Attention of prefill chunks over the mixed cache, reading the INT2 history
+ * directly: [Prefix log] "KVプールが上限だった — hybrid GDN の長文キャッシュ…"
+ * describes the prefill path that first expands the cached INT2 prefix into
+ * an fp16 workspace growing with the sequence; this call needs no such copy.
+ * Request b holds L0 = start_pos[b] tokens in the cache (sink and recent
+ * windows in BF16, history in INT2, page_table row b covering positions < L0)
+ * and brings chunk rows cu_q[b] .. cu_q[b+1] (positions L0, L0+1, ...).  For
+ * every chunk query i and query head h (KV head h/(Hq/Hkv)):
+ *   out = softmax over { the prefix as stored: logit q·k/√d against BF16 keys,
+ *         (q·R_K)·k̂/√d against INT2 keys } ∪ { the chunk's own keys at
+ *         positions L0 .. L0+i, at bf16 } of the values, the INT2 values
+ *         mapped back by R_Vᵀ.
+ * The chunk's keys and values are not written to the cache by this call;
+ * append them with oscar_quantize_append afterwards.
+ * Arguments (device unless marked):
+ *  q            [total_q][Hq][d] in cfg->q_dtype
+ *  k, v         [total_q][Hkv][d] in cfg->kv_dtype (the chunk's own keys / values)
+ *  total_q      host: rows of q, k, v
+ *  cu_q         int32 [batch+1], cu_q[0] = 0, non-decreasing, cu_q[batch] = total_q
+ *  start_pos    int32 [batch] prefix length L0 (0 <= L0 <= pt_stride)
+ *  req_idx      int32 [batch] window row, or NULL for b
+ *  page_table   int32 [batch][pt_stride]
+ *  batch        host, 0..4096; max_chunk host, the largest cu_q[b+1] - cu_q[b]
+ *  out          fp32 [total_q][Hq][d]
+ *  workspace    device, >= oscar_prefill_workspace_bytes(cfg, batch, total_q), 256-byte aligned
+ * Invalid prefix lengths or rows set OSCAR_DEV_BAD_LEN / _BAD_REQ and attend
+ * over the chunk alone; out-of-pool slots set OSCAR_DEV_BAD_SLOT and are skipped. */
+int oscar_prefill_attention(const oscar_config* cfg, const oscar_layer_cache* cache, const void* q,
+                            const void* k, const void* v, int64_t total_q, const int32_t* cu_q,
+                            const int32_t* start_pos, const int32_t* req_idx, const int32_t* page_table,
+                            int64_t pt_stride, int32_t batch, int32_t max_chunk, float* out,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- kernel timing (benchmarks) ----------------------------------------- */
 
 /* Event timing of the kernels: `enable` is a bit mask of kinds (bit k times
@@ -310,8 +351,9 @@ int oscar_decode_attention_noalloc(const oscar_config* cfg, const oscar_layer_ca
  * history kernel, 4 the window kernel (which also prepares the rotated
  * queries) and 5 the combine kernel of oscar_decode_attention; 1 the quantise
  * kernel (for appends of at most W tokens it also writes the window rows) and
- * 2 the window-copy kernel (larger appends) of oscar_quantize_append.  Kind 3
- * is reserved and never recorded.  A timed launch gets a CUDA event pair on
+ * 2 the window-copy kernel (larger appends) of oscar_quantize_append; 6 the
+ * attention kernel of oscar_prefill_attention.  Kind 3 is reserved and never
+ * recorded.  A timed launch gets a CUDA event pair on
  * the call's stream (two cudaEventRecord, which also separate it from its
  * neighbours). */
 int oscar_profile_enable(int32_t enable);

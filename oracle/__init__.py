@@ -23,6 +23,9 @@ Sources (web pages, cited by title and section):
   table of INT2 KV bytes per token.
 * [Scheduler log] "12GB の VRAM に 27B" scheduler article: page_size 1
   (token-granular page table).
+* [Prefix log] "KVプールが上限だった — hybrid GDN の長文キャッシュ…": the INT2
+  prefill path expands the cached prefix to fp16 in a workspace
+  (dequantize_prefix_kv) before attention.
 
 Modules:
   rotation   -- Hadamard, bit reversal, eigenbasis, R = U·H·P_br, covariances
@@ -31,6 +34,8 @@ Modules:
   cache      -- the three-region cache and its append semantics
   attention  -- exact-softmax decode attention over the mixed cache, and the
                 split/LSE merge
+  prefill    -- exact-softmax attention of a prefill chunk over the cached
+                prefix and its own keys (causal)
   accounting -- bytes and bits per token / element
 """
 
@@ -40,6 +45,7 @@ from .quant import (bf16_round, quantize_rows, dequantize_rows, pack_codes,
                     unpack_codes)
 from .cache import OracleConfig, OracleCache, regions
 from .attention import decode_attention, decode_attention_split
+from .prefill import prefill_attention
 from .accounting import (code_bytes_per_token, record_bytes, bits_per_element,
                          window_fraction)
 
@@ -47,6 +53,6 @@ __all__ = [
     "hadamard", "block_hadamard", "bitrev_indices", "eig_desc", "build_rotation", "covariance",
     "value_covariance", "bf16_round", "quantize_rows", "dequantize_rows",
     "pack_codes", "unpack_codes", "OracleConfig", "OracleCache", "regions",
-    "decode_attention", "decode_attention_split", "code_bytes_per_token",
+    "decode_attention", "decode_attention_split", "prefill_attention", "code_bytes_per_token",
     "record_bytes", "bits_per_element", "window_fraction",
 ]

@@ -74,7 +74,7 @@ __device__ __forceinline__ void quantize_store(const AppendParams& P, float (&y)
     __half s16, z16;
     sz_decide(mn, mx, r, s16, z16);
     const float s = __half2float(s16), z = __half2float(z16);
-    const float band = code_band(e, s);
+    const float band = s != 0.0f ? code_band(e, __frcp_rn(3.0f * s)) : 0.0f;
     uint32_t bits = 0;
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {

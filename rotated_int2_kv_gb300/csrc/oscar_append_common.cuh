@@ -98,20 +98,29 @@ __device__ __forceinline__ void sz_decide(float mn, float mx, float r, __half& s
 }
 
 // True when extremes anywhere in [mn - e, mn + e] × [mx - e, mx + e] could give
-// another (s, z): s grows with mx and falls with mn, z grows with mn.
+// another (s, z).  Every step of sz_decide is monotone, so the oracle's values
+// at any point of that box lie in intervals bounded with directed rounding:
+// lo in [rd(r·(mn - e)), ru(r·(mn + e))], and (hi - lo)/3 in
+// [rd((rd(r·(mx - e)) - ru(r·(mn + e)))·⅓↓), ru((ru(r·(mx + e)) - rd(r·(mn - e)))·⅓↑)];
+// the decision is certain when both ends of each interval round to the same fp16.
 __device__ __forceinline__ bool sz_uncertain(float mn, float mx, float r, float e) {
-    __half sa, za, sb, zb;
-    sz_decide(__fsub_rd(mn, e), __fadd_ru(mx, e), r, sa, za);   // widest range: largest s, smallest z
-    sz_decide(__fadd_ru(mn, e), __fsub_rd(mx, e), r, sb, zb);   // narrowest range: smallest s, largest z
-    return __half_as_ushort(sa) != __half_as_ushort(sb) || __half_as_ushort(za) != __half_as_ushort(zb);
+    constexpr float kThirdDn = 0.333333313465118408203125f;   // the fp32 neighbours of 1/3
+    constexpr float kThirdUp = 0.3333333432674407958984375f;
+    const float lo_a = __fmul_rd(r, __fsub_rd(mn, e)), lo_b = __fmul_ru(r, __fadd_ru(mn, e));
+    const float hi_a = __fmul_rd(r, __fsub_rd(mx, e)), hi_b = __fmul_ru(r, __fadd_ru(mx, e));
+    const float s_a = __fmul_rd(__fsub_rd(hi_a, lo_b), kThirdDn);
+    const float s_b = __fmul_ru(__fsub_ru(hi_b, lo_a), kThirdUp);
+    return __half_as_ushort(__float2half_rn(lo_a)) != __half_as_ushort(__float2half_rn(lo_b)) ||
+           __half_as_ushort(__float2half_rn(fmaxf(s_a, 0.0f))) != __half_as_ushort(__float2half_rn(s_b));
 }
 
 // Half-width in units of the quotient u = (y - z)/s of the band around a
 // rounding boundary (0.5, 1.5, 2.5) inside which y ± e may decide another code:
 // e/s plus the roundings of y - z and of the division (2^-21 relative for |u|
-// up to 3), with margin.
-__device__ __forceinline__ float code_band(float e, float s) {
-    return s != 0.0f ? __fmaf_ru(__fdiv_ru(e, s), 1.0f + 1.0f / 1048576.0f, 1.0f / 524288.0f) : 0.0f;
+// up to 3), with margin.  r3 is the fp32 reciprocal of 3s (within half an ulp),
+// so 3e·r3 is e/s to 2^-22.
+__device__ __forceinline__ float code_band(float e, float r3) {
+    return __fmaf_ru(__fmul_ru(3.0f * e, r3), 1.0f + 1.0f / 1048576.0f, 1.0f / 524288.0f);
 }
 
 // True when the correctly rounded quotient u lies within `band` of a rounding

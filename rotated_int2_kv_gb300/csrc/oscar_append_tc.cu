@@ -233,22 +233,28 @@ __device__ __forceinline__ float tc_dot2(const unsigned char* sB, const ExactSrc
     return __fadd_rn(s, c);
 }
 
+// One fp32 column of this thread's tensor-memory lane (warp-collective: the
+// column must be the same in every lane).
+__device__ __forceinline__ float load_col(uint32_t taddr) {
+    uint32_t v;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr));
+    tc5::wait_ld();
+    return __uint_as_float(v);
+}
+
 // Exact extremes of one group for the lanes whose (s, z) y ± e could change
-// (warp-collective; out of line, so the common path stays compact): the
-// extremes lie among the channels within 2e of the computed ones, which are
-// formed exactly.  Returns (min, max); meaningful for uncertain lanes.
-template <int D, int G>
-__device__ __noinline__ float2 tc_exact_extremes(uint32_t tgrp, const unsigned char* sB, ExactSrc src, bool unc,
-                                                 float mn, float mx, float e2, int ch0, int lane) {
-    const float tlo = __fadd_ru(mn, e2), thi = __fsub_rd(mx, e2);
+// (warp-collective; out of line, so the common path stays compact).  cm0 / cm1
+// mark this lane's candidate channels (y within 2e of the computed extremes) in
+// the group's channels 0-31 / 32-63 (cm1 for groups of 64 and up; larger groups
+// pass their other chunks through `more`): the exact extremes lie among them.
+// Returns (min, max) over the exact values of the candidates.
+template <int D>
+__device__ __noinline__ float2 tc_exact_extremes(const unsigned char* sB, ExactSrc src, uint32_t cm0, uint32_t cm1,
+                                                 int ch0, int lane) {
     float mne = INFINITY, mxe = -INFINITY;
 #pragma unroll 1
-    for (int c = 0; c < G / 32; ++c) {
-        float y[32];
-        load_y(tgrp + 32 * c, y);
-        uint32_t cm = 0;
-#pragma unroll
-        for (int q = 0; q < 32; ++q) cm |= (unc && (y[q] <= tlo || y[q] >= thi)) ? (1u << q) : 0u;
+    for (int c = 0; c < 2; ++c) {
+        uint32_t cm = c ? cm1 : cm0;
         uint32_t bal;
         while ((bal = __ballot_sync(0xffffffffu, cm != 0u)) != 0u) {
             const int L = __ffs(bal) - 1;
@@ -264,30 +270,40 @@ __device__ __noinline__ float2 tc_exact_extremes(uint32_t tgrp, const unsigned c
     return make_float2(mne, mxe);
 }
 
-// Codes of one 32-channel chunk by correctly rounded division, on the exact y
-// where y ± e straddles a boundary (warp-collective; out of line).
+// Re-decides the codes of one 32-channel chunk whose reciprocal-path quotient
+// lies near a half-integer (warp-collective; out of line): such a channel is
+// decided by correctly rounded division, on the exact y where y ± e straddles
+// a boundary, and patched into the chunk's two code words w.
 template <int D>
 __device__ __noinline__ uint2 tc_exact_codes(uint32_t tchunk, const unsigned char* sB, ExactSrc src, float zc,
-                                             float sc, float be, int ch0, int lane) {
+                                             float sc, float r3, float nb2, float be, uint2 w, int ch0, int lane) {
     float y[32];
     load_y(tchunk, y);
-    float2 cc[16];
+    uint32_t cm = 0;                              // channels to re-decide (the fast path's test)
 #pragma unroll
     for (int q = 0; q < 32; ++q) {
-        float u = sc != 0.0f ? __fdiv_rn(__fsub_rn(y[q], zc), sc) : 0.0f;
-        uint32_t mm = __ballot_sync(0xffffffffu, sc != 0.0f && code_near_boundary(u, be));
-        while (mm) {
-            const int L = __ffs(mm) - 1;
-            mm &= mm - 1u;
-            const float ye = tc_dot2<D>(sB, src, L, ch0 + q, lane);
-            if (lane == L) u = __fdiv_rn(__fsub_rn(ye, zc), sc);
-        }
-        const float cv = sc != 0.0f ? fminf(fmaxf(rintf(u), 0.0f), 3.0f) : 0.0f;
-        if (q & 1) cc[q >> 1].y = cv;
-        else cc[q >> 1].x = cv;
+        const float t = __saturatef(__fmul_rn(__fsub_rn(y[q], zc), r3));
+        const float qq = __fmul_rn(t, 3.0f);
+        const float dd = qq - rintf(qq);
+        cm |= (__fmaf_rn(dd, dd, nb2) >= 0.0f ? 1u : 0u) << q;
     }
-    uint2 w;
-    pack_codes32(cc, w.x, w.y);
+    uint32_t bal;
+    while ((bal = __ballot_sync(0xffffffffu, cm != 0u)) != 0u) {
+        const int L = __ffs(bal) - 1;
+        const int q = __shfl_sync(0xffffffffu, __ffs(cm) - 1, L);
+        const float yq = load_col(tchunk + q);    // every lane's y of channel q; lane L's is the one used
+        float u = sc != 0.0f ? __fdiv_rn(__fsub_rn(yq, zc), sc) : 0.0f;
+        if (__shfl_sync(0xffffffffu, (int)(sc != 0.0f && code_near_boundary(u, be)), L)) {
+            const float ye = tc_dot2<D>(sB, src, L, ch0 + q, lane);
+            u = __fdiv_rn(__fsub_rn(ye, zc), sc);
+        }
+        if (lane == L) {
+            cm &= cm - 1u;
+            const uint32_t c = sc != 0.0f ? (uint32_t)fminf(fmaxf(rintf(u), 0.0f), 3.0f) : 0u;
+            if (q < 16) w.x = (w.x & ~(3u << (2 * q))) | (c << (2 * q));
+            else w.y = (w.y & ~(3u << (2 * q - 32))) | (c << (2 * q - 32));
+        }
+    }
     return w;
 }
 
@@ -621,10 +637,26 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
             // (s, z) that y ± e could change: the extremes formed exactly (out of line)
             const bool unc = sz_uncertain(mn, mx, rclip, e);
             if (__any_sync(0xffffffffu, unc)) {
-                const float2 ex = tc_exact_extremes<D, G>(tacc + gi * G, sB, xsrc, unc, mn, mx, e2, gi * G, lane);
+                const float tlo = __fadd_ru(mn, e2), thi = __fsub_rd(mx, e2);
+                float mne = INFINITY, mxe = -INFINITY;
+#pragma unroll
+                for (int c2 = 0; c2 < NC; c2 += 2) {
+                    uint32_t cmk[2] = {0u, 0u};
+#pragma unroll
+                    for (int h2 = 0; h2 < 2 && c2 + h2 < NC; ++h2) {
+                        if (!kKeep) load_y(tacc + gi * G + 32 * (c2 + h2), yk[0]);
+                        const float (&y)[32] = yk[kKeep ? c2 + h2 : 0];
+#pragma unroll
+                        for (int q = 0; q < 32; ++q)
+                            cmk[h2] |= (unc && (y[q] <= tlo || y[q] >= thi)) ? (1u << q) : 0u;
+                    }
+                    const float2 ex = tc_exact_extremes<D>(sB, xsrc, cmk[0], cmk[1], gi * G + 32 * c2, lane);
+                    mne = fminf(mne, ex.x);
+                    mxe = fmaxf(mxe, ex.y);
+                }
                 if (unc) {
-                    mn = ex.x;
-                    mx = ex.y;
+                    mn = mne;
+                    mx = mxe;
                 }
             }
             __half s16, z16;
@@ -635,7 +667,7 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
             const float r3 = sc != 0.0f ? __frcp_rn(3.0f * sc) : 0.0f;   // 3·sc is exact (11-bit significand × 3)
             // a code is certain when its quotient is farther from a half-integer than
             // e/s plus the reciprocal path's 2^-21
-            const float be = code_band(e, sc);
+            const float be = code_band(e, r3);
             const float hb = 0.5f - (be + 1.0f / 2097152.0f);
             const float nb2 = hb > 0.0f ? -hb * hb : 0.0f;
             uint32_t tie = 0xFFFFFFFFu;
@@ -646,11 +678,14 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
                         tie);
             }
             if (__any_sync(0xffffffffu, !(tie >> 31))) {
-                // a quotient near a tie: decide the group by correctly rounded
+                // a quotient near a tie: re-decide those channels by correctly rounded
                 // division, on the exact y where y ± e straddles a boundary
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
-                    const uint2 w = tc_exact_codes<D>(tacc + gi * G + 32 * c, sB, xsrc, zc, sc, be, gi * G + 32 * c, lane);
+                    const uint2 w = tc_exact_codes<D>(tacc + gi * G + 32 * c, sB, xsrc, zc, sc, r3, nb2, be,
+                                                      make_uint2(words[gi * (G / 16) + 2 * c],
+                                                                 words[gi * (G / 16) + 2 * c + 1]),
+                                                      gi * G + 32 * c, lane);
                     words[gi * (G / 16) + 2 * c] = w.x;
                     words[gi * (G / 16) + 2 * c + 1] = w.y;
                 }

@@ -86,6 +86,12 @@ _SIGS = {
                                        ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
     "oscar_build_rotation_ex": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
                                  ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "oscar_prefill_workspace_bytes": ([ctypes.POINTER(CConfig), ctypes.c_int32, ctypes.c_int64,
+                                       ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+    "oscar_prefill_attention": ([ctypes.POINTER(CConfig), ctypes.POINTER(CLayerCache), ctypes.c_void_p,
+                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
     "oscar_device_status": ([ctypes.POINTER(ctypes.c_int32), ctypes.c_int32], ctypes.c_int),
     "oscar_selftest_bounded_wait": ([ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
     "oscar_profile_enable": ([ctypes.c_int32], ctypes.c_int),
@@ -338,6 +344,36 @@ def decode_attention(cache, q, page_table, seq_lens, max_seq_len, workspace, req
     return out
 
 
+def prefill_workspace_bytes(cfg, batch, total_q):
+    out = ctypes.c_size_t()
+    _check(lib().oscar_prefill_workspace_bytes(ctypes.byref(cfg.c()), batch, total_q, ctypes.byref(out)))
+    return out.value
+
+
+def prefill_attention(cache, q, k, v, cu_q, start_pos, page_table, max_chunk, req_idx=None, out=None,
+                      workspace=None, stream=None):
+    """Attention of prefill chunks over the cached prefix (see oscar_prefill_attention):
+    q (T, Hq, d), k, v (T, Hkv, d) -> out (T, Hq, d) fp32."""
+    cfg = cache.cfg
+    T = q.shape[0]
+    B = start_pos.shape[0]
+    if cu_q.shape[0] != B + 1:
+        raise ValueError("cu_q must have batch + 1 entries")
+    dev = _device_of(cache, q, k, v, cu_q, start_pos, page_table, req_idx, out, workspace)
+    with torch.cuda.device(dev):
+        if out is None:
+            out = torch.empty((T, cfg.num_q_heads, cfg.head_dim), dtype=torch.float32, device=dev)
+        if workspace is None:
+            workspace = torch.empty(max(prefill_workspace_bytes(cfg, B, T), 256), dtype=torch.uint8, device=dev)
+        _check(lib().oscar_prefill_attention(
+            ctypes.byref(cfg.c()), ctypes.byref(cache.c()), _ptr(q, cfg.q_dtype, "q"), _ptr(k, cfg.kv_dtype, "k"),
+            _ptr(v, cfg.kv_dtype, "v"), T, _ptr(cu_q, torch.int32, "cu_q"), _ptr(start_pos, torch.int32, "start_pos"),
+            _ptr(req_idx, torch.int32, "req_idx"), _ptr(page_table, torch.int32, "page_table"), page_table.shape[1],
+            B, int(max_chunk), _ptr(out, torch.float32, "out"), _ptr(workspace, torch.uint8, "workspace"),
+            workspace.numel(), _stream(stream, dev)))
+    return out
+
+
 def device_status(clear=True):
     f = ctypes.c_int32()
     _check(lib().oscar_device_status(ctypes.byref(f), int(bool(clear))))
@@ -349,7 +385,7 @@ def selftest_bounded_wait(budget_cycles, complete, stream=None):
     _check(lib().oscar_selftest_bounded_wait(int(budget_cycles), int(bool(complete)), _stream(stream)))
 
 
-PROF_HISTORY, PROF_QUANTIZE, PROF_WINDOW_COPY, PROF_PREP, PROF_WINDOW, PROF_COMBINE = 0, 1, 2, 3, 4, 5
+PROF_HISTORY, PROF_QUANTIZE, PROF_WINDOW_COPY, PROF_PREP, PROF_WINDOW, PROF_COMBINE, PROF_PREFILL = 0, 1, 2, 3, 4, 5, 6
 
 
 def profile_enable(kinds=(PROF_HISTORY,)):

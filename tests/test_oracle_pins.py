@@ -445,3 +445,46 @@ def test_split_merge_equals_single_pass():
     for chunk in (1, 5, 16, 64):
         b = oracle.decode_attention_split(cache, q, pt, lens, [0, 1, 2], chunk)
         assert np.abs(a - b).max() <= 1e-13
+
+
+def test_prefill_without_history_equals_textbook_causal_attention():
+    # prefix of 5 BF16 tokens (sink 4 + recent 8: no history), chunk of 6
+    # queries; GQA 6 mapping; every query sees the prefix and the chunk causally
+    d, Hq, Hkv = 16, 12, 2
+    cfg = oracle.OracleConfig(d, Hq, Hkv, 16, 4, 8, 0.9)
+    rng = np.random.default_rng(21)
+    L0, C = 5, 6
+    k = rng.standard_normal((L0 + C, Hkv, d)).astype(np.float32)
+    v = rng.standard_normal((L0 + C, Hkv, d)).astype(np.float32) + np.arange(Hkv)[None, :, None] * 10
+    cache = oracle.OracleCache(cfg, 16, 1, np.eye(d), np.eye(d))
+    cache.append(k[:L0], v[:L0], [0, L0], [0], [0], np.arange(16)[None])
+    q = rng.standard_normal((C, Hq, d))
+    out = oracle.prefill_attention(cache, q, k[L0:], v[L0:], np.arange(16)[None], L0, 0)
+    kb = oracle.bf16_round(k).astype(np.float64)
+    vb = oracle.bf16_round(v).astype(np.float64)
+    for i in range(C):
+        for h in range(Hq):
+            ref = _textbook_attention(q[i, h], kb[:L0 + i + 1, h // 6], vb[:L0 + i + 1, h // 6])
+            assert np.abs(out[i, h] - ref).max() <= 1e-12
+
+
+def test_prefill_of_one_token_equals_decode_with_a_wider_window():
+    # The cache before the append with recent window W, plus the new token at
+    # bf16, is the cache after the append with window W + 1: same sink, same
+    # history records [S, L0 - W), recent [L0 - W, L0 + 1).
+    d, Hq, Hkv, G, S, W = 32, 4, 2, 16, 4, 8
+    rng = np.random.default_rng(22)
+    Rk, _ = oracle.build_rotation(oracle.covariance(rng.standard_normal((256, d))), d)
+    Rv, _ = oracle.build_rotation(oracle.covariance(rng.standard_normal((256, d))), d)
+    L0 = 40
+    k = (rng.standard_normal((L0 + 1, Hkv, d)) * 3).astype(np.float32)
+    v = rng.standard_normal((L0 + 1, Hkv, d)).astype(np.float32)
+    pt = rng.permutation(64)[None, :L0 + 1]
+    a = oracle.OracleCache(oracle.OracleConfig(d, Hq, Hkv, G, S, W), 64, 1, Rk, Rv)
+    a.append(k[:L0], v[:L0], [0, L0], [0], [0], pt)
+    wide = oracle.OracleCache(oracle.OracleConfig(d, Hq, Hkv, G, S, W + 1), 64, 1, Rk, Rv)
+    wide.append(k, v, [0, L0 + 1], [0], [0], pt)
+    q = rng.standard_normal((1, Hq, d))
+    got = oracle.prefill_attention(a, q, k[L0:], v[L0:], pt, L0, 0)
+    want = oracle.decode_attention(wide, q, pt, [L0 + 1], [0])
+    assert np.abs(got - want).max() <= 1e-12
