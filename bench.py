@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-append", action="store_true")
+    ap.add_argument("--no-shapes", dest="shapes", action="store_false",
+                    help="skip the ragged GQA-8 / wide GQA-6 decode shapes and the prefill chunks of the default line")
     ap.add_argument("--workload", choices=["qwen8b-100k", "mid", "small", "b1-32k", "qwen32b-ragged", "gqa6-wide"],
                     default="qwen8b-100k",
                     help="small: batch 4 at 65,536 tokens (168 MB of INT2 records, > L2), for ncu captures; "
@@ -353,6 +355,132 @@ def workload_config(rec_tok=640):
             "parallelism": "replicas (independent requests per GPU)"}
 
 
+def set_workload(name):
+    """Sets the module's workload shape (the globals the builders read)."""
+    global B, HQ, HKV, D, G, L_BASE, LB, OUTLIERS, CYCLE
+    B, HQ, HKV, D, G, L_BASE, OUTLIERS, CYCLE = 32, 32, 8, 128, 64, 100_000, "fixed4", 100
+    if name == "small":
+        B, L_BASE = 4, 65536
+    elif name == "mid":
+        B, L_BASE = 8, 100_000
+    elif name == "b1-32k":
+        B, L_BASE = 1, 32_767
+    elif name == "qwen32b-ragged":
+        from rotated_int2_kv_gb300 import synth
+        B, HQ, HKV, D, G = 8, 64, 8, 128, 64
+        OUTLIERS, CYCLE = "per_head", 50
+        LB = synth.ragged_lengths(SEED, B, 65_536, 131_072).astype(np.int64) - 1
+    elif name == "gqa6-wide":
+        B, HQ, HKV, D, G, L_BASE = 5, 24, 4, 256, 128, 112_000
+    if name != "qwen32b-ragged":
+        LB = np.full(B, L_BASE, dtype=np.int64)
+
+
+def shape_measure(name, steps, warmup, hbm_peak):
+    """Decode steps of another workload shape (history kernel time, roofline,
+    clocks), for the extra keys of the default bench line."""
+    import torch
+    from rotated_int2_kv_gb300 import ops
+    saved = (B, HQ, HKV, D, G, L_BASE, LB, OUTLIERS, CYCLE)
+    try:
+        set_workload(name)
+        w = build_decode_workload(0, steps + warmup)
+        for i in range(warmup):
+            decode_step(w, i, "auto")
+        torch.cuda.synchronize()
+        clocks = ClockSampler(torch.cuda.current_device())
+        clocks.start()
+        time.sleep(0.3)
+        ops.profile_enable([ops.PROF_HISTORY])
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(steps):
+            decode_step(w, warmup + i, "auto")
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        hms, hn = ops.profile_read(ops.PROF_HISTORY)
+        ops.profile_enable(None)
+        clk = clocks.stop()
+        assert ops.device_status() == 0
+        rec_tok, _ = ops.cache_bytes_per_token(w["cfg"])
+        tokens, hist_bytes = 0, 0
+        for i in range(steps):
+            Ls = LB + (warmup + i) % CYCLE + 1
+            tokens += int(Ls.sum())
+            hist_bytes += sum(algorithmic_history_bytes(rec_tok, int(L)) for L in Ls)
+        achieved = (hist_bytes / hn) / (hms / hn / 1e3) / 1e9
+        out = {"workload": workload_config(rec_tok)["workload"], "value": tokens / (ms / 1e3), "unit": UNIT,
+               "ms_per_step": ms / steps, "steps": steps,
+               "history_ms_per_step": hms / hn, "bits_per_kv_element": float(np.mean((16.0 * 320 + (2 + 32.0 / G) * (LB - 320)) / LB)),
+               "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                            "frac": achieved / hbm_peak, "kernel": "history kernel (INT2 split-K)",
+                            "peak_source": "measured hbm_gbs"},
+               "clocks": clk}
+        del w
+        return out
+    finally:
+        globals().update(dict(zip(("B", "HQ", "HKV", "D", "G", "L_BASE", "LB", "OUTLIERS", "CYCLE"), saved)))
+        torch.cuda.empty_cache()
+
+
+def prefill_measure(name, L0, C, reps, bf16_peak):
+    """One request's prefill chunk of C queries over an L0-token prefix
+    (oscar_prefill_attention): time per call, chunk tokens/s and the
+    attention's algorithmic tensor rate (4·d flops per (query, head, key))."""
+    import torch
+    from rotated_int2_kv_gb300 import ops, synth
+    dev = torch.device("cuda")
+    hq, hkv, d, g_ = (32, 8, 128, 64) if name == "qwen8b" else (24, 4, 256, 128)
+    cfg = ops.Config(d, hq, hkv, g_, S_SINK, W_RECENT, 0.9)
+    Rk, Rv = rotations(d)
+    L = L0 + C
+    pt = synth.page_table(SEED, 1, L, L).to(dev)
+    cache = ops.LayerCache(cfg, L, 1, Rk, Rv, device=dev)
+    scales = synth.outlier_scales(SEED, hkv, d, "fixed4")
+    for p0 in range(0, L0, 8192):
+        n = min(8192, L0 - p0)
+        k, v = synth.kv_tokens(SEED, 0, p0, n, hkv, d, scales, device=dev)
+        ops.quantize_append(cache, k, v, torch.tensor([0, n], dtype=torch.int32, device=dev),
+                            torch.tensor([p0], dtype=torch.int32, device=dev), pt)
+    k, v = synth.kv_tokens(SEED, 0, L0, C, hkv, d, scales, device=dev)
+    q = synth.queries(SEED, 5, C, hq, d, device=dev)
+    cu = torch.tensor([0, C], dtype=torch.int32, device=dev)
+    st = torch.tensor([L0], dtype=torch.int32, device=dev)
+    ws = torch.empty(ops.prefill_workspace_bytes(cfg, 1, C), dtype=torch.uint8, device=dev)
+    out = torch.empty((C, hq, d), dtype=torch.float32, device=dev)
+    for _ in range(2):
+        ops.prefill_attention(cache, q, k, v, cu, st, pt, C, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    ops.profile_enable([ops.PROF_PREFILL])
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        ops.prefill_attention(cache, q, k, v, cu, st, pt, C, out=out, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    call_ms = e0.elapsed_time(e1) / reps
+    kms, kn = ops.profile_read(ops.PROF_PREFILL)
+    ops.profile_enable(None)
+    assert ops.device_status() == 0
+    keys = C * L0 + C * (C + 1) / 2                      # (query, key) pairs per head
+    flops = 4.0 * d * hq * keys
+    kern_ms = kms / max(kn, 1)
+    tf = flops / (kern_ms / 1e3) / 1e12
+    del cache, ws, out
+    torch.cuda.empty_cache()
+    return {"workload": "%s prefill chunk: %d queries over a %d-token prefix (%d INT2 history), %d q / %d KV heads, "
+                        "d %d, group %d, batch 1" % ("Qwen3-8B-shaped" if name == "qwen8b" else "GQA-6 wide-head",
+                                                     C, L0, max(0, L0 - 320), hq, hkv, d, g_),
+            "ms_per_call": call_ms, "attention_kernel_ms": kern_ms, "chunk_tokens_per_s": C / (call_ms / 1e3),
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": tf / bf16_peak, "kernel": "prefill_attn_kernel (mma.sync f16, INT2 in place)",
+                         "peak_source": "measured bf16_tflops (f16 runs at the bf16 rate)",
+                         "flops": "4*d per (query head, key) pair, causal within the chunk"}}
+
+
 # --------------------------------------------------------------------------
 def main():
     args = parse()
@@ -360,22 +488,7 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank, ws)
         return
-    global B, HQ, HKV, D, G, L_BASE, LB, OUTLIERS, CYCLE
-    if args.workload == "small":
-        B, L_BASE = 4, 65536
-    elif args.workload == "mid":
-        B, L_BASE = 8, 100_000
-    elif args.workload == "b1-32k":
-        B, L_BASE = 1, 32_767
-    elif args.workload == "qwen32b-ragged":
-        from rotated_int2_kv_gb300 import synth
-        B, HQ, HKV, D, G = 8, 64, 8, 128, 64
-        OUTLIERS, CYCLE = "per_head", 50
-        LB = synth.ragged_lengths(SEED, B, 65_536, 131_072).astype(np.int64) - 1
-    elif args.workload == "gqa6-wide":
-        B, HQ, HKV, D, G, L_BASE = 5, 24, 4, 256, 128, 112_000
-    if args.workload != "qwen32b-ragged":
-        LB = np.full(B, L_BASE, dtype=np.int64)
+    set_workload(args.workload)
     import torch
     from rotated_int2_kv_gb300 import ops
     if not os.path.exists(ops._LIB_PATH):
@@ -471,6 +584,10 @@ def main():
         line["e2e"] = e2e_measure(w, args, ws)
     if not args.no_append:
         line["append"] = append_measure()
+    if args.shapes and args.workload == "qwen8b-100k" and ws == 1:
+        line["shapes"] = {name: shape_measure(name, 400, 5, hbm_peak) for name in ("qwen32b-ragged", "gqa6-wide")}
+        line["prefill"] = {name: prefill_measure(name, 32768, 8192, 3, float(peaks.get("bf16_tflops", 1900.0)))
+                           for name in ("qwen8b", "gqa6-wide")}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         run, L = oracle_sample(w["seed"])
         run()

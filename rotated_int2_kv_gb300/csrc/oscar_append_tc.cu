@@ -243,18 +243,23 @@ __device__ __forceinline__ float load_col(uint32_t taddr) {
 }
 
 // Exact extremes of one group for the lanes whose (s, z) y ± e could change
-// (warp-collective; out of line, so the common path stays compact).  cm0 / cm1
-// mark this lane's candidate channels (y within 2e of the computed extremes) in
-// the group's channels 0-31 / 32-63 (cm1 for groups of 64 and up; larger groups
-// pass their other chunks through `more`): the exact extremes lie among them.
-// Returns (min, max) over the exact values of the candidates.
-template <int D>
-__device__ __noinline__ float2 tc_exact_extremes(const unsigned char* sB, ExactSrc src, uint32_t cm0, uint32_t cm1,
-                                                 int ch0, int lane) {
+// (warp-collective; out of line, so the common path stays compact): the
+// extremes lie among the channels within 2e of the computed ones (y reloaded
+// from the group's tensor-memory columns tgrp), which are formed exactly.
+// Returns (min, max) over the exact values of the candidates; meaningful for
+// the uncertain lanes.
+template <int D, int G>
+__device__ __noinline__ float2 tc_exact_extremes(uint32_t tgrp, const unsigned char* sB, ExactSrc src, bool unc,
+                                                 float mn, float mx, float e2, int ch0, int lane) {
+    const float tlo = __fadd_ru(mn, e2), thi = __fsub_rd(mx, e2);
     float mne = INFINITY, mxe = -INFINITY;
 #pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
-        uint32_t cm = c ? cm1 : cm0;
+    for (int c = 0; c < G / 32; ++c) {
+        float y[32];
+        load_y(tgrp + 32 * c, y);
+        uint32_t cm = 0;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) cm |= (unc && (y[q] <= tlo || y[q] >= thi)) ? (1u << q) : 0u;
         uint32_t bal;
         while ((bal = __ballot_sync(0xffffffffu, cm != 0u)) != 0u) {
             const int L = __ffs(bal) - 1;
@@ -604,7 +609,6 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
         const int slot = m[0];
         const ExactSrc xsrc{P.recent, src_new, P.kv_dtype, m[1] >> 16, *reinterpret_cast<const int64_t*>(m + 2)};
         uint8_t* rec = P.records + ((int64_t)(slot < 0 ? 0 : slot) * P.Hkv + (m[1] & 0xFFFF)) * P.rec_bytes;
-        uint32_t words[NW];
         constexpr int NC = G / 32;                // 32-channel chunks per group
         constexpr bool kKeep = G <= 64;           // the group's y stays in registers between the passes
         // e bounds |y - fl(x·R)| on every channel of the vector (kTcBound·‖y‖₂)
@@ -624,9 +628,12 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
             e = kTcBound * sqrtf(q2.x + q2.y);
         }
         const float e2 = __fmul_ru(2.0f, e);
-#pragma unroll
+        // one group at a time (not unrolled: the loop body stays small in the
+        // instruction cache); its codes and (s, z) go to the record at its end
+#pragma unroll 1
         for (int gi = 0; gi < ng; ++gi) {
             float yk[kKeep ? NC : 1][32];
+            uint32_t words[G / 16];
             float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
@@ -637,26 +644,10 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
             // (s, z) that y ± e could change: the extremes formed exactly (out of line)
             const bool unc = sz_uncertain(mn, mx, rclip, e);
             if (__any_sync(0xffffffffu, unc)) {
-                const float tlo = __fadd_ru(mn, e2), thi = __fsub_rd(mx, e2);
-                float mne = INFINITY, mxe = -INFINITY;
-#pragma unroll
-                for (int c2 = 0; c2 < NC; c2 += 2) {
-                    uint32_t cmk[2] = {0u, 0u};
-#pragma unroll
-                    for (int h2 = 0; h2 < 2 && c2 + h2 < NC; ++h2) {
-                        if (!kKeep) load_y(tacc + gi * G + 32 * (c2 + h2), yk[0]);
-                        const float (&y)[32] = yk[kKeep ? c2 + h2 : 0];
-#pragma unroll
-                        for (int q = 0; q < 32; ++q)
-                            cmk[h2] |= (unc && (y[q] <= tlo || y[q] >= thi)) ? (1u << q) : 0u;
-                    }
-                    const float2 ex = tc_exact_extremes<D>(sB, xsrc, cmk[0], cmk[1], gi * G + 32 * c2, lane);
-                    mne = fminf(mne, ex.x);
-                    mxe = fmaxf(mxe, ex.y);
-                }
+                const float2 ex = tc_exact_extremes<D, G>(tacc + gi * G, sB, xsrc, unc, mn, mx, e2, gi * G, lane);
                 if (unc) {
-                    mn = mne;
-                    mx = mxe;
+                    mn = ex.x;
+                    mx = ex.y;
                 }
             }
             __half s16, z16;
@@ -674,8 +665,7 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
                 if (!kKeep) load_y(tacc + gi * G + 32 * c, yk[0]);
-                codes32(yk[kKeep ? c : 0], zc, r3, nb2, words[gi * (G / 16) + 2 * c], words[gi * (G / 16) + 2 * c + 1],
-                        tie);
+                codes32(yk[kKeep ? c : 0], zc, r3, nb2, words[2 * c], words[2 * c + 1], tie);
             }
             if (__any_sync(0xffffffffu, !(tie >> 31))) {
                 // a quotient near a tie: re-decide those channels by correctly rounded
@@ -683,20 +673,24 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
                     const uint2 w = tc_exact_codes<D>(tacc + gi * G + 32 * c, sB, xsrc, zc, sc, r3, nb2, be,
-                                                      make_uint2(words[gi * (G / 16) + 2 * c],
-                                                                 words[gi * (G / 16) + 2 * c + 1]),
-                                                      gi * G + 32 * c, lane);
-                    words[gi * (G / 16) + 2 * c] = w.x;
-                    words[gi * (G / 16) + 2 * c + 1] = w.y;
+                                                      make_uint2(words[2 * c], words[2 * c + 1]), gi * G + 32 * c,
+                                                      lane);
+                    words[2 * c] = w.x;
+                    words[2 * c + 1] = w.y;
                 }
             }
-            if (slot >= 0) *reinterpret_cast<__half2*>(rec + rec_off_sz + 4 * gi) = __halves2half2(s16, z16);
-        }
-        if (slot >= 0) {
+            if (slot >= 0) {
+                *reinterpret_cast<__half2*>(rec + rec_off_sz + 4 * gi) = __halves2half2(s16, z16);
+                uint8_t* dst = rec + rec_off_codes + gi * (G / 4);
+                if constexpr (G >= 64) {
 #pragma unroll
-            for (int q = 0; q < NW / 4; ++q)
-                *reinterpret_cast<uint4*>(rec + rec_off_codes + 16 * q) =
-                    make_uint4(words[4 * q], words[4 * q + 1], words[4 * q + 2], words[4 * q + 3]);
+                    for (int q = 0; q < G / 64; ++q)
+                        *reinterpret_cast<uint4*>(dst + 16 * q) =
+                            make_uint4(words[4 * q], words[4 * q + 1], words[4 * q + 2], words[4 * q + 3]);
+                } else {
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(words[0], words[1]);
+                }
+            }
         }
     }
     if (aborted && gt == 0) {                     // copies or MMAs of the slot may still run: bounded drain
