@@ -61,6 +61,13 @@ extern "C" {
 #define OSCAR_DTYPE_BF16       0
 #define OSCAR_DTYPE_F32        1
 
+/* storage of a group's (scale, zero) pair in the INT2 records */
+#define OSCAR_SCALE_F16        0  /* two fp16 values (4 bytes per group)       */
+#define OSCAR_SCALE_E4M3       1  /* two float8 E4M3 values (2 bytes per group):
+                                     2 + 16/G bits per INT2 element, the 2.28
+                                     bits per element of [OSCAR news] at G = 64
+                                     and 128K context                         */
+
 /* Shape and quantisation parameters of one attention layer.
  *  head_dim      d: 64, 128 or 256.
  *  num_q_heads   Hq; num_kv_heads Hkv; Hq % Hkv == 0, 1 <= Hq/Hkv <= 16,
@@ -73,7 +80,12 @@ extern "C" {
  *  clip_ratio    r in (0, 1]: a group's quantisation range is
  *                [r·min, r·max] of its rotated values.
  *  kv_dtype      element type of the K/V rows handed to oscar_quantize_append.
- *  q_dtype       element type of q handed to oscar_decode_attention.       */
+ *  q_dtype       element type of q handed to oscar_decode_attention.
+ *  scale_dtype   OSCAR_SCALE_F16 (zero-initialised default) or
+ *                OSCAR_SCALE_E4M3: s = rnd((hi - lo)/3) and z = rnd(lo) are
+ *                rounded to fp16, or to E4M3 (nearest, ties to even, finite
+ *                values beyond ±448 saturate to ±448); codes are decided
+ *                against the rounded pair either way.                      */
 typedef struct {
     int32_t head_dim;
     int32_t num_q_heads;
@@ -84,15 +96,21 @@ typedef struct {
     float   clip_ratio;
     int32_t kv_dtype;
     int32_t q_dtype;
+    int32_t scale_dtype;
 } oscar_config;
 
 /* Device buffers of one layer's cache (all owned by the caller).
- *  records   INT2 pool, uint8 [num_slots][Hkv][rec_bytes], rec_bytes from
- *            oscar_record_bytes().  One (slot, KV head) record is
+ *  records   INT2 pool, uint8 [num_slots][slot_bytes]: slot i holds the
+ *            records of all KV heads, head h at byte h·rec_bytes, padded
+ *            with zeros to slot_bytes (oscar_slot_bytes(), a multiple of 16;
+ *            rec_bytes from oscar_record_bytes()).  One (slot, KV head)
+ *            record is
  *              [K codes d/4 B][V codes d/4 B][K (s,z) × d/G][V (s,z) × d/G]
- *            padded with zeros to a multiple of 16 bytes.  Channel j's 2-bit
- *            code sits at bits 2·(j%4) of byte j/4; (s, z) are fp16 pairs,
- *            scale first.  Base address 16-byte aligned.
+ *            padded with zeros: to a multiple of 16 bytes with fp16 pairs
+ *            (4 bytes each), so that slot_bytes = Hkv·rec_bytes, or to a
+ *            multiple of 8 bytes with E4M3 pairs (2 bytes each).  Channel j's
+ *            2-bit code sits at bits 2·(j%4) of byte j/4; each pair is scale
+ *            first.  Base address 16-byte aligned.
  *  sink      bf16 [max_reqs][S][Hkv][2][d]   (index 0 = K, 1 = V)
  *  recent    bf16 [max_reqs][W][Hkv][2][d]   ring: position p at p % W
  *  rot_k     fp32 [d][d] row-major R_K; rot_v likewise R_V (both orthogonal).
@@ -119,12 +137,17 @@ const char* oscar_version(void);
 /* Message of the last failing call on this thread ("" if none). */
 const char* oscar_last_error(void);
 
-/* Bytes of one (slot, KV head) record: d/2 + 8·d/G rounded up to 16.
- * 80 at d=128/G=64, 144 at d=256/G=128. */
+/* Bytes of one (slot, KV head) record: d/2 + 8·d/G rounded up to 16 with fp16
+ * (s, z), d/2 + 4·d/G rounded up to 8 with E4M3.  80 / 72 at d=128, G=64;
+ * 144 / 136 at d=256, G=128. */
 int oscar_record_bytes(const oscar_config* cfg, int64_t* out /*host*/);
 
+/* Bytes of one slot of the pool (the records of all KV heads): Hkv·rec_bytes
+ * rounded up to 16.  640 (fp16) / 576 (E4M3) at d=128, G=64, 8 KV heads. */
+int oscar_slot_bytes(const oscar_config* cfg, int64_t* out /*host*/);
+
 /* Storage per cached token of one layer, all KV heads:
- *  int2_bytes  INT2 record bytes (codes + scales + padding) per history token
+ *  int2_bytes  INT2 slot bytes (codes + scales + padding) per history token
  *  bf16_bytes  BF16 bytes per sink/recent token (2·Hkv·d·2).
  * The code share alone is Hkv·d·2·0.25 bytes ([Escha log] fix 1). */
 int oscar_cache_bytes_per_token(const oscar_config* cfg, int64_t* int2_bytes /*host*/,

@@ -29,8 +29,9 @@ Sources (web pages, cited by title and section):
 
 Modules:
   rotation   -- Hadamard, bit reversal, eigenbasis, R = U·H·P_br, covariances
-  quant      -- bf16 rounding, clipped group-wise asymmetric INT2 quantiser,
-                2-bit packing, record serialisation
+  quant      -- bf16 and E4M3 rounding, clipped group-wise asymmetric INT2
+                quantiser (fp16 or E4M3 scale and zero), 2-bit packing,
+                record and slot serialisation
   cache      -- the three-region cache and its append semantics
   attention  -- exact-softmax decode attention over the mixed cache, and the
                 split/LSE merge
@@ -41,7 +42,7 @@ Modules:
 
 from .rotation import (hadamard, block_hadamard, bitrev_indices, eig_desc, build_rotation,
                        covariance, value_covariance)
-from .quant import (bf16_round, quantize_rows, dequantize_rows, pack_codes,
+from .quant import (bf16_round, e4m3_round, quantize_rows, dequantize_rows, pack_codes,
                     unpack_codes)
 from .cache import OracleConfig, OracleCache, regions
 from .attention import decode_attention, decode_attention_split
@@ -51,7 +52,7 @@ from .accounting import (code_bytes_per_token, record_bytes, bits_per_element,
 
 __all__ = [
     "hadamard", "block_hadamard", "bitrev_indices", "eig_desc", "build_rotation", "covariance",
-    "value_covariance", "bf16_round", "quantize_rows", "dequantize_rows",
+    "value_covariance", "bf16_round", "e4m3_round", "quantize_rows", "dequantize_rows",
     "pack_codes", "unpack_codes", "OracleConfig", "OracleCache", "regions",
     "decode_attention", "decode_attention_split", "prefill_attention", "code_bytes_per_token",
     "record_bytes", "bits_per_element", "window_fraction",

@@ -16,11 +16,13 @@ def code_bytes_per_token(num_layers, num_kv_heads, head_dim):
     return num_layers * num_kv_heads * head_dim * 2 * 0.25
 
 
-def record_bytes(head_dim, group_size):
-    """Bytes of one (slot, KV head) record: K and V codes, fp16 (s, z) per group, 16 B padding."""
+def record_bytes(head_dim, group_size, scale_bits=16):
+    """Bytes of one (slot, KV head) record: K and V codes and (s, z) per group;
+    fp16 pairs (scale_bits 16) padded to 16 bytes, E4M3 pairs (8) to 8 bytes."""
     ng = head_dim // group_size
-    raw = head_dim // 2 + 8 * ng
-    return (raw + 15) // 16 * 16
+    raw = head_dim // 2 + 2 * 2 * (scale_bits // 8) * ng
+    al = 16 if scale_bits == 16 else 8
+    return (raw + al - 1) // al * al
 
 
 def window_fraction(L, sink=64, recent=256):
@@ -28,11 +30,11 @@ def window_fraction(L, sink=64, recent=256):
     return min(L, sink + recent) / L
 
 
-def bits_per_element(L, group_size, sink=64, recent=256):
-    """Average stored bits per KV element at context L with fp16 scale and zero.
+def bits_per_element(L, group_size, sink=64, recent=256, scale_bits=16):
+    """Average stored bits per KV element at context L.
 
     BF16 windows cost 16 bits; an INT2 element costs 2 bits plus its share of
-    the 32 bits of fp16 (s, z) per group of G channels.
+    the 2·scale_bits bits of (s, z) per group of G channels (fp16: 32, E4M3: 16).
     """
     w = min(L, sink + recent)
-    return (16.0 * w + (2.0 + 32.0 / group_size) * (L - w)) / L
+    return (16.0 * w + (2.0 + 2.0 * scale_bits / group_size) * (L - w)) / L

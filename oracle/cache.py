@@ -30,7 +30,7 @@ from dataclasses import dataclass
 import numpy as np
 
 from .quant import (bf16_round, bf16_bits, rotate_rows, quantize_rows,
-                    dequantize_rows, pack_record, record_layout)
+                    dequantize_rows, pack_record, record_layout, slot_bytes, pack_slots)
 
 
 @dataclass
@@ -42,6 +42,7 @@ class OracleConfig:
     sink: int = 64
     recent: int = 256
     clip_ratio: float = 0.9
+    scale_fmt: str = "f16"          # "f16" or "e4m3" (s, z) storage
 
     @property
     def gqa(self):
@@ -89,8 +90,8 @@ class OracleCache:
         d, H = cfg.head_dim, cfg.num_kv_heads
         Yk = rotate_rows(Xk.reshape(n * H, d), self.rot_k)
         Yv = rotate_rows(Xv.reshape(n * H, d), self.rot_v)
-        kc, ks, kz = quantize_rows(Yk, cfg.group_size, cfg.clip_ratio)
-        vc, vs, vz = quantize_rows(Yv, cfg.group_size, cfg.clip_ratio)
+        kc, ks, kz = quantize_rows(Yk, cfg.group_size, cfg.clip_ratio, cfg.scale_fmt)
+        vc, vs, vz = quantize_rows(Yv, cfg.group_size, cfg.clip_ratio, cfg.scale_fmt)
         ng = cfg.groups
         self.kc[slots] = kc.reshape(n, H, d)
         self.vc[slots] = vc.reshape(n, H, d)
@@ -157,14 +158,24 @@ class OracleCache:
         return dequantize_rows(self.vc[slots, h], self.vs[slots, h], self.vz[slots, h])
 
     def records(self):
-        """Device byte layout of the INT2 pool: (num_slots, Hkv, rec_bytes) uint8."""
+        """Per-head records of the INT2 pool: (num_slots, Hkv, rec_bytes) uint8."""
         cfg = self.cfg
         return pack_record(self.kc, self.ks, self.kz, self.vc, self.vs, self.vz,
-                           cfg.head_dim, cfg.group_size)
+                           cfg.head_dim, cfg.group_size, cfg.scale_fmt)
+
+    def slot_records(self):
+        """Device byte layout of the INT2 pool: (num_slots, slot_bytes) uint8,
+        the records of all KV heads of a slot back to back, padded to 16 bytes."""
+        cfg = self.cfg
+        return pack_slots(self.records(), self.slot_bytes())
+
+    def slot_bytes(self):
+        cfg = self.cfg
+        return slot_bytes(cfg.head_dim, cfg.group_size, cfg.num_kv_heads, cfg.scale_fmt)
 
     def window_bits(self):
         """Device layout of the BF16 windows: (sink bits, recent bits), uint16."""
         return bf16_bits(self.sink), bf16_bits(self.ring)
 
     def record_bytes(self):
-        return record_layout(self.cfg.head_dim, self.cfg.group_size)["bytes"]
+        return record_layout(self.cfg.head_dim, self.cfg.group_size, self.cfg.scale_fmt)["bytes"]

@@ -37,7 +37,8 @@ __device__ __forceinline__ void quantize_store(const AppendParams& P, float (&y)
     const float r = P.clip;
     const int rec_off_codes = mat ? D / 4 : 0;
     const int ng = D / P.G;
-    const int rec_off_sz = D / 2 + (mat ? 4 * ng : 0);
+    const bool fp8 = P.fp8 != 0;
+    const int rec_off_sz = D / 2 + (mat ? (fp8 ? 2 : 4) * ng : 0);
     auto group_extremes = [&](float& mn, float& mx) {
         mn = y[0];
         mx = y[0];
@@ -51,7 +52,7 @@ __device__ __forceinline__ void quantize_store(const AppendParams& P, float (&y)
     float mn, mx;
     group_extremes(mn, mx);
     uint32_t exact = 0;              // channels j of this lane whose y is already the compensated one
-    const bool unc = sz_uncertain(mn, mx, r, e);
+    const bool unc = sz_uncertain(mn, mx, r, e, fp8);
     if (__any_sync(0xffffffffu, unc)) {
         // the extremes of an uncertain group lie among its channels within 2e of
         // the computed ones: form those exactly and take the extremes again
@@ -71,9 +72,8 @@ __device__ __forceinline__ void quantize_store(const AppendParams& P, float (&y)
         }
         group_extremes(mn, mx);
     }
-    __half s16, z16;
-    sz_decide(mn, mx, r, s16, z16);
-    const float s = __half2float(s16), z = __half2float(z16);
+    const SZ sz = sz_decide(mn, mx, r, fp8);
+    const float s = sz.s, z = sz.z;
     const float band = s != 0.0f ? code_band(e, __frcp_rn(3.0f * s)) : 0.0f;
     uint32_t bits = 0;
 #pragma unroll
@@ -89,7 +89,7 @@ __device__ __forceinline__ void quantize_store(const AppendParams& P, float (&y)
         const uint32_t c = s != 0.0f ? (uint32_t)fminf(fmaxf(rintf(u), 0.0f), 3.0f) : 0u;
         bits |= c << (2 * j);
     }
-    uint8_t* rec = P.records + ((int64_t)slot * P.Hkv + h) * P.rec_bytes;
+    uint8_t* rec = P.records + (int64_t)slot * P.slot_bytes + (int64_t)h * P.rec_bytes;
     if (CPL >= 4) {
 #pragma unroll
         for (int bj = 0; bj < CPL / 4; ++bj)
@@ -98,11 +98,7 @@ __device__ __forceinline__ void quantize_store(const AppendParams& P, float (&y)
         const uint32_t other = __shfl_xor_sync(0xffffffffu, bits, 1);
         if ((lane & 1) == 0) rec[rec_off_codes + lane / 2] = (uint8_t)(bits | (other << 4));
     }
-    if ((lane % lpg) == 0) {
-        const int gi = lane / lpg;
-        __half2 sz = __halves2half2(s16, z16);
-        *reinterpret_cast<__half2*>(rec + rec_off_sz + 4 * gi) = sz;
-    }
+    if ((lane % lpg) == 0) store_sz(rec, rec_off_sz, lane / lpg, sz, fp8);
 }
 
 // Σ x² of a vector, summed over the warp (lane: channels lane·CPL ..).
@@ -887,7 +883,10 @@ extern "C" int oscar_quantize_append(const oscar_config* cfg, const oscar_layer_
     P.S = cfg->sink;
     P.W = cfg->recent;
     P.G = cfg->group_size;
-    P.rec_bytes = record_layout(cfg->head_dim, cfg->group_size).bytes;
+    const RecordLayout lay = record_layout(cfg->head_dim, cfg->group_size, cfg->scale_dtype);
+    P.rec_bytes = lay.bytes;
+    P.slot_bytes = slot_bytes(lay, cfg->num_kv_heads);
+    P.fp8 = cfg->scale_dtype == OSCAR_SCALE_E4M3;
     P.clip = cfg->clip_ratio;
     P.total_new = total_new;
     P.status = status_word();

@@ -1,6 +1,8 @@
 // Shared declarations of the append kernels (quantise-on-append).
 #pragma once
 
+#include <cuda_fp8.h>
+
 #include "oscar_internal.h"
 #include "oscar_device.cuh"
 
@@ -29,6 +31,8 @@ struct AppendParams {
     int64_t num_slots;
     int max_reqs;
     int Hkv, S, W, G, rec_bytes;
+    int64_t slot_bytes;         // pool stride of one slot (all KV heads)
+    int fp8;                    // (s, z) stored as E4M3 pairs (else fp16 pairs)
     float clip;
     int64_t total_new;
     int* status;
@@ -88,13 +92,46 @@ __device__ __forceinline__ int find_request(const int* prefix, int batch, int u)
 // Oishi's Dot2: error-free products and sums carried in a second fp32 word),
 // which is faithful to the exact product, and the decision is taken on them.
 
-// The fp16 (scale, zero) of a group from its extremes, in the order the
-// quantiser defines: lo = r·min, hi = r·max, s = fp16((hi - lo)/3), z = fp16(lo).
-__device__ __forceinline__ void sz_decide(float mn, float mx, float r, __half& s16, __half& z16) {
+// Storage rounding of a scale or zero: fp16 (nearest even), or float8 E4M3
+// (nearest even, finite values beyond ±448 saturated).  Returns the stored bit
+// pattern (16 or 8 bits); both roundings are monotone in x.
+__device__ __forceinline__ uint32_t sz_bits(float x, bool fp8) {
+    return fp8 ? (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3)
+               : (uint32_t)__half_as_ushort(__float2half_rn(x));
+}
+
+// Value of a stored scale or zero (exact in fp32 for both formats).
+__device__ __forceinline__ float sz_value(uint32_t bits, bool fp8) {
+    if (fp8) {
+        const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)bits, __NV_E4M3);
+        return __half2float(__half(h));
+    }
+    return __half2float(__ushort_as_half((unsigned short)bits));
+}
+
+// A group's stored (scale, zero) from its extremes, in the order the quantiser
+// defines: lo = r·min, hi = r·max, s = rnd((hi - lo)/3), z = rnd(lo), with rnd
+// the fp16 or E4M3 rounding; returns the bit patterns and their values.
+struct SZ {
+    uint32_t sb, zb;
+    float s, z;
+};
+__device__ __forceinline__ SZ sz_decide(float mn, float mx, float r, bool fp8) {
     const float lo = __fmul_rn(r, mn);
     const float hi = __fmul_rn(r, mx);
-    s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 3.0f));
-    z16 = __float2half_rn(lo);
+    SZ o;
+    o.sb = sz_bits(__fdiv_rn(__fsub_rn(hi, lo), 3.0f), fp8);
+    o.zb = sz_bits(lo, fp8);
+    o.s = sz_value(o.sb, fp8);
+    o.z = sz_value(o.zb, fp8);
+    return o;
+}
+
+// Writes the pair of group gi at byte `off` of a record: fp16 pairs (4 bytes,
+// 4-byte aligned) or E4M3 pairs (2 bytes, 2-byte aligned), scale first.
+__device__ __forceinline__ void store_sz(uint8_t* rec, int off, int gi, const SZ& v, bool fp8) {
+    if (fp8) *reinterpret_cast<uint16_t*>(rec + off + 2 * gi) = (uint16_t)(v.sb | (v.zb << 8));
+    else *reinterpret_cast<uint32_t*>(rec + off + 4 * gi) = v.sb | (v.zb << 16);
 }
 
 // True when extremes anywhere in [mn - e, mn + e] × [mx - e, mx + e] could give
@@ -102,16 +139,16 @@ __device__ __forceinline__ void sz_decide(float mn, float mx, float r, __half& s
 // at any point of that box lie in intervals bounded with directed rounding:
 // lo in [rd(r·(mn - e)), ru(r·(mn + e))], and (hi - lo)/3 in
 // [rd((rd(r·(mx - e)) - ru(r·(mn + e)))·⅓↓), ru((ru(r·(mx + e)) - rd(r·(mn - e)))·⅓↑)];
-// the decision is certain when both ends of each interval round to the same fp16.
-__device__ __forceinline__ bool sz_uncertain(float mn, float mx, float r, float e) {
+// the decision is certain when both ends of each interval round to the same
+// stored value (fp16 or E4M3).
+__device__ __forceinline__ bool sz_uncertain(float mn, float mx, float r, float e, bool fp8) {
     constexpr float kThirdDn = 0.333333313465118408203125f;   // the fp32 neighbours of 1/3
     constexpr float kThirdUp = 0.3333333432674407958984375f;
     const float lo_a = __fmul_rd(r, __fsub_rd(mn, e)), lo_b = __fmul_ru(r, __fadd_ru(mn, e));
     const float hi_a = __fmul_rd(r, __fsub_rd(mx, e)), hi_b = __fmul_ru(r, __fadd_ru(mx, e));
     const float s_a = __fmul_rd(__fsub_rd(hi_a, lo_b), kThirdDn);
     const float s_b = __fmul_ru(__fsub_ru(hi_b, lo_a), kThirdUp);
-    return __half_as_ushort(__float2half_rn(lo_a)) != __half_as_ushort(__float2half_rn(lo_b)) ||
-           __half_as_ushort(__float2half_rn(fmaxf(s_a, 0.0f))) != __half_as_ushort(__float2half_rn(s_b));
+    return sz_bits(lo_a, fp8) != sz_bits(lo_b, fp8) || sz_bits(fmaxf(s_a, 0.0f), fp8) != sz_bits(s_b, fp8);
 }
 
 // Half-width in units of the quotient u = (y - z)/s of the band around a

@@ -408,7 +408,8 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
     const bool vec_in = (reinterpret_cast<uintptr_t>(src_new) & 15) == 0;
     const float rclip = P.clip;
     const int rec_off_codes = mat ? D / 4 : 0;
-    const int rec_off_sz = D / 2 + (mat ? 4 * ng : 0);
+    const bool fp8 = P.fp8 != 0;
+    const int rec_off_sz = D / 2 + (mat ? (fp8 ? 2 : 4) * ng : 0);
     unsigned char* A = sA + e * C::A_BYTES;
     int* gmeta = meta + e * 2 * kTcRows * kMetaInts;
     uint64_t* bar = &bars[e];
@@ -608,7 +609,7 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
         const int* m = gmeta + (buf * kTcRows + gt) * kMetaInts;
         const int slot = m[0];
         const ExactSrc xsrc{P.recent, src_new, P.kv_dtype, m[1] >> 16, *reinterpret_cast<const int64_t*>(m + 2)};
-        uint8_t* rec = P.records + ((int64_t)(slot < 0 ? 0 : slot) * P.Hkv + (m[1] & 0xFFFF)) * P.rec_bytes;
+        uint8_t* rec = P.records + (int64_t)(slot < 0 ? 0 : slot) * P.slot_bytes + (int64_t)(m[1] & 0xFFFF) * P.rec_bytes;
         constexpr int NC = G / 32;                // 32-channel chunks per group
         constexpr bool kKeep = G <= 64;           // the group's y stays in registers between the passes
         // e bounds |y - fl(x·R)| on every channel of the vector (kTcBound·‖y‖₂)
@@ -642,7 +643,7 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
                 minmax32(y, mn, mx);
             }
             // (s, z) that y ± e could change: the extremes formed exactly (out of line)
-            const bool unc = sz_uncertain(mn, mx, rclip, e);
+            const bool unc = sz_uncertain(mn, mx, rclip, e, fp8);
             if (__any_sync(0xffffffffu, unc)) {
                 const float2 ex = tc_exact_extremes<D, G>(tacc + gi * G, sB, xsrc, unc, mn, mx, e2, gi * G, lane);
                 if (unc) {
@@ -650,12 +651,11 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
                     mx = ex.y;
                 }
             }
-            __half s16, z16;
-            sz_decide(mn, mx, rclip, s16, z16);
-            const float sc = __half2float(s16), zc = __half2float(z16);
+            const SZ sz = sz_decide(mn, mx, rclip, fp8);
+            const float sc = sz.s, zc = sz.z;
             // tcgen05.ld is warp-collective: every lane runs the same loads.  A flat
             // group (s = 0) takes r3 = 0, so its fast-path codes are all 0.
-            const float r3 = sc != 0.0f ? __frcp_rn(3.0f * sc) : 0.0f;   // 3·sc is exact (11-bit significand × 3)
+            const float r3 = sc != 0.0f ? __frcp_rn(3.0f * sc) : 0.0f;   // 3·sc is exact (≤ 11-bit significand × 3)
             // a code is certain when its quotient is farther from a half-integer than
             // e/s plus the reciprocal path's 2^-21
             const float be = code_band(e, r3);
@@ -680,9 +680,13 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
                 }
             }
             if (slot >= 0) {
-                *reinterpret_cast<__half2*>(rec + rec_off_sz + 4 * gi) = __halves2half2(s16, z16);
+                store_sz(rec, rec_off_sz, gi, sz, fp8);
                 uint8_t* dst = rec + rec_off_codes + gi * (G / 4);
-                if constexpr (G >= 64) {
+                if (fp8) {   // E4M3 records start on 8-byte boundaries
+#pragma unroll
+                    for (int q = 0; q < G / 32; ++q)
+                        *reinterpret_cast<uint2*>(dst + 8 * q) = make_uint2(words[2 * q], words[2 * q + 1]);
+                } else if constexpr (G >= 64) {
 #pragma unroll
                     for (int q = 0; q < G / 64; ++q)
                         *reinterpret_cast<uint4*>(dst + 16 * q) =

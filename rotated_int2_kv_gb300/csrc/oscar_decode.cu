@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(512) history_simt_kernel(DecodeParams P) {
                     }
                 }
                 const bool use = valid && slot >= 0;
-                const uint8_t* rec = P.records + ((int64_t)(use ? slot : 0) * P.Hkv + hk) * P.rec_bytes;
+                const uint8_t* rec = P.records + (int64_t)(use ? slot : 0) * P.slot_bytes + (int64_t)hk * P.rec_bytes;
                 // ---- logits, lane = token ----
                 float logit[GQ];
 #pragma unroll
@@ -316,8 +316,8 @@ __global__ void __launch_bounds__(512) history_simt_kernel(DecodeParams P) {
                                 }
                             }
                         }
-                        const __half2 sz = *reinterpret_cast<const __half2*>(rec + D / 2 + 4 * gi);
-                        const float s = __low2float(sz), z = __high2float(sz);
+                        const float2 sz = load_sz(rec + D / 2, gi, P.fp8);
+                        const float s = sz.x, z = sz.y;
 #pragma unroll
                         for (int j = 0; j < GQ; ++j) {
                             if (j < P.g) {
@@ -358,13 +358,13 @@ __global__ void __launch_bounds__(512) history_simt_kernel(DecodeParams P) {
                 for (int t = 0; t < ntok; ++t) {
                     const int st = __shfl_sync(0xffffffffu, use ? slot : -1, t);
                     if (st < 0) continue;
-                    const uint8_t* rt = P.records + ((int64_t)st * P.Hkv + hk) * P.rec_bytes;
+                    const uint8_t* rt = P.records + (int64_t)st * P.slot_bytes + (int64_t)hk * P.rec_bytes;
                     uint32_t bits;
                     if (CPL == 8) bits = *reinterpret_cast<const uint16_t*>(rt + D / 4 + lane * 2);
                     else if (CPL == 4) bits = rt[D / 4 + lane];
                     else bits = (rt[D / 4 + lane / 2] >> (4 * (lane & 1))) & 0xFu;
-                    const __half2 sz = *reinterpret_cast<const __half2*>(rt + D / 2 + 4 * ng + 4 * my_gi);
-                    const float s = __low2float(sz), z = __high2float(sz);
+                    const float2 sz = load_sz(rt + D / 2 + (P.fp8 ? 2 : 4) * ng, my_gi, P.fp8);
+                    const float s = sz.x, z = sz.y;
                     float cf[CPL];
 #pragma unroll
                     for (int c = 0; c < CPL; ++c) cf[c] = (float)((bits >> (2 * c)) & 3u);
@@ -1241,7 +1241,10 @@ static int decode_impl(const oscar_config* cfg, const oscar_layer_cache* cache, 
     P.W = cfg->recent;
     P.G = cfg->group_size;
     P.ng = cfg->head_dim / cfg->group_size;
-    P.rec_bytes = record_layout(cfg->head_dim, cfg->group_size).bytes;
+    const RecordLayout lay = record_layout(cfg->head_dim, cfg->group_size, cfg->scale_dtype);
+    P.rec_bytes = lay.bytes;
+    P.slot_bytes = slot_bytes(lay, cfg->num_kv_heads);
+    P.fp8 = cfg->scale_dtype == OSCAR_SCALE_E4M3;
     P.chunk = plan.chunk;
     P.n_ctas = plan.max_ctas;          // set by the history launcher
     P.par = 1;                         // set by the tensor-core history launcher

@@ -87,6 +87,8 @@ struct DecodeParams {
     int64_t num_slots;
     int max_reqs;
     int Hq, Hkv, g, S, W, G, ng, rec_bytes;
+    int64_t slot_bytes;  // pool stride of one slot (all KV heads)
+    int fp8;           // (s, z) stored as E4M3 pairs (else fp16 pairs)
     int chunk, n_frag_tiles, n_win_tiles;
     int n_ctas;        // history grid actually launched (<= plan.max_ctas)
     int par;           // partial slots per (CTA, request): stage parities of the history kernel

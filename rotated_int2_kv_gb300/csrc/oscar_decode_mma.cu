@@ -177,8 +177,9 @@ struct StageIter {
 };
 
 // D: head_dim; G: group size; NT: n8 tiles of (head, hi/lo) columns; WPH:
-// warps per head along channels (2 for d = 256); TTOK: tokens per stage.
-template <int D, int G, int NT, int WPH, int TTOK>
+// warps per head along channels (2 for d = 256); TTOK: tokens per stage; FP8:
+// (s, z) stored as E4M3 pairs (2 bytes) instead of fp16 pairs (4 bytes).
+template <int D, int G, int NT, int WPH, int TTOK, bool FP8>
 struct MmaCfg {
     static constexpr int kSliceCh = D / WPH;        // channels per warp
     static constexpr int kKS = kSliceCh / 16;       // k-steps (words of 16 codes) per warp
@@ -186,7 +187,9 @@ struct MmaCfg {
     static constexpr int kMT = kSliceCh / 16;       // P·V m-tiles per warp
     static constexpr int kMTG = G / 16;             // m-tiles per group
     static constexpr int kMQ = TTOK / 16;           // 16-token sub-tiles per stage
-    static constexpr int REC = (D / 2 + 8 * (D / G) + 15) / 16 * 16;   // record bytes per (slot, head)
+    static constexpr int PB = FP8 ? 2 : 4;                              // bytes per (s, z) pair
+    static constexpr int RAL = FP8 ? 8 : 16;                            // record alignment
+    static constexpr int REC = (D / 2 + 2 * PB * (D / G) + RAL - 1) / RAL * RAL;   // record bytes per (slot, head)
     static constexpr int NG = D / G;
     static constexpr int NR = 2 * kMQ;              // token rows per thread per stage
     static constexpr int XCH = WPH == 2 ? 2 * 2 * 32 * NT * NR : 0;   // logit exchange floats per head
@@ -201,7 +204,11 @@ struct MmaCfg {
     static_assert(G <= kSliceCh, "a warp's channel slice must hold whole groups");
     static_assert(G >= 32, "group size below 32 has no fast path");
     static_assert(TTOK == 32 || TTOK == 64, "stages of 32 or 64 tokens");
+    static_assert(G >= 64 || REC % 16 == 0, "the group-32 K path reads 16-byte words of a record");
 };
+
+// Bytes of one pool slot (the records of all KV heads, padded to 16).
+__host__ __device__ constexpr int slot_bytes_of(int hkv, int rec) { return (hkv * rec + 15) / 16 * 16; }
 
 // Shared-memory layout (byte offsets): [0, 64) full[8] and [64, 128) empty[8]
 // mbarriers; [128, 256) stage validity masks, two 64-bit words per ring slot;
@@ -212,14 +219,14 @@ constexpr int kSmemMask = 128, kSmemAbort = 256, kSmemTab = 384;
 // HKV > 0 fixes the KV head count (and so the stage row stride) at compile time.
 // HP splits a KV head's query group over HP warps (query heads 4·NT·hp ..),
 // each carrying NT n8 column tiles.
-template <int D, int G, int NT, int WPH, int TTOK, int PAR, int HKV, int HP>
+template <int D, int G, int NT, int WPH, int TTOK, int PAR, int HKV, int HP, bool FP8>
 __global__ void __launch_bounds__(256 * PAR * HP, 1)
 history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_log2) {
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     using namespace mma_detail;
-    using C = MmaCfg<D, G, NT, WPH, TTOK>;
+    using C = MmaCfg<D, G, NT, WPH, TTOK, FP8>;
     constexpr int KS = C::kKS, GW = C::kGW, MT = C::kMT, MTG = C::kMTG, MQ = C::kMQ;
-    constexpr int REC = C::REC, NG = C::NG, TT = TTOK, NR = C::NR;
+    constexpr int REC = C::REC, NG = C::NG, TT = TTOK, NR = C::NR, PB = C::PB;
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int Hkv = HKV > 0 ? HKV : P.Hkv;
@@ -233,8 +240,8 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
     const int r = lane >> 2, j = lane & 3;
     const int g = P.g;
     const uint32_t NS = 1u << ns_log2;
-    const int row = HKV > 0 ? row_bytes(HKV * REC) : trow;   // stage row stride of one token (all heads)
-    const int tok_bytes = Hkv * REC;
+    const int row = HKV > 0 ? row_bytes(slot_bytes_of(HKV, REC)) : trow;   // stage row stride of one token (all heads)
+    const int tok_bytes = slot_bytes_of(Hkv, REC);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + 8;
     uint64_t* vmw = reinterpret_cast<uint64_t*>(smem + kSmemMask);      // [8 slots][2] validity masks
@@ -309,10 +316,10 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         unsigned char* dst = stages + s * stage_bytes;
         // 16-byte cp.async of whole token records, completing on the stage's full
         // barrier through every thread's no-increment arrival
-        if constexpr (HKV > 0 && (HKV * REC) % 128 == 0 && TT == 64) {
+        if constexpr (HKV > 0 && slot_bytes_of(HKV, REC) % 128 == 0 && TT == 64) {
             // 8 tokens per warp: lane l copies chunks (l & 7) + 8u of tokens
             // tbeg + (l >> 3) and tbeg + 4 + (l >> 3) (4 records per instruction)
-            constexpr int kTB = HKV * REC;
+            constexpr int kTB = slot_bytes_of(HKV, REC);
             const int sa = ok0 ? nsl0 : -1;
 #pragma unroll
             for (int v = 0; v < 2; ++v) {
@@ -324,6 +331,21 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
 #pragma unroll
                     for (int u = 0; u < kTB / 128; ++u) cp_async16(d + 128 * u, src + 128 * u);
                 }
+            }
+        } else if constexpr (HKV > 0 && TT == 64 && (TT + HKV * WPH * HP - 1) / (HKV * WPH * HP) <= 32) {
+            // compile-time slot size: the (token, 16-byte chunk) pairs of the warp's
+            // tokens (at most 32, all in nsl0) flattened over the lanes, so every
+            // instruction moves 32 chunks
+            constexpr int kCh = slot_bytes_of(HKV, REC) / 16;
+            constexpr int kTpw = (TT + HKV * WPH * HP - 1) / (HKV * WPH * HP);   // = tpw
+            const int sa = ok0 ? nsl0 : -1;
+            const int nch = (tend - tbeg) * kCh;
+#pragma unroll
+            for (int c = lane; c < ((kTpw * kCh + 31) & ~31); c += 32) {
+                const int tt = c / kCh, ch = c - tt * kCh;
+                const int sl = __shfl_sync(0xffffffffu, sa, tt & 31);
+                if (c < nch && sl >= 0)
+                    cp_async16(dst + (tbeg + tt) * row + 16 * ch, P.records + (int64_t)sl * (kCh * 16) + 16 * ch);
             }
         } else {
             // any shape: the warp's tokens one at a time, lanes over 16-byte chunks
@@ -508,7 +530,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
 #pragma unroll
                         for (int gi = 0; gi < GW; ++gi) {
                             const int gg = wsl * GW + gi;
-                            const float2 sz = h2f(*reinterpret_cast<const uint32_t*>(tb + t * row + D / 2 + 4 * gg));
+                            const float2 sz = load_sz(tb + t * row + D / 2, gg, FP8);
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
                                 ts[nt] = fmaf(sz.x, sc[mb][gi][nt][2 * hf] + sc[mb][gi][nt][2 * hf + 1], ts[nt]);
@@ -523,7 +545,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
 #pragma unroll
                         for (int gi = 0; gi < GW; ++gi) {
                             const int gg = wsl * GW + gi;
-                            const float2 sz = h2f(*reinterpret_cast<const uint32_t*>(tb + t * row + D / 2 + 4 * gg));
+                            const float2 sz = load_sz(tb + t * row + D / 2, gg, FP8);
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
                                 const float2 Q = qs[nt][gi];       // (Σ q̃, Σ q̃/α)
@@ -601,8 +623,7 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
 #pragma unroll
                     for (int gi = 0; gi < GW; ++gi) {
                         // rows of invalid tokens hold finite stale data and get p = 0
-                        const float2 sz = h2f(*reinterpret_cast<const uint32_t*>(
-                            tb + t * row + D / 2 + 4 * (NG + wsl * GW + gi)));
+                        const float2 sz = load_sz(tb + t * row + D / 2 + PB * NG, wsl * GW + gi, FP8);
                         w[gi] = pv * sz.x;
                         Zsum[nt][gi] = fmaf(pv, sz.y, Zsum[nt][gi]);
                     }
@@ -781,15 +802,15 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
 
 // Shared-memory plan: (x_off, stages_off, ring depth log2, total bytes); false if it
 // does not fit.  Two stage parities need at least 4 stages (2 in flight).
-template <int D, int G, int NT, int WPH, int TTOK, int PAR, int HP>
+template <int D, int G, int NT, int WPH, int TTOK, int PAR, int HP, bool FP8>
 static bool mma_smem_plan(int Hkv, int* x_off, int* stages_off, int* ns_log2, size_t* total) {
-    using C = MmaCfg<D, G, NT, WPH, TTOK>;
+    using C = MmaCfg<D, G, NT, WPH, TTOK, FP8>;
     const int nwarps = Hkv * WPH * PAR * HP;
     // named barriers 1 .. Hkv·HP·PAR pair the channel-slice warps (ids up to 15)
     if (WPH == 2 && Hkv * HP * PAR > 15) return false;
     *x_off = kSmemTab + nwarps * C::TBL;
     *stages_off = (*x_off + Hkv * HP * PAR * C::XCH * 4 + 127) / 128 * 128;
-    const size_t stage = (size_t)TTOK * row_bytes(Hkv * C::REC);
+    const size_t stage = (size_t)TTOK * row_bytes(slot_bytes_of(Hkv, C::REC));
     int lg = 3;                                  // 8 stages when they fit, else 4, else 2
     while (lg > PAR && *stages_off + (stage << lg) > 224 * 1024) --lg;
     *ns_log2 = lg;
@@ -797,26 +818,27 @@ static bool mma_smem_plan(int Hkv, int* x_off, int* stages_off, int* ns_log2, si
     return *total <= 225 * 1024;
 }
 
-template <int D, int G, int NT, int WPH, int TTOK, int PAR, int HKV, int HP>
+template <int D, int G, int NT, int WPH, int TTOK, int PAR, int HKV, int HP, bool FP8>
 static int launch_mma(DecodeParams P, cudaStream_t st) {
     const int threads = 32 * P.Hkv * WPH * PAR * HP;
     int x_off, stages_off, ns_log2;
     size_t smem;
-    if (!mma_smem_plan<D, G, NT, WPH, TTOK, PAR, HP>(P.Hkv, &x_off, &stages_off, &ns_log2, &smem))
+    if (!mma_smem_plan<D, G, NT, WPH, TTOK, PAR, HP, FP8>(P.Hkv, &x_off, &stages_off, &ns_log2, &smem))
         return OSCAR_ERR_ARG;
-    auto kern = history_mma_kernel<D, G, NT, WPH, TTOK, PAR, HKV, HP>;
+    auto kern = history_mma_kernel<D, G, NT, WPH, TTOK, PAR, HKV, HP, FP8>;
     if (const int rc_ = ensure_dynamic_smem((const void*)kern, smem, "cudaFuncSetAttribute(history_mma_kernel)"))
         return rc_;
     const int grid = std::min(P.n_ctas, sm_count());
-    const int trow = row_bytes(P.Hkv * MmaCfg<D, G, NT, WPH, TTOK>::REC);
+    const int trow = row_bytes(slot_bytes_of(P.Hkv, MmaCfg<D, G, NT, WPH, TTOK, FP8>::REC));
     launch_dependent(kern, dim3(grid), dim3(threads), smem, st, P, x_off, stages_off, trow, ns_log2);
     return check_cuda("history_mma_kernel launch");
 }
 
-// Chooses the tensor-core kernel for the shape, or reports that none fits
-// (the caller then runs the CUDA-core kernel).  P.n_ctas is updated to the
-// grid that was launched.
-int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* launched) {
+// Chooses the tensor-core kernel for the shape and (s, z) format, or reports
+// that none fits (the caller then runs the CUDA-core kernel).  P.n_ctas is
+// updated to the grid that was launched.
+template <bool FP8>
+static int launch_history_mma_fmt(DecodeParams& P, int head_dim, cudaStream_t st, bool* launched) {
     *launched = false;
     if (P.Hkv > (head_dim == 256 ? 4 : 8) || P.g > 8) return OSCAR_OK;
     const int nt = (2 * P.g + 7) / 8;
@@ -833,7 +855,8 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
         *launched = true;
     };
 #define OSCAR_MMA_X(D_, G_, NT_, WPH_, TT_, PAR_, HKV_, HP_) \
-    go(mma_smem_plan<D_, G_, NT_, WPH_, TT_, PAR_, HP_>, launch_mma<D_, G_, NT_, WPH_, TT_, PAR_, HKV_, HP_>, PAR_, HKV_, \
+    go(mma_smem_plan<D_, G_, NT_, WPH_, TT_, PAR_, HP_, FP8>, launch_mma<D_, G_, NT_, WPH_, TT_, PAR_, HKV_, HP_, FP8>, \
+       PAR_, HKV_, \
        WPH_ * PAR_ * HP_)
 #define OSCAR_MMA_H(D_, G_, NT_, WPH_, TT_, PAR_, HKV_) OSCAR_MMA_X(D_, G_, NT_, WPH_, TT_, PAR_, HKV_, 1)
 #define OSCAR_MMA(D_, G_, NT_, WPH_, TT_, PAR_) OSCAR_MMA_H(D_, G_, NT_, WPH_, TT_, PAR_, 0)
@@ -869,6 +892,11 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
 #undef OSCAR_MMA_X
     if (*launched) P.n_ctas = std::min(P.n_ctas, sm_count());
     return rc;
+}
+
+int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* launched) {
+    return P.fp8 ? launch_history_mma_fmt<true>(P, head_dim, st, launched)
+                 : launch_history_mma_fmt<false>(P, head_dim, st, launched);
 }
 
 }  // namespace oscar

@@ -58,6 +58,8 @@ int validate_config(const oscar_config* cfg) {
         return fail(OSCAR_ERR_ARG, "kv_dtype must be OSCAR_DTYPE_BF16 or OSCAR_DTYPE_F32");
     if (cfg->q_dtype != OSCAR_DTYPE_BF16 && cfg->q_dtype != OSCAR_DTYPE_F32)
         return fail(OSCAR_ERR_ARG, "q_dtype must be OSCAR_DTYPE_BF16 or OSCAR_DTYPE_F32");
+    if (cfg->scale_dtype != OSCAR_SCALE_F16 && cfg->scale_dtype != OSCAR_SCALE_E4M3)
+        return fail(OSCAR_ERR_ARG, "scale_dtype must be OSCAR_SCALE_F16 or OSCAR_SCALE_E4M3");
     return OSCAR_OK;
 }
 
@@ -169,7 +171,16 @@ int oscar_record_bytes(const oscar_config* cfg, int64_t* out) {
     int rc = validate_config(cfg);
     if (rc) return rc;
     if (!out) return fail(OSCAR_ERR_NULL, "out is NULL");
-    *out = record_layout(cfg->head_dim, cfg->group_size).bytes;
+    *out = record_layout(cfg->head_dim, cfg->group_size, cfg->scale_dtype).bytes;
+    return OSCAR_OK;
+}
+
+int oscar_slot_bytes(const oscar_config* cfg, int64_t* out) {
+    clear_error();
+    int rc = validate_config(cfg);
+    if (rc) return rc;
+    if (!out) return fail(OSCAR_ERR_NULL, "out is NULL");
+    *out = slot_bytes(record_layout(cfg->head_dim, cfg->group_size, cfg->scale_dtype), cfg->num_kv_heads);
     return OSCAR_OK;
 }
 
@@ -178,7 +189,7 @@ int oscar_cache_bytes_per_token(const oscar_config* cfg, int64_t* int2_bytes, in
     int rc = validate_config(cfg);
     if (rc) return rc;
     if (!int2_bytes || !bf16_bytes) return fail(OSCAR_ERR_NULL, "output pointer is NULL");
-    *int2_bytes = (int64_t)cfg->num_kv_heads * record_layout(cfg->head_dim, cfg->group_size).bytes;
+    *int2_bytes = slot_bytes(record_layout(cfg->head_dim, cfg->group_size, cfg->scale_dtype), cfg->num_kv_heads);
     *bf16_bytes = (int64_t)cfg->num_kv_heads * 2 * cfg->head_dim * 2;
     return OSCAR_OK;
 }

@@ -12,24 +12,30 @@
 namespace oscar {
 
 // Record geometry of one (slot, KV head) entry of the INT2 pool:
-// [K codes d/4][V codes d/4][K (s,z) fp16 pairs x d/G][V (s,z) x d/G], padded to 16.
+// [K codes d/4][V codes d/4][K (s,z) pairs x d/G][V (s,z) x d/G]; fp16 pairs
+// (4 B) padded to 16 bytes, E4M3 pairs (2 B) padded to 8.  A slot holds the
+// records of all KV heads back to back (head h at h·bytes), padded to 16.
 struct RecordLayout {
-    int d, G, ng;
+    int d, G, ng, pair;
     int k_codes, v_codes, k_sz, v_sz, bytes;
 };
 
-inline RecordLayout record_layout(int d, int G) {
+inline RecordLayout record_layout(int d, int G, int scale_dtype) {
     RecordLayout r;
     r.d = d;
     r.G = G;
     r.ng = d / G;
+    r.pair = scale_dtype == OSCAR_SCALE_E4M3 ? 2 : 4;
     r.k_codes = 0;
     r.v_codes = d / 4;
     r.k_sz = d / 2;
-    r.v_sz = d / 2 + 4 * r.ng;
-    r.bytes = (d / 2 + 8 * r.ng + 15) / 16 * 16;
+    r.v_sz = d / 2 + r.pair * r.ng;
+    const int al = scale_dtype == OSCAR_SCALE_E4M3 ? 8 : 16;
+    r.bytes = (d / 2 + 2 * r.pair * r.ng + al - 1) / al * al;
     return r;
 }
+
+inline int64_t slot_bytes(const RecordLayout& r, int Hkv) { return ((int64_t)Hkv * r.bytes + 15) / 16 * 16; }
 
 // Thread-local error message; returns `code` for convenient `return fail(...)`.
 int fail(int code, const char* fmt, ...);

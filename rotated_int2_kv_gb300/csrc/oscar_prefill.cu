@@ -65,6 +65,8 @@ struct PrefillParams {
     int64_t num_slots;
     int max_reqs;
     int Hq, Hkv, g, S, W, G, ng, rec_bytes;
+    int64_t slot_bytes;   // pool stride of one slot (all KV heads)
+    int fp8;              // (s, z) stored as E4M3 pairs (else fp16 pairs)
     float qscale;
     // workspace
     __half* qh;       // [total_q][Hq][d] fp16 hi part of q̃
@@ -366,7 +368,8 @@ __global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(PrefillParams 
     };
 
     // ---- history tiles: INT2 records of KV head hk ----
-    const int rec_v = D / 4, rec_ks = D / 2, rec_vs = D / 2 + 4 * NG;
+    const bool fp8 = P.fp8 != 0;
+    const int rec_v = D / 4, rec_ks = D / 2, rec_vs = D / 2 + (fp8 ? 2 : 4) * NG;
     for (int t0 = S; t0 < hist_hi; t0 += TT) {
         const int nt = min(TT, hist_hi - t0);
         __syncthreads();                               // the previous tile's readers are done
@@ -380,7 +383,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(PrefillParams 
             if (tt < nt) {
                 const int sl = P.page_table[(int64_t)b * P.pt_stride + t0 + tt];
                 okt = sl >= 0 && sl < P.num_slots;
-                if (okt) rec = P.records + ((int64_t)sl * P.Hkv + hk) * P.rec_bytes;
+                if (okt) rec = P.records + (int64_t)sl * P.slot_bytes + (int64_t)hk * P.rec_bytes;
                 else if (mat == 0 && cc == 0) set_status(P.status, OSCAR_DEV_BAD_SLOT);
             }
             if (okt) {
@@ -395,7 +398,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(PrefillParams 
             if ((8 * cc) % G == 0) {                   // the group's (s, z): zero for invalid tokens
                 const int gi = (8 * cc) / G;
                 float2 sz = make_float2(0.f, 0.f);
-                if (okt) sz = __half22float2(*reinterpret_cast<const __half2*>(rec + (mat ? rec_vs : rec_ks) + 4 * gi));
+                if (okt) sz = load_sz(rec + (mat ? rec_vs : rec_ks), gi, fp8);
                 sSZ[(2 * mat) * TT * NG + tt * NG + gi] = sz.x;
                 sSZ[(2 * mat + 1) * TT * NG + tt * NG + gi] = sz.y;
             }
@@ -714,7 +717,10 @@ extern "C" int oscar_prefill_attention(const oscar_config* cfg, const oscar_laye
     P.W = cfg->recent;
     P.G = cfg->group_size;
     P.ng = cfg->head_dim / cfg->group_size;
-    P.rec_bytes = record_layout(cfg->head_dim, cfg->group_size).bytes;
+    const RecordLayout lay = record_layout(cfg->head_dim, cfg->group_size, cfg->scale_dtype);
+    P.rec_bytes = lay.bytes;
+    P.slot_bytes = slot_bytes(lay, cfg->num_kv_heads);
+    P.fp8 = cfg->scale_dtype == OSCAR_SCALE_E4M3;
     P.qscale = (float)(1.4426950408889634 / std::sqrt((double)cfg->head_dim));
     char* ws = static_cast<char*>(workspace);
     P.qh = reinterpret_cast<__half*>(ws + plan.off_qh);

@@ -20,6 +20,8 @@ ERR_NAMES = {-1: "OSCAR_ERR_ARG", -2: "OSCAR_ERR_NULL", -3: "OSCAR_ERR_WORKSPACE
              -4: "OSCAR_ERR_CUDA", -5: "OSCAR_ERR_NUMERIC"}
 DTYPE_BF16 = 0
 DTYPE_F32 = 1
+SCALE_F16 = 0     # (s, z) stored as fp16 pairs
+SCALE_E4M3 = 1    # (s, z) stored as float8 E4M3 pairs
 DEV_BAD_SLOT, DEV_BAD_LEN, DEV_BAD_REQ, DEV_TIMEOUT = 1, 2, 4, 8
 
 
@@ -34,7 +36,7 @@ class CConfig(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("group_size", ctypes.c_int32),
                 ("sink", ctypes.c_int32), ("recent", ctypes.c_int32),
                 ("clip_ratio", ctypes.c_float), ("kv_dtype", ctypes.c_int32),
-                ("q_dtype", ctypes.c_int32)]
+                ("q_dtype", ctypes.c_int32), ("scale_dtype", ctypes.c_int32)]
 
 
 class CLayerCache(ctypes.Structure):
@@ -50,6 +52,7 @@ _SIGS = {
     "oscar_version": ([], ctypes.c_char_p),
     "oscar_last_error": ([], ctypes.c_char_p),
     "oscar_record_bytes": ([ctypes.POINTER(CConfig), ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+    "oscar_slot_bytes": ([ctypes.POINTER(CConfig), ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
     "oscar_cache_bytes_per_token": ([ctypes.POINTER(CConfig), ctypes.POINTER(ctypes.c_int64),
                                      ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
     "oscar_covariance": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
@@ -136,6 +139,7 @@ class Config:
     clip_ratio: float = 0.9
     kv_dtype: torch.dtype = torch.bfloat16
     q_dtype: torch.dtype = torch.bfloat16
+    scale_fmt: str = "f16"          # "f16" or "e4m3": storage of each group's (s, z)
 
     def c(self):
         def code(dt):
@@ -144,9 +148,11 @@ class Config:
             if dt == torch.float32:
                 return DTYPE_F32
             raise ValueError("dtype must be torch.bfloat16 or torch.float32")
+        if self.scale_fmt not in ("f16", "e4m3"):
+            raise ValueError("scale_fmt must be 'f16' or 'e4m3'")
         return CConfig(self.head_dim, self.num_q_heads, self.num_kv_heads, self.group_size,
                        self.sink, self.recent, self.clip_ratio, code(self.kv_dtype),
-                       code(self.q_dtype))
+                       code(self.q_dtype), SCALE_E4M3 if self.scale_fmt == "e4m3" else SCALE_F16)
 
     @property
     def gqa(self):
@@ -160,6 +166,12 @@ def version():
 def record_bytes(cfg):
     out = ctypes.c_int64()
     _check(lib().oscar_record_bytes(ctypes.byref(cfg.c()), ctypes.byref(out)))
+    return out.value
+
+
+def slot_bytes(cfg):
+    out = ctypes.c_int64()
+    _check(lib().oscar_slot_bytes(ctypes.byref(cfg.c()), ctypes.byref(out)))
     return out.value
 
 
@@ -251,19 +263,35 @@ def value_covariance_device(scores, values, stream=None):
 # -- device cache -------------------------------------------------------------
 
 class LayerCache:
-    """Device buffers of one layer (allocated with PyTorch, owned here)."""
+    """Device buffers of one layer (allocated with PyTorch, owned here).
+
+    records: (num_slots, Hkv, rec_bytes) uint8 with fp16 (s, z), where a slot
+    is exactly the records of its KV heads; (num_slots, slot_bytes) with E4M3
+    (s, z), whose slots carry padding after the packed records (head_records()
+    gives the per-head view of either)."""
 
     def __init__(self, cfg, num_slots, max_reqs, rot_k, rot_v, device="cuda"):
         self.cfg = cfg
         rb = record_bytes(cfg)
+        sb = slot_bytes(cfg)
         H, d = cfg.num_kv_heads, cfg.head_dim
-        self.records = torch.zeros((num_slots, H, rb), dtype=torch.uint8, device=device)
+        shape = (num_slots, H, rb) if sb == H * rb else (num_slots, sb)
+        self.records = torch.zeros(shape, dtype=torch.uint8, device=device)
+        self.rec_bytes = rb
+        self.slot_bytes = sb
         self.sink = torch.zeros((max_reqs, max(cfg.sink, 1), H, 2, d), dtype=torch.bfloat16, device=device)
         self.recent = torch.zeros((max_reqs, cfg.recent, H, 2, d), dtype=torch.bfloat16, device=device)
         self.rot_k = torch.as_tensor(np.ascontiguousarray(rot_k, np.float32)).to(device)
         self.rot_v = torch.as_tensor(np.ascontiguousarray(rot_v, np.float32)).to(device)
         self.num_slots = num_slots
         self.max_reqs = max_reqs
+
+    def head_records(self):
+        """(num_slots, Hkv, rec_bytes) view of the records."""
+        H, rb = self.cfg.num_kv_heads, self.rec_bytes
+        if self.records.dim() == 3:
+            return self.records
+        return self.records.as_strided((self.num_slots, H, rb), (self.slot_bytes, rb, 1))
 
     def c(self):
         return CLayerCache(self.records.data_ptr(), self.sink.data_ptr(), self.recent.data_ptr(),

@@ -3,8 +3,9 @@ and classifying INT2 record mismatches against the acceptance rule
 
     codes are bit-exact except where the oracle's pre-rounding value
     u = (y - z)/s lies within 1e-6·max(1, |u|) of a rounding boundary, and
-    (s, z) are exact except where the fp32 value rounded to fp16 lies within
-    1e-6 relative of an fp16 rounding tie (all codes of such a group excused).
+    (s, z) are exact except where the fp32 value rounded to fp16 (or to E4M3
+    for one-byte scales) lies within 1e-6 relative of a rounding tie of that
+    format (all codes of such a group excused).
 
 Both kinds of boundary case are counted; `record_boundary_cases` keeps the
 counts of a test so that the session summary reports them.
@@ -31,6 +32,25 @@ def fp16_near_tie(x, band=0.0):
     return np.abs(x.astype(np.float64) - mid) <= np.maximum(REL_TIE * np.maximum(np.abs(x), 1e-30), band)
 
 
+_E4M3_GRID = None
+
+
+def e4m3_near_tie(x, band=0.0):
+    """True where fp32 x is within REL_TIE (relative), or within the absolute
+    `band`, of a midpoint between E4M3 neighbours.  Beyond ±448 every value
+    saturates to ±448, so there is no tie there."""
+    global _E4M3_GRID
+    if _E4M3_GRID is None:
+        b = np.array([i for i in range(256) if (i & 0x7F) != 0x7F], np.uint8)
+        _E4M3_GRID = np.unique(oq.e4m3_from_bits(b).astype(np.float64))
+    g = _E4M3_GRID
+    x = np.atleast_1d(np.asarray(x, np.float32)).astype(np.float64)
+    i = np.clip(np.searchsorted(g, x), 1, len(g) - 1)
+    mid = (g[i - 1] + g[i]) / 2
+    inside = (x >= g[0]) & (x <= g[-1])
+    return inside & (np.abs(x - mid) <= np.maximum(REL_TIE * np.maximum(np.abs(x), 1e-30), band))
+
+
 def classify_records(gpu_rec, ora_cache, slots, ora_y=None):
     """Compare GPU records with the oracle's for the given slots (all heads).
 
@@ -40,18 +60,22 @@ def classify_records(gpu_rec, ora_cache, slots, ora_y=None):
     """
     cfg = ora_cache.cfg
     d, G, H = cfg.head_dim, cfg.group_size, cfg.num_kv_heads
+    fmt = cfg.scale_fmt
+    near_tie = e4m3_near_tie if fmt == "e4m3" else fp16_near_tie
     ng = d // G
     r = np.float32(cfg.clip_ratio)
     slots = np.asarray(slots, dtype=np.int64)
     want = ora_cache.records()[slots]
     got = np.asarray(gpu_rec)[slots]
+    if got.ndim == 2:                      # slot layout (E4M3): per-head records
+        got = oq.head_records(got, H, ora_cache.record_bytes())
     stats = dict(exact=0, code_ties=0, sz_ties=0, bad=0, bad_examples=[])
     diff = (want != got).any(axis=-1)               # (n, H)
     stats["exact"] = int((~diff).sum()) * 2 * ng
     for i, h in zip(*np.nonzero(diff)):
         s = int(slots[i])
-        gk = oq.unpack_record(got[i, h], d, G)
-        wk = oq.unpack_record(want[i, h], d, G)
+        gk = oq.unpack_record(got[i, h], d, G, fmt)
+        wk = oq.unpack_record(want[i, h], d, G, fmt)
         for mat in (0, 1):
             gc, gs, gz = gk[3 * mat: 3 * mat + 3]
             wc, ws, wz = wk[3 * mat: 3 * mat + 3]
@@ -74,7 +98,7 @@ def classify_records(gpu_rec, ora_cache, slots, ora_y=None):
                 hi = np.float32(r * yg.max())
                 s32 = np.float32(np.float32(hi - lo) / np.float32(3.0))
                 if not same_sz:
-                    if fp16_near_tie(s32) or fp16_near_tie(lo):
+                    if near_tie(s32) or near_tie(lo):
                         stats["sz_ties"] += 1
                         continue
                     stats["bad"] += 1
@@ -101,7 +125,8 @@ def device_cache_from_oracle(ops, ocache, cfg, device="cuda"):
     """A LayerCache holding exactly the oracle cache's records and windows."""
     dc = ops.LayerCache(cfg, ocache.num_slots, ocache.max_reqs, ocache.rot_k.astype(np.float32),
                         ocache.rot_v.astype(np.float32), device=device)
-    dc.records.copy_(torch.from_numpy(ocache.records()))
+    rec = ocache.records() if dc.records.dim() == 3 else ocache.slot_records()
+    dc.records.copy_(torch.from_numpy(rec))
     sink_bits, ring_bits = ocache.window_bits()
     if cfg.sink > 0:
         dc.sink.copy_(torch.from_numpy(sink_bits.view(np.int16)).view(torch.bfloat16))

@@ -56,6 +56,28 @@ def test_record_and_token_bytes_match_oracle(ops):
         assert bf16 == 4 * 2 * d * 2
     # 640 B/token for the 8-KV-head d=128 layer
     assert ops.cache_bytes_per_token(_cfg(ops))[0] == 640
+    assert ops.slot_bytes(_cfg(ops)) == 640
+
+
+def test_e4m3_record_and_slot_bytes_match_oracle(ops):
+    from oracle import quant as oq
+    for d, G, H in ((128, 64, 8), (256, 128, 4), (128, 32, 2), (64, 64, 1), (128, 128, 3), (256, 256, 5)):
+        cfg = _cfg(ops, head_dim=d, group_size=G, num_q_heads=2 * H, num_kv_heads=H, scale_fmt="e4m3")
+        assert ops.record_bytes(cfg) == oracle.record_bytes(d, G, scale_bits=8) == oq.record_layout(d, G, "e4m3")["bytes"]
+        assert ops.slot_bytes(cfg) == oq.slot_bytes(d, G, H, "e4m3")
+        assert ops.cache_bytes_per_token(cfg)[0] == ops.slot_bytes(cfg)
+    # 576 B/token for the 8-KV-head d=128 layer with one-byte scale and zero
+    assert ops.cache_bytes_per_token(_cfg(ops, scale_fmt="e4m3"))[0] == 576
+
+
+def test_unknown_scale_format_rejected(ops):
+    c = _cfg(ops).c()
+    c.scale_dtype = 2
+    out = ctypes.c_int64()
+    assert ops.lib().oscar_record_bytes(ctypes.byref(c), ctypes.byref(out)) == -1
+    assert "scale_dtype" in ops.last_error()
+    with pytest.raises(ValueError):
+        _cfg(ops, scale_fmt="bf16").c()
 
 
 @pytest.mark.parametrize("field,value", [

@@ -33,20 +33,20 @@ def _misaligned(t):
 
 
 def run_append_scenario(d, Hq, Hkv, G, S, W, kv_dtype, calls, clip=0.9, mode="fixed4", pool_extra=37,
-                        seed=SEED, unaligned=False, rotations=None, keep=None):
+                        seed=SEED, unaligned=False, rotations=None, keep=None, scale_fmt="f16"):
     from rotated_int2_kv_gb300 import ops
     B = len(calls[0])
     Lfin = [sum(c[b] for c in calls) for b in range(B)]
     maxL = max(max(Lfin), 1)
     pool = B * maxL + pool_extra
-    cfg = ops.Config(d, Hq, Hkv, G, S, W, clip, kv_dtype=kv_dtype)
+    cfg = ops.Config(d, Hq, Hkv, G, S, W, clip, kv_dtype=kv_dtype, scale_fmt=scale_fmt)
     Rk, Rv = _rotations(d, seed) if rotations is None else rotations
     pt = synth.page_table(seed, B, maxL, pool, shuffled=True)
     req = torch.tensor(list(reversed(range(B))), dtype=torch.int32)   # window rows permuted
     max_reqs = B + 2
     dev = torch.device("cuda")
     dc = ops.LayerCache(cfg, pool, max_reqs, Rk, Rv, device=dev)
-    oc = oracle.OracleCache(oracle.OracleConfig(d, Hq, Hkv, G, S, W, clip), pool, max_reqs, Rk, Rv)
+    oc = oracle.OracleCache(oracle.OracleConfig(d, Hq, Hkv, G, S, W, clip, scale_fmt), pool, max_reqs, Rk, Rv)
     scales = synth.outlier_scales(seed, Hkv, d, mode)
     pos = [0] * B
     for call in calls:
@@ -75,7 +75,8 @@ def run_append_scenario(d, Hq, Hkv, G, S, W, kv_dtype, calls, clip=0.9, mode="fi
     hist_slots = np.array(sorted(hist_slots), dtype=np.int64)
     stats = classify_records(gpu_rec, oc, hist_slots)
     assert stats["bad"] == 0, stats
-    record_boundary_cases("append d%d G%d Hkv%d" % (d, G, Hkv), stats, len(hist_slots) * Hkv * 2 * (d // G))
+    record_boundary_cases("append d%d G%d Hkv%d %s" % (d, G, Hkv, scale_fmt), stats,
+                          len(hist_slots) * Hkv * 2 * (d // G))
     others = np.setdiff1d(np.arange(pool), hist_slots)
     assert not gpu_rec[others].any(), "records outside the history were written"
     # windows: bit-exact bf16
@@ -131,6 +132,27 @@ def test_large_appends_tiled_path(d, G, dtype, unaligned):
     calls = [[300, 290, 13], [2600, 2700, 1001]]
     st = run_append_scenario(d, 8, 2, G, 64, 256, dtype, calls, unaligned=unaligned)
     assert st["exact"] > 0
+
+
+@pytest.mark.parametrize("d,Hq,Hkv,G,S,W,calls", [
+    # tensor-core tiles (a 5,000-token fill), decode steps with ring spills
+    (128, 32, 8, 64, 64, 256, [[5000, 333, 1], [1, 1, 1], [1, 1, 1], [257, 1, 300]]),
+    # d 256 fp32 tiles and decode steps (the wide GQA-6 layer, group 128)
+    (256, 24, 4, 128, 64, 256, [[700, 2600], [1, 1], [300, 0], [1, 1]]),
+    # small ragged calls through the warp-per-vector kernels; group 32
+    (64, 12, 2, 32, 4, 8, [[5, 0, 17], [1, 1, 1], [20, 3, 0], [40, 1, 64]]),
+    # one group per head (group = head_dim): 68-byte records padded to 72, odd KV head count
+    (128, 6, 3, 128, 16, 32, [[1300, 20, 700], [1, 1, 1], [77, 0, 5]]),
+])
+def test_e4m3_scale_zero(d, Hq, Hkv, G, S, W, calls):
+    # one-byte (E4M3) scale and zero: packed records, slot layout, the same
+    # exact-decision rule with E4M3 rounding ties
+    from rotated_int2_kv_gb300 import ops
+    keep = {}
+    st = run_append_scenario(d, Hq, Hkv, G, S, W, torch.bfloat16, calls, scale_fmt="e4m3", keep=keep)
+    assert st["exact"] > 0
+    dc = keep["dc"]
+    assert dc.records.dim() == 2 and dc.records.shape[1] == ops.slot_bytes(keep["cfg"])
 
 
 def test_many_kv_heads():

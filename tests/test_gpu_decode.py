@@ -25,14 +25,14 @@ def _rotations(d, seed=SEED):
 
 
 def build_oracle_cache(d, Hq, Hkv, G, S, W, lens, kv_dtype=torch.bfloat16, mode="fixed4", clip=0.9,
-                       seed=SEED, shuffled=True, pt_width=None):
+                       seed=SEED, shuffled=True, pt_width=None, scale_fmt="f16"):
     B = len(lens)
     maxL = max(pt_width or 0, max(lens))
     pool = B * maxL + 11
     Rk, Rv = _rotations(d, seed)
     pt = synth.page_table(seed, B, maxL, pool, shuffled=shuffled)
     req = np.array(list(reversed(range(B))), np.int32)
-    oc = oracle.OracleCache(oracle.OracleConfig(d, Hq, Hkv, G, S, W, clip), pool, B + 1, Rk, Rv)
+    oc = oracle.OracleCache(oracle.OracleConfig(d, Hq, Hkv, G, S, W, clip, scale_fmt), pool, B + 1, Rk, Rv)
     scales = synth.outlier_scales(seed, Hkv, d, mode)
     ks, vs = [], []
     for b in range(B):
@@ -45,10 +45,11 @@ def build_oracle_cache(d, Hq, Hkv, G, S, W, lens, kv_dtype=torch.bfloat16, mode=
 
 
 def run_decode_case(d, Hq, Hkv, G, S, W, lens, q_dtype=torch.bfloat16, impl="auto", mode="fixed4",
-                    max_seq_len=None, step=0):
+                    max_seq_len=None, step=0, scale_fmt="f16"):
     from rotated_int2_kv_gb300 import ops
-    oc, pt, req = build_oracle_cache(d, Hq, Hkv, G, S, W, lens, mode=mode, pt_width=max_seq_len)
-    cfg = ops.Config(d, Hq, Hkv, G, S, W, 0.9, q_dtype=q_dtype)
+    oc, pt, req = build_oracle_cache(d, Hq, Hkv, G, S, W, lens, mode=mode, pt_width=max_seq_len,
+                                     scale_fmt=scale_fmt)
+    cfg = ops.Config(d, Hq, Hkv, G, S, W, 0.9, q_dtype=q_dtype, scale_fmt=scale_fmt)
     dc = device_cache_from_oracle(ops, oc, cfg)
     B = len(lens)
     q = synth.queries(SEED, step, B, Hq, d, dtype=q_dtype)
@@ -85,6 +86,19 @@ def test_gqa6_wide_heads(impl):
 @pytest.mark.parametrize("impl", ["auto", "simt"])
 def test_gqa8_ragged(impl):
     run_decode_case(128, 64, 8, 64, 64, 256, [4100, 1300, 2222], impl=impl, mode="per_head")
+
+
+@pytest.mark.parametrize("impl", ["auto", "simt"])
+@pytest.mark.parametrize("d,Hq,Hkv,G,lens,mode", [
+    (128, 32, 8, 64, [1, 321, 3000, 9000], "fixed4"),      # 576-byte slots, two warp sets
+    (128, 64, 8, 64, [4100, 1300, 2222], "per_head"),     # eight query heads per KV head
+    (256, 24, 4, 128, [2500, 777], "fixed4"),             # channel-split warps, 544-byte slots
+    (128, 8, 2, 32, [1500, 900], "fixed4"),               # group 32
+    (128, 6, 3, 128, [1700, 400, 2100], "fixed4"),        # 72-byte records, padded 224-byte slots
+    (128, 32, 2, 64, [3000, 700], "fixed4"),              # sixteen query heads per KV head
+])
+def test_e4m3_scale_zero(impl, d, Hq, Hkv, G, lens, mode):
+    run_decode_case(d, Hq, Hkv, G, 64, 256, lens, impl=impl, mode=mode, scale_fmt="e4m3")
 
 
 def test_small_windows_d64():
@@ -175,7 +189,8 @@ def test_workspace_and_length_errors():
     assert not out.any()
 
 
-def test_end_to_end_gpu_append_then_decode():
+@pytest.mark.parametrize("scale_fmt", ["f16", "e4m3"])
+def test_end_to_end_gpu_append_then_decode(scale_fmt):
     """Chunked GPU appends followed by decode steps, checked at every step:
     the GPU-built records against the oracle's (bit-exact except counted
     rounding ties), decode parity on identical cache contents, and the
@@ -190,10 +205,10 @@ def test_end_to_end_gpu_append_then_decode():
     pool = B * maxL
     Rk, Rv = _rotations(d)
     pt = synth.page_table(SEED, B, maxL, pool)
-    cfg = ops.Config(d, Hq, Hkv, G, S, W)
+    cfg = ops.Config(d, Hq, Hkv, G, S, W, scale_fmt=scale_fmt)
     dev = torch.device("cuda")
     dc = ops.LayerCache(cfg, pool, B, Rk, Rv)
-    oc = oracle.OracleCache(oracle.OracleConfig(d, Hq, Hkv, G, S, W), pool, B, Rk, Rv)
+    oc = oracle.OracleCache(oracle.OracleConfig(d, Hq, Hkv, G, S, W, scale_fmt=scale_fmt), pool, B, Rk, Rv)
     scales = synth.outlier_scales(SEED, Hkv, d)
     pos = [0, 0]
     req = np.arange(B, dtype=np.int32)

@@ -23,14 +23,14 @@ def _rotations(d, seed=SEED):
 
 
 def _run(d, Hq, Hkv, G, S, W, prefixes, chunks, heads=None, mode="fixed4", q_dtype=torch.bfloat16,
-         kv_dtype=torch.bfloat16):
+         kv_dtype=torch.bfloat16, scale_fmt="f16"):
     from rotated_int2_kv_gb300 import ops
     B = len(prefixes)
     maxL = max(p + c for p, c in zip(prefixes, chunks)) + 1
     pool = B * maxL + 11
     Rk, Rv = _rotations(d)
-    cfg = ops.Config(d, Hq, Hkv, G, S, W, 0.9, kv_dtype=kv_dtype, q_dtype=q_dtype)
-    ocfg = oracle.OracleConfig(d, Hq, Hkv, G, S, W, 0.9)
+    cfg = ops.Config(d, Hq, Hkv, G, S, W, 0.9, kv_dtype=kv_dtype, q_dtype=q_dtype, scale_fmt=scale_fmt)
+    ocfg = oracle.OracleConfig(d, Hq, Hkv, G, S, W, 0.9, scale_fmt)
     pt = synth.page_table(SEED, B, maxL, pool)
     req = np.arange(B, dtype=np.int32)[::-1].copy()          # window rows permuted
     oc = oracle.OracleCache(ocfg, pool, B, Rk, Rv)
@@ -77,6 +77,11 @@ def test_prefill_gqa6_wide_heads():
 
 def test_prefill_gqa8_and_group32_fp32_inputs():
     _run(128, 16, 2, 32, 16, 64, prefixes=[900, 0], chunks=[50, 20], q_dtype=torch.float32, kv_dtype=torch.float32)
+
+
+@pytest.mark.parametrize("d,Hq,Hkv,G", [(128, 32, 8, 64), (256, 24, 4, 128), (128, 6, 3, 128)])
+def test_prefill_e4m3_scale_zero(d, Hq, Hkv, G):
+    _run(d, Hq, Hkv, G, 64, 256, prefixes=[2100, 700], chunks=[77, 16], heads=(0, 1, Hq - 1), scale_fmt="e4m3")
 
 
 def test_prefill_d64_no_sink():

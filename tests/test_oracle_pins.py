@@ -229,6 +229,30 @@ def test_bf16_round_matches_torch():
     assert np.array_equal(oracle.bf16_round(x), ref)
 
 
+def test_e4m3_rounding_matches_torch():
+    # every finite E4M3 value decodes as torch's float8_e4m3fn and encodes back
+    torch = pytest.importorskip("torch")
+    b = np.array([i for i in range(256) if (i & 0x7F) != 0x7F], np.uint8)
+    v = oq.e4m3_from_bits(b)
+    assert np.array_equal(v, torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float32).numpy())
+    assert np.array_equal(oq.e4m3_bits(v), b)
+    assert float(v.max()) == 448.0 and float(v[v > 0].min()) == 2.0 ** -9
+    # rounding to nearest, ties to even, over the range where torch's cast is finite
+    rng = np.random.default_rng(70)
+    x = (rng.standard_normal(200000) * 10 ** rng.uniform(-5, 2.7, 200000)).astype(np.float32)
+    vs = np.unique(np.abs(v)).astype(np.float64)
+    mids = ((vs[:-1] + vs[1:]) / 2).astype(np.float32)     # exact midpoints (ties)
+    x = np.concatenate([x, mids, -mids])
+    x = x[np.abs(x) < 464]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float32).numpy()
+    assert np.array_equal(oracle.e4m3_round(x), ref)
+    # reading: finite values beyond the largest finite one saturate (torch gives NaN)
+    assert np.array_equal(oracle.e4m3_round(np.array([464, 1e6, -500], np.float32)), [448, 448, -448])
+    # signed zeros survive
+    z = oracle.e4m3_round(np.array([-0.0, -1e-4], np.float32))
+    assert np.all(z == 0) and np.all(np.signbit(z))
+
+
 def test_quantiser_exact_grid_round_trip():
     # values already on the INT2 grid come back exactly at clip ratio 1.0
     rng = np.random.default_rng(8)
@@ -245,6 +269,56 @@ def test_quantiser_exact_grid_round_trip():
     assert np.array_equal(s2.astype(np.float64), s)
     assert np.array_equal(z2.astype(np.float64), z)
     assert np.array_equal(oracle.dequantize_rows(c2, s2, z2), Y)
+
+
+def test_quantiser_e4m3_exact_grid_round_trip():
+    # with E4M3-exact s and z, values on the INT2 grid come back exactly at clip 1.0
+    rng = np.random.default_rng(71)
+    d, G = 128, 64
+    n = 200
+    codes = rng.integers(0, 4, size=(n, d)).astype(np.uint8)
+    codes.reshape(n, d // G, G)[:, :, 0] = 0
+    codes.reshape(n, d // G, G)[:, :, 1] = 3
+    s = (1.0 + rng.integers(0, 8, size=(n, d // G)) / 8.0) * 2.0 ** rng.integers(-5, 3, size=(n, d // G))
+    z = -(1.0 + rng.integers(0, 8, size=(n, d // G)) / 8.0) * 2.0 ** rng.integers(-3, 3, size=(n, d // G))
+    Y = (z[:, :, None] + codes.reshape(n, d // G, G) * s[:, :, None]).reshape(n, d)
+    assert np.array_equal(Y.astype(np.float32).astype(np.float64), Y)     # fp32-exact inputs
+    c2, s2, z2 = oracle.quantize_rows(Y.astype(np.float32), G, 1.0, "e4m3")
+    assert np.array_equal(c2, codes)
+    assert np.array_equal(s2.astype(np.float64), s)
+    assert np.array_equal(z2.astype(np.float64), z)
+    # the f16 path would keep (hi - lo)/3 at 11 bits: scales that are not E4M3
+    # values are rounded by the E4M3 path
+    Y3 = np.zeros((1, 64), np.float32)
+    Y3[0, 1] = 3 * 1.0625      # s = 1.0625 (fp16-exact, between E4M3 1.0 and 1.125)
+    c3, s3, z3 = oracle.quantize_rows(Y3, 64, 1.0, "e4m3")
+    assert float(s3[0, 0]) == 1.0 and float(z3[0, 0]) == 0.0
+    c4, s4, _ = oracle.quantize_rows(Y3, 64, 1.0, "f16")
+    assert float(s4[0, 0]) == 1.0625
+
+
+def test_quantiser_e4m3_code_is_the_nearest_level_brute_force():
+    rng = np.random.default_rng(72)
+    d, G = 64, 32
+    Y = (rng.standard_normal((300, d)) * 3).astype(np.float32)
+    codes, s, z = oracle.quantize_rows(Y, G, 0.9, "e4m3")
+    assert np.array_equal(oracle.e4m3_round(s.astype(np.float32)), s.astype(np.float32))
+    assert np.array_equal(oracle.e4m3_round(z.astype(np.float32)), z.astype(np.float32))
+    for i in range(300):
+        for gi in range(d // G):
+            yg = Y[i, gi * G:(gi + 1) * G]
+            lo = np.float32(np.float32(0.9) * yg.min())
+            hi = np.float32(np.float32(0.9) * yg.max())
+            assert float(s[i, gi]) == float(oracle.e4m3_round(np.float32(np.float32(hi - lo) / np.float32(3))))
+            assert float(z[i, gi]) == float(oracle.e4m3_round(lo))
+            s32 = np.float32(s[i, gi])
+            z32 = np.float32(z[i, gi])
+            for j in range(gi * G, (gi + 1) * G):
+                u = float(np.float32(np.float32(Y[i, j] - z32) / s32))
+                best = min(range(4), key=lambda k: (abs(u - k), k))
+                frac = u - math.floor(u)
+                if abs(frac - 0.5) > 1e-9 or u < 0 or u > 3:
+                    assert codes[i, j] == best
 
 
 def test_quantiser_code_is_the_nearest_level_brute_force():
@@ -304,6 +378,35 @@ def test_record_round_trip_and_size():
             assert np.array_equal(a, b)
 
 
+def test_e4m3_record_and_slot_layout():
+    rng = np.random.default_rng(73)
+    # (d, G, KV heads, record bytes, slot bytes): codes d/2 + 2-byte (s, z) pairs,
+    # records padded to 8 bytes and packed back to back, slots padded to 16
+    for d, G, H, rec_size, slot_size in ((128, 64, 8, 72, 576), (256, 128, 4, 136, 544),
+                                         (128, 128, 3, 72, 224), (64, 64, 1, 40, 48),
+                                         (128, 32, 2, 80, 160)):
+        ng = d // G
+        kc = rng.integers(0, 4, (5, H, d)).astype(np.uint8)
+        vc = rng.integers(0, 4, (5, H, d)).astype(np.uint8)
+        ks, kz, vs, vz = (oracle.e4m3_round(rng.standard_normal((5, H, ng)) * 4).astype(np.float16)
+                          for _ in range(4))
+        rec = oq.pack_record(kc, ks, kz, vc, vs, vz, d, G, "e4m3")
+        assert rec.shape == (5, H, rec_size) and oracle.record_bytes(d, G, scale_bits=8) == rec_size
+        # byte d/2 + 2gi holds the E4M3 bits of K's s of group gi, the next byte z
+        assert np.array_equal(rec[..., d // 2 + 1], oq.e4m3_bits(kz[..., 0]))
+        assert np.array_equal(rec[..., d // 2 + 2 * ng], oq.e4m3_bits(vs[..., 0]))
+        assert oq.slot_bytes(d, G, H, "e4m3") == slot_size
+        sl = oq.pack_slots(rec, slot_size)
+        assert sl.shape == (5, slot_size) and not sl[:, H * rec_size:].any()
+        assert np.array_equal(sl[:, rec_size:2 * rec_size] if H > 1 else sl[:, :rec_size], rec[:, min(1, H - 1)])
+        assert np.array_equal(oq.head_records(sl, H, rec_size), rec)
+        back = oq.unpack_record(rec, d, G, "e4m3")
+        for a, b in zip(back, (kc, ks, kz, vc, vs, vz)):
+            assert np.array_equal(a, b)
+    # the fp16 slot is the per-head records back to back (records already 16-byte multiples)
+    assert oq.slot_bytes(128, 64, 8) == 640
+
+
 # --------------------------------------------------------------------------
 # accounting (figures printed on the pages)
 # --------------------------------------------------------------------------
@@ -317,10 +420,15 @@ def test_accounting_matches_pages():
     assert oracle.code_bytes_per_token(10, 2, 256) / 1024 == gold["kib_per_token_10x2_d256"]
     assert round(100 * oracle.window_fraction(131072), 2) == gold["window_percent_128k"]
     assert round(oracle.bits_per_element(131072, 128), 2) == gold["bits_per_element"]
+    assert round(oracle.bits_per_element(131072, 64, scale_bits=8), 2) == gold["bits_per_element_g64_e4m3"]
     assert oracle.code_bytes_per_token(1, 1, 1) / 2 == gold["bytes_per_code"]
     # per-token record of an 8-KV-head, d=128, G=64 layer: 640 bytes
     assert 8 * oracle.record_bytes(128, 64) == 640
     assert 4 * oracle.record_bytes(256, 128) == 576
+    # E4M3 (s, z): 72-byte records, 576 bytes per token of 8 KV heads; the INT2
+    # region costs 2 + 16/64 = 2.25 bits per element
+    assert 8 * oracle.record_bytes(128, 64, scale_bits=8) == 576
+    assert 8 * oracle.record_bytes(128, 64, scale_bits=8) * 8 / (8 * 2 * 128) == 2.25
 
 
 # --------------------------------------------------------------------------

@@ -2,7 +2,7 @@
 
 import numpy as np
 
-from parity_util import REL_TIE, classify_records, fp16_near_tie
+from parity_util import REL_TIE, classify_records, e4m3_near_tie, fp16_near_tie
 
 
 def test_fp16_near_tie_bands():
@@ -16,14 +16,24 @@ def test_fp16_near_tie_bands():
     assert not fp16_near_tie(far, band=1e-5)
 
 
-def _tie_cache():
+def test_e4m3_near_tie_bands():
+    # 1.0625 is the midpoint between E4M3 1.0 and 1.125; 2^-10 between 0 and 2^-9
+    for mid in (1.0625, -1.0625, 2.0 ** -10, 432.0):
+        assert e4m3_near_tie(np.float32(mid))
+        assert not e4m3_near_tie(np.float32(mid * (1 + 4 * REL_TIE)))
+    assert not e4m3_near_tie(np.float32(1.03125))        # a quarter step
+    assert not e4m3_near_tie(np.float32(464.0))          # saturated range: no tie
+    assert e4m3_near_tie(np.float32(1.0625 + 1e-4), band=2e-4)
+
+
+def _tie_cache(scale_fmt="f16"):
     """An oracle cache with one history token whose K group 0 holds a value at a
     rounding boundary: R = I, clip 1, group min 0 and max 3 give s = 1 and
     z = 0, so channel 1 (y = 0.5) sits exactly on the boundary between codes 0
     and 1 and channel 2 (y = 1.203125) is far from any boundary."""
     import oracle
     d, G = 64, 64
-    cfg = oracle.OracleConfig(d, 1, 1, G, sink=0, recent=1, clip_ratio=1.0)
+    cfg = oracle.OracleConfig(d, 1, 1, G, sink=0, recent=1, clip_ratio=1.0, scale_fmt=scale_fmt)
     eye = np.eye(d)
     oc = oracle.OracleCache(cfg, 4, 1, eye, eye)
     rng = np.random.default_rng(3)
@@ -61,5 +71,29 @@ def test_classify_records_excuses_only_boundary_cases():
     ks4 = ks.copy()
     ks4[0] = np.nextafter(ks4[0], np.float16(2))
     off[0, 0] = oq.pack_record(kc, ks4, kz, vc, vs, vz, d, G)
+    st = classify_records(off, oc, [0])
+    assert st["bad"] == 1 and st["sz_ties"] == 0
+
+
+def test_classify_e4m3_slot_records():
+    # the same planted cases on E4M3 records held in the slot layout
+    from oracle import quant as oq
+    oc, d, G = _tie_cache("e4m3")
+    want = oc.records()
+    kc, ks, kz, vc, vs, vz = oq.unpack_record(want[0, 0], d, G, "e4m3")
+    assert float(ks[0]) == 1.0 and float(kz[0]) == 0.0 and kc[1] == 0 and kc[2] == 1
+    slots = oc.slot_records()
+    assert slots.shape == (4, oc.slot_bytes()) and classify_records(slots, oc, [0])["bad"] == 0
+    rb = oc.record_bytes()
+    tied = slots.copy()
+    kc2 = kc.copy()
+    kc2[1] = 1
+    tied[0, :rb] = oq.pack_record(kc2, ks, kz, vc, vs, vz, d, G, "e4m3")
+    st = classify_records(tied, oc, [0])
+    assert st["bad"] == 0 and st["code_ties"] == 1
+    off = slots.copy()
+    ks4 = ks.copy()
+    ks4[0] = np.float16(1.125)                          # one E4M3 step up
+    off[0, :rb] = oq.pack_record(kc, ks4, kz, vc, vs, vz, d, G, "e4m3")
     st = classify_records(off, oc, [0])
     assert st["bad"] == 1 and st["sz_ties"] == 0
