@@ -38,6 +38,7 @@ B, HQ, HKV, D, G = 32, 32, 8, 128, 64
 L_BASE = 100_000          # tokens cached before the first decode step
 LB = np.full(B, L_BASE, dtype=np.int64)   # per-request cached tokens; uniform unless a workload sets it
 OUTLIERS = "fixed4"       # K/V outlier-channel recipe of the synthetic inputs
+SCALE_FMT = "f16"         # storage of each group's (s, z): fp16 or E4M3 pairs
 CYCLE = 100               # decode steps of the sequence
 S_SINK, W_RECENT = 64, 256
 
@@ -54,9 +55,11 @@ def parse():
     ap.add_argument("--no-append", action="store_true")
     ap.add_argument("--no-shapes", dest="shapes", action="store_false",
                     help="skip the ragged GQA-8 / wide GQA-6 decode shapes and the prefill chunks of the default line")
-    ap.add_argument("--workload", choices=["qwen8b-100k", "mid", "small", "b1-32k", "qwen32b-ragged", "gqa6-wide"],
+    ap.add_argument("--workload", choices=["qwen8b-100k", "qwen8b-100k-e4m3", "mid", "small", "b1-32k",
+                                           "qwen32b-ragged", "gqa6-wide"],
                     default="qwen8b-100k",
-                    help="small: batch 4 at 65,536 tokens (168 MB of INT2 records, > L2), for ncu captures; "
+                    help="qwen8b-100k-e4m3: the default shape with one-byte (E4M3) scale and zero; "
+                         "small: batch 4 at 65,536 tokens (168 MB of INT2 records, > L2), for ncu captures; "
                          "mid: batch 8 at 100,000 tokens (0.51 GB); b1-32k: one request at 32,768 tokens "
                          "(launch-bound); qwen32b-ragged: 64 q / 8 KV heads, batch 8, lengths uniform in "
                          "[65,536, 131,072], per-head K outliers, 50-step cycle; gqa6-wide: 24 q / 4 KV heads, "
@@ -195,7 +198,7 @@ def build_decode_workload(rank, steps_total):
     from rotated_int2_kv_gb300 import ops, synth
     dev = torch.device("cuda")
     seed = SEED + 7919 * rank
-    cfg = ops.Config(D, HQ, HKV, G, S_SINK, W_RECENT, 0.9)
+    cfg = ops.Config(D, HQ, HKV, G, S_SINK, W_RECENT, 0.9, scale_fmt=SCALE_FMT)
     Rk, Rv = rotations(D)
     max_len = int(LB.max()) + CYCLE
     pool = B * max_len
@@ -252,6 +255,13 @@ def launches_per_step():
     return (1 if B <= W_RECENT else 2) + 3
 
 
+def bits_per_element():
+    """Stored bits per KV element of the workload's requests (mean): 16 in the
+    BF16 windows, 2 + 2·(scale bits)/G in the INT2 history."""
+    sb = 16.0 if SCALE_FMT == "f16" else 8.0
+    return float(np.mean((16.0 * 320 + (2 + 2 * sb / G) * (LB - 320)) / LB))
+
+
 def algorithmic_history_bytes(rec_bytes_per_token, L):
     hist = max(S_SINK, L - W_RECENT) - S_SINK      # history [S, max(S, L - W))
     return hist * (rec_bytes_per_token + 4)   # records + page-table entry
@@ -270,7 +280,7 @@ def oracle_sample(seed, L=None):
     Cv = oracle.covariance(synth.calib_samples(SEED, 1, D))
     Rk = oracle.build_rotation(Ck, D)[0].astype(np.float32)
     Rv = oracle.build_rotation(Cv, D)[0].astype(np.float32)
-    oc = oracle.OracleCache(oracle.OracleConfig(D, HQ, HKV, G, S_SINK, W_RECENT, 0.9), L, 1, Rk, Rv)
+    oc = oracle.OracleCache(oracle.OracleConfig(D, HQ, HKV, G, S_SINK, W_RECENT, 0.9, SCALE_FMT), L, 1, Rk, Rv)
     scales = synth.outlier_scales(seed, HKV, D, OUTLIERS)
     k, v = synth.kv_tokens(seed, 0, 0, L, HKV, D, scales)
     pt = np.arange(L, dtype=np.int64)[None, :]
@@ -296,19 +306,22 @@ def boundary_cases(w, n_hist=8192):
     from parity_util import classify_records
     L = S_SINK + n_hist + W_RECENT
     k, v = synth.kv_tokens(w["seed"], 0, 0, L, HKV, D, w["scales"], device="cuda")
-    oc = oracle.OracleCache(oracle.OracleConfig(D, HQ, HKV, G, S_SINK, W_RECENT, 0.9), L, 1, w["Rk"], w["Rv"])
+    oc = oracle.OracleCache(oracle.OracleConfig(D, HQ, HKV, G, S_SINK, W_RECENT, 0.9, SCALE_FMT), L, 1,
+                            w["Rk"], w["Rv"])
     oc.append(k.float().cpu().numpy(), v.float().cpu().numpy(), [0, L], [0], [0],
               np.arange(L, dtype=np.int64)[None, :], keep_y=True)
     hist = np.arange(S_SINK, S_SINK + n_hist)
-    got = np.zeros((L, HKV, w["cache"].records.shape[-1]), np.uint8)
-    got[hist] = w["cache"].records[w["pt"][0, S_SINK:S_SINK + n_hist].long()].cpu().numpy()
+    hr = w["cache"].head_records()
+    got = np.zeros((L, HKV, hr.shape[-1]), np.uint8)
+    got[hist] = hr[w["pt"][0, S_SINK:S_SINK + n_hist].long()].cpu().numpy()
     st = classify_records(got, oc, hist)
     return {"sample": "request 0, history tokens %d..%d (chunked-fill path), all KV heads, K and V"
                       % (S_SINK, S_SINK + n_hist - 1),
             "group_records": int(n_hist * HKV * 2 * (D // G)), "exact": st["exact"], "code_ties": st["code_ties"],
             "sz_ties": st["sz_ties"], "other_mismatches": st["bad"],
             "rule": "codes bit-exact except (y-z)/s within 1e-6*max(1,|u|) of a rounding boundary; (s, z) exact "
-                    "except the fp32 value within 1e-6 relative of an fp16 tie"}
+                    "except the fp32 value within 1e-6 relative of a rounding tie of the storage format (%s)"
+                    % ("fp16" if SCALE_FMT == "f16" else "E4M3")}
 
 
 def cpu_cores():
@@ -345,9 +358,10 @@ def workload_config(rec_tok=640):
            "contexts %d..%d (ragged)" % (int(LB.min()), int(LB.max())))
     shape = ("Qwen3-8B-shaped" if (HQ, HKV, D) == (32, 8, 128) else
              "Qwen3-32B-shaped" if (HQ, HKV, D) == (64, 8, 128) else "GQA-%d wide-head" % (HQ // HKV))
+    sz = "" if SCALE_FMT == "f16" else ", E4M3 scale and zero"
     return {"workload": "%s decode step (append 1 token + attention), batch %d, %s, %d q / %d KV heads, "
-                        "d %d, group %d, clip 0.9, shuffled page table, page_size 1"
-                        % (shape, B, ctx, HQ, HKV, D, G),
+                        "d %d, group %d%s, clip 0.9, shuffled page table, page_size 1"
+                        % (shape, B, ctx, HQ, HKV, D, G, sz),
             "batch": B, "context": int(LB.max()), "q_heads": HQ, "kv_heads": HKV, "head_dim": D, "group_size": G,
             "l2": ("inputs larger than L2 (%.2f GB INT2 history per step)" % hist_gb if hist_gb * 1e9 > 129e6 else
                    "inputs smaller than L2 (%.3f GB INT2 history, not flushed): a latency figure, not a "
@@ -357,9 +371,12 @@ def workload_config(rec_tok=640):
 
 def set_workload(name):
     """Sets the module's workload shape (the globals the builders read)."""
-    global B, HQ, HKV, D, G, L_BASE, LB, OUTLIERS, CYCLE
+    global B, HQ, HKV, D, G, L_BASE, LB, OUTLIERS, CYCLE, SCALE_FMT
     B, HQ, HKV, D, G, L_BASE, OUTLIERS, CYCLE = 32, 32, 8, 128, 64, 100_000, "fixed4", 100
-    if name == "small":
+    SCALE_FMT = "f16"
+    if name == "qwen8b-100k-e4m3":
+        SCALE_FMT = "e4m3"
+    elif name == "small":
         B, L_BASE = 4, 65536
     elif name == "mid":
         B, L_BASE = 8, 100_000
@@ -381,7 +398,7 @@ def shape_measure(name, steps, warmup, hbm_peak):
     clocks), for the extra keys of the default bench line."""
     import torch
     from rotated_int2_kv_gb300 import ops
-    saved = (B, HQ, HKV, D, G, L_BASE, LB, OUTLIERS, CYCLE)
+    saved = (B, HQ, HKV, D, G, L_BASE, LB, OUTLIERS, CYCLE, SCALE_FMT)
     try:
         set_workload(name)
         w = build_decode_workload(0, steps + warmup)
@@ -413,7 +430,7 @@ def shape_measure(name, steps, warmup, hbm_peak):
         achieved = (hist_bytes / hn) / (hms / hn / 1e3) / 1e9
         out = {"workload": workload_config(rec_tok)["workload"], "value": tokens / (ms / 1e3), "unit": UNIT,
                "ms_per_step": ms / steps, "steps": steps,
-               "history_ms_per_step": hms / hn, "bits_per_kv_element": float(np.mean((16.0 * 320 + (2 + 32.0 / G) * (LB - 320)) / LB)),
+               "history_ms_per_step": hms / hn, "bits_per_kv_element": bits_per_element(),
                "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                             "frac": achieved / hbm_peak, "kernel": "history kernel (INT2 split-K)",
                             "peak_source": "measured hbm_gbs"},
@@ -421,7 +438,8 @@ def shape_measure(name, steps, warmup, hbm_peak):
         del w
         return out
     finally:
-        globals().update(dict(zip(("B", "HQ", "HKV", "D", "G", "L_BASE", "LB", "OUTLIERS", "CYCLE"), saved)))
+        globals().update(dict(zip(("B", "HQ", "HKV", "D", "G", "L_BASE", "LB", "OUTLIERS", "CYCLE", "SCALE_FMT"),
+                                  saved)))
         torch.cuda.empty_cache()
 
 
@@ -577,7 +595,7 @@ def main():
                          "pct_of_8TBs": (achieved / 8000.0) if achieved else None},
             "kernel_ms_per_step": kernel_ms,
             "gpu_launches": launches_per_step() * args.steps,
-            "bits_per_kv_element": float(np.mean((16.0 * 320 + (2 + 32.0 / G) * (LB - 320)) / LB)),
+            "bits_per_kv_element": bits_per_element(),
             "clocks": clk}
     # ---- end to end through the C ABI with host buffers ----------------------
     if not args.no_e2e:
@@ -585,7 +603,8 @@ def main():
     if not args.no_append:
         line["append"] = append_measure()
     if args.shapes and args.workload == "qwen8b-100k" and ws == 1:
-        line["shapes"] = {name: shape_measure(name, 400, 5, hbm_peak) for name in ("qwen32b-ragged", "gqa6-wide")}
+        line["shapes"] = {name: shape_measure(name, 400, 5, hbm_peak)
+                          for name in ("qwen32b-ragged", "gqa6-wide", "qwen8b-100k-e4m3")}
         line["prefill"] = {name: prefill_measure(name, 32768, 8192, 3, float(peaks.get("bf16_tflops", 1900.0)))
                            for name in ("qwen8b", "gqa6-wide")}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -650,7 +669,7 @@ def append_measure():
     from rotated_int2_kv_gb300 import ops, synth
     dev = torch.device("cuda")
     L = 32768
-    cfg = ops.Config(D, HQ, HKV, G, S_SINK, W_RECENT, 0.9)
+    cfg = ops.Config(D, HQ, HKV, G, S_SINK, W_RECENT, 0.9, scale_fmt=SCALE_FMT)
     Rk, Rv = rotations(D)
     pt = synth.page_table(SEED, 1, L, L).to(dev)
     cache = ops.LayerCache(cfg, L, 1, Rk, Rv, device=dev)

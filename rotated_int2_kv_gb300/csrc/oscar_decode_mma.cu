@@ -131,6 +131,34 @@ __device__ __forceinline__ int named_bar_or(int id, int nthreads, int v) {
     return r;
 }
 
+// (s, z) of groups g0 .. g0 + N - 1 from the pair array at p (fp16 pairs of
+// 4 bytes or E4M3 pairs of 2 bytes): two groups per load when N is even (g0
+// even; p 8-byte aligned for fp16 pairs, 4-byte aligned for E4M3 pairs).
+template <int N, bool FP8>
+__device__ __forceinline__ void load_sz_groups(const unsigned char* p, int g0, float2 (&out)[N]) {
+    if constexpr (N % 2 == 0) {
+#pragma unroll
+        for (int q = 0; q < N; q += 2) {
+            if constexpr (FP8) {
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(p + 2 * (g0 + q));
+                uint32_t h0, h1;
+                asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+                    "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+                    : "=r"(h0), "=r"(h1) : "r"(w));
+                out[q] = h2f(h0);
+                out[q + 1] = h2f(h1);
+            } else {
+                const uint2 w = *reinterpret_cast<const uint2*>(p + 4 * (g0 + q));
+                out[q] = h2f(w.x);
+                out[q + 1] = h2f(w.y);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < N; ++q) out[q] = load_sz(p, g0 + q, FP8);
+    }
+}
+
 }  // namespace mma_detail
 
 // Row stride of one token's record in shared memory: rounded up to an odd
@@ -316,10 +344,13 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
         unsigned char* dst = stages + s * stage_bytes;
         // 16-byte cp.async of whole token records, completing on the stage's full
         // barrier through every thread's no-increment arrival
-        if constexpr (HKV > 0 && slot_bytes_of(HKV, REC) % 128 == 0 && TT == 64) {
-            // 8 tokens per warp: lane l copies chunks (l & 7) + 8u of tokens
-            // tbeg + (l >> 3) and tbeg + 4 + (l >> 3) (4 records per instruction)
+        if constexpr (HKV > 0 && TT == 64 && (TT + HKV * WPH * HP - 1) / (HKV * WPH * HP) <= 8) {
+            // at most 8 tokens per warp: lane l copies chunks (l & 7) + 8u of tokens
+            // tbeg + (l >> 3) and tbeg + 4 + (l >> 3) (4 records per instruction;
+            // a slot of 16·kCh bytes with kCh not a multiple of 8 leaves lanes idle
+            // in the last round)
             constexpr int kTB = slot_bytes_of(HKV, REC);
+            constexpr int kCh = kTB / 16;
             const int sa = ok0 ? nsl0 : -1;
 #pragma unroll
             for (int v = 0; v < 2; ++v) {
@@ -329,23 +360,9 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                     const uint8_t* src = P.records + (int64_t)sl * kTB + (lane & 7) * 16;
                     unsigned char* d = dst + (tbeg + tt) * row + (lane & 7) * 16;
 #pragma unroll
-                    for (int u = 0; u < kTB / 128; ++u) cp_async16(d + 128 * u, src + 128 * u);
+                    for (int u = 0; u < (kCh + 7) / 8; ++u)
+                        if (kCh % 8 == 0 || (lane & 7) + 8 * u < kCh) cp_async16(d + 128 * u, src + 128 * u);
                 }
-            }
-        } else if constexpr (HKV > 0 && TT == 64 && (TT + HKV * WPH * HP - 1) / (HKV * WPH * HP) <= 32) {
-            // compile-time slot size: the (token, 16-byte chunk) pairs of the warp's
-            // tokens (at most 32, all in nsl0) flattened over the lanes, so every
-            // instruction moves 32 chunks
-            constexpr int kCh = slot_bytes_of(HKV, REC) / 16;
-            constexpr int kTpw = (TT + HKV * WPH * HP - 1) / (HKV * WPH * HP);   // = tpw
-            const int sa = ok0 ? nsl0 : -1;
-            const int nch = (tend - tbeg) * kCh;
-#pragma unroll
-            for (int c = lane; c < ((kTpw * kCh + 31) & ~31); c += 32) {
-                const int tt = c / kCh, ch = c - tt * kCh;
-                const int sl = __shfl_sync(0xffffffffu, sa, tt & 31);
-                if (c < nch && sl >= 0)
-                    cp_async16(dst + (tbeg + tt) * row + 16 * ch, P.records + (int64_t)sl * (kCh * 16) + 16 * ch);
             }
         } else {
             // any shape: the warp's tokens one at a time, lanes over 16-byte chunks
@@ -527,10 +544,11 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                         float ts[NT], tz[NT];
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) { ts[nt] = 0.f; tz[nt] = 0.f; }
+                        float2 szk[GW];
+                        load_sz_groups<GW, FP8>(tb + t * row + D / 2, wsl * GW, szk);
 #pragma unroll
                         for (int gi = 0; gi < GW; ++gi) {
-                            const int gg = wsl * GW + gi;
-                            const float2 sz = load_sz(tb + t * row + D / 2, gg, FP8);
+                            const float2 sz = szk[gi];
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
                                 ts[nt] = fmaf(sz.x, sc[mb][gi][nt][2 * hf] + sc[mb][gi][nt][2 * hf + 1], ts[nt]);
@@ -542,10 +560,11 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                     } else {
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) lg[nt][i] = 0.f;
+                        float2 szk[GW];
+                        load_sz_groups<GW, FP8>(tb + t * row + D / 2, wsl * GW, szk);
 #pragma unroll
                         for (int gi = 0; gi < GW; ++gi) {
-                            const int gg = wsl * GW + gi;
-                            const float2 sz = load_sz(tb + t * row + D / 2, gg, FP8);
+                            const float2 sz = szk[gi];
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
                                 const float2 Q = qs[nt][gi];       // (Σ q̃, Σ q̃/α)
@@ -620,10 +639,11 @@ history_mma_kernel(DecodeParams P, int x_off, int stages_off, int trow, int ns_l
                     const float pv = fast_exp2(x[nt][i] - m_run[nt]);   // masked tokens: 2^-inf = 0
                     l_run[nt] += pv;
                     float w[GW];
+                    float2 szv[GW];   // rows of invalid tokens hold finite stale data and get p = 0
+                    load_sz_groups<GW, FP8>(tb + t * row + D / 2 + PB * NG, wsl * GW, szv);
 #pragma unroll
                     for (int gi = 0; gi < GW; ++gi) {
-                        // rows of invalid tokens hold finite stale data and get p = 0
-                        const float2 sz = load_sz(tb + t * row + D / 2 + PB * NG, wsl * GW + gi, FP8);
+                        const float2 sz = szv[gi];
                         w[gi] = pv * sz.x;
                         Zsum[nt][gi] = fmaf(pv, sz.y, Zsum[nt][gi]);
                     }

@@ -169,15 +169,10 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
 // pairs (2 bytes); both convert exactly.
 __device__ __forceinline__ float2 load_sz(const uint8_t* p, int gi, bool fp8) {
     if (fp8) {
-        // E4M3 byte b -> the fp16 with b's sign and b's 7 magnitude bits at bits
-        // 7..13: exponent field E, mantissa m·2^7, i.e. 2^(E-15)·(1 + m/8) for
-        // E > 0 and m·2^-17 for E = 0, both 2^-8 times the E4M3 value
-        const uint32_t v = *reinterpret_cast<const uint16_t*>(p + 2 * gi);
-        uint32_t y;
-        asm("prmt.b32 %0, %1, 0, 0x1404;" : "=r"(y) : "r"(v));            // bytes (0, b0, 0, b1)
-        const uint32_t h = ((y >> 1) & 0x3F803F80u) | (y & 0x80008000u);
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
-        return make_float2(f.x * 256.0f, f.y * 256.0f);
+        const unsigned short v = *reinterpret_cast<const unsigned short*>(p + 2 * gi);
+        uint32_t h;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));     // exact: every E4M3 value is an fp16
+        return __half22float2(*reinterpret_cast<const __half2*>(&h));
     }
     return __half22float2(*reinterpret_cast<const __half2*>(p + 4 * gi));
 }

@@ -36,7 +36,7 @@ def pytest_terminal_summary(terminalreporter, exitstatus, config):
     if not BOUNDARY_CASES:
         return
     tr = terminalreporter
-    tr.section("INT2 boundary cases (codes within 1e-6 of a rounding boundary; (s, z) at an fp16 tie)")
+    tr.section("INT2 boundary cases (codes within 1e-6 of a rounding boundary; (s, z) at a rounding tie of their format)")
     tc = ts = tn = 0
     for name, c, z, n in BOUNDARY_CASES:
         tr.write_line("%-40s code ties %4d   (s, z) ties %4d   of %d group records" % (name, c, z, n))

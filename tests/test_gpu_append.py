@@ -152,7 +152,8 @@ def test_e4m3_scale_zero(d, Hq, Hkv, G, S, W, calls):
     st = run_append_scenario(d, Hq, Hkv, G, S, W, torch.bfloat16, calls, scale_fmt="e4m3", keep=keep)
     assert st["exact"] > 0
     dc = keep["dc"]
-    assert dc.records.dim() == 2 and dc.records.shape[1] == ops.slot_bytes(keep["cfg"])
+    assert dc.records.numel() == dc.num_slots * ops.slot_bytes(keep["cfg"])
+    assert ops.record_bytes(keep["cfg"]) == (d // 2 + 4 * (d // G) + 7) // 8 * 8
 
 
 def test_many_kv_heads():
