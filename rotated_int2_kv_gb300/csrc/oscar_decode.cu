@@ -200,13 +200,10 @@ __device__ __forceinline__ void prep_slice(const DecodeParams& P, int hk, int b,
     }
 }
 
-// Runs the prep slice with the smallest head bucket that holds the query group.
-template <int D>
-__device__ __forceinline__ void prep_dispatch(const DecodeParams& P, int hk, int b, float* sm) {
-    if (P.g <= 4) prep_slice<D, 4>(P, hk, b, sm);
-    else if (P.g <= 8) prep_slice<D, 8>(P, hk, b, sm);
-    else prep_slice<D, 16>(P, hk, b, sm);
-}
+// Query-head bucket of the prep slice: the smallest of 4, 8, 16 that holds the
+// query group.  The window kernels are instantiated per bucket, so each carries
+// one prep variant (one copy of its code in the instruction cache).
+__host__ __device__ constexpr int prep_bucket(int g) { return g <= 4 ? 4 : g <= 8 ? 8 : 16; }
 
 // True when CTA i of an n-CTA history grid owns at least one of N chunks.
 __device__ __forceinline__ bool cta_has_work(int64_t i, int64_t N, int64_t n) {
@@ -405,14 +402,14 @@ constexpr int kCombThreads = 128;      // window kernel
 constexpr int kMergeThreads = 512;     // combine kernel
 constexpr int kWinTile = 64;
 
-template <int D>
+template <int D, int GQ>
 __global__ void __launch_bounds__(kCombThreads, D >= 256 ? 2 : 6) window_kernel(DecodeParams P) {
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     constexpr int kRowW = D / 2 + 1;               // words per staged bf16 row (odd: conflict-free)
     extern __shared__ __align__(16) float s_w[];
     const int hk = blockIdx.x, b = blockIdx.y, wt = (int)blockIdx.z - 1;
     if (wt < 0) {                                  // the first z-slice: query preparation
-        prep_dispatch<D>(P, hk, b, s_w);
+        prep_slice<D, GQ>(P, hk, b, s_w);
         return;
     }
     const int g = P.g, S = P.S, W = P.W;
@@ -611,7 +608,7 @@ struct WinMmaCfg {
     static constexpr int SMEM_WORDS = 2 * kWinTile * RW + KS * 128 + 4 * 128 + 2 * 32;
 };
 
-template <int D>
+template <int D, int GQ>
 __global__ void __launch_bounds__(128) window_mma_kernel(DecodeParams P) {
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     using namespace wmma_detail;
@@ -626,7 +623,7 @@ __global__ void __launch_bounds__(128) window_mma_kernel(DecodeParams P) {
     float* ssm = smx + 32;                                   // [4 warps][8 heads] sub-tile sum
     const int hk = blockIdx.x, b = blockIdx.y, wt = (int)blockIdx.z - 1;
     if (wt < 0) {                                  // the first z-slice (scheduled first): query preparation
-        prep_dispatch<D>(P, hk, b, reinterpret_cast<float*>(s_wm));
+        prep_slice<D, GQ>(P, hk, b, reinterpret_cast<float*>(s_wm));
         return;
     }
     const int g = P.g, S = P.S, W = P.W;
@@ -1134,25 +1131,28 @@ template <int D>
 static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
     // the window kernel's grid carries one more z-slice: the query preparation
     // of every (KV head, request)
-    const size_t psmem = (size_t)prep_smem_floats(D, P.g <= 4 ? 4 : P.g <= 8 ? 8 : 16) * 4;
+    const int gq = prep_bucket(P.g);
+    const size_t psmem = (size_t)prep_smem_floats(D, gq) * 4;
     int rc = OSCAR_OK;
+    const dim3 wgrid(P.Hkv, P.batch, P.n_win_tiles + 1);
     if (D <= 128 && P.g <= 8) {
         // tensor-core window: one block of 4 warps per (KV head, request, 64-token tile)
         constexpr int DW = D <= 128 ? D : 128;
         const size_t wsmem = std::max((size_t)WinMmaCfg<DW>::SMEM_WORDS * 4, psmem);
-        if (const int rc_ = ensure_dynamic_smem((const void*)window_mma_kernel<DW>, wsmem,
-                                                "cudaFuncSetAttribute(window_mma_kernel)"))
+        auto kern = gq == 4 ? window_mma_kernel<DW, 4> : window_mma_kernel<DW, 8>;
+        if (const int rc_ = ensure_dynamic_smem((const void*)kern, wsmem, "cudaFuncSetAttribute(window_mma_kernel)"))
             return rc_;
         const int prof_k = prof_begin(4, st);
-        launch_dependent(window_mma_kernel<DW>, dim3(P.Hkv, P.batch, P.n_win_tiles + 1), dim3(128), wsmem, st, P);
+        launch_dependent(kern, wgrid, dim3(128), wsmem, st, P);
         prof_end(prof_k, st);
     } else {
         const size_t wsmem = std::max(((size_t)P.g * D + (size_t)P.g * kWinTile + 2 * P.g) * 4 +
                                           (size_t)2 * kWinTile * (D / 2 + 1) * 4, psmem);
-        if (const int rc_ = ensure_dynamic_smem((const void*)window_kernel<D>, wsmem, "cudaFuncSetAttribute(window_kernel)"))
+        auto kern = gq == 4 ? window_kernel<D, 4> : gq == 8 ? window_kernel<D, 8> : window_kernel<D, 16>;
+        if (const int rc_ = ensure_dynamic_smem((const void*)kern, wsmem, "cudaFuncSetAttribute(window_kernel)"))
             return rc_;
         const int prof_k = prof_begin(4, st);
-        launch_dependent(window_kernel<D>, dim3(P.Hkv, P.batch, P.n_win_tiles + 1), dim3(kCombThreads), wsmem, st, P);
+        launch_dependent(kern, wgrid, dim3(kCombThreads), wsmem, st, P);
         prof_end(prof_k, st);
     }
     rc = check_cuda("window kernel launch");
@@ -1166,7 +1166,6 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
     if (!done) {
         const int nwarps = std::min(16, P.Hkv);
         const int threads = 32 * nwarps;
-        const int gq = P.g <= 4 ? 4 : (P.g <= 8 ? 8 : 16);
         const size_t smem = ((size_t)P.Hq * D + (size_t)nwarps * gq * 32) * 4;
         auto pick = [&](auto kern) -> int {
             if (const int rc_ = ensure_dynamic_smem((const void*)kern, smem, "cudaFuncSetAttribute(history_simt_kernel)"))
