@@ -241,17 +241,25 @@ def build_decode_workload(rank, steps_total):
 
 
 def decode_step(w, i, kernel):
+    """One decode step: the fused call (oscar_decode_step) for the default
+    kernels; the append and decode calls for the CUDA-core history path."""
     from rotated_int2_kv_gb300 import ops
     s = i % CYCLE
+    if kernel == "auto":
+        ops.decode_step(w["cache"], w["newk"][s], w["newv"][s], w["qs"][s], w["pt"], w["lens"][s], w["max_len"],
+                        w["ws"], out=w["out"])
+        return
     ops.quantize_append(w["cache"], w["newk"][s], w["newv"][s], w["cu1"], w["starts"][s], w["pt"])
     ops.decode_attention(w["cache"], w["qs"][s], w["pt"], w["lens"][s], w["max_len"], w["ws"], out=w["out"],
                          impl=kernel)
 
 
-def launches_per_step():
-    # append: one launch when the step appends at most W tokens (the window row
-    # writes ride with the quantisation), else quantise + window copy;
-    # decode: window (with the query preparation) + history + combine
+def launches_per_step(kernel="auto"):
+    # fused step: (append + query preparation + window tiles), history, combine;
+    # the two-call path: the append (one launch when the step appends at most W
+    # tokens, else quantise + window copy), then window + history + combine
+    if kernel == "auto":
+        return 3
     return (1 if B <= W_RECENT else 2) + 3
 
 
@@ -542,7 +550,8 @@ def main():
     # per-kernel breakdown from a separate pass (every launch between event pairs,
     # which costs the step some time, so it is not the timed region)
     nb = min(args.steps, 200)
-    kinds = ((ops.PROF_HISTORY, "history"), (ops.PROF_QUANTIZE, "append (quantise + window rows)"),
+    kinds = ((ops.PROF_HISTORY, "history"), (ops.PROF_STEP_PRE, "append + query prep + window (one launch)"),
+             (ops.PROF_QUANTIZE, "append (quantise + window rows)"),
              (ops.PROF_WINDOW_COPY, "window_copy"), (ops.PROF_WINDOW, "window + query prep"),
              (ops.PROF_COMBINE, "combine"))
     ops.profile_enable([k for k, _ in kinds])
@@ -594,7 +603,7 @@ def main():
                          "history_ms_per_step": hist_ms / max(hist_n, 1),
                          "pct_of_8TBs": (achieved / 8000.0) if achieved else None},
             "kernel_ms_per_step": kernel_ms,
-            "gpu_launches": launches_per_step() * args.steps,
+            "gpu_launches": launches_per_step(args.decode_kernel) * args.steps,
             "bits_per_kv_element": bits_per_element(),
             "clocks": clk}
     # ---- end to end through the C ABI with host buffers ----------------------
@@ -651,8 +660,12 @@ def e2e_measure(w, args, ws):
         dk.copy_(hk[s], non_blocking=True)
         dv.copy_(hv[s], non_blocking=True)
         dq.copy_(hq[s], non_blocking=True)
-        ops.quantize_append(w["cache"], dk, dv, w["cu1"], w["starts"][s], w["pt"])
-        ops.decode_attention(w["cache"], dq, w["pt"], w["lens"][s], w["max_len"], w["ws"], out=w["out"])
+        if args.decode_kernel == "auto":
+            ops.decode_step(w["cache"], dk, dv, dq, w["pt"], w["lens"][s], w["max_len"], w["ws"], out=w["out"])
+        else:
+            ops.quantize_append(w["cache"], dk, dv, w["cu1"], w["starts"][s], w["pt"])
+            ops.decode_attention(w["cache"], dq, w["pt"], w["lens"][s], w["max_len"], w["ws"], out=w["out"],
+                                 impl=args.decode_kernel)
         hout.copy_(w["out"], non_blocking=True)
         tokens += int((LB + s + 1).sum())
     e1.record(stream)

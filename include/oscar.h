@@ -293,6 +293,29 @@ int oscar_decode_attention(const oscar_config* cfg, const oscar_layer_cache* cac
                            int32_t batch, int32_t max_seq_len, float* out,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/* One fused decode step: the append of one new token per request followed
+ * by attention over the cache that includes it.  The result (out, and every
+ * byte written to the cache) is that of
+ *   oscar_quantize_append(k_new, v_new, cu_new = 0, 1, .., batch,
+ *                         start_pos = seq_lens - 1, req_idx, page_table)
+ *   oscar_decode_attention(q, page_table, seq_lens, req_idx, ...)
+ * on the same stream, in three launches instead of four: the append, the
+ * query preparation and the BF16 window tiles run in one grid (the window
+ * tiles read the new token from k_new / v_new, the append writes it to its
+ * window row and quantises the token leaving the recent window), then the
+ * history kernel and the combine.
+ * Arguments (device unless marked): as oscar_decode_attention, plus
+ *  k_new, v_new  [batch][Hkv][d] in cfg->kv_dtype: request b's new token,
+ *                position seq_lens[b] - 1.
+ * seq_lens counts the new token.  A request whose length or window row is
+ * invalid is flagged as by oscar_decode_attention and appends nothing. */
+int oscar_decode_step(const oscar_config* cfg, const oscar_layer_cache* cache,
+                      const void* k_new, const void* v_new, const void* q,
+                      const int32_t* page_table, int64_t pt_stride,
+                      const int32_t* seq_lens, const int32_t* req_idx,
+                      int32_t batch, int32_t max_seq_len, float* out,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* Same contract and arguments as oscar_decode_attention, but the history is
  * always processed by the CUDA-core (fp32 FFMA) kernel instead of the
  * tensor-core one.  Kept as the measured baseline for the choice of tensor
@@ -375,7 +398,9 @@ int oscar_prefill_attention(const oscar_config* cfg, const oscar_layer_cache* ca
  * queries) and 5 the combine kernel of oscar_decode_attention; 1 the quantise
  * kernel (for appends of at most W tokens it also writes the window rows) and
  * 2 the window-copy kernel (larger appends) of oscar_quantize_append; 6 the
- * attention kernel of oscar_prefill_attention.  Kind 3 is reserved and never
+ * attention kernel of oscar_prefill_attention; 7 the first launch of
+ * oscar_decode_step (append, query preparation and window tiles; its history
+ * kernel and combine are kinds 0 and 5).  Kind 3 is reserved and never
  * recorded.  A timed launch gets a CUDA event pair on
  * the call's stream (two cudaEventRecord, which also separate it from its
  * neighbours). */

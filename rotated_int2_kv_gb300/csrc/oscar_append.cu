@@ -19,98 +19,10 @@
 //     the spill reads of kernel 1 ahead of the ring overwrites.
 #include <algorithm>
 
-#include "oscar_append_common.cuh"
+#include "oscar_append_step.cuh"
 
 namespace oscar {
 
-// Quantises one rotated head vector held by a warp (lane: channels lane·CPL ..
-// lane·CPL + CPL - 1) and writes its codes and (s, z) pairs into the record.
-// y came from a sequential fp32 FMA chain and lies within e of x·R rounded to
-// fp32; every (s, z) or code decision that y ± e could change is taken again on
-// y values formed by the compensated dot product of xk (the vector's bf16
-// elements) with the columns of R (row-major, row stride D).
-template <int D, class XF>
-__device__ __forceinline__ void quantize_store(const AppendParams& P, float (&y)[D / 32], int slot, int h, int mat,
-                                               int lane, float e, XF xk, const float* R) {
-    constexpr int CPL = D / 32;
-    const int lpg = P.G / CPL;       // lanes per group (4..32)
-    const float r = P.clip;
-    const int rec_off_codes = mat ? D / 4 : 0;
-    const int ng = D / P.G;
-    const bool fp8 = P.fp8 != 0;
-    const int rec_off_sz = D / 2 + (mat ? (fp8 ? 2 : 4) * ng : 0);
-    auto group_extremes = [&](float& mn, float& mx) {
-        mn = y[0];
-        mx = y[0];
-#pragma unroll
-        for (int j = 1; j < CPL; ++j) { mn = fminf(mn, y[j]); mx = fmaxf(mx, y[j]); }
-        for (int off = 1; off < lpg; off <<= 1) {
-            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        }
-    };
-    float mn, mx;
-    group_extremes(mn, mx);
-    uint32_t exact = 0;              // channels j of this lane whose y is already the compensated one
-    const bool unc = sz_uncertain(mn, mx, r, e, fp8);
-    if (__any_sync(0xffffffffu, unc)) {
-        // the extremes of an uncertain group lie among its channels within 2e of
-        // the computed ones: form those exactly and take the extremes again
-        const float tlo = __fadd_ru(mn, __fmul_ru(2.0f, e)), thi = __fsub_rd(mx, __fmul_ru(2.0f, e));
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            uint32_t m = __ballot_sync(0xffffffffu, unc && (y[j] <= tlo || y[j] >= thi));
-            while (m) {
-                const int L = __ffs(m) - 1;
-                m &= m - 1;
-                const float ye = dot2_warp<D>(xk, R, D, L * CPL + j, lane);
-                if (lane == L) {
-                    y[j] = ye;
-                    exact |= 1u << j;
-                }
-            }
-        }
-        group_extremes(mn, mx);
-    }
-    const SZ sz = sz_decide(mn, mx, r, fp8);
-    const float s = sz.s, z = sz.z;
-    const float band = s != 0.0f ? code_band(e, __frcp_rn(3.0f * s)) : 0.0f;
-    uint32_t bits = 0;
-#pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-        float u = s != 0.0f ? __fdiv_rn(__fsub_rn(y[j], z), s) : 0.0f;
-        uint32_t m = __ballot_sync(0xffffffffu, s != 0.0f && !((exact >> j) & 1u) && code_near_boundary(u, band));
-        while (m) {
-            const int L = __ffs(m) - 1;
-            m &= m - 1;
-            const float ye = dot2_warp<D>(xk, R, D, L * CPL + j, lane);
-            if (lane == L) u = __fdiv_rn(__fsub_rn(ye, z), s);
-        }
-        const uint32_t c = s != 0.0f ? (uint32_t)fminf(fmaxf(rintf(u), 0.0f), 3.0f) : 0u;
-        bits |= c << (2 * j);
-    }
-    uint8_t* rec = P.records + (int64_t)slot * P.slot_bytes + (int64_t)h * P.rec_bytes;
-    if (CPL >= 4) {
-#pragma unroll
-        for (int bj = 0; bj < CPL / 4; ++bj)
-            rec[rec_off_codes + lane * (CPL / 4) + bj] = (uint8_t)(bits >> (8 * bj));
-    } else {  // CPL == 2: two lanes share a byte
-        const uint32_t other = __shfl_xor_sync(0xffffffffu, bits, 1);
-        if ((lane & 1) == 0) rec[rec_off_codes + lane / 2] = (uint8_t)(bits | (other << 4));
-    }
-    if ((lane % lpg) == 0) store_sz(rec, rec_off_sz, lane / lpg, sz, fp8);
-}
-
-// Σ x² of a vector, summed over the warp (lane: channels lane·CPL ..).
-template <int CPL>
-__device__ __forceinline__ float warp_sum_sq(const float (&x)[CPL]) {
-    float q = 0.0f;
-#pragma unroll
-    for (int j = 0; j < CPL; ++j) q = fmaf(x[j], x[j], q);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) q += __shfl_xor_sync(0xffffffffu, q, off);
-    return q;
-}
 
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads)
@@ -397,45 +309,6 @@ quantize_small_kernel(AppendParams P) {
     }
 }
 
-// 32 consecutive rows of one column of a 256-wide fp32 matrix (row stride 1024
-// bytes), all loads issued back to back in one statement.
-__device__ __forceinline__ void ld32_col256(const float* p, float (&r)[32]) {
-    asm volatile(
-        "ld.global.nc.f32 %0, [%32+0];\n\t"
-        "ld.global.nc.f32 %1, [%32+1024];\n\t"
-        "ld.global.nc.f32 %2, [%32+2048];\n\t"
-        "ld.global.nc.f32 %3, [%32+3072];\n\t"
-        "ld.global.nc.f32 %4, [%32+4096];\n\t"
-        "ld.global.nc.f32 %5, [%32+5120];\n\t"
-        "ld.global.nc.f32 %6, [%32+6144];\n\t"
-        "ld.global.nc.f32 %7, [%32+7168];\n\t"
-        "ld.global.nc.f32 %8, [%32+8192];\n\t"
-        "ld.global.nc.f32 %9, [%32+9216];\n\t"
-        "ld.global.nc.f32 %10, [%32+10240];\n\t"
-        "ld.global.nc.f32 %11, [%32+11264];\n\t"
-        "ld.global.nc.f32 %12, [%32+12288];\n\t"
-        "ld.global.nc.f32 %13, [%32+13312];\n\t"
-        "ld.global.nc.f32 %14, [%32+14336];\n\t"
-        "ld.global.nc.f32 %15, [%32+15360];\n\t"
-        "ld.global.nc.f32 %16, [%32+16384];\n\t"
-        "ld.global.nc.f32 %17, [%32+17408];\n\t"
-        "ld.global.nc.f32 %18, [%32+18432];\n\t"
-        "ld.global.nc.f32 %19, [%32+19456];\n\t"
-        "ld.global.nc.f32 %20, [%32+20480];\n\t"
-        "ld.global.nc.f32 %21, [%32+21504];\n\t"
-        "ld.global.nc.f32 %22, [%32+22528];\n\t"
-        "ld.global.nc.f32 %23, [%32+23552];\n\t"
-        "ld.global.nc.f32 %24, [%32+24576];\n\t"
-        "ld.global.nc.f32 %25, [%32+25600];\n\t"
-        "ld.global.nc.f32 %26, [%32+26624];\n\t"
-        "ld.global.nc.f32 %27, [%32+27648];\n\t"
-        "ld.global.nc.f32 %28, [%32+28672];\n\t"
-        "ld.global.nc.f32 %29, [%32+29696];\n\t"
-        "ld.global.nc.f32 %30, [%32+30720];\n\t"
-        "ld.global.nc.f32 %31, [%32+31744];\n\t"
-        : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7]), "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]), "=f"(r[14]), "=f"(r[15]), "=f"(r[16]), "=f"(r[17]), "=f"(r[18]), "=f"(r[19]), "=f"(r[20]), "=f"(r[21]), "=f"(r[22]), "=f"(r[23]), "=f"(r[24]), "=f"(r[25]), "=f"(r[26]), "=f"(r[27]), "=f"(r[28]), "=f"(r[29]), "=f"(r[30]), "=f"(r[31])
-        : "l"(p));
-}
 
 // Decode-step appends at d = 256, where R (256 KB) does not fit the shared-memory
 // staging: one block of D threads per head vector, thread c forming output
@@ -524,51 +397,6 @@ quantize_vec_kernel(AppendParams P) {
     }
 }
 
-// ---------------------------------------------------------------------------
-// Decode-step appends in one launch.  When a call appends at most W tokens in
-// total, every request's new tokens all land in a BF16 window (sink below S,
-// else the ring), and the tokens leaving the window are exactly the positions
-// q = p - W >= S of the new positions p: position q's ring row p % W is the one
-// that new position p overwrites.  So one warp per (new token, KV head) reads
-// the leaving row, writes the new row over it, and quantises the leaving row
-// into its history record (each lane reads and then writes the same elements,
-// which orders the two), in place of the quantise kernel followed by the
-// window copy.
-// ---------------------------------------------------------------------------
-
-// Resolves new row t (K or V of head h) of a decode-step append: request b,
-// position p, window row rq; false (with status bits) when the row is invalid.
-__device__ __forceinline__ bool resolve_new_row(const AppendParams& P, int64_t t, int& b, int& p, int& rq, int& bits) {
-    b = find_request(P.cu_new, P.batch, (int)t);
-    const int L0 = P.start_pos[b];
-    const int c0 = P.cu_new[b], n = P.cu_new[b + 1] - c0;
-    p = L0 + (int)(t - c0);
-    rq = P.req_idx ? P.req_idx[b] : b;
-    bits = 0;
-    if (L0 < 0 || t - c0 >= n) bits |= OSCAR_DEV_BAD_LEN;
-    if (rq < 0 || rq >= P.max_reqs) bits |= OSCAR_DEV_BAD_REQ;
-    return bits == 0;
-}
-
-// Row of position p (K or V of head h) in the sink or the recent ring of window row rq.
-__device__ __forceinline__ int64_t window_row(const AppendParams& P, int rq, int p, int h, int mat, int D) {
-    return p < P.S ? ((((int64_t)rq * P.S + p) * P.Hkv + h) * 2 + mat) * D
-                   : ((((int64_t)rq * P.W + p % P.W) * P.Hkv + h) * 2 + mat) * D;
-}
-
-// Slot of the history record of position q of request b, or -1 (with status bits).
-__device__ __forceinline__ int history_slot(const AppendParams& P, int b, int q, int& bits) {
-    if (q >= P.pt_stride) {
-        bits |= OSCAR_DEV_BAD_LEN;
-        return -1;
-    }
-    const int sl = P.page_table[(int64_t)b * P.pt_stride + q];
-    if (sl < 0 || sl >= P.num_slots) {
-        bits |= OSCAR_DEV_BAD_SLOT;
-        return -1;
-    }
-    return sl;
-}
 
 // d <= 128: one warp per (new token, KV head), R staged in shared memory.
 template <int D>
@@ -645,58 +473,12 @@ template <int D>
 __global__ void __launch_bounds__(D, 2)
 append_step_vec_kernel(AppendParams P) {
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
-    constexpr int CPL = D / 32;
     __shared__ float sx[D];
     __shared__ float sy[D];
     const int mat = blockIdx.y;
-    const float* R = mat ? P.rot_v : P.rot_k;
-    const void* src_new = mat ? P.v : P.k;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t total = P.total_new * P.Hkv;
-    for (int64_t e = blockIdx.x; e < total; e += gridDim.x) {
-        const int64_t t = e / P.Hkv;
-        const int h = (int)(e % P.Hkv);
-        int b, p, rq, bits;
-        const bool ok = resolve_new_row(P, t, b, p, rq, bits);
-        const int q = p - P.W;
-        const bool spill = ok && q >= P.S;
-        const int slot = spill ? history_slot(P, b, q, bits) : -1;
-        const float xs = spill ? bf16_bits_to_f32(P.recent[window_row(P, rq, q, h, mat, D) + tid]) : 0.f;
-        if (ok) {   // the new element over the leaving one (this thread read it above)
-            const float xn = load_elem(src_new, (t * P.Hkv + h) * D + tid, P.kv_dtype);
-            (p < P.S ? P.sink : P.recent)[window_row(P, rq, p, h, mat, D) + tid] = f32_to_bf16_bits(xn);
-        }
-        if (bits && tid == 0) set_status(P.status, bits);
-        if (slot < 0) continue;                      // the same decision in every thread
-        sx[tid] = xs;
-        __syncthreads();
-        float y = 0.f;
-        const float* rc = R + tid;
-        for (int k0 = 0; k0 < D; k0 += 32) {         // 32 rows of R in flight, then their FMAs in order
-            float r[32];
-            if constexpr (D == 256) {
-                ld32_col256(rc + (int64_t)k0 * D, r);
-            } else {
-#pragma unroll
-                for (int u = 0; u < 32; ++u) r[u] = __ldg(rc + (int64_t)(k0 + u) * D);
-            }
-#pragma unroll
-            for (int u = 0; u < 32; ++u) y = fmaf(sx[k0 + u], r[u], y);
-        }
-        sy[tid] = y;
-        __syncthreads();
-        if (warp == 0) {
-            float yv[CPL], xv[CPL];
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-                yv[j] = sy[lane * CPL + j];
-                xv[j] = sx[lane * CPL + j];
-            }
-            const float eb = fma_chain_bound<D>(warp_sum_sq<CPL>(xv));
-            quantize_store<D>(P, yv, slot, h, mat, lane, eb, [&](int k) { return sx[k]; }, R);
-        }
-        __syncthreads();                             // sx and sy are reused by the next item
-    }
+    for (int64_t e = blockIdx.x; e < total; e += gridDim.x)
+        append_vec_item<D>(P, e / P.Hkv, (int)(e % P.Hkv), mat, sx, sy);
 }
 
 // Copies the new rows that land in a BF16 window: positions below S go to the

@@ -18,6 +18,7 @@
 #include "oscar_internal.h"
 #include "oscar_device.cuh"
 #include "oscar_decode_common.cuh"
+#include "oscar_append_step.cuh"
 
 namespace oscar {
 
@@ -402,16 +403,23 @@ constexpr int kCombThreads = 128;      // window kernel
 constexpr int kMergeThreads = 512;     // combine kernel
 constexpr int kWinTile = 64;
 
-template <int D, int GQ>
-__global__ void __launch_bounds__(kCombThreads, D >= 256 ? 2 : 6) window_kernel(DecodeParams P) {
-    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
+// The new token of each request (position L - 1) read from the step's input
+// rows (row b: [batch][Hkv][d] K and V, element type dtype) instead of the
+// recent ring, for the fused decode step, whose append writes the ring in the
+// same launch.
+struct NewRowSrc {
+    const void* k;
+    const void* v;
+    int dtype;
+    int on;
+};
+
+// One 64-token window tile (wt) of KV head hk, request b on the CUDA cores:
+// the (m, l, o) partial of every query head of the KV head.  kCombThreads threads.
+template <int D>
+__device__ __forceinline__ void window_tile_simt(const DecodeParams& P, int hk, int b, int wt, float* s_w,
+                                                 NewRowSrc nr) {
     constexpr int kRowW = D / 2 + 1;               // words per staged bf16 row (odd: conflict-free)
-    extern __shared__ __align__(16) float s_w[];
-    const int hk = blockIdx.x, b = blockIdx.y, wt = (int)blockIdx.z - 1;
-    if (wt < 0) {                                  // the first z-slice: query preparation
-        prep_slice<D, GQ>(P, hk, b, s_w);
-        return;
-    }
     const int g = P.g, S = P.S, W = P.W;
     float* sq = s_w;                               // [g][D] q · qscale
     float* sp = sq + g * D;                        // [g][kWinTile] logits -> probabilities
@@ -450,11 +458,26 @@ __global__ void __launch_bounds__(kCombThreads, D >= 256 ? 2 : 6) window_kernel(
             const int t = i / C8, c8 = i % C8;
             const int tt = t0 + t;
             if (t < nt) {
-                const uint16_t* base = (tt < sink_end)
-                    ? P.sink + (((int64_t)rq * S + tt) * P.Hkv + hk) * 2 * D
-                    : P.recent + (((int64_t)rq * W + (rec_lo + tt - sink_end) % W) * P.Hkv + hk) * 2 * D;
-                kq[u] = *reinterpret_cast<const uint4*>(base + c8 * 8);
-                vq[u] = *reinterpret_cast<const uint4*>(base + D + c8 * 8);
+                const int pos = tt < sink_end ? tt : rec_lo + tt - sink_end;   // position in the request
+                if (nr.on && pos == L - 1) {           // the step's new token: from the input row
+                    const int64_t e0 = ((int64_t)b * P.Hkv + hk) * D + 8 * c8;
+                    uint32_t kw[4], vw[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        kw[e] = (uint32_t)f32_to_bf16_bits(load_elem(nr.k, e0 + 2 * e, nr.dtype)) |
+                                ((uint32_t)f32_to_bf16_bits(load_elem(nr.k, e0 + 2 * e + 1, nr.dtype)) << 16);
+                        vw[e] = (uint32_t)f32_to_bf16_bits(load_elem(nr.v, e0 + 2 * e, nr.dtype)) |
+                                ((uint32_t)f32_to_bf16_bits(load_elem(nr.v, e0 + 2 * e + 1, nr.dtype)) << 16);
+                    }
+                    kq[u] = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+                    vq[u] = make_uint4(vw[0], vw[1], vw[2], vw[3]);
+                } else {
+                    const uint16_t* base = (tt < sink_end)
+                        ? P.sink + (((int64_t)rq * S + tt) * P.Hkv + hk) * 2 * D
+                        : P.recent + (((int64_t)rq * W + (rec_lo + tt - sink_end) % W) * P.Hkv + hk) * 2 * D;
+                    kq[u] = *reinterpret_cast<const uint4*>(base + c8 * 8);
+                    vq[u] = *reinterpret_cast<const uint4*>(base + D + c8 * 8);
+                }
             }
         }
 #pragma unroll
@@ -549,6 +572,18 @@ __global__ void __launch_bounds__(kCombThreads, D >= 256 ? 2 : 6) window_kernel(
     }
 }
 
+template <int D, int GQ>
+__global__ void __launch_bounds__(kCombThreads, D >= 256 ? 2 : 6) window_kernel(DecodeParams P) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
+    extern __shared__ __align__(16) float s_w[];
+    const int hk = blockIdx.x, b = blockIdx.y, wt = (int)blockIdx.z - 1;
+    if (wt < 0) {                                  // the first z-slice: query preparation
+        prep_slice<D, GQ>(P, hk, b, s_w);
+        return;
+    }
+    window_tile_simt<D>(P, hk, b, wt, s_w, NewRowSrc{nullptr, nullptr, 0, 0});
+}
+
 // ---------------------------------------------------------------------------
 // window on the tensor cores (d <= 128, g <= 8): the same per-tile partials as
 // window_kernel, one block of 4 warps per (KV head, request, 64-token tile).
@@ -608,24 +643,20 @@ struct WinMmaCfg {
     static constexpr int SMEM_WORDS = 2 * kWinTile * RW + KS * 128 + 4 * 128 + 2 * 32;
 };
 
-template <int D, int GQ>
-__global__ void __launch_bounds__(128) window_mma_kernel(DecodeParams P) {
-    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
+// One 64-token window tile (wt) of KV head hk, request b: the (m, l, o) partial
+// of every query head of the KV head.  128 threads; s_wm: WinMmaCfg<D>::SMEM_WORDS.
+template <int D>
+__device__ __forceinline__ void window_tile_mma(const DecodeParams& P, int hk, int b, int wt, uint32_t* s_wm,
+                                                NewRowSrc nr) {
     using namespace wmma_detail;
     using C = WinMmaCfg<D>;
     constexpr int KS = C::KS, RW = C::RW, CPR = C::CPR, NTW = C::NTW;
-    extern __shared__ __align__(16) uint32_t s_wm[];
     uint32_t* sk = s_wm;                               // [64][RW] K rows
     uint32_t* sv = sk + kWinTile * RW;                 // [64][RW] V rows
     uint32_t* sqa = sv + kWinTile * RW;                // [KS][32 lanes][4] q fragments
     uint32_t* spa = sqa + KS * 128;                    // [4 sub-tiles][32 lanes][4] P fragments
     float* smx = reinterpret_cast<float*>(spa + 4 * 128);   // [4 warps][8 heads] sub-tile max
     float* ssm = smx + 32;                                   // [4 warps][8 heads] sub-tile sum
-    const int hk = blockIdx.x, b = blockIdx.y, wt = (int)blockIdx.z - 1;
-    if (wt < 0) {                                  // the first z-slice (scheduled first): query preparation
-        prep_slice<D, GQ>(P, hk, b, reinterpret_cast<float*>(s_wm));
-        return;
-    }
     const int g = P.g, S = P.S, W = P.W;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = lane >> 2, j = lane & 3;
@@ -649,10 +680,23 @@ __global__ void __launch_bounds__(128) window_mma_kernel(DecodeParams P) {
         const int mat = i / (kWinTile * CPR), t = (i / CPR) % kWinTile, c = i % CPR;
         const bool ok = t < nt;
         const int tt = t0 + (ok ? t : 0);
+        const int pos = tt < sink_end ? tt : rec_lo + tt - sink_end;   // position in the request
+        uint32_t* dst = (mat ? sv : sk) + t * RW + 4 * c;
+        if (nr.on && ok && pos == L - 1) {             // the step's new token: from the input row
+            const int64_t e0 = ((int64_t)b * P.Hkv + hk) * D + 8 * c;
+            const void* src = mat ? nr.v : nr.k;
+            uint32_t w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                w[u] = (uint32_t)f32_to_bf16_bits(load_elem(src, e0 + 2 * u, nr.dtype)) |
+                       ((uint32_t)f32_to_bf16_bits(load_elem(src, e0 + 2 * u + 1, nr.dtype)) << 16);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+            continue;
+        }
         const uint16_t* row = (tt < sink_end)
             ? P.sink + (((int64_t)rq * S + tt) * P.Hkv + hk) * 2 * D
             : P.recent + (((int64_t)rq * W + (rec_lo + tt - sink_end) % W) * P.Hkv + hk) * 2 * D;
-        cp_async16_zfill((mat ? sv : sk) + t * RW + 4 * c, row + mat * D + 8 * c, ok ? 16u : 0u);
+        cp_async16_zfill(dst, row + mat * D + 8 * c, ok ? 16u : 0u);
     }
     cp_async_commit();
     {   // q A fragments: entry (kk, lane l, reg e): row (l>>2) + 8·(e&1) (bf16 part / lo part),
@@ -761,6 +805,55 @@ __global__ void __launch_bounds__(128) window_mma_kernel(DecodeParams P) {
         for (int n = 0; n < NTW; ++n)
             *reinterpret_cast<float2*>(op + 8 * n + 2 * j) = make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
     }
+}
+
+template <int D, int GQ>
+__global__ void __launch_bounds__(128) window_mma_kernel(DecodeParams P) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
+    extern __shared__ __align__(16) uint32_t s_wm[];
+    const int hk = blockIdx.x, b = blockIdx.y, wt = (int)blockIdx.z - 1;
+    if (wt < 0) {                                  // the first z-slice (scheduled first): query preparation
+        prep_slice<D, GQ>(P, hk, b, reinterpret_cast<float*>(s_wm));
+        return;
+    }
+    window_tile_mma<D>(P, hk, b, wt, s_wm, NewRowSrc{nullptr, nullptr, 0, 0});
+}
+
+// ---------------------------------------------------------------------------
+// Fused decode step (oscar_decode_step), first of its three launches.  A decode
+// step appends one token per request and then attends; the append touches
+// only the BF16 ring row of the new token (over the token leaving the window)
+// and the history record of the leaving token, and the window attention reads
+// the new token from the step's input rows instead of the ring.  So the three
+// independent parts of a step's front run in one grid of 128-thread blocks:
+//  z = 0, 1:         the append of request y's new K (V) row of KV head x
+//                    (the leaving row quantised into its record by one
+//                    block per vector, thread c forming output channel c);
+//  z = 2:            query preparation of (KV head x, request y);
+//  z = 3 .. nwt + 2: window tile z - 3 of (KV head x, request y).
+// Blocks start in index order, so the longest chains (the appends) start first.
+// The history kernel and the combine follow as in oscar_decode_attention.
+// ---------------------------------------------------------------------------
+template <int D, int GQ, bool MMA>
+__global__ void __launch_bounds__(128) step_pre_kernel(DecodeParams P, AppendParams A, NewRowSrc nr) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
+    extern __shared__ __align__(16) uint32_t s_step[];
+    const int hk = blockIdx.x, b = blockIdx.y, z = (int)blockIdx.z;
+    if (z < 2) {
+        // request b's new token (input row b) is position L - 1; an invalid
+        // request is reported by its prep slice and appends nothing
+        int L, rq;
+        const bool ok = request_valid(P, b, &L, &rq);
+        float* sx = reinterpret_cast<float*>(s_step);
+        append_vec_resolved<D>(A, b, hk, z, b, L - 1, rq, ok, 0, sx, sx + D);
+        return;
+    }
+    if (z == 2) {
+        prep_slice<D, GQ>(P, hk, b, reinterpret_cast<float*>(s_step));
+        return;
+    }
+    if constexpr (MMA) window_tile_mma<D>(P, hk, b, z - 3, s_step, nr);
+    else window_tile_simt<D>(P, hk, b, z - 3, reinterpret_cast<float*>(s_step), nr);
 }
 
 // ---------------------------------------------------------------------------
@@ -1128,6 +1221,9 @@ int launch_history_mma(DecodeParams& P, int head_dim, cudaStream_t st, bool* lau
 }
 
 template <int D>
+static int launch_history_combine(DecodeParams& P, cudaStream_t st, int impl);
+
+template <int D>
 static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
     // the window kernel's grid carries one more z-slice: the query preparation
     // of every (KV head, request)
@@ -1157,6 +1253,15 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
     }
     rc = check_cuda("window kernel launch");
     if (rc) return rc;
+    return launch_history_combine<D>(P, st, impl);
+}
+
+// The history kernel (tensor cores when a variant fits, else CUDA cores) and
+// the combine, after the window partials and the rotated queries are written.
+template <int D>
+static int launch_history_combine(DecodeParams& P, cudaStream_t st, int impl) {
+    int rc = OSCAR_OK;
+    const int gq = prep_bucket(P.g);
     bool done = false;
     const int prof = prof_begin(0, st);
     if (impl != 1) {
@@ -1199,14 +1304,44 @@ static int launch_decode(DecodeParams& P, cudaStream_t st, int impl) {
     return check_cuda("combine_kernel launch");
 }
 
-static int decode_impl(const oscar_config* cfg, const oscar_layer_cache* cache, const void* q,
-                       const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens,
-                       const int32_t* req_idx, int32_t batch, int32_t max_seq_len, float* out,
-                       void* workspace, size_t workspace_bytes, void* stream, int impl) {
-    clear_error();
-    int rc = decode_validate(cfg, cache, batch, max_seq_len, pt_stride);
+// The fused decode step: one launch for the append, the query preparation and
+// the window tiles, then the history kernel and the combine.
+template <int D>
+static int launch_step(DecodeParams& P, const AppendParams& A, NewRowSrc nr, cudaStream_t st) {
+    const int gq = prep_bucket(P.g);
+    const size_t psmem = (size_t)prep_smem_floats(D, gq) * 4;
+    const size_t asmem = (size_t)2 * D * 4;
+    const dim3 grid(P.Hkv, P.batch, P.n_win_tiles + 3);
+    auto go = [&](auto kern, size_t wsmem) -> int {
+        const size_t smem = std::max(std::max(wsmem, psmem), asmem);
+        if (const int rc_ = ensure_dynamic_smem((const void*)kern, smem, "cudaFuncSetAttribute(step_pre_kernel)"))
+            return rc_;
+        const int prof_k = prof_begin(7, st);
+        launch_dependent(kern, grid, dim3(128), smem, st, P, A, nr);
+        prof_end(prof_k, st);
+        return check_cuda("step_pre_kernel launch");
+    };
+    int rc;
+    if constexpr (D <= 128) {
+        if (P.g <= 8) {
+            const size_t wsmem = (size_t)WinMmaCfg<D>::SMEM_WORDS * 4;
+            rc = gq == 4 ? go(step_pre_kernel<D, 4, true>, wsmem) : go(step_pre_kernel<D, 8, true>, wsmem);
+            if (rc) return rc;
+            return launch_history_combine<D>(P, st, 0);
+        }
+    }
+    const size_t wsmem = ((size_t)P.g * D + (size_t)P.g * kWinTile + 2 * P.g) * 4 + (size_t)2 * kWinTile * (D / 2 + 1) * 4;
+    rc = gq == 4 ? go(step_pre_kernel<D, 4, false>, wsmem)
+       : gq == 8 ? go(step_pre_kernel<D, 8, false>, wsmem) : go(step_pre_kernel<D, 16, false>, wsmem);
     if (rc) return rc;
-    if (batch == 0) return OSCAR_OK;
+    return launch_history_combine<D>(P, st, 0);
+}
+
+// Validates a decode call and fills P (batch > 0).
+static int decode_prepare(const oscar_config* cfg, const oscar_layer_cache* cache, const void* q,
+                          const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens,
+                          const int32_t* req_idx, int32_t batch, int32_t max_seq_len, float* out,
+                          void* workspace, size_t workspace_bytes, DecodeParams& P) {
     if (!q || !page_table || !seq_lens || !out) return fail(OSCAR_ERR_NULL, "q, page_table, seq_lens and out are required");
     const int nsm = sm_count();
     if (nsm <= 0) return OSCAR_ERR_CUDA;
@@ -1216,7 +1351,6 @@ static int decode_impl(const oscar_config* cfg, const oscar_layer_cache* cache, 
         return fail(OSCAR_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", workspace_bytes, plan.total);
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
         return fail(OSCAR_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-    DecodeParams P;
     P.q = q;
     P.q_dtype = cfg->q_dtype;
     P.page_table = page_table;
@@ -1264,6 +1398,21 @@ static int decode_impl(const oscar_config* cfg, const oscar_layer_cache* cache, 
     P.wo = reinterpret_cast<float*>(ws + plan.off_wo);
     P.status = status_word();
     if (!P.status) return OSCAR_ERR_CUDA;
+    return OSCAR_OK;
+}
+
+static int decode_impl(const oscar_config* cfg, const oscar_layer_cache* cache, const void* q,
+                       const int32_t* page_table, int64_t pt_stride, const int32_t* seq_lens,
+                       const int32_t* req_idx, int32_t batch, int32_t max_seq_len, float* out,
+                       void* workspace, size_t workspace_bytes, void* stream, int impl) {
+    clear_error();
+    int rc = decode_validate(cfg, cache, batch, max_seq_len, pt_stride);
+    if (rc) return rc;
+    if (batch == 0) return OSCAR_OK;
+    DecodeParams P;
+    rc = decode_prepare(cfg, cache, q, page_table, pt_stride, seq_lens, req_idx, batch, max_seq_len, out,
+                        workspace, workspace_bytes, P);
+    if (rc) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     switch (cfg->head_dim) {
         case 64: return launch_decode<64>(P, st, impl);
@@ -1286,6 +1435,56 @@ extern "C" int oscar_decode_attention_simt(const oscar_config* cfg, const oscar_
                                            void* workspace, size_t workspace_bytes, void* stream) {
     return decode_impl(cfg, cache, q, page_table, pt_stride, seq_lens, req_idx, batch, max_seq_len, out,
                        workspace, workspace_bytes, stream, 1);
+}
+
+extern "C" int oscar_decode_step(const oscar_config* cfg, const oscar_layer_cache* cache, const void* k_new,
+                                 const void* v_new, const void* q, const int32_t* page_table, int64_t pt_stride,
+                                 const int32_t* seq_lens, const int32_t* req_idx, int32_t batch,
+                                 int32_t max_seq_len, float* out, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+    clear_error();
+    int rc = decode_validate(cfg, cache, batch, max_seq_len, pt_stride);
+    if (rc) return rc;
+    if (batch == 0) return OSCAR_OK;
+    if (!k_new || !v_new) return fail(OSCAR_ERR_NULL, "k_new and v_new are required");
+    DecodeParams P;
+    rc = decode_prepare(cfg, cache, q, page_table, pt_stride, seq_lens, req_idx, batch, max_seq_len, out,
+                        workspace, workspace_bytes, P);
+    if (rc) return rc;
+    // the append of row b (position seq_lens[b] - 1): the fields the per-vector
+    // append reads; the request resolution is the fused kernel's
+    AppendParams A = {};
+    A.k = k_new;
+    A.v = v_new;
+    A.kv_dtype = cfg->kv_dtype;
+    A.req_idx = req_idx;
+    A.page_table = page_table;
+    A.pt_stride = pt_stride;
+    A.batch = batch;
+    A.records = cache->records;
+    A.sink = cache->sink;
+    A.recent = cache->recent;
+    A.rot_k = cache->rot_k;
+    A.rot_v = cache->rot_v;
+    A.num_slots = cache->num_slots;
+    A.max_reqs = cache->max_reqs;
+    A.Hkv = cfg->num_kv_heads;
+    A.S = cfg->sink;
+    A.W = cfg->recent;
+    A.G = cfg->group_size;
+    A.rec_bytes = P.rec_bytes;
+    A.slot_bytes = P.slot_bytes;
+    A.fp8 = P.fp8;
+    A.clip = cfg->clip_ratio;
+    A.total_new = batch;
+    A.status = P.status;
+    const NewRowSrc nr{k_new, v_new, cfg->kv_dtype, 1};
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    switch (cfg->head_dim) {
+        case 64: return launch_step<64>(P, A, nr, st);
+        case 128: return launch_step<128>(P, A, nr, st);
+        default: return launch_step<256>(P, A, nr, st);
+    }
 }
 
 // ---------------------------------------------------------------------------

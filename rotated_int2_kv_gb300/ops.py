@@ -70,6 +70,10 @@ _SIGS = {
                                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
+    "oscar_decode_step": ([ctypes.POINTER(CConfig), ctypes.POINTER(CLayerCache), ctypes.c_void_p, ctypes.c_void_p,
+                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                           ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                           ctypes.c_void_p], ctypes.c_int),
     "oscar_decode_attention_simt": ([ctypes.POINTER(CConfig), ctypes.POINTER(CLayerCache), ctypes.c_void_p,
                                      ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
@@ -372,6 +376,27 @@ def decode_attention(cache, q, page_table, seq_lens, max_seq_len, workspace, req
     return out
 
 
+def decode_step(cache, k_new, v_new, q, page_table, seq_lens, max_seq_len, workspace, req_idx=None, out=None,
+                stream=None):
+    """Fused decode step (oscar_decode_step): append k_new, v_new (B, Hkv, d), request b's
+    token at position seq_lens[b] - 1, then attend with q (B, Hq, d) -> out (B, Hq, d) fp32."""
+    cfg = cache.cfg
+    B = q.shape[0]
+    if k_new.shape[0] != B or v_new.shape[0] != B:
+        raise ValueError("k_new and v_new need one row per request")
+    dev = _device_of(cache, k_new, v_new, q, page_table, seq_lens, req_idx, out, workspace)
+    with torch.cuda.device(dev):
+        if out is None:
+            out = torch.empty((B, cfg.num_q_heads, cfg.head_dim), dtype=torch.float32, device=dev)
+        _check(lib().oscar_decode_step(
+            ctypes.byref(cfg.c()), ctypes.byref(cache.c()), _ptr(k_new, cfg.kv_dtype, "k_new"),
+            _ptr(v_new, cfg.kv_dtype, "v_new"), _ptr(q, cfg.q_dtype, "q"), _ptr(page_table, torch.int32, "page_table"),
+            page_table.shape[1], _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(req_idx, torch.int32, "req_idx"), B,
+            max_seq_len, _ptr(out, torch.float32, "out"), _ptr(workspace, torch.uint8, "workspace"),
+            workspace.numel(), _stream(stream, dev)))
+    return out
+
+
 def prefill_workspace_bytes(cfg, batch, total_q):
     out = ctypes.c_size_t()
     _check(lib().oscar_prefill_workspace_bytes(ctypes.byref(cfg.c()), batch, total_q, ctypes.byref(out)))
@@ -414,6 +439,7 @@ def selftest_bounded_wait(budget_cycles, complete, stream=None):
 
 
 PROF_HISTORY, PROF_QUANTIZE, PROF_WINDOW_COPY, PROF_PREP, PROF_WINDOW, PROF_COMBINE, PROF_PREFILL = 0, 1, 2, 3, 4, 5, 6
+PROF_STEP_PRE = 7
 
 
 def profile_enable(kinds=(PROF_HISTORY,)):
