@@ -39,8 +39,10 @@ namespace oscar {
 
 namespace {
 
-constexpr int kPfRows = 64;         // (query, head) rows per attention CTA: 4 warps × 16
-constexpr int kPfThreads = 128;
+// (query, head) rows of an attention CTA: 16 per warp, 8 warps for d <= 128 (the
+// expanded history tile is shared by 128 rows), 4 for d = 256 (register budget)
+__host__ __device__ constexpr int pf_warps(int D) { return D <= 128 ? 8 : 4; }
+constexpr int kPfMaxRows = 128;
 constexpr int kMaxPrefillBatch = 4096;
 
 struct PrefillParams {
@@ -252,19 +254,27 @@ __global__ void __launch_bounds__(D) prefill_dense_kernel(PrefillParams P) {
 // ---------------------------------------------------------------------------
 template <int D, int TT>
 struct PfCfg {
+    static constexpr int WARPS = pf_warps(D);
+    static constexpr int THREADS = 32 * WARPS;
+    static constexpr int ROWS = 16 * WARPS;            // (query, head) rows per CTA
     static constexpr int RS = D + 8;                   // halves per staged row (16-byte pad: conflict-free ldmatrix)
-    static constexpr int Q_HALVES = 2 * kPfRows * RS;  // q̃ hi, lo
+    static constexpr int Q_HALVES = 2 * ROWS * RS;     // q̃ hi, lo
     static constexpr int T_HALVES = 4 * TT * RS;       // history: K codes, V codes; BF16: K hi, K lo, V hi, V lo
-    static size_t smem(int ng) {
-        return (size_t)(Q_HALVES + T_HALVES) * 2 + (size_t)4 * TT * ng * 4 + (size_t)TT * 4;
+    static constexpr int RAW_MAX = D / 2 + 16 * (D / 32);   // largest record (group 32, fp16 pairs)
+    // shared bytes: q̃, tile, (s, z) [4][TT][ng], token validity [TT], slots [3][TT],
+    // raw records of two tiles [2][TT][rec_bytes]
+    static size_t smem(int ng, int rec_bytes) {
+        return (size_t)(Q_HALVES + T_HALVES) * 2 + (size_t)4 * TT * ng * 4 + (size_t)TT * 4 + (size_t)3 * TT * 4 +
+               (size_t)2 * TT * rec_bytes;
     }
 };
 
 template <int D, int G, int TT>
-__global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(PrefillParams P) {
+__global__ void __launch_bounds__(PfCfg<D, TT>::THREADS) prefill_attn_kernel(PrefillParams P) {
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     using C_ = PfCfg<D, TT>;
     constexpr int RS = C_::RS, KS = D / 16, NTO = D / 8, NTT = TT / 8, KT = TT / 16, NG = D / G;
+    constexpr int kPfRows = C_::ROWS, kPfThreads = C_::THREADS;
     constexpr int NTG = G / 8;                         // output n-tiles per group
     extern __shared__ __align__(16) unsigned char smem[];
     __half* sQh = reinterpret_cast<__half*>(smem);
@@ -272,6 +282,8 @@ __global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(PrefillParams 
     __half* sT = sQl + kPfRows * RS;                   // 4 tiles of TT rows
     float* sSZ = reinterpret_cast<float*>(sT + 4 * TT * RS);   // [4][TT][NG]: s_K, z_K, s_V, z_V
     int* sOk = reinterpret_cast<int*>(sSZ + 4 * TT * NG);      // [TT] token valid
+    int* sSlot = sOk + TT;                                     // [3][TT] slots of history tiles i, i+1, i+2 (mod 3)
+    unsigned char* sRaw = reinterpret_cast<unsigned char*>(sSlot + 3 * TT);   // [2][TT][rec_bytes] records
     const int rb = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = lane >> 2, j = lane & 3;
@@ -368,24 +380,59 @@ __global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(PrefillParams 
     };
 
     // ---- history tiles: INT2 records of KV head hk ----
+    // Pipeline over tiles of TT tokens: the records of tile i + 1 are copied
+    // (8-byte cp.async, slot ids from a shared table filled one tile earlier)
+    // while tile i is expanded and multiplied; the page-table entries of tile
+    // i + 2 are loaded at the start of iteration i.
     const bool fp8 = P.fp8 != 0;
+    const int rb_ = P.rec_bytes;
     const int rec_v = D / 4, rec_ks = D / 2, rec_vs = D / 2 + (fp8 ? 2 : 4) * NG;
-    for (int t0 = S; t0 < hist_hi; t0 += TT) {
+    const int nht = hist_hi > S ? (hist_hi - S + TT - 1) / TT : 0;
+    auto tile_slot = [&](int i) -> int {               // slot of token tid of history tile i, or -1
+        const int t = S + i * TT + tid;
+        if (tid >= TT || i >= nht || t >= hist_hi) return -1;
+        const int sl = P.page_table[(int64_t)b * P.pt_stride + t];
+        if (sl >= 0 && sl < P.num_slots) return sl;
+        set_status(P.status, OSCAR_DEV_BAD_SLOT);
+        return -1;
+    };
+    auto issue = [&](int i) {                          // records of tile i into raw buffer i & 1
+        const int nch = rb_ / 8;
+        const int* sl_ = sSlot + (i % 3) * TT;
+        unsigned char* dst = sRaw + (size_t)(i & 1) * TT * rb_;
+        for (int c = tid; c < TT * nch; c += kPfThreads) {
+            const int tt = c / nch, ch = c - tt * nch;
+            const int sl = sl_[tt];
+            if (sl >= 0)
+                cp_async8(dst + tt * rb_ + 8 * ch, P.records + (int64_t)sl * P.slot_bytes + (int64_t)hk * rb_ + 8 * ch);
+        }
+        cp_async_commit();
+    };
+    if (nht > 0) {
+        const int s0 = tile_slot(0), s1 = tile_slot(1);
+        if (tid < TT) {
+            sSlot[tid] = s0;
+            sSlot[TT + tid] = s1;
+        }
+        __syncthreads();
+        issue(0);
+    }
+    for (int i = 0; i < nht; ++i) {
+        const int t0 = S + i * TT;
         const int nt = min(TT, hist_hi - t0);
-        __syncthreads();                               // the previous tile's readers are done
+        const int s2 = tile_slot(i + 2);               // in flight through the wait and the expansion
+        cp_async_wait<0>();                            // this thread's copies of tile i
+        __syncthreads();                               // tile i's records visible; the previous tile's readers are done
+        if (i + 1 < nht) issue(i + 1);
+        const unsigned char* raw = sRaw + (size_t)(i & 1) * TT * rb_;
+        const int* slt = sSlot + (i % 3) * TT;
         // item (token, 8-channel chunk, K|V): 8 codes as fp16 values, one 16-byte store
-        for (int i = tid; i < TT * (D / 8) * 2; i += kPfThreads) {
-            const int mat = i / (TT * (D / 8));
-            const int tt = (i / (D / 8)) % TT, cc = i % (D / 8);
+        for (int it = tid; it < TT * (D / 8) * 2; it += kPfThreads) {
+            const int mat = it / (TT * (D / 8));
+            const int tt = (it / (D / 8)) % TT, cc = it % (D / 8);
+            const bool okt = tt < nt && slt[tt] >= 0;
+            const unsigned char* rec = raw + tt * rb_;
             uint4 val = make_uint4(0u, 0u, 0u, 0u);
-            bool okt = false;
-            const uint8_t* rec = nullptr;
-            if (tt < nt) {
-                const int sl = P.page_table[(int64_t)b * P.pt_stride + t0 + tt];
-                okt = sl >= 0 && sl < P.num_slots;
-                if (okt) rec = P.records + (int64_t)sl * P.slot_bytes + (int64_t)hk * P.rec_bytes;
-                else if (mat == 0 && cc == 0) set_status(P.status, OSCAR_DEV_BAD_SLOT);
-            }
             if (okt) {
                 const uint32_t cw = *reinterpret_cast<const uint16_t*>(rec + (mat ? rec_v : 0) + 2 * cc);
                 uint32_t w4[4];
@@ -404,6 +451,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_attn_kernel(PrefillParams 
             }
             if (mat == 0 && cc == 0) sOk[tt] = okt;
         }
+        if (tid < TT) sSlot[((i + 2) % 3) * TT + tid] = s2;   // read from the next iteration on
         __syncthreads();
         // S_g = q̃·c over group g's channels
         float sg[NG][NTT][4];
@@ -625,16 +673,17 @@ int launch_prefill(PrefillParams& P, int max_c, cudaStream_t st) {
     const int64_t dense = P.total_q + (int64_t)P.batch * (P.S + P.W);
     launch_dependent(prefill_dense_kernel<D>, dim3((unsigned)dense), dim3(D), 0, st, P);
     if (int rc = check_cuda("prefill_dense_kernel launch")) return rc;
-    const int rblocks = (int)(((int64_t)max_c * P.g + kPfRows - 1) / kPfRows);
     constexpr int TT = 32;
+    using C_ = PfCfg<D, TT>;
+    const int rblocks = (int)(((int64_t)max_c * P.g + C_::ROWS - 1) / C_::ROWS);
     const int prof = prof_begin(6, st);
     auto go = [&](auto kern, size_t smem) -> int {
         if (const int rc = ensure_dynamic_smem((const void*)kern, smem, "cudaFuncSetAttribute(prefill_attn_kernel)"))
             return rc;
-        launch_dependent(kern, dim3((unsigned)rblocks, P.Hkv, P.batch), dim3(kPfThreads), smem, st, P);
+        launch_dependent(kern, dim3((unsigned)rblocks, P.Hkv, P.batch), dim3(C_::THREADS), smem, st, P);
         return check_cuda("prefill_attn_kernel launch");
     };
-    auto smem_for = [&](int ng) { return PfCfg<D, TT>::smem(ng); };
+    auto smem_for = [&](int ng) { return C_::smem(ng, P.rec_bytes); };
     int rc;
     if (P.G == 32 && D >= 32) rc = go(prefill_attn_kernel<D, 32, TT>, smem_for(D / 32));
     else if (P.G == 64 && D >= 64) rc = go(prefill_attn_kernel<D, (D >= 64 ? 64 : 32), TT>, smem_for(D / 64));
@@ -680,7 +729,7 @@ extern "C" int oscar_prefill_attention(const oscar_config* cfg, const oscar_laye
         return fail(OSCAR_ERR_NULL, "q, k, v, cu_q, start_pos, page_table and out are required");
     if (pt_stride < 1) return fail(OSCAR_ERR_ARG, "pt_stride must be >= 1");
     if (max_chunk < 1 || max_chunk > total_q) return fail(OSCAR_ERR_ARG, "max_chunk must be in [1, total_q]");
-    if ((int64_t)max_chunk * (cfg->num_q_heads / cfg->num_kv_heads) > (int64_t)kPfRows * 65535)
+    if ((int64_t)max_chunk * (cfg->num_q_heads / cfg->num_kv_heads) > (int64_t)kPfMaxRows * 65535 / 2)
         return fail(OSCAR_ERR_ARG, "max_chunk too large");
     const int64_t dense = total_q + (int64_t)batch * (cfg->sink + cfg->recent);
     if (dense > 0x7FFFFFFF || total_q * cfg->num_q_heads > 0x7FFFFFFF || total_q > 65535LL * 65535LL)
