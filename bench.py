@@ -611,6 +611,8 @@ def main():
         line["e2e"] = e2e_measure(w, args, ws)
     if not args.no_append:
         line["append"] = append_measure()
+        if args.shapes and ws == 1:
+            line["append_d256"] = append_measure_d256()
     if args.shapes and args.workload == "qwen8b-100k" and ws == 1:
         line["shapes"] = {name: shape_measure(name, 400, 5, hbm_peak)
                           for name in ("qwen32b-ragged", "gqa6-wide", "qwen8b-100k-e4m3")}
@@ -731,6 +733,61 @@ def append_measure():
                          "peak_source": "measured hbm_gbs",
                          "tensor_tflops": mma_flops / (kern_ms / 1e3) / 1e12,
                          "tensor_frac_of_bf16_burst": mma_flops / (kern_ms / 1e3) / 1e12 / bf16_peak}}
+
+def append_measure_d256():
+    """Chunked-prefill append at head_dim 256: one 8,192-token chunk (L0 = 16,384) of a
+    GQA-6 wide-head layer (24 q / 4 KV heads, group 128): the fp32 FMA tiles."""
+    import torch
+    from rotated_int2_kv_gb300 import ops, synth
+    dev = torch.device("cuda")
+    d, hq, hkv, g_ = 256, 24, 4, 128
+    C, L0 = 8192, 16384
+    L = L0 + C
+    cfg = ops.Config(d, hq, hkv, g_, S_SINK, W_RECENT, 0.9)
+    Rk, Rv = rotations(d)
+    pt = synth.page_table(SEED, 1, L, L).to(dev)
+    cache = ops.LayerCache(cfg, L, 1, Rk, Rv, device=dev)
+    scales = synth.outlier_scales(SEED, hkv, d, "fixed4")
+    one = torch.zeros(1, dtype=torch.int32, device=dev)
+    for p0 in range(0, L0, C):
+        k, v = synth.kv_tokens(SEED, 0, p0, C, hkv, d, scales, device=dev)
+        ops.quantize_append(cache, k, v, torch.tensor([0, C], dtype=torch.int32, device=dev), one + p0, pt)
+    k, v = synth.kv_tokens(SEED, 0, L0, C, hkv, d, scales, device=dev)
+    cu = torch.tensor([0, C], dtype=torch.int32, device=dev)
+    st = one + L0
+    ops.quantize_append(cache, k, v, cu, st, pt)
+    torch.cuda.synchronize()
+    ops.profile_enable([ops.PROF_QUANTIZE, ops.PROF_WINDOW_COPY])
+    reps = 20
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        ops.quantize_append(cache, k, v, cu, st, pt)
+    e1.record()
+    torch.cuda.synchronize()
+    qms, qn = ops.profile_read(ops.PROF_QUANTIZE)
+    wms, wn = ops.profile_read(ops.PROF_WINDOW_COPY)
+    ops.profile_enable(None)
+    assert ops.device_status() == 0
+    call_ms = e0.elapsed_time(e1) / reps
+    kern_ms = qms / max(qn, 1)
+    n_hist = C                                           # positions entering the history per call
+    rec_tok, _ = ops.cache_bytes_per_token(cfg)
+    alg_bytes = n_hist * (hkv * d * 2 * 2 + rec_tok + 4)
+    flops = 2.0 * n_hist * hkv * 2 * d * d               # y = x·R for every K and V head vector
+    # fp32 FMA peak of the part: 152 SMs x 128 FMA lanes x 2 flops x 2.07 GHz
+    fma_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+    tf = flops / (kern_ms / 1e3) / 1e12
+    return {"workload": "one 8,192-token chunk appended at L0 = 16,384 (8,192 enter the history), GQA-6 wide-head "
+                        "layer: 24 q / 4 KV heads, d 256, group 128",
+            "value": alg_bytes / (call_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_call": call_ms,
+            "quantize_kernel_ms": kern_ms, "window_copy_kernel_ms": wms / max(wn, 1),
+            "roofline": {"bound": "alu", "achieved": tf, "peak": fma_peak, "unit": "TFLOP/s", "frac": tf / fma_peak,
+                         "kernel": "quantize_kernel<256> (fp32 FMA rotation + INT2)",
+                         "peak_source": "152 SMs x 128 fp32 FMA lanes x 2 flops x 2.07 GHz (nominal)",
+                         "hbm_gbs": alg_bytes / (kern_ms / 1e3) / 1e9}}
+
 
 if __name__ == "__main__":
     main()

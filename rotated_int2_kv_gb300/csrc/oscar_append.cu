@@ -602,7 +602,11 @@ static int launch_append(const AppendParams& P, int64_t total_new, cudaStream_t 
         if constexpr (D <= 128) {
             // large appends, d <= 128: rotation on the tensor cores
             rc = launch_quantize_tc<D>(P, max_vec, stream);
+        } else if (P.G <= 128) {
+            // d = 256: tensor cores, one half of the output channels per CTA
+            rc = launch_quantize_tc256(P, max_vec, stream);
         } else {
+            // group 256 spans both halves: fp32 FMA tiles
             launch_dependent(kern, dim3((unsigned)grid_x, 2), dim3(kAppendThreads), smem, stream, P);
             rc = check_cuda("quantize_kernel launch");
         }

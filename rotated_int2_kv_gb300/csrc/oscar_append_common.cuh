@@ -214,4 +214,8 @@ __device__ __forceinline__ float fma_chain_bound(float x_sq) {
 template <int D>
 int launch_quantize_tc(const AppendParams& P, int64_t max_vec, cudaStream_t stream);
 
+// Tensor-core rotation + quantisation of large appends at head_dim 256 (groups
+// of 32, 64 or 128 channels); returns OSCAR_OK after launching, or a negative status.
+int launch_quantize_tc256(const AppendParams& P, int64_t max_vec, cudaStream_t stream);
+
 }  // namespace oscar

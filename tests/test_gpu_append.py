@@ -124,11 +124,13 @@ def test_group_sizes(d, G):
 @pytest.mark.parametrize("d,G,dtype,unaligned", [
     (128, 64, torch.bfloat16, False), (128, 32, torch.bfloat16, False), (128, 128, torch.float32, False),
     (64, 64, torch.bfloat16, False), (64, 32, torch.float32, False), (128, 64, torch.bfloat16, True),
-    (256, 128, torch.bfloat16, False)])
+    (256, 128, torch.bfloat16, False), (256, 64, torch.bfloat16, False), (256, 32, torch.float32, False),
+    (256, 128, torch.bfloat16, True), (256, 256, torch.bfloat16, False)])
 def test_large_appends_tiled_path(d, G, dtype, unaligned):
     # the second call moves 12,600+ vectors into the history (the tiled kernels:
-    # tensor cores for d <= 128, fp32 FMA for d = 256): the ring's spilled tokens
-    # and new ones, a ragged last tile
+    # tensor cores, at d = 256 one half of the channels per CTA with R in two
+    # bf16 parts; fp32 FMA tiles for group 256): the ring's spilled tokens and
+    # new ones, a ragged last tile
     calls = [[300, 290, 13], [2600, 2700, 1001]]
     st = run_append_scenario(d, 8, 2, G, 64, 256, dtype, calls, unaligned=unaligned)
     assert st["exact"] > 0
