@@ -776,16 +776,22 @@ def append_measure_d256():
     rec_tok, _ = ops.cache_bytes_per_token(cfg)
     alg_bytes = n_hist * (hkv * d * 2 * 2 + rec_tok + 4)
     flops = 2.0 * n_hist * hkv * 2 * d * d               # y = x·R for every K and V head vector
-    # fp32 FMA peak of the part: 152 SMs x 128 FMA lanes x 2 flops x 2.07 GHz
-    fma_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
     tf = flops / (kern_ms / 1e3) / 1e12
     return {"workload": "one 8,192-token chunk appended at L0 = 16,384 (8,192 enter the history), GQA-6 wide-head "
                         "layer: 24 q / 4 KV heads, d 256, group 128",
             "value": alg_bytes / (call_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_call": call_ms,
             "quantize_kernel_ms": kern_ms, "window_copy_kernel_ms": wms / max(wn, 1),
-            "roofline": {"bound": "alu", "achieved": tf, "peak": fma_peak, "unit": "TFLOP/s", "frac": tf / fma_peak,
-                         "kernel": "quantize_kernel<256> (fp32 FMA rotation + INT2)",
-                         "peak_source": "152 SMs x 128 fp32 FMA lanes x 2 flops x 2.07 GHz (nominal)",
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s", "frac": tf / bf16_peak,
+                         "kernel": "quantize_tc256_kernel (tcgen05, R's half in two bf16 parts per CTA, exact INT2 "
+                                   "decisions)",
+                         "peak_source": "measured bf16_tflops",
+                         "flops": "2*d*d per K or V head vector (the rotation; the tensor cores run it as two bf16 parts)",
                          "hbm_gbs": alg_bytes / (kern_ms / 1e3) / 1e9}}
 
 
