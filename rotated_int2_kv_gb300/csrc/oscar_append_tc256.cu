@@ -19,12 +19,16 @@
 // cp.async per chunk).
 //
 // Exact decisions as in the head_dim <= 128 kernel: y differs from x·R rounded
-// to fp32 by at most e = k256Bound·‖x‖₂, the sum of the accumulation bound of
-// kind::f16 (twice the one measured over 8 k-steps, for 16 k-steps) and the
-// two-part residual (|R - hi - lo| <= 2^-18·|R|, so Σ|x||R - hi - lo| <=
-// 2^-18·‖x‖₂ for an orthogonal R); any (s, z) or code decision that y ± e could
-// change is taken again on y formed by a compensated dot product of the input
-// row with R's fp32 column in global memory.
+// to fp32 by at most e = (kAcc256 + ρ)·‖x‖₂, the sum of the accumulation bound of
+// kind::f16 (twice the one measured over 8 k-steps, for 16 k-steps, plus 1 ulp
+// of the result) and the two-part residual: with r = R - hi - lo,
+// |Σ_k x_k r[k][c]| <= ‖x‖₂·‖r[:, c]‖₂ (Cauchy-Schwarz), and ρ, the largest
+// column norm of r over the CTA's channels, is formed from R itself when the
+// parts are built (rounded up).  Elementwise |r| reaches 2^-17·|R|, so ρ
+// depends on R; for a dense orthogonal R of order 256 it is about 50·2^-24.
+// Any (s, z) or code decision that y ± e could change is taken again on y
+// formed by a compensated dot product of the input row with R's fp32 column in
+// global memory.
 #include <algorithm>
 #include <cstring>
 
@@ -49,9 +53,9 @@ constexpr int kABytes = kTcRows * kD * 2;         // one x tile (64 KB)
 constexpr int kBPart = kN * kD * 2;               // one part of R's half (64 KB)
 constexpr int kCPR = kD / 8;                      // 16-byte chunks per input row (32)
 constexpr size_t kSmem = 1024 + 2 * (size_t)kBPart + kABytes + (size_t)2 * kTcRows * kMetaInts * 4 + 128;
-// |y - fl(x·R)| <= k256Bound·‖x‖₂: accumulation 2·kTcErr + 1 ulp of the result,
-// and 64 (= 2^-18 / 2^-24) for the two-part residual, 1% margin, in units of 2^-24
-constexpr float k256Bound = 1.01f * (2.0f * kTcErr + 1.0f + 64.0f) / 16777216.0f;
+// accumulation part of the bound on |y - fl(x·R)| / ‖x‖₂: 2·kTcErr + 1 ulp of the
+// result, in units of 2^-24 (the residual part ρ is added per CTA; 1% margin on both)
+constexpr float kAcc256 = (2.0f * kTcErr + 1.0f) / 16777216.0f;
 
 __device__ __forceinline__ void cta_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -214,7 +218,11 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
     }
     // B: the two parts of R[:, 128·half .. +127] as 128 rows n × 256 k.  Item (n, j)
     // reads R[8j .. 8j+7][128·half + n] and stores its 16-byte chunk of both parts.
+    // Thread tid builds every chunk of channel n = tid (kThreads == kN) and sums
+    // the squares of r = R - hi - lo over its column, rounding up.
+    static_assert(kThreads == kN, "one channel of B per thread");
     constexpr int NB = kN * kCPR;
+    float rsq = 0.0f;
 #pragma unroll 1
     for (int i0 = tid; i0 < NB; i0 += 2 * kThreads) {
         float v[2][8];
@@ -237,13 +245,28 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
                 for (int q = 0; q < 4; ++q) w[q] = pack_bf16(bf16_part(v[u][2 * q], p), bf16_part(v[u][2 * q + 1], p));
                 *reinterpret_cast<uint4*>(sB + p * kBPart + tc5::sw128_offset(kN, n, j)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {             // r = bf16_part(v, 2) exactly (R - hi and R - hi - lo are exact in fp32)
+                const float r = bf16_part(v[u][q], 2);
+                rsq = __fmaf_ru(r, r, rsq);
+            }
         }
+    }
+    {   // ρ: the largest column norm of r over this CTA's channels (scratch is free after build_prefix)
+        float m = __fsqrt_ru(rsq);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (lane == 0) reinterpret_cast<float*>(scratch)[warp] = m;
     }
     tc5::fence_proxy_async();
     tc5::fence_before();
     __syncthreads();
     tc5::fence_after();
     const uint32_t tmem = *tslot;
+    float rho = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) rho = fmaxf(rho, reinterpret_cast<const float*>(scratch)[w]);
+    const float kBound = __fmul_ru(1.01f, __fadd_ru(kAcc256, rho));   // e = kBound·‖x‖₂
 
     const bool vec_in = (reinterpret_cast<uintptr_t>(src_new) & 15) == 0;
     const float rclip = P.clip;
@@ -451,7 +474,7 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
         uint8_t* rec = P.records + (int64_t)(slot < 0 ? 0 : slot) * P.slot_bytes + (int64_t)(m[1] & 0xFFFF) * P.rec_bytes;
         constexpr int NC = G / 32;
         constexpr bool kKeep = G <= 64;
-        const float e = k256Bound * sqrtf(xsq);
+        const float e = kBound * sqrtf(xsq);
         const float e2 = __fmul_ru(2.0f, e);
 #pragma unroll 1
         for (int gl = 0; gl < ngh; ++gl) {
