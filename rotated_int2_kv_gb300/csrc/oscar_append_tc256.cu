@@ -27,8 +27,16 @@
 // parts are built (rounded up).  Elementwise |r| reaches 2^-17·|R|, so ρ
 // depends on R; for a dense orthogonal R of order 256 it is about 50·2^-24.
 // Any (s, z) or code decision that y ± e could change is taken again on y
-// formed by a compensated dot product of the input row with R's fp32 column in
-// global memory.
+// formed by a compensated dot product of the input row with R's fp32 column.
+//
+// For the (s, z) decisions those products run on chip and in parallel: R's
+// half is also kept channel-major in tensor memory (lane n = channel n of the
+// half, columns 256 + k = R[k][n], fp32), a vector with an uncertain group
+// copies its bf16 row from the x tile into shared memory before the next tile
+// overwrites it, and each candidate (vector, channel) is queued to the thread
+// that owns the channel's lane, which forms every product queued to it from
+// its lane and the stashed rows.  A request that finds its channel's queue or
+// the row stash full takes the warp-serial path over global memory instead.
 #include <algorithm>
 #include <cstring>
 
@@ -48,7 +56,10 @@ constexpr int kD = 256;                           // input channels: K of the MM
 constexpr int kN = 128;                           // output channels per CTA: one half of y
 constexpr int kKS = kD / 16;                      // k-steps of 16
 constexpr int kThreads = 128;                     // one warpgroup: thread i owns tile row i
-constexpr uint32_t kCols = 128;                   // tensor-memory columns: one fp32 accumulator
+constexpr uint32_t kCols = 512;                   // tensor-memory columns: accumulator 0 .. 127, R's half 256 .. 511
+constexpr uint32_t kRtCol = 256;                  // first column of R's half, channel-major (fp32)
+constexpr int kQ = 4;                             // exact-y requests one channel takes per batch
+constexpr int kXS = kD + 8;                       // stride of a stashed bf16 row (528 B: rows on different banks)
 constexpr int kABytes = kTcRows * kD * 2;         // one x tile (64 KB)
 constexpr int kBPart = kN * kD * 2;               // one part of R's half (64 KB)
 constexpr int kCPR = kD / 8;                      // 16-byte chunks per input row (32)
@@ -140,6 +151,130 @@ __device__ __noinline__ float2 tc256_exact_extremes(uint32_t tgrp, const float* 
     return make_float2(mne, mxe);
 }
 
+// Shared-memory queues of one batch of on-chip exact products.
+struct RtQueues {
+    int* cnt;                 // [kN] requests queued to each channel
+    int* vec;                 // [kN][kQ] stash row of each request
+    float* y;                 // [kN][kQ] its exact y
+    const uint16_t* xs;       // stashed bf16 rows [xcap][kXS]
+};
+
+__device__ __forceinline__ void dot2_step(float& s, float& c, float x, float r) {
+    const float p = __fmul_rn(x, r);
+    const float pe = __fmaf_rn(x, r, -p);                            // x·r = p + pe exactly
+    const float t = __fadd_rn(s, p);
+    const float bp = __fsub_rn(t, s);
+    const float er = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(p, bp));   // s + p = t + er
+    s = t;
+    c = __fadd_rn(c, __fadd_rn(er, pe));
+}
+
+// fl(x·R[:, c]) for the n stashed rows queued to this thread's channel c (its
+// tensor-memory lane holds R[:, c] from column trt on): a compensated dot
+// product over k in order, four rows at a time.  Warp-collective (tensor-memory
+// loads): every lane calls it with the warp's largest n as nmax.
+__device__ __noinline__ void rt_exact_dots(uint32_t trt, const uint16_t* xs, const int* vec, float* yq, int n,
+                                           int nmax) {
+#pragma unroll 1
+    for (int r0 = 0; r0 < nmax; r0 += 4) {
+        const uint16_t* xr[4];
+        float s[4], c[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            xr[i] = r0 + i < n ? xs + (int64_t)vec[r0 + i] * kXS : nullptr;
+            s[i] = 0.0f;
+            c[i] = 0.0f;
+        }
+#pragma unroll 1
+        for (int kc = 0; kc < kD / 32; ++kc) {
+            float rr[32];
+            tc5::ld32(trt + 32 * kc, rr);
+            tc5::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (!xr[i]) continue;
+                const uint4* p = reinterpret_cast<const uint4*>(xr[i] + 32 * kc);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint4 u = p[w];
+                    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        dot2_step(s[i], c[i], __uint_as_float(wd[q] << 16), rr[8 * w + 2 * q]);
+                        dot2_step(s[i], c[i], __uint_as_float(wd[q] & 0xFFFF0000u), rr[8 * w + 2 * q + 1]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (r0 + i < n) yq[r0 + i] = __fadd_rn(s[i], c[i]);
+    }
+}
+
+// Exact extremes of one group for the threads whose (s, z) y ± e could change,
+// one batch for the whole CTA: every such thread queues its channels within 2e
+// of the computed extremes (tensor-memory columns tgrp; lch0 / gch0: the
+// group's first channel within the half / in y) with its stashed row xslot,
+// the channel owners form them, and the thread takes the min / max of its
+// exact values.  A thread without a stashed row, or whose request does not fit
+// a queue, takes the warp-serial path.  All threads call it (CTA barriers).
+template <int G>
+__device__ __noinline__ float2 rt_exact_extremes(RtQueues Q, uint32_t tgrp, uint32_t trt, bool unc, int xslot,
+                                                 float mn, float mx, float e2, int lch0, int gch0, const float* R,
+                                                 ExactSrc xsrc, int tid, int lane) {
+    const float tlo = __fadd_ru(mn, e2), thi = __fsub_rd(mx, e2);
+    bool over = unc && xslot < 0;
+    uint64_t mine = 0;                             // (channel | slot << 7) of each request, 10 bits apiece
+    int nm = 0;
+#pragma unroll 1
+    for (int c = 0; c < G / 32; ++c) {
+        float y[32];
+        load_y(tgrp + 32 * c, y);
+        uint32_t cm = 0;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) cm |= (unc && (y[q] <= tlo || y[q] >= thi)) ? (1u << q) : 0u;
+        while (cm && !over) {
+            const int ch = lch0 + 32 * c + __ffs(cm) - 1;
+            cm &= cm - 1u;
+            if (nm == 6) {                         // no room in `mine`: reserve nothing
+                over = true;
+                break;
+            }
+            const int sl = atomicAdd(Q.cnt + ch, 1);
+            if (sl < kQ) {                         // every reserved slot below kQ is written
+                Q.vec[ch * kQ + sl] = xslot;
+                mine |= (uint64_t)(ch | (sl << 7)) << (10 * nm);
+                ++nm;
+            } else {
+                over = true;
+            }
+        }
+    }
+    cta_bar();                                     // every request queued
+    const int n = min(Q.cnt[tid], kQ);
+    Q.cnt[tid] = 0;                                // the next batch queues after a later barrier
+    const int nmax = __reduce_max_sync(0xffffffffu, n);
+    if (nmax > 0) rt_exact_dots(trt, Q.xs, Q.vec + tid * kQ, Q.y + tid * kQ, n, nmax);
+    cta_bar();                                     // every exact y formed
+    float mne = INFINITY, mxe = -INFINITY;
+    if (unc && !over)
+        for (int i = 0; i < nm; ++i) {
+            const uint32_t en = (uint32_t)(mine >> (10 * i)) & 1023u;
+            const float v = Q.y[(en & 127u) * kQ + (en >> 7)];
+            mne = fminf(mne, v);
+            mxe = fmaxf(mxe, v);
+        }
+    if (__any_sync(0xffffffffu, over)) {
+        const float2 ex = tc256_exact_extremes<G>(tgrp, R, xsrc, over, mn, mx, e2, gch0, lane);
+        if (over) {
+            mne = ex.x;
+            mxe = ex.y;
+        }
+    }
+    return make_float2(mne, mxe);
+}
+
 // Re-decides the codes of one 32-channel chunk whose reciprocal-path quotient
 // lies near a half-integer (warp-collective, out of line); ch0: the chunk's
 // first channel of y (global index).
@@ -180,7 +315,7 @@ __device__ __noinline__ uint2 tc256_exact_codes(uint32_t tchunk, const float* R,
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
 quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                      int use_tma) {
+                      int use_tma, int xcap) {
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     static_assert(kN % G == 0, "a group lies within one half of the channels");
     constexpr int ngh = kN / G;                     // groups in this CTA's half
@@ -195,6 +330,13 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
     uint32_t* tslot = reinterpret_cast<uint32_t*>(full + 1);
     int* prefix = reinterpret_cast<int*>(tslot + 2);                       // batch + 1
     int* scratch = prefix + P.batch + 1;                                    // kThreads
+    int* nx = scratch + kThreads;                                           // rows stashed in this tile
+    RtQueues Q;
+    Q.cnt = nx + 4;                                                         // kN
+    Q.vec = Q.cnt + kN;                                                     // kN × kQ
+    Q.y = reinterpret_cast<float*>(Q.vec + kN * kQ);                        // kN × kQ
+    uint16_t* xs = reinterpret_cast<uint16_t*>((reinterpret_cast<uintptr_t>(Q.y + kN * kQ) + 15) & ~uintptr_t(15));
+    Q.xs = xs;                                                              // xcap × kXS
 
     const int mat = blockIdx.y, half = blockIdx.z;
     const float* R = mat ? P.rot_v : P.rot_k;
@@ -211,17 +353,27 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
         mbar_init(bar, 1);
         mbar_init(full, 1);
         fence_mbar_init();
+        *nx = 0;
     }
+    Q.cnt[tid] = 0;                                 // kThreads == kN
     if (warp == 0) {
         tc5::alloc(tslot, kCols);
         tc5::relinquish();
     }
+    tc5::fence_before();
+    __syncthreads();
+    tc5::fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t tacc = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's lanes, column 0
+    const uint32_t trt = tacc + kRtCol;             // R[:, 128·half + tid] in this thread's lane
     // B: the two parts of R[:, 128·half .. +127] as 128 rows n × 256 k.  Item (n, j)
     // reads R[8j .. 8j+7][128·half + n] and stores its 16-byte chunk of both parts.
-    // Thread tid builds every chunk of channel n = tid (kThreads == kN) and sums
-    // the squares of r = R - hi - lo over its column, rounding up.
+    // Thread tid builds every chunk of channel n = tid (kThreads == kN), writes
+    // the chunk's 8 fp32 values into its tensor-memory lane (columns kRtCol + 8j
+    // ..), and sums the squares of r = R - hi - lo over its column, rounding up.
     static_assert(kThreads == kN, "one channel of B per thread");
     constexpr int NB = kN * kCPR;
+    static_assert(NB % (2 * kThreads) == 0, "every item of the loop below is in range");
     float rsq = 0.0f;
 #pragma unroll 1
     for (int i0 = tid; i0 < NB; i0 += 2 * kThreads) {
@@ -231,12 +383,11 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
             const int i = i0 + u * kThreads;
             const int n = i % kN, j = i / kN;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) v[u][q] = i < NB ? R[(int64_t)(8 * j + q) * kD + kN * half + n] : 0.0f;
+            for (int q = 0; q < 8; ++q) v[u][q] = R[(int64_t)(8 * j + q) * kD + kN * half + n];
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int i = i0 + u * kThreads;
-            if (i >= NB) continue;
             const int n = i % kN, j = i / kN;
 #pragma unroll
             for (int p = 0; p < 2; ++p) {             // part 0: bf16(R), part 1: bf16(R - part 0)
@@ -250,8 +401,13 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
                 const float r = bf16_part(v[u][q], 2);
                 rsq = __fmaf_ru(r, r, rsq);
             }
+            uint32_t col[8];                          // j is the same in every lane of the warp
+#pragma unroll
+            for (int q = 0; q < 8; ++q) col[q] = __float_as_uint(v[u][q]);
+            tc5::st8(trt + 8 * j, col);
         }
     }
+    tc5::wait_st();
     {   // ρ: the largest column norm of r over this CTA's channels (scratch is free after build_prefix)
         float m = __fsqrt_ru(rsq);
 #pragma unroll
@@ -262,7 +418,6 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
     tc5::fence_before();
     __syncthreads();
     tc5::fence_after();
-    const uint32_t tmem = *tslot;
     float rho = 0.0f;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) rho = fmaxf(rho, reinterpret_cast<const float*>(scratch)[w]);
@@ -276,7 +431,6 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
     const int rec_off_sz = kD / 2 + (mat ? (fp8 ? 2 : 4) * ng : 0);
     const int gi0 = ngh * half;                     // first group of this half
     const CUtensorMap* tmap = mat ? &tm_v : &tm_k;
-    const uint32_t tacc = tmem + ((uint32_t)(32 * warp) << 16);
 
     // Vector gt of a tile is resolved in two stages one loop iteration apart (as
     // in the head_dim <= 128 kernel): locate() starts the page-table load,
@@ -430,6 +584,7 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
                     tc5::mma_bf16(tmem, ad0 + (ao >> 4), bd0 + (bo >> 4), idesc, !(p == 1 && kk == 0));
                 }
             tc5::commit(bar);
+            *nx = 0;                              // the last tile's stashed rows are done with (barrier above)
         }
         const int64_t nxt = tile + step;
         publish(pend, buf ^ 1);
@@ -460,6 +615,37 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
             break;
         }
         tc5::fence_after();
+        constexpr int NC = G / 32;
+        const float e = kBound * sqrtf(xsq);
+        const float e2 = __fmul_ru(2.0f, e);
+        // extremes of this thread's groups, and its x row stashed when one of
+        // their (s, z) could change (before the next tile's rows overwrite it)
+        float gmn[ngh], gmx[ngh];
+        uint32_t umask = 0;
+#pragma unroll
+        for (int gl = 0; gl < ngh; ++gl) {
+            float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                float y[32];
+                load_y(tacc + gl * G + 32 * c, y);
+                minmax32(y, mn, mx);
+            }
+            gmn[gl] = mn;
+            gmx[gl] = mx;
+            umask |= sz_uncertain(mn, mx, rclip, e, fp8) ? (1u << gl) : 0u;
+        }
+        int xslot = -1;
+        if (umask) {
+            const int sl = atomicAdd(nx, 1);
+            if (sl < xcap) {
+                xslot = sl;
+                uint4* dst = reinterpret_cast<uint4*>(xs + (int64_t)sl * kXS);
+#pragma unroll 8
+                for (int j = 0; j < kCPR; ++j) dst[j] = *reinterpret_cast<const uint4*>(A + tc5::sw128_offset(kTcRows, gt, j));
+            }
+        }
+        cta_bar();                                // rows stashed: the x tile may be overwritten
         cur_tma = false;
         if (nxt < ntiles) {
             cur_tma = use_tma && contiguous(buf ^ 1);
@@ -472,25 +658,21 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
         const int slot = m[0];
         const ExactSrc xsrc{P.recent, src_new, P.kv_dtype, m[1] >> 16, *reinterpret_cast<const int64_t*>(m + 2)};
         uint8_t* rec = P.records + (int64_t)(slot < 0 ? 0 : slot) * P.slot_bytes + (int64_t)(m[1] & 0xFFFF) * P.rec_bytes;
-        constexpr int NC = G / 32;
-        constexpr bool kKeep = G <= 64;
-        const float e = kBound * sqrtf(xsq);
-        const float e2 = __fmul_ru(2.0f, e);
 #pragma unroll 1
         for (int gl = 0; gl < ngh; ++gl) {
             const int gch = kN * half + gl * G;   // first channel of the group in y
-            float yk[kKeep ? NC : 1][32];
             uint32_t words[G / 16];
-            float mn = INFINITY, mx = -INFINITY;
+            float mn = gmn[0], mx = gmx[0];
 #pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                float (&y)[32] = yk[kKeep ? c : 0];
-                load_y(tacc + gl * G + 32 * c, y);
-                minmax32(y, mn, mx);
-            }
-            const bool unc = sz_uncertain(mn, mx, rclip, e, fp8);
-            if (__any_sync(0xffffffffu, unc)) {
-                const float2 ex = tc256_exact_extremes<G>(tacc + gl * G, R, xsrc, unc, mn, mx, e2, gch, lane);
+            for (int i = 1; i < ngh; ++i)
+                if (gl == i) {
+                    mn = gmn[i];
+                    mx = gmx[i];
+                }
+            const bool unc = (umask >> gl) & 1u;
+            if (cta_bar_or(unc)) {                // some (s, z) of the tile could change: one batch for the CTA
+                const float2 ex = rt_exact_extremes<G>(Q, tacc + gl * G, trt, unc, xslot, mn, mx, e2, gl * G, gch,
+                                                       R, xsrc, gt, lane);
                 if (unc) {
                     mn = ex.x;
                     mx = ex.y;
@@ -505,8 +687,9 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
             uint32_t tie = 0xFFFFFFFFu;
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
-                if (!kKeep) load_y(tacc + gl * G + 32 * c, yk[0]);
-                codes32(yk[kKeep ? c : 0], zc, r3, nb2, words[2 * c], words[2 * c + 1], tie);
+                float y[32];
+                load_y(tacc + gl * G + 32 * c, y);
+                codes32(y, zc, r3, nb2, words[2 * c], words[2 * c + 1], tie);
             }
             if (__any_sync(0xffffffffu, !(tie >> 31))) {
 #pragma unroll
@@ -543,7 +726,13 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
 
 template <int G>
 static int launch_tc256(const AppendParams& P, int64_t max_vec, cudaStream_t stream) {
-    const size_t smem = kSmem + (size_t)(P.batch + 1 + kThreads) * 4;
+    // prefix, scratch, the stash counter, the queues, 16 bytes of alignment, then
+    // as many stashed rows (up to 64) as the block's shared memory still holds
+    const size_t fixed = kSmem + (size_t)(P.batch + 1 + kThreads + 4 + kN + 2 * kN * kQ) * 4 + 16;
+    const int lim = max_dynamic_smem();
+    if (lim <= 0) return OSCAR_ERR_CUDA;
+    const int xcap = (int)std::min<int64_t>(64, std::max<int64_t>(0, ((int64_t)lim - (int64_t)fixed) / (kXS * 2)));
+    const size_t smem = fixed + (size_t)xcap * kXS * 2;
     auto kern = quantize_tc256_kernel<G>;
     if (const int rc_ = ensure_dynamic_smem((const void*)kern, smem, "cudaFuncSetAttribute(quantize_tc256_kernel)"))
         return rc_;
@@ -557,7 +746,7 @@ static int launch_tc256(const AppendParams& P, int64_t max_vec, cudaStream_t str
     const int use_tma = P.kv_dtype == OSCAR_DTYPE_BF16 && rows > 0 && rows < 0x7FFFFFFF &&
                         (reinterpret_cast<uintptr_t>(P.k) & 15) == 0 && (reinterpret_cast<uintptr_t>(P.v) & 15) == 0 &&
                         tc_encode_rows(&tk, P.k, rows, kD) && tc_encode_rows(&tv, P.v, rows, kD);
-    launch_dependent(kern, dim3((unsigned)grid_x, 2, 2), dim3(kThreads), smem, stream, P, tk, tv, use_tma);
+    launch_dependent(kern, dim3((unsigned)grid_x, 2, 2), dim3(kThreads), smem, stream, P, tk, tv, use_tma, xcap);
     return check_cuda("quantize_tc256_kernel launch");
 }
 

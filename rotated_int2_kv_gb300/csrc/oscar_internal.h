@@ -50,6 +50,8 @@ int* status_word();
 
 // Number of SMs of the current device (cached).
 int sm_count();
+// Largest dynamic shared memory per block (opt-in) of the current device; 0 on error.
+int max_dynamic_smem();
 
 // Converts the pending CUDA error (if any) into OSCAR_ERR_CUDA.
 int check_cuda(const char* what);

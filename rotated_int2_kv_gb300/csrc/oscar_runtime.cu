@@ -20,6 +20,8 @@ static constexpr int kMaxDevices = 64;
 // with relaxed atomics, so threads making their first call concurrently race
 // only to store the same value.
 static std::atomic<int> g_sm_count[kMaxDevices];
+// Largest dynamic shared memory a block may opt into, per device (same scheme).
+static std::atomic<int> g_max_smem[kMaxDevices];
 
 static int current_device() {
     int dev = -1;
@@ -73,6 +75,23 @@ int sm_count() {
             return 0;
         }
         g_sm_count[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+int max_dynamic_smem() {
+    const int dev = current_device();
+    if (dev < 0) {
+        fail(OSCAR_ERR_CUDA, "no current CUDA device");
+        return 0;
+    }
+    int n = g_max_smem[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess || n <= 0) {
+            fail(OSCAR_ERR_CUDA, "cannot query the shared-memory limit");
+            return 0;
+        }
+        g_max_smem[dev].store(n, std::memory_order_relaxed);
     }
     return n;
 }

@@ -96,6 +96,15 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
 }
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 8 consecutive 32-bit columns of this thread's tensor-memory lane from v (the
+// warp writes lanes 32·(warp mod 4) .. +31); complete with wait_st().
+__device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Tiled TMA load of the box at element coordinates (x, y) of a 2-D tensor map
 // into shared memory, completing (with its byte count) on `bar`.  x·element
 // size must be a multiple of 16 bytes.
