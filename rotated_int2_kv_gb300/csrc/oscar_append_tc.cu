@@ -56,6 +56,7 @@ using namespace tcq;
 constexpr int kSlots = 3;                  // warpgroups, each with its own tile in flight
 constexpr int kTcThreads = 128 * kSlots;
 constexpr uint32_t kTmemCols = 512;        // slot e's accumulator: columns 128·e .. 128·e + d
+constexpr int kXCap = 16;                  // stashed rows per warpgroup and tile, at most
 
 
 __device__ __forceinline__ void group_bar(int e) {
@@ -74,22 +75,30 @@ __device__ __forceinline__ bool group_bar_or(int e, bool v) {
 
 // fl(x·R[:, ch]) (compensated, faithful to the exact product) for the vector of
 // lane L, by the whole warp: lane l takes k = l·D/32 .. + D/32 - 1, x from the
-// vector's row in global memory, R exactly as hi + mid + lo from the bf16 parts
-// in shared memory (B operand layout), then a compensated sum over the warp.
+// vector's bf16 row stashed in shared memory (xrow, the same in every lane) or,
+// without one, from its row in global memory, R exactly as hi + mid + lo from
+// the bf16 parts in shared memory (B operand layout), then a compensated sum
+// over the warp.
 template <int D>
-__device__ __forceinline__ float tc_dot2(const unsigned char* sB, const ExactSrc& src, int L, int ch, int lane) {
+__device__ __forceinline__ float tc_dot2(const unsigned char* sB, const ExactSrc& src, const uint16_t* xrow, int L,
+                                         int ch, int lane) {
     constexpr int KPL = D / 32;                       // k per lane: 4 (d 128) or 2 (d 64)
     constexpr int B_PART = D * D * 2;
-    const int kd = __shfl_sync(0xffffffffu, src.kind, L);
-    const uint32_t olo = __shfl_sync(0xffffffffu, (uint32_t)(uint64_t)src.off, L);
-    const uint32_t ohi = __shfl_sync(0xffffffffu, (uint32_t)((uint64_t)src.off >> 32), L);
-    const int64_t o = (int64_t)(((uint64_t)ohi << 32) | olo) + lane * KPL;
     float x[KPL];
+    if (xrow) {
 #pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-        x[i] = kd == 1 ? bf16_bits_to_f32(src.recent[o + i])
-             : kd == 2 ? bf16_bits_to_f32(f32_to_bf16_bits(load_elem(src.src_new, o + i, src.kv_dtype)))
-                       : 0.0f;
+        for (int i = 0; i < KPL; ++i) x[i] = bf16_bits_to_f32(xrow[lane * KPL + i]);
+    } else {
+        const int kd = __shfl_sync(0xffffffffu, src.kind, L);
+        const uint32_t olo = __shfl_sync(0xffffffffu, (uint32_t)(uint64_t)src.off, L);
+        const uint32_t ohi = __shfl_sync(0xffffffffu, (uint32_t)((uint64_t)src.off >> 32), L);
+        const int64_t o = (int64_t)(((uint64_t)ohi << 32) | olo) + lane * KPL;
+#pragma unroll
+        for (int i = 0; i < KPL; ++i) {
+            x[i] = kd == 1 ? bf16_bits_to_f32(src.recent[o + i])
+                 : kd == 2 ? bf16_bits_to_f32(f32_to_bf16_bits(load_elem(src.src_new, o + i, src.kv_dtype)))
+                           : 0.0f;
+        }
     }
     const int k0 = lane * KPL;
     const uint32_t boff = tc5::sw128_offset(D, ch, k0 / 8) + (uint32_t)(k0 % 8) * 2;
@@ -129,8 +138,9 @@ __device__ __forceinline__ float tc_dot2(const unsigned char* sB, const ExactSrc
 // Returns (min, max) over the exact values of the candidates; meaningful for
 // the uncertain lanes.
 template <int D, int G>
-__device__ __noinline__ float2 tc_exact_extremes(uint32_t tgrp, const unsigned char* sB, ExactSrc src, bool unc,
-                                                 float mn, float mx, float e2, int ch0, int lane) {
+__device__ __noinline__ float2 tc_exact_extremes(uint32_t tgrp, const unsigned char* sB, ExactSrc src,
+                                                 const uint16_t* xs, int xslot, bool unc, float mn, float mx,
+                                                 float e2, int ch0, int lane) {
     const float tlo = __fadd_ru(mn, e2), thi = __fsub_rd(mx, e2);
     float mne = INFINITY, mxe = -INFINITY;
 #pragma unroll 1
@@ -144,7 +154,8 @@ __device__ __noinline__ float2 tc_exact_extremes(uint32_t tgrp, const unsigned c
         while ((bal = __ballot_sync(0xffffffffu, cm != 0u)) != 0u) {
             const int L = __ffs(bal) - 1;
             const int q = __shfl_sync(0xffffffffu, __ffs(cm) - 1, L);
-            const float ye = tc_dot2<D>(sB, src, L, ch0 + 32 * c + q, lane);
+            const int xl = __shfl_sync(0xffffffffu, xslot, L);
+            const float ye = tc_dot2<D>(sB, src, xl >= 0 ? xs + xl * (D + 8) : nullptr, L, ch0 + 32 * c + q, lane);
             if (lane == L) {
                 cm &= cm - 1u;
                 mne = fminf(mne, ye);
@@ -160,8 +171,9 @@ __device__ __noinline__ float2 tc_exact_extremes(uint32_t tgrp, const unsigned c
 // decided by correctly rounded division, on the exact y where y ± e straddles
 // a boundary, and patched into the chunk's two code words w.
 template <int D>
-__device__ __noinline__ uint2 tc_exact_codes(uint32_t tchunk, const unsigned char* sB, ExactSrc src, float zc,
-                                             float sc, float r3, float nb2, float be, uint2 w, int ch0, int lane) {
+__device__ __noinline__ uint2 tc_exact_codes(uint32_t tchunk, const unsigned char* sB, ExactSrc src,
+                                             const uint16_t* xs, int xslot, float zc, float sc, float r3, float nb2,
+                                             float be, uint2 w, int ch0, int lane) {
     float y[32];
     load_y(tchunk, y);
     uint32_t cm = 0;                              // channels to re-decide (the fast path's test)
@@ -179,7 +191,8 @@ __device__ __noinline__ uint2 tc_exact_codes(uint32_t tchunk, const unsigned cha
         const float yq = load_col(tchunk + q);    // every lane's y of channel q; lane L's is the one used
         float u = sc != 0.0f ? __fdiv_rn(__fsub_rn(yq, zc), sc) : 0.0f;
         if (__shfl_sync(0xffffffffu, (int)(sc != 0.0f && code_near_boundary(u, be)), L)) {
-            const float ye = tc_dot2<D>(sB, src, L, ch0 + q, lane);
+            const int xl = __shfl_sync(0xffffffffu, xslot, L);
+            const float ye = tc_dot2<D>(sB, src, xl >= 0 ? xs + xl * (D + 8) : nullptr, L, ch0 + q, lane);
             u = __fdiv_rn(__fsub_rn(ye, zc), sc);
         }
         if (lane == L) {
@@ -208,7 +221,7 @@ struct TcCfg {
 template <int D, int G>
 __global__ void __launch_bounds__(kTcThreads, 1)
 quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                   int use_tma) {
+                   int use_tma, int xcap) {
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     using C = TcCfg<D>;
     constexpr int ng = D / G;
@@ -224,6 +237,9 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
     uint32_t* tslot = reinterpret_cast<uint32_t*>(fulls + kSlots);
     int* prefix = reinterpret_cast<int*>(tslot + 2);                       // batch + 1
     int* scratch = prefix + P.batch + 1;                                    // kTcThreads
+    int* nxs = scratch + kTcThreads;                                        // [slots] rows stashed (4 ints)
+    uint16_t* xs_all = reinterpret_cast<uint16_t*>((reinterpret_cast<uintptr_t>(nxs + 4) + 15) & ~uintptr_t(15));
+    constexpr int XS = D + 8;                                               // stashed row stride (bf16 elements)
 
     const int mat = blockIdx.y;
     const float* R = mat ? P.rot_v : P.rot_k;
@@ -292,6 +308,8 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
     const int rec_off_sz = D / 2 + (mat ? (fp8 ? 2 : 4) * ng : 0);
     unsigned char* A = sA + e * C::A_BYTES;
     int* gmeta = meta + e * 2 * kTcRows * kMetaInts;
+    int* nx = nxs + e;                              // this group's stash: xcap rows of XS
+    const uint16_t* xs = xs_all + (int64_t)e * xcap * XS;
     uint64_t* bar = &bars[e];
     uint64_t* full = &fulls[e];
     const CUtensorMap* tmap = mat ? &tm_v : &tm_k;
@@ -463,6 +481,7 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
                     tc5::mma_bf16(dcol, ad0 + (ao >> 4), bd0 + (bo >> 4), idesc, !(p == 2 && kk == 0));
                 }
             tc5::commit(bar);
+            *nx = 0;                              // the last tile's stashed rows are done with (group barrier above)
         }
         const int64_t nxt = tile + step;
         publish(pend, buf ^ 1);                 // tile nxt: its page-table load was started one iteration ago
@@ -478,6 +497,51 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
             break;
         }
         tc5::fence_after();
+        constexpr int NC = G / 32;                // 32-channel chunks per group
+        constexpr bool kKeep = G <= 64;           // the group's y stays in registers between the passes
+        // err bounds |y - fl(x·R)| on every channel of the vector (kTcBound·‖y‖₂);
+        // with it, which (s, z) of the vector y ± err could change (umask)
+        float err;
+        uint32_t umask = 0;
+        {
+            float2 q2 = make_float2(0.0f, 0.0f);
+            float mn = INFINITY, mx = -INFINITY;
+            float gmn[ng], gmx[ng];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                float yy[32];
+                load_y(tacc + 32 * c, yy);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float2 v = make_float2(yy[2 * q], yy[2 * q + 1]);
+                    q2 = __ffma2_rn(v, v, q2);
+                }
+                minmax32(yy, mn, mx);
+                if ((32 * (c + 1)) % G == 0) {    // the last chunk of group 32·c / G
+                    gmn[32 * c / G] = mn;
+                    gmx[32 * c / G] = mx;
+                    mn = INFINITY;
+                    mx = -INFINITY;
+                }
+            }
+            err = kTcBound * sqrtf(q2.x + q2.y);
+#pragma unroll
+            for (int gi = 0; gi < ng; ++gi) umask |= sz_uncertain(gmn[gi], gmx[gi], rclip, err, fp8) ? (1u << gi) : 0u;
+        }
+        const float e2 = __fmul_ru(2.0f, err);
+        // the vector's bf16 row into the group's stash when some (s, z) is
+        // uncertain, before the next tile's rows overwrite the x tile
+        int xslot = -1;
+        if (umask) {
+            const int sl = atomicAdd(nx, 1);
+            if (sl < xcap) {
+                xslot = sl;
+                uint4* dst = reinterpret_cast<uint4*>(const_cast<uint16_t*>(xs) + sl * XS);
+#pragma unroll
+                for (int j = 0; j < C::CPR; ++j) dst[j] = *reinterpret_cast<const uint4*>(A + tc5::sw128_offset(kTcRows, gt, j));
+            }
+        }
+        group_bar(e);                             // rows stashed: the x tile may be overwritten
         cur_tma = false;
         if (nxt < ntiles) {
             cur_tma = use_tma && contiguous(buf ^ 1);
@@ -490,25 +554,6 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
         const int slot = m[0];
         const ExactSrc xsrc{P.recent, src_new, P.kv_dtype, m[1] >> 16, *reinterpret_cast<const int64_t*>(m + 2)};
         uint8_t* rec = P.records + (int64_t)(slot < 0 ? 0 : slot) * P.slot_bytes + (int64_t)(m[1] & 0xFFFF) * P.rec_bytes;
-        constexpr int NC = G / 32;                // 32-channel chunks per group
-        constexpr bool kKeep = G <= 64;           // the group's y stays in registers between the passes
-        // e bounds |y - fl(x·R)| on every channel of the vector (kTcBound·‖y‖₂)
-        float e;
-        {
-            float2 q2 = make_float2(0.0f, 0.0f);
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float yy[32];
-                load_y(tacc + 32 * c, yy);
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float2 v = make_float2(yy[2 * q], yy[2 * q + 1]);
-                    q2 = __ffma2_rn(v, v, q2);
-                }
-            }
-            e = kTcBound * sqrtf(q2.x + q2.y);
-        }
-        const float e2 = __fmul_ru(2.0f, e);
         // one group at a time (not unrolled: the loop body stays small in the
         // instruction cache); its codes and (s, z) go to the record at its end
 #pragma unroll 1
@@ -522,10 +567,11 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
                 load_y(tacc + gi * G + 32 * c, y);
                 minmax32(y, mn, mx);
             }
-            // (s, z) that y ± e could change: the extremes formed exactly (out of line)
-            const bool unc = sz_uncertain(mn, mx, rclip, e, fp8);
+            // (s, z) that y ± err could change: the extremes formed exactly (out of line)
+            const bool unc = (umask >> gi) & 1u;
             if (__any_sync(0xffffffffu, unc)) {
-                const float2 ex = tc_exact_extremes<D, G>(tacc + gi * G, sB, xsrc, unc, mn, mx, e2, gi * G, lane);
+                const float2 ex = tc_exact_extremes<D, G>(tacc + gi * G, sB, xsrc, xs, xslot, unc, mn, mx, e2, gi * G,
+                                                          lane);
                 if (unc) {
                     mn = ex.x;
                     mx = ex.y;
@@ -537,8 +583,8 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
             // group (s = 0) takes r3 = 0, so its fast-path codes are all 0.
             const float r3 = sc != 0.0f ? __frcp_rn(3.0f * sc) : 0.0f;   // 3·sc is exact (≤ 11-bit significand × 3)
             // a code is certain when its quotient is farther from a half-integer than
-            // e/s plus the reciprocal path's 2^-21
-            const float be = code_band(e, r3);
+            // err/s plus the reciprocal path's 2^-21
+            const float be = code_band(err, r3);
             const float hb = 0.5f - (be + 1.0f / 2097152.0f);
             const float nb2 = hb > 0.0f ? -hb * hb : 0.0f;
             uint32_t tie = 0xFFFFFFFFu;
@@ -549,10 +595,10 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
             }
             if (__any_sync(0xffffffffu, !(tie >> 31))) {
                 // a quotient near a tie: re-decide those channels by correctly rounded
-                // division, on the exact y where y ± e straddles a boundary
+                // division, on the exact y where y ± err straddles a boundary
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
-                    const uint2 w = tc_exact_codes<D>(tacc + gi * G + 32 * c, sB, xsrc, zc, sc, r3, nb2, be,
+                    const uint2 w = tc_exact_codes<D>(tacc + gi * G + 32 * c, sB, xsrc, xs, xslot, zc, sc, r3, nb2, be,
                                                       make_uint2(words[2 * c], words[2 * c + 1]), gi * G + 32 * c,
                                                       lane);
                     words[2 * c] = w.x;
@@ -631,8 +677,16 @@ bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int d) {
 template <int D, int G>
 static int launch_tc(const AppendParams& P, int64_t max_vec, cudaStream_t stream) {
     using C = TcCfg<D>;
-    // at least 116 KB, so that one CTA (and one tensor-memory allocation) sits on each SM
-    const size_t smem = std::max<size_t>(C::SMEM + (size_t)(P.batch + 1 + kTcThreads) * 4, 116 * 1024);
+    // prefix, scratch, the stash counters and 16 bytes of alignment, then each
+    // warpgroup's stash (up to kXCap rows of d + 8 bf16) as far as the block's
+    // shared memory holds it; at least 116 KB, so that one CTA (and one
+    // tensor-memory allocation) sits on each SM
+    const size_t fixed = C::SMEM + (size_t)(P.batch + 1 + kTcThreads + 4) * 4 + 16;
+    const int lim = max_dynamic_smem();
+    if (lim <= 0) return OSCAR_ERR_CUDA;
+    const int64_t row_bytes = (int64_t)kSlots * (D + 8) * 2;
+    const int xcap = (int)std::min<int64_t>(kXCap, std::max<int64_t>(0, ((int64_t)lim - (int64_t)fixed) / row_bytes));
+    const size_t smem = std::max<size_t>(fixed + (size_t)xcap * row_bytes, 116 * 1024);
     auto kern = quantize_tc_kernel<D, G>;
     if (const int rc_ = ensure_dynamic_smem((const void*)kern, smem, "cudaFuncSetAttribute(quantize_tc_kernel)"))
         return rc_;
@@ -646,7 +700,7 @@ static int launch_tc(const AppendParams& P, int64_t max_vec, cudaStream_t stream
     const int use_tma = P.kv_dtype == OSCAR_DTYPE_BF16 && rows > 0 && rows < 0x7FFFFFFF &&
                         (reinterpret_cast<uintptr_t>(P.k) & 15) == 0 && (reinterpret_cast<uintptr_t>(P.v) & 15) == 0 &&
                         encode_rows(&tk, P.k, rows, D) && encode_rows(&tv, P.v, rows, D);
-    launch_dependent(kern, dim3((unsigned)grid_x, 2), dim3(kTcThreads), smem, stream, P, tk, tv, use_tma);
+    launch_dependent(kern, dim3((unsigned)grid_x, 2), dim3(kTcThreads), smem, stream, P, tk, tv, use_tma, xcap);
     return check_cuda("quantize_tc_kernel launch");
 }
 
