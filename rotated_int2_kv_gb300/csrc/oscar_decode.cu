@@ -836,6 +836,16 @@ __global__ void __launch_bounds__(128) window_mma_kernel(DecodeParams P) {
 // ---------------------------------------------------------------------------
 template <int D, int GQ, bool MMA>
 __global__ void __launch_bounds__(128) step_pre_kernel(DecodeParams P, AppendParams A, NewRowSrc nr) {
+    {   // R_K and R_V are no kernel's output: their lines head for L2 while the
+        // previous grid drains (two lines per block; the first 2d²·4/256 blocks
+        // cover both matrices)
+        constexpr int64_t nl = (int64_t)D * D * 4 / 128;            // 128-byte lines of one matrix
+        const int64_t bid = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
+        if (threadIdx.x < 2) {
+            const int64_t l = (2 * bid + threadIdx.x) % (2 * nl);
+            prefetch_l2(reinterpret_cast<const char*>(l < nl ? A.rot_k : A.rot_v) + 128 * (l % nl));
+        }
+    }
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     extern __shared__ __align__(16) uint32_t s_step[];
     const int hk = blockIdx.x, b = blockIdx.y, z = (int)blockIdx.z;
@@ -1143,6 +1153,11 @@ __device__ __noinline__ void combine_sliced(const DecodeParams& P, const CombReq
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads, D == 128 ? 2 : 1) combine_kernel(DecodeParams P) {
+    {   // R_V is no kernel's output: its lines head for L2 while the history grid drains
+        constexpr int nl = D * D * 4 / 128;
+        const int bid = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+        if (threadIdx.x < 8) prefetch_l2(reinterpret_cast<const char*>(P.rot_v) + 128 * ((8 * bid + threadIdx.x) % nl));
+    }
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     extern __shared__ __align__(16) float s_c[];
     const int g = P.g;

@@ -68,6 +68,11 @@ __device__ __forceinline__ void grid_dep_sync() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// L2 prefetch hint for the 128-byte line at p (no data returns; nothing waits).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
+}
+
 __device__ __forceinline__ void set_status(int* word, int bits) {
     if (word) atomicOr(word, bits);
 }
