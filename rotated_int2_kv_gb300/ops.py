@@ -146,6 +146,13 @@ class Config:
     scale_fmt: str = "f16"          # "f16" or "e4m3": storage of each group's (s, z)
 
     def c(self):
+        # the C struct is rebuilt only when a field changed since the last call
+        key = (self.head_dim, self.num_q_heads, self.num_kv_heads, self.group_size, self.sink, self.recent,
+               self.clip_ratio, self.kv_dtype, self.q_dtype, self.scale_fmt)
+        memo = self.__dict__.get("_c_memo")
+        if memo is not None and memo[0] == key:
+            return memo[1]
+
         def code(dt):
             if dt == torch.bfloat16:
                 return DTYPE_BF16
@@ -154,9 +161,11 @@ class Config:
             raise ValueError("dtype must be torch.bfloat16 or torch.float32")
         if self.scale_fmt not in ("f16", "e4m3"):
             raise ValueError("scale_fmt must be 'f16' or 'e4m3'")
-        return CConfig(self.head_dim, self.num_q_heads, self.num_kv_heads, self.group_size,
-                       self.sink, self.recent, self.clip_ratio, code(self.kv_dtype),
-                       code(self.q_dtype), SCALE_E4M3 if self.scale_fmt == "e4m3" else SCALE_F16)
+        cc = CConfig(self.head_dim, self.num_q_heads, self.num_kv_heads, self.group_size,
+                     self.sink, self.recent, self.clip_ratio, code(self.kv_dtype),
+                     code(self.q_dtype), SCALE_E4M3 if self.scale_fmt == "e4m3" else SCALE_F16)
+        self.__dict__["_c_memo"] = (key, cc)
+        return cc
 
     @property
     def gqa(self):
@@ -297,9 +306,18 @@ class LayerCache:
             return self.records
         return self.records.as_strided((self.num_slots, H, rb), (self.slot_bytes, rb, 1))
 
+    def __setattr__(self, name, value):
+        object.__setattr__(self, name, value)
+        if name != "_c_struct":                      # any new buffer or size: rebuild the C struct
+            object.__setattr__(self, "_c_struct", None)
+
     def c(self):
-        return CLayerCache(self.records.data_ptr(), self.sink.data_ptr(), self.recent.data_ptr(),
-                           self.rot_k.data_ptr(), self.rot_v.data_ptr(), self.num_slots, self.max_reqs)
+        cs = self.__dict__.get("_c_struct")
+        if cs is None:
+            cs = CLayerCache(self.records.data_ptr(), self.sink.data_ptr(), self.recent.data_ptr(),
+                             self.rot_k.data_ptr(), self.rot_v.data_ptr(), self.num_slots, self.max_reqs)
+            object.__setattr__(self, "_c_struct", cs)
+        return cs
 
 
 def _ptr(t, dtype=None, name="tensor"):
@@ -314,7 +332,13 @@ def _ptr(t, dtype=None, name="tensor"):
     return t.data_ptr()
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream, device=None):
+    if stream is None and _raw_stream is not None:   # the current stream's handle, no Stream object
+        idx = device.index if device is not None and device.index is not None else torch.cuda.current_device()
+        return ctypes.c_void_p(_raw_stream(idx))
     s = torch.cuda.current_stream(device) if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
 
@@ -322,11 +346,11 @@ def _stream(stream, device=None):
 def _device_of(cache, *tensors):
     """The one CUDA device that holds the cache and every given tensor; the
     library launches on the current device, so the calls below make it current."""
-    dev = cache.records.device
+    di = cache.records.get_device()                  # device index (-1 for a CPU tensor)
     for t in tensors:
-        if t is not None and t.device != dev:
-            raise ValueError("all tensors must be on the cache's device %s (got %s)" % (dev, t.device))
-    return dev
+        if t is not None and t.get_device() != di:
+            raise ValueError("all tensors must be on the cache's device %s (got %s)" % (cache.records.device, t.device))
+    return cache.records.device
 
 
 def quantize_append(cache, k, v, cu_new, start_pos, page_table, req_idx=None, stream=None):
