@@ -57,8 +57,8 @@ constexpr int kN = 128;                           // output channels per CTA: on
 constexpr int kKS = kD / 16;                      // k-steps of 16
 constexpr int kThreads = 128;                     // one warpgroup: thread i owns tile row i
 constexpr uint32_t kCols = 512;                   // tensor-memory columns: accumulator 0 .. 127, R's half 256 .. 511
-constexpr uint32_t kRtCol = 256;                  // first column of R's half, channel-major (fp32)
-constexpr int kQ = 4;                             // exact-y requests one channel takes per batch
+constexpr uint32_t kRtCol = 256;                  // first column of R's half in tensor memory (fp32)
+constexpr int kQ = 12;                            // exact-y requests one channel takes per batch
 constexpr int kXS = kD + 8;                       // stride of a stashed bf16 row (528 B: rows on different banks)
 constexpr int kABytes = kTcRows * kD * 2;         // one x tile (64 KB)
 constexpr int kBPart = kN * kD * 2;               // one part of R's half (64 KB)
@@ -169,46 +169,60 @@ __device__ __forceinline__ void dot2_step(float& s, float& c, float x, float r) 
     c = __fadd_rn(c, __fadd_rn(er, pe));
 }
 
-// fl(x·R[:, c]) for the n stashed rows queued to this thread's channel c (its
-// tensor-memory lane holds R[:, c] from column trt on): a compensated dot
-// product over k in order, four rows at a time.  Warp-collective (tensor-memory
-// loads): every lane calls it with the warp's largest n as nmax.
-__device__ __noinline__ void rt_exact_dots(uint32_t trt, const uint16_t* xs, const int* vec, float* yq, int n,
-                                           int nmax) {
+// R's half in tensor memory: lane L of warp w holds, for m = 0 .. 3, the k-quarter
+// L mod 4 of channel 32w + L/4 + 8m of the half, R[64·(L mod 4) + kk][..] at
+// column kRtCol + 64m + kk (kk < 64).  So the four lanes of a quad hold the
+// four quarters of the same four channels, and one exact product is split
+// over them.
+//
+// fl(x·R[:, ch]) for every stashed row queued to the channels of this thread's
+// quad (cnt, vec: the queues; yq: the results, [kN][kQ]): each lane forms the
+// compensated dot product over its 64 k in order, and the quad sums the four
+// (sum, error) pairs with two compensated steps.  Warp-collective (tensor-memory
+// loads, shuffles): every thread of the warp calls it.
+__device__ __noinline__ void rt_exact_dots(uint32_t trt, const uint16_t* xs, const int* cnt, const int* vec,
+                                           float* yq, int warp, int lane) {
+    const int q = lane & 3, ci = lane >> 2;
 #pragma unroll 1
-    for (int r0 = 0; r0 < nmax; r0 += 4) {
-        const uint16_t* xr[4];
-        float s[4], c[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            xr[i] = r0 + i < n ? xs + (int64_t)vec[r0 + i] * kXS : nullptr;
-            s[i] = 0.0f;
-            c[i] = 0.0f;
-        }
+    for (int m = 0; m < 4; ++m) {
+        const int ch = 32 * warp + ci + 8 * m;      // channel of the half
+        const int n = min(cnt[ch], kQ);
+        const int nmax = __reduce_max_sync(0xffffffffu, n);
+        if (nmax == 0) continue;                    // warp-uniform
+        float ra[32], rb[32];
+        tc5::ld32(trt + 64 * m, ra);
+        tc5::ld32(trt + 64 * m + 32, rb);
+        tc5::wait_ld();
 #pragma unroll 1
-        for (int kc = 0; kc < kD / 32; ++kc) {
-            float rr[32];
-            tc5::ld32(trt + 32 * kc, rr);
-            tc5::wait_ld();
+        for (int r = 0; r < nmax; ++r) {
+            float s = 0.0f, c = 0.0f;
+            if (r < n) {
+                const uint4* p = reinterpret_cast<const uint4*>(xs + (int64_t)vec[ch * kQ + r] * kXS + 64 * q);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (!xr[i]) continue;
-                const uint4* p = reinterpret_cast<const uint4*>(xr[i] + 32 * kc);
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
+                for (int w = 0; w < 8; ++w) {
                     const uint4 u = p[w];
                     const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        dot2_step(s[i], c[i], __uint_as_float(wd[q] << 16), rr[8 * w + 2 * q]);
-                        dot2_step(s[i], c[i], __uint_as_float(wd[q] & 0xFFFF0000u), rr[8 * w + 2 * q + 1]);
+                    for (int i = 0; i < 4; ++i) {
+                        const float r0 = w < 4 ? ra[8 * w + 2 * i] : rb[8 * (w - 4) + 2 * i];
+                        const float r1 = w < 4 ? ra[8 * w + 2 * i + 1] : rb[8 * (w - 4) + 2 * i + 1];
+                        dot2_step(s, c, __uint_as_float(wd[i] << 16), r0);
+                        dot2_step(s, c, __uint_as_float(wd[i] & 0xFFFF0000u), r1);
                     }
                 }
             }
-        }
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if (r0 + i < n) yq[r0 + i] = __fadd_rn(s[i], c[i]);
+            for (int off = 1; off <= 2; off <<= 1) {  // the quad's four partial sums
+                const float so = __shfl_xor_sync(0xffffffffu, s, off);
+                const float co = __shfl_xor_sync(0xffffffffu, c, off);
+                const float t = __fadd_rn(s, so);
+                const float bp = __fsub_rn(t, s);
+                const float er = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(so, bp));
+                s = t;
+                c = __fadd_rn(__fadd_rn(c, co), er);
+            }
+            if (q == 0 && r < n) yq[ch * kQ + r] = __fadd_rn(s, c);
+        }
     }
 }
 
@@ -216,16 +230,18 @@ __device__ __noinline__ void rt_exact_dots(uint32_t trt, const uint16_t* xs, con
 // one batch for the whole CTA: every such thread queues its channels within 2e
 // of the computed extremes (tensor-memory columns tgrp; lch0 / gch0: the
 // group's first channel within the half / in y) with its stashed row xslot,
-// the channel owners form them, and the thread takes the min / max of its
-// exact values.  A thread without a stashed row, or whose request does not fit
-// a queue, takes the warp-serial path.  All threads call it (CTA barriers).
+// the quads holding the channels form them, and the thread takes the min /
+// max of its exact values.  A thread without a stashed row, or whose request
+// does not fit a queue, takes the warp-serial path.  All threads call it (CTA
+// barriers).
 template <int G>
 __device__ __noinline__ float2 rt_exact_extremes(RtQueues Q, uint32_t tgrp, uint32_t trt, bool unc, int xslot,
                                                  float mn, float mx, float e2, int lch0, int gch0, const float* R,
                                                  ExactSrc xsrc, int tid, int lane) {
     const float tlo = __fadd_ru(mn, e2), thi = __fsub_rd(mx, e2);
     bool over = unc && xslot < 0;
-    uint64_t mine = 0;                             // (channel | slot << 7) of each request, 10 bits apiece
+    uint64_t mine = 0;                             // (channel | slot << 7) of each request, 12 bits apiece
+    static_assert(kQ <= 16 && kN <= 128, "a request fits 12 bits");
     int nm = 0;
 #pragma unroll 1
     for (int c = 0; c < G / 32; ++c) {
@@ -237,14 +253,14 @@ __device__ __noinline__ float2 rt_exact_extremes(RtQueues Q, uint32_t tgrp, uint
         while (cm && !over) {
             const int ch = lch0 + 32 * c + __ffs(cm) - 1;
             cm &= cm - 1u;
-            if (nm == 6) {                         // no room in `mine`: reserve nothing
+            if (nm == 5) {                         // no room in `mine`: reserve nothing
                 over = true;
                 break;
             }
             const int sl = atomicAdd(Q.cnt + ch, 1);
             if (sl < kQ) {                         // every reserved slot below kQ is written
                 Q.vec[ch * kQ + sl] = xslot;
-                mine |= (uint64_t)(ch | (sl << 7)) << (10 * nm);
+                mine |= (uint64_t)(ch | (sl << 7)) << (12 * nm);
                 ++nm;
             } else {
                 over = true;
@@ -252,15 +268,13 @@ __device__ __noinline__ float2 rt_exact_extremes(RtQueues Q, uint32_t tgrp, uint
         }
     }
     cta_bar();                                     // every request queued
-    const int n = min(Q.cnt[tid], kQ);
+    rt_exact_dots(trt, Q.xs, Q.cnt, Q.vec, Q.y, tid >> 5, lane);
+    cta_bar();                                     // every exact y formed; every count read
     Q.cnt[tid] = 0;                                // the next batch queues after a later barrier
-    const int nmax = __reduce_max_sync(0xffffffffu, n);
-    if (nmax > 0) rt_exact_dots(trt, Q.xs, Q.vec + tid * kQ, Q.y + tid * kQ, n, nmax);
-    cta_bar();                                     // every exact y formed
     float mne = INFINITY, mxe = -INFINITY;
     if (unc && !over)
         for (int i = 0; i < nm; ++i) {
-            const uint32_t en = (uint32_t)(mine >> (10 * i)) & 1023u;
+            const uint32_t en = (uint32_t)(mine >> (12 * i)) & 4095u;
             const float v = Q.y[(en & 127u) * kQ + (en >> 7)];
             mne = fminf(mne, v);
             mxe = fmaxf(mxe, v);
@@ -365,12 +379,11 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
     tc5::fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tacc = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's lanes, column 0
-    const uint32_t trt = tacc + kRtCol;             // R[:, 128·half + tid] in this thread's lane
+    const uint32_t trt = tacc + kRtCol;             // this lane's share of R's half (quad layout)
     // B: the two parts of R[:, 128·half .. +127] as 128 rows n × 256 k.  Item (n, j)
     // reads R[8j .. 8j+7][128·half + n] and stores its 16-byte chunk of both parts.
-    // Thread tid builds every chunk of channel n = tid (kThreads == kN), writes
-    // the chunk's 8 fp32 values into its tensor-memory lane (columns kRtCol + 8j
-    // ..), and sums the squares of r = R - hi - lo over its column, rounding up.
+    // Thread tid builds every chunk of channel n = tid (kThreads == kN) and sums
+    // the squares of r = R - hi - lo over its column, rounding up.
     static_assert(kThreads == kN, "one channel of B per thread");
     constexpr int NB = kN * kCPR;
     static_assert(NB % (2 * kThreads) == 0, "every item of the loop below is in range");
@@ -401,13 +414,30 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
                 const float r = bf16_part(v[u][q], 2);
                 rsq = __fmaf_ru(r, r, rsq);
             }
-            uint32_t col[8];                          // j is the same in every lane of the warp
-#pragma unroll
-            for (int q = 0; q < 8; ++q) col[q] = __float_as_uint(v[u][q]);
-            tc5::st8(trt + 8 * j, col);
         }
     }
-    tc5::wait_st();
+    {   // R's half into tensor memory, quad layout (see rt_exact_dots): this lane's
+        // quarter of its four channels, 32 rows of R in flight
+        const int q = lane & 3, ci = lane >> 2;
+#pragma unroll 1
+        for (int m = 0; m < 4; ++m) {
+            const float* src = R + (int64_t)(64 * q) * kD + kN * half + 32 * warp + ci + 8 * m;
+#pragma unroll 1
+            for (int k0 = 0; k0 < 64; k0 += 32) {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __ldg(src + (int64_t)(k0 + i) * kD);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t col[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) col[i] = __float_as_uint(v[8 * j + i]);
+                    tc5::st8(trt + 64 * m + k0 + 8 * j, col);   // the same columns in every lane
+                }
+            }
+        }
+        tc5::wait_st();
+    }
     {   // ρ: the largest column norm of r over this CTA's channels (scratch is free after build_prefix)
         float m = __fsqrt_ru(rsq);
 #pragma unroll
