@@ -61,11 +61,18 @@ def outlier_scales(seed, num_kv_heads, head_dim, mode="fixed4"):
 
 
 def kv_tokens(seed, req, p0, n, num_kv_heads, head_dim, scales, device="cpu",
-              dtype=torch.bfloat16):
-    """K and V rows for positions [p0, p0+n) of request `req`: (n, Hkv, d) each."""
+              dtype=torch.bfloat16, shared=0.0):
+    """K and V rows for positions [p0, p0+n) of request `req`: (n, Hkv, d) each.
+    shared > 0 adds shared·base_h to every row of KV head h (base_h ~ N(0, 1),
+    one per head, K and V, the same for every request and position), before the
+    channel multipliers: rows that share one strong direction."""
     ks, vs = scales
     ks = ks.to(device)
     vs = vs.to(device)
+    base = None
+    if shared:
+        base = torch.randn((2, num_kv_heads, head_dim), generator=_gen(device, seed, 5),
+                           device=device, dtype=torch.float32) * float(shared)
     out_k = torch.empty((n, num_kv_heads, head_dim), dtype=dtype, device=device)
     out_v = torch.empty_like(out_k)
     if n == 0:
@@ -79,8 +86,12 @@ def kv_tokens(seed, req, p0, n, num_kv_heads, head_dim, scales, device="cpu",
         lo = max(p0, blk * BLOCK)
         hi = min(p0 + n, (blk + 1) * BLOCK)
         sl = slice(lo - blk * BLOCK, hi - blk * BLOCK)
-        out_k[lo - p0:hi - p0] = (raw[0, sl] * ks).to(dtype)
-        out_v[lo - p0:hi - p0] = (raw[1, sl] * vs).to(dtype)
+        rk, rv = raw[0, sl], raw[1, sl]
+        if base is not None:
+            rk = rk + base[0]
+            rv = rv + base[1]
+        out_k[lo - p0:hi - p0] = (rk * ks).to(dtype)
+        out_v[lo - p0:hi - p0] = (rv * vs).to(dtype)
     return out_k, out_v
 
 

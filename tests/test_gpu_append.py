@@ -33,7 +33,7 @@ def _misaligned(t):
 
 
 def run_append_scenario(d, Hq, Hkv, G, S, W, kv_dtype, calls, clip=0.9, mode="fixed4", pool_extra=37,
-                        seed=SEED, unaligned=False, rotations=None, keep=None, scale_fmt="f16"):
+                        seed=SEED, unaligned=False, rotations=None, keep=None, scale_fmt="f16", shared=0.0):
     from rotated_int2_kv_gb300 import ops
     B = len(calls[0])
     Lfin = [sum(c[b] for c in calls) for b in range(B)]
@@ -52,7 +52,7 @@ def run_append_scenario(d, Hq, Hkv, G, S, W, kv_dtype, calls, clip=0.9, mode="fi
     for call in calls:
         ks, vs = [], []
         for b in range(B):
-            k, v = synth.kv_tokens(seed, b, pos[b], call[b], Hkv, d, scales, dtype=kv_dtype)
+            k, v = synth.kv_tokens(seed, b, pos[b], call[b], Hkv, d, scales, dtype=kv_dtype, shared=shared)
             ks.append(k)
             vs.append(v)
         k = torch.cat(ks)
@@ -133,6 +133,18 @@ def test_large_appends_tiled_path(d, G, dtype, unaligned):
     # new ones, a ragged last tile
     calls = [[300, 290, 13], [2600, 2700, 1001]]
     st = run_append_scenario(d, 8, 2, G, 64, 256, dtype, calls, unaligned=unaligned)
+    assert st["exact"] > 0
+
+
+@pytest.mark.parametrize("d,G", [(256, 128), (256, 32), (128, 64), (128, 32)])
+def test_tiled_exact_paths_under_load(d, G):
+    # every row shares one strong direction per head, so the extremes of most
+    # vectors fall on the same few channels of y: at d 256 more exact products
+    # queue for one channel than a batch holds, and with group 32 more vectors
+    # of a tile have an uncertain (s, z) than the row stash holds, so the
+    # overflow paths (products over global memory) run next to the on-chip ones
+    calls = [[300, 290, 13], [2600, 2700, 1001]]
+    st = run_append_scenario(d, 8, 2, G, 64, 256, torch.bfloat16, calls, shared=8.0)
     assert st["exact"] > 0
 
 
