@@ -30,13 +30,13 @@
 // formed by a compensated dot product of the input row with R's fp32 column.
 //
 // For the (s, z) decisions those products run on chip and in parallel: R's
-// half is also kept channel-major in tensor memory (lane n = channel n of the
-// half, columns 256 + k = R[k][n], fp32), a vector with an uncertain group
-// copies its bf16 row from the x tile into shared memory before the next tile
-// overwrites it, and each candidate (vector, channel) is queued to the thread
-// that owns the channel's lane, which forms every product queued to it from
-// its lane and the stashed rows.  A request that finds its channel's queue or
-// the row stash full takes the warp-serial path over global memory instead.
+// half is also kept in tensor memory in fp32, each quad of lanes holding the
+// four k-quarters of four channels (see rt_exact_dots), a vector with an
+// uncertain group copies its bf16 row from the x tile into shared memory
+// before the next tile overwrites it, and each candidate (vector, channel) is
+// queued to the quad that holds the channel, whose four lanes form 64-term
+// parts of the product and add them.  A request that finds its channel's queue
+// or the row stash full takes the warp-serial path over global memory instead.
 #include <algorithm>
 #include <cstring>
 
