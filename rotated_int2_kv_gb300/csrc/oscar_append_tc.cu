@@ -37,7 +37,11 @@
 // in which some thread meets such a q in a group decides that group again with
 // correctly rounded division, forming y exactly (compensated dot product of
 // the input row with R's column) wherever y ± e straddles a boundary.  The
-// group's (s, z) are checked the same way at its extremes ± e first.
+// group's (s, z) are checked the same way at its extremes ± e first.  A vector
+// whose (s, z) could change copies its bf16 row from the x tile into a small
+// per-warpgroup stash before the next tile's rows overwrite the tile, so its
+// exact products read x from shared memory (others read their row in global
+// memory).
 // Tensor-memory loads (tcgen05.ld) are warp-collective, so every branch around
 // them is warp-uniform.
 #include <algorithm>
