@@ -30,11 +30,11 @@
 // formed by a compensated dot product of the input row with R's fp32 column.
 //
 // For the (s, z) decisions those products run on chip and in parallel: R's
-// half is also kept in tensor memory in fp32, each quad of lanes holding the
-// four k-quarters of four channels (see rt_exact_dots), a vector with an
+// half is also kept in tensor memory in fp32, each group of 8 lanes holding
+// the eight 32-k parts of eight channels (see rt_exact_dots), a vector with an
 // uncertain group copies its bf16 row from the x tile into shared memory
 // before the next tile overwrites it, and each candidate (vector, channel) is
-// queued to the quad that holds the channel, whose four lanes form 64-term
+// queued to the lane group that holds the channel, whose lanes form 32-term
 // parts of the product and add them.  A request that finds its channel's queue
 // or the row stash full takes the warp-serial path over global memory instead.
 #include <algorithm>
@@ -169,50 +169,51 @@ __device__ __forceinline__ void dot2_step(float& s, float& c, float x, float r) 
     c = __fadd_rn(c, __fadd_rn(er, pe));
 }
 
-// R's half in tensor memory: lane L of warp w holds, for m = 0 .. 3, the k-quarter
-// L mod 4 of channel 32w + L/4 + 8m of the half, R[64·(L mod 4) + kk][..] at
-// column kRtCol + 64m + kk (kk < 64).  So the four lanes of a quad hold the
-// four quarters of the same four channels, and one exact product is split
-// over them.
-//
+// R's half in tensor memory: the kLPC lanes of a lane group (lanes kLPC·i ..
+// kLPC·i + kLPC - 1 of warp w) hold the kLPC parts (kKP consecutive k each) of
+// the same kLPC channels; lane L holds, for m = 0 .. kLPC - 1, part L mod kLPC of
+// channel 32w + L/kLPC + (32/kLPC)·m of the half, R[kKP·(L mod kLPC) + kk][..]
+// at column kRtCol + kKP·m + kk (kk < kKP).  One exact product is split over
+// the lanes of a group.
+constexpr int kLPC = 8;                           // lanes per channel
+constexpr int kKP = kD / kLPC;                    // k per lane (32)
+static_assert(kKP == 32 && 32 % kLPC == 0, "one 32-column tensor-memory load per channel");
+
 // fl(x·R[:, ch]) for every stashed row queued to the channels of this thread's
-// quad (cnt, vec: the queues; yq: the results, [kN][kQ]): each lane forms the
-// compensated dot product over its 64 k in order, and the quad sums the four
-// (sum, error) pairs with two compensated steps.  Warp-collective (tensor-memory
-// loads, shuffles): every thread of the warp calls it.
+// lane group (cnt, vec: the queues; yq: the results, [kN][kQ]): each lane forms
+// the compensated dot product over its kKP k in order, and the group sums its
+// (sum, error) pairs with log2(kLPC) compensated shuffle steps.  Warp-collective
+// (tensor-memory loads, shuffles): every thread of the warp calls it.
 __device__ __noinline__ void rt_exact_dots(uint32_t trt, const uint16_t* xs, const int* cnt, const int* vec,
                                            float* yq, int warp, int lane) {
-    const int q = lane & 3, ci = lane >> 2;
+    const int part = lane % kLPC, ci = lane / kLPC;
 #pragma unroll 1
-    for (int m = 0; m < 4; ++m) {
-        const int ch = 32 * warp + ci + 8 * m;      // channel of the half
+    for (int m = 0; m < kLPC; ++m) {
+        const int ch = 32 * warp + ci + (32 / kLPC) * m;   // channel of the half
         const int n = min(cnt[ch], kQ);
         const int nmax = __reduce_max_sync(0xffffffffu, n);
         if (nmax == 0) continue;                    // warp-uniform
-        float ra[32], rb[32];
-        tc5::ld32(trt + 64 * m, ra);
-        tc5::ld32(trt + 64 * m + 32, rb);
+        float rr[32];
+        tc5::ld32(trt + kKP * m, rr);
         tc5::wait_ld();
 #pragma unroll 1
         for (int r = 0; r < nmax; ++r) {
             float s = 0.0f, c = 0.0f;
             if (r < n) {
-                const uint4* p = reinterpret_cast<const uint4*>(xs + (int64_t)vec[ch * kQ + r] * kXS + 64 * q);
+                const uint4* p = reinterpret_cast<const uint4*>(xs + (int64_t)vec[ch * kQ + r] * kXS + kKP * part);
 #pragma unroll
-                for (int w = 0; w < 8; ++w) {
+                for (int w = 0; w < kKP / 8; ++w) {
                     const uint4 u = p[w];
                     const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float r0 = w < 4 ? ra[8 * w + 2 * i] : rb[8 * (w - 4) + 2 * i];
-                        const float r1 = w < 4 ? ra[8 * w + 2 * i + 1] : rb[8 * (w - 4) + 2 * i + 1];
-                        dot2_step(s, c, __uint_as_float(wd[i] << 16), r0);
-                        dot2_step(s, c, __uint_as_float(wd[i] & 0xFFFF0000u), r1);
+                        dot2_step(s, c, __uint_as_float(wd[i] << 16), rr[8 * w + 2 * i]);
+                        dot2_step(s, c, __uint_as_float(wd[i] & 0xFFFF0000u), rr[8 * w + 2 * i + 1]);
                     }
                 }
             }
 #pragma unroll
-            for (int off = 1; off <= 2; off <<= 1) {  // the quad's four partial sums
+            for (int off = 1; off < kLPC; off <<= 1) {  // the group's partial sums
                 const float so = __shfl_xor_sync(0xffffffffu, s, off);
                 const float co = __shfl_xor_sync(0xffffffffu, c, off);
                 const float t = __fadd_rn(s, so);
@@ -221,7 +222,7 @@ __device__ __noinline__ void rt_exact_dots(uint32_t trt, const uint16_t* xs, con
                 s = t;
                 c = __fadd_rn(__fadd_rn(c, co), er);
             }
-            if (q == 0 && r < n) yq[ch * kQ + r] = __fadd_rn(s, c);
+            if (part == 0 && r < n) yq[ch * kQ + r] = __fadd_rn(s, c);
         }
     }
 }
@@ -230,7 +231,7 @@ __device__ __noinline__ void rt_exact_dots(uint32_t trt, const uint16_t* xs, con
 // one batch for the whole CTA: every such thread queues its channels within 2e
 // of the computed extremes (tensor-memory columns tgrp; lch0 / gch0: the
 // group's first channel within the half / in y) with its stashed row xslot,
-// the quads holding the channels form them, and the thread takes the min /
+// the lane groups holding the channels form them, and the thread takes the min /
 // max of its exact values.  A thread without a stashed row, or whose request
 // does not fit a queue, takes the warp-serial path.  All threads call it (CTA
 // barriers).
@@ -379,7 +380,7 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
     tc5::fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tacc = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's lanes, column 0
-    const uint32_t trt = tacc + kRtCol;             // this lane's share of R's half (quad layout)
+    const uint32_t trt = tacc + kRtCol;             // this lane's share of R's half (lane-group layout)
     // B: the two parts of R[:, 128·half .. +127] as 128 rows n × 256 k.  Item (n, j)
     // reads R[8j .. 8j+7][128·half + n] and stores its 16-byte chunk of both parts.
     // Thread tid builds every chunk of channel n = tid (kThreads == kN) and sums
@@ -416,24 +417,21 @@ quantize_tc256_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, 
             }
         }
     }
-    {   // R's half into tensor memory, quad layout (see rt_exact_dots): this lane's
-        // quarter of its four channels, 32 rows of R in flight
-        const int q = lane & 3, ci = lane >> 2;
+    {   // R's half into tensor memory, lane-group layout (see rt_exact_dots): this
+        // lane's part of its kLPC channels, 32 rows of R in flight
+        const int part = lane % kLPC, ci = lane / kLPC;
 #pragma unroll 1
-        for (int m = 0; m < 4; ++m) {
-            const float* src = R + (int64_t)(64 * q) * kD + kN * half + 32 * warp + ci + 8 * m;
-#pragma unroll 1
-            for (int k0 = 0; k0 < 64; k0 += 32) {
-                float v[32];
+        for (int m = 0; m < kLPC; ++m) {
+            const float* src = R + (int64_t)(kKP * part) * kD + kN * half + 32 * warp + ci + (32 / kLPC) * m;
+            float v[kKP];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = __ldg(src + (int64_t)(k0 + i) * kD);
+            for (int i = 0; i < kKP; ++i) v[i] = __ldg(src + (int64_t)i * kD);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t col[8];
+            for (int j = 0; j < kKP / 8; ++j) {
+                uint32_t col[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) col[i] = __float_as_uint(v[8 * j + i]);
-                    tc5::st8(trt + 64 * m + k0 + 8 * j, col);   // the same columns in every lane
-                }
+                for (int i = 0; i < 8; ++i) col[i] = __float_as_uint(v[8 * j + i]);
+                tc5::st8(trt + kKP * m + 8 * j, col);   // the same columns in every lane
             }
         }
         tc5::wait_st();
