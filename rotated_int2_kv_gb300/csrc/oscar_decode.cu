@@ -639,8 +639,8 @@ struct WinMmaCfg {
     static constexpr int RW = D / 2 + 4;       // words per staged row (≡ 4 mod 32: ldmatrix rows in distinct banks)
     static constexpr int CPR = D / 8;          // 16-byte chunks per row
     static constexpr int NTW = D / 32;         // n-tiles of 8 channels per warp in P·V
-    // shared words: K and V tiles, q fragments [KS][32][4], P fragments [4][32][4], max / sum [4][8] each
-    static constexpr int SMEM_WORDS = 2 * kWinTile * RW + KS * 128 + 4 * 128 + 2 * 32;
+    // shared words: one K-then-V tile, q fragments [KS][32][4], P fragments [4][32][4], max / sum [4][8] each
+    static constexpr int SMEM_WORDS = kWinTile * RW + KS * 128 + 4 * 128 + 2 * 32;
 };
 
 // One 64-token window tile (wt) of KV head hk, request b: the (m, l, o) partial
@@ -651,9 +651,11 @@ __device__ __forceinline__ void window_tile_mma(const DecodeParams& P, int hk, i
     using namespace wmma_detail;
     using C = WinMmaCfg<D>;
     constexpr int KS = C::KS, RW = C::RW, CPR = C::CPR, NTW = C::NTW;
-    uint32_t* sk = s_wm;                               // [64][RW] K rows
-    uint32_t* sv = sk + kWinTile * RW;                 // [64][RW] V rows
-    uint32_t* sqa = sv + kWinTile * RW;                // [KS][32 lanes][4] q fragments
+    // one row tile: K rows for the logits, then V rows over them for P·V (half
+    // the shared memory of two tiles: more blocks of the grid per SM)
+    uint32_t* sk = s_wm;                               // [64][RW] K rows, then V rows
+    uint32_t* sv = sk;
+    uint32_t* sqa = sk + kWinTile * RW;                // [KS][32 lanes][4] q fragments
     uint32_t* spa = sqa + KS * 128;                    // [4 sub-tiles][32 lanes][4] P fragments
     float* smx = reinterpret_cast<float*>(spa + 4 * 128);   // [4 warps][8 heads] sub-tile max
     float* ssm = smx + 32;                                   // [4 warps][8 heads] sub-tile sum
@@ -673,32 +675,35 @@ __device__ __forceinline__ void window_tile_mma(const DecodeParams& P, int hk, i
         if (tid < g) P.wml[pbase + (int64_t)tid * nwt] = make_float2(-1e30f, 0.f);
         return;
     }
-    // ---- every load of the tile in one round: K / V rows (cp.async) and q ----
+    // ---- the tile's rows of matrix mat (K 0, V 1) into the row tile (cp.async) ----
+    auto load_rows = [&](int mat) {
 #pragma unroll
-    for (int u = 0; u < 2 * kWinTile * CPR / 128; ++u) {
-        const int i = tid + 128 * u;
-        const int mat = i / (kWinTile * CPR), t = (i / CPR) % kWinTile, c = i % CPR;
-        const bool ok = t < nt;
-        const int tt = t0 + (ok ? t : 0);
-        const int pos = tt < sink_end ? tt : rec_lo + tt - sink_end;   // position in the request
-        uint32_t* dst = (mat ? sv : sk) + t * RW + 4 * c;
-        if (nr.on && ok && pos == L - 1) {             // the step's new token: from the input row
-            const int64_t e0 = ((int64_t)b * P.Hkv + hk) * D + 8 * c;
-            const void* src = mat ? nr.v : nr.k;
-            uint32_t w[4];
+        for (int u = 0; u < kWinTile * CPR / 128; ++u) {
+            const int i = tid + 128 * u;
+            const int t = i / CPR, c = i % CPR;
+            const bool ok = t < nt;
+            const int tt = t0 + (ok ? t : 0);
+            const int pos = tt < sink_end ? tt : rec_lo + tt - sink_end;   // position in the request
+            uint32_t* dst = sk + t * RW + 4 * c;
+            if (nr.on && ok && pos == L - 1) {         // the step's new token: from the input row
+                const int64_t e0 = ((int64_t)b * P.Hkv + hk) * D + 8 * c;
+                const void* src = mat ? nr.v : nr.k;
+                uint32_t w[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                w[u] = (uint32_t)f32_to_bf16_bits(load_elem(src, e0 + 2 * u, nr.dtype)) |
-                       ((uint32_t)f32_to_bf16_bits(load_elem(src, e0 + 2 * u + 1, nr.dtype)) << 16);
-            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-            continue;
+                for (int v = 0; v < 4; ++v)
+                    w[v] = (uint32_t)f32_to_bf16_bits(load_elem(src, e0 + 2 * v, nr.dtype)) |
+                           ((uint32_t)f32_to_bf16_bits(load_elem(src, e0 + 2 * v + 1, nr.dtype)) << 16);
+                *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+                continue;
+            }
+            const uint16_t* row = (tt < sink_end)
+                ? P.sink + (((int64_t)rq * S + tt) * P.Hkv + hk) * 2 * D
+                : P.recent + (((int64_t)rq * W + (rec_lo + tt - sink_end) % W) * P.Hkv + hk) * 2 * D;
+            cp_async16_zfill(dst, row + mat * D + 8 * c, ok ? 16u : 0u);
         }
-        const uint16_t* row = (tt < sink_end)
-            ? P.sink + (((int64_t)rq * S + tt) * P.Hkv + hk) * 2 * D
-            : P.recent + (((int64_t)rq * W + (rec_lo + tt - sink_end) % W) * P.Hkv + hk) * 2 * D;
-        cp_async16_zfill(dst, row + mat * D + 8 * c, ok ? 16u : 0u);
-    }
-    cp_async_commit();
+        cp_async_commit();
+    };
+    load_rows(0);                                      // K rows and q in one round
     {   // q A fragments: entry (kk, lane l, reg e): row (l>>2) + 8·(e&1) (bf16 part / lo part),
         // channels 16kk + 8·(e>>1) + 2·(l&3), +1.  Pairs (e = 2h, 2h+1) share their
         // loads, and every thread's loads are issued before the first is used.
@@ -760,7 +765,8 @@ __device__ __forceinline__ void window_tile_mma(const DecodeParams& P, int hk, i
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     if (j == 0) smx[warp * 8 + r] = mx;
-    __syncthreads();
+    __syncthreads();                                   // every warp's logits read the K rows
+    load_rows(1);                                      // V rows over them, in flight through the softmax
     const float m = fmaxf(fmaxf(smx[r], smx[8 + r]), fmaxf(smx[16 + r], smx[24 + r]));   // token 0 is valid: finite
     float pv[4];
 #pragma unroll
@@ -775,6 +781,7 @@ __device__ __forceinline__ void window_tile_mma(const DecodeParams& P, int hk, i
         split_bf16x2(pv[2], pv[3], pa[2], pa[3]);      // tokens 8+2j, 9+2j
         *reinterpret_cast<uint4*>(spa + (warp * 32 + lane) * 4) = make_uint4(pa[0], pa[1], pa[2], pa[3]);
     }
+    cp_async_wait<0>();                                // this thread's V rows landed
     __syncthreads();
     // ---- P·V: channels [d/4·warp, d/4·(warp+1)), all sub-tiles with tokens ----
     float o[NTW][4];
@@ -834,8 +841,10 @@ __global__ void __launch_bounds__(128) window_mma_kernel(DecodeParams P) {
 // Blocks start in index order, so the longest chains (the appends) start first.
 // The history kernel and the combine follow as in oscar_decode_attention.
 // ---------------------------------------------------------------------------
+// With the tensor-core window tiles (one 24 KB row tile per block) 8 blocks fit
+// an SM, so their registers are bounded to match (64 per thread).
 template <int D, int GQ, bool MMA>
-__global__ void __launch_bounds__(128) step_pre_kernel(DecodeParams P, AppendParams A, NewRowSrc nr) {
+__global__ void __launch_bounds__(128, MMA ? 8 : 1) step_pre_kernel(DecodeParams P, AppendParams A, NewRowSrc nr) {
     {   // R_K and R_V are no kernel's output: their lines head for L2 while the
         // previous grid drains (two lines per block; the first 2d²·4/256 blocks
         // cover both matrices)
