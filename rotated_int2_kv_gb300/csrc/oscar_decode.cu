@@ -841,10 +841,10 @@ __global__ void __launch_bounds__(128) window_mma_kernel(DecodeParams P) {
 // Blocks start in index order, so the longest chains (the appends) start first.
 // The history kernel and the combine follow as in oscar_decode_attention.
 // ---------------------------------------------------------------------------
-// With the tensor-core window tiles (one 24 KB row tile per block) 8 blocks fit
-// an SM, so their registers are bounded to match (64 per thread).
+// With the tensor-core window tiles (one 24 KB row tile per block) 9 blocks fit
+// an SM's shared memory, so their registers are bounded to match (56 per thread).
 template <int D, int GQ, bool MMA>
-__global__ void __launch_bounds__(128, MMA ? 8 : 1) step_pre_kernel(DecodeParams P, AppendParams A, NewRowSrc nr) {
+__global__ void __launch_bounds__(128, MMA ? 9 : 1) step_pre_kernel(DecodeParams P, AppendParams A, NewRowSrc nr) {
     {   // R_K and R_V are no kernel's output: their lines head for L2 while the
         // previous grid drains (two lines per block; the first 2d²·4/256 blocks
         // cover both matrices)
