@@ -269,8 +269,10 @@ struct PfCfg {
     }
 };
 
+// At d <= 128 two blocks share an SM (about 111 KB of shared memory each), so
+// registers are bounded to 128 per thread: 16 warps per SM instead of 8.
 template <int D, int G, int TT>
-__global__ void __launch_bounds__(PfCfg<D, TT>::THREADS) prefill_attn_kernel(PrefillParams P) {
+__global__ void __launch_bounds__(PfCfg<D, TT>::THREADS, D <= 128 ? 2 : 1) prefill_attn_kernel(PrefillParams P) {
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     using C_ = PfCfg<D, TT>;
     constexpr int RS = C_::RS, KS = D / 16, NTO = D / 8, NTT = TT / 8, KT = TT / 16, NG = D / G;
