@@ -269,10 +269,11 @@ struct PfCfg {
     }
 };
 
-// At d <= 128 two blocks share an SM (about 111 KB of shared memory each), so
-// registers are bounded to 128 per thread: 16 warps per SM instead of 8.
+// Two blocks share an SM: at d <= 128 (about 111 KB of shared memory each)
+// registers are bounded to 128 per thread, 16 warps per SM instead of 8; at d =
+// 256 the key tiles hold 16 tokens (about 104 KB per block), 8 warps instead of 4.
 template <int D, int G, int TT>
-__global__ void __launch_bounds__(PfCfg<D, TT>::THREADS, D <= 128 ? 2 : 1) prefill_attn_kernel(PrefillParams P) {
+__global__ void __launch_bounds__(PfCfg<D, TT>::THREADS, 2) prefill_attn_kernel(PrefillParams P) {
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     using C_ = PfCfg<D, TT>;
     constexpr int RS = C_::RS, KS = D / 16, NTO = D / 8, NTT = TT / 8, KT = TT / 16, NG = D / G;
@@ -675,7 +676,7 @@ int launch_prefill(PrefillParams& P, int max_c, cudaStream_t st) {
     const int64_t dense = P.total_q + (int64_t)P.batch * (P.S + P.W);
     launch_dependent(prefill_dense_kernel<D>, dim3((unsigned)dense), dim3(D), 0, st, P);
     if (int rc = check_cuda("prefill_dense_kernel launch")) return rc;
-    constexpr int TT = 32;
+    constexpr int TT = D >= 256 ? 16 : 32;          // key tile: two blocks per SM at d = 256 too
     using C_ = PfCfg<D, TT>;
     const int rblocks = (int)(((int64_t)max_c * P.g + C_::ROWS - 1) / C_::ROWS);
     const int prof = prof_begin(6, st);
