@@ -64,6 +64,12 @@ def parse():
                          "(launch-bound); qwen32b-ragged: 64 q / 8 KV heads, batch 8, lengths uniform in "
                          "[65,536, 131,072], per-head K outliers, 50-step cycle; gqa6-wide: 24 q / 4 KV heads, "
                          "d 256, group 128, batch 5 at 112,000 tokens")
+    ap.add_argument("--prefill-only", choices=["qwen8b", "gqa6-wide"], default=None,
+                    help="time only the prefill attention of one request (shape qwen8b: 32 q / 8 KV heads, d 128; "
+                         "gqa6-wide: 24 q / 4 KV heads, d 256) and print its measurement; --steps is the number "
+                         "of timed calls")
+    ap.add_argument("--prefill-prefix", type=int, default=32768, help="cached prefix of --prefill-only, tokens")
+    ap.add_argument("--prefill-chunk", type=int, default=8192, help="queries of --prefill-only's chunk")
     return ap.parse_args()
 
 
@@ -521,6 +527,17 @@ def main():
         from rotated_int2_kv_gb300 import build
         build.build()
     ops.lib()
+    if args.prefill_only:
+        peaks = {}
+        try:
+            peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        except (OSError, ValueError):
+            pass
+        if rank == 0:
+            print(json.dumps(prefill_measure(args.prefill_only, args.prefill_prefix, args.prefill_chunk,
+                                             max(args.steps, 1), float(peaks.get("bf16_tflops", 1900.0)))),
+                  flush=True)
+        return
     steps_total = args.steps + args.warmup
     w = build_decode_workload(rank, steps_total)
     stream = torch.cuda.current_stream()

@@ -45,3 +45,18 @@ def test_ragged_workload_lengths_and_description():
     # tokens of one step: every request at its own length
     s = 3
     assert int((b.LB + s + 1).sum()) == int(lens.sum()) + 8 * s
+
+
+def test_prefill_only_options():
+    b = _bench()
+    saved = sys.argv
+    try:
+        sys.argv = ["bench.py"]
+        a = b.parse()
+        assert a.prefill_only is None and (a.prefill_prefix, a.prefill_chunk) == (32768, 8192)
+        sys.argv = ["bench.py", "--prefill-only", "gqa6-wide", "--prefill-prefix", "8192", "--prefill-chunk", "1024",
+                    "--steps", "1"]
+        a = b.parse()
+        assert (a.prefill_only, a.prefill_prefix, a.prefill_chunk, a.steps) == ("gqa6-wide", 8192, 1024, 1)
+    finally:
+        sys.argv = saved
