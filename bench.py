@@ -68,6 +68,8 @@ def parse():
                     help="time only the prefill attention of one request (shape qwen8b: 32 q / 8 KV heads, d 128; "
                          "gqa6-wide: 24 q / 4 KV heads, d 256) and print its measurement; --steps is the number "
                          "of timed calls")
+    ap.add_argument("--calibration-only", action="store_true",
+                    help="time only the calibration statistics on the device (C_Q and C_S) and print them")
     ap.add_argument("--prefill-prefix", type=int, default=32768, help="cached prefix of --prefill-only, tokens")
     ap.add_argument("--prefill-chunk", type=int, default=8192, help="queries of --prefill-only's chunk")
     return ap.parse_args()
@@ -513,6 +515,55 @@ def prefill_measure(name, L0, C, reps, bf16_peak):
                          "flops": "4*d per (query head, key) pair, causal within the chunk"}}
 
 
+# GB300 fp64 on the CUDA cores: 1.25 TFLOP/s nominal (2 fp64 FMA per SM and
+# cycle x 152 SMs x 2.07 GHz x 2 flops = 1.26 TFLOP/s); no measured fp64 peak.
+FP64_PEAK_TFLOPS = 1.25
+
+
+def calibration_measure(reps):
+    """The calibration statistics on the device: C_Q over 65,536 key rows and
+    C_S over one 4,096-token sequence's scores, d 128, bf16 activations.
+    Time per call (CUDA events) and the fp64 rate of the algorithmic flops:
+    n·d(d+1) for C_Q (one triangle of XᵀX), 2·n_q·n_k·d + n_q·d(d+1) for C_S."""
+    import numpy as np
+    import torch
+    from rotated_int2_kv_gb300 import ops, synth
+    dev = torch.device("cuda")
+    d, n, nq = 128, 65536, 4096
+    x = torch.from_numpy(synth.calib_samples(SEED, 0, d, n=n).astype(np.float32)).to(torch.bfloat16).to(dev)
+    v = torch.from_numpy(synth.calib_samples(SEED, 1, d, n=nq).astype(np.float32)).to(torch.bfloat16).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(SEED)
+    scores = torch.softmax(torch.randn((nq, nq), generator=g, device=dev), dim=1)   # rows of attention weights
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    cq_ms = timed(lambda: ops.covariance_device(x))
+    cs_ms = timed(lambda: ops.value_covariance_device(scores, v))
+    assert ops.device_status() == 0
+    cq_tf = n * d * (d + 1) / (cq_ms / 1e3) / 1e12
+    cs_tf = (2.0 * nq * nq * d + nq * d * (d + 1)) / (cs_ms / 1e3) / 1e12
+    del x, v, scores
+    torch.cuda.empty_cache()
+    return {"workload": "C_Q of 65,536 bf16 rows and C_S of a 4,096 x 4,096 score matrix over 4,096 bf16 value rows, "
+                        "d 128, fp64 accumulation",
+            "covariance_ms": cq_ms, "value_covariance_ms": cs_ms, "covariance_fp64_tflops": cq_tf,
+            "roofline": {"bound": "alu", "achieved": cs_tf, "peak": FP64_PEAK_TFLOPS, "unit": "TFLOP/s",
+                         "frac": cs_tf / FP64_PEAK_TFLOPS, "kernel": "value covariance (Y = S V, then YᵀY; fp64 FMA)",
+                         "peak_source": "nominal fp64 rate (152 SMs x 2 FMA/cycle x 2.07 GHz)"}}
+
+
 # --------------------------------------------------------------------------
 def main():
     args = parse()
@@ -527,6 +578,10 @@ def main():
         from rotated_int2_kv_gb300 import build
         build.build()
     ops.lib()
+    if args.calibration_only:
+        if rank == 0:
+            print(json.dumps(calibration_measure(max(args.steps, 1))), flush=True)
+        return
     if args.prefill_only:
         peaks = {}
         try:
@@ -635,6 +690,7 @@ def main():
                           for name in ("qwen32b-ragged", "gqa6-wide", "qwen8b-100k-e4m3")}
         line["prefill"] = {name: prefill_measure(name, 32768, 8192, 3, float(peaks.get("bf16_tflops", 1900.0)))
                            for name in ("qwen8b", "gqa6-wide")}
+        line["calibration"] = calibration_measure(5)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         run, L = oracle_sample(w["seed"])
         run()

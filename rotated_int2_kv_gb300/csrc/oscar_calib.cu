@@ -12,7 +12,9 @@
 // round), split over the rows in slices whose partial d×d sums land in the
 // workspace and are added in slice order by a second kernel: the result does
 // not depend on scheduling.  C is symmetric, so only tile pairs (i <= j) are
-// formed and the reduction mirrors them.
+// formed and the reduction mirrors them.  Y = S·V is split the same way over
+// ranges of keys when its tiles alone would leave SMs idle, the ranges' partial
+// Y added in range order.
 #include <algorithm>
 
 #include "oscar_internal.h"
@@ -26,6 +28,7 @@ constexpr int kCT = 64;           // C tile: 64 × 64 outputs per block
 constexpr int kCRows = 32;        // rows staged per step
 constexpr int kCThreads = 256;    // 4 × 4 outputs per thread
 constexpr int kMaxSplits = 256;
+constexpr int64_t kMaxYPartBytes = 64ll << 20;   // partial sums of Y over key ranges, at most
 
 __device__ __forceinline__ double load_act(const void* base, int64_t i, int dtype) {
     if (dtype == OSCAR_DTYPE_BF16) return (double)bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(base)[i]);
@@ -113,14 +116,19 @@ __global__ void __launch_bounds__(256) cov_reduce_kernel(const double* part, int
     cov[e] = s / (double)n;
 }
 
-// Y = S·V (fp64 accumulation): one block per 64 × 64 tile of Y, over all of K.
+// Y = S·V (fp64 accumulation): one block per 64 × 64 tile of Y and range of
+// k_chunk keys (blockIdx.z), written to slab z of Y (n_q × d each); a range past
+// n_k writes zeros.
 __global__ void __launch_bounds__(kCThreads) score_values_kernel(const float* S, const void* V, int v_dtype,
-                                                                 int64_t n_q, int64_t n_k, int d, double* Y) {
+                                                                 int64_t n_q, int64_t n_k, int d, int64_t k_chunk,
+                                                                 double* Y) {
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     __shared__ double ss[kCT][kCRows + 1];   // S tile: [query][k]
     __shared__ double sv[kCRows][kCT];       // V tile: [k][channel]
     const int64_t q0 = (int64_t)blockIdx.y * kCT;
     const int c0 = blockIdx.x * kCT;
+    const int64_t kb = (int64_t)blockIdx.z * k_chunk, ke = min(n_k, kb + k_chunk);
+    Y += (int64_t)blockIdx.z * n_q * d;
     const int tid = threadIdx.x;
     const int tr = (tid / 16) * 4, tc = (tid % 16) * 4;
     double acc[4][4];
@@ -128,15 +136,15 @@ __global__ void __launch_bounds__(kCThreads) score_values_kernel(const float* S,
     for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) acc[a][b] = 0.0;
-    for (int64_t k0 = 0; k0 < n_k; k0 += kCRows) {
+    for (int64_t k0 = kb; k0 < ke; k0 += kCRows) {
         __syncthreads();
         for (int i = tid; i < kCT * kCRows; i += kCThreads) {
             const int qq = i / kCRows, kk = i % kCRows;
             const int64_t q = q0 + qq, k = k0 + kk;
-            ss[qq][kk] = (q < n_q && k < n_k) ? (double)S[q * n_k + k] : 0.0;
+            ss[qq][kk] = (q < n_q && k < ke) ? (double)S[q * n_k + k] : 0.0;
             const int kv = i / kCT, c = i % kCT;
             const int64_t k2 = k0 + kv;
-            sv[kv][c] = (k2 < n_k && c0 + c < d) ? load_act(V, k2 * d + c0 + c, v_dtype) : 0.0;
+            sv[kv][c] = (k2 < ke && c0 + c < d) ? load_act(V, k2 * d + c0 + c, v_dtype) : 0.0;
         }
         __syncthreads();
 #pragma unroll 4
@@ -164,12 +172,59 @@ __global__ void __launch_bounds__(kCThreads) score_values_kernel(const float* S,
     }
 }
 
-// Row slices of the covariance: enough blocks to fill the GPU a few times
-// over, at least 32 rows each.
+// Y[e] = Σ_z part[z][e] over the key ranges, in range order (a fixed summation
+// order, so repeated calls agree bit for bit).
+__global__ void __launch_bounds__(256) sum_splits_kernel(const double* part, int nsplit, int64_t nel, double* Y) {
+    grid_dep_sync();   // previous grid of the stream done (programmatic launch)
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= nel) return;
+    double s = part[e];
+    for (int z = 1; z < nsplit; ++z) s += part[(int64_t)z * nel + e];
+    Y[e] = s;
+}
+
+// Key ranges of Y = S·V.  The fp64 FMA rate bounds the product, so every SM
+// needs an equal share: when the 64 × 64 tiles of Y alone make less than
+// about 16 blocks per SM, the keys are split into ranges (multiples of 32
+// keys) until they do, within kMaxYPartBytes of partial sums.
+int score_splits(int64_t n_q, int64_t n_k, int d, int nsm) {
+    const int64_t tiles = (int64_t)((d + kCT - 1) / kCT) * ((n_q + kCT - 1) / kCT);
+    int64_t s = ((int64_t)std::max(1, nsm) * 16 + tiles - 1) / tiles;
+    s = std::min<int64_t>(s, (n_k + kCRows - 1) / kCRows);
+    s = std::min<int64_t>(s, std::max<int64_t>(1, kMaxYPartBytes / (n_q * d * (int64_t)sizeof(double))));
+    return (int)std::max<int64_t>(1, s);
+}
+
+// Keys per range for s ranges: a multiple of the 32-key staging step.
+int64_t score_chunk(int64_t n_k, int s) {
+    const int64_t per = (n_k + s - 1) / s;
+    return (per + kCRows - 1) / kCRows * kCRows;
+}
+
+size_t aligned256(size_t b) { return (b + 255) / 256 * 256; }
+
+// Blocks of cov_partial_kernel that one SM holds at once (4 at 64 registers
+// per thread).
+int cov_resident() {
+    static const int r = [] {
+        int nb = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, cov_partial_kernel, kCThreads, 0) != cudaSuccess ||
+            nb < 1) {
+            (void)cudaGetLastError();
+            nb = 4;
+        }
+        return nb;
+    }();
+    return r;
+}
+
+// Row slices of the covariance, at least 32 rows each: tile pairs × slices
+// fill the SMs' resident blocks once, rounded down (the fp64 FMA rate bounds
+// the kernel, so a block past a whole wave would run alone after it).
 int cov_slices(int64_t n, int d, int nsm) {
     const int nt = (d + kCT - 1) / kCT;
     const int pairs = nt * (nt + 1) / 2;
-    int64_t s = ((int64_t)std::max(1, nsm) * 4 + pairs - 1) / pairs;
+    int64_t s = (int64_t)std::max(1, nsm) * cov_resident() / pairs;
     s = std::min<int64_t>(s, (n + kCRows - 1) / kCRows);
     return (int)std::max<int64_t>(1, std::min<int64_t>(s, kMaxSplits));
 }
@@ -233,8 +288,9 @@ extern "C" int oscar_value_covariance_workspace_bytes(int64_t n_q, int64_t n_k, 
     if (int rc = validate_dims(n_q, d)) return rc;
     const int nsm = sm_count();
     if (nsm <= 0) return OSCAR_ERR_CUDA;
-    const size_t y = ((size_t)n_q * d * sizeof(double) + 255) / 256 * 256;
-    *bytes = y + (size_t)cov_slices(n_q, d, nsm) * d * d * sizeof(double);
+    const size_t y = aligned256((size_t)n_q * d * sizeof(double));
+    const int sk = score_splits(n_q, n_k, d, nsm);
+    *bytes = y + (sk > 1 ? sk * y : 0) + (size_t)cov_slices(n_q, d, nsm) * d * d * sizeof(double);
     return OSCAR_OK;
 }
 
@@ -251,15 +307,28 @@ extern "C" int oscar_value_covariance_device(const float* scores, const void* va
     const int nsm = sm_count();
     if (nsm <= 0) return OSCAR_ERR_CUDA;
     const int ns = cov_slices(n_q, d, nsm);
-    const size_t y = ((size_t)n_q * d * sizeof(double) + 255) / 256 * 256;
-    const size_t need = y + (size_t)ns * d * d * sizeof(double);
+    const int sk = score_splits(n_q, n_k, d, nsm);
+    const size_t y = aligned256((size_t)n_q * d * sizeof(double));
+    const size_t yparts = sk > 1 ? sk * y : 0;
+    const size_t need = y + yparts + (size_t)ns * d * d * sizeof(double);
     if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
         return fail(OSCAR_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes", need);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    double* Y = static_cast<double*>(workspace);
-    double* part = reinterpret_cast<double*>(static_cast<char*>(workspace) + y);
-    launch_dependent(score_values_kernel, dim3((unsigned)((d + kCT - 1) / kCT), (unsigned)((n_q + kCT - 1) / kCT)),
-                     dim3(kCThreads), 0, st, scores, values, v_dtype, n_q, n_k, (int)d, Y);
+    char* ws = static_cast<char*>(workspace);
+    double* Y = reinterpret_cast<double*>(ws);
+    double* Yp = reinterpret_cast<double*>(ws + y);              // sk slabs of nel doubles (sk > 1)
+    double* part = reinterpret_cast<double*>(ws + y + yparts);
+    const int64_t nel = n_q * d;
+    launch_dependent(score_values_kernel,
+                     dim3((unsigned)((d + kCT - 1) / kCT), (unsigned)((n_q + kCT - 1) / kCT), (unsigned)sk),
+                     dim3(kCThreads), 0, st, scores, values, v_dtype, n_q, n_k, (int)d, score_chunk(n_k, sk),
+                     sk > 1 ? Yp : Y);
     if (int rc = check_cuda("score_values_kernel launch")) return rc;
+    if (sk > 1) {
+        // slab z of the partial sums starts nel doubles after slab z - 1 (sk·nel·8 <= yparts bytes)
+        launch_dependent(sum_splits_kernel, dim3((unsigned)((nel + 255) / 256)), dim3(256), 0, st, (const double*)Yp,
+                         sk, nel, Y);
+        if (int rc = check_cuda("sum_splits_kernel launch")) return rc;
+    }
     return launch_cov(Y, 2 /* fp64 rows */, n_q, d, cov, part, ns, st);
 }

@@ -58,5 +58,9 @@ def test_prefill_only_options():
                     "--steps", "1"]
         a = b.parse()
         assert (a.prefill_only, a.prefill_prefix, a.prefill_chunk, a.steps) == ("gqa6-wide", 8192, 1024, 1)
+        assert not a.calibration_only
+        sys.argv = ["bench.py", "--calibration-only", "--steps", "3"]
+        a = b.parse()
+        assert a.calibration_only and a.steps == 3
     finally:
         sys.argv = saved

@@ -54,6 +54,24 @@ def test_value_covariance_matches_oracle(n_q, n_k, d, vdt):
     assert _rel(got, want) <= 1e-12
 
 
+@pytest.mark.parametrize("n_q,n_k,d", [(40000, 40, 256), (64, 4000, 128)])
+def test_value_covariance_split_paths_and_determinism(n_q, n_k, d):
+    # (40000, 40, 256): Y fills the GPU and its partial sums would pass 64 MB, so the
+    # keys are not split; (64, 4000, 128): two tiles of Y, the keys split into many
+    # ranges whose partial Y are added in a fixed order
+    from rotated_int2_kv_gb300 import ops
+    rng = np.random.default_rng(SEED + n_k)
+    S = rng.random((n_q, n_k)).astype(np.float32)
+    S /= S.sum(axis=1, keepdims=True)
+    V = torch.from_numpy(rng.standard_normal((n_k, d)).astype(np.float32)).to(torch.bfloat16)
+    Sd, Vd = torch.from_numpy(S).cuda(), V.cuda()
+    got = ops.value_covariance_device(Sd, Vd).cpu().numpy()
+    again = ops.value_covariance_device(Sd, Vd).cpu().numpy()
+    assert np.array_equal(got, again)
+    want = oracle.value_covariance(S.astype(np.float64), V.float().numpy().astype(np.float64))
+    assert _rel(got, want) <= 1e-12
+
+
 def test_rotation_from_device_covariance():
     # the library's rotation from the device C_Q equals the oracle's rotation from its C_Q
     from rotated_int2_kv_gb300 import ops
