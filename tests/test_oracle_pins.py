@@ -326,8 +326,16 @@ def test_quantiser_code_is_the_nearest_level_brute_force():
     d, G = 64, 32
     Y = (rng.standard_normal((300, d)) * 3).astype(np.float32)
     codes, s, z = oracle.quantize_rows(Y, G, 0.9)
+    assert s.dtype == np.float16 and z.dtype == np.float16
     for i in range(300):
         for gi in range(d // G):
+            # the stored pair is the fp16 rounding (numpy's IEEE conversion) of the
+            # fp32 (hi - lo)/3 and lo of the clipped group
+            yg = Y[i, gi * G:(gi + 1) * G]
+            lo = np.float32(np.float32(0.9) * yg.min())
+            hi = np.float32(np.float32(0.9) * yg.max())
+            assert float(s[i, gi]) == float(np.float16(np.float32(np.float32(hi - lo) / np.float32(3))))
+            assert float(z[i, gi]) == float(np.float16(lo))
             s32 = np.float32(s[i, gi])
             z32 = np.float32(z[i, gi])
             for j in range(gi * G, (gi + 1) * G):
