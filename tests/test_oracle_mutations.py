@@ -216,6 +216,18 @@ def _record_bytes_unpadded(orig):
     return f
 
 
+def _quantize_into_rotations_swapped(orig):
+    # the cache rotates history keys by R_V and values by R_K
+    def f(self, slots, Xk, Xv, keep_y=False):
+        rk, rv = self.rot_k, self.rot_v
+        self.rot_k, self.rot_v = rv, rk
+        try:
+            return orig(self, slots, Xk, Xv, keep_y)
+        finally:
+            self.rot_k, self.rot_v = rk, rv
+    return f
+
+
 class _CacheView:
     """A cache whose rotation attribute is seen transposed by the oracle."""
 
@@ -352,6 +364,23 @@ CASES = [
      lambda mp: mp.setattr(P, "bf16_round", lambda x: np.asarray(x, np.float32)),
      [pins.test_prefill_without_history_equals_textbook_causal_attention,
       pins.test_prefill_of_one_token_equals_decode_with_a_wider_window]),
+    ("history keys rotated by R_V and values by R_K",
+     lambda mp: mp.setattr(C.OracleCache, "_quantize_into",
+                           _quantize_into_rotations_swapped(C.OracleCache._quantize_into)),
+     [pins.test_decode_history_on_grid_equals_textbook_attention, pins.test_chunked_append_equals_token_by_token,
+      pins.test_prefill_of_one_token_equals_decode_with_a_wider_window]),
+    ("positions entering the history shifted by one",
+     lambda mp: _plant_np(mp, C, arange=lambda a, b: np.arange(a + 1, b + 1)),
+     [pins.test_decode_history_on_grid_equals_textbook_attention, pins.test_chunked_append_equals_token_by_token,
+      pins.test_prefill_of_one_token_equals_decode_with_a_wider_window]),
+    ("clip ratio ignored",
+     lambda mp: _plant(mp, Q, "quantize_rows",
+                       lambda o: (lambda Y, G, r, scale_fmt="f16": o(Y, G, 1.0, scale_fmt))),
+     [pins.test_quantiser_code_is_the_nearest_level_brute_force]),
+    ("rows rotated by Rᵀ",
+     lambda mp: _plant(mp, Q, "rotate_rows", lambda o: (lambda X, Rm: o(X, np.asarray(Rm).T))),
+     [pins.test_decode_history_on_grid_equals_textbook_attention, pins.test_chunked_append_equals_token_by_token,
+      pins.test_rotation_invariance_of_logits_and_attention]),
     ("bits per element without the BF16 windows",
      lambda mp: _plant(mp, ACC, "bits_per_element", _bits_without_windows),
      [pins.test_accounting_matches_pages]),

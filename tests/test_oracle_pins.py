@@ -515,17 +515,19 @@ def test_decode_all_bf16_equals_textbook_attention():
 
 
 def test_decode_history_on_grid_equals_textbook_attention():
-    # R a permutation (orthogonal, exact in fp32); history keys/values chosen so
-    # that their rotated images lie exactly on the INT2 grid at clip 1.0: then
-    # the mixed cache reproduces textbook attention on the original vectors.
+    # R_K and R_V two different permutations (orthogonal, exact in fp32); history
+    # keys and values chosen so that their images under their own rotation lie
+    # exactly on the INT2 grid at clip 1.0: then the mixed cache reproduces
+    # textbook attention on the original vectors (and a cache that rotated keys
+    # by R_V, or values by R_K, would not).
     d, G, S, W = 32, 16, 2, 3
     cfg = oracle.OracleConfig(d, 4, 1, G, S, W, 1.0)
     rng = np.random.default_rng(14)
-    perm = rng.permutation(d)
-    R = np.eye(d)[:, perm]                     # (x R)[j] = x[perm[j]]
+    Rk = np.eye(d)[:, rng.permutation(d)]      # (x R)[j] = x[perm[j]]
+    Rv = np.eye(d)[:, rng.permutation(d)]
     L = 20
 
-    def on_grid(n):
+    def on_grid(n, R):
         c = rng.integers(0, 4, (n, d))
         c[:, 0::G] = 0
         c[:, 1::G] = 3
@@ -534,10 +536,10 @@ def test_decode_history_on_grid_equals_textbook_attention():
         y = (z[:, :, None] + c.reshape(n, d // G, G) * s[:, :, None]).reshape(n, d)
         return y @ R.T                          # x with x R = y
 
-    k = on_grid(L)[:, None, :].astype(np.float32)
-    v = on_grid(L)[:, None, :].astype(np.float32)
+    k = on_grid(L, Rk)[:, None, :].astype(np.float32)
+    v = on_grid(L, Rv)[:, None, :].astype(np.float32)
     assert np.array_equal(oracle.bf16_round(k), k)
-    cache = oracle.OracleCache(cfg, 32, 1, R, R)
+    cache = oracle.OracleCache(cfg, 32, 1, Rk, Rv)
     pt = rng.permutation(32)[None, :L]
     cache.append(k, v, [0, L], [0], [0], pt)
     q = rng.standard_normal((1, 4, d))
