@@ -138,6 +138,20 @@ def _e4m3_saturating_at_240(orig):
     return f
 
 
+def _ties_away(orig, dtype):
+    # round to nearest with ties away from zero: at a tie the two neighbours of
+    # x round differently; take the one of larger magnitude
+    def f(x):
+        xa = np.asarray(x, dtype=dtype)
+        up = np.asarray(orig(np.nextafter(xa, np.asarray(np.inf, dtype))), np.float64)
+        dn = np.asarray(orig(np.nextafter(xa, np.asarray(-np.inf, dtype))), np.float64)
+        r = np.asarray(orig(xa), np.float64)
+        tie = (up != dn) & (r != xa.astype(np.float64))
+        away = np.where(np.abs(up) >= np.abs(dn), up, dn)
+        return np.where(tie, away, r).astype(np.asarray(orig(xa)).dtype)
+    return f
+
+
 def _pack_high_bits_first(orig):
     def f(codes):
         codes = np.asarray(codes, dtype=np.uint8)
@@ -240,6 +254,26 @@ class _CacheView:
         return np.ascontiguousarray(v.T) if k == self._which else v
 
 
+class _CacheIdentity:
+    """A cache whose rotation attribute is seen as the identity by the oracle."""
+
+    def __init__(self, cache, which):
+        self._c = cache
+        self._which = which
+
+    def __getattr__(self, k):
+        v = getattr(self._c, k)
+        return np.eye(v.shape[0]) if k == self._which else v
+
+
+def _attention_without(which):
+    def make(orig):
+        def f(cache, *a, **k):
+            return orig(_CacheIdentity(cache, which), *a, **k)
+        return f
+    return make
+
+
 def _attention_with_transposed(which):
     def make(orig):
         def f(cache, *a, **k):
@@ -292,12 +326,22 @@ CASES = [
     ("bf16 rounding truncates",
      lambda mp: _plant(mp, Q, "bf16_round", _bf16_truncating),
      [pins.test_bf16_round_matches_torch]),
+    ("bf16 rounding with ties away from zero",
+     lambda mp: _plant(mp, Q, "bf16_round", lambda o: _ties_away(o, np.float32)),
+     [pins.test_bf16_round_matches_torch]),
+    ("E4M3 rounding with ties away from zero",
+     lambda mp: _plant(mp, Q, "e4m3_round", lambda o: _ties_away(o, np.float32)),
+     [pins.test_e4m3_rounding_matches_torch]),
     ("E4M3 saturates at 240",
      lambda mp: _plant(mp, Q, "e4m3_round", _e4m3_saturating_at_240),
      [pins.test_e4m3_rounding_matches_torch]),
     ("codes rounded down instead of to nearest",
      lambda mp: _plant_np(mp, Q, rint=np.floor),
      [pins.test_quantiser_code_is_the_nearest_level_brute_force, pins.test_quantiser_exact_grid_round_trip]),
+    ("codes at an exact half rounded away from zero",
+     lambda mp: _plant_np(mp, Q, rint=lambda x: np.sign(x) * np.floor(np.abs(x) + 0.5)),
+     [pins.test_quantiser_code_is_the_nearest_level_brute_force, pins.test_quantiser_exact_grid_round_trip,
+      pins.test_quantiser_ties_round_to_even]),
     ("codes clamped to [0, 2]",
      lambda mp: _plant_np(mp, Q, clip=lambda x, a, b: np.clip(x, a, 2.0)),
      [pins.test_quantiser_code_is_the_nearest_level_brute_force, pins.test_quantiser_exact_grid_round_trip]),
@@ -381,6 +425,18 @@ CASES = [
      lambda mp: _plant(mp, Q, "rotate_rows", lambda o: (lambda X, Rm: o(X, np.asarray(Rm).T))),
      [pins.test_decode_history_on_grid_equals_textbook_attention, pins.test_chunked_append_equals_token_by_token,
       pins.test_rotation_invariance_of_logits_and_attention]),
+    ("history output not rotated back by R_Vᵀ (decode)",
+     lambda mp: _plant(mp, A, "decode_attention", _attention_without("rot_v")),
+     [pins.test_decode_history_on_grid_equals_textbook_attention]),
+    ("history logits against the unrotated query (decode)",
+     lambda mp: _plant(mp, A, "decode_attention", _attention_without("rot_k")),
+     [pins.test_decode_history_on_grid_equals_textbook_attention]),
+    ("history output not rotated back by R_Vᵀ (prefill)",
+     lambda mp: _plant(mp, P, "prefill_attention", _attention_without("rot_v")),
+     [pins.test_prefill_of_one_token_equals_decode_with_a_wider_window]),
+    ("history logits against the unrotated query (prefill)",
+     lambda mp: _plant(mp, P, "prefill_attention", _attention_without("rot_k")),
+     [pins.test_prefill_of_one_token_equals_decode_with_a_wider_window]),
     ("bits per element without the BF16 windows",
      lambda mp: _plant(mp, ACC, "bits_per_element", _bits_without_windows),
      [pins.test_accounting_matches_pages]),

@@ -354,6 +354,17 @@ def test_quantiser_code_is_the_nearest_level_brute_force():
     assert float(z[0, 0]) == float(np.float16(np.float32(0.9) * np.float32(-10.0)))
 
 
+def test_quantiser_ties_round_to_even():
+    # the code of a quotient exactly halfway between two levels is the even one
+    # (rint, half to even): with s = 1 and z = 0, u = 0.5, 1.5, 2.5 give 0, 2, 2
+    Y = np.zeros((1, 32), np.float32)
+    Y[0, 1] = 3.0                               # min 0 and max 3 at clip 1.0
+    Y[0, 2:5] = [0.5, 1.5, 2.5]
+    c, s, z = oracle.quantize_rows(Y, 32, 1.0)
+    assert float(s[0, 0]) == 1.0 and float(z[0, 0]) == 0.0
+    assert list(c[0, :5]) == [0, 3, 0, 2, 2]
+
+
 def test_quantiser_flat_group():
     Y = np.full((2, 64), 1.25, np.float32)
     c, s, z = oracle.quantize_rows(Y, 64, 0.9)
