@@ -11,7 +11,9 @@ The oracle's sources are never edited; monkeypatch restores every name after
 each case.
 """
 
+import inspect
 import sys
+import types
 
 import numpy as np
 import pytest
@@ -51,6 +53,28 @@ class _NumpyWith:
 
 def _plant_np(mp, module, **over):
     mp.setattr(module, "np", _NumpyWith(**over))
+
+
+def _plant_src(mp, module, old, new):
+    """Run `module`'s source with `old` replaced by `new` (in memory: the file is
+    only read) and put the mutated module's functions and classes wherever the
+    oracle's modules hold the originals."""
+    src = inspect.getsource(module)
+    assert src.count(old) == 1, old
+    mut = types.ModuleType(module.__name__)
+    mut.__dict__.update(__name__=module.__name__, __package__="oracle", __file__=module.__file__)
+    exec(compile(src.replace(old, new), module.__file__, "exec"), mut.__dict__)
+    swaps = {}
+    for attr, val in vars(module).items():
+        if (inspect.isfunction(val) or inspect.isclass(val)) and val.__module__ == module.__name__:
+            swaps[id(val)] = mut.__dict__[attr]
+    n = 0
+    for mod in _oracle_modules():
+        for attr, val in list(vars(mod).items()):
+            if id(val) in swaps:
+                mp.setattr(mod, attr, swaps[id(val)])
+                n += 1
+    assert n > 0
 
 
 def _fails(test_fn):
@@ -441,6 +465,81 @@ CASES = [
      lambda mp: _plant(mp, ACC, "bits_per_element", _bits_without_windows),
      [pins.test_accounting_matches_pages]),
 ]
+
+
+# Source-level mistakes: (module, expression as written, expression with the
+# mistake, pins).  Pins of each module:
+ROT_PINS = [pins.test_hadamard_matches_golden_and_closed_form, pins.test_bitrev_golden_and_involution,
+            pins.test_eig_desc_two_by_two_closed_form, pins.test_eig_desc_diagonal_is_sorting_permutation_and_signs,
+            pins.test_eig_desc_reconstructs_random_covariance, pins.test_rotation_without_covariance_is_the_pages_hadamard,
+            pins.test_rotation_is_orthogonal_and_factorises, pins.test_block_hadamard_closed_form_and_orthogonality,
+            pins.test_bitrev_spreads_every_importance_block_over_every_group, pins.test_covariances_against_explicit_sums]
+QUANT_PINS = [pins.test_bf16_round_matches_torch, pins.test_e4m3_rounding_matches_torch,
+              pins.test_quantiser_exact_grid_round_trip, pins.test_quantiser_e4m3_exact_grid_round_trip,
+              pins.test_quantiser_e4m3_code_is_the_nearest_level_brute_force,
+              pins.test_quantiser_code_is_the_nearest_level_brute_force, pins.test_quantiser_ties_round_to_even,
+              pins.test_quantiser_flat_group, pins.test_packing_golden_and_round_trip,
+              pins.test_record_round_trip_and_size, pins.test_e4m3_record_and_slot_layout]
+CACHE_PINS = [pins.test_regions, pins.test_chunked_append_equals_token_by_token,
+              pins.test_decode_all_bf16_equals_textbook_attention,
+              pins.test_decode_history_on_grid_equals_textbook_attention,
+              pins.test_prefill_of_one_token_equals_decode_with_a_wider_window]
+ATT_PINS = [pins.test_decode_all_bf16_equals_textbook_attention,
+            pins.test_decode_history_on_grid_equals_textbook_attention, pins.test_split_merge_equals_single_pass,
+            pins.test_rotation_invariance_of_logits_and_attention,
+            pins.test_prefill_of_one_token_equals_decode_with_a_wider_window]
+PF_PINS = [pins.test_prefill_without_history_equals_textbook_causal_attention,
+           pins.test_prefill_of_one_token_equals_decode_with_a_wider_window]
+ACC_PINS = [pins.test_accounting_matches_pages, pins.test_record_round_trip_and_size]
+
+SRC_CASES = [
+    (R, "h = np.block([[h, h], [h, -h]])", "h = np.block([[h, h], [-h, h]])", ROT_PINS),
+    (R, "r |= 1 << (nbits - 1 - b)", "r |= 1 << (nbits - 1 - b) if b else 0", ROT_PINS),
+    (R, 'order = np.argsort(-w, kind="stable")', 'order = np.argsort(w, kind="stable")', ROT_PINS),
+    (R, "if col[i] < 0:", "if col[i] > 0:", ROT_PINS),
+    (R, "M = M[:, bitrev_indices(d)]", "M = M[bitrev_indices(d), :]", ROT_PINS),
+    (R, "M = U @ block_hadamard(d, block)", "M = block_hadamard(d, block) @ U", ROT_PINS),
+    (R, "Hb = hadamard(block) / np.sqrt(block)", "Hb = hadamard(block) / block", ROT_PINS),
+    (R, "return X.T @ X / X.shape[0]", "return X.T @ X / X.shape[1]", ROT_PINS),
+    (Q, "lo = (r * mn).astype(np.float32)", "lo = mn.astype(np.float32)", QUANT_PINS),
+    (Q, "/ np.float32(3.0)).astype(np.float32)", "/ np.float32(4.0)).astype(np.float32)", QUANT_PINS),
+    (Q, "z16 = _round_scale(lo, scale_fmt)", "z16 = _round_scale(hi, scale_fmt)", QUANT_PINS),
+    (Q, "c = np.where(s_f == 0.0, 0.0, c)", "c = np.where(s_f == 0.0, 1.0, c)", QUANT_PINS),
+    (Q, "return (s * c + z).reshape(n, d)", "return (s * c - z).reshape(n, d)", QUANT_PINS),
+    (Q, "(c[..., 1] << 2) | (c[..., 2] << 4)", "(c[..., 2] << 2) | (c[..., 1] << 4)", QUANT_PINS),
+    (Q, "raw = d // 2 + 2 * pb * ng", "raw = d // 2 + pb * ng", QUANT_PINS),
+    (Q, "e = np.maximum(ex - 1, -6)", "e = np.maximum(ex - 1, -7)", QUANT_PINS),
+    (Q, "r = np.minimum(r, 448.0)", "r = np.minimum(r, 480.0)", QUANT_PINS),
+    (C, "old = pos < L0", "old = pos <= L0", CACHE_PINS),
+    (C, "Xk[old] = self.ring[rq, pos[old] % W, :, 0, :]", "Xk[old] = self.ring[rq, (pos[old] + 1) % W, :, 0, :]",
+     CACHE_PINS),
+    (C, "self.ring[rq, p % W, :, 1, :] = xv[p - L0]", "self.ring[rq, p % W, :, 1, :] = xk[p - L0]", CACHE_PINS),
+    (C, "xv = bf16_round(v[c0:c1])", "xv = np.asarray(v[c0:c1], np.float32)", CACHE_PINS),
+    (C, "hist_hi = max(S, L - W)", "hist_hi = max(S, L - W + 1)", CACHE_PINS),
+    (C, "Yv = rotate_rows(Xv.reshape(n * H, d), self.rot_v)", "Yv = rotate_rows(Xv.reshape(n * H, d), self.rot_k)",
+     CACHE_PINS),
+    (A, "den = ep.sum() + eh.sum()", "den = ep.sum()", ATT_PINS),
+    (A, "lp = (Kp @ qv) * scale\n            lh", "lp = (Kp @ qr) * scale\n            lh", ATT_PINS),
+    (A, "den = sum(np.exp(p[0] - M) * p[1] for p in parts)", "den = sum(p[1] for p in parts)", ATT_PINS),
+    (A, "o_rot = sum((np.exp(p[0] - M) * p[2] for p in parts if p[3]),", "o_rot = sum((p[2] for p in parts if p[3]),",
+     ATT_PINS),
+    (A, "Kp.append(cache.ring[rq, pos % W, kvh, 0, :].astype(np.float64))",
+     "Kp.append(cache.ring[rq, pos % W, kvh, 1, :].astype(np.float64))", ATT_PINS),
+    (P, "causal = np.tril(np.ones((C, C), dtype=bool))", "causal = np.tril(np.ones((C, C), dtype=bool), -1)",
+     PF_PINS),
+    (P, "den = ep.sum(axis=1) + eh.sum(axis=1) + ec.sum(axis=1)", "den = ep.sum(axis=1) + ec.sum(axis=1)", PF_PINS),
+    (P, "num = ep @ Vp + ec @ vc[:, kvh, :]", "num = ep @ Vp + ec @ kc[:, kvh, :]", PF_PINS),
+    (ACC, "raw = head_dim // 2 + 2 * 2 * (scale_bits // 8) * ng", "raw = head_dim // 4 + 2 * 2 * (scale_bits // 8) * ng",
+     ACC_PINS),
+    (ACC, "(2.0 + 2.0 * scale_bits / group_size)", "(2.0 + scale_bits / group_size)", ACC_PINS),
+]
+
+
+@pytest.mark.parametrize("case", SRC_CASES, ids=["%s: %s" % (c[0].__name__.split(".")[-1], c[2]) for c in SRC_CASES])
+def test_source_mistake_fails_a_pin(case, monkeypatch):
+    module, old, new, covering = case
+    _plant_src(monkeypatch, module, old, new)
+    assert any(_fails(t) for t in covering), "no pin caught the planted mistake"
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
