@@ -510,6 +510,15 @@ SRC_CASES = [
     (Q, "raw = d // 2 + 2 * pb * ng", "raw = d // 2 + pb * ng", QUANT_PINS),
     (Q, "e = np.maximum(ex - 1, -6)", "e = np.maximum(ex - 1, -7)", QUANT_PINS),
     (Q, "r = np.minimum(r, 448.0)", "r = np.minimum(r, 480.0)", QUANT_PINS),
+    (Q, "exp_field = np.where(normal, e + 7, 0)", "exp_field = np.where(normal, e + 8, 0)", QUANT_PINS),
+    (Q, "np.ldexp(1.0 + m / 8.0, ef - 7)", "np.ldexp(1.0 + m / 8.0, ef - 8)", QUANT_PINS),
+    (Q, "out[..., :flat.shape[-1]] = flat", "out[..., slot_size - flat.shape[-1]:] = flat", QUANT_PINS),
+    (Q, "return (raw + 15) // 16 * 16", "return (raw + 7) // 8 * 8", QUANT_PINS),
+    (Q, "return (x32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)",
+     "return (x32.view(np.uint32) >> np.uint32(15)).astype(np.uint16)", QUANT_PINS + CACHE_PINS),
+    (ACC, "return num_layers * num_kv_heads * head_dim * 2 * 0.25", "return num_layers * num_kv_heads * head_dim * 0.25",
+     ACC_PINS),
+    (ACC, "return min(L, sink + recent) / L", "return (sink + recent) / L", ACC_PINS),
     (C, "old = pos < L0", "old = pos <= L0", CACHE_PINS),
     (C, "Xk[old] = self.ring[rq, pos[old] % W, :, 0, :]", "Xk[old] = self.ring[rq, (pos[old] + 1) % W, :, 0, :]",
      CACHE_PINS),

@@ -227,6 +227,10 @@ def test_bf16_round_matches_torch():
     x[:4] = [0.0, -0.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8]   # ties to even
     ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
     assert np.array_equal(oracle.bf16_round(x), ref)
+    # the stored windows hold the bf16 bit patterns: torch's, and back to the values
+    tb = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oq.bf16_bits(ref), tb)
+    assert np.array_equal(oq.bf16_from_bits(tb), ref)
 
 
 def test_e4m3_rounding_matches_torch():
@@ -438,6 +442,10 @@ def test_accounting_matches_pages():
     assert oracle.code_bytes_per_token(16, 4, 256) / 1024 == gold["kib_per_token_16x4_d256"]
     assert oracle.code_bytes_per_token(10, 2, 256) / 1024 == gold["kib_per_token_10x2_d256"]
     assert round(100 * oracle.window_fraction(131072), 2) == gold["window_percent_128k"]
+    # a request no longer than the two windows is held in BF16 entirely
+    assert oracle.window_fraction(100) == 1.0 and oracle.window_fraction(320) == 1.0
+    assert oracle.window_fraction(640) == 0.5
+    assert oracle.bits_per_element(320, 64) == 16.0
     assert round(oracle.bits_per_element(131072, 128), 2) == gold["bits_per_element"]
     assert round(oracle.bits_per_element(131072, 64, scale_bits=8), 2) == gold["bits_per_element_g64_e4m3"]
     assert oracle.code_bytes_per_token(1, 1, 1) / 2 == gold["bytes_per_code"]
