@@ -183,3 +183,25 @@ def test_block_hadamard_rotation_matches_oracle(ops, d, B):
     assert np.abs(R64 @ R64.T - np.eye(d)).max() <= 1e-12
     with pytest.raises(ops.OscarError):
         ops.build_rotation(C, d, hadamard_block=3)
+
+
+def test_calibration_arguments_rejected_before_launch(ops):
+    # the device calibration entry points check their arguments on the host
+    # before any CUDA call (so these run without a GPU): -1 argument, -2 NULL
+    L = ops.lib()
+    nb = ctypes.c_size_t()
+    assert L.oscar_covariance_workspace_bytes(0, 8, ctypes.byref(nb)) == -1
+    assert L.oscar_covariance_workspace_bytes(10, 0, ctypes.byref(nb)) == -1
+    assert L.oscar_covariance_workspace_bytes(10, 4097, ctypes.byref(nb)) == -1
+    assert L.oscar_covariance_workspace_bytes(10, 8, None) == -2
+    assert L.oscar_covariance_device(None, 0, 10, 8, 16, 16, 1 << 20, None) == -2
+    assert L.oscar_covariance_device(16, 0, 10, 8, None, 16, 1 << 20, None) == -2
+    assert L.oscar_covariance_device(16, 7, 10, 8, 16, 16, 1 << 20, None) == -1     # unknown dtype
+    assert L.oscar_covariance_device(16, 0, 0, 8, 16, 16, 1 << 20, None) == -1      # no rows
+    assert L.oscar_value_covariance_workspace_bytes(10, 0, 8, ctypes.byref(nb)) == -1
+    assert L.oscar_value_covariance_workspace_bytes(10, 5, 0, ctypes.byref(nb)) == -1
+    assert L.oscar_value_covariance_workspace_bytes(10, 5, 8, None) == -2
+    assert L.oscar_value_covariance_device(None, 16, 0, 10, 5, 8, 16, 16, 1 << 20, None) == -2
+    assert L.oscar_value_covariance_device(16, 16, 7, 10, 5, 8, 16, 16, 1 << 20, None) == -1
+    assert L.oscar_value_covariance_device(16, 16, 0, 10, 0, 8, 16, 16, 1 << 20, None) == -1
+    assert L.oscar_value_covariance_device(16, 16, 0, 65535 * 64 + 1, 5, 8, 16, 16, 1 << 20, None) == -1
