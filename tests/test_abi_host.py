@@ -205,3 +205,56 @@ def test_calibration_arguments_rejected_before_launch(ops):
     assert L.oscar_value_covariance_device(16, 16, 7, 10, 5, 8, 16, 16, 1 << 20, None) == -1
     assert L.oscar_value_covariance_device(16, 16, 0, 10, 0, 8, 16, 16, 1 << 20, None) == -1
     assert L.oscar_value_covariance_device(16, 16, 0, 65535 * 64 + 1, 5, 8, 16, 16, 1 << 20, None) == -1
+
+
+def test_prefill_arguments_and_workspace_on_the_host(ops):
+    L = ops.lib()
+    cfg = _cfg(ops)                               # d 128, 32 q / 8 KV heads, group 64, 64 sink + 256 recent
+    c = ctypes.byref(cfg.c())
+    good = ops.CLayerCache(16, 16, 16, 16, 16, 10, 1)
+    nb = ctypes.c_size_t()
+    assert L.oscar_prefill_workspace_bytes(c, -1, 10, ctypes.byref(nb)) == -1
+    assert L.oscar_prefill_workspace_bytes(c, 1, -1, ctypes.byref(nb)) == -1
+    assert L.oscar_prefill_workspace_bytes(c, 1, 10, None) == -2
+    # the workspace holds the chunk's rotated queries (fp16 hi and lo, per-group
+    # sums) and the rotated BF16 tokens it sees (its own and both windows, K and V
+    # as fp16 hi and lo): it does not grow with the cached prefix, which the call
+    # does not even take
+    al = lambda x: (x + 255) // 256 * 256
+    for batch, tq in ((1, 100), (1, 8192), (3, 1000)):
+        assert L.oscar_prefill_workspace_bytes(c, batch, tq, ctypes.byref(nb)) == 0
+        dense = tq + batch * (64 + 256)
+        want = 2 * al(tq * 32 * 128 * 2) + al(tq * 32 * 2 * 4) + 2 * al(dense * 8 * 2 * 128 * 2)
+        assert nb.value == want
+    args = lambda **kw: dict(dict(q=16, k=16, v=16, total_q=10, cu=16, st=16, rq=16, pt=16, pts=100, batch=1,
+                                  mc=10, out=16, ws=None, wsb=0), **kw)
+
+    def call(**kw):
+        a = args(**kw)
+        return L.oscar_prefill_attention(c, ctypes.byref(good), a["q"], a["k"], a["v"], a["total_q"], a["cu"],
+                                         a["st"], a["rq"], a["pt"], a["pts"], a["batch"], a["mc"], a["out"],
+                                         a["ws"], a["wsb"], None)
+
+    assert call(batch=0) == 0 and call(total_q=0, mc=0) == 0       # nothing to do
+    assert call(batch=-1) == -1 and call(batch=4097) == -1
+    assert call(q=None) == -2 and call(out=None) == -2 and call(pt=None) == -2
+    assert call(pts=0) == -1
+    assert call(mc=0) == -1 and call(mc=11) == -1                  # max_chunk in [1, total_q]
+    assert call(ws=None) == -3 and call(ws=16, wsb=1 << 30) == -3  # missing or misaligned workspace
+
+
+def test_decode_step_arguments_on_the_host(ops):
+    L = ops.lib()
+    cfg = _cfg(ops)
+    c = ctypes.byref(cfg.c())
+    good = ops.CLayerCache(16, 16, 16, 16, 16, 10, 1)
+
+    def call(kn=16, vn=16, pts=16, batch=1, msl=16):
+        return L.oscar_decode_step(c, ctypes.byref(good), kn, vn, 16, 16, pts, 16, 16, batch, msl, 16, 256,
+                                   1 << 20, None)
+
+    assert call(batch=0) == 0                                       # empty batch: no-op
+    assert call(batch=-1) == -1 and call(batch=4097) == -1
+    assert call(msl=0) == -1
+    assert call(pts=8) == -1                                        # pt_stride < max_seq_len
+    assert call(kn=None) == -2 and call(vn=None) == -2
