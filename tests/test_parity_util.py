@@ -97,3 +97,23 @@ def test_classify_e4m3_slot_records():
     off[0, :rb] = oq.pack_record(kc, ks4, kz, vc, vs, vz, d, G, "e4m3")
     st = classify_records(off, oc, [0])
     assert st["bad"] == 1 and st["sz_ties"] == 0
+
+
+def test_classify_records_band_is_the_stated_rule():
+    # a flipped code is excused only when its quotient lies within 1e-6 of the
+    # boundary: the oracle's y of the tied channel is moved 2^-21 (4.8e-7) and
+    # 2^-18 (3.8e-6) past u = 0.5, with s = 1 and z = 0 unchanged
+    from oracle import quant as oq
+    oc, d, G = _tie_cache()
+    want = oc.records()
+    kc, ks, kz, vc, vs, vz = oq.unpack_record(want[0, 0], d, G)
+    kc2 = kc.copy()
+    kc2[1] = 1
+    flipped = want.copy()
+    flipped[0, 0] = oq.pack_record(kc2, ks, kz, vc, vs, vz, d, G)
+    ky, vy = oc.ky[0], oc.vy[0]
+    for dy, bad in ((2.0 ** -21, 0), (2.0 ** -18, 1)):
+        ky2 = ky.copy()
+        ky2[0, 1] = np.float32(0.5 + dy)
+        st = classify_records(flipped, oc, [0], ora_y={0: (ky2, vy)})
+        assert st["bad"] == bad and st["code_ties"] == 1 - bad
