@@ -2,7 +2,7 @@
 
 import numpy as np
 
-from parity_util import REL_TIE, classify_records, e4m3_near_tie, fp16_near_tie
+from parity_util import ATOL, REL_TIE, RTOL_L2, attn_errors, classify_records, e4m3_near_tie, fp16_near_tie
 
 
 def test_fp16_near_tie_bands():
@@ -117,3 +117,18 @@ def test_classify_records_band_is_the_stated_rule():
         ky2[0, 1] = np.float32(0.5 + dy)
         st = classify_records(flipped, oc, [0], ora_y={0: (ky2, vy)})
         assert st["bad"] == bad and st["code_ties"] == 1 - bad
+
+
+def test_attention_error_measures():
+    # max-abs over every element and relative L2 over the whole output, against
+    # values worked by hand; the bounds are the stated 2e-3 and 1e-3
+    want = np.zeros((2, 3, 4))
+    want[0, 0, :] = [3.0, 4.0, 0.0, 0.0]                 # |want| = 5
+    got = want.copy()
+    got[1, 2, 3] = 0.004                                  # one element off by 4e-3
+    err, rel = attn_errors(got, want)
+    assert err == 0.004 and abs(rel - 0.004 / 5.0) < 1e-15
+    got[0, 1, 0] = -0.003
+    err, rel = attn_errors(got, want)
+    assert err == 0.004 and abs(rel - 0.005 / 5.0) < 1e-15   # sqrt(0.004^2 + 0.003^2) = 0.005
+    assert (ATOL, RTOL_L2) == (2e-3, 1e-3)
