@@ -229,7 +229,6 @@ quantize_tc_kernel(AppendParams P, const __grid_constant__ CUtensorMap tm_k, con
     grid_dep_sync();   // previous grid of the stream done (programmatic launch)
     using C = TcCfg<D>;
     constexpr int ng = D / G;
-    constexpr int NW = D / 16;                      // code words per vector
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

@@ -260,7 +260,6 @@ struct PfCfg {
     static constexpr int RS = D + 8;                   // halves per staged row (16-byte pad: conflict-free ldmatrix)
     static constexpr int Q_HALVES = 2 * ROWS * RS;     // q̃ hi, lo
     static constexpr int T_HALVES = 4 * TT * RS;       // history: K codes, V codes; BF16: K hi, K lo, V hi, V lo
-    static constexpr int RAW_MAX = D / 2 + 16 * (D / 32);   // largest record (group 32, fp16 pairs)
     // shared bytes: q̃, tile, (s, z) [4][TT][ng], token validity [TT], slots [3][TT],
     // raw records of two tiles [2][TT][rec_bytes]
     static size_t smem(int ng, int rec_bytes) {
